@@ -1,0 +1,551 @@
+#!/usr/bin/env python3
+"""Benchmark of the compressed-KV decode path on GB300.
+
+Workload (N=1): the heavy-load LLaMA3-70B-shaped layer -- GQA 64 query / 8 KV heads,
+head_dim 128, batch 512, KV length 2048, fp16 N(0,1) from a seed.  One timed step is
+one decode step of every method on that batch, all through the C ABI:
+  FP16      append the new token, attend over the full cache
+  H2O-512   append, attend (writing logits / lse), accumulate scores, evict to 64 + 448
+  KIVI-4    append (quantising a group when the residual fills), attend
+  Stream-512 append, attend, evict to 64 sinks + 448 recent
+value = tokens produced per second by the whole step (4 methods x batch per step).
+The H2O prefill score pass over the 2048-token prompt and the random eviction of the
+reasoning-trace workload are timed in the same run and reported under "rows".
+
+--impl reference times the fp64 CPU oracle on the host's cores on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "compressed-KV decode attn tokens/s and achieved HBM GB/s (% of ~8 TB/s), 1 GB300"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 10:   # sampler is up before timing
+                time.sleep(0.01)
+            self.n_before = len(self.lines)
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines[getattr(self, "n_before", 0):]:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------ GPU arm
+
+def slot_bytes(n_slots, B, Hkv, Hq, D):
+    """Algorithmic bytes of one slot-cache attention launch: K and V of the attended slots,
+    the queries and the outputs."""
+    return B * Hkv * n_slots * D * 2 * 2 + 2 * B * Hq * D * 2
+
+
+def kivi_bytes(T, R, B, Hkv, Hq, D, bits):
+    G = 32
+    n_q = G * (max(0, T - R) // G)
+    block = G * D * bits // 8 + 4 * D
+    ring = (R + G) * D * 2 * 2
+    return B * Hkv * ((n_q // G) * 2 * block + ring) + 2 * B * Hq * D * 2
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import kv_cache_compression_split_gb300 as kvc
+    from kv_cache_compression_split_gb300 import build as kbuild
+    from kv_cache_compression_split_gb300 import workloads as W
+
+    kbuild.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    w = W.HEAVY
+    B, Hq, Hkv, D, T0 = w.B, w.Hq, w.Hkv, w.D, w.T
+    S_total = args.steps + args.warmup
+    g = Hq // Hkv
+    n_heavy, n_recent, n_sink = w.n_heavy, w.n_recent, w.n_sink
+    rows = {}
+
+    with torch.cuda.stream(stream):
+        # ---------------- set-up (untimed): prompt caches of 2047 tokens, then each
+        # timed step appends token number 2048, 2049, ...
+        K, V = W.kv_tensors(w, T=T0 - 1, device=dev, seed_offset=rank)
+        Cfp = T0 + S_total + 8
+        fp = kvc.SlotCache.empty(B, Hkv, Cfp, D, device=dev)
+        kvc.kvc_append(fp, K, V, stream=stream)
+
+        # H2O: prefill score pass over the prompt (timed as its own row), evict to 512
+        Qp = W.q_tensor(w, device=dev, L=T0 - 1, seed_offset=rank)
+        scores_full = torch.zeros(B, Hkv, Cfp, dtype=torch.float32, device=dev)
+        ws_pre = torch.empty(kvc.kvc_h2o_workspace_size(B, Hq, T0 - 1) // 4, dtype=torch.float32,
+                             device=dev)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        kvc.kvc_h2o_accumulate_prefill(Qp, fp.K, scores_full, ws_pre, T0 - 1, stream=stream)
+        pre_ms = []
+        for _ in range(2):
+            ev0.record(stream)
+            kvc.kvc_h2o_accumulate_prefill(Qp, fp.K, scores_full, ws_pre, T0 - 1, stream=stream)
+            ev1.record(stream)
+            ev1.synchronize()
+            pre_ms.append(ev0.elapsed_time(ev1))
+        L = T0 - 1
+        flops = 2 * 2 * B * Hq * (L * (L + 1) // 2) * D
+        rows["h2o_prefill_score_pass"] = {
+            "ms": min(pre_ms), "tflops": flops / (min(pre_ms) * 1e-3) / 1e12,
+            "shape": f"Qp[{B},{Hq},{L},{D}] x Kp[{B},{Hkv},{L},{D}], causal, two passes"}
+        del Qp, ws_pre
+        Ch = 520
+        tmp = kvc.SlotCache(K=fp.K.clone(), V=fp.V.clone(), pos=fp.pos.clone(), n=fp.n.clone(),
+                            seqlen=fp.seqlen.clone())
+        kvc.kvc_h2o_evict(tmp, scores_full, n_heavy, n_recent, stream=stream)
+        h2o = kvc.SlotCache.empty(B, Hkv, Ch, D, device=dev)
+        h2o.K[:, :, :512] = tmp.K[:, :, :512]
+        h2o.V[:, :, :512] = tmp.V[:, :, :512]
+        h2o.pos[:, :, :512] = tmp.pos[:, :, :512]
+        h2o.n.copy_(tmp.n)
+        h2o.seqlen.copy_(tmp.seqlen)
+        h2o_scores = torch.zeros(B, Hkv, Ch, dtype=torch.float32, device=dev)
+        h2o_scores[:, :, :512] = scores_full[:, :, :512]
+        del scores_full
+        # StreamingLLM: prefill gather to 64 sinks + 448 recent
+        tmp.K.copy_(fp.K)
+        tmp.V.copy_(fp.V)
+        tmp.pos.copy_(fp.pos)
+        tmp.n.copy_(fp.n)
+        tmp.seqlen.copy_(fp.seqlen)
+        kvc.kvc_stream_evict(tmp, n_sink, n_recent, stream=stream)
+        st = kvc.SlotCache.empty(B, Hkv, Ch, D, device=dev)
+        st.K[:, :, :512] = tmp.K[:, :, :512]
+        st.V[:, :, :512] = tmp.V[:, :, :512]
+        st.pos[:, :, :512] = tmp.pos[:, :, :512]
+        st.n.copy_(tmp.n)
+        st.seqlen.copy_(tmp.seqlen)
+        del tmp
+        # KIVI-4: the prompt through the packer
+        Cq = 32 * ((T0 + S_total) // 32 + 1)
+        kv4 = kvc.QuantCache.empty(B, Hkv, Cq, D, 4, w.kivi_R, device=dev)
+        kvc.kvc_append_quant(kv4, K, V, stream=stream)
+        del K, V
+
+        # per-step inputs, resident in HBM (distinct for every step and method)
+        gq = W.generator(w.seed + 900 + rank, dev)
+        qs = torch.randn(S_total, 4, B, Hq, D, generator=gq, device=dev).half()
+        kn = torch.randn(S_total, 4, B, Hkv, 1, D, generator=gq, device=dev).half()
+        vn = torch.randn(S_total, 4, B, Hkv, 1, D, generator=gq, device=dev).half()
+        outs = torch.empty(4, B, Hq, D, dtype=torch.float16, device=dev)
+        logits = torch.empty(B, Hq, Ch, dtype=torch.float32, device=dev)
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+
+        def ws_for(cache):
+            nb = kvc.kvc_workspace_size(cache, qs[0, 0])
+            return torch.empty(max(nb // 4, 1), dtype=torch.float32, device=dev), nb
+
+        ws_fp, nb_fp = ws_for(fp)
+        ws_h2o, nb_h2o = ws_for(h2o)
+        ws_st, nb_st = ws_for(st)
+        ws_kv, nb_kv = ws_for(kv4)
+        launches_per_step = ((2 + 1 + (nb_fp > 0)) + (2 + 1 + (nb_h2o > 0) + 2) + (2 + 3) +
+                             (2 + 1 + (nb_st > 0) + 1))
+        torch.cuda.synchronize(dev)
+
+    names = ["fp16_append", "fp16_attend", "h2o_append", "h2o_attend", "h2o_accumulate",
+             "h2o_evict", "kivi4_append", "kivi4_attend", "stream_append", "stream_attend",
+             "stream_evict"]
+
+    def step(i, ev=None, host=None):
+        """One decode step of all four methods; ev: per-call events; host: pinned inputs."""
+        def mark(k):
+            if ev is not None:
+                ev[k].record(stream)
+        if host is not None:
+            qs[i].copy_(host["q"], non_blocking=True)
+            kn[i].copy_(host["k"], non_blocking=True)
+            vn[i].copy_(host["v"], non_blocking=True)
+        mark(0)
+        kvc.kvc_append(fp, kn[i, 0], vn[i, 0], stream=stream); mark(1)
+        kvc.kvc_decode_attend(fp, qs[i, 0], outs[0], workspace=ws_fp, stream=stream); mark(2)
+        kvc.kvc_append(h2o, kn[i, 1], vn[i, 1], stream=stream); mark(3)
+        kvc.kvc_decode_attend(h2o, qs[i, 1], outs[1], logits=logits, lse=lse, workspace=ws_h2o,
+                              stream=stream); mark(4)
+        kvc.kvc_h2o_accumulate_decode(h2o, h2o_scores, logits, lse, Hq, stream=stream); mark(5)
+        kvc.kvc_h2o_evict(h2o, h2o_scores, n_heavy, n_recent, stream=stream); mark(6)
+        kvc.kvc_append_quant(kv4, kn[i, 2], vn[i, 2], stream=stream); mark(7)
+        kvc.kvc_decode_attend(kv4, qs[i, 2], outs[2], workspace=ws_kv, stream=stream); mark(8)
+        kvc.kvc_append(st, kn[i, 3], vn[i, 3], stream=stream); mark(9)
+        kvc.kvc_decode_attend(st, qs[i, 3], outs[3], workspace=ws_st, stream=stream); mark(10)
+        kvc.kvc_stream_evict(st, n_sink, n_recent, stream=stream); mark(11)
+        if host is not None:
+            host["o"].copy_(outs, non_blocking=True)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---------------- device-resident timing
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize(dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        clk = ClockSampler(dev.index)
+        clk.start()
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(args.warmup + k, ev=evs[k])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        clocks = clk.stop()
+        barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    per_call = {nm: [] for nm in names}
+    for k in range(args.steps):
+        for j, nm in enumerate(names):
+            per_call[nm].append(evs[k][j].elapsed_time(evs[k][j + 1]))
+    status = kvc.kvc_read_device_status(stream)
+
+    # algorithmic bytes per step of each attention launch (sizes of the timed steps)
+    hbm_peak, peak_kind = _peaks()
+    steps_T = [T0 + args.warmup + k for k in range(args.steps)]   # tokens attended (FP16)
+    b_fp = [slot_bytes(t, B, Hkv, Hq, D) for t in steps_T]
+    b_h2o = slot_bytes(513, B, Hkv, Hq, D)
+    b_st = slot_bytes(513, B, Hkv, Hq, D)
+    b_kv = [kivi_bytes(t, w.kivi_R, B, Hkv, Hq, D, 4) for t in steps_T]
+    ms = lambda nm: sum(per_call[nm])
+    slot_bytes_total = sum(b_fp) + b_h2o * args.steps + b_st * args.steps
+    slot_ms = ms("fp16_attend") + ms("h2o_attend") + ms("stream_attend")
+    kernels = {
+        "attend_slots(fp16+h2o+stream)": {"bytes_per_step": slot_bytes_total / args.steps,
+                                          "ms_per_step": slot_ms / args.steps},
+        "attend_fp16": {"bytes_per_step": sum(b_fp) / args.steps,
+                        "ms_per_step": ms("fp16_attend") / args.steps},
+        "attend_h2o512": {"bytes_per_step": b_h2o, "ms_per_step": ms("h2o_attend") / args.steps},
+        "attend_stream512": {"bytes_per_step": b_st, "ms_per_step": ms("stream_attend") / args.steps},
+        "attend_kivi4": {"bytes_per_step": sum(b_kv) / args.steps,
+                         "ms_per_step": ms("kivi4_attend") / args.steps},
+    }
+    for kd in kernels.values():
+        kd["gbs"] = kd["bytes_per_step"] / (kd["ms_per_step"] * 1e-3) / 1e9
+        kd["frac_of_hbm"] = kd["gbs"] / hbm_peak
+    methods = {
+        "fp16": ms("fp16_append") + ms("fp16_attend"),
+        "h2o512": ms("h2o_append") + ms("h2o_attend") + ms("h2o_accumulate") + ms("h2o_evict"),
+        "kivi4": ms("kivi4_append") + ms("kivi4_attend"),
+        "stream512": ms("stream_append") + ms("stream_attend") + ms("stream_evict"),
+    }
+    methods = {k: {"ms_per_step": v / args.steps, "tokens_per_s": B / (v / args.steps * 1e-3)}
+               for k, v in methods.items()}
+    for k, v in methods.items():
+        v["speedup_vs_fp16"] = methods["fp16"]["ms_per_step"] / v["ms_per_step"]
+    calls = {nm: sum(v) / len(v) for nm, v in per_call.items()}
+
+    # ---------------- end to end: host buffers, copies inside the timed region
+    with torch.cuda.stream(stream):
+        host = {"q": torch.empty(4, B, Hq, D, dtype=torch.float16).pin_memory(),
+                "k": torch.empty(4, B, Hkv, 1, D, dtype=torch.float16).pin_memory(),
+                "v": torch.empty(4, B, Hkv, 1, D, dtype=torch.float16).pin_memory(),
+                "o": torch.empty(4, B, Hq, D, dtype=torch.float16).pin_memory()}
+        host["q"].copy_(qs[0].cpu())
+        host["k"].copy_(kn[0].cpu())
+        host["v"].copy_(vn[0].cpu())
+        n_e2e = max(3, min(args.steps, 8))
+        # the caches keep growing: reuse the last warmup slots' inputs to stay in capacity
+        base = S_total - n_e2e
+        fp.n.sub_(n_e2e)
+        fp.seqlen.sub_(n_e2e)
+        kv4.len.sub_(n_e2e)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(n_e2e):
+            step(base + k, host=host)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    h2d = sum(t.numel() * t.element_size() for t in (host["q"], host["k"], host["v"]))
+    d2h = host["o"].numel() * host["o"].element_size()
+
+    # ---------------- random eviction rows (reasoning-trace shape), timed in the same run
+    rows.update(random_rows(kvc, W, dev, stream))
+
+    ms_per_step = total_ms / args.steps
+    res = {
+        "ms_per_step": ms_per_step, "e2e_ms_per_step": e2e_ms, "calls_ms": calls,
+        "kernels": kernels, "methods": methods, "rows": rows, "clocks": clocks,
+        "device_status": status, "tokens_per_step": 4 * B,
+        "launches_per_step": launches_per_step, "h2d": h2d, "d2h": d2h,
+        "hbm_peak": hbm_peak, "peak_kind": peak_kind,
+        "splits": {"fp16": nb_fp, "h2o": nb_h2o, "stream": nb_st, "kivi": nb_kv},
+    }
+    return res
+
+
+def random_rows(kvc, W, dev, stream):
+    """Random eviction on the reasoning-trace workload: a cache of 1024 locked prompt tokens +
+    341 kept + 1024 new generated tokens per KV head is evicted to keep 0.25 of the 1365
+    candidates, then decode attention runs over the 1365 kept slots."""
+    import torch
+    w = W.REASONING
+    B, Hq, Hkv, D = w.B, w.Hq, w.Hkv, w.D
+    n0 = 1024 + 341 + 1024
+    reps = 5
+    out = {}
+    with torch.cuda.stream(stream):
+        K, V = W.kv_tensors(w, T=n0, device=dev)
+        C = n0 + 8
+        base = kvc.SlotCache.empty(B, Hkv, C, D, device=dev)
+        kvc.kvc_append(base, K, V, stream=stream)
+        caches = []
+        for _ in range(reps):
+            c = kvc.SlotCache(K=base.K.clone(), V=base.V.clone(), pos=base.pos.clone(),
+                              n=base.n.clone(), seqlen=base.seqlen.clone())
+            caches.append(c)
+        q = W.q_tensor(w, device=dev)
+        o = torch.empty_like(q)
+        ws = torch.empty(max(kvc.kvc_workspace_size(base, q) // 4, 1), dtype=torch.float32,
+                         device=dev)
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        torch.cuda.synchronize(dev)
+        for r in range(reps):
+            flush.add_(1)          # evict the cache from L2 between repetitions
+            ev[r][0].record(stream)
+            kvc.kvc_random_evict(caches[r], 1024, 0.25, W.RANDOM_EVICT_SEED, r, stream=stream)
+            ev[r][1].record(stream)
+            kvc.kvc_decode_attend(caches[r], q, o, workspace=ws, stream=stream)
+            ev[r][2].record(stream)
+        torch.cuda.synchronize(dev)
+        t_ev = sorted(e[0].elapsed_time(e[1]) for e in ev[1:])
+        t_at = sorted(e[1].elapsed_time(e[2]) for e in ev[1:])
+        kept = int(caches[0].n[0, 0].item())
+    moved_bytes = B * Hkv * (n0 * 4 + 2 * 256 * D * 2 * 2)   # pos scan + ~256 moved rows r/w
+    att_bytes = slot_bytes(kept, B, Hkv, Hq, D)
+    out["random_evict_reasoning"] = {
+        "ms": statistics.median(t_ev), "kept_per_head": kept,
+        "shape": f"B={B} Hkv={Hkv} D={D}: {n0} -> {kept} slots per head"}
+    out["random_attend_reasoning"] = {
+        "ms": statistics.median(t_at), "slots": kept,
+        "gbs": att_bytes / (statistics.median(t_at) * 1e-3) / 1e9,
+        "tokens_per_s": B / (statistics.median(t_at) * 1e-3)}
+    return out
+
+
+# ------------------------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(n_seq: int, threads: int):
+    """Time the fp64 oracle on n_seq sequences (all 8 KV heads) of the heavy-load workload,
+    one decode step of each method; returns (seconds, tokens produced = 4 * n_seq)."""
+    import numpy as np
+    import oracle as orc
+    from kv_cache_compression_split_gb300 import workloads as W
+    w = W.HEAVY
+    Hq, Hkv, D, T = w.Hq, w.Hkv, w.D, w.T
+    K, V = W.kv_tensors(w, T=T, B=n_seq)
+    q = W.q_tensor(w, B=n_seq)
+    K16, V16, q16 = K.numpy(), V.numpy(), q.numpy()
+    t0 = time.perf_counter()
+    # FP16: full attention over T tokens
+    orc.decode_attend(q16, K16, V16, np.full((n_seq, Hkv), T), threads=threads)
+    # StreamingLLM-512: keep-set, gather, attention over 513
+    keep = orc.stream_keep(np.arange(T), T, w.n_sink, w.n_recent + 1)
+    idx = np.flatnonzero(keep)
+    Ks, Vs = K16[:, :, idx], V16[:, :, idx]
+    orc.decode_attend(q16, Ks, Vs, np.full((n_seq, Hkv), len(idx)), threads=threads)
+    # H2O-512: attention over 513 with logits, accumulate, keep-set per unit
+    _, lse, lg = orc.decode_attend(q16, Ks, Vs, np.full((n_seq, Hkv), len(idx)),
+                                   want_logits=True, threads=threads)
+    sc = orc.h2o_accumulate(np.zeros((n_seq, Hkv, len(idx))), lg, lse,
+                            np.full((n_seq, Hkv), len(idx)))
+    for b in range(n_seq):
+        for h in range(Hkv):
+            orc.h2o_keep(idx.astype(np.int32), sc[b, h], T, w.n_heavy, w.n_recent)
+    # KIVI-4: quantise the unit's history and attend (the oracle has no incremental state)
+    g = Hq // Hkv
+    n_q = orc.kivi_nq(T, w.kivi_R)
+    for b in range(n_seq):
+        for h in range(Hkv):
+            qz = orc.kivi_quantize_unit(K16[b, h, :n_q], V16[b, h, :n_q], n_q, 4)
+            orc.kivi_attend_unit(q16[b, h * g:(h + 1) * g], K16[b, h], V16[b, h], T, w.kivi_R, 4,
+                                 qz=qz)
+    return time.perf_counter() - t0, 4 * n_seq
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    import oracle as orc
+    orc.build()
+    threads = cpu_cores()
+    n_seq = args.ref_seqs
+    for _ in range(args.warmup):
+        oracle_sample(max(1, n_seq // 4), threads)
+    times, toks = [], 0
+    for _ in range(args.steps):
+        dt, tk = oracle_sample(n_seq, threads)
+        times.append(dt)
+        toks += tk
+    value = toks / sum(times)
+    sample = (f"{n_seq} sequences x 8 KV heads of the heavy-load workload per step, one decode "
+              f"step of FP16, StreamingLLM-512, H2O-512 and KIVI-4 (oracle, fp64)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "heavy-gqa64x8-b512-d128-t2048", "global_batch": n_seq,
+                       "seq_len": 2048, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--ref-seqs", type=int, default=4)
+    ap.add_argument("--cpu-seqs", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    # the CPU baseline (oracle) runs first, before any CUDA context exists
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle as orc
+        orc.build()
+        threads = cpu_cores()
+        dt, tk = oracle_sample(args.cpu_seqs, threads)
+        cpu = {"value": tk / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{args.cpu_seqs} sequences x 8 KV heads of the heavy-load workload, one "
+                         f"decode step of FP16, StreamingLLM-512, H2O-512 and KIVI-4 "
+                         f"({dt:.1f} s of fp64 oracle work)"}
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res = run_gpu(args, rank, world)
+    ms = res["ms_per_step"]
+    e2e_ms = res["e2e_ms_per_step"]
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = t.tolist()
+    if rank == 0:
+        dom = res["kernels"]["attend_slots(fp16+h2o+stream)"]
+        line = {
+            "metric": METRIC, "value": world * res["tokens_per_step"] / (ms * 1e-3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": {"workload": "heavy-gqa64x8-b512-d128-t2048", "global_batch": 512 * world,
+                       "seq_len": 2048, "parallelism": f"replicas x{world}",
+                       "methods": ["fp16", "h2o512", "kivi4", "stream512"],
+                       "l2": "inputs larger than L2 (8 GB of cache read per step)"},
+            "e2e": {"value": world * res["tokens_per_step"] / (e2e_ms * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+            "gpu_launches": res["launches_per_step"] * args.steps,
+            "roofline": {"bound": "hbm", "kernel": "k_attend_slots",
+                         "achieved": dom["gbs"], "peak": res["hbm_peak"], "unit": "GB/s",
+                         "frac": dom["frac_of_hbm"], "traffic": None,
+                         "peak_source": res["peak_kind"]},
+            "cpu_baseline": cpu,
+            "clocks": res["clocks"],
+            "kernels": res["kernels"], "methods": res["methods"], "rows": res["rows"],
+            "calls_ms": res["calls_ms"], "device_status": res["device_status"],
+        }
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,314 @@
+"""Python binding of libkvc.so -- the GB300 compressed-KV decode library.
+
+This module only marshals arguments: it builds the C descriptor structs from
+torch tensors (device memory owned by the caller) and calls the C ABI declared
+in include/kvc.h with the same function names.  Every step of the path runs in
+the library's CUDA kernels; there is no Python or CPU fallback -- if the
+library is missing, importing a function raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvc.so")
+_lib = None
+_lock = threading.Lock()
+
+KVC_OK, KVC_ERR_INVALID_ARG, KVC_ERR_UNSUPPORTED, KVC_ERR_CAPACITY = 0, 1, 2, 3
+KVC_ERR_WORKSPACE, KVC_ERR_CUDA, KVC_ERR_DEVICE = 4, 5, 6
+KVC_DEV_CAPACITY, KVC_DEV_TIMEOUT = 0x1, 0x2
+KVC_KIND_SLOTS, KVC_KIND_KIVI = 0, 1
+KVC_H2O_DECODE, KVC_H2O_PREFILL = 0, 1
+KIVI_GROUP = 32
+
+
+class KvcError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {kvc_status_string(status)}")
+
+
+class SlotCacheDesc(C.Structure):
+    _fields_ = [("B", C.c_int), ("Hkv", C.c_int), ("D", C.c_int), ("C", C.c_int),
+                ("K", C.c_void_p), ("V", C.c_void_p), ("pos", C.c_void_p), ("n", C.c_void_p),
+                ("seqlen", C.c_void_p)]
+
+
+class QuantCacheDesc(C.Structure):
+    _fields_ = [("B", C.c_int), ("Hkv", C.c_int), ("D", C.c_int), ("bits", C.c_int),
+                ("R", C.c_int), ("Cq", C.c_int), ("k_blocks", C.c_void_p),
+                ("v_blocks", C.c_void_p), ("k_res", C.c_void_p), ("v_res", C.c_void_p),
+                ("len", C.c_void_p)]
+
+
+class AttendArgs(C.Structure):
+    _fields_ = [("kind", C.c_int), ("Hq", C.c_int), ("q", C.c_void_p), ("o", C.c_void_p),
+                ("slots", C.POINTER(SlotCacheDesc)), ("quant", C.POINTER(QuantCacheDesc)),
+                ("logits", C.c_void_p), ("lse", C.c_void_p), ("workspace", C.c_void_p),
+                ("workspace_bytes", C.c_size_t), ("num_splits", C.c_int),
+                ("softmax_scale", C.c_float)]
+
+
+class H2OArgs(C.Structure):
+    _fields_ = [("mode", C.c_int), ("B", C.c_int), ("Hq", C.c_int), ("Hkv", C.c_int),
+                ("D", C.c_int), ("C", C.c_int), ("scores", C.c_void_p), ("logits", C.c_void_p),
+                ("lse", C.c_void_p), ("n", C.c_void_p), ("L", C.c_int), ("qp", C.c_void_p),
+                ("kp", C.c_void_p), ("kp_cap", C.c_int), ("workspace", C.c_void_p),
+                ("workspace_bytes", C.c_size_t), ("softmax_scale", C.c_float)]
+
+
+def lib():
+    """Load libkvc.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with "
+                                  "`python -m kv_cache_compression_split_gb300.build`")
+            L = C.CDLL(LIB_PATH)
+            P, i, st = C.c_void_p, C.c_int, C.c_int
+            sig = {
+                "kvc_kivi_block_bytes": (C.c_size_t, [i, i]),
+                "kvc_append": (st, [C.POINTER(SlotCacheDesc), P, P, i, P]),
+                "kvc_append_quant": (st, [C.POINTER(QuantCacheDesc), P, P, i, P]),
+                "kvc_workspace_size": (C.c_size_t, [C.POINTER(AttendArgs)]),
+                "kvc_decode_attend": (st, [C.POINTER(AttendArgs), P]),
+                "kvc_h2o_workspace_size": (C.c_size_t, [C.POINTER(H2OArgs)]),
+                "kvc_h2o_accumulate": (st, [C.POINTER(H2OArgs), P]),
+                "kvc_h2o_evict": (st, [C.POINTER(SlotCacheDesc), P, i, i, P]),
+                "kvc_stream_evict": (st, [C.POINTER(SlotCacheDesc), i, i, P]),
+                "kvc_random_evict": (st, [C.POINTER(SlotCacheDesc), i, C.c_double, C.c_uint64,
+                                          C.c_uint32, P]),
+                "kvc_status_string": (C.c_char_p, [i]),
+                "kvc_read_device_status": (st, [C.POINTER(C.c_int), P]),
+            }
+            for name, (res, args) in sig.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != KVC_OK:
+        raise KvcError(status, where)
+
+
+# ----------------------------------------------------------------------------- C ABI, same names
+
+def kvc_status_string(status: int) -> str:
+    return lib().kvc_status_string(int(status)).decode()
+
+
+def kvc_kivi_block_bytes(D: int, bits: int) -> int:
+    return int(lib().kvc_kivi_block_bytes(D, bits))
+
+
+def kvc_append(cache: "SlotCache", k_new, v_new, stream=None):
+    d = cache.desc()
+    _check(lib().kvc_append(C.byref(d), _ptr(k_new), _ptr(v_new), int(k_new.shape[2]),
+                            _stream(stream)), "kvc_append")
+
+
+def kvc_append_quant(cache: "QuantCache", k_new, v_new, stream=None):
+    d = cache.desc()
+    _check(lib().kvc_append_quant(C.byref(d), _ptr(k_new), _ptr(v_new), int(k_new.shape[2]),
+                                  _stream(stream)), "kvc_append_quant")
+
+
+def _attend_args(cache, q, o, logits=None, lse=None, workspace=None, num_splits=0, scale=0.0):
+    a = AttendArgs()
+    keep = []
+    if isinstance(cache, SlotCache):
+        d = cache.desc()
+        keep.append(d)
+        a.kind = KVC_KIND_SLOTS
+        a.slots = C.pointer(d)
+    else:
+        d = cache.desc()
+        keep.append(d)
+        a.kind = KVC_KIND_KIVI
+        a.quant = C.pointer(d)
+    a.Hq = int(q.shape[1])
+    a.q, a.o = _ptr(q), _ptr(o)
+    a.logits, a.lse = _ptr(logits), _ptr(lse)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    a.num_splits = int(num_splits)
+    a.softmax_scale = float(scale)
+    return a, keep
+
+
+def kvc_workspace_size(cache, q, num_splits: int = 0) -> int:
+    a, _keep = _attend_args(cache, q, None, num_splits=num_splits)
+    return int(lib().kvc_workspace_size(C.byref(a)))
+
+
+def kvc_decode_attend(cache, q, o, logits=None, lse=None, workspace=None, num_splits: int = 0,
+                      softmax_scale: float = 0.0, stream=None):
+    a, _keep = _attend_args(cache, q, o, logits, lse, workspace, num_splits, softmax_scale)
+    _check(lib().kvc_decode_attend(C.byref(a), _stream(stream)), "kvc_decode_attend")
+
+
+def _h2o_args(mode, B, Hq, Hkv, D, Cc, scores, logits=None, lse=None, n=None, L=0, qp=None,
+              kp=None, kp_cap=0, workspace=None, scale=0.0):
+    a = H2OArgs()
+    a.mode, a.B, a.Hq, a.Hkv, a.D, a.C = mode, B, Hq, Hkv, D, Cc
+    a.scores, a.logits, a.lse, a.n = _ptr(scores), _ptr(logits), _ptr(lse), _ptr(n)
+    a.L, a.qp, a.kp, a.kp_cap = int(L), _ptr(qp), _ptr(kp), int(kp_cap)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    a.softmax_scale = float(scale)
+    return a
+
+
+def kvc_h2o_workspace_size(B: int, Hq: int, L: int) -> int:
+    a = _h2o_args(KVC_H2O_PREFILL, B, Hq, 1, 128, 1, None, L=L)
+    return int(lib().kvc_h2o_workspace_size(C.byref(a)))
+
+
+def kvc_h2o_accumulate_decode(cache: "SlotCache", scores, logits, lse, Hq: int, stream=None):
+    a = _h2o_args(KVC_H2O_DECODE, cache.B, Hq, cache.Hkv, cache.D, cache.C, scores, logits, lse,
+                  cache.n)
+    _check(lib().kvc_h2o_accumulate(C.byref(a), _stream(stream)), "kvc_h2o_accumulate")
+
+
+def kvc_h2o_accumulate_prefill(qp, kp, scores, workspace, L: int, stream=None):
+    B, Hq, _, D = qp.shape
+    _, Hkv, kp_cap, _ = kp.shape
+    a = _h2o_args(KVC_H2O_PREFILL, B, Hq, Hkv, D, int(scores.shape[-1]), scores, L=L, qp=qp,
+                  kp=kp, kp_cap=kp_cap, workspace=workspace)
+    _check(lib().kvc_h2o_accumulate(C.byref(a), _stream(stream)), "kvc_h2o_accumulate")
+
+
+def kvc_h2o_accumulate(args: H2OArgs, stream=None):
+    _check(lib().kvc_h2o_accumulate(C.byref(args), _stream(stream)), "kvc_h2o_accumulate")
+
+
+def kvc_h2o_evict(cache: "SlotCache", scores, n_heavy: int, n_recent: int, stream=None):
+    d = cache.desc()
+    _check(lib().kvc_h2o_evict(C.byref(d), _ptr(scores), n_heavy, n_recent, _stream(stream)),
+           "kvc_h2o_evict")
+
+
+def kvc_stream_evict(cache: "SlotCache", n_sink: int, n_recent: int, stream=None):
+    d = cache.desc()
+    _check(lib().kvc_stream_evict(C.byref(d), n_sink, n_recent, _stream(stream)),
+           "kvc_stream_evict")
+
+
+def kvc_random_evict(cache: "SlotCache", prompt_len: int, keep_ratio: float, seed: int,
+                     epoch: int, stream=None):
+    d = cache.desc()
+    _check(lib().kvc_random_evict(C.byref(d), prompt_len, float(keep_ratio),
+                                  seed & (2**64 - 1), epoch & 0xffffffff, _stream(stream)),
+           "kvc_random_evict")
+
+
+def kvc_read_device_status(stream=None) -> int:
+    out = C.c_int(0)
+    st = lib().kvc_read_device_status(C.byref(out), _stream(stream))
+    if st not in (KVC_OK, KVC_ERR_DEVICE):
+        raise KvcError(st, "kvc_read_device_status")
+    return out.value
+
+
+# ----------------------------------------------------------------------------- cache holders
+
+@dataclass
+class SlotCache:
+    """fp16 slot cache in device memory (layout documented in include/kvc.h)."""
+    K: torch.Tensor
+    V: torch.Tensor
+    pos: torch.Tensor
+    n: torch.Tensor
+    seqlen: torch.Tensor
+
+    @property
+    def B(self): return self.K.shape[0]
+
+    @property
+    def Hkv(self): return self.K.shape[1]
+
+    @property
+    def C(self): return self.K.shape[2]
+
+    @property
+    def D(self): return self.K.shape[3]
+
+    @classmethod
+    def empty(cls, B, Hkv, C_, D, device="cuda"):
+        return cls(K=torch.zeros(B, Hkv, C_, D, dtype=torch.float16, device=device),
+                   V=torch.zeros(B, Hkv, C_, D, dtype=torch.float16, device=device),
+                   pos=torch.full((B, Hkv, C_), -1, dtype=torch.int32, device=device),
+                   n=torch.zeros(B, Hkv, dtype=torch.int32, device=device),
+                   seqlen=torch.zeros(B, dtype=torch.int32, device=device))
+
+    def desc(self) -> SlotCacheDesc:
+        return SlotCacheDesc(self.B, self.Hkv, self.D, self.C, _ptr(self.K), _ptr(self.V),
+                             _ptr(self.pos), _ptr(self.n), _ptr(self.seqlen))
+
+
+@dataclass
+class QuantCache:
+    """KIVI cache in device memory (layout documented in include/kvc.h)."""
+    k_blocks: torch.Tensor
+    v_blocks: torch.Tensor
+    k_res: torch.Tensor
+    v_res: torch.Tensor
+    len: torch.Tensor
+    bits: int
+    R: int
+
+    @property
+    def B(self): return self.k_res.shape[0]
+
+    @property
+    def Hkv(self): return self.k_res.shape[1]
+
+    @property
+    def D(self): return self.k_res.shape[3]
+
+    @property
+    def Cq(self): return self.k_blocks.shape[2] * KIVI_GROUP
+
+    @classmethod
+    def empty(cls, B, Hkv, Cq, D, bits, R, device="cuda"):
+        assert Cq % KIVI_GROUP == 0
+        bb = KIVI_GROUP * D * bits // 8 + 4 * D
+        ng = Cq // KIVI_GROUP
+        return cls(k_blocks=torch.zeros(B, Hkv, ng, bb, dtype=torch.uint8, device=device),
+                   v_blocks=torch.zeros(B, Hkv, ng, bb, dtype=torch.uint8, device=device),
+                   k_res=torch.zeros(B, Hkv, R + KIVI_GROUP, D, dtype=torch.float16, device=device),
+                   v_res=torch.zeros(B, Hkv, R + KIVI_GROUP, D, dtype=torch.float16, device=device),
+                   len=torch.zeros(B, dtype=torch.int32, device=device), bits=bits, R=R)
+
+    def desc(self) -> QuantCacheDesc:
+        return QuantCacheDesc(self.B, self.Hkv, self.D, self.bits, self.R, self.Cq,
+                              _ptr(self.k_blocks), _ptr(self.v_blocks), _ptr(self.k_res),
+                              _ptr(self.v_res), _ptr(self.len))

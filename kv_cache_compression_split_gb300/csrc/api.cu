@@ -1,0 +1,420 @@
+// api.cu -- the extern "C" entry points of libkvc.so: argument validation,
+// launch planning, tensor-map encoding and the device status word.
+// Every entry point validates on the host and enqueues nothing on error.
+#include "kvc_internal.h"
+
+#include <cudaTypedefs.h>
+#include <limits.h>
+#include <math.h>
+#include <mutex>
+
+namespace kvc {
+
+namespace {
+
+__device__ int g_status;   // KVC_DEV_* bits, one word per device
+
+constexpr int MAX_DEVICES = 64;
+constexpr int EVICT_MAX_SLOTS = 65536;
+
+int *g_status_ptr[MAX_DEVICES];
+int g_sm_count[MAX_DEVICES];
+std::mutex g_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
+        return -1;
+    return dev;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool head_dim_ok(int D) { return D == 64 || D == 128; }
+
+} // namespace
+
+int *dev_status_ptr()
+{
+    const int dev = current_device();
+    if (dev < 0)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess)
+            return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int sm_count()
+{
+    const int dev = current_device();
+    if (dev < 0)
+        return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sm_count[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = v > 0 ? v : 1;
+    }
+    return g_sm_count[dev];
+}
+
+bool encode_tmap_2d_f16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                        uint32_t box_inner, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn || !aligned16(base) || rows == 0 || rows > (uint64_t)INT_MAX)
+        return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested)
+{
+    SlotAttendPlan pl{1, tiles_per_unit > 0 ? tiles_per_unit : 1};
+    if (tiles_per_unit <= 0)
+        return pl;
+    int S = 1;
+    if (requested > 0) {
+        S = requested < tiles_per_unit ? requested : tiles_per_unit;
+    } else {
+        const double slots = 2.0 * sm_count();
+        double best = 1e300;
+        const int smax = tiles_per_unit < 64 ? tiles_per_unit : 64;
+        for (int s = 1; s <= smax; ++s) {
+            const double waves = ceil(units * (double)s / slots);
+            const double cost = waves * (ceil(tiles_per_unit / (double)s) + 1.5) + (s > 1 ? 0.5 : 0.0);
+            if (cost < best - 1e-9) {
+                best = cost;
+                S = s;
+            }
+        }
+    }
+    pl.splits = S;
+    pl.tiles_per_split = (tiles_per_unit + S - 1) / S;
+    pl.splits = (tiles_per_unit + pl.tiles_per_split - 1) / pl.tiles_per_split;
+    return pl;
+}
+
+namespace {
+
+kvc_status check_slot_cache(const kvc_slot_cache *c)
+{
+    if (!c || !c->K || !c->V || !c->pos || !c->n || !c->seqlen)
+        return KVC_ERR_INVALID_ARG;
+    if (c->B <= 0 || c->Hkv <= 0 || c->C <= 0)
+        return KVC_ERR_INVALID_ARG;
+    if (!head_dim_ok(c->D))
+        return KVC_ERR_UNSUPPORTED;
+    if (!aligned16(c->K) || !aligned16(c->V) || !aligned16(c->pos))
+        return KVC_ERR_INVALID_ARG;
+    if ((long long)c->B * c->Hkv * c->C > (long long)INT_MAX)
+        return KVC_ERR_UNSUPPORTED;
+    return KVC_OK;
+}
+
+kvc_status check_quant_cache(const kvc_quant_cache *c)
+{
+    if (!c || !c->k_blocks || !c->v_blocks || !c->k_res || !c->v_res || !c->len)
+        return KVC_ERR_INVALID_ARG;
+    if (c->B <= 0 || c->Hkv <= 0 || c->R < 0 || c->Cq < 0 || c->Cq % KIVI_G != 0)
+        return KVC_ERR_INVALID_ARG;
+    if (!head_dim_ok(c->D) || (c->bits != 2 && c->bits != 4))
+        return KVC_ERR_UNSUPPORTED;
+    if (!aligned16(c->k_blocks) || !aligned16(c->v_blocks) || !aligned16(c->k_res) ||
+        !aligned16(c->v_res))
+        return KVC_ERR_INVALID_ARG;
+    if ((long long)c->B * c->Hkv * (c->R + KIVI_G) > (long long)INT_MAX)
+        return KVC_ERR_UNSUPPORTED;
+    return KVC_OK;
+}
+
+kvc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
+
+struct AttendPlanFull {
+    kvc_status st;
+    int B, Hkv, D;
+    SlotAttendPlan plan;
+    size_t ws;
+};
+
+AttendPlanFull plan_full(const kvc_attend_args *a)
+{
+    AttendPlanFull f{};
+    f.st = KVC_ERR_INVALID_ARG;
+    if (!a)
+        return f;
+    if (a->kind == KVC_KIND_SLOTS) {
+        if (check_slot_cache(a->slots) != KVC_OK) {
+            f.st = check_slot_cache(a->slots);
+            return f;
+        }
+        f.B = a->slots->B;
+        f.Hkv = a->slots->Hkv;
+        f.D = a->slots->D;
+        const int tiles = (a->slots->C + TILE - 1) / TILE;
+        f.plan = plan_attend(f.B * f.Hkv, tiles, a->num_splits);
+        f.ws = f.plan.splits > 1 ? (size_t)f.B * a->Hq * f.plan.splits * (f.D + 2) * sizeof(float)
+                                 : 0;
+    } else if (a->kind == KVC_KIND_KIVI) {
+        if (check_quant_cache(a->quant) != KVC_OK) {
+            f.st = check_quant_cache(a->quant);
+            return f;
+        }
+        f.B = a->quant->B;
+        f.Hkv = a->quant->Hkv;
+        f.D = a->quant->D;
+        const int tiles = (a->quant->Cq / KIVI_G + 1) / 2;
+        f.plan = plan_attend(f.B * f.Hkv, tiles > 0 ? tiles : 1, a->num_splits);
+        f.ws = (size_t)f.B * a->Hq * (f.plan.splits + 1) * (f.D + 2) * sizeof(float);
+    } else {
+        return f;
+    }
+    if (a->Hq <= 0 || a->Hq % f.Hkv != 0)
+        return f;
+    if (a->Hq / f.Hkv > 8) {
+        f.st = KVC_ERR_UNSUPPORTED;
+        return f;
+    }
+    f.st = KVC_OK;
+    return f;
+}
+
+} // namespace
+} // namespace kvc
+
+using namespace kvc;
+
+extern "C" {
+
+size_t kvc_kivi_block_bytes(int D, int bits)
+{
+    if (!head_dim_ok(D) || (bits != 2 && bits != 4))
+        return 0;
+    return (size_t)KIVI_G * D * bits / 8 + 4 * (size_t)D;
+}
+
+kvc_status kvc_append(const kvc_slot_cache *cache, const uint16_t *k_new, const uint16_t *v_new,
+                      int n_new, cudaStream_t stream)
+{
+    kvc_status st = check_slot_cache(cache);
+    if (st != KVC_OK)
+        return st;
+    if (n_new < 0 || (n_new > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))))
+        return KVC_ERR_INVALID_ARG;
+    if (n_new > cache->C)
+        return KVC_ERR_CAPACITY;
+    if (n_new == 0)
+        return KVC_OK;
+    return from_cuda(launch_append_slots(*cache, k_new, v_new, n_new, stream));
+}
+
+kvc_status kvc_append_quant(const kvc_quant_cache *cache, const uint16_t *k_new,
+                            const uint16_t *v_new, int n_new, cudaStream_t stream)
+{
+    kvc_status st = check_quant_cache(cache);
+    if (st != KVC_OK)
+        return st;
+    if (n_new < 0 || (n_new > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))))
+        return KVC_ERR_INVALID_ARG;
+    if (n_new == 0)
+        return KVC_OK;
+    if ((long long)n_new > (long long)cache->Cq + cache->R + KIVI_G)
+        return KVC_ERR_CAPACITY;
+    return from_cuda(launch_append_quant(*cache, k_new, v_new, n_new, stream));
+}
+
+size_t kvc_workspace_size(const kvc_attend_args *args)
+{
+    AttendPlanFull f = plan_full(args);
+    return f.st == KVC_OK ? f.ws : 0;
+}
+
+kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
+{
+    AttendPlanFull f = plan_full(a);
+    if (f.st != KVC_OK)
+        return f.st;
+    if (!a->q || !a->o || !aligned16(a->q))
+        return KVC_ERR_INVALID_ARG;
+    if (a->kind == KVC_KIND_KIVI && a->logits)
+        return KVC_ERR_UNSUPPORTED;
+    if (f.ws > 0 && (!a->workspace || a->workspace_bytes < f.ws || !aligned16(a->workspace)))
+        return KVC_ERR_WORKSPACE;
+    const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / sqrtf((float)f.D);
+    float *part_o = static_cast<float *>(a->workspace);
+    if (a->kind == KVC_KIND_SLOTS) {
+        const kvc_slot_cache &c = *a->slots;
+        float *part_ml = part_o ? part_o + (size_t)f.B * a->Hq * f.plan.splits * f.D : nullptr;
+        AttendLaunch L{f.B, a->Hq, c.Hkv, c.D, c.C, a->q, a->o, c.K, c.V, c.n, a->logits, a->lse,
+                       part_o, part_ml, f.plan.splits, f.plan.tiles_per_split, scale};
+        return from_cuda(launch_attend_slots(L, stream));
+    }
+    const kvc_quant_cache &c = *a->quant;
+    float *part_ml = part_o + (size_t)f.B * a->Hq * (f.plan.splits + 1) * f.D;
+    KiviAttendLaunch L{f.B, a->Hq, c.Hkv, c.D, c.bits, c.R, c.Cq, a->q, a->o, c.k_blocks,
+                       c.v_blocks, c.k_res, c.v_res, c.len, a->lse, part_o, part_ml,
+                       f.plan.splits, f.plan.tiles_per_split, scale};
+    return from_cuda(launch_attend_kivi(L, stream));
+}
+
+size_t kvc_h2o_workspace_size(const kvc_h2o_args *a)
+{
+    if (!a || a->mode != KVC_H2O_PREFILL || a->L <= 0 || a->B <= 0 || a->Hq <= 0)
+        return 0;
+    const size_t lpad = (size_t)((a->L + 63) / 64) * 64;
+    return (size_t)a->B * a->Hq * lpad * sizeof(float);
+}
+
+kvc_status kvc_h2o_accumulate(const kvc_h2o_args *a, cudaStream_t stream)
+{
+    if (!a || !a->scores || a->B <= 0 || a->Hkv <= 0 || a->Hq <= 0 || a->C <= 0)
+        return KVC_ERR_INVALID_ARG;
+    if (a->Hq % a->Hkv != 0)
+        return KVC_ERR_INVALID_ARG;
+    if (a->mode == KVC_H2O_DECODE) {
+        if (!a->logits || !a->lse || !a->n)
+            return KVC_ERR_INVALID_ARG;
+        return from_cuda(launch_h2o_decode_acc(*a, stream));
+    }
+    if (a->mode != KVC_H2O_PREFILL)
+        return KVC_ERR_INVALID_ARG;
+    if (!head_dim_ok(a->D))
+        return KVC_ERR_UNSUPPORTED;
+    if (!a->qp || !a->kp || a->L <= 0 || !aligned16(a->qp) || !aligned16(a->kp))
+        return KVC_ERR_INVALID_ARG;
+    if (a->L > a->kp_cap || a->L > a->C)
+        return KVC_ERR_CAPACITY;
+    if ((long long)a->B * a->Hq * a->L > (long long)INT_MAX ||
+        (long long)a->B * a->Hkv * a->kp_cap > (long long)INT_MAX)
+        return KVC_ERR_UNSUPPORTED;
+    const size_t need = kvc_h2o_workspace_size(a);
+    if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace))
+        return KVC_ERR_WORKSPACE;
+    return from_cuda(launch_h2o_prefill(*a, static_cast<float *>(a->workspace), stream));
+}
+
+static kvc_status evict_common(const kvc_slot_cache *cache)
+{
+    kvc_status st = check_slot_cache(cache);
+    if (st != KVC_OK)
+        return st;
+    if (cache->C > EVICT_MAX_SLOTS)
+        return KVC_ERR_UNSUPPORTED;
+    return KVC_OK;
+}
+
+kvc_status kvc_h2o_evict(const kvc_slot_cache *cache, float *scores, int n_heavy, int n_recent,
+                         cudaStream_t stream)
+{
+    kvc_status st = evict_common(cache);
+    if (st != KVC_OK)
+        return st;
+    if (!scores || n_heavy < 0 || n_recent < 0)
+        return KVC_ERR_INVALID_ARG;
+    EvictLaunch e{};
+    e.kind = EVICT_H2O;
+    e.c = *cache;
+    e.scores = scores;
+    e.n_heavy = n_heavy;
+    e.n_recent = n_recent;
+    return from_cuda(launch_evict(e, stream));
+}
+
+kvc_status kvc_stream_evict(const kvc_slot_cache *cache, int n_sink, int n_recent,
+                            cudaStream_t stream)
+{
+    kvc_status st = evict_common(cache);
+    if (st != KVC_OK)
+        return st;
+    if (n_sink < 0 || n_recent < 0)
+        return KVC_ERR_INVALID_ARG;
+    EvictLaunch e{};
+    e.kind = EVICT_STREAM;
+    e.c = *cache;
+    e.n_sink = n_sink;
+    e.n_recent = n_recent;
+    return from_cuda(launch_evict(e, stream));
+}
+
+kvc_status kvc_random_evict(const kvc_slot_cache *cache, int prompt_len, double keep_ratio,
+                            uint64_t seed, uint32_t epoch, cudaStream_t stream)
+{
+    kvc_status st = evict_common(cache);
+    if (st != KVC_OK)
+        return st;
+    if (prompt_len < 0 || !(keep_ratio >= 0.0 && keep_ratio <= 1.0))
+        return KVC_ERR_INVALID_ARG;
+    EvictLaunch e{};
+    e.kind = EVICT_RANDOM;
+    e.c = *cache;
+    e.prompt_len = prompt_len;
+    e.keep_ratio = keep_ratio;
+    e.seed = seed;
+    e.epoch = epoch;
+    return from_cuda(launch_evict(e, stream));
+}
+
+const char *kvc_status_string(kvc_status s)
+{
+    switch (s) {
+    case KVC_OK:
+        return "KVC_OK";
+    case KVC_ERR_INVALID_ARG:
+        return "KVC_ERR_INVALID_ARG: null, misaligned or out-of-range argument";
+    case KVC_ERR_UNSUPPORTED:
+        return "KVC_ERR_UNSUPPORTED: shape or format outside what the kernels handle";
+    case KVC_ERR_CAPACITY:
+        return "KVC_ERR_CAPACITY: size exceeds a capacity";
+    case KVC_ERR_WORKSPACE:
+        return "KVC_ERR_WORKSPACE: workspace missing or too small";
+    case KVC_ERR_CUDA:
+        return "KVC_ERR_CUDA: a CUDA runtime call or launch failed";
+    case KVC_ERR_DEVICE:
+        return "KVC_ERR_DEVICE: a kernel flagged an inconsistent cache or an expired wait";
+    }
+    return "KVC_ERR_UNKNOWN";
+}
+
+kvc_status kvc_read_device_status(int *out, cudaStream_t stream)
+{
+    if (!out)
+        return KVC_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(stream) != cudaSuccess)
+        return KVC_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess)
+        return KVC_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess)
+        return KVC_ERR_CUDA;
+    *out = v;
+    return v ? KVC_ERR_DEVICE : KVC_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,436 @@
+// attend_slots.cu -- split-KV decode attention over an fp16 slot cache (and
+// over the fp16 residual ring of a KIVI cache), plus the split combine.
+//
+// One CTA handles one (sequence b, KV head hk, split) work item: the g query
+// heads of hk against the split's token range.  A producer warp streams K and
+// V tiles of 64 tokens into shared memory with 2-D TMA (128-byte swizzle,
+// mbarrier-tracked, NSTAGE deep); four consumer warps each take 16 tokens of a
+// tile and compute, with mma.sync m16n8k16 (tokens on M, query heads on N):
+//   S^T = K_tile Q^T          (16 tokens x 8 heads, fp32)
+//   online softmax per head   (running max m, running sum l, base-2 exponent)
+//   O^T += V_tile^T P^T       (D x 8 heads, fp32; P^T is the S^T fragment
+//                              transposed in registers with movmatrix)
+// The four warps' (m, l, O) are merged through shared memory at the end.
+// With one split the CTA writes o and lse directly; otherwise it writes a
+// partial (m, l, unnormalised O) that the combine kernel merges.
+//
+// Method: scaled dot-product attention of one decode query over the kept
+// cache ("Rethinking KV Cache Compression" guide, §16 "Prefill、decode、TP 的
+// 性能账": each decode step reads the whole kept history, so the step is
+// bandwidth bound and every byte is read once).
+#include "kvc_device.cuh"
+#include "kvc_internal.h"
+
+#include <math.h>
+
+namespace kvc {
+
+namespace {
+
+constexpr int NCW = 4;                 // consumer warps (16 tokens of a tile each)
+constexpr int NTHREADS = (NCW + 1) * 32;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+template <int D> struct SlotCfg {
+    static constexpr int NBOX = D / 64;                 // 64-half (128-byte) boxes per row
+    static constexpr int TILE_BYTES = TILE * D * 2;     // one K or V tile
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K + V
+    static constexpr int NSTAGE = (D == 128) ? 3 : 6;
+    static constexpr int SMEM = NSTAGE * STAGE_BYTES + 1024 + 2 * NSTAGE * 8;
+    static_assert(NCW * (8 * D + 16) * 4 <= NSTAGE * STAGE_BYTES, "combine scratch must fit");
+};
+
+struct SlotParams {
+    int Hq, Hkv, C, g;
+    int splits, tiles_per_split;
+    int part_splits, part_offset;   // partial array geometry (ring mode writes one slot)
+    const uint16_t *q;
+    uint16_t *o;
+    const int32_t *n;               // valid slots per unit (slot mode)
+    const int32_t *len;             // tokens per sequence (ring mode)
+    int R;                          // residual length (ring mode)
+    float *logits, *lse;
+    float *part_o, *part_ml;
+    float scale, scale_log2;
+    int *status;
+};
+
+__device__ __forceinline__ void consumer_bar()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
+}
+
+// RING = false: slots [0, n) of a slot cache are valid.
+// RING = true : the unit's C = R + 32 ring slots; slot s holds the newest
+//               position p < T with p = s (mod C), valid when p >= n_q.
+template <int D, bool RING>
+__global__ void __launch_bounds__(NTHREADS, 2)
+    k_attend_slots(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const SlotParams p)
+{
+    using Cfg = SlotCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES);
+    uint64_t *empty = full + Cfg::NSTAGE;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int unit = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+    const int b = unit / p.Hkv, hk = unit % p.Hkv;
+
+    // token range of this split
+    int n_valid, ring_T = 0, ring_nres = 0;
+    if (RING) {
+        ring_T = p.len[b];
+        int over = ring_T - p.R;
+        int n_q = over > 0 ? (over / KIVI_G) * KIVI_G : 0;
+        ring_nres = ring_T - n_q;
+        n_valid = p.C;   // scan the whole ring, mask by age
+    } else {
+        n_valid = p.n[unit];
+        if (n_valid > p.C) {
+            if (threadIdx.x == 0)
+                flag_error(p.status, DEV_CAPACITY);
+            n_valid = p.C;
+        }
+        if (n_valid < 0)
+            n_valid = 0;
+    }
+    const int t_begin = split * p.tiles_per_split * TILE;
+    const int t_end = min(n_valid, t_begin + p.tiles_per_split * TILE);
+    const int ntiles = t_end > t_begin ? (t_end - t_begin + TILE - 1) / TILE : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Cfg::NSTAGE; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NCW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == NCW) {
+        // ---------------- producer: TMA K/V tiles into the stage ring
+        if (lane == 0 && ntiles > 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            const int row0 = unit * p.C + t_begin;
+            for (int i = 0; i < ntiles; ++i) {
+                const int st = i % Cfg::NSTAGE;
+                if (i >= Cfg::NSTAGE && !mbar_wait(&empty[st], ((i / Cfg::NSTAGE) & 1) ^ 1)) {
+                    flag_error(p.status, DEV_TIMEOUT);
+                    break;
+                }
+                uint8_t *kt = smem + st * Cfg::STAGE_BYTES;
+                uint8_t *vt = kt + Cfg::TILE_BYTES;
+                mbar_arrive_expect_tx(&full[st], Cfg::STAGE_BYTES);
+#pragma unroll
+                for (int j = 0; j < Cfg::NBOX; ++j) {
+                    tma_load_2d(kt + j * TILE * 128, &tmK, &full[st], 64 * j, row0 + i * TILE);
+                    tma_load_2d(vt + j * TILE * 128, &tmV, &full[st], 64 * j, row0 + i * TILE);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int r = lane >> 2, c = lane & 3;
+    const int mi = lane >> 3, ri = lane & 7;
+
+    // Q^T as the B operand: b0 = Q[head r][16s + 2c, +1], b1 = Q[head r][16s + 2c + 8, +1]
+    uint32_t qf[D / 16][2];
+    {
+        const bool hv = r < p.g;
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+            p.q + ((size_t)b * p.Hq + hk * p.g + (hv ? r : 0)) * D);
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+            qf[s][0] = hv ? qrow[8 * s + c] : 0u;
+            qf[s][1] = hv ? qrow[8 * s + c + 4] : 0u;
+        }
+    }
+
+    float acc[D / 16][4];
+#pragma unroll
+    for (int m = 0; m < D / 16; ++m)
+        acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+    float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
+    const int h0 = 2 * c, h1 = 2 * c + 1;
+    float *lg0 = nullptr, *lg1 = nullptr;
+    if (!RING && p.logits) {
+        const size_t rowbase = ((size_t)b * p.Hq + hk * p.g) * p.C;
+        lg0 = h0 < p.g ? p.logits + rowbase + (size_t)h0 * p.C : nullptr;
+        lg1 = h1 < p.g ? p.logits + rowbase + (size_t)h1 * p.C : nullptr;
+    }
+
+    for (int i = 0; i < ntiles; ++i) {
+        const int st = i % Cfg::NSTAGE;
+        if (!mbar_wait(&full[st], (i / Cfg::NSTAGE) & 1)) {
+            flag_error(p.status, DEV_TIMEOUT);
+            break;
+        }
+        const int tok0 = t_begin + i * TILE + 16 * warp;
+        if (tok0 < t_end) {
+            const uint32_t kbase = smem_u32(smem + st * Cfg::STAGE_BYTES);
+            const uint32_t vbase = kbase + Cfg::TILE_BYTES;
+
+            float sa[4] = {0.f, 0.f, 0.f, 0.f};
+            const int krow = 16 * warp + ri + 8 * (mi & 1);
+#pragma unroll
+            for (int s = 0; s < D / 16; ++s) {
+                const int ch = 2 * s + (mi >> 1);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(swz128(kbase + (ch >> 3) * TILE * 128, krow, ch & 7), a0, a1, a2, a3);
+                mma16816(sa, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+            }
+
+            const int ta = tok0 + r, tb = tok0 + r + 8;
+            bool va = ta < t_end, vb = tb < t_end;
+            if (RING) {
+                const int CR = p.C;
+                va = va && ((ring_T - 1 - ta) % CR + CR) % CR < ring_nres;
+                vb = vb && ((ring_T - 1 - tb) % CR + CR) % CR < ring_nres;
+            }
+            if (!RING && lg0) {
+                if (va) lg0[ta] = sa[0] * p.scale;
+                if (vb) lg0[tb] = sa[2] * p.scale;
+            }
+            if (!RING && lg1) {
+                if (va) lg1[ta] = sa[1] * p.scale;
+                if (vb) lg1[tb] = sa[3] * p.scale;
+            }
+            const float x0 = va ? sa[0] * p.scale_log2 : -INFINITY;
+            const float x1 = va ? sa[1] * p.scale_log2 : -INFINITY;
+            const float x2 = vb ? sa[2] * p.scale_log2 : -INFINITY;
+            const float x3 = vb ? sa[3] * p.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
+            const float al0 = mn0 == -INFINITY ? 1.f : ex2(m_run0 - mn0);
+            const float al1 = mn1 == -INFINITY ? 1.f : ex2(m_run1 - mn1);
+            const float p0 = mn0 == -INFINITY ? 0.f : ex2(x0 - mn0);
+            const float p2 = mn0 == -INFINITY ? 0.f : ex2(x2 - mn0);
+            const float p1 = mn1 == -INFINITY ? 0.f : ex2(x1 - mn1);
+            const float p3 = mn1 == -INFINITY ? 0.f : ex2(x3 - mn1);
+            m_run0 = mn0;
+            m_run1 = mn1;
+            l_run0 = l_run0 * al0 + p0 + p2;
+            l_run1 = l_run1 * al1 + p1 + p3;
+#pragma unroll
+            for (int m = 0; m < D / 16; ++m) {
+                acc[m][0] *= al0;
+                acc[m][1] *= al1;
+                acc[m][2] *= al0;
+                acc[m][3] *= al1;
+            }
+            const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
+            const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
+            const int vrow = 16 * warp + ri + 8 * (mi >> 1);
+#pragma unroll
+            for (int m = 0; m < D / 16; ++m) {
+                const int ch = 2 * m + (mi & 1);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(swz128(vbase + (ch >> 3) * TILE * 128, vrow, ch & 7), a0, a1, a2, a3);
+                mma16816(acc[m], a0, a1, a2, a3, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[st]);
+    }
+
+    // ---------------- merge the four warps
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, off);
+        l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, off);
+    }
+    consumer_bar();   // every consumer is past its last shared-memory read
+    float *redO = reinterpret_cast<float *>(smem);        // [NCW][8][D]
+    float *redM = redO + NCW * 8 * D;                     // [NCW][8]
+    float *redL = redM + NCW * 8;                         // [NCW][8]
+    {
+        float *w = redO + warp * 8 * D;
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) {
+            w[h0 * D + 16 * m + r] = acc[m][0];
+            w[h1 * D + 16 * m + r] = acc[m][1];
+            w[h0 * D + 16 * m + r + 8] = acc[m][2];
+            w[h1 * D + 16 * m + r + 8] = acc[m][3];
+        }
+        if (r == 0) {
+            redM[warp * 8 + h0] = m_run0;
+            redM[warp * 8 + h1] = m_run1;
+            redL[warp * 8 + h0] = l_run0;
+            redL[warp * 8 + h1] = l_run1;
+        }
+    }
+    consumer_bar();
+    const bool single = (p.part_o == nullptr);
+    for (int e = threadIdx.x; e < p.g * D; e += NCW * 32) {
+        const int h = e / D, d = e % D;
+        float ms = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w)
+            ms = fmaxf(ms, redM[w * 8 + h]);
+        float ls = 0.f, os = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+            const float mw = redM[w * 8 + h];
+            const float sc = mw == -INFINITY ? 0.f : ex2(mw - ms);
+            ls += sc * redL[w * 8 + h];
+            os += sc * redO[(w * 8 + h) * D + d];
+        }
+        if (single) {
+            const size_t oi = ((size_t)b * p.Hq + hk * p.g + h) * D + d;
+            p.o[oi] = __half_as_ushort(__float2half_rn(ls > 0.f ? os / ls : 0.f));
+            if (d == 0 && p.lse)
+                p.lse[(size_t)b * p.Hq + hk * p.g + h] =
+                    ls > 0.f ? (ms + __log2f(ls)) * LN2 : -INFINITY;
+        } else {
+            const size_t pi = ((size_t)unit * p.part_splits + p.part_offset + split) * p.g + h;
+            p.part_o[pi * D + d] = os;
+            if (d == 0) {
+                p.part_ml[2 * pi] = ls > 0.f ? ms : -INFINITY;
+                p.part_ml[2 * pi + 1] = ls;
+            }
+        }
+    }
+}
+
+// Merge split partials: o = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s.
+__global__ void k_combine(int Hq, int Hkv, int g, int D, int splits, const float *__restrict__ part_o,
+                          const float *__restrict__ part_ml, uint16_t *__restrict__ o,
+                          float *__restrict__ lse)
+{
+    const int bh = blockIdx.x;
+    const int b = bh / Hq, hq = bh % Hq, hk = hq / g, h = hq % g;
+    const size_t base = ((size_t)(b * Hkv + hk) * splits) * g + h;
+    float ms = -INFINITY;
+    for (int s = 0; s < splits; ++s)
+        ms = fmaxf(ms, part_ml[2 * (base + (size_t)s * g)]);
+    float ls = 0.f;
+    for (int s = 0; s < splits; ++s) {
+        const float m = part_ml[2 * (base + (size_t)s * g)];
+        ls += (m == -INFINITY ? 0.f : ex2(m - ms)) * part_ml[2 * (base + (size_t)s * g) + 1];
+    }
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float os = 0.f;
+        for (int s = 0; s < splits; ++s) {
+            const float m = part_ml[2 * (base + (size_t)s * g)];
+            if (m != -INFINITY)
+                os += ex2(m - ms) * part_o[(base + (size_t)s * g) * D + d];
+        }
+        o[(size_t)bh * D + d] = __half_as_ushort(__float2half_rn(ls > 0.f ? os / ls : 0.f));
+    }
+    if (threadIdx.x == 0 && lse)
+        lse[bh] = ls > 0.f ? (ms + __log2f(ls)) * LN2 : -INFINITY;
+}
+
+template <int D, bool RING>
+cudaError_t launch_slots_impl(const CUtensorMap &tk, const CUtensorMap &tv, const SlotParams &sp,
+                              int grid, cudaStream_t s)
+{
+    using Cfg = SlotCfg<D>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(k_attend_slots<D, RING>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+        if (e != cudaSuccess)
+            return e;
+        configured_device = dev;
+    }
+    k_attend_slots<D, RING><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
+{
+    const int units = a.B * a.Hkv;
+    CUtensorMap tk, tv;
+    const uint64_t rows = (uint64_t)units * a.C;
+    if (!encode_tmap_2d_f16(&tk, a.K, a.D, rows, 64, TILE) ||
+        !encode_tmap_2d_f16(&tv, a.V, a.D, rows, 64, TILE))
+        return cudaErrorInvalidValue;
+    SlotParams sp{};
+    sp.Hq = a.Hq;
+    sp.Hkv = a.Hkv;
+    sp.C = a.C;
+    sp.g = a.Hq / a.Hkv;
+    sp.splits = a.splits;
+    sp.tiles_per_split = a.tiles_per_split;
+    sp.part_splits = a.splits;
+    sp.part_offset = 0;
+    sp.q = a.q;
+    sp.o = a.o;
+    sp.n = a.n;
+    sp.len = nullptr;
+    sp.R = 0;
+    sp.logits = a.logits;
+    sp.lse = a.splits == 1 ? a.lse : nullptr;
+    sp.part_o = a.splits == 1 ? nullptr : a.part_o;
+    sp.part_ml = a.splits == 1 ? nullptr : a.part_ml;
+    sp.scale = a.scale;
+    sp.scale_log2 = a.scale * LOG2E;
+    sp.status = dev_status_ptr();
+    const int grid = units * a.splits;
+    cudaError_t e = a.D == 128 ? launch_slots_impl<128, false>(tk, tv, sp, grid, s)
+                               : launch_slots_impl<64, false>(tk, tv, sp, grid, s);
+    if (e != cudaSuccess || a.splits == 1)
+        return e;
+    return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);
+}
+
+// Residual ring of a KIVI cache: one work item per unit, written as partial
+// number `part_offset` of `part_splits`.
+cudaError_t launch_attend_ring(int B, int Hq, int Hkv, int D, int R, const uint16_t *q,
+                               const uint16_t *k_res, const uint16_t *v_res, const int32_t *len,
+                               float *part_o, float *part_ml, int part_splits, int part_offset,
+                               float scale, cudaStream_t s)
+{
+    const int units = B * Hkv;
+    const int CR = R + KIVI_G;
+    CUtensorMap tk, tv;
+    if (!encode_tmap_2d_f16(&tk, k_res, D, (uint64_t)units * CR, 64, TILE) ||
+        !encode_tmap_2d_f16(&tv, v_res, D, (uint64_t)units * CR, 64, TILE))
+        return cudaErrorInvalidValue;
+    SlotParams sp{};
+    sp.Hq = Hq;
+    sp.Hkv = Hkv;
+    sp.C = CR;
+    sp.g = Hq / Hkv;
+    sp.splits = 1;
+    sp.tiles_per_split = (CR + TILE - 1) / TILE;
+    sp.part_splits = part_splits;
+    sp.part_offset = part_offset;
+    sp.q = q;
+    sp.len = len;
+    sp.R = R;
+    sp.part_o = part_o;
+    sp.part_ml = part_ml;
+    sp.scale = scale;
+    sp.scale_log2 = scale * LOG2E;
+    sp.status = dev_status_ptr();
+    return D == 128 ? launch_slots_impl<128, true>(tk, tv, sp, units, s)
+                    : launch_slots_impl<64, true>(tk, tv, sp, units, s);
+}
+
+cudaError_t launch_combine(int B, int Hq, int Hkv, int D, int splits, const float *part_o,
+                           const float *part_ml, uint16_t *o, float *lse, cudaStream_t s)
+{
+    k_combine<<<B * Hq, D, 0, s>>>(Hq, Hkv, Hq / Hkv, D, splits, part_o, part_ml, o, lse);
+    return cudaGetLastError();
+}
+
+} // namespace kvc

@@ -1,0 +1,379 @@
+// evict.cu -- keep-set selection and in-place compaction of slot caches.
+//
+// One CTA per (sequence, KV head) unit:
+//   1. decide the keep set
+//        H2O    ("Rethinking KV Cache Compression" guide, §2 and §16 "4 种方法
+//               逐步执行"): the recent window pos >= T - n_recent, plus the
+//               n_heavy other slots with the largest accumulated scores (ties:
+//               lower position) -- a radix select of the n_heavy-th smallest
+//               composite key (descending-score bits << 32 | pos);
+//        Stream (same page): pos < n_sink or pos >= T - n_recent, closed form;
+//        Random ("KV Cache 驱逐实战", section "参考实现"): prompt slots stay;
+//               n_keep = max(1, int(n_cand * keep_ratio)) candidates with the
+//               smallest 64-bit Philox4x32-10 keys (ties: lower position),
+//               drawn independently in every head;
+//   2. compact: with n' kept slots, the k-th hole in [0, n') receives the k-th
+//      kept slot of [n', n) (mark and compact, "Practical Online KV Cache
+//      Compaction for LLM Agents", §4.2; the pos array is the logical ->
+//      physical map).  Sources and destinations never overlap, so the moves
+//      run in parallel; K, V, pos (and H2O scores) move together.
+#include "kvc_device.cuh"
+#include "kvc_internal.h"
+
+namespace kvc {
+
+namespace {
+
+constexpr int ETHREADS = 256;
+constexpr int NWARPS = ETHREADS / 32;
+constexpr int HOLE_CAP = 2048;   // hole/tail pairs handled per compaction round
+constexpr int MAX_SLOTS = 65536; // slot capacity the keep bitmask covers
+
+struct EvictParams {
+    int Hkv, D, C;
+    uint16_t *K, *V;
+    int32_t *pos, *n;
+    const int32_t *seqlen;
+    float *scores;
+    int n_heavy, n_recent, n_sink, prompt_len;
+    double keep_ratio;
+    uint32_t seed_lo, seed_hi, epoch;
+    int *status;
+};
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of
+// (c0,c1,c2,c3) -> (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)),
+// M0 = 0xD2511F53, M1 = 0xCD9E8D57, key bumped by (0x9E3779B9, 0xBB67AE85).
+__device__ __forceinline__ uint64_t philox_key(uint32_t k0, uint32_t k1, uint32_t c0, uint32_t c1,
+                                               uint32_t c2, uint32_t c3)
+{
+#pragma unroll
+    for (int rnd = 0; rnd < 10; ++rnd) {
+        if (rnd > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return ((uint64_t)c0 << 32) | c1;
+}
+
+// Order-preserving map of a float to uint32, reversed so larger scores give
+// smaller keys.
+__device__ __forceinline__ uint32_t desc_bits(float x)
+{
+    uint32_t u = __float_as_uint(x);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ~u;
+}
+
+struct Shared {
+    uint32_t hist[256];
+    int warp_tot[NWARPS];
+    int bcast[4];
+    uint32_t keep[MAX_SLOTS / 32];
+    int hole[HOLE_CAP];
+    int mv_src[HOLE_CAP];
+    int mv_dst[HOLE_CAP];
+};
+
+// Exclusive block-wide scan of one int per thread; returns the exclusive
+// prefix and sets *total.  All threads must call it.
+__device__ __forceinline__ int block_scan(int v, int *total, Shared &sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off)
+            x += y;
+    }
+    if (lane == 31)
+        sh.warp_tot[warp] = x;
+    __syncthreads();
+    int base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) {
+        if (w < warp)
+            base += sh.warp_tot[w];
+        tot += sh.warp_tot[w];
+    }
+    __syncthreads();
+    *total = tot;
+    return base + x - v;
+}
+
+__device__ __forceinline__ int block_count(bool pred, Shared &sh)
+{
+    int tot;
+    block_scan(pred ? 1 : 0, &tot, sh);
+    return tot;
+}
+
+// k-th smallest (1-based) of key(j) over slots j < n with filt(j), radix 8 bits
+// at a time from the top of `nbits`.  Returns the key value; *rank_left gets
+// how many slots equal to it are within the first k.
+template <typename KeyFn, typename FiltFn>
+__device__ uint64_t radix_select(int n, int k, int nbits, KeyFn key, FiltFn filt, int *rank_left,
+                                 Shared &sh)
+{
+    uint64_t prefix = 0, mask = 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int shift = nbits - 8; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += ETHREADS)
+            sh.hist[i] = 0;
+        __syncthreads();
+        for (int j = threadIdx.x; j < n; j += ETHREADS) {
+            if (!filt(j))
+                continue;
+            const uint64_t kk = key(j);
+            if ((kk & mask) == prefix)
+                atomicAdd(&sh.hist[(kk >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int s = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                s += (int)sh.hist[8 * lane + i];
+            int incl = s;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off)
+                    incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, incl >= k);
+            const int src = hit ? __ffs(hit) - 1 : 31;
+            if (lane == src) {
+                int cum = incl - s, dsel = 8 * lane + 7;
+                for (int i = 0; i < 8; ++i) {
+                    const int h = (int)sh.hist[8 * lane + i];
+                    if (cum + h >= k) {
+                        dsel = 8 * lane + i;
+                        break;
+                    }
+                    cum += h;
+                }
+                sh.bcast[0] = dsel;
+                sh.bcast[1] = k - cum;
+            }
+        }
+        __syncthreads();
+        prefix |= (uint64_t)sh.bcast[0] << shift;
+        mask |= (uint64_t)0xff << shift;
+        k = sh.bcast[1];
+        __syncthreads();
+    }
+    *rank_left = k;
+    return prefix;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(ETHREADS) k_evict(const EvictParams p)
+{
+    __shared__ Shared sh;
+    const int unit = blockIdx.x, b = unit / p.Hkv, hk = unit % p.Hkv;
+    int n = p.n[unit];
+    if (n > p.C || n < 0) {
+        if (threadIdx.x == 0)
+            flag_error(p.status, DEV_CAPACITY);
+        return;
+    }
+    const long T = p.seqlen[b];
+    const int32_t *pos = p.pos + (size_t)unit * p.C;
+    float *sc = p.scores ? p.scores + (size_t)unit * p.C : nullptr;
+
+    // ---- 1. keep predicate
+    uint64_t kth = 0;
+    uint32_t pth = 0;
+    int n_new = 0;
+    if (KIND == EVICT_H2O) {
+        const long rt = T - p.n_recent;
+        auto is_recent = [&](int j) { return (long)pos[j] >= rt; };
+        int n_rec = 0;
+        for (int base = 0; base < n; base += ETHREADS) {
+            const int j = base + threadIdx.x;
+            n_rec += block_count(j < n && is_recent(j), sh);
+        }
+        const int n_cand = n - n_rec;
+        const int take = min(p.n_heavy, n_cand);
+        if (take >= n_cand)
+            return; // nothing to drop
+        n_new = n_rec + take;
+        if (take > 0) {
+            int left;
+            kth = radix_select(
+                n, take, 64,
+                [&](int j) { return ((uint64_t)desc_bits(sc[j]) << 32) | (uint32_t)pos[j]; },
+                [&](int j) { return !is_recent(j); }, &left, sh);
+        }
+    } else if (KIND == EVICT_STREAM) {
+        int kept = 0;
+        for (int base = 0; base < n; base += ETHREADS) {
+            const int j = base + threadIdx.x;
+            const bool k = j < n && ((long)pos[j] < p.n_sink || (long)pos[j] >= T - p.n_recent);
+            kept += block_count(k, sh);
+        }
+        if (kept == n)
+            return;
+        n_new = kept;
+    } else {
+        int n_cand = 0;
+        for (int base = 0; base < n; base += ETHREADS) {
+            const int j = base + threadIdx.x;
+            n_cand += block_count(j < n && pos[j] >= p.prompt_len, sh);
+        }
+        if (n_cand == 0)
+            return;
+        int n_keep = (int)((double)n_cand * p.keep_ratio);
+        n_keep = n_keep < 1 ? 1 : (n_keep > n_cand ? n_cand : n_keep);
+        if (n_keep == n_cand)
+            return;
+        n_new = n - n_cand + n_keep;
+        auto rkey = [&](int j) {
+            return philox_key(p.seed_lo, p.seed_hi, (uint32_t)pos[j], (uint32_t)hk, (uint32_t)b,
+                              p.epoch);
+        };
+        int left;
+        kth = radix_select(n, n_keep, 64, rkey, [&](int j) { return pos[j] >= p.prompt_len; },
+                           &left, sh);
+        // among candidates whose key equals the threshold keep the `left` lowest positions
+        int left2;
+        pth = (uint32_t)radix_select(
+            n, left, 32, [&](int j) { return (uint64_t)(uint32_t)pos[j]; },
+            [&](int j) { return pos[j] >= p.prompt_len && rkey(j) == kth; }, &left2, sh);
+    }
+
+    auto keep = [&](int j) -> bool {
+        if (KIND == EVICT_H2O) {
+            if ((long)pos[j] >= T - p.n_recent)
+                return true;
+            return (((uint64_t)desc_bits(sc[j]) << 32) | (uint32_t)pos[j]) <= kth &&
+                   p.n_heavy > 0;
+        } else if (KIND == EVICT_STREAM) {
+            return (long)pos[j] < p.n_sink || (long)pos[j] >= T - p.n_recent;
+        } else {
+            if (pos[j] < p.prompt_len)
+                return true;
+            const uint64_t k = philox_key(p.seed_lo, p.seed_hi, (uint32_t)pos[j], (uint32_t)hk,
+                                          (uint32_t)b, p.epoch);
+            return k < kth || (k == kth && (uint32_t)pos[j] <= pth);
+        }
+    };
+
+    // ---- 2. keep flags, taken once before any slot moves (moves change pos)
+    for (int base = 0; base < n; base += ETHREADS) {
+        const int j = base + threadIdx.x;
+        const unsigned bits = __ballot_sync(0xffffffffu, j < n && keep(j));
+        if ((threadIdx.x & 31) == 0 && j < n)
+            sh.keep[j >> 5] = bits;
+    }
+    __syncthreads();
+    auto kept = [&](int j) { return (sh.keep[j >> 5] >> (j & 31)) & 1u; };
+
+    // ---- 3. compaction: k-th hole of [0, n_new) <- k-th kept slot of [n_new, n).
+    // Holes and tail-kept slots are equal in number; ranks are assigned in
+    // slot order in rounds of HOLE_CAP pairs.
+    int n_pairs = 0;
+    for (int base = 0; base < n_new; base += ETHREADS) {
+        const int j = base + threadIdx.x;
+        n_pairs += block_count(j < n_new && !kept(j), sh);
+    }
+    const int D = p.D;
+    for (int round0 = 0; round0 < n_pairs; round0 += HOLE_CAP) {
+        int seen = 0;
+        for (int base = 0; base < n_new; base += ETHREADS) {
+            const int j = base + threadIdx.x;
+            const bool h = j < n_new && !kept(j);
+            int tot;
+            const int rk = seen + block_scan(h ? 1 : 0, &tot, sh);
+            if (h && rk >= round0 && rk < round0 + HOLE_CAP)
+                sh.hole[rk - round0] = j;
+            seen += tot;
+        }
+        seen = 0;
+        for (int base = n_new; base < n; base += ETHREADS) {
+            const int j = base + threadIdx.x;
+            const bool t = j < n && kept(j);
+            int tot;
+            const int rk = seen + block_scan(t ? 1 : 0, &tot, sh);
+            if (t && rk >= round0 && rk < round0 + HOLE_CAP) {
+                sh.mv_src[rk - round0] = j;
+                sh.mv_dst[rk - round0] = sh.hole[rk - round0];
+            }
+            seen += tot;
+        }
+        __syncthreads();
+        const int cnt = min(HOLE_CAP, n_pairs - round0);
+        // move rows: one warp per pair; 16-byte chunks of K then V
+        const int chunks = D / 8;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        for (int k = warp; k < cnt; k += NWARPS) {
+            const size_t src = (size_t)unit * p.C + sh.mv_src[k];
+            const size_t dst = (size_t)unit * p.C + sh.mv_dst[k];
+            uint4 *K4 = reinterpret_cast<uint4 *>(p.K), *V4 = reinterpret_cast<uint4 *>(p.V);
+            for (int ch = lane; ch < 2 * chunks; ch += 32) {
+                if (ch < chunks)
+                    K4[dst * chunks + ch] = K4[src * chunks + ch];
+                else
+                    V4[dst * chunks + ch - chunks] = V4[src * chunks + ch - chunks];
+            }
+            if (lane == 0) {
+                p.pos[dst] = p.pos[src];
+                if (sc)
+                    p.scores[dst] = p.scores[src];
+            }
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0)
+        p.n[unit] = n_new;
+}
+
+} // namespace
+
+cudaError_t launch_evict(const EvictLaunch &e, cudaStream_t s)
+{
+    EvictParams p{};
+    p.Hkv = e.c.Hkv;
+    p.D = e.c.D;
+    p.C = e.c.C;
+    p.K = e.c.K;
+    p.V = e.c.V;
+    p.pos = e.c.pos;
+    p.n = e.c.n;
+    p.seqlen = e.c.seqlen;
+    p.scores = e.scores;
+    p.n_heavy = e.n_heavy;
+    p.n_recent = e.n_recent;
+    p.n_sink = e.n_sink;
+    p.prompt_len = e.prompt_len;
+    p.keep_ratio = e.keep_ratio;
+    p.seed_lo = (uint32_t)(e.seed & 0xffffffffu);
+    p.seed_hi = (uint32_t)(e.seed >> 32);
+    p.epoch = e.epoch;
+    p.status = dev_status_ptr();
+    const int grid = e.c.B * e.c.Hkv;
+    switch (e.kind) {
+    case EVICT_H2O:
+        k_evict<EVICT_H2O><<<grid, ETHREADS, 0, s>>>(p);
+        break;
+    case EVICT_STREAM:
+        k_evict<EVICT_STREAM><<<grid, ETHREADS, 0, s>>>(p);
+        break;
+    default:
+        k_evict<EVICT_RANDOM><<<grid, ETHREADS, 0, s>>>(p);
+        break;
+    }
+    return cudaGetLastError();
+}
+
+} // namespace kvc

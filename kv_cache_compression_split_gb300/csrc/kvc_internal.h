@@ -1,0 +1,86 @@
+// kvc_internal.h -- host-side glue shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+constexpr int TILE = 64;           // tokens per pipeline stage of the decode kernels
+constexpr int KIVI_G = KVC_KIVI_GROUP;
+
+// Device status word of the current device (set-up once per device).
+int *dev_status_ptr();
+
+// SM count of the current device.
+int sm_count();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+bool encode_tmap_2d_f16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                        uint32_t box_inner, uint32_t box_rows);
+
+struct SlotAttendPlan {
+    int splits;
+    int tiles_per_split;
+};
+
+// Split plan shared by kvc_workspace_size and kvc_decode_attend.
+SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested_splits);
+
+// ---- launchers (each returns a cudaError_t of the launch) ----
+
+struct AttendLaunch {
+    int B, Hq, Hkv, D, C;
+    const uint16_t *q;
+    uint16_t *o;
+    const uint16_t *K, *V;
+    const int32_t *n;
+    float *logits, *lse;
+    float *part_o, *part_ml;
+    int splits, tiles_per_split;
+    float scale;
+};
+cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s);
+
+struct KiviAttendLaunch {
+    int B, Hq, Hkv, D, bits, R, Cq;
+    const uint16_t *q;
+    uint16_t *o;
+    const uint8_t *kb, *vb;
+    const uint16_t *k_res, *v_res;
+    const int32_t *len;
+    float *lse;
+    float *part_o, *part_ml;
+    int splits, tiles_per_split;
+    float scale;
+};
+cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s);
+
+cudaError_t launch_combine(int B, int Hq, int Hkv, int D, int splits, const float *part_o,
+                           const float *part_ml, uint16_t *o, float *lse, cudaStream_t s);
+
+cudaError_t launch_append_slots(const kvc_slot_cache &c, const uint16_t *k_new,
+                                const uint16_t *v_new, int n_new, cudaStream_t s);
+cudaError_t launch_append_quant(const kvc_quant_cache &c, const uint16_t *k_new,
+                                const uint16_t *v_new, int n_new, cudaStream_t s);
+
+cudaError_t launch_h2o_decode_acc(const kvc_h2o_args &a, cudaStream_t s);
+cudaError_t launch_h2o_prefill(const kvc_h2o_args &a, float *lse_ws, cudaStream_t s);
+
+enum EvictKind { EVICT_H2O = 0, EVICT_STREAM = 1, EVICT_RANDOM = 2 };
+struct EvictLaunch {
+    EvictKind kind;
+    kvc_slot_cache c;
+    float *scores;
+    int n_heavy, n_recent, n_sink, prompt_len;
+    double keep_ratio;
+    uint64_t seed;
+    uint32_t epoch;
+};
+cudaError_t launch_evict(const EvictLaunch &e, cudaStream_t s);
+
+} // namespace kvc

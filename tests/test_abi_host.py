@@ -1,0 +1,70 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function that
+include/kvc.h declares, and answers host-side queries (no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    from kv_cache_compression_split_gb300 import build
+    build.build()
+    import kv_cache_compression_split_gb300 as k
+    k.lib()
+    return k
+
+
+def _declared():
+    hdr = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    return sorted(set(re.findall(r"KVC_API\s+[\w\s\*]+?\b(kvc_\w+)\s*\(", hdr)))
+
+
+def test_every_declared_symbol_is_exported(kvc):
+    names = _declared()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(kvc.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_host_queries(kvc):
+    assert kvc.kvc_kivi_block_bytes(128, 4) == 32 * 128 * 4 // 8 + 4 * 128 == 2560
+    assert kvc.kvc_kivi_block_bytes(128, 2) == 1536
+    assert kvc.kvc_kivi_block_bytes(64, 4) == 1280
+    assert kvc.kvc_kivi_block_bytes(96, 4) == 0      # unsupported head dim
+    assert kvc.kvc_kivi_block_bytes(128, 3) == 0     # unsupported width
+    assert "INVALID_ARG" in kvc.kvc_status_string(kvc.KVC_ERR_INVALID_ARG)
+    assert kvc.kvc_status_string(kvc.KVC_OK) == "KVC_OK"
+
+
+def test_null_arguments_are_rejected_without_touching_a_gpu(kvc):
+    lib = kvc.lib()
+    assert lib.kvc_append(None, None, None, 1, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_append_quant(None, None, None, 1, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_decode_attend(None, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_h2o_accumulate(None, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_h2o_evict(None, None, 1, 1, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_stream_evict(None, 1, 1, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_random_evict(None, 0, 0.5, 1, 0, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_read_device_status(None, None) == kvc.KVC_ERR_INVALID_ARG
+    # a descriptor with an unsupported head dim (pointers are never dereferenced on the host)
+    d = kvc.SlotCacheDesc(1, 1, 96, 16, 16, 16, 16, 16, 16)
+    assert lib.kvc_stream_evict(ctypes.byref(d), 1, 1, None) == kvc.KVC_ERR_UNSUPPORTED
+    d = kvc.SlotCacheDesc(1, 1, 128, 16, 16, 17, 16, 16, 16)     # misaligned V
+    assert lib.kvc_stream_evict(ctypes.byref(d), 1, 1, None) == kvc.KVC_ERR_INVALID_ARG
+    q = kvc.QuantCacheDesc(1, 1, 128, 3, 16, 32, 16, 16, 16, 16, 16)
+    assert lib.kvc_append_quant(ctypes.byref(q), None, None, 0, None) == kvc.KVC_ERR_UNSUPPORTED
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "kv_cache_compression_split_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f), errors="ignore").read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
+                assert "oracle.c" not in src and "liboracle" not in src, f

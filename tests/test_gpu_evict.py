@@ -1,0 +1,272 @@
+"""GPU parity: StreamingLLM, H2O and random eviction (keep-sets bit-exact vs the oracle,
+H2O scores within 1e-4 relative, compacted K/V/pos exact) and the append path."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import (SCORE_REL_TOL, assert_o_close, device_status_clean, np16,
+                     slot_cache_from)
+
+pytestmark = pytest.mark.gpu
+SEED = 0x243F6A8885A308D3
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    import kv_cache_compression_split_gb300 as k
+    k.lib()
+    return k
+
+
+def _units(cache):
+    """Per unit: (pos array of valid slots, K rows, V rows) on the host."""
+    n = cache.n.cpu().numpy()
+    pos = cache.pos.cpu().numpy()
+    K = cache.K.cpu().numpy().view(np.uint16)
+    V = cache.V.cpu().numpy().view(np.uint16)
+    return n, pos, K, V
+
+
+def _assert_content(cache, Kseq, Vseq, b, hk, expect_pos):
+    """Valid slots of unit (b,hk) hold exactly expect_pos, each with its original K/V row."""
+    n, pos, K, V = _units(cache)
+    nn = n[b, hk]
+    got = pos[b, hk, :nn]
+    assert sorted(got.tolist()) == sorted(int(p) for p in expect_pos), f"unit ({b},{hk})"
+    ks = Kseq[b, hk].cpu().numpy().view(np.uint16)
+    vs = Vseq[b, hk].cpu().numpy().view(np.uint16)
+    assert np.array_equal(K[b, hk, :nn], ks[got]) and np.array_equal(V[b, hk, :nn], vs[got])
+
+
+def test_append_then_capacity(kvc):
+    g = torch.Generator().manual_seed(1)
+    B, Hkv, C, D = 2, 3, 40, 64
+    k1 = torch.randn(B, Hkv, 30, D, generator=g).half().cuda()
+    v1 = torch.randn(B, Hkv, 30, D, generator=g).half().cuda()
+    cache = kvc.SlotCache.empty(B, Hkv, C, D)
+    kvc.kvc_append(cache, k1, v1)
+    kvc.kvc_append(cache, k1[:, :, :5].contiguous(), v1[:, :, :5].contiguous())
+    torch.cuda.synchronize()
+    assert cache.n.cpu().eq(35).all() and cache.seqlen.cpu().eq(35).all()
+    assert torch.equal(cache.K[:, :, :30], k1) and torch.equal(cache.V[:, :, 30:35], v1[:, :, :5])
+    assert cache.pos[0, 0, :35].cpu().tolist() == list(range(35))
+    assert device_status_clean(kvc)
+    kvc.kvc_append(cache, k1[:, :, :10].contiguous(), v1[:, :, :10].contiguous())   # 45 > 40
+    torch.cuda.synchronize()
+    assert kvc.kvc_read_device_status() & kvc.KVC_DEV_CAPACITY
+    assert cache.n.cpu().eq(35).all()     # units left unchanged
+
+
+@pytest.mark.parametrize("T,n_sink,n_recent", [(2048, 64, 448), (96, 4, 12), (10, 4, 12),
+                                               (700, 0, 100)])
+def test_stream_prefill_and_decode(kvc, orc, T, n_sink, n_recent):
+    g = torch.Generator().manual_seed(T)
+    B, Hkv, D = 2, 4, 128
+    C = T + 8
+    Kseq = torch.randn(B, Hkv, C, D, generator=g).half()
+    Vseq = torch.randn(B, Hkv, C, D, generator=g).half()
+    cache = slot_cache_from(kvc, Kseq, Vseq, np.full((B, Hkv), T), C, seqlen=[T] * B)
+    kvc.kvc_stream_evict(cache, n_sink, n_recent)
+    torch.cuda.synchronize()
+    keep = orc.stream_keep(np.arange(T), T, n_sink, n_recent)
+    for b in range(B):
+        for hk in range(Hkv):
+            _assert_content(cache, Kseq, Vseq, b, hk, np.flatnonzero(keep))
+    # decode: the next token is appended, attended over, then the window slides
+    kvc.kvc_append(cache, Kseq[:, :, T:T + 1].cuda().contiguous(), Vseq[:, :, T:T + 1].cuda().contiguous())
+    kvc.kvc_stream_evict(cache, n_sink, n_recent)
+    torch.cuda.synchronize()
+    keep = orc.stream_keep(np.arange(T + 1), T + 1, n_sink, n_recent)
+    for b in range(B):
+        for hk in range(Hkv):
+            _assert_content(cache, Kseq, Vseq, b, hk, np.flatnonzero(keep))
+    assert device_status_clean(kvc)
+
+
+def _check_keep_with_ties(keep_gpu_pos, pos, score_ref, T, n_heavy, n_recent):
+    """GPU keep-set == oracle keep-set, except swaps between candidates whose oracle scores
+    tie within 1e-6 relative."""
+    keep_ref, margin = None, None
+    import oracle as orc
+    keep_ref, margin = orc.h2o_keep(pos, score_ref, T, n_heavy, n_recent)
+    ref_set = set(pos[keep_ref].tolist())
+    got_set = set(int(p) for p in keep_gpu_pos)
+    if ref_set == got_set:
+        return 0
+    extra, missing = got_set - ref_set, ref_set - got_set
+    sc = {int(p): s for p, s in zip(pos, score_ref)}
+    assert len(extra) == len(missing)
+    for a, m in zip(sorted(extra, key=lambda p: -sc[p]), sorted(missing, key=lambda p: sc[p])):
+        assert abs(sc[a] - sc[m]) <= 1e-6 * max(abs(sc[a]), abs(sc[m])), (a, m, sc[a], sc[m])
+    return len(extra)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,D,n_heavy,n_recent", [
+    (1, 4, 4, 64, 64, 8, 8), (2, 8, 2, 300, 128, 16, 40), (1, 16, 2, 1000, 128, 64, 448),
+    (2, 4, 4, 130, 64, 200, 8)])
+def test_h2o_prefill_scores_and_evict(kvc, orc, B, Hq, Hkv, L, D, n_heavy, n_recent):
+    g = torch.Generator().manual_seed(L + Hq)
+    C = L + 4
+    Qp = torch.randn(B, Hq, L, D, generator=g).half()
+    Kseq = torch.randn(B, Hkv, C, D, generator=g).half()
+    Vseq = torch.randn(B, Hkv, C, D, generator=g).half()
+    cache = slot_cache_from(kvc, Kseq, Vseq, np.full((B, Hkv), L), C, seqlen=[L] * B)
+    scores = torch.zeros(B, Hkv, C, dtype=torch.float32, device="cuda")
+    ws = torch.empty(kvc.kvc_h2o_workspace_size(B, Hq, L) // 4, dtype=torch.float32, device="cuda")
+    kvc.kvc_h2o_accumulate_prefill(Qp.cuda(), cache.K, scores, ws, L)
+    torch.cuda.synchronize()
+    ref = orc.h2o_prefill_scores(np16(Qp), np16(Kseq), L, threads=4)
+    got = scores.cpu().numpy().astype(np.float64)[..., :L]
+    np.testing.assert_allclose(got, ref, rtol=SCORE_REL_TOL, atol=0)
+    kvc.kvc_h2o_evict(cache, scores, n_heavy, n_recent)
+    torch.cuda.synchronize()
+    n, pos, _, _ = _units(cache)
+    for b in range(B):
+        for hk in range(Hkv):
+            _check_keep_with_ties(pos[b, hk, :n[b, hk]], np.arange(L, dtype=np.int32), ref[b, hk],
+                                  L, n_heavy, n_recent)
+            # scores travel with their slots
+            sc = scores[b, hk, :n[b, hk]].cpu().numpy()
+            np.testing.assert_allclose(sc, ref[b, hk][pos[b, hk, :n[b, hk]]], rtol=SCORE_REL_TOL)
+            _assert_content(cache, Kseq, Vseq, b, hk, pos[b, hk, :n[b, hk]])
+    assert device_status_clean(kvc)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D", [(4, 64, 8, 128), (3, 8, 8, 64)])
+def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D):
+    """One decode step from a seeded post-prefill state: 64 heavy slots from [0, 1600) plus the
+    recent 448; append token 2048, attend over 513 slots, accumulate, evict back to 512."""
+    T, n_heavy, n_recent = 2048, 64, 448
+    g = torch.Generator().manual_seed(B * Hq)
+    rng = np.random.default_rng(B * Hq)
+    C = 520
+    Kseq = torch.randn(B, Hkv, T + 1, D, generator=g).half()
+    Vseq = torch.randn(B, Hkv, T + 1, D, generator=g).half()
+    q = torch.randn(B, Hq, D, generator=g).half()
+    cache = kvc.SlotCache.empty(B, Hkv, C, D)
+    pos0 = np.zeros((B, Hkv, 512), np.int32)
+    sc0 = np.zeros((B, Hkv, C), np.float32)
+    for b in range(B):
+        for hk in range(Hkv):
+            heavy = np.sort(rng.choice(T - n_recent, n_heavy, replace=False))
+            p = np.concatenate([heavy, np.arange(T - n_recent, T)]).astype(np.int32)
+            p = rng.permutation(p)                  # slot order is free
+            pos0[b, hk] = p
+            sc0[b, hk, :512] = rng.uniform(0.0, 4.0, 512).astype(np.float32)
+    pos_t = torch.from_numpy(pos0).long()
+    cache.K[:, :, :512] = torch.gather(Kseq, 2, pos_t[..., None].expand(-1, -1, -1, D)).cuda()
+    cache.V[:, :, :512] = torch.gather(Vseq, 2, pos_t[..., None].expand(-1, -1, -1, D)).cuda()
+    cache.pos[:, :, :512] = torch.from_numpy(pos0).cuda()
+    cache.n.fill_(512)
+    cache.seqlen.fill_(T)
+    scores = torch.from_numpy(sc0).cuda()
+    # the step
+    kvc.kvc_append(cache, Kseq[:, :, T:].cuda().contiguous(), Vseq[:, :, T:].cuda().contiguous())
+    o = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+    logits = torch.empty(B, Hq, C, dtype=torch.float32, device="cuda")
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), dtype=torch.float32,
+                     device="cuda")
+    kvc.kvc_decode_attend(cache, q.cuda(), o, logits=logits, lse=lse, workspace=ws)
+    kvc.kvc_h2o_accumulate_decode(cache, scores, logits, lse, Hq)
+    scores_after_acc = scores.clone()
+    kvc.kvc_h2o_evict(cache, scores, n_heavy, n_recent)
+    torch.cuda.synchronize()
+    # oracle from the same seeded state
+    pos513 = np.concatenate([pos0, np.full((B, Hkv, 1), T, np.int32)], axis=2)
+    Kc = np.take_along_axis(np16(Kseq), pos513[..., None].astype(np.int64), axis=2)
+    Vc = np.take_along_axis(np16(Vseq), pos513[..., None].astype(np.int64), axis=2)
+    ref_o, ref_lse, ref_lg = orc.decode_attend(np16(q), Kc, Vc, np.full((B, Hkv), 513),
+                                               want_logits=True)
+    assert_o_close(np16(o), ref_o)
+    sc_ref = np.concatenate([sc0[..., :512].astype(np.float64), np.zeros((B, Hkv, 1))], axis=2)
+    sc_ref = orc.h2o_accumulate(sc_ref, ref_lg, ref_lse, np.full((B, Hkv), 513))
+    np.testing.assert_allclose(scores_after_acc.cpu().numpy()[..., :513], sc_ref,
+                               rtol=SCORE_REL_TOL)
+    n, pos, _, _ = _units(cache)
+    assert (n == 512).all()
+    for b in range(B):
+        for hk in range(Hkv):
+            _check_keep_with_ties(pos[b, hk, :512], pos513[b, hk], sc_ref[b, hk], T + 1, n_heavy,
+                                  n_recent)
+            _assert_content(cache, Kseq, Vseq, b, hk, pos[b, hk, :512])
+    assert device_status_clean(kvc)
+
+
+def test_random_tiny_two_evictions(kvc, orc):
+    """Tiny workload: prompt 64 tokens with the first 16 locked, keep 0.5; evict after the prompt
+    (48 candidates -> 24), then after 32 more tokens (56 -> 28)."""
+    from kv_cache_compression_split_gb300 import workloads as W
+    w = W.TINY
+    B, Hkv, D, C = w.B, w.Hkv, w.D, 128
+    Kseq, Vseq = W.kv_tensors(w, T=96)
+    cache = kvc.SlotCache.empty(B, Hkv, C, D)
+    kvc.kvc_append(cache, Kseq[:, :, :64].cuda().contiguous(), Vseq[:, :, :64].cuda().contiguous())
+    kvc.kvc_random_evict(cache, w.prompt_len, w.keep_ratio, SEED, 0)
+    torch.cuda.synchronize()
+    _, pos, _, _ = _units(cache)
+    expect = {}
+    for hk in range(Hkv):
+        keep = orc.random_keep(np.arange(64), w.prompt_len, w.keep_ratio, SEED, 0, 0, hk)
+        expect[hk] = np.flatnonzero(keep)
+        assert len(expect[hk]) == 16 + 24
+        _assert_content(cache, Kseq, Vseq, 0, hk, expect[hk])
+    sets = [frozenset(expect[h].tolist()) for h in range(Hkv)]
+    assert len(set(sets)) == Hkv              # per-head draws differ; no union
+    kvc.kvc_append(cache, Kseq[:, :, 64:96].cuda().contiguous(), Vseq[:, :, 64:96].cuda().contiguous())
+    kvc.kvc_random_evict(cache, w.prompt_len, w.keep_ratio, SEED, 1)
+    torch.cuda.synchronize()
+    n, pos, _, _ = _units(cache)
+    for hk in range(Hkv):
+        p1 = np.concatenate([expect[hk], np.arange(64, 96)]).astype(np.int32)
+        keep = orc.random_keep(p1, w.prompt_len, w.keep_ratio, SEED, 1, 0, hk)
+        assert n[0, hk] == 16 + 28
+        _assert_content(cache, Kseq, Vseq, 0, hk, p1[keep])
+    assert device_status_clean(kvc)
+
+
+def test_random_reasoning_cadence(kvc, orc):
+    """Reasoning-trace workload shape (GQA 64/8, D 128, locked prompt 1024): three evictions
+    every 1024 generated tokens at keep 0.25 -> per head 1024 + 256, + 320, + 336 slots."""
+    from kv_cache_compression_split_gb300 import workloads as W
+    w = W.REASONING
+    B, Hkv, D = 4, w.Hkv, w.D
+    steps = 3
+    T_all = 1024 + 1024 * steps
+    Kseq, Vseq = W.kv_tensors(w, T=T_all, B=B)
+    C = 2048 + 512
+    cache = kvc.SlotCache.empty(B, Hkv, C, D)
+    kvc.kvc_append(cache, Kseq[:, :, :2048].cuda().contiguous(), Vseq[:, :, :2048].cuda().contiguous())
+    cur = {(b, h): np.arange(2048, dtype=np.int32) for b in range(B) for h in range(Hkv)}
+    for e in range(steps):
+        if e > 0:
+            t0 = 1024 + 1024 * e
+            kvc.kvc_append(cache, Kseq[:, :, t0:t0 + 1024].cuda().contiguous(),
+                           Vseq[:, :, t0:t0 + 1024].cuda().contiguous())
+            for k in cur:
+                cur[k] = np.concatenate([cur[k], np.arange(t0, t0 + 1024, dtype=np.int32)])
+        kvc.kvc_random_evict(cache, 1024, 0.25, SEED, e)
+        torch.cuda.synchronize()
+        for (b, h), p in cur.items():
+            keep = orc.random_keep(p, 1024, 0.25, SEED, e, b, h)
+            cur[(b, h)] = p[keep]
+        n, _, _, _ = _units(cache)
+        assert (n == 1024 + [256, 320, 336][e]).all()
+    for b in range(B):
+        for h in range(Hkv):
+            _assert_content(cache, Kseq, Vseq, b, h, cur[(b, h)])
+    assert device_status_clean(kvc)
+
+
+def test_random_ratio_one_and_empty_candidates(kvc):
+    g = torch.Generator().manual_seed(3)
+    B, Hkv, C, D = 1, 2, 64, 64
+    K = torch.randn(B, Hkv, C, D, generator=g).half()
+    cache = slot_cache_from(kvc, K, K, np.full((B, Hkv), 40), C, seqlen=[40])
+    before = cache.K.clone()
+    kvc.kvc_random_evict(cache, 8, 1.0, SEED, 0)       # keep all
+    kvc.kvc_random_evict(cache, 40, 0.5, SEED, 1)      # no candidates: no-op
+    torch.cuda.synchronize()
+    assert cache.n.cpu().eq(40).all() and torch.equal(cache.K, before)
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_random_evict(cache, 8, 1.5, SEED, 0)

@@ -1,0 +1,166 @@
+"""GPU parity: KIVI packing (bit-exact vs the oracle) and KIVI decode attention."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_o_close, device_status_clean, np16
+
+pytestmark = pytest.mark.gpu
+G = 32
+# The per-channel K scale is folded into the query, q~ = q * s rounded to binary16 (relative
+# error <= 2^-12 per product), so a KIVI logit carries up to ~1e-3 absolute error on these
+# inputs; the outputs still meet the 2e-3 bound, which assert_o_close checks.
+KIVI_LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    import kv_cache_compression_split_gb300 as k
+    k.lib()
+    return k
+
+
+def _build(kvc, Kseq, Vseq, bits, R, Cq, chunks, offsets=None):
+    """Append Kseq/Vseq [B,Hkv,T,D] through kvc_append_quant in the given chunk sizes.
+    offsets[b] tokens of sequence b are pre-placed in the residual ring first (ragged lengths)."""
+    B, Hkv, T, D = Kseq.shape
+    cache = kvc.QuantCache.empty(B, Hkv, Cq, D, bits, R)
+    off = np.zeros(B, np.int64) if offsets is None else np.asarray(offsets)
+    for b in range(B):
+        for p in range(off[b]):
+            cache.k_res[b, :, p % (R + G)] = Kseq[b, :, p]
+            cache.v_res[b, :, p % (R + G)] = Vseq[b, :, p]
+    cache.len.copy_(torch.as_tensor(off, dtype=torch.int32))
+    # per sequence b the appended stream is Kseq[b, :, off[b]:]
+    t = 0
+    for n_new in chunks:
+        kn = torch.stack([Kseq[b, :, off[b] + t: off[b] + t + n_new] for b in range(B)]).contiguous()
+        vn = torch.stack([Vseq[b, :, off[b] + t: off[b] + t + n_new] for b in range(B)]).contiguous()
+        kvc.kvc_append_quant(cache, kn, vn)
+        t += n_new
+    torch.cuda.synchronize()
+    return cache, off + t
+
+
+def _check_unit(orc, cache, Kseq, Vseq, b, hk, T, bits, R):
+    D = Kseq.shape[-1]
+    n_q = orc.kivi_nq(T, R)
+    Kb = np16(Kseq[b, hk, :T])
+    Vb = np16(Vseq[b, hk, :T])
+    if n_q > 0:
+        qz = orc.kivi_quantize_unit(Kb[:n_q], Vb[:n_q], n_q, bits)
+        kb, vb = orc.kivi_pack_unit(qz, D, bits)
+        gk = cache.k_blocks[b, hk, :n_q // G].cpu().numpy()
+        gv = cache.v_blocks[b, hk, :n_q // G].cpu().numpy()
+        assert np.array_equal(gk, kb), f"K blocks differ at unit ({b},{hk})"
+        assert np.array_equal(gv, vb), f"V blocks differ at unit ({b},{hk})"
+    kr = cache.k_res[b, hk].cpu().numpy().view(np.uint16)
+    vr = cache.v_res[b, hk].cpu().numpy().view(np.uint16)
+    for p in range(n_q, T):
+        s = p % (R + G)
+        assert np.array_equal(kr[s], Kb[p].view(np.uint16)) and np.array_equal(vr[s], Vb[p].view(np.uint16))
+
+
+@pytest.mark.parametrize("D,bits,R", [(128, 4, 128), (128, 2, 128), (64, 4, 16), (64, 2, 0),
+                                      (128, 4, 100)])
+def test_pack_bit_exact_with_flushes(kvc, orc, D, bits, R):
+    g = torch.Generator().manual_seed(D + bits + R)
+    B, Hkv = 3, 2
+    chunks = [70] + [1] * 45 + [129, 3]
+    offsets = [0, 5, min(R + G - 1, 37)]
+    T = max(offsets) + sum(chunks)
+    Kseq = (torch.randn(B, Hkv, T, D, generator=g) + torch.rand(1, Hkv, 1, D, generator=g) * 4 - 2).half()
+    Vseq = (torch.randn(B, Hkv, T, D, generator=g) * 3).half()
+    Kseq[0, 0, 32:64, 7] = 0.5         # a constant channel in one group -> scale 0
+    Vseq[1, 1, 40, :] = -0.0           # a zero token -> zero stored as +0
+    cache, lens = _build(kvc, Kseq.cuda(), Vseq.cuda(), bits, R, Cq=512, chunks=chunks,
+                         offsets=offsets)
+    assert cache.len.cpu().tolist() == list(lens)
+    for b in range(B):
+        for hk in range(Hkv):
+            _check_unit(orc, cache, Kseq, Vseq, b, hk, int(lens[b]), bits, R)
+    assert device_status_clean(kvc)
+
+
+def _attend(kvc, cache, q):
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), dtype=torch.float32,
+                     device="cuda")
+    kvc.kvc_decode_attend(cache, q, o, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+@pytest.mark.parametrize("D,bits,R,Hq,Hkv", [(64, 4, 16, 4, 4), (128, 4, 128, 8, 1),
+                                             (128, 2, 128, 16, 2), (64, 2, 0, 4, 2),
+                                             (128, 4, 100, 3, 3)])
+def test_attention_small(kvc, orc, D, bits, R, Hq, Hkv):
+    g = torch.Generator().manual_seed(7 * D + bits + Hq)
+    B = 3
+    chunks = [150, 1, 1, 33]
+    offsets = [0, 9, 30]
+    T = max(offsets) + sum(chunks)
+    Kseq = (torch.randn(B, Hkv, T, D, generator=g) + torch.rand(1, Hkv, 1, D, generator=g) * 4 - 2).half()
+    Vseq = (torch.randn(B, Hkv, T, D, generator=g) + torch.rand(1, Hkv, 1, D, generator=g) * 4 - 2).half()
+    q = torch.randn(B, Hq, D, generator=g).half()
+    cache, lens = _build(kvc, Kseq.cuda(), Vseq.cuda(), bits, R, Cq=256, chunks=chunks,
+                         offsets=offsets)
+    o, lse = _attend(kvc, cache, q.cuda())
+    gq = Hq // Hkv
+    for b in range(B):
+        for hk in range(Hkv):
+            T_b = int(lens[b])
+            ref, ref_lse = orc.kivi_attend_unit(np16(q[b, hk * gq:(hk + 1) * gq]),
+                                                np16(Kseq[b, hk]), np16(Vseq[b, hk]), T_b, R, bits)
+            assert_o_close(np16(o[b, hk * gq:(hk + 1) * gq]), ref, what=f"b={b} hk={hk}")
+            np.testing.assert_allclose(lse[b, hk * gq:(hk + 1) * gq].cpu().numpy(), ref_lse,
+                                       atol=KIVI_LSE_TOL, rtol=0)
+    assert device_status_clean(kvc)
+
+
+@pytest.mark.parametrize("wname,bits", [("kivi-b32-h32-d128-t4096", 2),
+                                        ("kivi-b32-h32-d128-t4096", 4),
+                                        ("heavy-gqa64x8-b512-d128-t2048", 4)])
+def test_full_size_sampled(kvc, orc, wname, bits):
+    """Full-size caches built by one bulk append (the prompt) and one decode append; sampled
+    units are checked bit-exactly (blocks, ring) and for attention."""
+    from kv_cache_compression_split_gb300 import workloads as W
+    w = W.WORKLOADS[wname]
+    K, V = W.kv_tensors(w, device="cuda")
+    q = W.q_tensor(w, device="cuda")
+    Cq = orc.kivi_nq(w.T, w.kivi_R)
+    cache = kvc.QuantCache.empty(w.B, w.Hkv, Cq, w.D, bits, w.kivi_R)
+    kvc.kvc_append_quant(cache, K[:, :, :w.T - 1].contiguous(), V[:, :, :w.T - 1].contiguous())
+    kvc.kvc_append_quant(cache, K[:, :, w.T - 1:].contiguous(), V[:, :, w.T - 1:].contiguous())
+    o, lse = _attend(kvc, cache, q)
+    rng = np.random.default_rng(1)
+    gq = w.Hq // w.Hkv
+    for b in sorted(set(rng.integers(0, w.B, 4).tolist()) | {w.B - 1}):
+        hk = int(rng.integers(0, w.Hkv))
+        Kb, Vb = np16(K[b, hk]), np16(V[b, hk])
+        n_q = orc.kivi_nq(w.T, w.kivi_R)
+        qz = orc.kivi_quantize_unit(Kb[:n_q], Vb[:n_q], n_q, bits)
+        kb, vb = orc.kivi_pack_unit(qz, w.D, bits)
+        assert np.array_equal(cache.k_blocks[b, hk].cpu().numpy(), kb)
+        assert np.array_equal(cache.v_blocks[b, hk].cpu().numpy(), vb)
+        ref, _ = orc.kivi_attend_unit(np16(q[b, hk * gq:(hk + 1) * gq]), Kb, Vb, w.T, w.kivi_R,
+                                      bits, qz=qz)
+        assert_o_close(np16(o[b, hk * gq:(hk + 1) * gq]), ref, what=f"b={b} hk={hk}")
+    assert device_status_clean(kvc)
+
+
+def test_capacity_overflow_is_flagged(kvc):
+    cache = kvc.QuantCache.empty(1, 1, 32, 64, 4, 16)
+    k = torch.zeros(1, 1, 100, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(kvc.KvcError) as e:       # more new tokens than the cache can hold
+        kvc.kvc_append_quant(cache, k, k)
+    assert e.value.status == kvc.KVC_ERR_CAPACITY
+    k = torch.zeros(1, 1, 40, 64, dtype=torch.float16, device="cuda")
+    kvc.kvc_append_quant(cache, k, k)            # T = 40: everything in the residual
+    torch.cuda.synchronize()
+    assert kvc.kvc_read_device_status() == 0
+    kvc.kvc_append_quant(cache, k, k)            # T = 80: n_q = 64 > Cq = 32, seen on the device
+    torch.cuda.synchronize()
+    assert kvc.kvc_read_device_status() & kvc.KVC_DEV_CAPACITY
+    assert kvc.kvc_read_device_status() == 0     # reading clears it
