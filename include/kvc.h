@@ -215,6 +215,30 @@ KVC_API size_t kvc_workspace_size(const kvc_attend_args *args);
  */
 KVC_API kvc_status kvc_decode_attend(const kvc_attend_args *args, cudaStream_t stream);
 
+/* Size of the library-owned scratch array used by kvc_decode_attend_noalloc. */
+#define KVC_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * kvc_decode_attend_noalloc -- kvc_decode_attend for callers that cannot
+ * allocate device memory on their decode path (for example a serving engine
+ * that gives all free device memory to its KV-cache pool at start-up, or a
+ * plugin host that forbids cudaMalloc / cudaFree in its enqueue callback
+ * because they synchronise the device).  The pages describe no such variant;
+ * it is an interface convenience of this library.
+ *
+ * Same arguments and results as kvc_decode_attend, except that args->workspace
+ * and args->workspace_bytes are ignored: the split scratch comes from one
+ * fixed device array of KVC_NOALLOC_SCRATCH_BYTES that the library owns (held
+ * by every GPU that loads the library until the process exits).  The call
+ * allocates nothing.  Arguments whose kvc_workspace_size exceeds
+ * KVC_NOALLOC_SCRATCH_BYTES are rejected with KVC_ERR_WORKSPACE.
+ * The first call on a device looks up that array's device address
+ * (cudaGetSymbolAddress) with the device current; make that first call before
+ * any stream capture.  All calls on a device share the array, so calls whose
+ * kernels may overlap on the GPU (unordered streams) race; order them.
+ */
+KVC_API kvc_status kvc_decode_attend_noalloc(const kvc_attend_args *args, cudaStream_t stream);
+
 enum { KVC_H2O_DECODE = 0, KVC_H2O_PREFILL = 1 };
 
 /*

@@ -26,6 +26,7 @@ KVC_DEV_CAPACITY, KVC_DEV_TIMEOUT = 0x1, 0x2
 KVC_KIND_SLOTS, KVC_KIND_KIVI = 0, 1
 KVC_H2O_DECODE, KVC_H2O_PREFILL = 0, 1
 KIVI_GROUP = 32
+KVC_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class KvcError(RuntimeError):
@@ -79,6 +80,7 @@ def lib():
                 "kvc_append_quant": (st, [C.POINTER(QuantCacheDesc), P, P, i, P]),
                 "kvc_workspace_size": (C.c_size_t, [C.POINTER(AttendArgs)]),
                 "kvc_decode_attend": (st, [C.POINTER(AttendArgs), P]),
+                "kvc_decode_attend_noalloc": (st, [C.POINTER(AttendArgs), P]),
                 "kvc_h2o_workspace_size": (C.c_size_t, [C.POINTER(H2OArgs)]),
                 "kvc_h2o_accumulate": (st, [C.POINTER(H2OArgs), P]),
                 "kvc_h2o_evict": (st, [C.POINTER(SlotCacheDesc), P, i, i, P]),
@@ -173,6 +175,16 @@ def kvc_decode_attend(cache, q, o, logits=None, lse=None, workspace=None, num_sp
                       softmax_scale: float = 0.0, stream=None):
     a, _keep = _attend_args(cache, q, o, logits, lse, workspace, num_splits, softmax_scale)
     _check(lib().kvc_decode_attend(C.byref(a), _stream(stream)), "kvc_decode_attend")
+
+
+def kvc_decode_attend_noalloc(cache, q, o, logits=None, lse=None, num_splits: int = 0,
+                              softmax_scale: float = 0.0, stream=None):
+    """kvc_decode_attend without a caller workspace: for callers that cannot allocate device
+    memory on their decode path, the split scratch comes from a fixed array the library owns
+    (KVC_NOALLOC_SCRATCH_BYTES per GPU).  Calls that may overlap on the GPU race on it."""
+    a, _keep = _attend_args(cache, q, o, logits, lse, None, num_splits, softmax_scale)
+    _check(lib().kvc_decode_attend_noalloc(C.byref(a), _stream(stream)),
+           "kvc_decode_attend_noalloc")
 
 
 def _h2o_args(mode, B, Hq, Hkv, D, Cc, scores, logits=None, lse=None, n=None, L=0, qp=None,
