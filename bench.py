@@ -107,6 +107,12 @@ def slot_bytes(n_slots, B, Hkv, Hq, D):
     return B * Hkv * n_slots * D * 2 * 2 + 2 * B * Hq * D * 2
 
 
+# DRAM bytes (read + write) per (sequence, KV head) unit and cached token that ncu measured
+# for k_attend_slots on the FP16 cache (64-sequence case of the heavy-load workload:
+# dram__bytes_read.sum + dram__bytes_write.sum = 542.1 MB over 64 x 8 units x 2048 tokens).
+SLOT_ATTEND_DRAM_BYTES_PER_UNIT_TOKEN = 542.1e6 / (64 * 8 * 2048)
+
+
 def kivi_bytes(T, R, B, Hkv, Hq, D, bits):
     G = 32
     n_q = G * (max(0, T - R) // G)
@@ -340,7 +346,10 @@ def run_gpu(args, rank, world):
     rows.update(random_rows(kvc, W, dev, stream))
 
     ms_per_step = total_ms / args.steps
+    t_avg = sum(steps_T) / len(steps_T)
+    fp16_traffic = SLOT_ATTEND_DRAM_BYTES_PER_UNIT_TOKEN * B * Hkv * t_avg
     res = {
+        "fp16_traffic": fp16_traffic,
         "ms_per_step": ms_per_step, "e2e_ms_per_step": e2e_ms, "calls_ms": calls,
         "kernels": kernels, "methods": methods, "rows": rows, "clocks": clocks,
         "device_status": status, "tokens_per_step": 4 * B,
@@ -441,6 +450,61 @@ def oracle_sample(n_seq: int, threads: int):
     return time.perf_counter() - t0, 4 * n_seq
 
 
+def run_profile(args):
+    """Small case of one kernel for ncu captures: the heavy-load workload cut to
+    --profile-batch sequences (still larger than L2), one warm-up and two measured launches."""
+    import torch
+    import kv_cache_compression_split_gb300 as kvc
+    from kv_cache_compression_split_gb300 import build as kbuild
+    from kv_cache_compression_split_gb300 import workloads as W
+    kbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = W.HEAVY
+    B, Hq, Hkv, D, T = args.profile_batch, w.Hq, w.Hkv, w.D, w.T
+    K, V = W.kv_tensors(w, T=T, B=B, device=dev)
+    q = W.q_tensor(w, B=B, device=dev)
+    o = torch.empty_like(q)
+    what = args.profile
+    if what in ("attend_fp16", "attend_h2o", "h2o_evict", "stream_evict"):
+        n_slots = T if what == "attend_fp16" else 513
+        cache = kvc.SlotCache.empty(B, Hkv, n_slots + 7, D, device=dev)
+        kvc.kvc_append(cache, K[:, :, :n_slots].contiguous(), V[:, :, :n_slots].contiguous())
+        ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), device=dev)
+        logits = torch.empty(B, Hq, cache.C, dtype=torch.float32, device=dev)
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+        scores = torch.rand(B, Hkv, cache.C, device=dev)
+        for _ in range(3):
+            if what.startswith("attend"):
+                kvc.kvc_decode_attend(cache, q, o, logits=logits if what == "attend_h2o" else None,
+                                      lse=lse, workspace=ws)
+            elif what == "h2o_evict":
+                c = kvc.SlotCache(cache.K, cache.V, cache.pos.clone(), cache.n.clone(), cache.seqlen)
+                kvc.kvc_h2o_evict(c, scores.clone(), w.n_heavy, w.n_recent)
+            else:
+                c = kvc.SlotCache(cache.K, cache.V, cache.pos.clone(), cache.n.clone(), cache.seqlen)
+                kvc.kvc_stream_evict(c, w.n_sink, w.n_recent)
+    elif what == "attend_kivi4":
+        cache = kvc.QuantCache.empty(B, Hkv, T, D, 4, w.kivi_R, device=dev)
+        kvc.kvc_append_quant(cache, K, V)
+        ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), device=dev)
+        for _ in range(3):
+            kvc.kvc_decode_attend(cache, q, o, workspace=ws)
+    elif what == "prefill":
+        L = 1024
+        qp = W.q_tensor(w, B=max(1, B // 8), L=L, device=dev)
+        kp = K[:max(1, B // 8), :, :L].contiguous()
+        sc = torch.zeros(kp.shape[0], Hkv, L, device=dev)
+        ws = torch.empty(kvc.kvc_h2o_workspace_size(kp.shape[0], Hq, L) // 4, device=dev)
+        for _ in range(3):
+            kvc.kvc_h2o_accumulate_prefill(qp, kp, sc, ws, L)
+    else:
+        raise SystemExit(f"unknown --profile {what}")
+    torch.cuda.synchronize()
+    assert kvc.kvc_read_device_status() == 0
+    print(f"profile case {what}: ok")
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -485,11 +549,18 @@ def main():
     ap.add_argument("--ref-seqs", type=int, default=4)
     ap.add_argument("--cpu-seqs", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None,
+                    help="run one kernel on a small case for ncu: attend_fp16, attend_h2o, "
+                         "attend_kivi4, h2o_evict, stream_evict, prefill")
+    ap.add_argument("--profile-batch", type=int, default=64)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
@@ -522,7 +593,7 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, e2e_ms = t.tolist()
     if rank == 0:
-        dom = res["kernels"]["attend_slots(fp16+h2o+stream)"]
+        dom = res["kernels"]["attend_fp16"]
         line = {
             "metric": METRIC, "value": world * res["tokens_per_step"] / (ms * 1e-3), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -531,13 +602,15 @@ def main():
             "config": {"workload": "heavy-gqa64x8-b512-d128-t2048", "global_batch": 512 * world,
                        "seq_len": 2048, "parallelism": f"replicas x{world}",
                        "methods": ["fp16", "h2o512", "kivi4", "stream512"],
+                       "kv_len": "2048 + step index (each step appends one token)",
                        "l2": "inputs larger than L2 (8 GB of cache read per step)"},
             "e2e": {"value": world * res["tokens_per_step"] / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
-            "roofline": {"bound": "hbm", "kernel": "k_attend_slots",
+            "roofline": {"bound": "hbm", "kernel": "k_attend_slots (FP16 cache launch)",
                          "achieved": dom["gbs"], "peak": res["hbm_peak"], "unit": "GB/s",
-                         "frac": dom["frac_of_hbm"], "traffic": None,
+                         "frac": dom["frac_of_hbm"], "traffic": res["fp16_traffic"],
+                         "algorithmic_bytes": dom["bytes_per_step"],
                          "peak_source": res["peak_kind"]},
             "cpu_baseline": cpu,
             "clocks": res["clocks"],
