@@ -125,8 +125,8 @@ typedef struct kvc_slot_cache {
  *     of every word) and 2i+1 (high 16 bits).  Its word r*W + k (r in [0,8),
  *     k in [0,W), W = D*bits/128) holds in field j (bits [bits*j, bits*(j+1))
  *     of each 16-bit half) channel d = 16*(k*(8/bits) + j/2) + 8*(j%2) + r.
- *     Then for each of the 32 tokens: D/32 fp16 scales followed by D/32 fp16
- *     zeros.
+ *     Then the V scales as D/32 rows of 32 fp16 values (row j holds channel
+ *     group j of tokens 0..31), then the V zeros in the same [D/32][32] order.
  *   k_res, v_res [B, Hkv, R + 32, D] fp16 residual rings;  len [B] int32.
  */
 typedef struct kvc_quant_cache {

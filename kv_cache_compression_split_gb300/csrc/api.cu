@@ -189,9 +189,12 @@ AttendPlanFull plan_full(const kvc_attend_args *a)
         f.B = a->quant->B;
         f.Hkv = a->quant->Hkv;
         f.D = a->quant->D;
-        const int tiles = (a->quant->Cq / KIVI_G + 1) / 2;
+        // quantised tiles of four groups; the residual ring joins the last split
+        const int tiles = (a->quant->Cq / KIVI_G + 3) / 4;
         f.plan = plan_attend(f.B * f.Hkv, tiles > 0 ? tiles : 1, a->num_splits);
-        f.ws = (size_t)f.B * a->Hq * (f.plan.splits + 1) * (f.D + 2) * sizeof(float);
+        f.ws = f.plan.splits > 1
+                   ? (size_t)f.B * a->Hq * f.plan.splits * (f.D + 2) * sizeof(float)
+                   : 0;
     } else {
         return f;
     }
@@ -276,7 +279,7 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         return from_cuda(launch_attend_slots(L, stream));
     }
     const kvc_quant_cache &c = *a->quant;
-    float *part_ml = part_o + (size_t)f.B * a->Hq * (f.plan.splits + 1) * f.D;
+    float *part_ml = part_o ? part_o + (size_t)f.B * a->Hq * f.plan.splits * f.D : nullptr;
     KiviAttendLaunch L{f.B, a->Hq, c.Hkv, c.D, c.bits, c.R, c.Cq, a->q, a->o, c.k_blocks,
                        c.v_blocks, c.k_res, c.v_res, c.len, a->lse, part_o, part_ml,
                        f.plan.splits, f.plan.tiles_per_split, scale};

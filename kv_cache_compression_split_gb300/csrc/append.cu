@@ -207,8 +207,8 @@ __global__ void __launch_bounds__(QTHREADS)
                     mx = v;
             }
             const GroupQ q = group_params(mn, mnb, mx, BITS);
-            vsz[t * 2 * NG + j] = q.scale_bits;
-            vsz[t * 2 * NG + NG + j] = q.zero_bits;
+            vsz[j * G + t] = q.scale_bits;
+            vsz[NG * G + j * G + t] = q.zero_bits;
             for (int e = 0; e < G; ++e)
                 cv[t][j * G + e] = (uint8_t)quant_code(h2fix(xv[t][j * G + e]), q, CMAX);
         }

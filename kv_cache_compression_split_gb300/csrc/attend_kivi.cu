@@ -1,24 +1,28 @@
-// attend_kivi.cu -- split-KV decode attention over the quantised part of a
-// KIVI cache ("Rethinking KV Cache Compression" guide, §16 "4 种方法逐步执行":
-// the decode read dequantises the old cache or uses a quantised kernel).
+// attend_kivi.cu -- split-KV decode attention over a KIVI cache ("Rethinking KV
+// Cache Compression" guide, §16 "4 种方法逐步执行": the decode read dequantises
+// the old cache or uses a quantised kernel; the newest tokens stay in fp16).
 //
-// One CTA per (sequence, KV head, split); a producer lane streams the packed
-// K and V group blocks of 64 tokens (two groups) into shared memory with 1-D
-// bulk TMA copies; four consumer warps take 16 tokens each and never
-// materialise dequantised values:
-//   K (per-channel scale s_d, zero z_d per group):
+// One CTA per (sequence, KV head, split).  A producer lane streams tiles into a
+// shared-memory ring: quantised tiles of four 32-token groups (1-D bulk copies
+// of the packed K and V group blocks) and, in the unit's last split, residual
+// tiles of 32 fp16 ring slots (2-D TMA, 128-byte swizzle).  Four consumer
+// warps work on a tile: warp w takes group w of a quantised tile, warps 0-1
+// take 16 slots each of a residual tile.  Nothing is dequantised to memory:
+//
+//   K (per-channel scale s_d and zero z_d of the group):
 //     q . k_t = sum_d (q_d s_d) c_{t,d} + sum_d q_d z_d
-//     -> the scaled query q~ = q * s (fp16) is the MMA's B operand, the codes
-//        c (exact small integers in fp16) are the A operand, the bias
-//        sum_d q_d z_d is added to the fp32 scores.
-//   V (per-token scale s_t, zero z_t per 32 channels):
+//   the scaled query q~ = q * s (binary16) is the B operand of S^T = C Q~^T
+//   and the bias sum_d q_d z_d (fp32) is added to the scores.
+//   V (per-token scale s_t and zero z_t of each 32-channel group):
 //     sum_t p_t v_{t,d} = sum_t (p_t s_t) c_{t,d} + sum_t p_t z_t
-//     -> p~ = p * s_t (fp16) is the B operand of O^T += C^T P~^T, and the
-//        zero term is accumulated per (head, channel group) beside it.
-// Codes become fp16 with the binary16 exponent trick: a field f OR-ed into
-// 0x6400 (1024.0) reads as 1024 + f, and subtracting 1024 is exact.
-// Results are written as split partials; the fp16 residual ring is attended
-// by the slot kernel as one more partial and the combine kernel merges them.
+//   p~ = p * s_t (binary16) is the B operand of O^T += C^T P~^T; the zero term
+//   Z[group][head] = sum_t z_t p_t is one more MMA per 16 tokens.
+//
+// Codes enter the MMA as binary16 subnormals: masking a packed word leaves the
+// bit pattern c << (bits*j), which reads as c * 2^(bits*j - 24) exactly, so a
+// single AND per pair of codes is the whole conversion.  The power-of-two
+// field weights are divided out of the K operand (q~ / 2^(bits*j)) or undone
+// per output row at the end, and the 2^-24 is undone in the fp32 results.
 #include "kvc_device.cuh"
 #include "kvc_internal.h"
 
@@ -26,16 +30,14 @@
 
 namespace kvc {
 
-cudaError_t launch_attend_ring(int B, int Hq, int Hkv, int D, int R, const uint16_t *q,
-                               const uint16_t *k_res, const uint16_t *v_res, const int32_t *len,
-                               float *part_o, float *part_ml, int part_splits, int part_offset,
-                               float scale, cudaStream_t s);
-
 namespace {
 
 constexpr int NCW = 4;
 constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+constexpr float TWO24 = 16777216.0f;
+constexpr float TWOM24 = 1.0f / 16777216.0f;
 
 template <int D, int BITS> struct KiviCfg {
     static constexpr int G = KIVI_G;
@@ -45,23 +47,32 @@ template <int D, int BITS> struct KiviCfg {
     static constexpr int W = D * BITS / 128;           // V words per lane-row per pair
     static constexpr int FPW = 32 / BITS;              // fields per word
     static constexpr int HALF = FPW / 2;               // fields per 16-bit half
+    static constexpr int QUART = HALF / 2;             // fields taken before shifting by 8
+    static constexpr int MPW = 8 / BITS;               // V m-tiles per word
     static constexpr int CODE_BYTES = G * D * BITS / 8;
     static constexpr int BLOCK = CODE_BYTES + 4 * D;
-    static constexpr int STAGE_BYTES = 4 * BLOCK;      // 2 K blocks + 2 V blocks
-    static constexpr int NSTAGE = (BITS == 4) ? 8 : 12;
-    static constexpr int SMEM = NSTAGE * STAGE_BYTES + 128 + 2 * NSTAGE * 8;
-    static constexpr uint32_t MM = ((1u << BITS) - 1) | (((1u << BITS) - 1) << 16);
+    static constexpr int QG = NCW;                     // groups per quantised tile
+    static constexpr int QT_BYTES = 2 * QG * BLOCK;
+    static constexpr int RS = 32;                      // ring slots per residual tile
+    static constexpr int NBOX = D / 64;
+    static constexpr int RT_BYTES = 2 * RS * D * 2;
+    static constexpr int STAGE_BYTES =
+        ((QT_BYTES > RT_BYTES ? QT_BYTES : RT_BYTES) + 1023) / 1024 * 1024;
+    static constexpr int NSTAGE = (81920 / STAGE_BYTES) < 3 ? 3 : (81920 / STAGE_BYTES);
+    static constexpr int SMEM = NSTAGE * STAGE_BYTES + 1024 + 2 * NSTAGE * 8;
     static_assert(NCW * (8 * D + 16) * 4 <= NSTAGE * STAGE_BYTES, "combine scratch must fit");
 };
 
 struct KiviParams {
-    int Hq, Hkv, g, Cq, R;
-    int splits, tiles_per_split, part_splits;
+    int Hq, Hkv, g, Cq, R, CR;
+    int splits, qtiles_per_split;
     const uint16_t *q;
+    uint16_t *o;
+    float *lse;
     const uint8_t *kb, *vb;
     const int32_t *len;
     float *part_o, *part_ml;
-    float scale_log2;
+    float scale, scale_log2;
     int *status;
 };
 
@@ -70,26 +81,38 @@ __device__ __forceinline__ void consumer_bar()
     asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
 }
 
-__device__ __forceinline__ uint32_t hsub1024(uint32_t x)
+// Code field pair j (j < 16/BITS) of a packed word: fields j and j + 16/BITS
+// (one per 16-bit half) masked in place.  Pairs j < 8/BITS come from w, the
+// others from w >> 8, so a field never reaches the binary16 exponent: the bit
+// pattern reads as two subnormals c_lo * 2^(BITS*(j mod 8/BITS) - 24), c_hi * (same).
+template <int BITS> __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int j)
 {
-    const __half2 h = *reinterpret_cast<const __half2 *>(&x);
-    const __half2 r = __hsub2(h, __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
-    return *reinterpret_cast<const uint32_t *>(&r);
+    constexpr int QUART = 8 / BITS;
+    constexpr uint32_t M = ((1u << BITS) - 1) | (((1u << BITS) - 1) << 16);
+    return (j < QUART ? w : w8) & (M << (BITS * (j % QUART)));
 }
 
-template <int BITS>
-__device__ __forceinline__ uint32_t field_pair(uint32_t w, int j, uint32_t mm)
+// Weight 2^(BITS * (j mod 8/BITS)) that code_pair leaves on field pair j (times 2^-24).
+template <int BITS> __host__ __device__ constexpr float pair_weight(int j)
 {
-    return hsub1024(((w >> (BITS * j)) & mm) | 0x64006400u);
+    return (float)(1u << (BITS * (j % (8 / BITS))));
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
+{
+    __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
 }
 
 template <int D, int BITS>
-__global__ void __launch_bounds__(NTHREADS, 2) k_attend_kivi(const KiviParams p)
+__global__ void __launch_bounds__(NTHREADS, 2)
+    k_attend_kivi(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const KiviParams p)
 {
     using Cfg = KiviCfg<D, BITS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES);
     uint64_t *empty = full + Cfg::NSTAGE;
 
@@ -105,10 +128,13 @@ __global__ void __launch_bounds__(NTHREADS, 2) k_attend_kivi(const KiviParams p)
             flag_error(p.status, DEV_CAPACITY);
         n_groups = p.Cq / Cfg::G;
     }
-    const int unit_tiles = (n_groups + 1) / 2;
-    const int tile0 = split * p.tiles_per_split;
-    const int tile1 = min(unit_tiles, tile0 + p.tiles_per_split);
-    const int ntiles = tile1 > tile0 ? tile1 - tile0 : 0;
+    const int n_res = T - n_groups * Cfg::G;
+    const int unit_qtiles = (n_groups + Cfg::QG - 1) / Cfg::QG;
+    const int qt0 = split * p.qtiles_per_split;
+    const int qt1 = min(unit_qtiles, qt0 + p.qtiles_per_split);
+    const int nq = qt1 > qt0 ? qt1 - qt0 : 0;
+    const int nr = (split == p.splits - 1) ? (p.CR + Cfg::RS - 1) / Cfg::RS : 0;
+    const int ntiles = nr + nq;            // residual tiles first, then quantised tiles
     const uint8_t *kblocks = p.kb + (size_t)unit * (p.Cq / Cfg::G) * Cfg::BLOCK;
     const uint8_t *vblocks = p.vb + (size_t)unit * (p.Cq / Cfg::G) * Cfg::BLOCK;
 
@@ -122,122 +148,100 @@ __global__ void __launch_bounds__(NTHREADS, 2) k_attend_kivi(const KiviParams p)
     __syncthreads();
 
     if (warp == NCW) {
-        if (lane == 0) {
+        if (lane == 0 && ntiles > 0) {
+            if (nr > 0) {
+                prefetch_tmap(&tmK);
+                prefetch_tmap(&tmV);
+            }
             for (int i = 0; i < ntiles; ++i) {
                 const int st = i % Cfg::NSTAGE;
                 if (i >= Cfg::NSTAGE && !mbar_wait(&empty[st], ((i / Cfg::NSTAGE) & 1) ^ 1)) {
                     flag_error(p.status, DEV_TIMEOUT);
                     break;
                 }
-                const int g0 = 2 * (tile0 + i);
-                const int ng = min(2, n_groups - g0);
                 uint8_t *dst = smem + st * Cfg::STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[st], 2 * ng * Cfg::BLOCK);
-                bulk_load(dst, kblocks + (size_t)g0 * Cfg::BLOCK, ng * Cfg::BLOCK, &full[st]);
-                bulk_load(dst + 2 * Cfg::BLOCK, vblocks + (size_t)g0 * Cfg::BLOCK,
-                          ng * Cfg::BLOCK, &full[st]);
+                if (i < nr) {
+                    mbar_arrive_expect_tx(&full[st], Cfg::RT_BYTES);
+                    const int row = unit * p.CR + i * Cfg::RS;
+#pragma unroll
+                    for (int j = 0; j < Cfg::NBOX; ++j) {
+                        tma_load_2d(dst + j * Cfg::RS * 128, &tmK, &full[st], 64 * j, row);
+                        tma_load_2d(dst + (Cfg::NBOX + j) * Cfg::RS * 128, &tmV, &full[st], 64 * j,
+                                    row);
+                    }
+                } else {
+                    const int g0 = (qt0 + i - nr) * Cfg::QG;
+                    const int ng = min(Cfg::QG, n_groups - g0);
+                    mbar_arrive_expect_tx(&full[st], 2 * ng * Cfg::BLOCK);
+                    bulk_load(dst, kblocks + (size_t)g0 * Cfg::BLOCK, ng * Cfg::BLOCK, &full[st]);
+                    bulk_load(dst + Cfg::QG * Cfg::BLOCK, vblocks + (size_t)g0 * Cfg::BLOCK,
+                              ng * Cfg::BLOCK, &full[st]);
+                }
             }
         }
         return;
     }
 
-    const int r = lane >> 2, c = lane & 3;
+    const int r = lane >> 2, c = lane & 3, mi = lane >> 3, ri = lane & 7;
     const int h0 = 2 * c, h1 = 2 * c + 1;
-    const int gi = warp >> 1;            // group of the tile this warp works on
-    const int tslice = 16 * (warp & 1);  // first token of the warp's slice in the group
+    const bool hv = r < p.g;
+    const uint16_t *qrow = p.q + ((size_t)b * p.Hq + hk * p.g + (hv ? r : 0)) * D;
 
-    // this lane's query values (head r) over its channel range [c*D/4, (c+1)*D/4)
-    float qv[D / 4];
+    // fp16 query fragments for the residual tiles (B = Q^T, as in the slot kernel)
+    uint32_t qf[D / 16][2];
+    // query pairs for the quantised tiles: lane c covers channels [c D/4, (c+1) D/4);
+    // pair pi holds channels (lo, lo + HALF) divided by the pair's field weight
+    uint32_t qpair[D / 8];
+    float qz[D / 4];
     {
-        const bool hv = r < p.g;
-        const uint16_t *qrow = p.q + ((size_t)b * p.Hq + hk * p.g + (hv ? r : 0)) * D + c * (D / 4);
+        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+            qf[s][0] = hv ? q32[8 * s + c] : 0u;
+            qf[s][1] = hv ? q32[8 * s + c + 4] : 0u;
+        }
 #pragma unroll
         for (int i = 0; i < D / 4; ++i)
-            qv[i] = hv ? __half2float(__ushort_as_half(qrow[i])) : 0.f;
+            qz[i] = hv ? __half2float(__ushort_as_half(qrow[c * (D / 4) + i])) : 0.f;
+#pragma unroll
+        for (int pi = 0; pi < D / 8; ++pi) {
+            const int j = pi % Cfg::HALF;
+            const int lo = Cfg::FPW * (pi / Cfg::HALF) + j;
+            const float wgt = 1.0f / pair_weight<BITS>(j);
+            qpair[pi] = pack_half2(qz[lo] * wgt, qz[lo + Cfg::HALF] * wgt);
+        }
     }
 
     float acc[D / 16][4];
 #pragma unroll
     for (int m = 0; m < D / 16; ++m)
         acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
-    float zacc[Cfg::NG];
-#pragma unroll
-    for (int j = 0; j < Cfg::NG; ++j)
-        zacc[j] = 0.f;
+    float zacc[4] = {0.f, 0.f, 0.f, 0.f};   // Z[group r][heads 2c, 2c+1] (rows r < NG)
     float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
+    bool code_units = false;                // acc scaled to the quantised tiles' units
 
-    for (int i = 0; i < ntiles; ++i) {
-        const int st = i % Cfg::NSTAGE;
-        if (!mbar_wait(&full[st], (i / Cfg::NSTAGE) & 1)) {
-            flag_error(p.status, DEV_TIMEOUT);
-            break;
+    // online-softmax update for a 16-token row block; x* are log2-domain scores
+    auto softmax16 = [&](float x0, float x1, float x2, float x3, float &p0, float &p1, float &p2,
+                         float &p3) {
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
-        const int g0 = 2 * (tile0 + i);
-        if (g0 + gi < n_groups) {
-            const uint8_t *kblk = smem + st * Cfg::STAGE_BYTES + gi * Cfg::BLOCK;
-            const uint8_t *vblk = smem + st * Cfg::STAGE_BYTES + (2 + gi) * Cfg::BLOCK;
-            const __half *ks = reinterpret_cast<const __half *>(kblk + Cfg::CODE_BYTES);
-
-            // ---- q~ = q * s (B operand pairs) and bias sum_d q_d z_d for head r
-            uint32_t qt[D / 8];
-            float beta = 0.f;
-            {
-                const __half *ksl = ks + c * (D / 4);
-                const __half *kzl = ks + D + c * (D / 4);
-#pragma unroll
-                for (int pi = 0; pi < D / 8; ++pi) {
-                    const int lo = Cfg::FPW * (pi / Cfg::HALF) + (pi % Cfg::HALF);
-                    const int hi = lo + Cfg::HALF;
-                    qt[pi] = pack_half2(qv[lo] * __half2float(ksl[lo]),
-                                        qv[hi] * __half2float(ksl[hi]));
-                }
-#pragma unroll
-                for (int e = 0; e < D / 4; ++e)
-                    beta += qv[e] * __half2float(kzl[e]);
-                beta += __shfl_xor_sync(0xffffffffu, beta, 1);
-                beta += __shfl_xor_sync(0xffffffffu, beta, 2);
-            }
-            const float beta0 = __shfl_sync(0xffffffffu, beta, 4 * h0);
-            const float beta1 = __shfl_sync(0xffffffffu, beta, 4 * h1);
-
-            // ---- S^T = C_K Q~^T over the warp's 16 tokens
-            float sa[4] = {0.f, 0.f, 0.f, 0.f};
-            {
-                const uint32_t *kw = reinterpret_cast<const uint32_t *>(kblk);
-                uint32_t wa[Cfg::WPL], wb[Cfg::WPL];
-#pragma unroll
-                for (int k = 0; k < Cfg::WPL; ++k) {
-                    wa[k] = kw[(tslice + r) * Cfg::WK + c * Cfg::WPL + k];
-                    wb[k] = kw[(tslice + r + 8) * Cfg::WK + c * Cfg::WPL + k];
-                }
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s) {
-                    const int pa = 2 * s, pb = 2 * s + 1;
-                    const uint32_t a0 = field_pair<BITS>(wa[pa / Cfg::HALF], pa % Cfg::HALF, Cfg::MM);
-                    const uint32_t a1 = field_pair<BITS>(wb[pa / Cfg::HALF], pa % Cfg::HALF, Cfg::MM);
-                    const uint32_t a2 = field_pair<BITS>(wa[pb / Cfg::HALF], pb % Cfg::HALF, Cfg::MM);
-                    const uint32_t a3 = field_pair<BITS>(wb[pb / Cfg::HALF], pb % Cfg::HALF, Cfg::MM);
-                    mma16816(sa, a0, a1, a2, a3, qt[pa], qt[pb]);
-                }
-            }
-            const float x0 = (sa[0] + beta0) * p.scale_log2;
-            const float x1 = (sa[1] + beta1) * p.scale_log2;
-            const float x2 = (sa[2] + beta0) * p.scale_log2;
-            const float x3 = (sa[3] + beta1) * p.scale_log2;
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
-            const float al0 = ex2(m_run0 - mn0), al1 = ex2(m_run1 - mn1);
-            const float p0 = ex2(x0 - mn0), p2 = ex2(x2 - mn0);
-            const float p1 = ex2(x1 - mn1), p3 = ex2(x3 - mn1);
-            m_run0 = mn0;
-            m_run1 = mn1;
-            l_run0 = l_run0 * al0 + p0 + p2;
-            l_run1 = l_run1 * al1 + p1 + p3;
+        const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
+        const bool z0 = mn0 == -INFINITY, z1 = mn1 == -INFINITY;
+        const float al0 = z0 ? 1.f : ex2(m_run0 - mn0);
+        const float al1 = z1 ? 1.f : ex2(m_run1 - mn1);
+        p0 = z0 ? 0.f : ex2(x0 - mn0);
+        p2 = z0 ? 0.f : ex2(x2 - mn0);
+        p1 = z1 ? 0.f : ex2(x1 - mn1);
+        p3 = z1 ? 0.f : ex2(x3 - mn1);
+        m_run0 = mn0;
+        m_run1 = mn1;
+        l_run0 = l_run0 * al0 + p0 + p2;
+        l_run1 = l_run1 * al1 + p1 + p3;
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
             for (int m = 0; m < D / 16; ++m) {
                 acc[m][0] *= al0;
@@ -245,56 +249,176 @@ __global__ void __launch_bounds__(NTHREADS, 2) k_attend_kivi(const KiviParams p)
                 acc[m][2] *= al0;
                 acc[m][3] *= al1;
             }
-            // alpha of head r (the zero-term accumulator is per head r)
-            const float ala = __shfl_sync(0xffffffffu, al0, r >> 1);
-            const float alb = __shfl_sync(0xffffffffu, al1, r >> 1);
-            const float al_r = (r & 1) ? alb : ala;
+            zacc[0] *= al0;
+            zacc[1] *= al1;
+        }
+    };
 
-            // P^T fragments: pb0 = (p[t=2c][r], p[t=2c+1][r]), pb1 = tokens 2c+8, 2c+9
-            const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
-            const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
-            const float2 pf0 = __half22float2(*reinterpret_cast<const __half2 *>(&pb0));
-            const float2 pf1 = __half22float2(*reinterpret_cast<const __half2 *>(&pb1));
-
-            // per-token V scales / zeros of this lane's four tokens
-            const __half *vsz = reinterpret_cast<const __half *>(vblk + Cfg::CODE_BYTES);
-            const int tk[4] = {tslice + 2 * c, tslice + 2 * c + 1, tslice + 2 * c + 8,
-                               tslice + 2 * c + 9};
-            const float pv[4] = {pf0.x, pf0.y, pf1.x, pf1.y};
-            uint32_t ptb0[Cfg::NG], ptb1[Cfg::NG];
+    for (int i = 0; i < ntiles; ++i) {
+        const int st = i % Cfg::NSTAGE;
+        if (!mbar_wait(&full[st], (i / Cfg::NSTAGE) & 1)) {
+            flag_error(p.status, DEV_TIMEOUT);
+            break;
+        }
+        uint8_t *tile = smem + st * Cfg::STAGE_BYTES;
+        if (i < nr) {
+            // ---------------- fp16 residual tile: warps 0, 1 take 16 ring slots each
+            const int s0 = i * Cfg::RS + 16 * warp;
+            if (warp < 2 && s0 < p.CR) {
+                const uint32_t kbase = smem_u32(tile);
+                const uint32_t vbase = kbase + Cfg::NBOX * Cfg::RS * 128;
+                float sa[4] = {0.f, 0.f, 0.f, 0.f};
+                const int krow = 16 * warp + ri + 8 * (mi & 1);
 #pragma unroll
-            for (int j = 0; j < Cfg::NG; ++j) {
-                float sv[4], zv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    sv[e] = __half2float(vsz[tk[e] * 2 * Cfg::NG + j]);
-                    zv[e] = __half2float(vsz[tk[e] * 2 * Cfg::NG + Cfg::NG + j]);
+                for (int s = 0; s < D / 16; ++s) {
+                    const int ch = 2 * s + (mi >> 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(swz128(kbase + (ch >> 3) * Cfg::RS * 128, krow, ch & 7), a0, a1, a2, a3);
+                    mma16816(sa, a0, a1, a2, a3, qf[s][0], qf[s][1]);
                 }
-                ptb0[j] = pack_half2(pv[0] * sv[0], pv[1] * sv[1]);
-                ptb1[j] = pack_half2(pv[2] * sv[2], pv[3] * sv[3]);
-                zacc[j] = zacc[j] * al_r + pv[0] * zv[0] + pv[1] * zv[1] + pv[2] * zv[2] +
-                          pv[3] * zv[3];
-            }
-
-            // ---- O^T += C_V^T P~^T per 16-channel m-tile (m-tile m lies in group m/2)
-            {
-                const uint32_t *vw = reinterpret_cast<const uint32_t *>(vblk);
-                const int pc = 8 * (warp & 1) + c;   // token pair (2c, 2c+1) of the slice
-                uint32_t wa[Cfg::W], wb[Cfg::W];
-#pragma unroll
-                for (int k = 0; k < Cfg::W; ++k) {
-                    wa[k] = vw[pc * 2 * Cfg::WK + r * Cfg::W + k];
-                    wb[k] = vw[(pc + 4) * 2 * Cfg::WK + r * Cfg::W + k];
-                }
+                const int ta = s0 + r, tb = s0 + r + 8;
+                const bool va = ta < p.CR && ((T - 1 - ta) % p.CR + p.CR) % p.CR < n_res;
+                const bool vb = tb < p.CR && ((T - 1 - tb) % p.CR + p.CR) % p.CR < n_res;
+                float p0, p1, p2, p3;
+                softmax16(va ? sa[0] * p.scale_log2 : -INFINITY, va ? sa[1] * p.scale_log2 : -INFINITY,
+                          vb ? sa[2] * p.scale_log2 : -INFINITY, vb ? sa[3] * p.scale_log2 : -INFINITY,
+                          p0, p1, p2, p3);
+                const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
+                const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
+                const int vrow = 16 * warp + ri + 8 * (mi >> 1);
 #pragma unroll
                 for (int m = 0; m < D / 16; ++m) {
-                    constexpr int MPW = 8 / BITS;     // m-tiles per word
-                    const int k = m / MPW, jj = m % MPW;
-                    const uint32_t a0 = field_pair<BITS>(wa[k], 2 * jj, Cfg::MM);
-                    const uint32_t a1 = field_pair<BITS>(wa[k], 2 * jj + 1, Cfg::MM);
-                    const uint32_t a2 = field_pair<BITS>(wb[k], 2 * jj, Cfg::MM);
-                    const uint32_t a3 = field_pair<BITS>(wb[k], 2 * jj + 1, Cfg::MM);
-                    mma16816(acc[m], a0, a1, a2, a3, ptb0[m / 2], ptb1[m / 2]);
+                    const int ch = 2 * m + (mi & 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(swz128(vbase + (ch >> 3) * Cfg::RS * 128, vrow, ch & 7), a0, a1, a2, a3);
+                    mma16816(acc[m], a0, a1, a2, a3, pb0, pb1);
+                }
+            }
+        } else {
+            // ---------------- quantised tile: warp w takes group w (32 tokens)
+            const int g0 = (qt0 + i - nr) * Cfg::QG;
+            if (g0 + warp < n_groups) {
+                if (!code_units) {
+                    // switch the accumulator to the quantised tiles' units
+#pragma unroll
+                    for (int m = 0; m < D / 16; ++m) {
+                        const int jj = m % Cfg::MPW;
+                        const float wr = pair_weight<BITS>(2 * jj) * TWOM24;
+                        const float wr8 = pair_weight<BITS>(2 * jj + 1) * TWOM24;
+                        acc[m][0] *= wr;
+                        acc[m][1] *= wr;
+                        acc[m][2] *= wr8;
+                        acc[m][3] *= wr8;
+                    }
+                    code_units = true;
+                }
+                const uint8_t *kblk = tile + warp * Cfg::BLOCK;
+                const uint8_t *vblk = tile + (Cfg::QG + warp) * Cfg::BLOCK;
+                const uint32_t *ksz = reinterpret_cast<const uint32_t *>(kblk + Cfg::CODE_BYTES);
+                const uint16_t *vsz = reinterpret_cast<const uint16_t *>(vblk + Cfg::CODE_BYTES);
+
+                // q~ pairs (B operand) and the bias sum_d q_d z_d for head r
+                uint32_t qt[D / 8];
+                float beta = 0.f;
+                {
+                    const uint32_t *sl = ksz + c * (D / 8);          // scales of my channels
+                    const uint32_t *zl = ksz + D / 2 + c * (D / 8);  // zeros of my channels
+                    uint32_t sw[D / 8];
+#pragma unroll
+                    for (int e = 0; e < D / 8; ++e)
+                        sw[e] = sl[e];
+#pragma unroll
+                    for (int pi = 0; pi < D / 8; ++pi) {
+                        const int lo = Cfg::FPW * (pi / Cfg::HALF) + pi % Cfg::HALF;
+                        const int hi = lo + Cfg::HALF;
+                        const uint32_t wa = sw[lo >> 1], wb = sw[hi >> 1];
+                        const uint32_t sp = __byte_perm(wa, wb, ((lo & 1) ? 0x0032 : 0x0010) |
+                                                                    ((hi & 1) ? 0x7600 : 0x5400));
+                        qt[pi] = hmul2_u32(qpair[pi], sp);
+                    }
+#pragma unroll
+                    for (int e = 0; e < D / 8; ++e) {
+                        const float2 zf = __half22float2(*reinterpret_cast<const __half2 *>(&zl[e]));
+                        beta = fmaf(qz[2 * e], zf.x, beta);
+                        beta = fmaf(qz[2 * e + 1], zf.y, beta);
+                    }
+                    beta += __shfl_xor_sync(0xffffffffu, beta, 1);
+                    beta += __shfl_xor_sync(0xffffffffu, beta, 2);
+                }
+                const float bias0 = __shfl_sync(0xffffffffu, beta, 4 * h0) * p.scale_log2;
+                const float bias1 = __shfl_sync(0xffffffffu, beta, 4 * h1) * p.scale_log2;
+                const float sk = TWO24 * p.scale_log2;
+
+                const uint32_t *kw = reinterpret_cast<const uint32_t *>(kblk);
+                const uint32_t *vw = reinterpret_cast<const uint32_t *>(vblk);
+#pragma unroll
+                for (int rb = 0; rb < 2; ++rb) {
+                    // ---- S^T = C_K Q~^T over tokens [16 rb, 16 rb + 16) of the group
+                    float sa[4] = {0.f, 0.f, 0.f, 0.f};
+                    {
+                        uint32_t wa[Cfg::WPL], wb[Cfg::WPL];
+#pragma unroll
+                        for (int k = 0; k < Cfg::WPL; ++k) {
+                            wa[k] = kw[(16 * rb + r) * Cfg::WK + c * Cfg::WPL + k];
+                            wb[k] = kw[(16 * rb + r + 8) * Cfg::WK + c * Cfg::WPL + k];
+                        }
+#pragma unroll
+                        for (int s = 0; s < D / 16; ++s) {
+                            const int pa = 2 * s, pb = 2 * s + 1;
+                            const int ka = pa / Cfg::HALF, kb2 = pb / Cfg::HALF;
+                            const uint32_t a0 = code_pair<BITS>(wa[ka], wa[ka] >> 8, pa % Cfg::HALF);
+                            const uint32_t a1 = code_pair<BITS>(wb[ka], wb[ka] >> 8, pa % Cfg::HALF);
+                            const uint32_t a2 = code_pair<BITS>(wa[kb2], wa[kb2] >> 8, pb % Cfg::HALF);
+                            const uint32_t a3 = code_pair<BITS>(wb[kb2], wb[kb2] >> 8, pb % Cfg::HALF);
+                            mma16816(sa, a0, a1, a2, a3, qt[pa], qt[pb]);
+                        }
+                    }
+                    float p0, p1, p2, p3;
+                    softmax16(fmaf(sa[0], sk, bias0), fmaf(sa[1], sk, bias1),
+                              fmaf(sa[2], sk, bias0), fmaf(sa[3], sk, bias1), p0, p1, p2, p3);
+                    // P^T fragments: pb0 = p[tokens 2c, 2c+1][head r], pb1 = tokens 2c+8, 2c+9
+                    const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
+                    const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
+                    const int t0 = 16 * rb + 2 * c;
+                    // ---- zero term Z[group][head] += sum_t z_t p_t (A rows = channel groups)
+                    {
+                        const bool zr = r < Cfg::NG;
+                        const uint32_t *zz = reinterpret_cast<const uint32_t *>(vsz + Cfg::NG * Cfg::G);
+                        const uint32_t za0 = zr ? zz[(r * Cfg::G + t0) >> 1] : 0u;
+                        const uint32_t za2 = zr ? zz[(r * Cfg::G + t0 + 8) >> 1] : 0u;
+                        float zc[4] = {zacc[0], zacc[1], zacc[2], zacc[3]};
+                        mma16816(zc, za0, 0u, za2, 0u, pb0, pb1);
+                        zacc[0] = zc[0];
+                        zacc[1] = zc[1];
+                    }
+                    // ---- O^T += C_V^T P~^T, m-tile m in channel group m/2
+                    uint32_t ptb0[Cfg::NG], ptb1[Cfg::NG];
+                    {
+                        const uint32_t *ss = reinterpret_cast<const uint32_t *>(vsz);
+#pragma unroll
+                        for (int gd = 0; gd < Cfg::NG; ++gd) {
+                            ptb0[gd] = hmul2_u32(pb0, ss[(gd * Cfg::G + t0) >> 1]);
+                            ptb1[gd] = hmul2_u32(pb1, ss[(gd * Cfg::G + t0 + 8) >> 1]);
+                        }
+                    }
+                    {
+                        const int pc = 8 * rb + c;   // token pair (2c, 2c+1) of the row block
+                        uint32_t wa[Cfg::W], wb[Cfg::W];
+#pragma unroll
+                        for (int k = 0; k < Cfg::W; ++k) {
+                            wa[k] = vw[pc * 2 * Cfg::WK + r * Cfg::W + k];
+                            wb[k] = vw[(pc + 4) * 2 * Cfg::WK + r * Cfg::W + k];
+                        }
+#pragma unroll
+                        for (int m = 0; m < D / 16; ++m) {
+                            const int k = m / Cfg::MPW, jj = m % Cfg::MPW;
+                            const uint32_t a0 = code_pair<BITS>(wa[k], wa[k] >> 8, 2 * jj);
+                            const uint32_t a1 = code_pair<BITS>(wa[k], wa[k] >> 8, 2 * jj + 1);
+                            const uint32_t a2 = code_pair<BITS>(wb[k], wb[k] >> 8, 2 * jj);
+                            const uint32_t a3 = code_pair<BITS>(wb[k], wb[k] >> 8, 2 * jj + 1);
+                            mma16816(acc[m], a0, a1, a2, a3, ptb0[m / 2], ptb1[m / 2]);
+                        }
+                    }
                 }
             }
         }
@@ -303,42 +427,49 @@ __global__ void __launch_bounds__(NTHREADS, 2) k_attend_kivi(const KiviParams p)
             mbar_arrive(&empty[st]);
     }
 
-    // ---------------- finish: zero term into O, merge the warps, write partials
+    // ---------------- back to plain units, add the zero term, merge the warps
+    if (code_units) {
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) {
+            const int jj = m % Cfg::MPW;
+            const float wr = TWO24 / pair_weight<BITS>(2 * jj);
+            const float wr8 = TWO24 / pair_weight<BITS>(2 * jj + 1);
+            acc[m][0] *= wr;
+            acc[m][1] *= wr;
+            acc[m][2] *= wr8;
+            acc[m][3] *= wr8;
+        }
+    }
+#pragma unroll
+    for (int gd = 0; gd < Cfg::NG; ++gd) {
+        const float z0 = __shfl_sync(0xffffffffu, zacc[0], 4 * gd + c);
+        const float z1 = __shfl_sync(0xffffffffu, zacc[1], 4 * gd + c);
+        acc[2 * gd][0] += z0;
+        acc[2 * gd][1] += z1;
+        acc[2 * gd][2] += z0;
+        acc[2 * gd][3] += z1;
+        acc[2 * gd + 1][0] += z0;
+        acc[2 * gd + 1][1] += z1;
+        acc[2 * gd + 1][2] += z0;
+        acc[2 * gd + 1][3] += z1;
+    }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, off);
         l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, off);
-    }
-#pragma unroll
-    for (int j = 0; j < Cfg::NG; ++j) {
-        zacc[j] += __shfl_xor_sync(0xffffffffu, zacc[j], 1);
-        zacc[j] += __shfl_xor_sync(0xffffffffu, zacc[j], 2);
-    }
-    float z0[Cfg::NG], z1[Cfg::NG];
-#pragma unroll
-    for (int j = 0; j < Cfg::NG; ++j) {
-        z0[j] = __shfl_sync(0xffffffffu, zacc[j], 4 * h0);
-        z1[j] = __shfl_sync(0xffffffffu, zacc[j], 4 * h1);
-    }
-#pragma unroll
-    for (int m = 0; m < D / 16; ++m) {
-        acc[m][0] += z0[m / 2];
-        acc[m][1] += z1[m / 2];
-        acc[m][2] += z0[m / 2];
-        acc[m][3] += z1[m / 2];
     }
     consumer_bar();
     float *redO = reinterpret_cast<float *>(smem);
     float *redM = redO + NCW * 8 * D;
     float *redL = redM + NCW * 8;
     {
-        float *w = redO + warp * 8 * D;
+        float *wo = redO + warp * 8 * D;
 #pragma unroll
         for (int m = 0; m < D / 16; ++m) {
-            w[h0 * D + 16 * m + r] = acc[m][0];
-            w[h1 * D + 16 * m + r] = acc[m][1];
-            w[h0 * D + 16 * m + r + 8] = acc[m][2];
-            w[h1 * D + 16 * m + r + 8] = acc[m][3];
+            wo[h0 * D + 16 * m + r] = acc[m][0];
+            wo[h1 * D + 16 * m + r] = acc[m][1];
+            wo[h0 * D + 16 * m + r + 8] = acc[m][2];
+            wo[h1 * D + 16 * m + r + 8] = acc[m][3];
         }
         if (r == 0) {
             redM[warp * 8 + h0] = m_run0;
@@ -348,6 +479,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) k_attend_kivi(const KiviParams p)
         }
     }
     consumer_bar();
+    const bool single = p.part_o == nullptr;
     for (int e = threadIdx.x; e < p.g * D; e += NCW * 32) {
         const int h = e / D, d = e % D;
         float ms = -INFINITY;
@@ -362,17 +494,26 @@ __global__ void __launch_bounds__(NTHREADS, 2) k_attend_kivi(const KiviParams p)
             ls += sc * redL[w * 8 + h];
             os += sc * redO[(w * 8 + h) * D + d];
         }
-        const size_t pi = ((size_t)unit * p.part_splits + split) * p.g + h;
-        p.part_o[pi * D + d] = os;
-        if (d == 0) {
-            p.part_ml[2 * pi] = ls > 0.f ? ms : -INFINITY;
-            p.part_ml[2 * pi + 1] = ls;
+        if (single) {
+            const size_t oi = ((size_t)b * p.Hq + hk * p.g + h) * D + d;
+            p.o[oi] = __half_as_ushort(__float2half_rn(ls > 0.f ? os / ls : 0.f));
+            if (d == 0 && p.lse)
+                p.lse[(size_t)b * p.Hq + hk * p.g + h] =
+                    ls > 0.f ? (ms + __log2f(ls)) * LN2 : -INFINITY;
+        } else {
+            const size_t pi = ((size_t)unit * p.splits + split) * p.g + h;
+            p.part_o[pi * D + d] = os;
+            if (d == 0) {
+                p.part_ml[2 * pi] = ls > 0.f ? ms : -INFINITY;
+                p.part_ml[2 * pi + 1] = ls;
+            }
         }
     }
 }
 
 template <int D, int BITS>
-cudaError_t launch_kivi_impl(const KiviParams &kp, int grid, cudaStream_t s)
+cudaError_t launch_kivi_impl(const CUtensorMap &tk, const CUtensorMap &tv, const KiviParams &kp,
+                             int grid, cudaStream_t s)
 {
     using Cfg = KiviCfg<D, BITS>;
     static int configured_device = -1;
@@ -385,7 +526,7 @@ cudaError_t launch_kivi_impl(const KiviParams &kp, int grid, cudaStream_t s)
             return e;
         configured_device = dev;
     }
-    k_attend_kivi<D, BITS><<<grid, NTHREADS, Cfg::SMEM, s>>>(kp);
+    k_attend_kivi<D, BITS><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, kp);
     return cudaGetLastError();
 }
 
@@ -393,36 +534,43 @@ cudaError_t launch_kivi_impl(const KiviParams &kp, int grid, cudaStream_t s)
 
 cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s)
 {
+    const int CR = a.R + KIVI_G;
+    CUtensorMap tk, tv;
+    const uint64_t rows = (uint64_t)a.B * a.Hkv * CR;
+    if (!encode_tmap_2d_f16(&tk, a.k_res, a.D, rows, 64, 32) ||
+        !encode_tmap_2d_f16(&tv, a.v_res, a.D, rows, 64, 32))
+        return cudaErrorInvalidValue;
     KiviParams kp{};
     kp.Hq = a.Hq;
     kp.Hkv = a.Hkv;
     kp.g = a.Hq / a.Hkv;
     kp.Cq = a.Cq;
     kp.R = a.R;
+    kp.CR = CR;
     kp.splits = a.splits;
-    kp.tiles_per_split = a.tiles_per_split;
-    kp.part_splits = a.splits + 1;
+    kp.qtiles_per_split = a.tiles_per_split;
     kp.q = a.q;
+    kp.o = a.o;
+    kp.lse = a.lse;
     kp.kb = a.kb;
     kp.vb = a.vb;
     kp.len = a.len;
-    kp.part_o = a.part_o;
-    kp.part_ml = a.part_ml;
+    kp.part_o = a.splits > 1 ? a.part_o : nullptr;
+    kp.part_ml = a.splits > 1 ? a.part_ml : nullptr;
+    kp.scale = a.scale;
     kp.scale_log2 = a.scale * LOG2E;
     kp.status = dev_status_ptr();
     const int grid = a.B * a.Hkv * a.splits;
     cudaError_t e;
     if (a.D == 128)
-        e = a.bits == 4 ? launch_kivi_impl<128, 4>(kp, grid, s) : launch_kivi_impl<128, 2>(kp, grid, s);
+        e = a.bits == 4 ? launch_kivi_impl<128, 4>(tk, tv, kp, grid, s)
+                        : launch_kivi_impl<128, 2>(tk, tv, kp, grid, s);
     else
-        e = a.bits == 4 ? launch_kivi_impl<64, 4>(kp, grid, s) : launch_kivi_impl<64, 2>(kp, grid, s);
-    if (e != cudaSuccess)
+        e = a.bits == 4 ? launch_kivi_impl<64, 4>(tk, tv, kp, grid, s)
+                        : launch_kivi_impl<64, 2>(tk, tv, kp, grid, s);
+    if (e != cudaSuccess || a.splits == 1)
         return e;
-    e = launch_attend_ring(a.B, a.Hq, a.Hkv, a.D, a.R, a.q, a.k_res, a.v_res, a.len, a.part_o,
-                           a.part_ml, a.splits + 1, a.splits, a.scale, s);
-    if (e != cudaSuccess)
-        return e;
-    return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits + 1, a.part_o, a.part_ml, a.o, a.lse, s);
+    return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);
 }
 
 } // namespace kvc

@@ -1,5 +1,5 @@
-// attend_slots.cu -- split-KV decode attention over an fp16 slot cache (and
-// over the fp16 residual ring of a KIVI cache), plus the split combine.
+// attend_slots.cu -- split-KV decode attention over an fp16 slot cache, plus
+// the split combine (shared with the KIVI kernel).
 //
 // One CTA handles one (sequence b, KV head hk, split) work item: the g query
 // heads of hk against the split's token range.  A producer warp streams K and
@@ -44,12 +44,9 @@ template <int D> struct SlotCfg {
 struct SlotParams {
     int Hq, Hkv, C, g;
     int splits, tiles_per_split;
-    int part_splits, part_offset;   // partial array geometry (ring mode writes one slot)
     const uint16_t *q;
     uint16_t *o;
-    const int32_t *n;               // valid slots per unit (slot mode)
-    const int32_t *len;             // tokens per sequence (ring mode)
-    int R;                          // residual length (ring mode)
+    const int32_t *n;               // valid slots per unit
     float *logits, *lse;
     float *part_o, *part_ml;
     float scale, scale_log2;
@@ -61,10 +58,8 @@ __device__ __forceinline__ void consumer_bar()
     asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
 }
 
-// RING = false: slots [0, n) of a slot cache are valid.
-// RING = true : the unit's C = R + 32 ring slots; slot s holds the newest
-//               position p < T with p = s (mod C), valid when p >= n_q.
-template <int D, bool RING>
+// Slots [0, n) of each unit are valid.
+template <int D>
 __global__ void __launch_bounds__(NTHREADS, 2)
     k_attend_slots(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const SlotParams p)
@@ -81,23 +76,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const int b = unit / p.Hkv, hk = unit % p.Hkv;
 
     // token range of this split
-    int n_valid, ring_T = 0, ring_nres = 0;
-    if (RING) {
-        ring_T = p.len[b];
-        int over = ring_T - p.R;
-        int n_q = over > 0 ? (over / KIVI_G) * KIVI_G : 0;
-        ring_nres = ring_T - n_q;
-        n_valid = p.C;   // scan the whole ring, mask by age
-    } else {
-        n_valid = p.n[unit];
-        if (n_valid > p.C) {
-            if (threadIdx.x == 0)
-                flag_error(p.status, DEV_CAPACITY);
-            n_valid = p.C;
-        }
-        if (n_valid < 0)
-            n_valid = 0;
+    int n_valid = p.n[unit];
+    if (n_valid > p.C) {
+        if (threadIdx.x == 0)
+            flag_error(p.status, DEV_CAPACITY);
+        n_valid = p.C;
     }
+    if (n_valid < 0)
+        n_valid = 0;
     const int t_begin = split * p.tiles_per_split * TILE;
     const int t_end = min(n_valid, t_begin + p.tiles_per_split * TILE);
     const int ntiles = t_end > t_begin ? (t_end - t_begin + TILE - 1) / TILE : 0;
@@ -160,7 +146,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
     const int h0 = 2 * c, h1 = 2 * c + 1;
     float *lg0 = nullptr, *lg1 = nullptr;
-    if (!RING && p.logits) {
+    if (p.logits) {
         const size_t rowbase = ((size_t)b * p.Hq + hk * p.g) * p.C;
         lg0 = h0 < p.g ? p.logits + rowbase + (size_t)h0 * p.C : nullptr;
         lg1 = h1 < p.g ? p.logits + rowbase + (size_t)h1 * p.C : nullptr;
@@ -188,17 +174,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             }
 
             const int ta = tok0 + r, tb = tok0 + r + 8;
-            bool va = ta < t_end, vb = tb < t_end;
-            if (RING) {
-                const int CR = p.C;
-                va = va && ((ring_T - 1 - ta) % CR + CR) % CR < ring_nres;
-                vb = vb && ((ring_T - 1 - tb) % CR + CR) % CR < ring_nres;
-            }
-            if (!RING && lg0) {
+            const bool va = ta < t_end, vb = tb < t_end;
+            if (lg0) {
                 if (va) lg0[ta] = sa[0] * p.scale;
                 if (vb) lg0[tb] = sa[2] * p.scale;
             }
-            if (!RING && lg1) {
+            if (lg1) {
                 if (va) lg1[ta] = sa[1] * p.scale;
                 if (vb) lg1[tb] = sa[3] * p.scale;
             }
@@ -295,7 +276,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 p.lse[(size_t)b * p.Hq + hk * p.g + h] =
                     ls > 0.f ? (ms + __log2f(ls)) * LN2 : -INFINITY;
         } else {
-            const size_t pi = ((size_t)unit * p.part_splits + p.part_offset + split) * p.g + h;
+            const size_t pi = ((size_t)unit * p.splits + split) * p.g + h;
             p.part_o[pi * D + d] = os;
             if (d == 0) {
                 p.part_ml[2 * pi] = ls > 0.f ? ms : -INFINITY;
@@ -334,7 +315,7 @@ __global__ void k_combine(int Hq, int Hkv, int g, int D, int splits, const float
         lse[bh] = ls > 0.f ? (ms + __log2f(ls)) * LN2 : -INFINITY;
 }
 
-template <int D, bool RING>
+template <int D>
 cudaError_t launch_slots_impl(const CUtensorMap &tk, const CUtensorMap &tv, const SlotParams &sp,
                               int grid, cudaStream_t s)
 {
@@ -343,13 +324,13 @@ cudaError_t launch_slots_impl(const CUtensorMap &tk, const CUtensorMap &tv, cons
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_attend_slots<D, RING>,
+        cudaError_t e = cudaFuncSetAttribute(k_attend_slots<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
         if (e != cudaSuccess)
             return e;
         configured_device = dev;
     }
-    k_attend_slots<D, RING><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
+    k_attend_slots<D><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
     return cudaGetLastError();
 }
 
@@ -370,13 +351,9 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
     sp.g = a.Hq / a.Hkv;
     sp.splits = a.splits;
     sp.tiles_per_split = a.tiles_per_split;
-    sp.part_splits = a.splits;
-    sp.part_offset = 0;
     sp.q = a.q;
     sp.o = a.o;
     sp.n = a.n;
-    sp.len = nullptr;
-    sp.R = 0;
     sp.logits = a.logits;
     sp.lse = a.splits == 1 ? a.lse : nullptr;
     sp.part_o = a.splits == 1 ? nullptr : a.part_o;
@@ -385,45 +362,11 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
     sp.scale_log2 = a.scale * LOG2E;
     sp.status = dev_status_ptr();
     const int grid = units * a.splits;
-    cudaError_t e = a.D == 128 ? launch_slots_impl<128, false>(tk, tv, sp, grid, s)
-                               : launch_slots_impl<64, false>(tk, tv, sp, grid, s);
+    cudaError_t e = a.D == 128 ? launch_slots_impl<128>(tk, tv, sp, grid, s)
+                               : launch_slots_impl<64>(tk, tv, sp, grid, s);
     if (e != cudaSuccess || a.splits == 1)
         return e;
     return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);
-}
-
-// Residual ring of a KIVI cache: one work item per unit, written as partial
-// number `part_offset` of `part_splits`.
-cudaError_t launch_attend_ring(int B, int Hq, int Hkv, int D, int R, const uint16_t *q,
-                               const uint16_t *k_res, const uint16_t *v_res, const int32_t *len,
-                               float *part_o, float *part_ml, int part_splits, int part_offset,
-                               float scale, cudaStream_t s)
-{
-    const int units = B * Hkv;
-    const int CR = R + KIVI_G;
-    CUtensorMap tk, tv;
-    if (!encode_tmap_2d_f16(&tk, k_res, D, (uint64_t)units * CR, 64, TILE) ||
-        !encode_tmap_2d_f16(&tv, v_res, D, (uint64_t)units * CR, 64, TILE))
-        return cudaErrorInvalidValue;
-    SlotParams sp{};
-    sp.Hq = Hq;
-    sp.Hkv = Hkv;
-    sp.C = CR;
-    sp.g = Hq / Hkv;
-    sp.splits = 1;
-    sp.tiles_per_split = (CR + TILE - 1) / TILE;
-    sp.part_splits = part_splits;
-    sp.part_offset = part_offset;
-    sp.q = q;
-    sp.len = len;
-    sp.R = R;
-    sp.part_o = part_o;
-    sp.part_ml = part_ml;
-    sp.scale = scale;
-    sp.scale_log2 = scale * LOG2E;
-    sp.status = dev_status_ptr();
-    return D == 128 ? launch_slots_impl<128, true>(tk, tv, sp, units, s)
-                    : launch_slots_impl<64, true>(tk, tv, sp, units, s);
 }
 
 cudaError_t launch_combine(int B, int Hq, int Hkv, int D, int splits, const float *part_o,

@@ -359,7 +359,9 @@ ORC_API void orc_kivi_quantize_unit(int D, int G, int bits, long n_q, const uint
  *   D/G zeros) f16].  Pair i holds tokens 2i (low 16 bits of every word) and
  *   2i+1 (high 16 bits).  Word index r*W + k (r in [0,8), k in [0,W),
  *   W = D*bits/128); field j (bits [bits*j, bits*(j+1)) of each 16-bit half)
- *   holds channel d = 16*(k*(8/bits) + j/2) + 8*(j%2) + r.
+ *   holds channel d = 16*(k*(8/bits) + j/2) + 8*(j%2) + r.  Then the V scales
+ *   as D/G rows of G values (row j: channel group j of tokens 0..G-1), then the
+ *   V zeros in the same order.
  */
 ORC_API void orc_kivi_pack_group(int D, int G, int bits, const uint8_t *k_codes,
                                  const uint16_t *k_scale, const uint16_t *k_zero,
@@ -397,12 +399,11 @@ ORC_API void orc_kivi_pack_group(int D, int G, int bits, const uint8_t *k_codes,
             }
     uint16_t *vs = (uint16_t *)(v_block + (size_t)(G / 2) * (2 * WK) * 4);
     int ng = D / G;
-    for (int t = 0; t < G; ++t) {
-        for (int j = 0; j < ng; ++j) {
-            vs[t * 2 * ng + j] = v_scale[t * ng + j];
-            vs[t * 2 * ng + ng + j] = v_zero[t * ng + j];
+    for (int j = 0; j < ng; ++j)
+        for (int t = 0; t < G; ++t) {
+            vs[j * G + t] = v_scale[t * ng + j];
+            vs[ng * G + j * G + t] = v_zero[t * ng + j];
         }
-    }
 }
 
 /*

@@ -82,20 +82,20 @@ def test_pack_bit_exact_with_flushes(kvc, orc, D, bits, R):
     assert device_status_clean(kvc)
 
 
-def _attend(kvc, cache, q):
+def _attend(kvc, cache, q, splits=0):
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device="cuda")
-    ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), dtype=torch.float32,
+    ws = torch.empty(max(kvc.kvc_workspace_size(cache, q, splits) // 4, 1), dtype=torch.float32,
                      device="cuda")
-    kvc.kvc_decode_attend(cache, q, o, lse=lse, workspace=ws)
+    kvc.kvc_decode_attend(cache, q, o, lse=lse, workspace=ws, num_splits=splits)
     torch.cuda.synchronize()
     return o, lse
 
 
-@pytest.mark.parametrize("D,bits,R,Hq,Hkv", [(64, 4, 16, 4, 4), (128, 4, 128, 8, 1),
-                                             (128, 2, 128, 16, 2), (64, 2, 0, 4, 2),
-                                             (128, 4, 100, 3, 3)])
-def test_attention_small(kvc, orc, D, bits, R, Hq, Hkv):
+@pytest.mark.parametrize("D,bits,R,Hq,Hkv,splits", [
+    (64, 4, 16, 4, 4, 0), (128, 4, 128, 8, 1, 0), (128, 2, 128, 16, 2, 0), (64, 2, 0, 4, 2, 0),
+    (128, 4, 100, 3, 3, 0), (128, 4, 128, 8, 2, 1), (128, 2, 16, 8, 2, 3), (64, 4, 16, 8, 1, 2)])
+def test_attention_small(kvc, orc, D, bits, R, Hq, Hkv, splits):
     g = torch.Generator().manual_seed(7 * D + bits + Hq)
     B = 3
     chunks = [150, 1, 1, 33]
@@ -106,7 +106,7 @@ def test_attention_small(kvc, orc, D, bits, R, Hq, Hkv):
     q = torch.randn(B, Hq, D, generator=g).half()
     cache, lens = _build(kvc, Kseq.cuda(), Vseq.cuda(), bits, R, Cq=256, chunks=chunks,
                          offsets=offsets)
-    o, lse = _attend(kvc, cache, q.cuda())
+    o, lse = _attend(kvc, cache, q.cuda(), splits)
     gq = Hq // Hkv
     for b in range(B):
         for hk in range(Hkv):

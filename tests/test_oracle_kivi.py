@@ -161,8 +161,8 @@ def _unpack_from_spec(kb, vb, D, bits):
                     assert vc[2 * i, d] == 255 and vc[2 * i + 1, d] == 255
                     vc[2 * i, d] = (word >> (bits * j)) & mask
                     vc[2 * i + 1, d] = (word >> (16 + bits * j)) & mask
-    vs = vb[G * WK * 4:].view(np.uint16).reshape(G, 2, D // G)
-    return kc, ks[:D], ks[D:], vc, vs[:, 0], vs[:, 1]
+    vs = vb[G * WK * 4:].view(np.uint16).reshape(2, D // G, G)
+    return kc, ks[:D], ks[D:], vc, vs[0].T, vs[1].T
 
 
 @pytest.mark.parametrize("D", [64, 128])

@@ -71,17 +71,17 @@ def test_kivi_cache_matches_workspace_entry_point(kvc):
     cache = kvc.QuantCache.empty(B, Hkv, 256, D, 4, 32)
     kvc.kvc_append_quant(cache, K, V)
     torch.cuda.synchronize()
-    o_ref, lse_ref = _reference(kvc, cache, q, splits=0)
-    for o, lse in _twice(kvc, cache, q, splits=0):
+    o_ref, lse_ref = _reference(kvc, cache, q, splits=2)
+    for o, lse in _twice(kvc, cache, q, splits=2):
         assert_o_close(np16(o), np16(o_ref).astype(np.float64))
         assert torch.allclose(lse, lse_ref, atol=1e-4, rtol=0)
 
 
 def test_too_much_scratch_is_rejected(kvc):
     B, Hq, Hkv, D = 256, 64, 8, 128
-    cache = kvc.QuantCache.empty(B, Hkv, 64, D, 4, 16)
+    cache = kvc.QuantCache.empty(B, Hkv, 512, D, 4, 16)
     q = torch.zeros(B, Hq, D, dtype=torch.float16, device="cuda")
-    assert kvc.kvc_workspace_size(cache, q) > kvc.KVC_NOALLOC_SCRATCH_BYTES
+    assert kvc.kvc_workspace_size(cache, q, num_splits=4) > kvc.KVC_NOALLOC_SCRATCH_BYTES
     with pytest.raises(kvc.KvcError) as e:
-        kvc.kvc_decode_attend_noalloc(cache, q, torch.empty_like(q))
+        kvc.kvc_decode_attend_noalloc(cache, q, torch.empty_like(q), num_splits=4)
     assert e.value.status == kvc.KVC_ERR_WORKSPACE
