@@ -122,9 +122,10 @@ typedef struct kvc_slot_cache {
  *     t's word w, field i (bits [bits*i, bits*(i+1))) holds channel
  *     d = (32/bits)*w + i.  Then D fp16 scales (per channel), then D fp16 zeros.
  *   V block: 16 token pairs of 2*WK words.  Pair i holds tokens 2i (low 16 bits
- *     of every word) and 2i+1 (high 16 bits).  Its word r*W + k (r in [0,8),
- *     k in [0,W), W = D*bits/128) holds in field j (bits [bits*j, bits*(j+1))
- *     of each 16-bit half) channel d = 16*(k*(8/bits) + j/2) + 8*(j%2) + r.
+ *     of every word) and 2i+1 (high 16 bits).  Its word ((r + 2i) mod 8)*W + k
+ *     (r in [0,8), k in [0,W), W = D*bits/128) holds in field j (bits
+ *     [bits*j, bits*(j+1)) of each 16-bit half) channel
+ *     d = 16*(k*(8/bits) + j/2) + 8*(j%2) + r.
  *     Then the V scales as D/32 rows of 32 fp16 values (row j holds channel
  *     group j of tokens 0..31), then the V zeros in the same [D/32][32] order.
  *   k_res, v_res [B, Hkv, R + 32, D] fp16 residual rings;  len [B] int32.

@@ -224,11 +224,12 @@ __global__ void __launch_bounds__(QTHREADS)
                 word |= (uint32_t)ck[t][(32 / BITS) * w + f] << (BITS * f);
             kw[i] = word;
         }
-        // pack V token pairs: word r*W + k, field j holds channel
-        // 16*(k*(8/BITS) + j/2) + 8*(j%2) + r; low half token 2i, high half 2i+1
+        // pack V token pairs: word ((rr + 2 pair) mod 8)*W + k, field j holds channel
+        // 16*(k*(8/BITS) + j/2) + 8*(j%2) + rr; low half token 2i, high half 2i+1
         uint32_t *vw = reinterpret_cast<uint32_t *>(vblk);
         for (int i = threadIdx.x; i < (G / 2) * 8 * W; i += QTHREADS) {
             const int pair = i / (8 * W), rk = i % (8 * W), rr = rk / W, k = rk % W;
+            const int slot = pair * 8 * W + ((rr + 2 * pair) & 7) * W + k;
             uint32_t word = 0;
 #pragma unroll
             for (int j = 0; j < 16 / BITS; ++j) {
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(QTHREADS)
                 word |= (uint32_t)cv[2 * pair][d] << (BITS * j);
                 word |= (uint32_t)cv[2 * pair + 1][d] << (16 + BITS * j);
             }
-            vw[i] = word;
+            vw[slot] = word;
         }
         __syncthreads();
     }

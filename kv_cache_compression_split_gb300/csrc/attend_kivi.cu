@@ -187,43 +187,23 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const bool hv = r < p.g;
     const uint16_t *qrow = p.q + ((size_t)b * p.Hq + hk * p.g + (hv ? r : 0)) * D;
 
-    // fp16 query fragments for the residual tiles (B = Q^T, as in the slot kernel)
-    uint32_t qf[D / 16][2];
-    // query pairs for the quantised tiles: lane c covers channels [c D/4, (c+1) D/4);
-    // pair pi holds channels (lo, lo + HALF) divided by the pair's field weight
-    uint32_t qpair[D / 8];
-    float qz[D / 4];
-    {
-        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
-#pragma unroll
-        for (int s = 0; s < D / 16; ++s) {
-            qf[s][0] = hv ? q32[8 * s + c] : 0u;
-            qf[s][1] = hv ? q32[8 * s + c + 4] : 0u;
-        }
-#pragma unroll
-        for (int i = 0; i < D / 4; ++i)
-            qz[i] = hv ? __half2float(__ushort_as_half(qrow[c * (D / 4) + i])) : 0.f;
-#pragma unroll
-        for (int pi = 0; pi < D / 8; ++pi) {
-            const int j = pi % Cfg::HALF;
-            const int lo = Cfg::FPW * (pi / Cfg::HALF) + j;
-            const float wgt = 1.0f / pair_weight<BITS>(j);
-            qpair[pi] = pack_half2(qz[lo] * wgt, qz[lo + Cfg::HALF] * wgt);
-        }
-    }
-
     float acc[D / 16][4];
 #pragma unroll
     for (int m = 0; m < D / 16; ++m)
         acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
-    float zacc[4] = {0.f, 0.f, 0.f, 0.f};   // Z[group r][heads 2c, 2c+1] (rows r < NG)
+    float zacc[2] = {0.f, 0.f};   // Z[group r][heads 2c, 2c+1] (meaningful for r < NG)
     float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
-    bool code_units = false;                // acc scaled to the quantised tiles' units
 
-    // online-softmax update for a 16-token row block; x* are log2-domain scores
-    auto softmax16 = [&](float x0, float x1, float x2, float x3, float &p0, float &p1, float &p2,
-                         float &p3) {
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+    // online-softmax update over the scores a lane holds (N values per head);
+    // x*: log2-domain scores of heads 2c (xa) and 2c+1 (xb); p* returns exp2(x - m)
+    auto softmax_update = [&](auto &xa, auto &xb, int N) {
+        float mx0 = xa[0], mx1 = xb[0];
+#pragma unroll
+        for (int e = 1; e < 4; ++e)
+            if (e < N) {
+                mx0 = fmaxf(mx0, xa[e]);
+                mx1 = fmaxf(mx1, xb[e]);
+            }
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -233,14 +213,19 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const bool z0 = mn0 == -INFINITY, z1 = mn1 == -INFINITY;
         const float al0 = z0 ? 1.f : ex2(m_run0 - mn0);
         const float al1 = z1 ? 1.f : ex2(m_run1 - mn1);
-        p0 = z0 ? 0.f : ex2(x0 - mn0);
-        p2 = z0 ? 0.f : ex2(x2 - mn0);
-        p1 = z1 ? 0.f : ex2(x1 - mn1);
-        p3 = z1 ? 0.f : ex2(x3 - mn1);
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (e < N) {
+                xa[e] = z0 ? 0.f : ex2(xa[e] - mn0);
+                xb[e] = z1 ? 0.f : ex2(xb[e] - mn1);
+                s0 += xa[e];
+                s1 += xb[e];
+            }
         m_run0 = mn0;
         m_run1 = mn1;
-        l_run0 = l_run0 * al0 + p0 + p2;
-        l_run1 = l_run1 * al1 + p1 + p3;
+        l_run0 = l_run0 * al0 + s0;
+        l_run1 = l_run1 * al1 + s1;
         if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
             for (int m = 0; m < D / 16; ++m) {
@@ -254,18 +239,30 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         }
     };
 
-    for (int i = 0; i < ntiles; ++i) {
-        const int st = i % Cfg::NSTAGE;
-        if (!mbar_wait(&full[st], (i / Cfg::NSTAGE) & 1)) {
-            flag_error(p.status, DEV_TIMEOUT);
-            break;
+    int i = 0;
+    // ======================= fp16 residual tiles (last split only)
+    if (nr > 0) {
+        // Q^T as the B operand: Q[head r][16s + 2c, +1] and [16s + 2c + 8, +1]
+        uint32_t qf[D / 16][2];
+        {
+            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
+#pragma unroll
+            for (int s = 0; s < D / 16; ++s) {
+                qf[s][0] = hv ? q32[8 * s + c] : 0u;
+                qf[s][1] = hv ? q32[8 * s + c + 4] : 0u;
+            }
         }
-        uint8_t *tile = smem + st * Cfg::STAGE_BYTES;
-        if (i < nr) {
-            // ---------------- fp16 residual tile: warps 0, 1 take 16 ring slots each
+        for (; i < nr; ++i) {
+            const int st = i % Cfg::NSTAGE;
+            if (!mbar_wait(&full[st], (i / Cfg::NSTAGE) & 1)) {
+                flag_error(p.status, DEV_TIMEOUT);
+                i = ntiles;
+                break;
+            }
+            // warps 0, 1 take 16 ring slots each
             const int s0 = i * Cfg::RS + 16 * warp;
             if (warp < 2 && s0 < p.CR) {
-                const uint32_t kbase = smem_u32(tile);
+                const uint32_t kbase = smem_u32(smem + st * Cfg::STAGE_BYTES);
                 const uint32_t vbase = kbase + Cfg::NBOX * Cfg::RS * 128;
                 float sa[4] = {0.f, 0.f, 0.f, 0.f};
                 const int krow = 16 * warp + ri + 8 * (mi & 1);
@@ -279,12 +276,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 const int ta = s0 + r, tb = s0 + r + 8;
                 const bool va = ta < p.CR && ((T - 1 - ta) % p.CR + p.CR) % p.CR < n_res;
                 const bool vb = tb < p.CR && ((T - 1 - tb) % p.CR + p.CR) % p.CR < n_res;
-                float p0, p1, p2, p3;
-                softmax16(va ? sa[0] * p.scale_log2 : -INFINITY, va ? sa[1] * p.scale_log2 : -INFINITY,
-                          vb ? sa[2] * p.scale_log2 : -INFINITY, vb ? sa[3] * p.scale_log2 : -INFINITY,
-                          p0, p1, p2, p3);
-                const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
-                const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
+                float xa[2] = {va ? sa[0] * p.scale_log2 : -INFINITY, vb ? sa[2] * p.scale_log2 : -INFINITY};
+                float xb[2] = {va ? sa[1] * p.scale_log2 : -INFINITY, vb ? sa[3] * p.scale_log2 : -INFINITY};
+                softmax_update(xa, xb, 2);
+                const uint32_t pb0 = movmatrix_t(pack_half2(xa[0], xb[0]));
+                const uint32_t pb1 = movmatrix_t(pack_half2(xa[1], xb[1]));
                 const int vrow = 16 * warp + ri + 8 * (mi >> 1);
 #pragma unroll
                 for (int m = 0; m < D / 16; ++m) {
@@ -294,131 +290,171 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                     mma16816(acc[m], a0, a1, a2, a3, pb0, pb1);
                 }
             }
-        } else {
-            // ---------------- quantised tile: warp w takes group w (32 tokens)
-            const int g0 = (qt0 + i - nr) * Cfg::QG;
-            if (g0 + warp < n_groups) {
-                if (!code_units) {
-                    // switch the accumulator to the quantised tiles' units
-#pragma unroll
-                    for (int m = 0; m < D / 16; ++m) {
-                        const int jj = m % Cfg::MPW;
-                        const float wr = pair_weight<BITS>(2 * jj) * TWOM24;
-                        const float wr8 = pair_weight<BITS>(2 * jj + 1) * TWOM24;
-                        acc[m][0] *= wr;
-                        acc[m][1] *= wr;
-                        acc[m][2] *= wr8;
-                        acc[m][3] *= wr8;
-                    }
-                    code_units = true;
-                }
-                const uint8_t *kblk = tile + warp * Cfg::BLOCK;
-                const uint8_t *vblk = tile + (Cfg::QG + warp) * Cfg::BLOCK;
-                const uint32_t *ksz = reinterpret_cast<const uint32_t *>(kblk + Cfg::CODE_BYTES);
-                const uint16_t *vsz = reinterpret_cast<const uint16_t *>(vblk + Cfg::CODE_BYTES);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[st]);
+        }
+    }
 
-                // q~ pairs (B operand) and the bias sum_d q_d z_d for head r
-                uint32_t qt[D / 8];
-                float beta = 0.f;
-                {
-                    const uint32_t *sl = ksz + c * (D / 8);          // scales of my channels
-                    const uint32_t *zl = ksz + D / 2 + c * (D / 8);  // zeros of my channels
-                    uint32_t sw[D / 8];
+    // ======================= quantised tiles: warp w takes group w (32 tokens)
+    // query pairs: lane c covers channels [c D/4, (c+1) D/4); pair pi holds channels
+    // (lo, lo + HALF) divided by the pair's field weight.  qh: the same channels in order.
+    uint32_t qpair[D / 8], qh[D / 8];
+    {
+        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow + c * (D / 4));
 #pragma unroll
-                    for (int e = 0; e < D / 8; ++e)
-                        sw[e] = sl[e];
+        for (int e = 0; e < D / 8; ++e)
+            qh[e] = hv ? q32[e] : 0u;
 #pragma unroll
-                    for (int pi = 0; pi < D / 8; ++pi) {
-                        const int lo = Cfg::FPW * (pi / Cfg::HALF) + pi % Cfg::HALF;
-                        const int hi = lo + Cfg::HALF;
-                        const uint32_t wa = sw[lo >> 1], wb = sw[hi >> 1];
-                        const uint32_t sp = __byte_perm(wa, wb, ((lo & 1) ? 0x0032 : 0x0010) |
-                                                                    ((hi & 1) ? 0x7600 : 0x5400));
-                        qt[pi] = hmul2_u32(qpair[pi], sp);
-                    }
+        for (int pi = 0; pi < D / 8; ++pi) {
+            const int j = pi % Cfg::HALF;
+            const int lo = Cfg::FPW * (pi / Cfg::HALF) + j, hi = lo + Cfg::HALF;
+            const __half2 wl = *reinterpret_cast<const __half2 *>(&qh[lo >> 1]);
+            const __half2 wh = *reinterpret_cast<const __half2 *>(&qh[hi >> 1]);
+            const float qlo = (lo & 1) ? __high2float(wl) : __low2float(wl);
+            const float qhi = (hi & 1) ? __high2float(wh) : __low2float(wh);
+            const float wgt = 1.0f / pair_weight<BITS>(j);
+            qpair[pi] = pack_half2(qlo * wgt, qhi * wgt);
+        }
+    }
+    bool code_units = false;   // acc scaled to the quantised tiles' units
+    for (; i < ntiles; ++i) {
+        const int st = i % Cfg::NSTAGE;
+        if (!mbar_wait(&full[st], (i / Cfg::NSTAGE) & 1)) {
+            flag_error(p.status, DEV_TIMEOUT);
+            break;
+        }
+        const int g0 = (qt0 + i - nr) * Cfg::QG;
+        if (g0 + warp < n_groups) {
+            if (!code_units) {
 #pragma unroll
-                    for (int e = 0; e < D / 8; ++e) {
-                        const float2 zf = __half22float2(*reinterpret_cast<const __half2 *>(&zl[e]));
-                        beta = fmaf(qz[2 * e], zf.x, beta);
-                        beta = fmaf(qz[2 * e + 1], zf.y, beta);
-                    }
-                    beta += __shfl_xor_sync(0xffffffffu, beta, 1);
-                    beta += __shfl_xor_sync(0xffffffffu, beta, 2);
+                for (int m = 0; m < D / 16; ++m) {
+                    const int jj = m % Cfg::MPW;
+                    const float wr = pair_weight<BITS>(2 * jj) * TWOM24;
+                    const float wr8 = pair_weight<BITS>(2 * jj + 1) * TWOM24;
+                    acc[m][0] *= wr;
+                    acc[m][1] *= wr;
+                    acc[m][2] *= wr8;
+                    acc[m][3] *= wr8;
                 }
-                const float bias0 = __shfl_sync(0xffffffffu, beta, 4 * h0) * p.scale_log2;
-                const float bias1 = __shfl_sync(0xffffffffu, beta, 4 * h1) * p.scale_log2;
-                const float sk = TWO24 * p.scale_log2;
+                code_units = true;
+            }
+            const uint8_t *tile = smem + st * Cfg::STAGE_BYTES;
+            const uint8_t *kblk = tile + warp * Cfg::BLOCK;
+            const uint8_t *vblk = tile + (Cfg::QG + warp) * Cfg::BLOCK;
+            const uint32_t *ksz = reinterpret_cast<const uint32_t *>(kblk + Cfg::CODE_BYTES);
+            const uint32_t *vss = reinterpret_cast<const uint32_t *>(vblk + Cfg::CODE_BYTES);
+            const uint32_t *vzz = vss + Cfg::NG * Cfg::G / 2;
 
+            // ---- q~ pairs (B operand) and the bias sum_d q_d z_d of head r
+            uint32_t qt[D / 8];
+            float beta = 0.f;
+            {
+                const uint32_t *sl = ksz + c * (D / 8);
+                const uint32_t *zl = ksz + D / 2 + c * (D / 8);
+                uint32_t sw[D / 8];
+#pragma unroll
+                for (int e = 0; e < D / 8; ++e)
+                    sw[e] = sl[e];
+#pragma unroll
+                for (int pi = 0; pi < D / 8; ++pi) {
+                    const int lo = Cfg::FPW * (pi / Cfg::HALF) + pi % Cfg::HALF;
+                    const int hi = lo + Cfg::HALF;
+                    const uint32_t sp = __byte_perm(sw[lo >> 1], sw[hi >> 1],
+                                                    ((lo & 1) ? 0x0032 : 0x0010) |
+                                                        ((hi & 1) ? 0x7600 : 0x5400));
+                    qt[pi] = hmul2_u32(qpair[pi], sp);
+                }
+#pragma unroll
+                for (int e = 0; e < D / 8; ++e) {
+                    const uint32_t zw = zl[e];
+                    const float2 zf = __half22float2(*reinterpret_cast<const __half2 *>(&zw));
+                    const float2 qf2 = __half22float2(*reinterpret_cast<const __half2 *>(&qh[e]));
+                    beta = fmaf(qf2.x, zf.x, beta);
+                    beta = fmaf(qf2.y, zf.y, beta);
+                }
+                beta += __shfl_xor_sync(0xffffffffu, beta, 1);
+                beta += __shfl_xor_sync(0xffffffffu, beta, 2);
+            }
+            const float bias0 = __shfl_sync(0xffffffffu, beta, 4 * h0) * p.scale_log2;
+            const float bias1 = __shfl_sync(0xffffffffu, beta, 4 * h1) * p.scale_log2;
+            const float sk = TWO24 * p.scale_log2;
+
+            // ---- S^T = C_K Q~^T for both 16-token row blocks of the group
+            float sa0[4] = {0.f, 0.f, 0.f, 0.f}, sa1[4] = {0.f, 0.f, 0.f, 0.f};
+            {
                 const uint32_t *kw = reinterpret_cast<const uint32_t *>(kblk);
-                const uint32_t *vw = reinterpret_cast<const uint32_t *>(vblk);
+                uint32_t w0[Cfg::WPL], w1[Cfg::WPL], w2[Cfg::WPL], w3[Cfg::WPL];
 #pragma unroll
-                for (int rb = 0; rb < 2; ++rb) {
-                    // ---- S^T = C_K Q~^T over tokens [16 rb, 16 rb + 16) of the group
-                    float sa[4] = {0.f, 0.f, 0.f, 0.f};
-                    {
-                        uint32_t wa[Cfg::WPL], wb[Cfg::WPL];
+                for (int k = 0; k < Cfg::WPL; ++k) {
+                    w0[k] = kw[(r)*Cfg::WK + c * Cfg::WPL + k];
+                    w1[k] = kw[(r + 8) * Cfg::WK + c * Cfg::WPL + k];
+                    w2[k] = kw[(r + 16) * Cfg::WK + c * Cfg::WPL + k];
+                    w3[k] = kw[(r + 24) * Cfg::WK + c * Cfg::WPL + k];
+                }
 #pragma unroll
-                        for (int k = 0; k < Cfg::WPL; ++k) {
-                            wa[k] = kw[(16 * rb + r) * Cfg::WK + c * Cfg::WPL + k];
-                            wb[k] = kw[(16 * rb + r + 8) * Cfg::WK + c * Cfg::WPL + k];
-                        }
+                for (int s = 0; s < D / 16; ++s) {
+                    const int pa = 2 * s, pb = 2 * s + 1;
+                    const int ka = pa / Cfg::HALF, kb2 = pb / Cfg::HALF;
+                    const int ja = pa % Cfg::HALF, jb = pb % Cfg::HALF;
+                    mma16816(sa0, code_pair<BITS>(w0[ka], w0[ka] >> 8, ja),
+                             code_pair<BITS>(w1[ka], w1[ka] >> 8, ja),
+                             code_pair<BITS>(w0[kb2], w0[kb2] >> 8, jb),
+                             code_pair<BITS>(w1[kb2], w1[kb2] >> 8, jb), qt[pa], qt[pb]);
+                    mma16816(sa1, code_pair<BITS>(w2[ka], w2[ka] >> 8, ja),
+                             code_pair<BITS>(w3[ka], w3[ka] >> 8, ja),
+                             code_pair<BITS>(w2[kb2], w2[kb2] >> 8, jb),
+                             code_pair<BITS>(w3[kb2], w3[kb2] >> 8, jb), qt[pa], qt[pb]);
+                }
+            }
+            // scores of heads 2c (xa) and 2c+1 (xb) at tokens r, r+8, 16+r, 24+r
+            float xa[4] = {fmaf(sa0[0], sk, bias0), fmaf(sa0[2], sk, bias0),
+                           fmaf(sa1[0], sk, bias0), fmaf(sa1[2], sk, bias0)};
+            float xb[4] = {fmaf(sa0[1], sk, bias1), fmaf(sa0[3], sk, bias1),
+                           fmaf(sa1[1], sk, bias1), fmaf(sa1[3], sk, bias1)};
+            softmax_update(xa, xb, 4);
+
+            const uint32_t *vw = reinterpret_cast<const uint32_t *>(vblk);
 #pragma unroll
-                        for (int s = 0; s < D / 16; ++s) {
-                            const int pa = 2 * s, pb = 2 * s + 1;
-                            const int ka = pa / Cfg::HALF, kb2 = pb / Cfg::HALF;
-                            const uint32_t a0 = code_pair<BITS>(wa[ka], wa[ka] >> 8, pa % Cfg::HALF);
-                            const uint32_t a1 = code_pair<BITS>(wb[ka], wb[ka] >> 8, pa % Cfg::HALF);
-                            const uint32_t a2 = code_pair<BITS>(wa[kb2], wa[kb2] >> 8, pb % Cfg::HALF);
-                            const uint32_t a3 = code_pair<BITS>(wb[kb2], wb[kb2] >> 8, pb % Cfg::HALF);
-                            mma16816(sa, a0, a1, a2, a3, qt[pa], qt[pb]);
-                        }
-                    }
-                    float p0, p1, p2, p3;
-                    softmax16(fmaf(sa[0], sk, bias0), fmaf(sa[1], sk, bias1),
-                              fmaf(sa[2], sk, bias0), fmaf(sa[3], sk, bias1), p0, p1, p2, p3);
-                    // P^T fragments: pb0 = p[tokens 2c, 2c+1][head r], pb1 = tokens 2c+8, 2c+9
-                    const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
-                    const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
-                    const int t0 = 16 * rb + 2 * c;
-                    // ---- zero term Z[group][head] += sum_t z_t p_t (A rows = channel groups)
-                    {
-                        const bool zr = r < Cfg::NG;
-                        const uint32_t *zz = reinterpret_cast<const uint32_t *>(vsz + Cfg::NG * Cfg::G);
-                        const uint32_t za0 = zr ? zz[(r * Cfg::G + t0) >> 1] : 0u;
-                        const uint32_t za2 = zr ? zz[(r * Cfg::G + t0 + 8) >> 1] : 0u;
-                        float zc[4] = {zacc[0], zacc[1], zacc[2], zacc[3]};
-                        mma16816(zc, za0, 0u, za2, 0u, pb0, pb1);
-                        zacc[0] = zc[0];
-                        zacc[1] = zc[1];
-                    }
-                    // ---- O^T += C_V^T P~^T, m-tile m in channel group m/2
-                    uint32_t ptb0[Cfg::NG], ptb1[Cfg::NG];
-                    {
-                        const uint32_t *ss = reinterpret_cast<const uint32_t *>(vsz);
+            for (int rb = 0; rb < 2; ++rb) {
+                // P^T fragments: pb0 = p[tokens 2c, 2c+1][head r], pb1 = tokens 2c+8, 2c+9
+                const uint32_t pb0 = movmatrix_t(pack_half2(xa[2 * rb], xb[2 * rb]));
+                const uint32_t pb1 = movmatrix_t(pack_half2(xa[2 * rb + 1], xb[2 * rb + 1]));
+                const int t0 = 16 * rb + 2 * c;
+                // zero term Z[group][head] += sum_t z_t p_t (A rows = channel groups)
+                {
+                    const bool zr = r < Cfg::NG;
+                    const uint32_t za0 = zr ? vzz[(r * Cfg::G + t0) >> 1] : 0u;
+                    const uint32_t za2 = zr ? vzz[(r * Cfg::G + t0 + 8) >> 1] : 0u;
+                    float zc[4] = {zacc[0], zacc[1], 0.f, 0.f};
+                    mma16816(zc, za0, 0u, za2, 0u, pb0, pb1);
+                    zacc[0] = zc[0];
+                    zacc[1] = zc[1];
+                }
+                // p~ = p * s_V per channel group (B operands)
+                uint32_t ptb0[Cfg::NG], ptb1[Cfg::NG];
 #pragma unroll
-                        for (int gd = 0; gd < Cfg::NG; ++gd) {
-                            ptb0[gd] = hmul2_u32(pb0, ss[(gd * Cfg::G + t0) >> 1]);
-                            ptb1[gd] = hmul2_u32(pb1, ss[(gd * Cfg::G + t0 + 8) >> 1]);
-                        }
-                    }
-                    {
-                        const int pc = 8 * rb + c;   // token pair (2c, 2c+1) of the row block
-                        uint32_t wa[Cfg::W], wb[Cfg::W];
+                for (int gd = 0; gd < Cfg::NG; ++gd) {
+                    ptb0[gd] = hmul2_u32(pb0, vss[(gd * Cfg::G + t0) >> 1]);
+                    ptb1[gd] = hmul2_u32(pb1, vss[(gd * Cfg::G + t0 + 8) >> 1]);
+                }
+                // O^T += C_V^T P~^T, m-tile m in channel group m/2; pair chunks are
+                // stored rotated by twice the pair index
+                const int pc = 8 * rb + c, pd = pc + 4;
+                uint32_t wa[Cfg::W], wb[Cfg::W];
 #pragma unroll
-                        for (int k = 0; k < Cfg::W; ++k) {
-                            wa[k] = vw[pc * 2 * Cfg::WK + r * Cfg::W + k];
-                            wb[k] = vw[(pc + 4) * 2 * Cfg::WK + r * Cfg::W + k];
-                        }
+                for (int k = 0; k < Cfg::W; ++k) {
+                    wa[k] = vw[pc * 2 * Cfg::WK + ((r + 2 * pc) & 7) * Cfg::W + k];
+                    wb[k] = vw[pd * 2 * Cfg::WK + ((r + 2 * pd) & 7) * Cfg::W + k];
+                }
 #pragma unroll
-                        for (int m = 0; m < D / 16; ++m) {
-                            const int k = m / Cfg::MPW, jj = m % Cfg::MPW;
-                            const uint32_t a0 = code_pair<BITS>(wa[k], wa[k] >> 8, 2 * jj);
-                            const uint32_t a1 = code_pair<BITS>(wa[k], wa[k] >> 8, 2 * jj + 1);
-                            const uint32_t a2 = code_pair<BITS>(wb[k], wb[k] >> 8, 2 * jj);
-                            const uint32_t a3 = code_pair<BITS>(wb[k], wb[k] >> 8, 2 * jj + 1);
-                            mma16816(acc[m], a0, a1, a2, a3, ptb0[m / 2], ptb1[m / 2]);
-                        }
-                    }
+                for (int m = 0; m < D / 16; ++m) {
+                    const int k = m / Cfg::MPW, jj = m % Cfg::MPW;
+                    mma16816(acc[m], code_pair<BITS>(wa[k], wa[k] >> 8, 2 * jj),
+                             code_pair<BITS>(wa[k], wa[k] >> 8, 2 * jj + 1),
+                             code_pair<BITS>(wb[k], wb[k] >> 8, 2 * jj),
+                             code_pair<BITS>(wb[k], wb[k] >> 8, 2 * jj + 1), ptb0[m / 2],
+                             ptb1[m / 2]);
                 }
             }
         }

@@ -357,9 +357,9 @@ ORC_API void orc_kivi_quantize_unit(int D, int G, int bits, long n_q, const uint
  *   holds channel d = (32/bits)*w + i.
  * V block (bytes): [G/2 token pairs x 2*WK u32 words][G tokens x (D/G scales,
  *   D/G zeros) f16].  Pair i holds tokens 2i (low 16 bits of every word) and
- *   2i+1 (high 16 bits).  Word index r*W + k (r in [0,8), k in [0,W),
- *   W = D*bits/128); field j (bits [bits*j, bits*(j+1)) of each 16-bit half)
- *   holds channel d = 16*(k*(8/bits) + j/2) + 8*(j%2) + r.  Then the V scales
+ *   2i+1 (high 16 bits).  Word index ((r + 2i) mod 8)*W + k (r in [0,8),
+ *   k in [0,W), W = D*bits/128); field j (bits [bits*j, bits*(j+1)) of each
+ *   16-bit half) holds channel d = 16*(k*(8/bits) + j/2) + 8*(j%2) + r.  Then the V scales
  *   as D/G rows of G values (row j: channel group j of tokens 0..G-1), then the
  *   V zeros in the same order.
  */
@@ -395,7 +395,7 @@ ORC_API void orc_kivi_pack_group(int D, int G, int bits, const uint8_t *k_codes,
                     word |= (uint32_t)v_codes[(2 * i) * D + d] << (bits * j);
                     word |= (uint32_t)v_codes[(2 * i + 1) * D + d] << (16 + bits * j);
                 }
-                vw[(size_t)i * (2 * WK) + r * W + k] = word;
+                vw[(size_t)i * (2 * WK) + ((r + 2 * i) % 8) * W + k] = word;
             }
     uint16_t *vs = (uint16_t *)(v_block + (size_t)(G / 2) * (2 * WK) * 4);
     int ng = D / G;

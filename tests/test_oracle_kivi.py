@@ -155,7 +155,7 @@ def _unpack_from_spec(kb, vb, D, bits):
     for i in range(G // 2):
         for r in range(8):
             for k in range(W):
-                word = int(vw[i, r, k])
+                word = int(vw[i, (r + 2 * i) % 8, k])
                 for j in range(16 // bits):
                     d = 16 * (k * (8 // bits) + j // 2) + 8 * (j % 2) + r
                     assert vc[2 * i, d] == 255 and vc[2 * i + 1, d] == 255
