@@ -2,7 +2,8 @@
 // Cache Compression" guide, §16 "4 种方法逐步执行": the decode read dequantises
 // the old cache or uses a quantised kernel; the newest tokens stay in fp16).
 //
-// One CTA per (sequence, KV head, split).  A producer lane streams tiles into a
+// Work items are (sequence, KV head, split); persistent CTAs take them
+// round-robin.  A producer lane streams the tiles of all its items into one
 // shared-memory ring: quantised tiles of four 32-token groups (1-D bulk copies
 // of the packed K and V group blocks) and, in the unit's last split, residual
 // tiles of 32 fp16 ring slots (2-D TMA, 128-byte swizzle).  Four consumer
@@ -59,13 +60,14 @@ template <int D, int BITS> struct KiviCfg {
     static constexpr int STAGE_BYTES =
         ((QT_BYTES > RT_BYTES ? QT_BYTES : RT_BYTES) + 1023) / 1024 * 1024;
     static constexpr int NSTAGE = (81920 / STAGE_BYTES) < 3 ? 3 : (81920 / STAGE_BYTES);
-    static constexpr int SMEM = NSTAGE * STAGE_BYTES + 1024 + 2 * NSTAGE * 8;
-    static_assert(NCW * (8 * D + 16) * 4 <= NSTAGE * STAGE_BYTES, "combine scratch must fit");
+    static constexpr int RED_STRIDE = D + 4;   // padded per-head row of the merge scratch
+    static constexpr int RED_BYTES = (NCW - 1) * 8 * (RED_STRIDE + 2) * 4;
+    static constexpr int SMEM = NSTAGE * STAGE_BYTES + RED_BYTES + 2 * NSTAGE * 8 + 1024;
 };
 
 struct KiviParams {
     int Hq, Hkv, g, Cq, R, CR;
-    int splits, qtiles_per_split;
+    int splits, qtiles_per_split, n_items;
     const uint16_t *q;
     uint16_t *o;
     float *lse;
@@ -104,6 +106,38 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
+struct KiviItem {
+    int unit, split, b, hk, T, n_groups, n_res, qt0, nq, nr;
+};
+
+template <int D, int BITS>
+__device__ __forceinline__ KiviItem kivi_item(const KiviParams &p, int item)
+{
+    using Cfg = KiviCfg<D, BITS>;
+    KiviItem w;
+    w.unit = item / p.splits;
+    w.split = item % p.splits;
+    w.b = w.unit / p.Hkv;
+    w.hk = w.unit % p.Hkv;
+    w.T = p.len[w.b];
+    const int over = w.T - p.R;
+    w.n_groups = over > 0 ? over / Cfg::G : 0;
+    if (w.n_groups * Cfg::G > p.Cq) {
+        if (threadIdx.x == 0)
+            flag_error(p.status, DEV_CAPACITY);
+        w.n_groups = p.Cq / Cfg::G;
+    }
+    w.n_res = w.T - w.n_groups * Cfg::G;
+    const int unit_qtiles = (w.n_groups + Cfg::QG - 1) / Cfg::QG;
+    w.qt0 = w.split * p.qtiles_per_split;
+    const int qt1 = min(unit_qtiles, w.qt0 + p.qtiles_per_split);
+    w.nq = qt1 > w.qt0 ? qt1 - w.qt0 : 0;
+    w.nr = (w.split == p.splits - 1) ? (p.CR + Cfg::RS - 1) / Cfg::RS : 0;
+    return w;
+}
+
+// Persistent CTAs: CTA k handles work items k, k + gridDim.x, ... (an item is one
+// (sequence, KV head, split)); one TMA pipeline runs across all of its items.
 template <int D, int BITS>
 __global__ void __launch_bounds__(NTHREADS, 2)
     k_attend_kivi(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -113,32 +147,16 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES);
+    float *red = reinterpret_cast<float *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES +
+                                                  Cfg::RED_BYTES);
     uint64_t *empty = full + Cfg::NSTAGE;
+    __shared__ int s_abort;   // set when a wait ran out; every warp then stops
+    volatile int *abort = &s_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int unit = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
-    const int b = unit / p.Hkv, hk = unit % p.Hkv;
-
-    const int T = p.len[b];
-    const int over = T - p.R;
-    int n_groups = over > 0 ? over / Cfg::G : 0;
-    if (n_groups * Cfg::G > p.Cq) {
-        if (threadIdx.x == 0)
-            flag_error(p.status, DEV_CAPACITY);
-        n_groups = p.Cq / Cfg::G;
-    }
-    const int n_res = T - n_groups * Cfg::G;
-    const int unit_qtiles = (n_groups + Cfg::QG - 1) / Cfg::QG;
-    const int qt0 = split * p.qtiles_per_split;
-    const int qt1 = min(unit_qtiles, qt0 + p.qtiles_per_split);
-    const int nq = qt1 > qt0 ? qt1 - qt0 : 0;
-    const int nr = (split == p.splits - 1) ? (p.CR + Cfg::RS - 1) / Cfg::RS : 0;
-    const int ntiles = nr + nq;            // residual tiles first, then quantised tiles
-    const uint8_t *kblocks = p.kb + (size_t)unit * (p.Cq / Cfg::G) * Cfg::BLOCK;
-    const uint8_t *vblocks = p.vb + (size_t)unit * (p.Cq / Cfg::G) * Cfg::BLOCK;
-
     if (threadIdx.x == 0) {
+        s_abort = 0;
         for (int i = 0; i < Cfg::NSTAGE; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], NCW);
@@ -148,34 +166,40 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     __syncthreads();
 
     if (warp == NCW) {
-        if (lane == 0 && ntiles > 0) {
-            if (nr > 0) {
-                prefetch_tmap(&tmK);
-                prefetch_tmap(&tmV);
-            }
-            for (int i = 0; i < ntiles; ++i) {
-                const int st = i % Cfg::NSTAGE;
-                if (i >= Cfg::NSTAGE && !mbar_wait(&empty[st], ((i / Cfg::NSTAGE) & 1) ^ 1)) {
-                    flag_error(p.status, DEV_TIMEOUT);
-                    break;
-                }
-                uint8_t *dst = smem + st * Cfg::STAGE_BYTES;
-                if (i < nr) {
-                    mbar_arrive_expect_tx(&full[st], Cfg::RT_BYTES);
-                    const int row = unit * p.CR + i * Cfg::RS;
-#pragma unroll
-                    for (int j = 0; j < Cfg::NBOX; ++j) {
-                        tma_load_2d(dst + j * Cfg::RS * 128, &tmK, &full[st], 64 * j, row);
-                        tma_load_2d(dst + (Cfg::NBOX + j) * Cfg::RS * 128, &tmV, &full[st], 64 * j,
-                                    row);
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            int it = 0;
+            for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+                const KiviItem w = kivi_item<D, BITS>(p, item);
+                const uint8_t *kblocks = p.kb + (size_t)w.unit * (p.Cq / Cfg::G) * Cfg::BLOCK;
+                const uint8_t *vblocks = p.vb + (size_t)w.unit * (p.Cq / Cfg::G) * Cfg::BLOCK;
+                const int ntiles = w.nr + w.nq;   // residual tiles first, then quantised tiles
+                for (int i = 0; i < ntiles; ++i, ++it) {
+                    const int st = it % Cfg::NSTAGE;
+                    if (it >= Cfg::NSTAGE &&
+                        !mbar_wait_or_abort(&empty[st], ((it / Cfg::NSTAGE) & 1) ^ 1, abort)) {
+                        flag_error(p.status, DEV_TIMEOUT);
+                        return;
                     }
-                } else {
-                    const int g0 = (qt0 + i - nr) * Cfg::QG;
-                    const int ng = min(Cfg::QG, n_groups - g0);
-                    mbar_arrive_expect_tx(&full[st], 2 * ng * Cfg::BLOCK);
-                    bulk_load(dst, kblocks + (size_t)g0 * Cfg::BLOCK, ng * Cfg::BLOCK, &full[st]);
-                    bulk_load(dst + Cfg::QG * Cfg::BLOCK, vblocks + (size_t)g0 * Cfg::BLOCK,
-                              ng * Cfg::BLOCK, &full[st]);
+                    uint8_t *dst = smem + st * Cfg::STAGE_BYTES;
+                    if (i < w.nr) {
+                        mbar_arrive_expect_tx(&full[st], Cfg::RT_BYTES);
+                        const int row = w.unit * p.CR + i * Cfg::RS;
+#pragma unroll
+                        for (int j = 0; j < Cfg::NBOX; ++j) {
+                            tma_load_2d(dst + j * Cfg::RS * 128, &tmK, &full[st], 64 * j, row);
+                            tma_load_2d(dst + (Cfg::NBOX + j) * Cfg::RS * 128, &tmV, &full[st],
+                                        64 * j, row);
+                        }
+                    } else {
+                        const int g0 = (w.qt0 + i - w.nr) * Cfg::QG;
+                        const int ng = min(Cfg::QG, w.n_groups - g0);
+                        mbar_arrive_expect_tx(&full[st], 2 * ng * Cfg::BLOCK);
+                        bulk_load(dst, kblocks + (size_t)g0 * Cfg::BLOCK, ng * Cfg::BLOCK, &full[st]);
+                        bulk_load(dst + Cfg::QG * Cfg::BLOCK, vblocks + (size_t)g0 * Cfg::BLOCK,
+                                  ng * Cfg::BLOCK, &full[st]);
+                    }
                 }
             }
         }
@@ -185,8 +209,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const int r = lane >> 2, c = lane & 3, mi = lane >> 3, ri = lane & 7;
     const int h0 = 2 * c, h1 = 2 * c + 1;
     const bool hv = r < p.g;
-    const uint16_t *qrow = p.q + ((size_t)b * p.Hq + hk * p.g + (hv ? r : 0)) * D;
+    int it = 0;
 
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+    const KiviItem wi = kivi_item<D, BITS>(p, item);
+    const int b = wi.b, hk = wi.hk, T = wi.T, n_groups = wi.n_groups, n_res = wi.n_res;
+    const int qt0 = wi.qt0, nr = wi.nr, ntiles = wi.nr + wi.nq;
+    const uint16_t *qrow = p.q + ((size_t)b * p.Hq + hk * p.g + (hv ? r : 0)) * D;
     float acc[D / 16][4];
 #pragma unroll
     for (int m = 0; m < D / 16; ++m)
@@ -252,11 +281,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 qf[s][1] = hv ? q32[8 * s + c + 4] : 0u;
             }
         }
-        for (; i < nr; ++i) {
-            const int st = i % Cfg::NSTAGE;
-            if (!mbar_wait(&full[st], (i / Cfg::NSTAGE) & 1)) {
+        for (; i < nr; ++i, ++it) {
+            const int st = it % Cfg::NSTAGE;
+            if (!mbar_wait_or_abort(&full[st], (it / Cfg::NSTAGE) & 1, abort)) {
                 flag_error(p.status, DEV_TIMEOUT);
-                i = ntiles;
+                i = ntiles + 1;
                 break;
             }
             // warps 0, 1 take 16 ring slots each
@@ -318,9 +347,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         }
     }
     bool code_units = false;   // acc scaled to the quantised tiles' units
-    for (; i < ntiles; ++i) {
-        const int st = i % Cfg::NSTAGE;
-        if (!mbar_wait(&full[st], (i / Cfg::NSTAGE) & 1)) {
+    for (; i < ntiles; ++i, ++it) {
+        const int st = it % Cfg::NSTAGE;
+        if (!mbar_wait_or_abort(&full[st], (it / Cfg::NSTAGE) & 1, abort)) {
             flag_error(p.status, DEV_TIMEOUT);
             break;
         }
@@ -480,79 +509,122 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     for (int gd = 0; gd < Cfg::NG; ++gd) {
         const float z0 = __shfl_sync(0xffffffffu, zacc[0], 4 * gd + c);
         const float z1 = __shfl_sync(0xffffffffu, zacc[1], 4 * gd + c);
-        acc[2 * gd][0] += z0;
-        acc[2 * gd][1] += z1;
-        acc[2 * gd][2] += z0;
-        acc[2 * gd][3] += z1;
-        acc[2 * gd + 1][0] += z0;
-        acc[2 * gd + 1][1] += z1;
-        acc[2 * gd + 1][2] += z0;
-        acc[2 * gd + 1][3] += z1;
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) {
+            acc[2 * gd + mm][0] += z0;
+            acc[2 * gd + mm][1] += z1;
+            acc[2 * gd + mm][2] += z0;
+            acc[2 * gd + mm][3] += z1;
+        }
     }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, off);
         l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, off);
     }
-    consumer_bar();
-    float *redO = reinterpret_cast<float *>(smem);
-    float *redM = redO + NCW * 8 * D;
-    float *redL = redM + NCW * 8;
-    {
-        float *wo = redO + warp * 8 * D;
+    consumer_bar();   // warp 0 has finished reading the previous item's scratch
+    if (*abort)
+        break;        // every consumer warp sees the same flag after the barrier
+    constexpr int RS = Cfg::RED_STRIDE;
+    if (warp > 0) {
+        float *wo = red + (warp - 1) * 8 * (RS + 2);
 #pragma unroll
         for (int m = 0; m < D / 16; ++m) {
-            wo[h0 * D + 16 * m + r] = acc[m][0];
-            wo[h1 * D + 16 * m + r] = acc[m][1];
-            wo[h0 * D + 16 * m + r + 8] = acc[m][2];
-            wo[h1 * D + 16 * m + r + 8] = acc[m][3];
+            wo[h0 * RS + 16 * m + r] = acc[m][0];
+            wo[h1 * RS + 16 * m + r] = acc[m][1];
+            wo[h0 * RS + 16 * m + r + 8] = acc[m][2];
+            wo[h1 * RS + 16 * m + r + 8] = acc[m][3];
         }
         if (r == 0) {
-            redM[warp * 8 + h0] = m_run0;
-            redM[warp * 8 + h1] = m_run1;
-            redL[warp * 8 + h0] = l_run0;
-            redL[warp * 8 + h1] = l_run1;
+            wo[8 * RS + 2 * h0] = m_run0;
+            wo[8 * RS + 2 * h0 + 1] = l_run0;
+            wo[8 * RS + 2 * h1] = m_run1;
+            wo[8 * RS + 2 * h1 + 1] = l_run1;
         }
     }
     consumer_bar();
-    const bool single = p.part_o == nullptr;
-    for (int e = threadIdx.x; e < p.g * D; e += NCW * 32) {
-        const int h = e / D, d = e % D;
-        float ms = -INFINITY;
+    if (warp == 0) {
+        float ms0 = m_run0, ms1 = m_run1;
 #pragma unroll
-        for (int w = 0; w < NCW; ++w)
-            ms = fmaxf(ms, redM[w * 8 + h]);
-        float ls = 0.f, os = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) {
-            const float mw = redM[w * 8 + h];
-            const float sc = mw == -INFINITY ? 0.f : ex2(mw - ms);
-            ls += sc * redL[w * 8 + h];
-            os += sc * redO[(w * 8 + h) * D + d];
+        for (int v = 0; v < NCW - 1; ++v) {
+            const float *wo = red + v * 8 * (RS + 2) + 8 * RS;
+            ms0 = fmaxf(ms0, wo[2 * h0]);
+            ms1 = fmaxf(ms1, wo[2 * h1]);
         }
-        if (single) {
-            const size_t oi = ((size_t)b * p.Hq + hk * p.g + h) * D + d;
-            p.o[oi] = __half_as_ushort(__float2half_rn(ls > 0.f ? os / ls : 0.f));
-            if (d == 0 && p.lse)
-                p.lse[(size_t)b * p.Hq + hk * p.g + h] =
-                    ls > 0.f ? (ms + __log2f(ls)) * LN2 : -INFINITY;
-        } else {
-            const size_t pi = ((size_t)unit * p.splits + split) * p.g + h;
-            p.part_o[pi * D + d] = os;
-            if (d == 0) {
-                p.part_ml[2 * pi] = ls > 0.f ? ms : -INFINITY;
-                p.part_ml[2 * pi + 1] = ls;
+        float sc0[NCW], sc1[NCW];
+        sc0[0] = m_run0 == -INFINITY ? 0.f : ex2(m_run0 - ms0);
+        sc1[0] = m_run1 == -INFINITY ? 0.f : ex2(m_run1 - ms1);
+        float ls0 = sc0[0] * l_run0, ls1 = sc1[0] * l_run1;
+#pragma unroll
+        for (int v = 0; v < NCW - 1; ++v) {
+            const float *wo = red + v * 8 * (RS + 2) + 8 * RS;
+            const float mw0 = wo[2 * h0], mw1 = wo[2 * h1];
+            sc0[v + 1] = mw0 == -INFINITY ? 0.f : ex2(mw0 - ms0);
+            sc1[v + 1] = mw1 == -INFINITY ? 0.f : ex2(mw1 - ms1);
+            ls0 += sc0[v + 1] * wo[2 * h0 + 1];
+            ls1 += sc1[v + 1] * wo[2 * h1 + 1];
+        }
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) {
+            float o[4] = {acc[m][0] * sc0[0], acc[m][1] * sc1[0], acc[m][2] * sc0[0],
+                          acc[m][3] * sc1[0]};
+#pragma unroll
+            for (int v = 0; v < NCW - 1; ++v) {
+                const float *wo = red + v * 8 * (RS + 2);
+                o[0] += sc0[v + 1] * wo[h0 * RS + 16 * m + r];
+                o[1] += sc1[v + 1] * wo[h1 * RS + 16 * m + r];
+                o[2] += sc0[v + 1] * wo[h0 * RS + 16 * m + r + 8];
+                o[3] += sc1[v + 1] * wo[h1 * RS + 16 * m + r + 8];
+            }
+            acc[m][0] = o[0];
+            acc[m][1] = o[1];
+            acc[m][2] = o[2];
+            acc[m][3] = o[3];
+        }
+        const bool single = p.part_o == nullptr;
+        const int hs[2] = {h0, h1};
+        const float lss[2] = {ls0, ls1}, mss[2] = {ms0, ms1};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = hs[e];
+            if (h >= p.g)
+                continue;
+            if (single) {
+                const float inv = lss[e] > 0.f ? 1.f / lss[e] : 0.f;
+                uint16_t *orow = p.o + ((size_t)b * p.Hq + hk * p.g + h) * D;
+#pragma unroll
+                for (int m = 0; m < D / 16; ++m) {
+                    orow[16 * m + r] = __half_as_ushort(__float2half_rn(acc[m][e] * inv));
+                    orow[16 * m + r + 8] = __half_as_ushort(__float2half_rn(acc[m][2 + e] * inv));
+                }
+                if (r == 0 && p.lse)
+                    p.lse[(size_t)b * p.Hq + hk * p.g + h] =
+                        lss[e] > 0.f ? (mss[e] + __log2f(lss[e])) * LN2 : -INFINITY;
+            } else {
+                const size_t pi = ((size_t)wi.unit * p.splits + wi.split) * p.g + h;
+                float *po = p.part_o + pi * D;
+#pragma unroll
+                for (int m = 0; m < D / 16; ++m) {
+                    po[16 * m + r] = acc[m][e];
+                    po[16 * m + r + 8] = acc[m][2 + e];
+                }
+                if (r == 0) {
+                    p.part_ml[2 * pi] = lss[e] > 0.f ? mss[e] : -INFINITY;
+                    p.part_ml[2 * pi + 1] = lss[e];
+                }
             }
         }
     }
+    }   // items
 }
 
 template <int D, int BITS>
 cudaError_t launch_kivi_impl(const CUtensorMap &tk, const CUtensorMap &tv, const KiviParams &kp,
-                             int grid, cudaStream_t s)
+                             cudaStream_t s)
 {
     using Cfg = KiviCfg<D, BITS>;
     static int configured_device = -1;
+    static int resident = 1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
@@ -560,8 +632,17 @@ cudaError_t launch_kivi_impl(const CUtensorMap &tk, const CUtensorMap &tv, const
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
         if (e != cudaSuccess)
             return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attend_kivi<D, BITS>,
+                                                          NTHREADS, Cfg::SMEM);
+        if (e != cudaSuccess)
+            return e;
+        resident = (per_sm > 0 ? per_sm : 1) * sm_count();
         configured_device = dev;
     }
+    const int grid = kp.n_items < resident ? kp.n_items : resident;
+    if (grid <= 0)
+        return cudaSuccess;
     k_attend_kivi<D, BITS><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, kp);
     return cudaGetLastError();
 }
@@ -596,14 +677,14 @@ cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s)
     kp.scale = a.scale;
     kp.scale_log2 = a.scale * LOG2E;
     kp.status = dev_status_ptr();
-    const int grid = a.B * a.Hkv * a.splits;
+    kp.n_items = a.B * a.Hkv * a.splits;
     cudaError_t e;
     if (a.D == 128)
-        e = a.bits == 4 ? launch_kivi_impl<128, 4>(tk, tv, kp, grid, s)
-                        : launch_kivi_impl<128, 2>(tk, tv, kp, grid, s);
+        e = a.bits == 4 ? launch_kivi_impl<128, 4>(tk, tv, kp, s)
+                        : launch_kivi_impl<128, 2>(tk, tv, kp, s);
     else
-        e = a.bits == 4 ? launch_kivi_impl<64, 4>(tk, tv, kp, grid, s)
-                        : launch_kivi_impl<64, 2>(tk, tv, kp, grid, s);
+        e = a.bits == 4 ? launch_kivi_impl<64, 4>(tk, tv, kp, s)
+                        : launch_kivi_impl<64, 2>(tk, tv, kp, s);
     if (e != cudaSuccess || a.splits == 1)
         return e;
     return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);
