@@ -183,6 +183,10 @@ enum { KVC_KIND_SLOTS = 0, KVC_KIND_KIVI = 1 };
  *               (may be NULL when that size is 0)
  *   num_splits  KV splits per unit (0 = chosen from the SM count)
  *   softmax_scale 0 for 1/sqrt(D)
+ *   h2o_scores  optional [B, Hkv, C] fp32 (slot caches only; needs logits and
+ *               lse): the step's attention probabilities are added to the
+ *               heavy-hitter scores in the same launch, exactly as
+ *               kvc_h2o_accumulate(KVC_H2O_DECODE) would add them
  */
 typedef struct kvc_attend_args {
     int kind;
@@ -197,6 +201,7 @@ typedef struct kvc_attend_args {
     size_t workspace_bytes;
     int num_splits;
     float softmax_scale;
+    float *h2o_scores;
 } kvc_attend_args;
 
 /* Workspace bytes kvc_decode_attend needs for these arguments (0 if none). */

@@ -53,7 +53,7 @@ class AttendArgs(C.Structure):
                 ("slots", C.POINTER(SlotCacheDesc)), ("quant", C.POINTER(QuantCacheDesc)),
                 ("logits", C.c_void_p), ("lse", C.c_void_p), ("workspace", C.c_void_p),
                 ("workspace_bytes", C.c_size_t), ("num_splits", C.c_int),
-                ("softmax_scale", C.c_float)]
+                ("softmax_scale", C.c_float), ("h2o_scores", C.c_void_p)]
 
 
 class H2OArgs(C.Structure):
@@ -143,7 +143,8 @@ def kvc_append_quant(cache: "QuantCache", k_new, v_new, stream=None):
                                   _stream(stream)), "kvc_append_quant")
 
 
-def _attend_args(cache, q, o, logits=None, lse=None, workspace=None, num_splits=0, scale=0.0):
+def _attend_args(cache, q, o, logits=None, lse=None, workspace=None, num_splits=0, scale=0.0,
+                 h2o_scores=None):
     a = AttendArgs()
     keep = []
     if isinstance(cache, SlotCache):
@@ -163,6 +164,7 @@ def _attend_args(cache, q, o, logits=None, lse=None, workspace=None, num_splits=
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     a.num_splits = int(num_splits)
     a.softmax_scale = float(scale)
+    a.h2o_scores = _ptr(h2o_scores)
     return a, keep
 
 
@@ -172,8 +174,9 @@ def kvc_workspace_size(cache, q, num_splits: int = 0) -> int:
 
 
 def kvc_decode_attend(cache, q, o, logits=None, lse=None, workspace=None, num_splits: int = 0,
-                      softmax_scale: float = 0.0, stream=None):
-    a, _keep = _attend_args(cache, q, o, logits, lse, workspace, num_splits, softmax_scale)
+                      softmax_scale: float = 0.0, h2o_scores=None, stream=None):
+    a, _keep = _attend_args(cache, q, o, logits, lse, workspace, num_splits, softmax_scale,
+                            h2o_scores)
     _check(lib().kvc_decode_attend(C.byref(a), _stream(stream)), "kvc_decode_attend")
 
 

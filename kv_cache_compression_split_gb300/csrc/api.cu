@@ -265,8 +265,10 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         return f.st;
     if (!a->q || !a->o || !aligned16(a->q))
         return KVC_ERR_INVALID_ARG;
-    if (a->kind == KVC_KIND_KIVI && a->logits)
+    if (a->kind == KVC_KIND_KIVI && (a->logits || a->h2o_scores))
         return KVC_ERR_UNSUPPORTED;
+    if (a->h2o_scores && (!a->logits || !a->lse))
+        return KVC_ERR_INVALID_ARG;
     if (f.ws > 0 && (!a->workspace || a->workspace_bytes < f.ws || !aligned16(a->workspace)))
         return KVC_ERR_WORKSPACE;
     const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / sqrtf((float)f.D);
@@ -275,8 +277,24 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         const kvc_slot_cache &c = *a->slots;
         float *part_ml = part_o ? part_o + (size_t)f.B * a->Hq * f.plan.splits * f.D : nullptr;
         AttendLaunch L{f.B, a->Hq, c.Hkv, c.D, c.C, a->q, a->o, c.K, c.V, c.n, a->logits, a->lse,
-                       part_o, part_ml, f.plan.splits, f.plan.tiles_per_split, scale};
-        return from_cuda(launch_attend_slots(L, stream));
+                       part_o, part_ml, f.plan.splits, f.plan.tiles_per_split, scale,
+                       a->h2o_scores};
+        cudaError_t e = launch_attend_slots(L, stream);
+        if (e != cudaSuccess || !a->h2o_scores || f.plan.splits == 1)
+            return from_cuda(e);
+        // several splits: the probabilities need the combined lse first
+        kvc_h2o_args h{};
+        h.mode = KVC_H2O_DECODE;
+        h.B = f.B;
+        h.Hq = a->Hq;
+        h.Hkv = c.Hkv;
+        h.D = c.D;
+        h.C = c.C;
+        h.scores = a->h2o_scores;
+        h.logits = a->logits;
+        h.lse = a->lse;
+        h.n = c.n;
+        return from_cuda(launch_h2o_decode_acc(h, stream));
     }
     const kvc_quant_cache &c = *a->quant;
     float *part_ml = part_o ? part_o + (size_t)f.B * a->Hq * f.plan.splits * f.D : nullptr;

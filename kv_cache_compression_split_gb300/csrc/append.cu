@@ -54,6 +54,54 @@ __global__ void k_append_slots(int Hkv, int D, int C, int n_new, const uint4 *__
     }
 }
 
+// Short appends (a few tokens, the decode case): one CTA per sequence, one
+// warp per KV head; after a CTA barrier thread 0 bumps the sequence's counters,
+// so no second launch is needed.
+__global__ void k_append_small(int Hkv, int D, int C, int n_new, const uint4 *__restrict__ k_new,
+                               const uint4 *__restrict__ v_new, uint4 *__restrict__ K,
+                               uint4 *__restrict__ V, int32_t *__restrict__ pos,
+                               int32_t *__restrict__ n, int32_t *__restrict__ seqlen, int *status)
+{
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int T0 = seqlen[b];
+    const int cpt = D / 8;
+    __shared__ int s_bad;
+    if (threadIdx.x == 0)
+        s_bad = 0;
+    __syncthreads();
+    for (int hk = warp; hk < Hkv; hk += nw) {
+        const int unit = b * Hkv + hk;
+        const int n0 = n[unit];
+        if (n0 < 0 || n0 + n_new > C) {
+            if (lane == 0)
+                s_bad = 1;
+            continue;
+        }
+        for (int i = lane; i < 2 * n_new * cpt; i += 32) {
+            const int kv = i / (n_new * cpt), e = i % (n_new * cpt);
+            const int t = e / cpt, ch = e % cpt;
+            const size_t src = ((size_t)unit * n_new + t) * cpt + ch;
+            const size_t dst = ((size_t)unit * C + n0 + t) * cpt + ch;
+            if (kv == 0)
+                K[dst] = k_new[src];
+            else
+                V[dst] = v_new[src];
+        }
+        for (int t = lane; t < n_new; t += 32)
+            pos[(size_t)unit * C + n0 + t] = T0 + t;
+        __syncwarp();
+        if (lane == 0)
+            n[unit] = n0 + n_new;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        seqlen[b] = T0 + n_new;
+        if (s_bad)
+            flag_error(status, DEV_CAPACITY);
+    }
+}
+
 __global__ void k_append_bump(int B, int Hkv, int C, int n_new, int32_t *n, int32_t *seqlen)
 {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -282,6 +330,14 @@ cudaError_t launch_quant_impl(const kvc_quant_cache &c, const uint16_t *k_new,
 cudaError_t launch_append_slots(const kvc_slot_cache &c, const uint16_t *k_new,
                                 const uint16_t *v_new, int n_new, cudaStream_t s)
 {
+    if (n_new <= 8) {
+        const int warps = c.Hkv < 16 ? c.Hkv : 16;
+        k_append_small<<<c.B, 32 * warps, 0, s>>>(
+            c.Hkv, c.D, c.C, n_new, reinterpret_cast<const uint4 *>(k_new),
+            reinterpret_cast<const uint4 *>(v_new), reinterpret_cast<uint4 *>(c.K),
+            reinterpret_cast<uint4 *>(c.V), c.pos, c.n, c.seqlen, dev_status_ptr());
+        return cudaGetLastError();
+    }
     const int units = c.B * c.Hkv;
     const long chunks = (long)n_new * (c.D / 8);
     int gy = (int)((chunks + 255) / 256);

@@ -50,6 +50,7 @@ struct SlotParams {
     float *logits, *lse;
     float *part_o, *part_ml;
     float scale, scale_log2;
+    float *h2o_scores;              // optional: add this step's probabilities (one split)
     int *status;
 };
 
@@ -284,6 +285,56 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             }
         }
     }
+    if (single && p.h2o_scores) {
+        // H2O decode scores: score[j] += sum_h exp(logit_hj - lse_h) over this unit's
+        // query heads (logits written above by this CTA; log2 domain here)
+        __shared__ float s_lse2[8];
+        if (threadIdx.x < p.g) {
+            const int h = threadIdx.x;
+            float ms = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NCW; ++w)
+                ms = fmaxf(ms, redM[w * 8 + h]);
+            float ls = 0.f;
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) {
+                const float mw = redM[w * 8 + h];
+                ls += (mw == -INFINITY ? 0.f : ex2(mw - ms)) * redL[w * 8 + h];
+            }
+            s_lse2[h] = ls > 0.f ? ms + __log2f(ls) : INFINITY;
+        }
+        consumer_bar();
+        const float *lrow = p.logits + ((size_t)b * p.Hq + hk * p.g) * p.C;
+        float *sc = p.h2o_scores + (size_t)unit * p.C;
+        // four slots per thread per round, every load issued before any is used
+        constexpr int U = 4;
+        for (int j0 = threadIdx.x; j0 < t_end; j0 += U * NCW * 32) {
+            float add[U], old[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u * NCW * 32;
+                add[u] = 0.f;
+                old[u] = j < t_end ? sc[j] : 0.f;
+            }
+            for (int h = 0; h < p.g; ++h) {
+                float lg[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = j0 + u * NCW * 32;
+                    lg[u] = j < t_end ? lrow[(size_t)h * p.C + j] : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    add[u] += ex2(fmaf(lg[u], LOG2E, -s_lse2[h]));
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u * NCW * 32;
+                if (j < t_end)
+                    sc[j] = old[u] + add[u];
+            }
+        }
+    }
 }
 
 // Merge split partials: o = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s.
@@ -360,6 +411,7 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
     sp.part_ml = a.splits == 1 ? nullptr : a.part_ml;
     sp.scale = a.scale;
     sp.scale_log2 = a.scale * LOG2E;
+    sp.h2o_scores = a.splits == 1 ? a.h2o_scores : nullptr;
     sp.status = dev_status_ptr();
     const int grid = units * a.splits;
     cudaError_t e = a.D == 128 ? launch_slots_impl<128>(tk, tv, sp, grid, s)

@@ -1,6 +1,7 @@
 // evict.cu -- keep-set selection and in-place compaction of slot caches.
 //
-// One CTA per (sequence, KV head) unit:
+// One CTA per (sequence, KV head) unit (one warp per unit for caches of at
+// most 1024 slots, the decode-sized H2O and StreamingLLM caches):
 //   1. decide the keep set
 //        H2O    ("Rethinking KV Cache Compression" guide, §2 and §16 "4 种方法
 //               逐步执行"): the recent window pos >= T - n_recent, plus the
@@ -338,6 +339,171 @@ __global__ void __launch_bounds__(ETHREADS) k_evict(const EvictParams p)
         p.n[unit] = n_new;
 }
 
+// ------------------------------------------------------------------------
+// Decode-sized caches (C <= WE_MAX_SLOTS): one warp per unit, warp-level
+// primitives only (no CTA barriers), so every unit of the batch is resident at
+// once.  Same keep rules and the same fill-the-holes-from-the-tail compaction.
+// ------------------------------------------------------------------------
+constexpr int WE_WARPS = 8;
+constexpr int WE_MAX_SLOTS = 1024;
+
+template <typename KeyFn, typename FiltFn>
+__device__ uint64_t warp_radix_select(int n, int k, KeyFn key, FiltFn filt, uint32_t *hist)
+{
+    const int lane = threadIdx.x & 31;
+    uint64_t prefix = 0, mask = 0;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            hist[8 * lane + i] = 0;
+        __syncwarp();
+        for (int base = 0; base < n; base += 32) {
+            const int j = base + lane;
+            if (j < n && filt(j)) {
+                const uint64_t kk = key(j);
+                if ((kk & mask) == prefix)
+                    atomicAdd(&hist[(kk >> shift) & 255u], 1u);
+            }
+        }
+        __syncwarp();
+        int s = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            s += (int)hist[8 * lane + i];
+        int incl = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off)
+                incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= k);
+        const int src = hit ? __ffs(hit) - 1 : 31;
+        int digit = 0, left = 0;
+        if (lane == src) {
+            int cum = incl - s;
+            digit = 8 * lane + 7;
+            for (int i = 0; i < 8; ++i) {
+                const int h = (int)hist[8 * lane + i];
+                if (cum + h >= k) {
+                    digit = 8 * lane + i;
+                    break;
+                }
+                cum += h;
+            }
+            left = k - cum;
+        }
+        digit = __shfl_sync(0xffffffffu, digit, src);
+        k = __shfl_sync(0xffffffffu, left, src);
+        prefix |= (uint64_t)digit << shift;
+        mask |= (uint64_t)0xff << shift;
+        __syncwarp();
+    }
+    return prefix;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams p, int n_units)
+{
+    __shared__ uint32_t s_keep[WE_WARPS][WE_MAX_SLOTS / 32];
+    __shared__ uint32_t s_hist[WE_WARPS][256];
+    __shared__ uint16_t s_hole[WE_WARPS][WE_MAX_SLOTS / 2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int unit = blockIdx.x * WE_WARPS + warp;
+    if (unit >= n_units)
+        return;
+    const int n = p.n[unit];
+    if (n > p.C || n < 0) {
+        if (lane == 0)
+            flag_error(p.status, DEV_CAPACITY);
+        return;
+    }
+    const long T = p.seqlen[unit / p.Hkv];
+    const int32_t *pos = p.pos + (size_t)unit * p.C;
+    float *sc = p.scores ? p.scores + (size_t)unit * p.C : nullptr;
+    uint32_t *keep = s_keep[warp];
+    const long rt = T - p.n_recent;
+    int n_new = 0;
+
+    if (KIND == EVICT_STREAM) {
+        for (int base = 0; base < n; base += 32) {
+            const int j = base + lane;
+            const bool k = j < n && ((long)pos[j] < p.n_sink || (long)pos[j] >= rt);
+            const unsigned m = __ballot_sync(0xffffffffu, k);
+            if (lane == 0)
+                keep[base >> 5] = m;
+            n_new += __popc(m);
+        }
+        if (n_new == n)
+            return;
+    } else {
+        int n_rec = 0;
+        for (int base = 0; base < n; base += 32) {
+            const int j = base + lane;
+            const unsigned m = __ballot_sync(0xffffffffu, j < n && (long)pos[j] >= rt);
+            if (lane == 0)
+                keep[base >> 5] = m;
+            n_rec += __popc(m);
+        }
+        const int take = min(p.n_heavy, n - n_rec);
+        if (take >= n - n_rec)
+            return;   // nothing to drop
+        n_new = n_rec + take;
+        if (take > 0) {
+            auto key = [&](int j) { return ((uint64_t)desc_bits(sc[j]) << 32) | (uint32_t)pos[j]; };
+            auto cand = [&](int j) { return (long)pos[j] < rt; };
+            const uint64_t kth = warp_radix_select(n, take, key, cand, s_hist[warp]);
+            for (int base = 0; base < n; base += 32) {
+                const int j = base + lane;
+                const unsigned m = __ballot_sync(0xffffffffu, j < n && cand(j) && key(j) <= kth);
+                if (lane == 0)
+                    keep[base >> 5] |= m;
+            }
+        }
+    }
+    __syncwarp();
+
+    // holes of [0, n_new) by rank
+    int nh = 0;
+    for (int base = 0; base < n_new; base += 32) {
+        const int j = base + lane;
+        const bool h = j < n_new && !((keep[base >> 5] >> lane) & 1u);
+        const unsigned m = __ballot_sync(0xffffffffu, h);
+        if (h)
+            s_hole[warp][nh + __popc(m & ((1u << lane) - 1u))] = (uint16_t)j;
+        nh += __popc(m);
+    }
+    __syncwarp();
+    // kept slots of [n_new, n) fill the holes in order; the warp moves one row at a time
+    const int chunks = p.D / 8;
+    uint4 *K4 = reinterpret_cast<uint4 *>(p.K), *V4 = reinterpret_cast<uint4 *>(p.V);
+    int done = 0;
+    for (int base = n_new; base < n; base += 32) {
+        const int j = base + lane;
+        const bool t = j < n && ((keep[j >> 5] >> (j & 31)) & 1u);
+        unsigned m = __ballot_sync(0xffffffffu, t);
+        while (m) {
+            const int l = __ffs(m) - 1;
+            m &= m - 1;
+            const size_t src = (size_t)unit * p.C + base + l;
+            const size_t dst = (size_t)unit * p.C + s_hole[warp][done++];
+            for (int ch = lane; ch < 2 * chunks; ch += 32) {
+                if (ch < chunks)
+                    K4[dst * chunks + ch] = K4[src * chunks + ch];
+                else
+                    V4[dst * chunks + ch - chunks] = V4[src * chunks + ch - chunks];
+            }
+            if (lane == 0) {
+                p.pos[dst] = p.pos[src];
+                if (sc)
+                    p.scores[dst] = p.scores[src];
+            }
+        }
+    }
+    if (lane == 0)
+        p.n[unit] = n_new;
+}
+
 } // namespace
 
 cudaError_t launch_evict(const EvictLaunch &e, cudaStream_t s)
@@ -361,16 +527,24 @@ cudaError_t launch_evict(const EvictLaunch &e, cudaStream_t s)
     p.seed_hi = (uint32_t)(e.seed >> 32);
     p.epoch = e.epoch;
     p.status = dev_status_ptr();
-    const int grid = e.c.B * e.c.Hkv;
+    const int units = e.c.B * e.c.Hkv;
+    const bool small = e.c.C <= WE_MAX_SLOTS;
+    const int wgrid = (units + WE_WARPS - 1) / WE_WARPS;
     switch (e.kind) {
     case EVICT_H2O:
-        k_evict<EVICT_H2O><<<grid, ETHREADS, 0, s>>>(p);
+        if (small)
+            k_evict_warp<EVICT_H2O><<<wgrid, WE_WARPS * 32, 0, s>>>(p, units);
+        else
+            k_evict<EVICT_H2O><<<units, ETHREADS, 0, s>>>(p);
         break;
     case EVICT_STREAM:
-        k_evict<EVICT_STREAM><<<grid, ETHREADS, 0, s>>>(p);
+        if (small)
+            k_evict_warp<EVICT_STREAM><<<wgrid, WE_WARPS * 32, 0, s>>>(p, units);
+        else
+            k_evict<EVICT_STREAM><<<units, ETHREADS, 0, s>>>(p);
         break;
     default:
-        k_evict<EVICT_RANDOM><<<grid, ETHREADS, 0, s>>>(p);
+        k_evict<EVICT_RANDOM><<<units, ETHREADS, 0, s>>>(p);
         break;
     }
     return cudaGetLastError();

@@ -43,6 +43,7 @@ struct AttendLaunch {
     float *part_o, *part_ml;
     int splits, tiles_per_split;
     float scale;
+    float *h2o_scores;
 };
 cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s);
 

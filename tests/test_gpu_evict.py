@@ -103,7 +103,7 @@ def _check_keep_with_ties(keep_gpu_pos, pos, score_ref, T, n_heavy, n_recent):
 
 @pytest.mark.parametrize("B,Hq,Hkv,L,D,n_heavy,n_recent", [
     (1, 4, 4, 64, 64, 8, 8), (2, 8, 2, 300, 128, 16, 40), (1, 16, 2, 1000, 128, 64, 448),
-    (2, 4, 4, 130, 64, 200, 8)])
+    (2, 4, 4, 130, 64, 200, 8), (1, 8, 1, 1500, 128, 64, 448)])
 def test_h2o_prefill_scores_and_evict(kvc, orc, B, Hq, Hkv, L, D, n_heavy, n_recent):
     g = torch.Generator().manual_seed(L + Hq)
     C = L + 4
@@ -132,8 +132,11 @@ def test_h2o_prefill_scores_and_evict(kvc, orc, B, Hq, Hkv, L, D, n_heavy, n_rec
     assert device_status_clean(kvc)
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,D", [(4, 64, 8, 128), (3, 8, 8, 64)])
-def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D):
+@pytest.mark.parametrize("B,Hq,Hkv,D,fused,splits", [(4, 64, 8, 128, False, 0),
+                                                     (3, 8, 8, 64, False, 0),
+                                                     (4, 64, 8, 128, True, 1),
+                                                     (3, 8, 8, 64, True, 3)])
+def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, fused, splits):
     """One decode step from a seeded post-prefill state: 64 heavy slots from [0, 1600) plus the
     recent 448; append token 2048, attend over 513 slots, accumulate, evict back to 512."""
     T, n_heavy, n_recent = 2048, 64, 448
@@ -165,10 +168,15 @@ def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D):
     o = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
     logits = torch.empty(B, Hq, C, dtype=torch.float32, device="cuda")
     lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
-    ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), dtype=torch.float32,
+    ws = torch.empty(max(kvc.kvc_workspace_size(cache, q, splits) // 4, 1), dtype=torch.float32,
                      device="cuda")
-    kvc.kvc_decode_attend(cache, q.cuda(), o, logits=logits, lse=lse, workspace=ws)
-    kvc.kvc_h2o_accumulate_decode(cache, scores, logits, lse, Hq)
+    if fused:   # probabilities added to the scores by the attention launch itself
+        kvc.kvc_decode_attend(cache, q.cuda(), o, logits=logits, lse=lse, workspace=ws,
+                              num_splits=splits, h2o_scores=scores)
+    else:
+        kvc.kvc_decode_attend(cache, q.cuda(), o, logits=logits, lse=lse, workspace=ws,
+                              num_splits=splits)
+        kvc.kvc_h2o_accumulate_decode(cache, scores, logits, lse, Hq)
     scores_after_acc = scores.clone()
     kvc.kvc_h2o_evict(cache, scores, n_heavy, n_recent)
     torch.cuda.synchronize()
