@@ -205,6 +205,7 @@ def run_gpu(args, rank, world):
         kn = torch.randn(S_total, 4, B, Hkv, 1, D, generator=gq, device=dev).half()
         vn = torch.randn(S_total, 4, B, Hkv, 1, D, generator=gq, device=dev).half()
         outs = torch.empty(4, B, Hq, D, dtype=torch.float16, device=dev)
+        outs_base = outs
         logits = torch.empty(B, Hq, Ch, dtype=torch.float32, device=dev)
         lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
 
@@ -227,15 +228,13 @@ def run_gpu(args, rank, world):
              "h2o_evict", "kivi4_append", "kivi4_attend", "stream_append", "stream_attend",
              "stream_evict"]
 
-    def step(i, ev=None, host=None):
-        """One decode step of all four methods; ev: per-call events; host: pinned inputs."""
+    def step(i, ev=None, outs_override=None):
+        """One decode step of all four methods on the launch stream; ev: per-call events."""
+        outs = outs_base if outs_override is None else outs_override
+
         def mark(k):
             if ev is not None:
                 ev[k].record(stream)
-        if host is not None:
-            qs[i].copy_(host["q"], non_blocking=True)
-            kn[i].copy_(host["k"], non_blocking=True)
-            vn[i].copy_(host["v"], non_blocking=True)
         mark(0)
         kvc.kvc_append(fp, kn[i, 0], vn[i, 0], stream=stream); mark(1)
         kvc.kvc_decode_attend(fp, qs[i, 0], outs[0], workspace=ws_fp, stream=stream); mark(2)
@@ -250,8 +249,6 @@ def run_gpu(args, rank, world):
         kvc.kvc_append(st, kn[i, 3], vn[i, 3], stream=stream); mark(9)
         kvc.kvc_decode_attend(st, qs[i, 3], outs[3], workspace=ws_st, stream=stream); mark(10)
         kvc.kvc_stream_evict(st, n_sink, n_recent, stream=stream); mark(11)
-        if host is not None:
-            host["o"].copy_(outs, non_blocking=True)
 
     def barrier():
         if world > 1:
@@ -319,33 +316,66 @@ def run_gpu(args, rank, world):
         v["speedup_vs_fp16"] = methods["fp16"]["ms_per_step"] / v["ms_per_step"]
     calls = {nm: sum(v) / len(v) for nm, v in per_call.items() if nm != "h2o_unused"}
 
-    # ---------------- end to end: host buffers, copies inside the timed region
-    with torch.cuda.stream(stream):
-        host = {"q": torch.empty(4, B, Hq, D, dtype=torch.float16).pin_memory(),
+    # ---------------- end to end: host buffers, copies inside the timed region.
+    # Every step uploads its own queries and new K/V from pinned host memory and
+    # reads its four outputs back; uploads of step k+1 run on a copy stream while
+    # step k computes, and outputs alternate between two device buffers.
+    n_e2e = max(3, min(args.steps, 8))
+    base = S_total - n_e2e
+    host_in = [{"q": torch.empty(4, B, Hq, D, dtype=torch.float16).pin_memory(),
                 "k": torch.empty(4, B, Hkv, 1, D, dtype=torch.float16).pin_memory(),
-                "v": torch.empty(4, B, Hkv, 1, D, dtype=torch.float16).pin_memory(),
-                "o": torch.empty(4, B, Hq, D, dtype=torch.float16).pin_memory()}
-        host["q"].copy_(qs[0].cpu())
-        host["k"].copy_(kn[0].cpu())
-        host["v"].copy_(vn[0].cpu())
-        n_e2e = max(3, min(args.steps, 8))
-        # the caches keep growing: reuse the last warmup slots' inputs to stay in capacity
-        base = S_total - n_e2e
+                "v": torch.empty(4, B, Hkv, 1, D, dtype=torch.float16).pin_memory()}
+               for _ in range(n_e2e)]
+    host_out = [torch.empty(4, B, Hq, D, dtype=torch.float16).pin_memory() for _ in range(n_e2e)]
+    for k in range(n_e2e):
+        host_in[k]["q"].copy_(qs[base + k].cpu())
+        host_in[k]["k"].copy_(kn[base + k].cpu())
+        host_in[k]["v"].copy_(vn[base + k].cpu())
+    outs2 = [outs, torch.empty_like(outs)]
+    copy_stream = torch.cuda.Stream(dev)
+    # the caches keep growing: reuse the last warm-up slots' step indices to stay in capacity
+    with torch.cuda.stream(stream):
         fp.n.sub_(n_e2e)
         fp.seqlen.sub_(n_e2e)
         kv4.len.sub_(n_e2e)
-        barrier()
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for k in range(n_e2e):
-            step(base + k, host=host)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev_in = [torch.cuda.Event() for _ in range(n_e2e)]
+    ev_done = [torch.cuda.Event() for _ in range(n_e2e)]
+    ev_free = [torch.cuda.Event() for _ in range(n_e2e)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    copy_stream.wait_event(e0)
+
+    def upload(k):
+        with torch.cuda.stream(copy_stream):
+            qs[base + k].copy_(host_in[k]["q"], non_blocking=True)
+            kn[base + k].copy_(host_in[k]["k"], non_blocking=True)
+            vn[base + k].copy_(host_in[k]["v"], non_blocking=True)
+            ev_in[k].record(copy_stream)
+
+    upload(0)
+    for k in range(n_e2e):
+        if k + 1 < n_e2e:
+            upload(k + 1)
+        o_buf = outs2[k % 2]
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev_in[k])
+            if k >= 2:
+                stream.wait_event(ev_free[k - 2])   # that output buffer has been read back
+            step_outs = o_buf
+            step(base + k, outs_override=step_outs)
+            ev_done[k].record(stream)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_done[k])
+            host_out[k].copy_(o_buf, non_blocking=True)
+            ev_free[k].record(copy_stream)
+    e1.record(copy_stream)
+    torch.cuda.synchronize(dev)
+    barrier()
     e2e_ms = e0.elapsed_time(e1) / n_e2e
-    h2d = sum(t.numel() * t.element_size() for t in (host["q"], host["k"], host["v"]))
-    d2h = host["o"].numel() * host["o"].element_size()
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
+    d2h = host_out[0].numel() * host_out[0].element_size()
 
     # ---------------- random eviction rows (reasoning-trace shape), timed in the same run
     rows.update(random_rows(kvc, W, dev, stream))

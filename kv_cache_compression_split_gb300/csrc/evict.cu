@@ -449,9 +449,46 @@ __global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams 
         if (take >= n - n_rec)
             return;   // nothing to drop
         n_new = n_rec + take;
-        if (take > 0) {
-            auto key = [&](int j) { return ((uint64_t)desc_bits(sc[j]) << 32) | (uint32_t)pos[j]; };
-            auto cand = [&](int j) { return (long)pos[j] < rt; };
+        auto key = [&](int j) { return ((uint64_t)desc_bits(sc[j]) << 32) | (uint32_t)pos[j]; };
+        auto cand = [&](int j) { return (long)pos[j] < rt; };
+        const int drops = n - n_rec - take;
+        if (take > 0 && drops <= 4) {
+            // few drops (the decode step drops one): keep every candidate, then remove
+            // the worst -- the largest (descending score, position) key -- drops times
+            for (int base = 0; base < n; base += 32) {
+                const int j = base + lane;
+                const unsigned m = __ballot_sync(0xffffffffu, j < n && cand(j));
+                if (lane == 0)
+                    keep[base >> 5] |= m;
+            }
+            __syncwarp();
+            for (int d = 0; d < drops; ++d) {
+                uint64_t best = 0;
+                int bj = -1;
+                for (int base = 0; base < n; base += 32) {
+                    const int j = base + lane;
+                    if (j < n && cand(j) && ((keep[base >> 5] >> lane) & 1u)) {
+                        const uint64_t k = key(j);
+                        if (bj < 0 || k > best) {
+                            best = k;
+                            bj = j;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const uint64_t ok = __shfl_xor_sync(0xffffffffu, best, off);
+                    const int oj = __shfl_xor_sync(0xffffffffu, bj, off);
+                    if (oj >= 0 && (bj < 0 || ok > best)) {
+                        best = ok;
+                        bj = oj;
+                    }
+                }
+                if (lane == 0)
+                    keep[bj >> 5] &= ~(1u << (bj & 31));
+                __syncwarp();
+            }
+        } else if (take > 0) {
             const uint64_t kth = warp_radix_select(n, take, key, cand, s_hist[warp]);
             for (int base = 0; base < n; base += 32) {
                 const int j = base + lane;
