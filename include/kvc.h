@@ -290,7 +290,10 @@ KVC_API kvc_status kvc_h2o_accumulate(const kvc_h2o_args *args, cudaStream_t str
 /*
  * kvc_h2o_evict -- per unit keep the recent window (positions >= seqlen[b] -
  * n_recent) and the n_heavy other slots with the largest scores (ties: lower
- * position first); compact K, V, pos and scores [B, Hkv, C] and set n.
+ * position first); compact K, V, pos and scores [B, Hkv, C] and set n.  The
+ * scores of the freed slots [n', n) are set to 0, so a token appended there
+ * later starts from a zero score (new slots beyond the old n must be 0 too:
+ * zero the whole scores array when the cache is created).
  * A unit with at most n_heavy + n_recent slots is unchanged.
  * Source: "Rethinking KV Cache Compression" guide, §2 (64 heavy + 448 recent)
  * and §16 "4 种方法逐步执行".

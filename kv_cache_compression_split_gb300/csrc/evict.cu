@@ -335,6 +335,10 @@ __global__ void __launch_bounds__(ETHREADS) k_evict(const EvictParams p)
         }
         __syncthreads();
     }
+    // freed slots start from a zero score when a later token is appended there
+    if (sc)
+        for (int j = n_new + threadIdx.x; j < n; j += ETHREADS)
+            sc[j] = 0.f;
     if (threadIdx.x == 0)
         p.n[unit] = n_new;
 }
@@ -536,6 +540,12 @@ __global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams 
                     p.scores[dst] = p.scores[src];
             }
         }
+    }
+    // freed slots start from a zero score when a later token is appended there
+    if (sc) {
+        __syncwarp();
+        for (int j = n_new + lane; j < n; j += 32)
+            sc[j] = 0.f;
     }
     if (lane == 0)
         p.n[unit] = n_new;

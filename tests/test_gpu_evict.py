@@ -193,6 +193,7 @@ def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, fused, splits):
                                rtol=SCORE_REL_TOL)
     n, pos, _, _ = _units(cache)
     assert (n == 512).all()
+    assert (scores[:, :, 512:].cpu() == 0).all()     # the freed slot starts from zero
     for b in range(B):
         for hk in range(Hkv):
             _check_keep_with_ties(pos[b, hk, :512], pos513[b, hk], sc_ref[b, hk], T + 1, n_heavy,
