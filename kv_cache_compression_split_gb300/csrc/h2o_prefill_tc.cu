@@ -1,0 +1,493 @@
+// h2o_prefill_tc.cu -- the H2O prefill score pass on the 5th-generation tensor
+// cores (tcgen05.mma, accumulators in TMEM).
+//
+// The heavy-hitter score of prompt token j is the attention it receives from
+// every later prompt row, summed over the query heads of its KV head
+// ("Rethinking KV Cache Compression" guide, §16 "局限与最终结论": flash attention
+// never materialises the probabilities, so scoring needs an extra pass):
+//   pass 1  lse_i = log2 sum_{j <= i} 2^(s_ij)          (s = scale log2e q_i . k_j)
+//   pass 2  score_j = sum_{h in group} sum_{i >= j} 2^(s_ij - lse_i)
+//
+// A work item is one 128-row "stationary" tile held in shared memory -- a query
+// tile in pass 1, a key tile in pass 2 -- against every 128-row tile of the
+// other operand it meets under the causal mask, streamed through a TMA ring.
+// Causal items are paired (t, nt-1-t) so all pairs cost the same; the CTAs are
+// persistent and walk the pairs round-robin.  One thread issues tcgen05.mma
+// (M = N = 128, fp16 in, fp32 out) into one of two TMEM accumulators, so the
+// next product runs while four epilogue warps read the previous one: a thread
+// owns one TMEM lane, i.e. one query row (pass 1: online max / sum) or one key
+// row (pass 2: sum of probabilities over the tile's queries).  The epilogue
+// classifies each 32-column chunk per warp as fully inside the causal window,
+// fully outside (skipped) or cut by it (masked), so only the diagonal and the
+// ragged tail pay for masks; its arithmetic runs on packed fp32 pairs.
+#include "kvc_device.cuh"
+#include "kvc_internal.h"
+
+#include <math.h>
+
+namespace kvc {
+
+namespace {
+
+constexpr int TT = 128;                  // rows of every tile
+constexpr int NEPI = 4;                  // epilogue warps (one per TMEM lane quarter)
+constexpr int NTHR = (2 + NEPI) * 32;    // warp 0: TMA producer, warp 1: MMA issuer
+constexpr int NS = 2;                    // streaming stages
+constexpr int TMEM_COLS = 2 * TT;        // two fp32 accumulators of 128 columns
+constexpr int CTAS_PER_SM = 2;
+constexpr float LOG2E = 1.4426950408889634f;
+
+template <int D> struct TcCfg {
+    static constexpr int NBOX = D / 64;
+    static constexpr int BOX_BYTES = TT * 128;
+    static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
+    static constexpr int LSE_BYTES = NEPI * TT * 4;
+    // at most two CTAs per SM: each holds half of the SM's 512 TMEM columns
+    static constexpr int SMEM_USED = (1 + NS) * TILE_BYTES + LSE_BYTES + 256 + 1024;
+    static constexpr int SMEM = SMEM_USED > 80 * 1024 ? SMEM_USED : 80 * 1024;
+    static constexpr uint32_t IDESC = idesc_f16_f32(TT, TT);
+};
+
+struct TcParams {
+    int Hq, Hkv, g, L, Lpad, kp_cap, C, nt, npairs, n_work;
+    float *lse2;
+    float *scores;
+    float scale_log2;
+    int *status;
+};
+
+// The CTA's work items in order: pair w covers tiles w % npairs and
+// nt - 1 - w % npairs of the (head or unit) w / npairs.
+struct ItemCursor {
+    int w, h;
+    __device__ bool get(const TcParams &p, int &outer, int &t) const
+    {
+        if (w >= p.n_work)
+            return false;
+        outer = w / p.npairs;
+        const int pair = w % p.npairs;
+        t = h == 0 ? pair : p.nt - 1 - pair;
+        return true;
+    }
+    __device__ void advance(const TcParams &p, int step)
+    {
+        const int pair = w % p.npairs;
+        if (h == 0 && pair != p.nt - 1 - pair) {
+            h = 1;
+        } else {
+            h = 0;
+            w += step;
+        }
+    }
+};
+
+// Stream tile s of an item on tile t: pass 1 key tile s; pass 2 query tile
+// qt of head hh of the group.
+struct StreamTile {
+    int hh, qt;
+};
+template <int PASS> __device__ __forceinline__ StreamTile stream_tile(const TcParams &p, int t, int s)
+{
+    if (PASS == 1)
+        return {0, s};
+    const int per = p.nt - t;
+    return {s / per, t + s % per};
+}
+
+template <int PASS> __device__ __forceinline__ int n_stream(const TcParams &p, int t)
+{
+    return PASS == 1 ? t + 1 : p.g * (p.nt - t);
+}
+
+enum ChunkClass { CH_NONE = 0, CH_FULL = 1, CH_PART = 2 };
+
+// Pass 1: fold 32 key columns j0 + c into the online (m, l) of query row gi.
+template <bool MASK>
+__device__ __forceinline__ void p1_chunk(const float *v, int j0, int gi, int L, float scale,
+                                         float &m, float &l)
+{
+    float x[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+        x[c] = (!MASK || (j0 + c <= gi && j0 + c < L)) ? v[c] : -INFINITY;
+    float c0 = fmax3f(x[0], x[1], x[2]), c1 = fmax3f(x[8], x[9], x[10]);
+    float c2 = fmax3f(x[16], x[17], x[18]), c3 = fmax3f(x[24], x[25], x[26]);
+#pragma unroll
+    for (int k = 3; k < 7; k += 2) {
+        c0 = fmax3f(c0, x[k], x[k + 1]);
+        c1 = fmax3f(c1, x[8 + k], x[9 + k]);
+        c2 = fmax3f(c2, x[16 + k], x[17 + k]);
+        c3 = fmax3f(c3, x[24 + k], x[25 + k]);
+    }
+    const float mx = fmaxf(fmax3f(c0, c1, x[7]), fmax3f(c2, c3, fmax3f(x[15], x[23], x[31])));
+    const float mn = fmaxf(m, mx * scale);
+    const float ref = mn == -INFINITY ? 0.f : mn;
+    const float2 sc2 = make_float2(scale, scale), nr2 = make_float2(-ref, -ref);
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+        const float2 y0 = ffma2(make_float2(x[c], x[c + 1]), sc2, nr2);
+        const float2 y1 = ffma2(make_float2(x[c + 2], x[c + 3]), sc2, nr2);
+        a0 = fadd2(a0, make_float2(ex2(y0.x), ex2(y0.y)));
+        a1 = fadd2(a1, make_float2(ex2(y1.x), ex2(y1.y)));
+    }
+    const float2 a = fadd2(a0, a1);
+    l = l * ex2(m - ref) + (a.x + a.y);
+    m = mn;
+}
+
+// Pass 2: sum over 32 query columns i0 + c of 2^(s scale - lse_i) for key row gi;
+// nlse holds -lse_i of those columns.
+template <bool MASK>
+__device__ __forceinline__ float p2_chunk(const float *v, const float *nlse, int i0, int gi, int L,
+                                          float scale)
+{
+    const float2 sc2 = make_float2(scale, scale);
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+        const float4 nl = *reinterpret_cast<const float4 *>(nlse + c);
+        const float2 y0 = ffma2(make_float2(v[c], v[c + 1]), sc2, make_float2(nl.x, nl.y));
+        const float2 y1 = ffma2(make_float2(v[c + 2], v[c + 3]), sc2, make_float2(nl.z, nl.w));
+        float e[4] = {ex2(y0.x), ex2(y0.y), ex2(y1.x), ex2(y1.y)};
+        if (MASK) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                e[u] = (i0 + c + u >= gi && i0 + c + u < L) ? e[u] : 0.f;
+        }
+        a0 = fadd2(a0, make_float2(e[0], e[1]));
+        a1 = fadd2(a1, make_float2(e[2], e[3]));
+    }
+    const float2 a = fadd2(a0, a1);
+    return a.x + a.y;
+}
+
+template <int D, int PASS>
+__global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
+    k_prefill_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const TcParams p)
+{
+    using Cfg = TcCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *stat = smem;                                   // stationary tile
+    uint8_t *ring = smem + Cfg::TILE_BYTES;                 // NS streaming tiles
+    float *lse_buf = reinterpret_cast<float *>(smem + (1 + NS) * Cfg::TILE_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (1 + NS) * Cfg::TILE_BYTES + Cfg::LSE_BYTES);
+    uint64_t *s_full = bars, *s_empty = bars + NS;
+    uint64_t *acc_full = bars + 2 * NS, *acc_empty = bars + 2 * NS + 2;
+    uint64_t *stat_full = bars + 2 * NS + 4, *stat_empty = bars + 2 * NS + 5;
+    uint64_t *mma_done = bars + 2 * NS + 6;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    volatile int *abort = &s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // (b, hk) and the head (pass 1) / KV unit (pass 2) of an item's outer index
+    auto decode = [&](int outer, int &b, int &hk, int &bh, int &unit) {
+        if (PASS == 1) {
+            bh = outer;
+            b = bh / p.Hq;
+            hk = (bh % p.Hq) / p.g;
+            unit = b * p.Hkv + hk;
+        } else {
+            bh = 0;
+            unit = outer;
+            b = unit / p.Hkv;
+            hk = unit % p.Hkv;
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], NEPI);
+        }
+        mbar_init(stat_full, 1);
+        mbar_init(stat_empty, 1);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&s_tmem, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            int it = 0, n_stat = 0, outer, t;
+            bool ok = true;
+            for (ItemCursor cur{(int)blockIdx.x, 0}; ok && cur.get(p, outer, t);
+                 cur.advance(p, gridDim.x)) {
+                int b, hk, bh, unit;
+                decode(outer, b, hk, bh, unit);
+                if (n_stat > 0 && !mbar_wait_or_abort(stat_empty, (n_stat - 1) & 1, abort))
+                    break;
+                ++n_stat;
+                mbar_arrive_expect_tx(stat_full, Cfg::TILE_BYTES);
+#pragma unroll
+                for (int j = 0; j < Cfg::NBOX; ++j) {
+                    if (PASS == 1)
+                        tma_load_2d(stat + j * Cfg::BOX_BYTES, &tmQ, stat_full, 64 * j,
+                                    bh * p.L + t * TT);
+                    else
+                        tma_load_2d(stat + j * Cfg::BOX_BYTES, &tmK, stat_full, 64 * j,
+                                    unit * p.kp_cap + t * TT);
+                }
+                const int ns = n_stream<PASS>(p, t);
+                for (int s = 0; s < ns; ++s, ++it) {
+                    const int st = it % NS;
+                    if (it >= NS && !mbar_wait_or_abort(&s_empty[st], ((it / NS) & 1) ^ 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *dst = ring + st * Cfg::TILE_BYTES;
+                    const StreamTile sp = stream_tile<PASS>(p, t, s);
+                    mbar_arrive_expect_tx(&s_full[st], Cfg::TILE_BYTES);
+#pragma unroll
+                    for (int j = 0; j < Cfg::NBOX; ++j) {
+                        if (PASS == 1)
+                            tma_load_2d(dst + j * Cfg::BOX_BYTES, &tmK, &s_full[st], 64 * j,
+                                        unit * p.kp_cap + sp.qt * TT);
+                        else
+                            tma_load_2d(dst + j * Cfg::BOX_BYTES, &tmQ, &s_full[st], 64 * j,
+                                        (b * p.Hq + hk * p.g + sp.hh) * p.L + sp.qt * TT);
+                    }
+                }
+            }
+            // Every copy has landed before the CTA leaves.  Normally the MMA
+            // thread consumed them all; after a timeout this bounds the wait.
+            for (int i = it > NS ? it - NS : 0; i < it; ++i)
+                mbar_wait(&s_full[i % NS], (i / NS) & 1);
+            if (n_stat > 0)
+                mbar_wait(stat_full, (n_stat - 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int it = 0, tc = 0, n_item = 0, outer, t;
+            bool ok = true;
+            for (ItemCursor cur{(int)blockIdx.x, 0}; ok && cur.get(p, outer, t);
+                 cur.advance(p, gridDim.x), ++n_item) {
+                if (!mbar_wait_or_abort(stat_full, n_item & 1, abort))
+                    break;
+                tc_fence_after();
+                const uint32_t sbase = smem_u32(stat);
+                const int ns = n_stream<PASS>(p, t);
+                for (int s = 0; s < ns; ++s, ++it, ++tc) {
+                    const int st = it % NS, buf = tc & 1;
+                    if (!mbar_wait_or_abort(&s_full[st], (it / NS) & 1, abort) ||
+                        (tc >= 2 && !mbar_wait_or_abort(&acc_empty[buf], ((tc / 2) & 1) ^ 1, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t rbase = smem_u32(ring + st * Cfg::TILE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * Cfg::BOX_BYTES + (kk & 3) * 32;
+                        umma_f16(tmem + buf * TT, sdesc_k_sw128(sbase + off),
+                                 sdesc_k_sw128(rbase + off), Cfg::IDESC, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&s_empty[st]);
+                    umma_commit(&acc_full[buf]);
+                }
+                umma_commit(stat_empty);
+            }
+            // every product this thread issued has finished before TMEM is released
+            umma_commit(mma_done);
+            mbar_wait(mma_done, 0);
+        }
+    } else {
+        // ------------------------------------------------ epilogue warps
+        const int quarter = warp & 3;              // TMEM lanes [32 quarter, 32 quarter + 32)
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+        float *my_lse = lse_buf + (warp - 2) * TT;
+        int tc = 0, outer, t;
+        bool ok = true;
+        for (ItemCursor cur{(int)blockIdx.x, 0}; ok && cur.get(p, outer, t);
+             cur.advance(p, gridDim.x)) {
+            int b, hk, bh, unit;
+            decode(outer, b, hk, bh, unit);
+            const int ns = n_stream<PASS>(p, t);
+            const int r0 = t * TT + 32 * quarter;   // first row of this warp
+            const int gi = r0 + lane;               // this thread's query (1) / key (2) row
+            float m = -INFINITY, l = 0.f;           // pass 1
+            double acc = 0.0;                       // pass 2
+            // pass 2: the lse of the next tile's 128 queries, one float4 per lane
+            const float *lse_head = p.lse2 + (size_t)(b * p.Hq + hk * p.g) * p.Lpad;
+            float4 nxt = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (PASS == 2) {
+                const StreamTile sp = stream_tile<PASS>(p, t, 0);
+                nxt = reinterpret_cast<const float4 *>(lse_head + (size_t)sp.hh * p.Lpad +
+                                                       sp.qt * TT)[lane];
+            }
+            for (int s = 0; s < ns; ++s, ++tc) {
+                const int buf = tc & 1;
+                const StreamTile sp = stream_tile<PASS>(p, t, s);
+                if (PASS == 2) {
+                    reinterpret_cast<float4 *>(my_lse)[lane] =
+                        make_float4(-nxt.x, -nxt.y, -nxt.z, -nxt.w);
+                    if (s + 1 < ns) {
+                        const StreamTile sn = stream_tile<PASS>(p, t, s + 1);
+                        nxt = reinterpret_cast<const float4 *>(lse_head + (size_t)sn.hh * p.Lpad +
+                                                               sn.qt * TT)[lane];
+                    }
+                }
+                // one lane waits, so that the whole warp takes the same branch
+                int got = 0;
+                if (lane == 0)
+                    got = mbar_wait_or_abort(&acc_full[buf], (tc / 2) & 1, abort) ? 1 : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // warp-uniform class of each 32-column chunk
+                int cls[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int c0 = sp.qt * TT + 32 * k;   // first key (1) / query (2) column
+                    if (PASS == 1)
+                        cls[k] = (c0 >= p.L || c0 > r0 + 31)          ? CH_NONE
+                                 : (c0 + 31 <= r0 && c0 + 31 < p.L)   ? CH_FULL
+                                                                      : CH_PART;
+                    else
+                        cls[k] = (c0 >= p.L || c0 + 31 < r0)          ? CH_NONE
+                                 : (c0 >= r0 + 31 && c0 + 31 < p.L)   ? CH_FULL
+                                                                      : CH_PART;
+                }
+                float tile_sum = 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float v[64];
+                    const bool need = cls[2 * half] != CH_NONE || cls[2 * half + 1] != CH_NONE;
+                    if (need)
+                        tmem_ld64(lane_addr + buf * TT + 64 * half, v);
+                    if (half == 1) {
+                        // the tile is in registers: hand the accumulator back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(&acc_empty[buf]);
+                    }
+                    if (PASS == 2 && half == 0)
+                        __syncwarp();   // my_lse written by every lane
+#pragma unroll
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        const int k = 2 * half + k2;
+                        const int c0 = sp.qt * TT + 32 * k;
+                        if (PASS == 1) {
+                            if (cls[k] == CH_FULL)
+                                p1_chunk<false>(v + 32 * k2, c0, gi, p.L, p.scale_log2, m, l);
+                            else if (cls[k] == CH_PART)
+                                p1_chunk<true>(v + 32 * k2, c0, gi, p.L, p.scale_log2, m, l);
+                        } else {
+                            if (cls[k] == CH_FULL)
+                                tile_sum += p2_chunk<false>(v + 32 * k2, my_lse + 32 * k, c0, gi,
+                                                            p.L, p.scale_log2);
+                            else if (cls[k] == CH_PART)
+                                tile_sum += p2_chunk<true>(v + 32 * k2, my_lse + 32 * k, c0, gi,
+                                                           p.L, p.scale_log2);
+                        }
+                    }
+                }
+                if (PASS == 2) {
+                    acc += (double)tile_sum;
+                    __syncwarp();   // my_lse is rewritten for the next tile
+                }
+            }
+            if (!ok)
+                break;
+            if (gi < p.L) {
+                if (PASS == 1)
+                    p.lse2[(size_t)bh * p.Lpad + gi] = m + __log2f(l);
+                else
+                    p.scores[(size_t)unit * p.C + gi] = (float)acc;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort)
+        flag_error(p.status, DEV_TIMEOUT);
+}
+
+template <int D, int PASS>
+cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const TcParams &tp,
+                      cudaStream_t s)
+{
+    using Cfg = TcCfg<D>;
+    static int configured = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured != dev) {
+        cudaError_t e = cudaFuncSetAttribute(k_prefill_tc<D, PASS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+        if (e != cudaSuccess)
+            return e;
+        configured = dev;
+    }
+    const int cap = CTAS_PER_SM * sm_count();
+    const int grid = tp.n_work < cap ? tp.n_work : cap;
+    k_prefill_tc<D, PASS><<<grid, NTHR, Cfg::SMEM, s>>>(tq, tk, tp);
+    return cudaGetLastError();
+}
+
+template <int D> cudaError_t prefill_tc_impl(const kvc_h2o_args &a, float *lse_ws, cudaStream_t s)
+{
+    TcParams tp{};
+    tp.Hq = a.Hq;
+    tp.Hkv = a.Hkv;
+    tp.g = a.Hq / a.Hkv;
+    tp.L = a.L;
+    tp.nt = (a.L + TT - 1) / TT;
+    tp.Lpad = tp.nt * TT;
+    tp.npairs = (tp.nt + 1) / 2;
+    tp.kp_cap = a.kp_cap;
+    tp.C = a.C;
+    tp.lse2 = lse_ws;
+    tp.scores = a.scores;
+    const float scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / sqrtf((float)a.D);
+    tp.scale_log2 = scale * LOG2E;
+    tp.status = dev_status_ptr();
+    CUtensorMap tq, tk;
+    if (!encode_tmap_2d_f16(&tq, a.qp, D, (uint64_t)a.B * a.Hq * a.L, 64, TT) ||
+        !encode_tmap_2d_f16(&tk, a.kp, D, (uint64_t)a.B * a.Hkv * a.kp_cap, 64, TT))
+        return cudaErrorInvalidValue;
+    tp.n_work = a.B * a.Hq * tp.npairs;
+    cudaError_t e = launch_tc<D, 1>(tq, tk, tp, s);
+    if (e != cudaSuccess)
+        return e;
+    tp.n_work = a.B * a.Hkv * tp.npairs;
+    return launch_tc<D, 2>(tq, tk, tp, s);
+}
+
+} // namespace
+
+cudaError_t launch_h2o_prefill(const kvc_h2o_args &a, float *lse_ws, cudaStream_t s)
+{
+    return a.D == 128 ? prefill_tc_impl<128>(a, lse_ws, s) : prefill_tc_impl<64>(a, lse_ws, s);
+}
+
+} // namespace kvc

@@ -70,6 +70,7 @@ cudaError_t launch_append_quant(const kvc_quant_cache &c, const uint16_t *k_new,
                                 const uint16_t *v_new, int n_new, cudaStream_t s);
 
 cudaError_t launch_h2o_decode_acc(const kvc_h2o_args &a, cudaStream_t s);
+// Two tcgen05 passes over the causal prompt; lse_ws holds B*Hq*ceil(L/128)*128 floats.
 cudaError_t launch_h2o_prefill(const kvc_h2o_args &a, float *lse_ws, cudaStream_t s);
 
 enum EvictKind { EVICT_H2O = 0, EVICT_STREAM = 1, EVICT_RANDOM = 2 };

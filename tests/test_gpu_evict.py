@@ -103,7 +103,8 @@ def _check_keep_with_ties(keep_gpu_pos, pos, score_ref, T, n_heavy, n_recent):
 
 @pytest.mark.parametrize("B,Hq,Hkv,L,D,n_heavy,n_recent", [
     (1, 4, 4, 64, 64, 8, 8), (2, 8, 2, 300, 128, 16, 40), (1, 16, 2, 1000, 128, 64, 448),
-    (2, 4, 4, 130, 64, 200, 8), (1, 8, 1, 1500, 128, 64, 448), (2, 4, 4, 20, 64, 13, 4)])
+    (2, 4, 4, 130, 64, 200, 8), (1, 8, 1, 1500, 128, 64, 448), (2, 4, 4, 20, 64, 13, 4),
+    (1, 8, 2, 512, 128, 32, 64), (3, 6, 3, 384, 64, 20, 30), (1, 2, 1, 129, 128, 16, 16)])
 def test_h2o_prefill_scores_and_evict(kvc, orc, B, Hq, Hkv, L, D, n_heavy, n_recent):
     g = torch.Generator().manual_seed(L + Hq)
     C = L + 4
