@@ -526,9 +526,9 @@ def run_profile(args):
         for _ in range(3):
             kvc.kvc_decode_attend(cache, q, o, workspace=ws)
     elif what == "prefill":
-        L = 1024
-        qp = W.q_tensor(w, B=max(1, B // 8), L=L, device=dev)
-        kp = K[:max(1, B // 8), :, :L].contiguous()
+        L = T - 1
+        qp = W.q_tensor(w, B=max(1, B // 4), L=L, device=dev)
+        kp = K[:max(1, B // 4), :, :L].contiguous()
         sc = torch.zeros(kp.shape[0], Hkv, L, device=dev)
         ws = torch.empty(kvc.kvc_h2o_workspace_size(kp.shape[0], Hq, L) // 4, device=dev)
         for _ in range(3):

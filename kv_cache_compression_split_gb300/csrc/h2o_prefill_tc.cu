@@ -7,6 +7,8 @@
 // never materialises the probabilities, so scoring needs an extra pass):
 //   pass 1  lse_i = log2 sum_{j <= i} 2^(s_ij)          (s = scale log2e q_i . k_j)
 //   pass 2  score_j = sum_{h in group} sum_{i >= j} 2^(s_ij - lse_i)
+// Pass 1 stores -lse_i; pass 2 brings each query tile's 128 values into a small
+// shared-memory ring with the tile, so its epilogue reads them from there.
 //
 // A work item is one 128-row "stationary" tile held in shared memory -- a query
 // tile in pass 1, a key tile in pass 2 -- against every 128-row tile of the
@@ -14,12 +16,14 @@
 // Causal items are paired (t, nt-1-t) so all pairs cost the same; the CTAs are
 // persistent and walk the pairs round-robin.  One thread issues tcgen05.mma
 // (M = N = 128, fp16 in, fp32 out) into one of two TMEM accumulators, so the
-// next product runs while four epilogue warps read the previous one: a thread
-// owns one TMEM lane, i.e. one query row (pass 1: online max / sum) or one key
-// row (pass 2: sum of probabilities over the tile's queries).  The epilogue
-// classifies each 32-column chunk per warp as fully inside the causal window,
-// fully outside (skipped) or cut by it (masked), so only the diagonal and the
-// ragged tail pay for masks; its arithmetic runs on packed fp32 pairs.
+// next product runs while eight epilogue warps read the previous one.  TMEM
+// lane r is row r of the product (a query row in pass 1, a key row in pass 2);
+// the two warps of a lane quarter take one half of the 128 columns each, keep a
+// partial row state (online max / sum, or a probability sum) and merge it at
+// the end of the item.  Each 32-column chunk is classified per warp as inside
+// the causal window, outside it (skipped) or cut by it (masked), so only the
+// diagonal and the ragged tail pay for masks; the arithmetic runs on packed
+// fp32 pairs.
 #include "kvc_device.cuh"
 #include "kvc_internal.h"
 
@@ -30,9 +34,11 @@ namespace kvc {
 namespace {
 
 constexpr int TT = 128;                  // rows of every tile
-constexpr int NEPI = 4;                  // epilogue warps (one per TMEM lane quarter)
+constexpr int NQ = 4;                    // TMEM lane quarters
+constexpr int NEPI = 2 * NQ;             // epilogue warps: two column halves per quarter
 constexpr int NTHR = (2 + NEPI) * 32;    // warp 0: TMA producer, warp 1: MMA issuer
 constexpr int NS = 2;                    // streaming stages
+constexpr int NL = 4;                    // pass 2: -lse slots of 128 floats
 constexpr int TMEM_COLS = 2 * TT;        // two fp32 accumulators of 128 columns
 constexpr int CTAS_PER_SM = 2;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -41,16 +47,17 @@ template <int D> struct TcCfg {
     static constexpr int NBOX = D / 64;
     static constexpr int BOX_BYTES = TT * 128;
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
-    static constexpr int LSE_BYTES = NEPI * TT * 4;
+    static constexpr int LSE_BYTES = NL * TT * 4;
+    static constexpr int MERGE_BYTES = NQ * 32 * 8;          // row state of the second column half
+    static constexpr int SMEM_USED = (1 + NS) * TILE_BYTES + LSE_BYTES + MERGE_BYTES + 512 + 1024;
     // at most two CTAs per SM: each holds half of the SM's 512 TMEM columns
-    static constexpr int SMEM_USED = (1 + NS) * TILE_BYTES + LSE_BYTES + 256 + 1024;
     static constexpr int SMEM = SMEM_USED > 80 * 1024 ? SMEM_USED : 80 * 1024;
     static constexpr uint32_t IDESC = idesc_f16_f32(TT, TT);
 };
 
 struct TcParams {
     int Hq, Hkv, g, L, Lpad, kp_cap, C, nt, npairs, n_work;
-    float *lse2;
+    float *nlse;        // [B*Hq, Lpad]: -lse of every prompt row (pass 1 writes, pass 2 reads)
     float *scores;
     float scale_log2;
     int *status;
@@ -81,22 +88,35 @@ struct ItemCursor {
     }
 };
 
-// Stream tile s of an item on tile t: pass 1 key tile s; pass 2 query tile
-// qt of head hh of the group.
-struct StreamTile {
+// Walks the stream tiles of an item on tile t in order: pass 1 key tiles
+// qt = 0 .. t; pass 2 query tiles qt = t .. nt-1 of group head hh = 0, then of
+// head 1, and so on.
+template <int PASS> struct StreamWalk {
     int hh, qt;
+    __device__ explicit StreamWalk(int t) : hh(0), qt(PASS == 1 ? 0 : t) {}
+    __device__ void next(const TcParams &p, int t)
+    {
+        if (PASS == 1) {
+            ++qt;
+        } else if (++qt == p.nt) {
+            qt = t;
+            ++hh;
+        }
+    }
 };
-template <int PASS> __device__ __forceinline__ StreamTile stream_tile(const TcParams &p, int t, int s)
-{
-    if (PASS == 1)
-        return {0, s};
-    const int per = p.nt - t;
-    return {s / per, t + s % per};
-}
 
 template <int PASS> __device__ __forceinline__ int n_stream(const TcParams &p, int t)
 {
     return PASS == 1 ? t + 1 : p.g * (p.nt - t);
+}
+
+// 2^x as an ordered statement: the exponentials of one chunk are issued before
+// the next chunk's TMEM load, so a thread never holds two chunks at once.
+__device__ __forceinline__ float ex2o(float x)
+{
+    float y;
+    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 enum ChunkClass { CH_NONE = 0, CH_FULL = 1, CH_PART = 2 };
@@ -128,11 +148,11 @@ __device__ __forceinline__ void p1_chunk(const float *v, int j0, int gi, int L, 
     for (int c = 0; c < 32; c += 4) {
         const float2 y0 = ffma2(make_float2(x[c], x[c + 1]), sc2, nr2);
         const float2 y1 = ffma2(make_float2(x[c + 2], x[c + 3]), sc2, nr2);
-        a0 = fadd2(a0, make_float2(ex2(y0.x), ex2(y0.y)));
-        a1 = fadd2(a1, make_float2(ex2(y1.x), ex2(y1.y)));
+        a0 = fadd2(a0, make_float2(ex2o(y0.x), ex2o(y0.y)));
+        a1 = fadd2(a1, make_float2(ex2o(y1.x), ex2o(y1.y)));
     }
     const float2 a = fadd2(a0, a1);
-    l = l * ex2(m - ref) + (a.x + a.y);
+    l = l * ex2o(m - ref) + (a.x + a.y);
     m = mn;
 }
 
@@ -149,7 +169,7 @@ __device__ __forceinline__ float p2_chunk(const float *v, const float *nlse, int
         const float4 nl = *reinterpret_cast<const float4 *>(nlse + c);
         const float2 y0 = ffma2(make_float2(v[c], v[c + 1]), sc2, make_float2(nl.x, nl.y));
         const float2 y1 = ffma2(make_float2(v[c + 2], v[c + 3]), sc2, make_float2(nl.z, nl.w));
-        float e[4] = {ex2(y0.x), ex2(y0.y), ex2(y1.x), ex2(y1.y)};
+        float e[4] = {ex2o(y0.x), ex2o(y0.y), ex2o(y1.x), ex2o(y1.y)};
         if (MASK) {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -160,6 +180,45 @@ __device__ __forceinline__ float p2_chunk(const float *v, const float *nlse, int
     }
     const float2 a = fadd2(a0, a1);
     return a.x + a.y;
+}
+
+// Fold this warp's two 32-column chunks of one accumulator tile (TMEM columns
+// taddr .. taddr + 63 of the warp's lanes) into the thread's row state, handing
+// the accumulator back once both chunks are in registers.  Returns the pass-2
+// sum of the chunks (0 in pass 1).
+template <int PASS>
+__device__ __forceinline__ float fold_tile(uint32_t taddr, uint64_t *acc_empty, int cls0, int cls1,
+                                           int col0, int gi, const TcParams &p, const float *nlse,
+                                           float &m, float &l)
+{
+    const int lane = threadIdx.x & 31;
+    float tile_sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int cls = k == 0 ? cls0 : cls1;
+        float v[32];
+        if (cls != CH_NONE)
+            tmem_ld32(taddr + 32 * k, v);
+        if (k == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acc_empty);
+        }
+        const int c0 = col0 + 32 * k;
+        if (PASS == 1) {
+            if (cls == CH_FULL)
+                p1_chunk<false>(v, c0, gi, p.L, p.scale_log2, m, l);
+            else if (cls == CH_PART)
+                p1_chunk<true>(v, c0, gi, p.L, p.scale_log2, m, l);
+        } else {
+            if (cls == CH_FULL)
+                tile_sum += p2_chunk<false>(v, nlse + 32 * k, c0, gi, p.L, p.scale_log2);
+            else if (cls == CH_PART)
+                tile_sum += p2_chunk<true>(v, nlse + 32 * k, c0, gi, p.L, p.scale_log2);
+        }
+    }
+    return tile_sum;
 }
 
 template <int D, int PASS>
@@ -174,11 +233,15 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
     uint8_t *stat = smem;                                   // stationary tile
     uint8_t *ring = smem + Cfg::TILE_BYTES;                 // NS streaming tiles
     float *lse_buf = reinterpret_cast<float *>(smem + (1 + NS) * Cfg::TILE_BYTES);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (1 + NS) * Cfg::TILE_BYTES + Cfg::LSE_BYTES);
+    double *merge = reinterpret_cast<double *>(smem + (1 + NS) * Cfg::TILE_BYTES + Cfg::LSE_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (1 + NS) * Cfg::TILE_BYTES + Cfg::LSE_BYTES +
+                                                  Cfg::MERGE_BYTES);
     uint64_t *s_full = bars, *s_empty = bars + NS;
     uint64_t *acc_full = bars + 2 * NS, *acc_empty = bars + 2 * NS + 2;
     uint64_t *stat_full = bars + 2 * NS + 4, *stat_empty = bars + 2 * NS + 5;
     uint64_t *mma_done = bars + 2 * NS + 6;
+    uint64_t *mrg_full = bars + 2 * NS + 7, *mrg_empty = bars + 2 * NS + 7 + NQ;
+    uint64_t *l_full = bars + 2 * NS + 7 + 2 * NQ, *l_empty = l_full + NL;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     volatile int *abort = &s_abort;
@@ -213,6 +276,14 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
         mbar_init(stat_full, 1);
         mbar_init(stat_empty, 1);
         mbar_init(mma_done, 1);
+        for (int q = 0; q < NQ; ++q) {
+            mbar_init(&mrg_full[q], 32);
+            mbar_init(&mrg_empty[q], 32);
+        }
+        for (int i = 0; i < NL; ++i) {
+            mbar_init(&l_full[i], 1);
+            mbar_init(&l_empty[i], NEPI);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -235,7 +306,7 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
                  cur.advance(p, gridDim.x)) {
                 int b, hk, bh, unit;
                 decode(outer, b, hk, bh, unit);
-                if (n_stat > 0 && !mbar_wait_or_abort(stat_empty, (n_stat - 1) & 1, abort))
+                if (n_stat > 0 && !mbar_sleep_or_abort(stat_empty, (n_stat - 1) & 1, abort))
                     break;
                 ++n_stat;
                 mbar_arrive_expect_tx(stat_full, Cfg::TILE_BYTES);
@@ -249,14 +320,26 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
                                     unit * p.kp_cap + t * TT);
                 }
                 const int ns = n_stream<PASS>(p, t);
-                for (int s = 0; s < ns; ++s, ++it) {
+                StreamWalk<PASS> sp(t);
+                for (int s = 0; s < ns; ++s, ++it, sp.next(p, t)) {
                     const int st = it % NS;
-                    if (it >= NS && !mbar_wait_or_abort(&s_empty[st], ((it / NS) & 1) ^ 1, abort)) {
+                    if (it >= NS && !mbar_sleep_or_abort(&s_empty[st], ((it / NS) & 1) ^ 1, abort)) {
                         ok = false;
                         break;
                     }
                     uint8_t *dst = ring + st * Cfg::TILE_BYTES;
-                    const StreamTile sp = stream_tile<PASS>(p, t, s);
+                    if (PASS == 2) {
+                        const int ls = it % NL;
+                        if (it >= NL &&
+                            !mbar_sleep_or_abort(&l_empty[ls], ((it / NL) & 1) ^ 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&l_full[ls], TT * 4);
+                        bulk_load(lse_buf + ls * TT,
+                                  p.nlse + (size_t)(b * p.Hq + hk * p.g + sp.hh) * p.Lpad + sp.qt * TT,
+                                  TT * 4, &l_full[ls]);
+                    }
                     mbar_arrive_expect_tx(&s_full[st], Cfg::TILE_BYTES);
 #pragma unroll
                     for (int j = 0; j < Cfg::NBOX; ++j) {
@@ -273,6 +356,9 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
             // thread consumed them all; after a timeout this bounds the wait.
             for (int i = it > NS ? it - NS : 0; i < it; ++i)
                 mbar_wait(&s_full[i % NS], (i / NS) & 1);
+            if (PASS == 2)
+                for (int i = it > NL ? it - NL : 0; i < it; ++i)
+                    mbar_wait(&l_full[i % NL], (i / NL) & 1);
             if (n_stat > 0)
                 mbar_wait(stat_full, (n_stat - 1) & 1);
         }
@@ -283,15 +369,16 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
             bool ok = true;
             for (ItemCursor cur{(int)blockIdx.x, 0}; ok && cur.get(p, outer, t);
                  cur.advance(p, gridDim.x), ++n_item) {
-                if (!mbar_wait_or_abort(stat_full, n_item & 1, abort))
+                if (!mbar_sleep_or_abort(stat_full, n_item & 1, abort))
                     break;
                 tc_fence_after();
                 const uint32_t sbase = smem_u32(stat);
                 const int ns = n_stream<PASS>(p, t);
                 for (int s = 0; s < ns; ++s, ++it, ++tc) {
                     const int st = it % NS, buf = tc & 1;
-                    if (!mbar_wait_or_abort(&s_full[st], (it / NS) & 1, abort) ||
-                        (tc >= 2 && !mbar_wait_or_abort(&acc_empty[buf], ((tc / 2) & 1) ^ 1, abort))) {
+                    if (!mbar_sleep_or_abort(&s_full[st], (it / NS) & 1, abort) ||
+                        (tc >= 2 &&
+                         !mbar_sleep_or_abort(&acc_empty[buf], ((tc / 2) & 1) ^ 1, abort))) {
                         ok = false;
                         break;
                     }
@@ -314,13 +401,14 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
         }
     } else {
         // ------------------------------------------------ epilogue warps
+        const int e = warp - 2;
         const int quarter = warp & 3;              // TMEM lanes [32 quarter, 32 quarter + 32)
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
-        float *my_lse = lse_buf + (warp - 2) * TT;
-        int tc = 0, outer, t;
+        const int half = e / NQ;                   // columns [64 half, 64 half + 64)
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16) + 64 * half;
+        int tc = 0, n_item = 0, outer, t;
         bool ok = true;
         for (ItemCursor cur{(int)blockIdx.x, 0}; ok && cur.get(p, outer, t);
-             cur.advance(p, gridDim.x)) {
+             cur.advance(p, gridDim.x), ++n_item) {
             int b, hk, bh, unit;
             decode(outer, b, hk, bh, unit);
             const int ns = n_stream<PASS>(p, t);
@@ -328,97 +416,91 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
             const int gi = r0 + lane;               // this thread's query (1) / key (2) row
             float m = -INFINITY, l = 0.f;           // pass 1
             double acc = 0.0;                       // pass 2
-            // pass 2: the lse of the next tile's 128 queries, one float4 per lane
-            const float *lse_head = p.lse2 + (size_t)(b * p.Hq + hk * p.g) * p.Lpad;
-            float4 nxt = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (PASS == 2) {
-                const StreamTile sp = stream_tile<PASS>(p, t, 0);
-                nxt = reinterpret_cast<const float4 *>(lse_head + (size_t)sp.hh * p.Lpad +
-                                                       sp.qt * TT)[lane];
-            }
-            for (int s = 0; s < ns; ++s, ++tc) {
+            float run = 0.f;
+            StreamWalk<PASS> sp(t);
+            for (int s = 0; s < ns; ++s, ++tc, sp.next(p, t)) {
                 const int buf = tc & 1;
-                const StreamTile sp = stream_tile<PASS>(p, t, s);
-                if (PASS == 2) {
-                    reinterpret_cast<float4 *>(my_lse)[lane] =
-                        make_float4(-nxt.x, -nxt.y, -nxt.z, -nxt.w);
-                    if (s + 1 < ns) {
-                        const StreamTile sn = stream_tile<PASS>(p, t, s + 1);
-                        nxt = reinterpret_cast<const float4 *>(lse_head + (size_t)sn.hh * p.Lpad +
-                                                               sn.qt * TT)[lane];
-                    }
-                }
-                // one lane waits, so that the whole warp takes the same branch
-                int got = 0;
-                if (lane == 0)
-                    got = mbar_wait_or_abort(&acc_full[buf], (tc / 2) & 1, abort) ? 1 : 0;
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) {
+                const int ls = tc % NL;
+                // pass 2: the tile's -lse has landed in slot ls (every lane
+                // acquires it); then one lane waits for the accumulator
+                bool got = PASS == 1 || mbar_sleep_or_abort(&l_full[ls], (tc / NL) & 1, abort);
+                if (lane == 0 && got)
+                    got = mbar_sleep_or_abort(&acc_full[buf], (tc / 2) & 1, abort);
+                if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // warp-uniform class of each 32-column chunk
-                int cls[4];
+                // Tiles off the diagonal lie wholly inside the causal window;
+                // otherwise each of this warp's 32-column chunks is classified.
+                const int col0 = sp.qt * TT + 64 * half;   // first key (1) / query (2) column
+                const float *nl = lse_buf + ls * TT + 64 * half;
+                const bool inside =
+                    PASS == 1 ? sp.qt < t : (sp.qt > t && sp.qt * TT + TT <= p.L);
+                float tile_sum;
+                if (inside) {
+                    tile_sum = fold_tile<PASS>(lane_addr + buf * TT, &acc_empty[buf], CH_FULL,
+                                               CH_FULL, col0, gi, p, nl, m, l);
+                } else {
+                    int cls[2];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int c0 = sp.qt * TT + 32 * k;   // first key (1) / query (2) column
-                    if (PASS == 1)
-                        cls[k] = (c0 >= p.L || c0 > r0 + 31)          ? CH_NONE
-                                 : (c0 + 31 <= r0 && c0 + 31 < p.L)   ? CH_FULL
-                                                                      : CH_PART;
-                    else
-                        cls[k] = (c0 >= p.L || c0 + 31 < r0)          ? CH_NONE
-                                 : (c0 >= r0 + 31 && c0 + 31 < p.L)   ? CH_FULL
-                                                                      : CH_PART;
-                }
-                float tile_sum = 0.f;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float v[64];
-                    const bool need = cls[2 * half] != CH_NONE || cls[2 * half + 1] != CH_NONE;
-                    if (need)
-                        tmem_ld64(lane_addr + buf * TT + 64 * half, v);
-                    if (half == 1) {
-                        // the tile is in registers: hand the accumulator back
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(&acc_empty[buf]);
+                    for (int k = 0; k < 2; ++k) {
+                        const int c0 = col0 + 32 * k;
+                        if (PASS == 1)
+                            cls[k] = (c0 >= p.L || c0 > r0 + 31)          ? CH_NONE
+                                     : (c0 + 31 <= r0 && c0 + 31 < p.L)   ? CH_FULL
+                                                                          : CH_PART;
+                        else
+                            cls[k] = (c0 >= p.L || c0 + 31 < r0)          ? CH_NONE
+                                     : (c0 >= r0 + 31 && c0 + 31 < p.L)   ? CH_FULL
+                                                                          : CH_PART;
                     }
-                    if (PASS == 2 && half == 0)
-                        __syncwarp();   // my_lse written by every lane
-#pragma unroll
-                    for (int k2 = 0; k2 < 2; ++k2) {
-                        const int k = 2 * half + k2;
-                        const int c0 = sp.qt * TT + 32 * k;
-                        if (PASS == 1) {
-                            if (cls[k] == CH_FULL)
-                                p1_chunk<false>(v + 32 * k2, c0, gi, p.L, p.scale_log2, m, l);
-                            else if (cls[k] == CH_PART)
-                                p1_chunk<true>(v + 32 * k2, c0, gi, p.L, p.scale_log2, m, l);
-                        } else {
-                            if (cls[k] == CH_FULL)
-                                tile_sum += p2_chunk<false>(v + 32 * k2, my_lse + 32 * k, c0, gi,
-                                                            p.L, p.scale_log2);
-                            else if (cls[k] == CH_PART)
-                                tile_sum += p2_chunk<true>(v + 32 * k2, my_lse + 32 * k, c0, gi,
-                                                           p.L, p.scale_log2);
-                        }
-                    }
+                    tile_sum = fold_tile<PASS>(lane_addr + buf * TT, &acc_empty[buf], cls[0],
+                                               cls[1], col0, gi, p, nl, m, l);
                 }
                 if (PASS == 2) {
-                    acc += (double)tile_sum;
-                    __syncwarp();   // my_lse is rewritten for the next tile
+                    // fp32 over the tiles of one query head, fp64 across heads
+                    run += tile_sum;
+                    if (sp.qt == p.nt - 1) {
+                        acc += (double)run;
+                        run = 0.f;
+                    }
+                    __syncwarp();   // every lane has read the slot
+                    if (lane == 0)
+                        mbar_arrive(&l_empty[ls]);
                 }
             }
             if (!ok)
                 break;
-            if (gi < p.L) {
+            // merge the two column halves of each row: the second half hands its
+            // state over through shared memory (bounded waits both ways)
+            double *mq = merge + quarter * 32;
+            if (half == 1) {
+                const bool drained = n_item == 0 ||
+                                  mbar_sleep_or_abort(&mrg_empty[quarter], (n_item - 1) & 1, abort);
+                if (!__all_sync(0xffffffffu, drained))
+                    break;
                 if (PASS == 1)
-                    p.lse2[(size_t)bh * p.Lpad + gi] = m + __log2f(l);
+                    reinterpret_cast<float2 *>(mq)[lane] = make_float2(m, l);
                 else
-                    p.scores[(size_t)unit * p.C + gi] = (float)acc;
+                    mq[lane] = acc;
+                mbar_arrive(&mrg_full[quarter]);
+            } else {
+                const bool ready = mbar_sleep_or_abort(&mrg_full[quarter], n_item & 1, abort);
+                if (!__all_sync(0xffffffffu, ready))
+                    break;
+                double other = mq[lane];
+                mbar_arrive(&mrg_empty[quarter]);
+                if (gi < p.L) {
+                    if (PASS == 1) {
+                        const float2 o = *reinterpret_cast<const float2 *>(&other);
+                        const float mm = fmaxf(m, o.x);
+                        const float ll = l * ex2o(m - mm) + o.y * ex2o(o.x - mm);
+                        p.nlse[(size_t)bh * p.Lpad + gi] = -(mm + __log2f(ll));
+                    } else {
+                        p.scores[(size_t)unit * p.C + gi] = (float)(acc + other);
+                    }
+                }
             }
         }
     }
@@ -466,7 +548,7 @@ template <int D> cudaError_t prefill_tc_impl(const kvc_h2o_args &a, float *lse_w
     tp.npairs = (tp.nt + 1) / 2;
     tp.kp_cap = a.kp_cap;
     tp.C = a.C;
-    tp.lse2 = lse_ws;
+    tp.nlse = lse_ws;
     tp.scores = a.scores;
     const float scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / sqrtf((float)a.D);
     tp.scale_log2 = scale * LOG2E;

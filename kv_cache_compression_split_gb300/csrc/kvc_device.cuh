@@ -111,6 +111,41 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parit
     }
 }
 
+// As mbar_wait_or_abort, for a thread with nothing else to do: each try_wait
+// asks to sleep up to SLEEP_HINT_NS until the phase completes, so waiting
+// threads do not take issue slots from the warps that work.
+constexpr uint32_t SLEEP_HINT_NS = 20000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(SLEEP_HINT_NS)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_sleep_or_abort(uint64_t *bar, uint32_t parity,
+                                                    volatile int *abort)
+{
+    if (mbar_try_wait_sleep(bar, parity))
+        return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity))
+            return true;
+        if (*abort)
+            return false;
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
@@ -318,29 +353,33 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64])
 
 // ---------------------------------------------------------------- packed fp32
 
-__device__ __forceinline__ uint64_t f2_bits(float2 a)
-{
-    return (uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32);
-}
-
-__device__ __forceinline__ float2 f2_from_bits(uint64_t d)
-{
-    return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
-}
-
-// a * b + c on both halves, rounded to nearest (one fma.rn.f32x2).
+// a * b + c on both halves, rounded to nearest (one fma.rn.f32x2; the pairs are
+// formed with vector moves, which cost nothing when the registers are adjacent).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
 {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
-    return f2_from_bits(d);
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
 }
 
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b)
 {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-    return f2_from_bits(d);
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
 }
 
 // max of three (one max.f32 with three sources).
