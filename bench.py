@@ -109,7 +109,7 @@ def slot_bytes(n_slots, B, Hkv, Hq, D):
 
 # DRAM bytes (read + write) per (sequence, KV head) unit and cached token that ncu measured
 # for k_attend_slots on the FP16 cache (64-sequence case of the heavy-load workload:
-# dram__bytes_read.sum + dram__bytes_write.sum = 542.1 MB over 64 x 8 units x 2048 tokens).
+# dram__bytes_read.sum + dram__bytes_write.sum = 538.0 + 4.1 MB over 64 x 8 units x 2048 tokens).
 SLOT_ATTEND_DRAM_BYTES_PER_UNIT_TOKEN = 542.1e6 / (64 * 8 * 2048)
 
 
