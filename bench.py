@@ -390,7 +390,9 @@ def run_gpu(args, rank, world):
     h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
     d2h = host_out[0].numel() * host_out[0].element_size()
 
-    # ---------------- random eviction rows (reasoning-trace shape), timed in the same run
+    # ---------------- H2O variants and random eviction rows, timed in the same run
+    rows.update(h2o_variant_rows(kvc, dev, stream, h2o, h2o_scores, qs[:, 1], kn[:, 1], vn[:, 1],
+                                 n_heavy, n_recent))
     rows.update(random_rows(kvc, W, dev, stream))
 
     ms_per_step = total_ms / args.steps
@@ -408,6 +410,59 @@ def run_gpu(args, rank, world):
         "splits": {"fp16": nb_fp, "h2o": nb_h2o, "stream": nb_st, "kivi": nb_kv},
     }
     return res
+
+
+def h2o_variant_rows(kvc, dev, stream, src, src_scores, qs, kn, vn, n_heavy, n_recent):
+    """The two H2O variants of "Practical Online KV Cache Compaction for LLM Agents" on the
+    heavy-load H2O-512 state: the decayed activity score (decay 0.99, §4.1) with an eviction every
+    step, and batched eviction (trigger at 110% of the 512 budget, §5.2) with plain scores.  Each
+    step is append + attention with the fused score update (+ eviction); two full trigger cycles
+    (2 x 51 steps) are timed, so the batched row's cost is amortised over its compactions."""
+    import torch
+    B, Hkv, _, D = src.K.shape
+    Hq = qs.shape[2]
+    budget = n_heavy + n_recent
+    trigger = (11 * budget + 9) // 10           # first count above 110%: 564 for 512
+    steps = 2 * (trigger - budget)
+    C = trigger + 8
+    out = {}
+    with torch.cuda.stream(stream):
+        o = torch.empty(B, Hq, D, dtype=torch.float16, device=dev)
+        logits = torch.empty(B, Hq, C, dtype=torch.float32, device=dev)
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+        for name, decay, trig in (("h2o512_decay", 0.99, None), ("h2o512_batched", 0.0, trigger)):
+            c = kvc.SlotCache.empty(B, Hkv, C, D, device=dev)
+            c.K[:, :, :budget] = src.K[:, :, :budget]
+            c.V[:, :, :budget] = src.V[:, :, :budget]
+            c.pos[:, :, :budget] = src.pos[:, :, :budget]
+            c.n.copy_(src.n)
+            c.seqlen.copy_(src.seqlen)
+            sc = torch.zeros(B, Hkv, C, dtype=torch.float32, device=dev)
+            sc[:, :, :budget] = src_scores[:, :, :budget]
+            ws = torch.empty(max(kvc.kvc_workspace_size(c, qs[0], 1) // 4, 1), dtype=torch.float32,
+                             device=dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for i in range(steps):
+                k = i % qs.shape[0]
+                kvc.kvc_append(c, kn[k], vn[k], stream=stream)
+                kvc.kvc_decode_attend(c, qs[k], o, logits=logits, lse=lse, workspace=ws,
+                                      num_splits=1, h2o_scores=sc, h2o_decay=decay, stream=stream)
+                if trig is None:
+                    kvc.kvc_h2o_evict(c, sc, n_heavy, n_recent, stream=stream)
+                else:
+                    kvc.kvc_h2o_evict_when(c, sc, n_heavy, n_recent, trig, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / steps
+            out[name] = {"ms_per_step": ms, "tokens_per_s": B / (ms * 1e-3), "steps": steps,
+                         "shape": f"B={B} GQA {Hq}/{Hkv} D={D}, budget {budget}" +
+                                  (f", decay {decay}, evict every step" if trig is None else
+                                   f", evict when n >= {trig} (slots attended {budget + 1}.."
+                                   f"{trig})")}
+            del c, sc, ws
+    return out
 
 
 def random_rows(kvc, W, dev, stream):

@@ -184,9 +184,11 @@ enum { KVC_KIND_SLOTS = 0, KVC_KIND_KIVI = 1 };
  *   num_splits  KV splits per unit (0 = chosen from the SM count)
  *   softmax_scale 0 for 1/sqrt(D)
  *   h2o_scores  optional [B, Hkv, C] fp32 (slot caches only; needs logits and
- *               lse): the step's attention probabilities are added to the
+ *               lse): the step's attention probabilities are folded into the
  *               heavy-hitter scores in the same launch, exactly as
- *               kvc_h2o_accumulate(KVC_H2O_DECODE) would add them
+ *               kvc_h2o_accumulate(KVC_H2O_DECODE) with decay h2o_decay would
+ *   h2o_decay   0 (plain H2O, scores += p) or lambda in (0, 1) (decayed
+ *               scores = lambda * scores + (1 - lambda) * p); see kvc_h2o_args
  */
 typedef struct kvc_attend_args {
     int kind;
@@ -202,6 +204,7 @@ typedef struct kvc_attend_args {
     int num_splits;
     float softmax_scale;
     float *h2o_scores;
+    float h2o_decay;
 } kvc_attend_args;
 
 /* Workspace bytes kvc_decode_attend needs for these arguments (0 if none). */
@@ -250,9 +253,16 @@ enum { KVC_H2O_DECODE = 0, KVC_H2O_PREFILL = 1 };
 /*
  * H2O score arguments.
  *   scores   [B, Hkv, C] fp32, one accumulated score per slot
- * DECODE:  scores[b,hk,j] += sum over the query heads h of KV head hk of
+ * DECODE:  p[b,hk,j] = sum over the query heads h of KV head hk of
  *          exp(logits[b,h,j] - lse[b,h]) for j < n[b,hk]  (logits, lse from
- *          kvc_decode_attend; n [B, Hkv])
+ *          kvc_decode_attend; n [B, Hkv]), then
+ *            decay == 0:          scores[b,hk,j] += p[b,hk,j]
+ *            0 < decay < 1:       scores[b,hk,j] = decay * scores[b,hk,j]
+ *                                                  + (1 - decay) * p[b,hk,j]
+ *          The decayed form is the incremental activity score
+ *          A_i <- lambda A_i + (1 - lambda) attn_i (lambda = 0.99 on the page) of
+ *          "Practical Online KV Cache Compaction for LLM Agents", §4.1; PREFILL
+ *          ignores decay.
  * PREFILL: scores[b,hk,j] = sum over the query heads h of hk, and over prompt
  *          rows i >= j, of softmax_i(scale * qp[b,h,i] . kp[b,hk,.])_j for
  *          j < L (causal prompt of L tokens); qp [B, Hq, L, D] fp16, kp the
@@ -273,6 +283,7 @@ typedef struct kvc_h2o_args {
     void *workspace;
     size_t workspace_bytes;
     float softmax_scale;
+    float decay;
 } kvc_h2o_args;
 
 KVC_API size_t kvc_h2o_workspace_size(const kvc_h2o_args *args);
@@ -300,6 +311,19 @@ KVC_API kvc_status kvc_h2o_accumulate(const kvc_h2o_args *args, cudaStream_t str
  */
 KVC_API kvc_status kvc_h2o_evict(const kvc_slot_cache *cache, float *scores, int n_heavy, int n_recent,
                          cudaStream_t stream);
+
+/*
+ * kvc_h2o_evict_when -- batched H2O eviction: exactly kvc_h2o_evict for the
+ * units with n[b,hk] >= trigger; every other unit is left unchanged.  With
+ * trigger = 1.1 x (n_heavy + n_recent) a unit is compacted once every ~10% of
+ * the budget in new tokens instead of at every step ("Practical Online KV
+ * Cache Compaction for LLM Agents", §5.2: compact when the cache passes 110% of
+ * its target, or every K = 50 tokens).  The check runs on the device, so the
+ * call never reads n back and can sit in a captured graph.  trigger must be
+ * > 0; a trigger at or below n_heavy + n_recent is kvc_h2o_evict.
+ */
+KVC_API kvc_status kvc_h2o_evict_when(const kvc_slot_cache *cache, float *scores, int n_heavy,
+                              int n_recent, int trigger, cudaStream_t stream);
 
 /*
  * kvc_stream_evict -- StreamingLLM: keep positions < n_sink and positions

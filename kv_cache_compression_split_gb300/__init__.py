@@ -53,7 +53,8 @@ class AttendArgs(C.Structure):
                 ("slots", C.POINTER(SlotCacheDesc)), ("quant", C.POINTER(QuantCacheDesc)),
                 ("logits", C.c_void_p), ("lse", C.c_void_p), ("workspace", C.c_void_p),
                 ("workspace_bytes", C.c_size_t), ("num_splits", C.c_int),
-                ("softmax_scale", C.c_float), ("h2o_scores", C.c_void_p)]
+                ("softmax_scale", C.c_float), ("h2o_scores", C.c_void_p),
+                ("h2o_decay", C.c_float)]
 
 
 class H2OArgs(C.Structure):
@@ -61,7 +62,8 @@ class H2OArgs(C.Structure):
                 ("D", C.c_int), ("C", C.c_int), ("scores", C.c_void_p), ("logits", C.c_void_p),
                 ("lse", C.c_void_p), ("n", C.c_void_p), ("L", C.c_int), ("qp", C.c_void_p),
                 ("kp", C.c_void_p), ("kp_cap", C.c_int), ("workspace", C.c_void_p),
-                ("workspace_bytes", C.c_size_t), ("softmax_scale", C.c_float)]
+                ("workspace_bytes", C.c_size_t), ("softmax_scale", C.c_float),
+                ("decay", C.c_float)]
 
 
 def lib():
@@ -84,6 +86,7 @@ def lib():
                 "kvc_h2o_workspace_size": (C.c_size_t, [C.POINTER(H2OArgs)]),
                 "kvc_h2o_accumulate": (st, [C.POINTER(H2OArgs), P]),
                 "kvc_h2o_evict": (st, [C.POINTER(SlotCacheDesc), P, i, i, P]),
+                "kvc_h2o_evict_when": (st, [C.POINTER(SlotCacheDesc), P, i, i, i, P]),
                 "kvc_stream_evict": (st, [C.POINTER(SlotCacheDesc), i, i, P]),
                 "kvc_random_evict": (st, [C.POINTER(SlotCacheDesc), i, C.c_double, C.c_uint64,
                                           C.c_uint32, P]),
@@ -144,7 +147,7 @@ def kvc_append_quant(cache: "QuantCache", k_new, v_new, stream=None):
 
 
 def _attend_args(cache, q, o, logits=None, lse=None, workspace=None, num_splits=0, scale=0.0,
-                 h2o_scores=None):
+                 h2o_scores=None, h2o_decay=0.0):
     a = AttendArgs()
     keep = []
     if isinstance(cache, SlotCache):
@@ -165,6 +168,7 @@ def _attend_args(cache, q, o, logits=None, lse=None, workspace=None, num_splits=
     a.num_splits = int(num_splits)
     a.softmax_scale = float(scale)
     a.h2o_scores = _ptr(h2o_scores)
+    a.h2o_decay = float(h2o_decay)
     return a, keep
 
 
@@ -174,9 +178,10 @@ def kvc_workspace_size(cache, q, num_splits: int = 0) -> int:
 
 
 def kvc_decode_attend(cache, q, o, logits=None, lse=None, workspace=None, num_splits: int = 0,
-                      softmax_scale: float = 0.0, h2o_scores=None, stream=None):
+                      softmax_scale: float = 0.0, h2o_scores=None, h2o_decay: float = 0.0,
+                      stream=None):
     a, _keep = _attend_args(cache, q, o, logits, lse, workspace, num_splits, softmax_scale,
-                            h2o_scores)
+                            h2o_scores, h2o_decay)
     _check(lib().kvc_decode_attend(C.byref(a), _stream(stream)), "kvc_decode_attend")
 
 
@@ -191,7 +196,7 @@ def kvc_decode_attend_noalloc(cache, q, o, logits=None, lse=None, num_splits: in
 
 
 def _h2o_args(mode, B, Hq, Hkv, D, Cc, scores, logits=None, lse=None, n=None, L=0, qp=None,
-              kp=None, kp_cap=0, workspace=None, scale=0.0):
+              kp=None, kp_cap=0, workspace=None, scale=0.0, decay=0.0):
     a = H2OArgs()
     a.mode, a.B, a.Hq, a.Hkv, a.D, a.C = mode, B, Hq, Hkv, D, Cc
     a.scores, a.logits, a.lse, a.n = _ptr(scores), _ptr(logits), _ptr(lse), _ptr(n)
@@ -199,6 +204,7 @@ def _h2o_args(mode, B, Hq, Hkv, D, Cc, scores, logits=None, lse=None, n=None, L=
     a.workspace = _ptr(workspace)
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     a.softmax_scale = float(scale)
+    a.decay = float(decay)
     return a
 
 
@@ -207,9 +213,10 @@ def kvc_h2o_workspace_size(B: int, Hq: int, L: int) -> int:
     return int(lib().kvc_h2o_workspace_size(C.byref(a)))
 
 
-def kvc_h2o_accumulate_decode(cache: "SlotCache", scores, logits, lse, Hq: int, stream=None):
+def kvc_h2o_accumulate_decode(cache: "SlotCache", scores, logits, lse, Hq: int,
+                              decay: float = 0.0, stream=None):
     a = _h2o_args(KVC_H2O_DECODE, cache.B, Hq, cache.Hkv, cache.D, cache.C, scores, logits, lse,
-                  cache.n)
+                  cache.n, decay=decay)
     _check(lib().kvc_h2o_accumulate(C.byref(a), _stream(stream)), "kvc_h2o_accumulate")
 
 
@@ -229,6 +236,13 @@ def kvc_h2o_evict(cache: "SlotCache", scores, n_heavy: int, n_recent: int, strea
     d = cache.desc()
     _check(lib().kvc_h2o_evict(C.byref(d), _ptr(scores), n_heavy, n_recent, _stream(stream)),
            "kvc_h2o_evict")
+
+
+def kvc_h2o_evict_when(cache: "SlotCache", scores, n_heavy: int, n_recent: int, trigger: int,
+                       stream=None):
+    d = cache.desc()
+    _check(lib().kvc_h2o_evict_when(C.byref(d), _ptr(scores), n_heavy, n_recent, int(trigger),
+                                    _stream(stream)), "kvc_h2o_evict_when")
 
 
 def kvc_stream_evict(cache: "SlotCache", n_sink: int, n_recent: int, stream=None):

@@ -269,6 +269,9 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         return KVC_ERR_UNSUPPORTED;
     if (a->h2o_scores && (!a->logits || !a->lse))
         return KVC_ERR_INVALID_ARG;
+    float h2o_keep = 1.f, h2o_add = 1.f;
+    if (!h2o_decay_weights(a->h2o_decay, &h2o_keep, &h2o_add))
+        return KVC_ERR_INVALID_ARG;
     if (f.ws > 0 && (!a->workspace || a->workspace_bytes < f.ws || !aligned16(a->workspace)))
         return KVC_ERR_WORKSPACE;
     const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / sqrtf((float)f.D);
@@ -278,7 +281,7 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         float *part_ml = part_o ? part_o + (size_t)f.B * a->Hq * f.plan.splits * f.D : nullptr;
         AttendLaunch L{f.B, a->Hq, c.Hkv, c.D, c.C, a->q, a->o, c.K, c.V, c.n, a->logits, a->lse,
                        part_o, part_ml, f.plan.splits, f.plan.tiles_per_split, scale,
-                       a->h2o_scores};
+                       a->h2o_scores, h2o_keep, h2o_add};
         cudaError_t e = launch_attend_slots(L, stream);
         if (e != cudaSuccess || !a->h2o_scores || f.plan.splits == 1)
             return from_cuda(e);
@@ -294,6 +297,7 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         h.logits = a->logits;
         h.lse = a->lse;
         h.n = c.n;
+        h.decay = a->h2o_decay;
         return from_cuda(launch_h2o_decode_acc(h, stream));
     }
     const kvc_quant_cache &c = *a->quant;
@@ -319,7 +323,8 @@ kvc_status kvc_h2o_accumulate(const kvc_h2o_args *a, cudaStream_t stream)
     if (a->Hq % a->Hkv != 0)
         return KVC_ERR_INVALID_ARG;
     if (a->mode == KVC_H2O_DECODE) {
-        if (!a->logits || !a->lse || !a->n)
+        float keep, add;
+        if (!a->logits || !a->lse || !a->n || !h2o_decay_weights(a->decay, &keep, &add))
             return KVC_ERR_INVALID_ARG;
         return from_cuda(launch_h2o_decode_acc(*a, stream));
     }
@@ -364,6 +369,24 @@ kvc_status kvc_h2o_evict(const kvc_slot_cache *cache, float *scores, int n_heavy
     e.scores = scores;
     e.n_heavy = n_heavy;
     e.n_recent = n_recent;
+    return from_cuda(launch_evict(e, stream));
+}
+
+kvc_status kvc_h2o_evict_when(const kvc_slot_cache *cache, float *scores, int n_heavy,
+                              int n_recent, int trigger, cudaStream_t stream)
+{
+    kvc_status st = evict_common(cache);
+    if (st != KVC_OK)
+        return st;
+    if (!scores || n_heavy < 0 || n_recent < 0 || trigger <= 0)
+        return KVC_ERR_INVALID_ARG;
+    EvictLaunch e{};
+    e.kind = EVICT_H2O;
+    e.c = *cache;
+    e.scores = scores;
+    e.n_heavy = n_heavy;
+    e.n_recent = n_recent;
+    e.trigger = trigger;
     return from_cuda(launch_evict(e, stream));
 }
 

@@ -51,6 +51,7 @@ struct SlotParams {
     float *part_o, *part_ml;
     float scale, scale_log2;
     float *h2o_scores;              // optional: add this step's probabilities (one split)
+    float h2o_keep, h2o_add;        // scores = keep * scores + add * p
     int *status;
 };
 
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             for (int u = 0; u < U; ++u) {
                 const int j = j0 + u * NCW * 32;
                 if (j < t_end)
-                    sc[j] = old[u] + add[u];
+                    sc[j] = fmaf(old[u], p.h2o_keep, add[u] * p.h2o_add);
             }
         }
     }
@@ -412,6 +413,8 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
     sp.scale = a.scale;
     sp.scale_log2 = a.scale * LOG2E;
     sp.h2o_scores = a.splits == 1 ? a.h2o_scores : nullptr;
+    sp.h2o_keep = a.h2o_keep;
+    sp.h2o_add = a.h2o_add;
     sp.status = dev_status_ptr();
     const int grid = units * a.splits;
     cudaError_t e = a.D == 128 ? launch_slots_impl<128>(tk, tv, sp, grid, s)

@@ -37,6 +37,7 @@ struct EvictParams {
     const int32_t *seqlen;
     float *scores;
     int n_heavy, n_recent, n_sink, prompt_len;
+    int trigger;        // H2O: units with n < trigger are left unchanged
     double keep_ratio;
     uint32_t seed_lo, seed_hi, epoch;
     int *status;
@@ -188,6 +189,8 @@ __global__ void __launch_bounds__(ETHREADS) k_evict(const EvictParams p)
             flag_error(p.status, DEV_CAPACITY);
         return;
     }
+    if (KIND == EVICT_H2O && n < p.trigger)
+        return;   // batched eviction: this unit has not reached its trigger
     const long T = p.seqlen[b];
     const int32_t *pos = p.pos + (size_t)unit * p.C;
     float *sc = p.scores ? p.scores + (size_t)unit * p.C : nullptr;
@@ -422,6 +425,8 @@ __global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams 
             flag_error(p.status, DEV_CAPACITY);
         return;
     }
+    if (KIND == EVICT_H2O && n < p.trigger)
+        return;   // batched eviction: this unit has not reached its trigger
     const long T = p.seqlen[unit / p.Hkv];
     const int32_t *pos = p.pos + (size_t)unit * p.C;
     float *sc = p.scores ? p.scores + (size_t)unit * p.C : nullptr;
@@ -569,6 +574,7 @@ cudaError_t launch_evict(const EvictLaunch &e, cudaStream_t s)
     p.n_recent = e.n_recent;
     p.n_sink = e.n_sink;
     p.prompt_len = e.prompt_len;
+    p.trigger = e.trigger;
     p.keep_ratio = e.keep_ratio;
     p.seed_lo = (uint32_t)(e.seed & 0xffffffffu);
     p.seed_hi = (uint32_t)(e.seed >> 32);

@@ -44,6 +44,7 @@ struct AttendLaunch {
     int splits, tiles_per_split;
     float scale;
     float *h2o_scores;
+    float h2o_keep, h2o_add;   // scores = keep * scores + add * p
 };
 cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s);
 
@@ -69,6 +70,10 @@ cudaError_t launch_append_slots(const kvc_slot_cache &c, const uint16_t *k_new,
 cudaError_t launch_append_quant(const kvc_quant_cache &c, const uint16_t *k_new,
                                 const uint16_t *v_new, int n_new, cudaStream_t s);
 
+// Weights of the decode score update scores = keep * scores + add * p for a
+// decay of 0 (plain: 1, 1) or lambda in (0, 1) (lambda, 1 - lambda); false
+// for any other decay.
+bool h2o_decay_weights(float decay, float *keep, float *add);
 cudaError_t launch_h2o_decode_acc(const kvc_h2o_args &a, cudaStream_t s);
 // Two tcgen05 passes over the causal prompt; lse_ws holds B*Hq*ceil(L/128)*128 floats.
 cudaError_t launch_h2o_prefill(const kvc_h2o_args &a, float *lse_ws, cudaStream_t s);
@@ -79,6 +84,7 @@ struct EvictLaunch {
     kvc_slot_cache c;
     float *scores;
     int n_heavy, n_recent, n_sink, prompt_len;
+    int trigger;   // H2O: only units with n >= trigger are evicted (0: all)
     double keep_ratio;
     uint64_t seed;
     uint32_t epoch;

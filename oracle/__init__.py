@@ -58,7 +58,7 @@ def _L():
                 "orc_kivi_pack_group": (None, [i, i, i, P, P, P, P, P, P, P, P]),
                 "orc_kivi_attend_unit": (None, [i, i, i, l, l, P, P, P, P, P, P, P, P, P, d, P, P]),
                 "orc_h2o_prefill_scores": (None, [i, i, i, i, i, l, l, P, P, d, P, i]),
-                "orc_h2o_accumulate": (None, [i, i, i, i, P, P, P, P]),
+                "orc_h2o_accumulate": (None, [i, i, i, i, P, P, P, C.c_double, P]),
                 "orc_h2o_keep": (i, [i, P, P, l, i, i, P, P]),
                 "orc_stream_keep": (i, [i, P, l, i, i, P]),
                 "orc_philox4x32_10": (None, [P, P, P]),
@@ -236,15 +236,17 @@ def h2o_prefill_scores(Qp, Kp, L: int, scale: float | None = None, threads: int 
     return scores
 
 
-def h2o_accumulate(scores, logits, lse, n):
-    """scores[b,hk,j] += sum_{h in group(hk)} exp(logits[b,h,j] - lse[b,h]) for j < n[b,hk]."""
+def h2o_accumulate(scores, logits, lse, n, decay: float = 0.0):
+    """p[b,hk,j] = sum_{h in group(hk)} exp(logits[b,h,j] - lse[b,h]) for j < n[b,hk];
+    decay 0: scores += p; decay in (0, 1): scores = decay * scores + (1 - decay) * p."""
     scores = np.ascontiguousarray(np.array(scores, dtype=np.float64))
     logits = np.ascontiguousarray(np.asarray(logits, dtype=np.float64))
     lse = np.ascontiguousarray(np.asarray(lse, dtype=np.float64))
     B, Hkv, Cc = scores.shape
     Hq = logits.shape[1]
     n = _i32(n).reshape(B, Hkv)
-    _L().orc_h2o_accumulate(B, Hq, Hkv, Cc, _ptr(n), _ptr(logits), _ptr(lse), _ptr(scores))
+    _L().orc_h2o_accumulate(B, Hq, Hkv, Cc, _ptr(n), _ptr(logits), _ptr(lse), float(decay),
+                            _ptr(scores))
     return scores
 
 

@@ -520,24 +520,35 @@ ORC_API void orc_h2o_prefill_scores(int B, int Hq, int Hkv, int D, int L, long k
 }
 
 /*
- * Decode accumulation: for every valid slot j of unit (b, hk),
- *   score[j] += sum over the unit's query heads h of exp(logit[h][j] - lse[h]).
+ * Decode accumulation: for every valid slot j of unit (b, hk), with
+ *   p[j] = sum over the unit's query heads h of exp(logit[h][j] - lse[h]),
+ * decay == 0 (plain H2O, "Rethinking KV Cache Compression" §16):
+ *   score[j] += p[j];
+ * 0 < decay < 1 (the incremental activity score A_i <- lambda A_i +
+ * (1 - lambda) attn_i of "Practical Online KV Cache Compaction for LLM
+ * Agents", §4.1, with attn_i summed over the KV head's query group):
+ *   score[j] = decay * score[j] + (1 - decay) * p[j].
  * logits [B,Hq,C] f64 and lse [B,Hq] are the oracle's own attention outputs.
  */
 ORC_API void orc_h2o_accumulate(int B, int Hq, int Hkv, int C, const int32_t *n,
-                                const double *logits, const double *lse, double *scores)
+                                const double *logits, const double *lse, double decay,
+                                double *scores)
 {
     int g = Hq / Hkv;
     for (int b = 0; b < B; ++b)
         for (int hk = 0; hk < Hkv; ++hk) {
             int nn = n[b * Hkv + hk];
             double *sc = scores + ((size_t)b * Hkv + hk) * C;
-            for (int hh = 0; hh < g; ++hh) {
-                int h = hk * g + hh;
-                const double *lg = logits + ((size_t)b * Hq + h) * C;
-                double ls = lse[(size_t)b * Hq + h];
-                for (int j = 0; j < nn; ++j)
-                    sc[j] += exp(lg[j] - ls);
+            for (int j = 0; j < nn; ++j) {
+                double p = 0.0;
+                for (int hh = 0; hh < g; ++hh) {
+                    int h = hk * g + hh;
+                    p += exp(logits[((size_t)b * Hq + h) * C + j] - lse[(size_t)b * Hq + h]);
+                }
+                if (decay == 0.0)
+                    sc[j] += p;
+                else
+                    sc[j] = decay * sc[j] + (1.0 - decay) * p;
             }
         }
 }

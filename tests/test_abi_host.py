@@ -58,6 +58,20 @@ def test_null_arguments_are_rejected_without_touching_a_gpu(kvc):
     assert lib.kvc_stream_evict(ctypes.byref(d), 1, 1, None) == kvc.KVC_ERR_INVALID_ARG
     q = kvc.QuantCacheDesc(1, 1, 128, 3, 16, 32, 16, 16, 16, 16, 16)
     assert lib.kvc_append_quant(ctypes.byref(q), None, None, 0, None) == kvc.KVC_ERR_UNSUPPORTED
+    # batched H2O eviction: null cache, and a trigger that is not positive
+    assert lib.kvc_h2o_evict_when(None, None, 64, 448, 563, None) == kvc.KVC_ERR_INVALID_ARG
+    d = kvc.SlotCacheDesc(1, 1, 128, 16, 16, 16, 16, 16, 16)
+    assert lib.kvc_h2o_evict_when(ctypes.byref(d), 16, 64, 448, 0, None) == kvc.KVC_ERR_INVALID_ARG
+    # decay outside {0} U (0, 1) is refused before anything is launched
+    for bad in (1.0, 1.5, -0.1, float("nan")):
+        h = kvc._h2o_args(kvc.KVC_H2O_DECODE, 1, 1, 1, 128, 16, None, decay=bad)
+        h.scores = h.logits = h.lse = h.n = 16
+        assert lib.kvc_h2o_accumulate(ctypes.byref(h), None) == kvc.KVC_ERR_INVALID_ARG, bad
+        a = kvc.AttendArgs()
+        a.kind, a.Hq, a.q, a.o, a.slots = kvc.KVC_KIND_SLOTS, 1, 16, 16, ctypes.pointer(d)
+        a.logits = a.lse = a.h2o_scores = 16
+        a.h2o_decay = bad
+        assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_INVALID_ARG, bad
 
 
 def test_product_path_does_not_import_the_oracle():

@@ -133,13 +133,17 @@ def test_h2o_prefill_scores_and_evict(kvc, orc, B, Hq, Hkv, L, D, n_heavy, n_rec
     assert device_status_clean(kvc)
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,D,fused,splits", [(4, 64, 8, 128, False, 0),
-                                                     (3, 8, 8, 64, False, 0),
-                                                     (4, 64, 8, 128, True, 1),
-                                                     (3, 8, 8, 64, True, 3)])
-def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, fused, splits):
+@pytest.mark.parametrize("B,Hq,Hkv,D,fused,splits,decay", [(4, 64, 8, 128, False, 0, 0.0),
+                                                           (3, 8, 8, 64, False, 0, 0.0),
+                                                           (4, 64, 8, 128, True, 1, 0.0),
+                                                           (3, 8, 8, 64, True, 3, 0.0),
+                                                           (4, 64, 8, 128, True, 1, 0.99),
+                                                           (3, 8, 8, 64, False, 0, 0.9),
+                                                           (3, 8, 8, 64, True, 3, 0.99)])
+def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, fused, splits, decay):
     """One decode step from a seeded post-prefill state: 64 heavy slots from [0, 1600) plus the
-    recent 448; append token 2048, attend over 513 slots, accumulate, evict back to 512."""
+    recent 448; append token 2048, attend over 513 slots, accumulate (plain, or the decayed
+    activity score with decay lambda), evict back to 512."""
     T, n_heavy, n_recent = 2048, 64, 448
     g = torch.Generator().manual_seed(B * Hq)
     rng = np.random.default_rng(B * Hq)
@@ -173,11 +177,11 @@ def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, fused, splits):
                      device="cuda")
     if fused:   # probabilities added to the scores by the attention launch itself
         kvc.kvc_decode_attend(cache, q.cuda(), o, logits=logits, lse=lse, workspace=ws,
-                              num_splits=splits, h2o_scores=scores)
+                              num_splits=splits, h2o_scores=scores, h2o_decay=decay)
     else:
         kvc.kvc_decode_attend(cache, q.cuda(), o, logits=logits, lse=lse, workspace=ws,
                               num_splits=splits)
-        kvc.kvc_h2o_accumulate_decode(cache, scores, logits, lse, Hq)
+        kvc.kvc_h2o_accumulate_decode(cache, scores, logits, lse, Hq, decay=decay)
     scores_after_acc = scores.clone()
     kvc.kvc_h2o_evict(cache, scores, n_heavy, n_recent)
     torch.cuda.synchronize()
@@ -189,7 +193,8 @@ def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, fused, splits):
                                                want_logits=True)
     assert_o_close(np16(o), ref_o)
     sc_ref = np.concatenate([sc0[..., :512].astype(np.float64), np.zeros((B, Hkv, 1))], axis=2)
-    sc_ref = orc.h2o_accumulate(sc_ref, ref_lg, ref_lse, np.full((B, Hkv), 513))
+    sc_ref = orc.h2o_accumulate(sc_ref, ref_lg, ref_lse, np.full((B, Hkv), 513),
+                                decay=float(np.float32(decay)))
     np.testing.assert_allclose(scores_after_acc.cpu().numpy()[..., :513], sc_ref,
                                rtol=SCORE_REL_TOL)
     n, pos, _, _ = _units(cache)
@@ -200,6 +205,63 @@ def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, fused, splits):
             _check_keep_with_ties(pos[b, hk, :512], pos513[b, hk], sc_ref[b, hk], T + 1, n_heavy,
                                   n_recent)
             _assert_content(cache, Kseq, Vseq, b, hk, pos[b, hk, :512])
+    assert device_status_clean(kvc)
+
+
+@pytest.mark.parametrize("C", [600, 1100])   # warp-per-unit and CTA-per-unit kernels
+def test_h2o_evict_when_trigger(kvc, orc, C):
+    """Batched H2O eviction ("Practical Online KV Cache Compaction for LLM Agents", §5.2): units
+    at or above the trigger (here 563 = 110% of a 512 budget) compact to 64 heavy + 448 recent
+    exactly as kvc_h2o_evict would; units below it stay bit-identical."""
+    B, Hkv, D, T = 2, 4, 128, 3000
+    n_heavy, n_recent, trigger = 64, 448, 563
+    counts = np.array([[512, 562, 563, 600], [570, 540, 563, 513]], np.int32)
+    rng = np.random.default_rng(563)
+    g = torch.Generator().manual_seed(563)
+    Kseq = torch.randn(B, Hkv, T, D, generator=g).half()
+    Vseq = torch.randn(B, Hkv, T, D, generator=g).half()
+    cache = kvc.SlotCache.empty(B, Hkv, C, D)
+    pos0 = np.zeros((B, Hkv, C), np.int32)
+    sc0 = np.zeros((B, Hkv, C), np.float32)
+    for b in range(B):
+        for hk in range(Hkv):
+            nn = counts[b, hk]
+            heavy = np.sort(rng.choice(T - n_recent, nn - n_recent, replace=False))
+            p = rng.permutation(np.concatenate([heavy, np.arange(T - n_recent, T)]))
+            pos0[b, hk, :nn] = p
+            sc0[b, hk, :nn] = rng.uniform(0.0, 4.0, nn).astype(np.float32)
+    pos_t = torch.from_numpy(pos0).long()
+    cache.K.copy_(torch.gather(Kseq, 2, pos_t[..., None].expand(-1, -1, -1, D)).cuda())
+    cache.V.copy_(torch.gather(Vseq, 2, pos_t[..., None].expand(-1, -1, -1, D)).cuda())
+    cache.pos.copy_(torch.from_numpy(pos0).cuda())
+    cache.n.copy_(torch.from_numpy(counts).cuda())
+    cache.seqlen.fill_(T)
+    scores = torch.from_numpy(sc0).cuda()
+    K_before, V_before = cache.K.clone(), cache.V.clone()
+    kvc.kvc_h2o_evict_when(cache, scores, n_heavy, n_recent, trigger)
+    torch.cuda.synchronize()
+    n, pos, _, _ = _units(cache)
+    sc = scores.cpu().numpy()
+    for b in range(B):
+        for hk in range(Hkv):
+            nn = counts[b, hk]
+            if nn < trigger:
+                assert n[b, hk] == nn
+                assert np.array_equal(pos[b, hk], pos0[b, hk])
+                assert np.array_equal(sc[b, hk], sc0[b, hk])
+                assert torch.equal(cache.K[b, hk], K_before[b, hk])
+                assert torch.equal(cache.V[b, hk], V_before[b, hk])
+            else:
+                assert n[b, hk] == n_heavy + n_recent
+                _check_keep_with_ties(pos[b, hk, :512], pos0[b, hk, :nn],
+                                      sc0[b, hk, :nn].astype(np.float64), T, n_heavy, n_recent)
+                _assert_content(cache, Kseq, Vseq, b, hk, pos[b, hk, :512])
+                assert (sc[b, hk, 512:] == 0).all()
+                order = np.argsort(pos[b, hk, :512])
+                src = {int(p): s for p, s in zip(pos0[b, hk, :nn], sc0[b, hk, :nn])}
+                assert np.array_equal(sc[b, hk, :512][order],
+                                      np.array([src[int(p)] for p in pos[b, hk, :512][order]],
+                                               np.float32))
     assert device_status_clean(kvc)
 
 

@@ -81,6 +81,38 @@ def test_decode_accumulate_adds_g(orc):
             assert np.array_equal(out[b, hk, nn:], base[b, hk, nn:])
 
 
+@pytest.mark.parametrize("decay", [0.5, 0.9, 0.99])
+def test_decayed_accumulate_conservation_and_geometric_series(orc, decay):
+    """Decayed activity score ("Practical Online KV Cache Compaction for LLM Agents", §4.1):
+    A <- decay * A + (1 - decay) * p.  Pins: the group's probabilities sum to g per step, so
+    sum_j A' = decay * sum_j A + (1 - decay) * g; repeating one step k times gives the closed form
+    A_k = decay^k A_0 + (1 - decay^k) p; slots at or beyond n are untouched."""
+    rng = np.random.default_rng(31)
+    B, Hq, Hkv, C, D = 2, 8, 2, 24, 64
+    g = Hq // Hkv
+    q = rng.standard_normal((B, Hq, D)).astype(np.float16)
+    K = rng.standard_normal((B, Hkv, C, D)).astype(np.float16)
+    n = np.array([[24, 24], [9, 9]], np.int32)
+    _, lse, logits = orc.decode_attend(q, K, K, n, want_logits=True)
+    logits = np.nan_to_num(logits, nan=-np.inf)
+    base = rng.uniform(0, 3, (B, Hkv, C))
+    one = orc.h2o_accumulate(base, logits, lse, n, decay=decay)
+    p = orc.h2o_accumulate(np.zeros_like(base), logits, lse, n)   # plain: the step's p
+    acc = base.copy()
+    for _ in range(5):
+        acc = orc.h2o_accumulate(acc, logits, lse, n, decay=decay)
+    for b in range(B):
+        for hk in range(Hkv):
+            nn = n[b, hk]
+            assert one[b, hk, :nn].sum() == pytest.approx(
+                decay * base[b, hk, :nn].sum() + (1 - decay) * g, rel=1e-13)
+            np.testing.assert_allclose(
+                acc[b, hk, :nn], decay ** 5 * base[b, hk, :nn] + (1 - decay ** 5) * p[b, hk, :nn],
+                rtol=1e-12)
+            assert np.array_equal(one[b, hk, nn:], base[b, hk, nn:])
+            assert np.array_equal(acc[b, hk, nn:], base[b, hk, nn:])
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_h2o_keep_matches_full_sort(orc, seed):
     rng = np.random.default_rng(seed)
