@@ -595,6 +595,10 @@ def run_profile(args):
         ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), device=dev)
         for _ in range(3):
             kvc.kvc_decode_attend(cache, q, o, workspace=ws)
+    elif what == "kivi_pack":
+        for _ in range(3):
+            cache = kvc.QuantCache.empty(B, Hkv, T, D, 4, w.kivi_R, device=dev)
+            kvc.kvc_append_quant(cache, K, V)
     elif what == "prefill":
         L = T - 1
         qp = W.q_tensor(w, B=max(1, B // 4), L=L, device=dev)
@@ -645,6 +649,160 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_grid(args):
+    """Throughput profile grid: batch x KV length x method on the heavy-load head layout (GQA 64/8,
+    D 128), the per-method cost table a router consumes.  Per (B, T) cell and method:
+      prefill_ms  compress a T-token prompt: FP16 append; KIVI-b pack; StreamingLLM and H2O evict
+                  to 64 + 448 (H2O after its two-pass score pass); random eviction at each keep
+                  ratio with the first min(1024, T/2) tokens locked
+      decode_ms   one decode step: append + attention (+ H2O's fused score update + eviction, or
+                  StreamingLLM's eviction) over the cache the prefill left; for random eviction,
+                  attention over the kept slots
+    Every timing is the median of 3 repetitions after one warm-up, with L2 flushed (a 512 MB
+    write) before each; one JSON line per cell."""
+    import torch
+    import kv_cache_compression_split_gb300 as kvc
+    from kv_cache_compression_split_gb300 import build as kbuild
+    kbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    Hq, Hkv, D, R = 64, 8, 128, 128
+    n_heavy, n_recent, n_sink = 64, 448, 64
+    ratios = [1.0, 0.75, 0.5, 0.25, 0.125]
+    batches = [int(x) for x in args.grid_batches.split(",")]
+    lengths = [int(x) for x in args.grid_lengths.split(",")]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, setup=None, reps=3):
+        ts = []
+        for r in range(reps + 1):
+            if setup is not None:
+                setup()
+            flush.add_(1)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if r > 0:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    def ws_for(cache, q, splits=0):
+        nb = kvc.kvc_workspace_size(cache, q, splits)
+        return torch.empty(max(nb // 4, 1), dtype=torch.float32, device=dev)
+
+    for B in batches:
+        for T in lengths:
+            cell = {"B": B, "T": T, "heads": f"GQA {Hq}/{Hkv}", "D": D, "prefill_ms": {},
+                    "decode_ms": {}, "decode_tokens_per_s": {}, "slots_attended": {}}
+            with torch.cuda.stream(stream):
+                gen = torch.Generator(device=dev)
+                gen.manual_seed(1000 + B + T)
+                K = torch.randn(B, Hkv, T, D, generator=gen, device=dev, dtype=torch.float16)
+                V = torch.randn(B, Hkv, T, D, generator=gen, device=dev, dtype=torch.float16)
+                q = torch.randn(B, Hq, D, generator=gen, device=dev, dtype=torch.float16)
+                kn = torch.randn(B, Hkv, 1, D, generator=gen, device=dev, dtype=torch.float16)
+                vn = torch.randn(B, Hkv, 1, D, generator=gen, device=dev, dtype=torch.float16)
+                o = torch.empty_like(q)
+                C = T + 8
+                fp = kvc.SlotCache.empty(B, Hkv, C, D, device=dev)
+
+                def refill():
+                    fp.n.zero_()
+                    fp.seqlen.zero_()
+                    kvc.kvc_append(fp, K, V, stream=stream)
+
+                def rewind(n):
+                    fp.n.fill_(n)
+                    fp.seqlen.fill_(n)
+
+                # ---- FP16
+                cell["prefill_ms"]["fp16"] = timed(lambda: kvc.kvc_append(fp, K, V, stream=stream),
+                                                   setup=lambda: rewind(0))
+                ws = ws_for(fp, q)
+
+                def fp_step():
+                    kvc.kvc_append(fp, kn, vn, stream=stream)
+                    kvc.kvc_decode_attend(fp, q, o, workspace=ws, stream=stream)
+                cell["decode_ms"]["fp16"] = timed(fp_step, setup=lambda: rewind(T))
+                cell["slots_attended"]["fp16"] = T + 1
+                # ---- random eviction sweep (prompt locked), attention over the kept slots
+                prompt = min(1024, T // 2)
+                for r in ratios:
+                    name = f"random{r:g}"
+                    cell["prefill_ms"][name] = timed(
+                        lambda: kvc.kvc_random_evict(fp, prompt, r, 0x243F6A8885A308D3, 0,
+                                                     stream=stream), setup=refill)
+                    kept = prompt + max(1, int((T - prompt) * r))
+                    cell["decode_ms"][name] = timed(
+                        lambda: kvc.kvc_decode_attend(fp, q, o, workspace=ws, stream=stream))
+                    cell["slots_attended"][name] = kept
+                # ---- StreamingLLM: evict the prompt to 64 sinks + 448 recent, then steady steps
+                cell["prefill_ms"]["stream512"] = timed(
+                    lambda: kvc.kvc_stream_evict(fp, n_sink, n_recent, stream=stream), setup=refill)
+                ws_s = ws_for(fp, q)
+
+                def stream_step():
+                    kvc.kvc_append(fp, kn, vn, stream=stream)
+                    kvc.kvc_decode_attend(fp, q, o, workspace=ws_s, stream=stream)
+                    kvc.kvc_stream_evict(fp, n_sink, n_recent, stream=stream)
+                cell["decode_ms"]["stream512"] = timed(stream_step)
+                cell["slots_attended"]["stream512"] = n_sink + n_recent + 1
+                # ---- H2O: two-pass prefill score pass (in batch chunks of <= 8 GB of queries)
+                # then evict to 64 heavy + 448 recent; decode steps with the fused update
+                scores = torch.zeros(B, Hkv, C, dtype=torch.float32, device=dev)
+                bc = max(1, min(B, (8 << 30) // (Hq * T * D * 2)))
+                qp = torch.randn(bc, Hq, T, D, generator=gen, device=dev, dtype=torch.float16)
+                pws = torch.empty(kvc.kvc_h2o_workspace_size(bc, Hq, T) // 4, dtype=torch.float32,
+                                  device=dev)
+
+                def h2o_prefill():
+                    for b0 in range(0, B, bc):
+                        b1 = min(B, b0 + bc)
+                        kvc.kvc_h2o_accumulate_prefill(qp[:b1 - b0], fp.K[b0:b1], scores[b0:b1],
+                                                       pws, T, stream=stream)
+                    kvc.kvc_h2o_evict(fp, scores, n_heavy, n_recent, stream=stream)
+                cell["prefill_ms"]["h2o512"] = timed(h2o_prefill, setup=refill, reps=1)
+                del qp, pws
+                logits = torch.empty(B, Hq, C, dtype=torch.float32, device=dev)
+                lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+                ws_h = ws_for(fp, q, 1)
+
+                def h2o_step():
+                    kvc.kvc_append(fp, kn, vn, stream=stream)
+                    kvc.kvc_decode_attend(fp, q, o, logits=logits, lse=lse, workspace=ws_h,
+                                          num_splits=1, h2o_scores=scores, stream=stream)
+                    kvc.kvc_h2o_evict(fp, scores, n_heavy, n_recent, stream=stream)
+                cell["decode_ms"]["h2o512"] = timed(h2o_step)
+                cell["slots_attended"]["h2o512"] = n_heavy + n_recent + 1
+                del fp, scores, logits, lse
+                # ---- KIVI-4 / KIVI-2: pack the prompt, then append + attention
+                for bits in (4, 2):
+                    name = f"kivi{bits}"
+                    kv = kvc.QuantCache.empty(B, Hkv, 32 * ((T + 1) // 32 + 1), D, bits, R,
+                                              device=dev)
+                    cell["prefill_ms"][name] = timed(
+                        lambda: kvc.kvc_append_quant(kv, K, V, stream=stream),
+                        setup=lambda: kv.len.zero_())
+                    ws_k = ws_for(kv, q)
+
+                    def kivi_step():
+                        kvc.kvc_append_quant(kv, kn, vn, stream=stream)
+                        kvc.kvc_decode_attend(kv, q, o, workspace=ws_k, stream=stream)
+                    cell["decode_ms"][name] = timed(kivi_step, setup=lambda: kv.len.fill_(T))
+                    cell["slots_attended"][name] = T + 1
+                    del kv, ws_k
+                del K, V
+            torch.cuda.synchronize(dev)
+            status = kvc.kvc_read_device_status(stream)
+            cell["device_status"] = status
+            cell["decode_tokens_per_s"] = {k: B / (v * 1e-3) for k, v in cell["decode_ms"].items()}
+            print(json.dumps(cell), flush=True)
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -656,8 +814,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None,
                     help="run one kernel on a small case for ncu: attend_fp16, attend_h2o, "
-                         "attend_kivi4, h2o_evict, stream_evict, prefill")
+                         "attend_kivi4, h2o_evict, stream_evict, prefill, kivi_pack")
     ap.add_argument("--profile-batch", type=int, default=64)
+    ap.add_argument("--grid", action="store_true",
+                    help="throughput profile grid over batch x KV length x method (JSON lines)")
+    ap.add_argument("--grid-batches", default="1,16,128,512")
+    ap.add_argument("--grid-lengths", default="1024,4096,16384")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -665,6 +827,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     if args.profile:
         run_profile(args)
+        return
+    if args.grid:
+        run_grid(args)
         return
     if args.impl == "reference":
         if rank == 0:

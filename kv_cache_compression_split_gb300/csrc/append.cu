@@ -126,39 +126,250 @@ struct GroupQ {
     uint16_t zero_bits, scale_bits;
 };
 
-__device__ __forceinline__ GroupQ group_params(long long mn, uint16_t mn_bits, long long mx,
-                                               int bits)
+// binary16 bits of the correctly rounded (to nearest, ties to even) value of
+// range * 2^-24 / CMAX, for an integer 0 <= range < 2^42 and odd CMAX, in
+// integer arithmetic: in units of 2^-24 binary16 has spacing 1 below 2^10
+// (subnormals) and 2^k on [2^(k+10), 2^(k+11)), and its encoding k * 2^10 + m
+// is continuous, so a carry of the rounded mantissa m into 2^11 lands on the
+// next binade by itself.
+template <int CMAX> __device__ __forceinline__ uint16_t scale_bits_rn(unsigned long long range)
+{
+    const unsigned long long q0 = range / CMAX;          // floor of the quotient
+    if (q0 < 1024) {
+        const unsigned long long r = range - q0 * CMAX;
+        return (uint16_t)(q0 + (2 * r > CMAX));         // CMAX odd: no exact ties
+    }
+    const int k = 53 - __clzll((long long)q0);           // quotient in [2^(k+10), 2^(k+11))
+    const unsigned long long div = (unsigned long long)CMAX << k;
+    const unsigned long long m = q0 >> k;                 // floor(range / div)
+    const unsigned long long r2 = 2 * (range - m * div);
+    const unsigned long long mm = m + (r2 > div || (r2 == div && (m & 1)));
+    return (uint16_t)(((unsigned long long)k << 10) + mm);
+}
+
+template <int BITS>
+__device__ __forceinline__ GroupQ group_params(long long mn, uint16_t mn_bits, long long mx)
 {
     GroupQ q;
     q.zero_bits = (mn_bits == 0x8000) ? (uint16_t)0 : mn_bits;
     q.zero_fix = mn;
-    const double quot = (double)(mx - mn) * 0x1p-24 / (double)((1 << bits) - 1);
-    q.scale_bits = __half_as_ushort(__double2half(quot));
+    q.scale_bits = scale_bits_rn<(1 << BITS) - 1>((unsigned long long)(mx - mn));
     q.scale_fix = h2fix(q.scale_bits);
     return q;
 }
 
-__device__ __forceinline__ int quant_code(long long x, const GroupQ &q, int cmax)
+// Code of x: round-half-even((x - zero) / scale) clamped to [0, cmax], exact.
+// The estimate is formed in fp32 from the binary16 values (x - zero rounded
+// once, times 1/scale), which puts it within one of the true quotient; the
+// exact integer remainder (values in units of 2^-24) then decides, ties to the
+// even code.  No 64-bit integer is converted to or from floating point.
+__device__ __forceinline__ int quant_code_inv(uint16_t xb, long long zero_fix, float zero_f,
+                                              long long scale_fix, float inv, int cmax)
 {
-    if (q.scale_fix == 0)
+    if (scale_fix == 0)
         return 0;
-    const long long diff = x - q.zero_fix; // >= 0
-    long long c = (long long)rintf((float)diff / (float)q.scale_fix);
-    const long long rem2 = 2 * (diff - c * q.scale_fix);
-    if (rem2 > q.scale_fix)
+    const long long diff = h2fix(xb) - zero_fix;   // >= 0
+    const float est = (__half2float(__ushort_as_half(xb)) - zero_f) * inv;
+    long long c = (long long)__float2int_rn(fminf(est, 1048576.f));
+    const long long rem2 = 2 * (diff - c * scale_fix);
+    if (rem2 > scale_fix)
         c += 1;
-    else if (rem2 < -q.scale_fix)
+    else if (rem2 < -scale_fix)
         c -= 1;
-    else if (rem2 == q.scale_fix)
+    else if (rem2 == scale_fix)
         c += (c & 1);
-    else if (rem2 == -q.scale_fix)
+    else if (rem2 == -scale_fix)
         c -= (c & 1);
     return (int)(c < 0 ? 0 : (c > cmax ? cmax : c));
 }
 
 constexpr int QTHREADS = 256;
 
+// Shared staging of one 32-token group: fp16 inputs, then codes.
+template <int D> struct __align__(16) GroupSmem {
+    uint16_t xk[KIVI_G][D];
+    uint16_t xv[KIVI_G][D];
+    uint8_t ck[KIVI_G][D];
+    uint8_t cv[KIVI_G][D];
+    long long zfix[2 * D];       // per K channel, then per V (token, channel group)
+    long long sfix[2 * D];
+    float zf[2 * D];             // zero as fp32
+    float inv[2 * D];            // 1 / scale (an estimate; the remainder fixes the code)
+};
+
+// quant_code_inv with a fast path: the fp32 estimate is within 3e-6 of the
+// true quotient whenever it is below cmax + 1 (three roundings of relative
+// 2^-24 on a quotient of at most 16), so unless it lies within 1e-4 of a
+// rounding midpoint its nearest integer is the exact code; an estimate of
+// cmax + 1 or more means a code clamped to cmax, and a zero reciprocal (scale 0)
+// gives code 0.  Only near-midpoints read the exact parameters of set pi.
+template <int D>
+__device__ __forceinline__ int quant_code_fast(uint16_t xb, float zero_f, float inv, int pi,
+                                               const GroupSmem<D> &sm, int cmax)
+{
+    const float est = (__half2float(__ushort_as_half(xb)) - zero_f) * inv;
+    if (est >= (float)(cmax + 1))
+        return cmax;
+    const float fr = est - floorf(est);
+    if (fabsf(fr - 0.5f) < 1e-4f)
+        return quant_code_inv(xb, sm.zfix[pi], zero_f, sm.sfix[pi], inv, cmax);
+    const int c = __float2int_rn(est);
+    return c < 0 ? 0 : (c > cmax ? cmax : c);
+}
+
+// Quantise and pack group g of one unit (all threads of the CTA take part):
+// gather its 32 tokens (old ones from the residual ring, new ones from the
+// input), compute the K per-channel and V per-(token, channel-group)
+// scale / zero, the codes, and write the K and V blocks.
 template <int D, int BITS>
+__device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16_t *kn,
+                                           const uint16_t *vn, const uint16_t *kr,
+                                           const uint16_t *vr, uint8_t *kblk, uint8_t *vblk,
+                                           GroupSmem<D> &sm)
+{
+    constexpr int G = KIVI_G;
+    constexpr int WK = D * BITS / 32;           // u32 words per K token row
+    constexpr int W = D * BITS / 128;           // words per lane-row of a V pair
+    constexpr int CODE_BYTES = G * D * BITS / 8;
+    constexpr int CMAX = (1 << BITS) - 1;
+    constexpr int NG = D / G;                   // V channel groups per token
+    for (int i = threadIdx.x; i < G * D / 8; i += QTHREADS) {
+        const int t = i / (D / 8), ch = i % (D / 8);
+        const long p = g * G + t;
+        const uint4 *sk, *sv;
+        if (p < T0) {
+            const long slot = p % CR;
+            sk = reinterpret_cast<const uint4 *>(kr + slot * D) + ch;
+            sv = reinterpret_cast<const uint4 *>(vr + slot * D) + ch;
+        } else {
+            sk = reinterpret_cast<const uint4 *>(kn + (p - T0) * D) + ch;
+            sv = reinterpret_cast<const uint4 *>(vn + (p - T0) * D) + ch;
+        }
+        reinterpret_cast<uint4 *>(&sm.xk[t][0])[ch] = *sk;
+        reinterpret_cast<uint4 *>(&sm.xv[t][0])[ch] = *sv;
+    }
+    __syncthreads();
+    uint16_t *ksz = reinterpret_cast<uint16_t *>(kblk + CODE_BYTES);
+    uint16_t *vsz = reinterpret_cast<uint16_t *>(vblk + CODE_BYTES);
+    // 1. parameters: D K channels (over the group's 32 tokens) and G * NG = D V
+    //    (token, 32-channel group) sets, one thread each.  Binary16 values compare
+    //    exactly as fp32, so any scan order finds the same extremes (equal values
+    //    share their bits except +-0, and a -0 zero point is stored as +0); the V
+    //    scan starts at a per-thread rotation so that a warp's reads fall in
+    //    distinct banks.
+    for (int i = threadIdx.x; i < 2 * D; i += QTHREADS) {
+        const bool isk = i < D;
+        const int a = isk ? i : i - D;
+        const int t = a / NG, j = a % NG;       // V: token t, channel group j
+        const int rot = 2 * (t + 8 * (j >> 1));
+        auto val = [&](int e) -> uint16_t {
+            return isk ? sm.xk[e][a] : sm.xv[t][j * G + ((e + rot) & (G - 1))];
+        };
+        uint16_t mnb = val(0), mxb = mnb;
+        float mnf = __half2float(__ushort_as_half(mnb)), mxf = mnf;
+        for (int e = 1; e < G; ++e) {
+            const uint16_t hb = val(e);
+            const float v = __half2float(__ushort_as_half(hb));
+            if (v < mnf) {
+                mnf = v;
+                mnb = hb;
+            }
+            if (v > mxf) {
+                mxf = v;
+                mxb = hb;
+            }
+        }
+        const GroupQ q = group_params<BITS>(h2fix(mnb), mnb, h2fix(mxb));
+        if (isk) {
+            ksz[a] = q.scale_bits;
+            ksz[D + a] = q.zero_bits;
+        } else {
+            vsz[j * G + t] = q.scale_bits;
+            vsz[NG * G + j * G + t] = q.zero_bits;
+        }
+        sm.zfix[i] = q.zero_fix;
+        sm.sfix[i] = q.scale_fix;
+        sm.zf[i] = __half2float(__ushort_as_half(mnb));
+        // a zero scale gives a zero reciprocal, so the fast path yields code 0
+        sm.inv[i] = q.scale_fix ? 1.0f / __half2float(__ushort_as_half(q.scale_bits)) : 0.f;
+    }
+    __syncthreads();
+    // 2. codes of the 2 * G * D elements, four channels (one word of codes) per step
+    for (int i = threadIdx.x; i < 2 * G * D / 4; i += QTHREADS) {
+        const bool isk = i < G * D / 4;
+        const int e = 4 * (isk ? i : i - G * D / 4);
+        const int t = e / D, d0 = e % D;
+        const uint2 xw = *reinterpret_cast<const uint2 *>(isk ? &sm.xk[t][d0] : &sm.xv[t][d0]);
+        const uint16_t xs[4] = {(uint16_t)(xw.x & 0xffff), (uint16_t)(xw.x >> 16),
+                                (uint16_t)(xw.y & 0xffff), (uint16_t)(xw.y >> 16)};
+        float zf[4], inv[4];
+        int pis[4];
+        if (isk) {   // per-channel parameters of channels d0 .. d0 + 3
+            const float4 z4 = *reinterpret_cast<const float4 *>(&sm.zf[d0]);
+            const float4 i4 = *reinterpret_cast<const float4 *>(&sm.inv[d0]);
+            zf[0] = z4.x, zf[1] = z4.y, zf[2] = z4.z, zf[3] = z4.w;
+            inv[0] = i4.x, inv[1] = i4.y, inv[2] = i4.z, inv[3] = i4.w;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                pis[u] = d0 + u;
+        } else {     // the four channels share one (token, channel group) set
+            const int pi = D + t * NG + d0 / G;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                zf[u] = sm.zf[pi];
+                inv[u] = sm.inv[pi];
+                pis[u] = pi;
+            }
+        }
+        uint32_t word = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            word |= (uint32_t)quant_code_fast(xs[u], zf[u], inv[u], pis[u], sm, CMAX) << (8 * u);
+        *reinterpret_cast<uint32_t *>(isk ? &sm.ck[t][d0] : &sm.cv[t][d0]) = word;
+    }
+    __syncthreads();
+    // 3. pack K token rows: field i of word w holds channel (32/BITS)*w + i
+    uint32_t *kw = reinterpret_cast<uint32_t *>(kblk);
+    for (int i = threadIdx.x; i < G * WK; i += QTHREADS) {
+        const int t = i / WK, w = i % WK;
+        uint32_t word = 0;
+#pragma unroll
+        for (int f = 0; f < 32 / BITS; ++f)
+            word |= (uint32_t)sm.ck[t][(32 / BITS) * w + f] << (BITS * f);
+        kw[i] = word;
+    }
+    // pack V token pairs: word ((rr + 2 pair) mod 8)*W + k, field j holds channel
+    // 16*(k*(8/BITS) + j/2) + 8*(j%2) + rr; low half token 2i, high half 2i+1
+    uint32_t *vw = reinterpret_cast<uint32_t *>(vblk);
+    for (int i = threadIdx.x; i < (G / 2) * 8 * W; i += QTHREADS) {
+        const int pair = i / (8 * W), rk = i % (8 * W), rr = rk / W, k = rk % W;
+        const int slot = pair * 8 * W + ((rr + 2 * pair) & 7) * W + k;
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 16 / BITS; ++j) {
+            const int d = 16 * (k * (8 / BITS) + j / 2) + 8 * (j % 2) + rr;
+            word |= (uint32_t)sm.cv[2 * pair][d] << (BITS * j);
+            word |= (uint32_t)sm.cv[2 * pair + 1][d] << (16 + BITS * j);
+        }
+        vw[slot] = word;
+    }
+    __syncthreads();
+}
+
+// n_q (tokens quantised) at length T: 32 * floor(max(0, T - R) / 32).
+__device__ __forceinline__ long kivi_nq(long T, int R)
+{
+    const long over = T - R;
+    return over > 0 ? (over / KIVI_G) * KIVI_G : 0;
+}
+
+// Append n_new tokens to every unit of a KIVI cache.  GROUPS: CTA (unit, y)
+// quantises the groups flushed by this append with index = y mod gridDim.y.
+// RESIDUAL: the new tokens that stay fp16 are written to their ring slots.  A
+// single launch may do both only when it is one CTA per unit (the ring slots
+// it writes may be ones a flushed group still reads); bulk appends run the
+// groups on a wide grid first and the residual in a second launch.
+template <int D, int BITS, bool GROUPS, bool RESIDUAL>
 __global__ void __launch_bounds__(QTHREADS)
     k_append_quant(int Hkv, int R, int Cq, int n_new, const uint16_t *__restrict__ k_new,
                    const uint16_t *__restrict__ v_new, uint8_t *__restrict__ kb,
@@ -166,141 +377,43 @@ __global__ void __launch_bounds__(QTHREADS)
                    uint16_t *__restrict__ v_res, const int32_t *__restrict__ len, int *status)
 {
     constexpr int G = KIVI_G;
-    constexpr int WK = D * BITS / 32;           // u32 words per K token row
-    constexpr int W = D * BITS / 128;           // words per lane-row of a V pair
-    constexpr int CODE_BYTES = G * D * BITS / 8;
-    constexpr int BLOCK = CODE_BYTES + 4 * D;
-    constexpr int CMAX = (1 << BITS) - 1;
-    constexpr int NG = D / G;                   // V channel groups per token
-
-    __shared__ uint16_t xk[G][D];
-    __shared__ uint16_t xv[G][D];
-    __shared__ uint8_t ck[G][D];
-    __shared__ uint8_t cv[G][D];
+    constexpr int BLOCK = G * D * BITS / 8 + 4 * D;
+    __shared__ GroupSmem<D> sm;
 
     const int unit = blockIdx.x;
     const int b = unit / Hkv;
     const int CR = R + G;
     const long T0 = len[b], T1 = T0 + n_new;
-    auto nq = [&](long T) -> long {
-        const long over = T - R;
-        return over > 0 ? (over / G) * G : 0;
-    };
-    const long nq0 = nq(T0), nq1 = nq(T1);
+    const long nq0 = kivi_nq(T0, R), nq1 = kivi_nq(T1, R);
     if (nq1 > Cq) {
-        if (threadIdx.x == 0)
+        if (threadIdx.x == 0 && blockIdx.y == 0 && (GROUPS || !RESIDUAL))
             flag_error(status, DEV_CAPACITY);
         return;
     }
     const uint16_t *kn = k_new + (size_t)unit * n_new * D;
     const uint16_t *vn = v_new + (size_t)unit * n_new * D;
-    const uint16_t *kr = k_res + (size_t)unit * CR * D;
-    const uint16_t *vr = v_res + (size_t)unit * CR * D;
 
-    for (long g = nq0 / G; g < nq1 / G; ++g) {
-        // gather the group's 32 tokens (ring for old tokens, input for new ones)
-        for (int i = threadIdx.x; i < G * D / 8; i += QTHREADS) {
-            const int t = i / (D / 8), ch = i % (D / 8);
-            const long p = g * G + t;
-            const uint4 *sk, *sv;
-            if (p < T0) {
-                const long slot = p % CR;
-                sk = reinterpret_cast<const uint4 *>(kr + slot * D) + ch;
-                sv = reinterpret_cast<const uint4 *>(vr + slot * D) + ch;
-            } else {
-                sk = reinterpret_cast<const uint4 *>(kn + (p - T0) * D) + ch;
-                sv = reinterpret_cast<const uint4 *>(vn + (p - T0) * D) + ch;
-            }
-            reinterpret_cast<uint4 *>(&xk[t][0])[ch] = *sk;
-            reinterpret_cast<uint4 *>(&xv[t][0])[ch] = *sv;
-        }
-        __syncthreads();
-
-        uint8_t *kblk = kb + ((size_t)unit * (Cq / G) + g) * BLOCK;
-        uint8_t *vblk = vb + ((size_t)unit * (Cq / G) + g) * BLOCK;
-        uint16_t *ksz = reinterpret_cast<uint16_t *>(kblk + CODE_BYTES);
-        uint16_t *vsz = reinterpret_cast<uint16_t *>(vblk + CODE_BYTES);
-
-        // K: per channel over the group's tokens
-        for (int d = threadIdx.x; d < D; d += QTHREADS) {
-            long long mn = h2fix(xk[0][d]), mx = mn;
-            uint16_t mnb = xk[0][d];
-            for (int t = 1; t < G; ++t) {
-                const long long v = h2fix(xk[t][d]);
-                if (v < mn) {
-                    mn = v;
-                    mnb = xk[t][d];
-                }
-                if (v > mx)
-                    mx = v;
-            }
-            const GroupQ q = group_params(mn, mnb, mx, BITS);
-            ksz[d] = q.scale_bits;
-            ksz[D + d] = q.zero_bits;
-            for (int t = 0; t < G; ++t)
-                ck[t][d] = (uint8_t)quant_code(h2fix(xk[t][d]), q, CMAX);
-        }
-        // V: per token over channel groups of 32
-        for (int i = threadIdx.x; i < G * NG; i += QTHREADS) {
-            const int t = i / NG, j = i % NG;
-            long long mn = h2fix(xv[t][j * G]), mx = mn;
-            uint16_t mnb = xv[t][j * G];
-            for (int e = 1; e < G; ++e) {
-                const long long v = h2fix(xv[t][j * G + e]);
-                if (v < mn) {
-                    mn = v;
-                    mnb = xv[t][j * G + e];
-                }
-                if (v > mx)
-                    mx = v;
-            }
-            const GroupQ q = group_params(mn, mnb, mx, BITS);
-            vsz[j * G + t] = q.scale_bits;
-            vsz[NG * G + j * G + t] = q.zero_bits;
-            for (int e = 0; e < G; ++e)
-                cv[t][j * G + e] = (uint8_t)quant_code(h2fix(xv[t][j * G + e]), q, CMAX);
-        }
-        __syncthreads();
-
-        // pack K token rows: field i of word w holds channel (32/BITS)*w + i
-        uint32_t *kw = reinterpret_cast<uint32_t *>(kblk);
-        for (int i = threadIdx.x; i < G * WK; i += QTHREADS) {
-            const int t = i / WK, w = i % WK;
-            uint32_t word = 0;
-#pragma unroll
-            for (int f = 0; f < 32 / BITS; ++f)
-                word |= (uint32_t)ck[t][(32 / BITS) * w + f] << (BITS * f);
-            kw[i] = word;
-        }
-        // pack V token pairs: word ((rr + 2 pair) mod 8)*W + k, field j holds channel
-        // 16*(k*(8/BITS) + j/2) + 8*(j%2) + rr; low half token 2i, high half 2i+1
-        uint32_t *vw = reinterpret_cast<uint32_t *>(vblk);
-        for (int i = threadIdx.x; i < (G / 2) * 8 * W; i += QTHREADS) {
-            const int pair = i / (8 * W), rk = i % (8 * W), rr = rk / W, k = rk % W;
-            const int slot = pair * 8 * W + ((rr + 2 * pair) & 7) * W + k;
-            uint32_t word = 0;
-#pragma unroll
-            for (int j = 0; j < 16 / BITS; ++j) {
-                const int d = 16 * (k * (8 / BITS) + j / 2) + 8 * (j % 2) + rr;
-                word |= (uint32_t)cv[2 * pair][d] << (BITS * j);
-                word |= (uint32_t)cv[2 * pair + 1][d] << (16 + BITS * j);
-            }
-            vw[slot] = word;
-        }
-        __syncthreads();
+    if (GROUPS) {
+        const uint16_t *kr = k_res + (size_t)unit * CR * D;
+        const uint16_t *vr = v_res + (size_t)unit * CR * D;
+        for (long g = nq0 / G + blockIdx.y; g < nq1 / G; g += gridDim.y)
+            pack_group<D, BITS>(g, T0, CR, kn, vn, kr, vr,
+                                kb + ((size_t)unit * (Cq / G) + g) * BLOCK,
+                                vb + ((size_t)unit * (Cq / G) + g) * BLOCK, sm);
     }
-
-    // residual: new tokens that stay in fp16 go to ring slot p mod (R + 32)
-    const long r0 = nq1 > T0 ? nq1 : T0;
-    uint4 *krw = reinterpret_cast<uint4 *>(k_res + (size_t)unit * CR * D);
-    uint4 *vrw = reinterpret_cast<uint4 *>(v_res + (size_t)unit * CR * D);
-    const long total = (T1 - r0) * (D / 8);
-    for (long i = threadIdx.x; i < total; i += QTHREADS) {
-        const long p = r0 + i / (D / 8);
-        const int ch = (int)(i % (D / 8));
-        const long slot = p % CR;
-        krw[slot * (D / 8) + ch] = reinterpret_cast<const uint4 *>(kn + (p - T0) * D)[ch];
-        vrw[slot * (D / 8) + ch] = reinterpret_cast<const uint4 *>(vn + (p - T0) * D)[ch];
+    if (RESIDUAL) {
+        // new tokens that stay in fp16 go to ring slot p mod (R + 32)
+        const long r0 = nq1 > T0 ? nq1 : T0;
+        uint4 *krw = reinterpret_cast<uint4 *>(k_res + (size_t)unit * CR * D);
+        uint4 *vrw = reinterpret_cast<uint4 *>(v_res + (size_t)unit * CR * D);
+        const long total = (T1 - r0) * (D / 8);
+        for (long i = blockIdx.y * QTHREADS + threadIdx.x; i < total; i += gridDim.y * QTHREADS) {
+            const long p = r0 + i / (D / 8);
+            const int ch = (int)(i % (D / 8));
+            const long slot = p % CR;
+            krw[slot * (D / 8) + ch] = reinterpret_cast<const uint4 *>(kn + (p - T0) * D)[ch];
+            vrw[slot * (D / 8) + ch] = reinterpret_cast<const uint4 *>(vn + (p - T0) * D)[ch];
+        }
     }
 }
 
@@ -315,9 +428,28 @@ template <int D, int BITS>
 cudaError_t launch_quant_impl(const kvc_quant_cache &c, const uint16_t *k_new,
                               const uint16_t *v_new, int n_new, cudaStream_t s)
 {
-    k_append_quant<D, BITS><<<c.B * c.Hkv, QTHREADS, 0, s>>>(
-        c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res, c.len,
-        dev_status_ptr());
+    const int units = c.B * c.Hkv;
+    if (n_new <= KIVI_G) {
+        // decode-sized: at most two groups flush; one CTA per unit does both parts
+        k_append_quant<D, BITS, true, true><<<units, QTHREADS, 0, s>>>(
+            c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
+            c.len, dev_status_ptr());
+    } else {
+        // bulk: the flushed groups of every unit spread over the grid, then the residual
+        const long max_groups = n_new / KIVI_G + 1;
+        const long fill = (8L * sm_count() + units - 1) / units;  // >= ~8 CTAs per SM in total
+        int gy = (int)(max_groups < fill ? max_groups : fill);
+        gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
+        k_append_quant<D, BITS, true, false><<<dim3(units, gy), QTHREADS, 0, s>>>(
+            c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
+            c.len, dev_status_ptr());
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+        k_append_quant<D, BITS, false, true><<<units, QTHREADS, 0, s>>>(
+            c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
+            c.len, dev_status_ptr());
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;

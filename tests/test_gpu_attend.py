@@ -116,3 +116,20 @@ def test_argument_errors_enqueue_nothing(kvc):
     with pytest.raises(kvc.KvcError) as e:   # more than one split needs a workspace
         kvc.kvc_decode_attend(big, q, torch.empty_like(q), num_splits=2)
     assert e.value.status == kvc.KVC_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("T", [16384, 32768])
+def test_long_single_sequence_auto_splits(kvc, orc, T):
+    """One sequence of the heavy-load head layout (GQA 64/8, D 128) at long context, in the launch
+    configuration of the throughput profile grid (automatic splits): every unit is checked."""
+    B, Hq, Hkv, D = 1, 64, 8, 128
+    g = torch.Generator().manual_seed(T)
+    K = torch.randn(B, Hkv, T, D, generator=g).half()
+    V = torch.randn(B, Hkv, T, D, generator=g).half()
+    q = torch.randn(B, Hq, D, generator=g).half()
+    cache = slot_cache_from(kvc, K, V, np.full((B, Hkv), T), T + 8)
+    o, lse, _ = _run(kvc, cache, q.cuda())
+    ref, ref_lse, _ = orc.decode_attend(np16(q), np16(K), np16(V), np.full((B, Hkv), T, np.int32))
+    assert_o_close(np16(o), ref)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, atol=LSE_ABS_TOL, rtol=0)
+    assert device_status_clean(kvc)

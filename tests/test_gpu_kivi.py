@@ -164,3 +164,69 @@ def test_capacity_overflow_is_flagged(kvc):
     torch.cuda.synchronize()
     assert kvc.kvc_read_device_status() & kvc.KVC_DEV_CAPACITY
     assert kvc.kvc_read_device_status() == 0     # reading clears it
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_long_single_sequence_auto_splits(kvc, orc, bits):
+    """One sequence of the heavy-load head layout (GQA 64/8, D 128) at 16384 tokens, in the
+    launch configuration of the throughput profile grid (automatic splits): every unit's blocks
+    are bit-exact and its attention matches the oracle."""
+    B, Hq, Hkv, D, T, R = 1, 64, 8, 128, 16384, 128
+    g = torch.Generator().manual_seed(T + bits)
+    K = torch.randn(B, Hkv, T, D, generator=g).half()
+    V = torch.randn(B, Hkv, T, D, generator=g).half()
+    q = torch.randn(B, Hq, D, generator=g).half()
+    n_q = orc.kivi_nq(T, R)
+    cache = kvc.QuantCache.empty(B, Hkv, n_q, D, bits, R)
+    kvc.kvc_append_quant(cache, K.cuda(), V.cuda())
+    o, _ = _attend(kvc, cache, q.cuda())
+    gq = Hq // Hkv
+    for hk in range(Hkv):
+        Kb, Vb = np16(K[0, hk]), np16(V[0, hk])
+        qz = orc.kivi_quantize_unit(Kb[:n_q], Vb[:n_q], n_q, bits)
+        kb, vb = orc.kivi_pack_unit(qz, D, bits)
+        assert np.array_equal(cache.k_blocks[0, hk].cpu().numpy(), kb)
+        assert np.array_equal(cache.v_blocks[0, hk].cpu().numpy(), vb)
+        ref, _ = orc.kivi_attend_unit(np16(q[0, hk * gq:(hk + 1) * gq]), Kb, Vb, T, R, bits, qz=qz)
+        assert_o_close(np16(o[0, hk * gq:(hk + 1) * gq]), ref, what=f"hk={hk}")
+    assert device_status_clean(kvc)
+
+
+def _crafted_kv(rng, T, D, kind):
+    """[T, D] fp16 tensors whose 32-token K groups and 32-channel V groups hit the quantiser's
+    edge cases: 'wide' spans 10^-6 .. 10^4 per 32x32 block (subnormal scales, large ranges),
+    'coarse' multiples of 0.25 (exact ties at half-steps), 'flat' constant and signed-zero
+    groups mixed with ordinary ones (degenerate scale 0, zero point -0)."""
+    if kind == "wide":
+        x = rng.standard_normal((T, D)) * np.repeat(np.repeat(
+            10.0 ** rng.uniform(-6, 4, (T // 32, D // 32)), 32, 0), 32, 1)
+    elif kind == "coarse":
+        x = rng.integers(-8, 8, (T, D)) * 0.25
+    else:
+        x = rng.standard_normal((T, D))
+        x[:32] = 1.5                                   # constant K and V groups
+        x[32:64, :32] = -0.0
+        x[32:64, 32:64] = np.where(rng.random((32, 32)) < 0.5, -0.0, 0.0)
+        x[64:96, :] = np.where(rng.random((32, D)) < 0.1, rng.standard_normal((32, D)), 0.0)
+    return x.astype(np.float16)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("kind", ["wide", "coarse", "flat"])
+def test_pack_bit_exact_crafted(kvc, orc, bits, kind):
+    """Bulk pack of crafted groups (wide-range, tie-heavy, degenerate) is bit-exact."""
+    rng = np.random.default_rng(bits * 7 + len(kind))
+    B, Hkv, D, T, R = 2, 2, 128, 288, 32
+    K = np.stack([np.stack([_crafted_kv(rng, T, D, kind) for _ in range(Hkv)]) for _ in range(B)])
+    V = np.stack([np.stack([_crafted_kv(rng, T, D, kind) for _ in range(Hkv)]) for _ in range(B)])
+    n_q = orc.kivi_nq(T, R)
+    cache = kvc.QuantCache.empty(B, Hkv, n_q, D, bits, R)
+    kvc.kvc_append_quant(cache, torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
+    torch.cuda.synchronize()
+    for b in range(B):
+        for hk in range(Hkv):
+            qz = orc.kivi_quantize_unit(K[b, hk, :n_q], V[b, hk, :n_q], n_q, bits)
+            kb, vb = orc.kivi_pack_unit(qz, D, bits)
+            assert np.array_equal(cache.k_blocks[b, hk].cpu().numpy(), kb), (b, hk)
+            assert np.array_equal(cache.v_blocks[b, hk].cpu().numpy(), vb), (b, hk)
+    assert device_status_clean(kvc)
