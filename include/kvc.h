@@ -87,12 +87,29 @@ typedef enum kvc_status {
  * are valid and hold the tokens whose absolute positions are in pos[].
  * Slot order is free (attention does not depend on it); evictions compact the
  * kept slots into [0, n') by moving kept slots from the tail into the holes.
- *   K, V   [B, Hkv, C, D] fp16
+ *   K, V   [B, Hkv, C, D] fp16 (dense layout), or page pools (paged layout)
  *   pos    [B, Hkv, C]    int32, absolute token position of each slot
  *   n      [B, Hkv]       int32, valid slots of each unit
  *   seqlen [B]            int32, tokens generated so far by sequence b (the
  *                         absolute position the next appended token gets)
+ *   block_table  NULL for the dense layout.  Paged layout: [B, Hkv, C / 64]
+ *                int32; slot j of unit (b, h) is row j % 64 of page
+ *                block_table[b][h][j / 64], and K, V are pools of
+ *                [num_pages, 64, D] fp16 shared by all units.  C must be a
+ *                multiple of KVC_PAGE_SLOTS.  The caller owns the pool and the
+ *                table: every slot a call writes must map to a page in
+ *                [0, num_pages) that no other unit uses (entries of slots
+ *                beyond a unit's pages may be -1, so units of a ragged batch
+ *                hold only the pages they need).  A write through an entry
+ *                outside [0, num_pages) is skipped and sets KVC_DEV_CAPACITY.
+ *   num_pages    pages in each pool (paged layout only)
+ * The paged layout is the block layout of paged attention, which splits the
+ * cache into blocks so that it can be allocated non-contiguously and batched
+ * continuously ("Rethinking KV Cache Compression" guide, §16 "前置背景、复现方法
+ * 与结论边界"); here every (sequence, KV head) unit has its own page list because
+ * the eviction methods compact each head on its own.
  */
+#define KVC_PAGE_SLOTS 64
 typedef struct kvc_slot_cache {
     int B, Hkv, D, C;
     uint16_t *K;
@@ -100,6 +117,8 @@ typedef struct kvc_slot_cache {
     int32_t *pos;
     int32_t *n;
     int32_t *seqlen;
+    const int32_t *block_table;
+    int num_pages;
 } kvc_slot_cache;
 
 /*

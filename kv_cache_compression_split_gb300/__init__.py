@@ -12,6 +12,7 @@ import ctypes as C
 import os
 import threading
 from dataclasses import dataclass
+from typing import Optional
 
 import torch
 
@@ -26,6 +27,7 @@ KVC_DEV_CAPACITY, KVC_DEV_TIMEOUT = 0x1, 0x2
 KVC_KIND_SLOTS, KVC_KIND_KIVI = 0, 1
 KVC_H2O_DECODE, KVC_H2O_PREFILL = 0, 1
 KIVI_GROUP = 32
+PAGE_SLOTS = 64            # KVC_PAGE_SLOTS: slots per page of the paged layout
 KVC_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -38,7 +40,7 @@ class KvcError(RuntimeError):
 class SlotCacheDesc(C.Structure):
     _fields_ = [("B", C.c_int), ("Hkv", C.c_int), ("D", C.c_int), ("C", C.c_int),
                 ("K", C.c_void_p), ("V", C.c_void_p), ("pos", C.c_void_p), ("n", C.c_void_p),
-                ("seqlen", C.c_void_p)]
+                ("seqlen", C.c_void_p), ("block_table", C.c_void_p), ("num_pages", C.c_int)]
 
 
 class QuantCacheDesc(C.Structure):
@@ -271,24 +273,30 @@ def kvc_read_device_status(stream=None) -> int:
 
 @dataclass
 class SlotCache:
-    """fp16 slot cache in device memory (layout documented in include/kvc.h)."""
+    """fp16 slot cache in device memory (layout documented in include/kvc.h).  Dense layout:
+    K, V [B, Hkv, C, D].  Paged layout: K, V are page pools [num_pages, 64, D] and
+    block_table [B, Hkv, C // 64] int32 maps each unit's 64-slot pages into them."""
     K: torch.Tensor
     V: torch.Tensor
     pos: torch.Tensor
     n: torch.Tensor
     seqlen: torch.Tensor
+    block_table: Optional[torch.Tensor] = None
 
     @property
-    def B(self): return self.K.shape[0]
+    def B(self): return self.pos.shape[0]
 
     @property
-    def Hkv(self): return self.K.shape[1]
+    def Hkv(self): return self.pos.shape[1]
 
     @property
-    def C(self): return self.K.shape[2]
+    def C(self): return self.pos.shape[2]
 
     @property
-    def D(self): return self.K.shape[3]
+    def D(self): return self.K.shape[-1]
+
+    @property
+    def num_pages(self): return self.K.shape[0] if self.block_table is not None else 0
 
     @classmethod
     def empty(cls, B, Hkv, C_, D, device="cuda"):
@@ -298,9 +306,26 @@ class SlotCache:
                    n=torch.zeros(B, Hkv, dtype=torch.int32, device=device),
                    seqlen=torch.zeros(B, dtype=torch.int32, device=device))
 
+    @classmethod
+    def empty_paged(cls, B, Hkv, C_, D, num_pages, block_table=None, device="cuda"):
+        """Paged cache: pools of num_pages pages of 64 slots; block_table [B, Hkv, C_ // 64]
+        (default: unit u owns pages u * C_ / 64 .. (u + 1) * C_ / 64 - 1)."""
+        if C_ % PAGE_SLOTS:
+            raise ValueError("C must be a multiple of 64 in the paged layout")
+        if block_table is None:
+            block_table = torch.arange(B * Hkv * (C_ // PAGE_SLOTS), dtype=torch.int32,
+                                       device=device).view(B, Hkv, C_ // PAGE_SLOTS)
+        return cls(K=torch.zeros(num_pages, PAGE_SLOTS, D, dtype=torch.float16, device=device),
+                   V=torch.zeros(num_pages, PAGE_SLOTS, D, dtype=torch.float16, device=device),
+                   pos=torch.full((B, Hkv, C_), -1, dtype=torch.int32, device=device),
+                   n=torch.zeros(B, Hkv, dtype=torch.int32, device=device),
+                   seqlen=torch.zeros(B, dtype=torch.int32, device=device),
+                   block_table=block_table.to(device=device, dtype=torch.int32).contiguous())
+
     def desc(self) -> SlotCacheDesc:
         return SlotCacheDesc(self.B, self.Hkv, self.D, self.C, _ptr(self.K), _ptr(self.V),
-                             _ptr(self.pos), _ptr(self.n), _ptr(self.seqlen))
+                             _ptr(self.pos), _ptr(self.n), _ptr(self.seqlen),
+                             _ptr(self.block_table), self.num_pages)
 
 
 @dataclass

@@ -135,6 +135,12 @@ kvc_status check_slot_cache(const kvc_slot_cache *c)
         return KVC_ERR_INVALID_ARG;
     if ((long long)c->B * c->Hkv * c->C > (long long)INT_MAX)
         return KVC_ERR_UNSUPPORTED;
+    if (c->block_table) {   // paged layout: whole pages per unit, a pool of num_pages
+        if (c->C % KVC_PAGE_SLOTS != 0 || c->num_pages <= 0)
+            return KVC_ERR_INVALID_ARG;
+        if ((long long)c->num_pages * KVC_PAGE_SLOTS > (long long)INT_MAX)
+            return KVC_ERR_UNSUPPORTED;
+    }
     return KVC_OK;
 }
 
@@ -281,7 +287,7 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         float *part_ml = part_o ? part_o + (size_t)f.B * a->Hq * f.plan.splits * f.D : nullptr;
         AttendLaunch L{f.B, a->Hq, c.Hkv, c.D, c.C, a->q, a->o, c.K, c.V, c.n, a->logits, a->lse,
                        part_o, part_ml, f.plan.splits, f.plan.tiles_per_split, scale,
-                       a->h2o_scores, h2o_keep, h2o_add};
+                       a->h2o_scores, h2o_keep, h2o_add, c.block_table, c.num_pages};
         cudaError_t e = launch_attend_slots(L, stream);
         if (e != cudaSuccess || !a->h2o_scores || f.plan.splits == 1)
             return from_cuda(e);

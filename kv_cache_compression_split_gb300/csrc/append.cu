@@ -29,7 +29,7 @@ __global__ void k_append_slots(int Hkv, int D, int C, int n_new, const uint4 *__
                                const uint4 *__restrict__ v_new, uint4 *__restrict__ K,
                                uint4 *__restrict__ V, int32_t *__restrict__ pos,
                                const int32_t *__restrict__ n, const int32_t *__restrict__ seqlen,
-                               int *status)
+                               const SlotRows rows, int *status)
 {
     const int unit = blockIdx.x;
     const int b = unit / Hkv;
@@ -46,7 +46,13 @@ __global__ void k_append_slots(int Hkv, int D, int C, int n_new, const uint4 *__
          idx += (long)gridDim.y * blockDim.x) {
         const int t = (int)(idx / cpt), ch = (int)(idx % cpt);
         const size_t src = ((size_t)unit * n_new + t) * cpt + ch;
-        const size_t dst = ((size_t)unit * C + n0 + t) * cpt + ch;
+        const long row = rows.row(unit, n0 + t);
+        if (row < 0) {   // no page behind this slot
+            if (ch == 0)
+                flag_error(status, DEV_CAPACITY);
+            continue;
+        }
+        const size_t dst = (size_t)row * cpt + ch;
         K[dst] = k_new[src];
         V[dst] = v_new[src];
         if (ch == 0)
@@ -60,7 +66,8 @@ __global__ void k_append_slots(int Hkv, int D, int C, int n_new, const uint4 *__
 __global__ void k_append_small(int Hkv, int D, int C, int n_new, const uint4 *__restrict__ k_new,
                                const uint4 *__restrict__ v_new, uint4 *__restrict__ K,
                                uint4 *__restrict__ V, int32_t *__restrict__ pos,
-                               int32_t *__restrict__ n, int32_t *__restrict__ seqlen, int *status)
+                               int32_t *__restrict__ n, int32_t *__restrict__ seqlen,
+                               const SlotRows rows, int *status)
 {
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -82,7 +89,12 @@ __global__ void k_append_small(int Hkv, int D, int C, int n_new, const uint4 *__
             const int kv = i / (n_new * cpt), e = i % (n_new * cpt);
             const int t = e / cpt, ch = e % cpt;
             const size_t src = ((size_t)unit * n_new + t) * cpt + ch;
-            const size_t dst = ((size_t)unit * C + n0 + t) * cpt + ch;
+            const long row = rows.row(unit, n0 + t);
+            if (row < 0) {   // no page behind this slot
+                s_bad = 1;
+                continue;
+            }
+            const size_t dst = (size_t)row * cpt + ch;
             if (kv == 0)
                 K[dst] = k_new[src];
             else
@@ -467,7 +479,8 @@ cudaError_t launch_append_slots(const kvc_slot_cache &c, const uint16_t *k_new,
         k_append_small<<<c.B, 32 * warps, 0, s>>>(
             c.Hkv, c.D, c.C, n_new, reinterpret_cast<const uint4 *>(k_new),
             reinterpret_cast<const uint4 *>(v_new), reinterpret_cast<uint4 *>(c.K),
-            reinterpret_cast<uint4 *>(c.V), c.pos, c.n, c.seqlen, dev_status_ptr());
+            reinterpret_cast<uint4 *>(c.V), c.pos, c.n, c.seqlen,
+            SlotRows{c.block_table, c.C, c.num_pages}, dev_status_ptr());
         return cudaGetLastError();
     }
     const int units = c.B * c.Hkv;
@@ -481,6 +494,7 @@ cudaError_t launch_append_slots(const kvc_slot_cache &c, const uint16_t *k_new,
                                         reinterpret_cast<const uint4 *>(v_new),
                                         reinterpret_cast<uint4 *>(c.K),
                                         reinterpret_cast<uint4 *>(c.V), c.pos, c.n, c.seqlen,
+                                        SlotRows{c.block_table, c.C, c.num_pages},
                                         dev_status_ptr());
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)

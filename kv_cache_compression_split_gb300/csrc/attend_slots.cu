@@ -52,6 +52,7 @@ struct SlotParams {
     float scale, scale_log2;
     float *h2o_scores;              // optional: add this step's probabilities (one split)
     float h2o_keep, h2o_add;        // scores = keep * scores + add * p
+    SlotRows rows;                  // dense or paged K / V rows
     int *status;
 };
 
@@ -104,8 +105,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         if (lane == 0 && ntiles > 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            const int row0 = unit * p.C + t_begin;
             for (int i = 0; i < ntiles; ++i) {
+                // a tile is one page in the paged layout (t_begin is a multiple of 64);
+                // a bad table entry reads past the pool (zero fill) and is flagged
+                long row = p.rows.row(unit, t_begin + i * TILE);
+                if (row < 0) {
+                    flag_error(p.status, DEV_CAPACITY);
+                    row = (long)p.rows.num_pages * TILE;
+                }
                 const int st = i % Cfg::NSTAGE;
                 if (i >= Cfg::NSTAGE && !mbar_wait(&empty[st], ((i / Cfg::NSTAGE) & 1) ^ 1)) {
                     flag_error(p.status, DEV_TIMEOUT);
@@ -116,8 +123,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 mbar_arrive_expect_tx(&full[st], Cfg::STAGE_BYTES);
 #pragma unroll
                 for (int j = 0; j < Cfg::NBOX; ++j) {
-                    tma_load_2d(kt + j * TILE * 128, &tmK, &full[st], 64 * j, row0 + i * TILE);
-                    tma_load_2d(vt + j * TILE * 128, &tmV, &full[st], 64 * j, row0 + i * TILE);
+                    tma_load_2d(kt + j * TILE * 128, &tmK, &full[st], 64 * j, (int)row);
+                    tma_load_2d(vt + j * TILE * 128, &tmV, &full[st], 64 * j, (int)row);
                 }
             }
         }
@@ -392,7 +399,8 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
 {
     const int units = a.B * a.Hkv;
     CUtensorMap tk, tv;
-    const uint64_t rows = (uint64_t)units * a.C;
+    const uint64_t rows =
+        a.block_table ? (uint64_t)a.num_pages * TILE : (uint64_t)units * a.C;
     if (!encode_tmap_2d_f16(&tk, a.K, a.D, rows, 64, TILE) ||
         !encode_tmap_2d_f16(&tv, a.V, a.D, rows, 64, TILE))
         return cudaErrorInvalidValue;
@@ -415,6 +423,7 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
     sp.h2o_scores = a.splits == 1 ? a.h2o_scores : nullptr;
     sp.h2o_keep = a.h2o_keep;
     sp.h2o_add = a.h2o_add;
+    sp.rows = SlotRows{a.block_table, a.C, a.num_pages};
     sp.status = dev_status_ptr();
     const int grid = units * a.splits;
     cudaError_t e = a.D == 128 ? launch_slots_impl<128>(tk, tv, sp, grid, s)

@@ -38,6 +38,7 @@ struct EvictParams {
     float *scores;
     int n_heavy, n_recent, n_sink, prompt_len;
     int trigger;        // H2O: units with n < trigger are left unchanged
+    SlotRows rows;      // K / V rows of each slot (dense or paged)
     double keep_ratio;
     uint32_t seed_lo, seed_hi, epoch;
     int *status;
@@ -323,12 +324,18 @@ __global__ void __launch_bounds__(ETHREADS) k_evict(const EvictParams p)
         for (int k = warp; k < cnt; k += NWARPS) {
             const size_t src = (size_t)unit * p.C + sh.mv_src[k];
             const size_t dst = (size_t)unit * p.C + sh.mv_dst[k];
+            const long rs = p.rows.row(unit, sh.mv_src[k]), rd = p.rows.row(unit, sh.mv_dst[k]);
             uint4 *K4 = reinterpret_cast<uint4 *>(p.K), *V4 = reinterpret_cast<uint4 *>(p.V);
-            for (int ch = lane; ch < 2 * chunks; ch += 32) {
-                if (ch < chunks)
-                    K4[dst * chunks + ch] = K4[src * chunks + ch];
-                else
-                    V4[dst * chunks + ch - chunks] = V4[src * chunks + ch - chunks];
+            if (rs < 0 || rd < 0) {   // no page behind a slot: skip the row, flag it
+                if (lane == 0)
+                    flag_error(p.status, DEV_CAPACITY);
+            } else {
+                for (int ch = lane; ch < 2 * chunks; ch += 32) {
+                    if (ch < chunks)
+                        K4[rd * chunks + ch] = K4[rs * chunks + ch];
+                    else
+                        V4[rd * chunks + ch - chunks] = V4[rs * chunks + ch - chunks];
+                }
             }
             if (lane == 0) {
                 p.pos[dst] = p.pos[src];
@@ -531,13 +538,20 @@ __global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams 
         while (m) {
             const int l = __ffs(m) - 1;
             m &= m - 1;
+            const int hole = s_hole[warp][done++];
             const size_t src = (size_t)unit * p.C + base + l;
-            const size_t dst = (size_t)unit * p.C + s_hole[warp][done++];
-            for (int ch = lane; ch < 2 * chunks; ch += 32) {
-                if (ch < chunks)
-                    K4[dst * chunks + ch] = K4[src * chunks + ch];
-                else
-                    V4[dst * chunks + ch - chunks] = V4[src * chunks + ch - chunks];
+            const size_t dst = (size_t)unit * p.C + hole;
+            const long rs = p.rows.row(unit, base + l), rd = p.rows.row(unit, hole);
+            if (rs < 0 || rd < 0) {   // no page behind a slot: skip the row, flag it
+                if (lane == 0)
+                    flag_error(p.status, DEV_CAPACITY);
+            } else {
+                for (int ch = lane; ch < 2 * chunks; ch += 32) {
+                    if (ch < chunks)
+                        K4[rd * chunks + ch] = K4[rs * chunks + ch];
+                    else
+                        V4[rd * chunks + ch - chunks] = V4[rs * chunks + ch - chunks];
+                }
             }
             if (lane == 0) {
                 p.pos[dst] = p.pos[src];
@@ -575,6 +589,7 @@ cudaError_t launch_evict(const EvictLaunch &e, cudaStream_t s)
     p.n_sink = e.n_sink;
     p.prompt_len = e.prompt_len;
     p.trigger = e.trigger;
+    p.rows = SlotRows{e.c.block_table, e.c.C, e.c.num_pages};
     p.keep_ratio = e.keep_ratio;
     p.seed_lo = (uint32_t)(e.seed & 0xffffffffu);
     p.seed_hi = (uint32_t)(e.seed >> 32);

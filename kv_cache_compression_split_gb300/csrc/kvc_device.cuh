@@ -35,6 +35,26 @@ __device__ __forceinline__ void flag_error(int *status, int bit)
         atomicOr(status, bit);
 }
 
+// ---------------------------------------------------------------- slot rows
+
+constexpr int PAGE_SLOTS = 64;   // KVC_PAGE_SLOTS
+
+// Row of the K / V arrays that slot `slot` of unit `unit` occupies: unit * C +
+// slot in the dense layout; block_table[unit][slot / 64] * 64 + slot % 64 in
+// the paged layout (the arrays are then page pools).  -1 when the table entry
+// lies outside the pool.
+struct SlotRows {
+    const int32_t *table;   // nullptr: dense layout
+    int C, num_pages;
+    __device__ __forceinline__ long row(int unit, int slot) const
+    {
+        if (!table)
+            return (long)unit * C + slot;
+        const int pg = table[(size_t)unit * (C / PAGE_SLOTS) + slot / PAGE_SLOTS];
+        return (pg < 0 || pg >= num_pages) ? -1L : (long)pg * PAGE_SLOTS + slot % PAGE_SLOTS;
+    }
+};
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)

@@ -45,6 +45,8 @@ struct AttendLaunch {
     float scale;
     float *h2o_scores;
     float h2o_keep, h2o_add;   // scores = keep * scores + add * p
+    const int32_t *block_table; // paged layout (nullptr: dense)
+    int num_pages;
 };
 cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s);
 

@@ -58,6 +58,11 @@ def test_null_arguments_are_rejected_without_touching_a_gpu(kvc):
     assert lib.kvc_stream_evict(ctypes.byref(d), 1, 1, None) == kvc.KVC_ERR_INVALID_ARG
     q = kvc.QuantCacheDesc(1, 1, 128, 3, 16, 32, 16, 16, 16, 16, 16)
     assert lib.kvc_append_quant(ctypes.byref(q), None, None, 0, None) == kvc.KVC_ERR_UNSUPPORTED
+    # paged layout: C must be whole pages and the pool must not be empty
+    d = kvc.SlotCacheDesc(1, 1, 128, 100, 16, 16, 16, 16, 16, 16, 4)
+    assert lib.kvc_stream_evict(ctypes.byref(d), 1, 1, None) == kvc.KVC_ERR_INVALID_ARG
+    d = kvc.SlotCacheDesc(1, 1, 128, 128, 16, 16, 16, 16, 16, 16, 0)
+    assert lib.kvc_stream_evict(ctypes.byref(d), 1, 1, None) == kvc.KVC_ERR_INVALID_ARG
     # batched H2O eviction: null cache, and a trigger that is not positive
     assert lib.kvc_h2o_evict_when(None, None, 64, 448, 563, None) == kvc.KVC_ERR_INVALID_ARG
     d = kvc.SlotCacheDesc(1, 1, 128, 16, 16, 16, 16, 16, 16)

@@ -1,0 +1,180 @@
+"""Paged slot-cache layout (block tables of 64-slot pages in a shared pool).
+
+Every slot-cache operation runs on a dense cache and on a paged cache whose units own shuffled
+pages of one pool; the paged run must give bit-identical logical contents (K, V, pos, n,
+scores) and outputs -- the dense path is pinned to the oracle by the other test files.  A
+ragged batch (units holding only the pages they need, -1 beyond) is checked against the oracle
+directly, and a write through a missing page is skipped and flagged."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_o_close, device_status_clean, np16
+
+pytestmark = pytest.mark.gpu
+SEED = 0x243F6A8885A308D3
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    import kv_cache_compression_split_gb300 as k
+    k.lib()
+    return k
+
+
+def _gather(cache):
+    """Logical [B, Hkv, C, D] K and V of a paged cache (through its block table)."""
+    B, Hkv, C, D = cache.B, cache.Hkv, cache.C, cache.D
+    tbl = cache.block_table.long().clamp(min=0)                     # [B, Hkv, C/64]
+    rows = (tbl[..., :, None] * 64 + torch.arange(64, device=tbl.device)).reshape(B, Hkv, C)
+    K = cache.K.reshape(-1, D)[rows.reshape(-1)].reshape(B, Hkv, C, D)
+    V = cache.V.reshape(-1, D)[rows.reshape(-1)].reshape(B, Hkv, C, D)
+    return K, V
+
+
+def _assert_same(dense, paged, scores_d=None, scores_p=None):
+    torch.cuda.synchronize()
+    assert torch.equal(dense.n, paged.n) and torch.equal(dense.seqlen, paged.seqlen)
+    Kp, Vp = _gather(paged)
+    for b in range(dense.B):
+        for h in range(dense.Hkv):
+            nn = int(dense.n[b, h])
+            assert torch.equal(dense.pos[b, h, :nn], paged.pos[b, h, :nn])
+            assert torch.equal(dense.K[b, h, :nn], Kp[b, h, :nn]), (b, h)
+            assert torch.equal(dense.V[b, h, :nn], Vp[b, h, :nn]), (b, h)
+            if scores_d is not None:
+                assert torch.equal(scores_d[b, h, :nn], scores_p[b, h, :nn])
+
+
+def _attend(kvc, cache, q, logits=False, scores=None, decay=0.0):
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device="cuda")
+    lg = torch.empty(q.shape[0], q.shape[1], cache.C, dtype=torch.float32, device="cuda") \
+        if logits else None
+    splits = 1 if scores is not None else 0
+    ws = torch.empty(max(kvc.kvc_workspace_size(cache, q, splits) // 4, 1), device="cuda")
+    kvc.kvc_decode_attend(cache, q, o, logits=lg, lse=lse, workspace=ws, num_splits=splits,
+                          h2o_scores=scores, h2o_decay=decay)
+    return o, lse
+
+
+def _pair(kvc, B, Hkv, C, D, spare=7, seed=0):
+    """A dense cache and a paged twin whose units own shuffled pages of one pool."""
+    dense = kvc.SlotCache.empty(B, Hkv, C, D)
+    npu = C // 64
+    num_pages = B * Hkv * npu + spare
+    perm = torch.from_numpy(np.random.default_rng(seed).permutation(num_pages)[:B * Hkv * npu]
+                            .astype(np.int32)).view(B, Hkv, npu)
+    paged = kvc.SlotCache.empty_paged(B, Hkv, C, D, num_pages, block_table=perm)
+    return dense, paged
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_paged_equals_dense_through_every_method(kvc, D):
+    B, Hq, Hkv, C, P, steps = 3, 16, 4, 704, 600, 6
+    n_heavy, n_recent, n_sink = 40, 100, 16
+    g = torch.Generator().manual_seed(D)
+    Ks = torch.randn(B, Hkv, P + steps, D, generator=g).half().cuda()
+    Vs = torch.randn(B, Hkv, P + steps, D, generator=g).half().cuda()
+    qs = torch.randn(steps + 1, B, Hq, D, generator=g).half().cuda()
+    prompt_k, prompt_v = Ks[:, :, :P].contiguous(), Vs[:, :, :P].contiguous()
+    # FP16: bulk append of the prompt, then attention (automatic splits)
+    dense, paged = _pair(kvc, B, Hkv, C, D, seed=D)
+    for c in (dense, paged):
+        kvc.kvc_append(c, prompt_k, prompt_v)
+    _assert_same(dense, paged)
+    od, ld = _attend(kvc, dense, qs[0])
+    op, lp = _attend(kvc, paged, qs[0])
+    assert torch.equal(od, op) and torch.equal(ld, lp)
+    # H2O: seeded scores, evict to budget, then decode steps with the fused update and the
+    # batched trigger; StreamingLLM and random eviction on twins of the same prompt
+    rng = np.random.default_rng(D)
+    sc0 = torch.from_numpy(rng.uniform(0, 4, (B, Hkv, C)).astype(np.float32)).cuda()
+    sd, sp = sc0.clone(), sc0.clone()
+    kvc.kvc_h2o_evict(dense, sd, n_heavy, n_recent)
+    kvc.kvc_h2o_evict(paged, sp, n_heavy, n_recent)
+    _assert_same(dense, paged, sd, sp)
+    for t in range(steps):
+        kn = Ks[:, :, P + t:P + t + 1].contiguous()
+        vn = Vs[:, :, P + t:P + t + 1].contiguous()
+        outs = []
+        for c, s in ((dense, sd), (paged, sp)):
+            kvc.kvc_append(c, kn, vn)
+            outs.append(_attend(kvc, c, qs[t + 1], logits=True, scores=s, decay=0.99))
+            kvc.kvc_h2o_evict_when(c, s, n_heavy, n_recent, n_heavy + n_recent + 3)
+        assert torch.equal(outs[0][0], outs[1][0])
+        _assert_same(dense, paged, sd, sp)
+    for evict in ("stream", "random"):
+        dense, paged = _pair(kvc, B, Hkv, C, D, seed=D + len(evict))
+        for c in (dense, paged):
+            kvc.kvc_append(c, prompt_k, prompt_v)
+            if evict == "stream":
+                kvc.kvc_stream_evict(c, n_sink, n_recent)
+            else:
+                kvc.kvc_random_evict(c, 64, 0.25, SEED, 0)
+        _assert_same(dense, paged)
+        od, _ = _attend(kvc, dense, qs[1])
+        op, _ = _attend(kvc, paged, qs[1])
+        assert torch.equal(od, op)
+    assert device_status_clean(kvc)
+
+
+def test_ragged_paged_batch_against_oracle(kvc, orc):
+    """Units of one batch hold different token counts and only the pages those need (-1
+    beyond); decode attention over them matches the oracle unit by unit."""
+    B, Hq, Hkv, D, C = 2, 8, 4, 128, 1024
+    counts = np.array([[1000, 65, 1, 640], [257, 0, 999, 64]], np.int32)
+    g = torch.Generator().manual_seed(5)
+    K = torch.randn(B, Hkv, C, D, generator=g).half()
+    V = torch.randn(B, Hkv, C, D, generator=g).half()
+    q = torch.randn(B, Hq, D, generator=g).half()
+    need = (counts + 63) // 64
+    num_pages = int(need.sum()) + 3
+    order = np.random.default_rng(6).permutation(num_pages)
+    table = np.full((B, Hkv, C // 64), -1, np.int32)
+    k = 0
+    for b in range(B):
+        for h in range(Hkv):
+            table[b, h, :need[b, h]] = order[k:k + need[b, h]]
+            k += need[b, h]
+    cache = kvc.SlotCache.empty_paged(B, Hkv, C, D, num_pages,
+                                      block_table=torch.from_numpy(table))
+    rows, src = [], []
+    for b in range(B):
+        for h in range(Hkv):
+            j = np.arange(counts[b, h])
+            rows.append(table[b, h, j // 64].astype(np.int64) * 64 + j % 64)
+            src.append((b * Hkv + h) * C + j)
+    rows = torch.from_numpy(np.concatenate(rows)).cuda()
+    src = torch.from_numpy(np.concatenate(src)).cuda()
+    cache.K.view(-1, D)[rows] = K.cuda().reshape(-1, D)[src]
+    cache.V.view(-1, D)[rows] = V.cuda().reshape(-1, D)[src]
+    cache.n.copy_(torch.from_numpy(counts).cuda())
+    cache.seqlen.copy_(torch.from_numpy(counts.max(1)).cuda())
+    for splits in (0, 1, 3):
+        o = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+        ws = torch.empty(max(kvc.kvc_workspace_size(cache, q.cuda(), splits) // 4, 1),
+                         device="cuda")
+        kvc.kvc_decode_attend(cache, q.cuda(), o, workspace=ws, num_splits=splits)
+        ref, _, _ = orc.decode_attend(np16(q), np16(K), np16(V), counts)
+        assert_o_close(np16(o), ref, what=f"splits={splits}")
+    assert device_status_clean(kvc)
+
+
+def test_write_through_a_missing_page_is_flagged(kvc):
+    """A unit whose next slot has no page (-1 entry): the append skips the row and sets the
+    capacity bit; nothing outside the pool is written."""
+    B, Hkv, D, C = 1, 2, 128, 128
+    table = torch.tensor([[[0, -1], [1, 2]]], dtype=torch.int32)
+    cache = kvc.SlotCache.empty_paged(B, Hkv, C, D, 3, block_table=table)
+    cache.n.fill_(64)                      # unit 0 is full up to its only page
+    cache.seqlen.fill_(64)
+    guard = cache.K.clone()
+    k = torch.ones(B, Hkv, 1, D, dtype=torch.float16, device="cuda")
+    kvc.kvc_append(cache, k, k)
+    torch.cuda.synchronize()
+    assert kvc.kvc_read_device_status() & kvc.KVC_DEV_CAPACITY
+    # unit 1's slot 64 landed in its second page (pool page 2, row 0); unit 0 wrote nothing
+    assert torch.equal(cache.K[2, 0], k[0, 1, 0])
+    assert torch.equal(cache.K[0], guard[0]) and torch.equal(cache.K[1], guard[1])
+    assert kvc.kvc_read_device_status() == 0
