@@ -394,6 +394,7 @@ def run_gpu(args, rank, world):
     rows.update(h2o_variant_rows(kvc, dev, stream, h2o, h2o_scores, qs[:, 1], kn[:, 1], vn[:, 1],
                                  n_heavy, n_recent))
     rows.update(random_rows(kvc, W, dev, stream))
+    rows.update(paged_rows(kvc, dev, stream, fp, kv4, qs[0, 0], T0))
 
     ms_per_step = total_ms / args.steps
     eager_ms = evs[0][0].elapsed_time(evs[-1][11]) / args.steps
@@ -462,6 +463,77 @@ def h2o_variant_rows(kvc, dev, stream, src, src_scores, qs, kn, vn, n_heavy, n_r
                                    f", evict when n >= {trig} (slots attended {budget + 1}.."
                                    f"{trig})")}
             del c, sc, ws
+    return out
+
+
+def paged_rows(kvc, dev, stream, dense, kv4, q, T):
+    """Decode attention on the heavy-load caches, dense and in the paged layout (pages of one
+    pool handed out in a shuffled order), same data: FP16 over the first T slots, and KIVI-4
+    (128-token pages of four group blocks) over the cache as the timed steps left it."""
+    import torch
+    B, Hkv, D = dense.B, dense.Hkv, dense.D
+    Cp = 64 * ((T + 63) // 64)
+    npu = Cp // 64
+    num_pages = B * Hkv * npu
+    out = {}
+    with torch.cuda.stream(stream):
+        perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(64))
+        table = perm.to(torch.int32).view(B, Hkv, npu).to(dev)
+        paged = kvc.SlotCache.empty_paged(B, Hkv, Cp, D, num_pages, block_table=table, device=dev)
+        rows = (table.long()[..., None] * 64 + torch.arange(64, device=dev)).reshape(-1)
+        src = dense.K[:, :, :Cp].reshape(-1, D)
+        paged.K.view(-1, D)[rows] = src
+        paged.V.view(-1, D)[rows] = dense.V[:, :, :Cp].reshape(-1, D)
+        paged.n.fill_(T)
+        paged.seqlen.fill_(T)
+        view = kvc.SlotCache(K=dense.K, V=dense.V, pos=dense.pos, n=torch.full_like(dense.n, T),
+                             seqlen=dense.seqlen)
+        o = torch.empty_like(q)
+        for name, c in (("fp16_attend_dense_T", view), ("fp16_attend_paged_T", paged)):
+            ws = torch.empty(max(kvc.kvc_workspace_size(c, q) // 4, 1), dtype=torch.float32,
+                             device=dev)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(6)]
+            for e0, e1 in ev:
+                e0.record(stream)
+                kvc.kvc_decode_attend(c, q, o, workspace=ws, stream=stream)
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev[1:])
+            out[name] = {"ms": ms, "slots": T,
+                         "gbs": slot_bytes(T, B, Hkv, q.shape[1], D) / (ms * 1e-3) / 1e9,
+                         "layout": "paged, 64-slot pages in shuffled order" if c is paged
+                                   else "dense"}
+        del paged
+        # KIVI-4: the same blocks, reached through a shuffled page table
+        B_, Hkv_, ng, bb = kv4.k_blocks.shape
+        npu = ng // 4
+        nump = B_ * Hkv_ * npu
+        perm = torch.randperm(nump, generator=torch.Generator().manual_seed(128))
+        ktab = perm.to(torch.int32).view(B_, Hkv_, npu).to(dev)
+        pk = kvc.QuantCache.empty_paged(B_, Hkv_, npu * 128, kv4.D, kv4.bits, kv4.R, nump,
+                                        block_table=ktab, device=dev)
+        idx = (ktab.long()[..., None] * 4 + torch.arange(4, device=dev)).reshape(-1)
+        pk.k_blocks.view(-1, bb)[idx] = kv4.k_blocks[:, :, :npu * 4].reshape(-1, bb)
+        pk.v_blocks.view(-1, bb)[idx] = kv4.v_blocks[:, :, :npu * 4].reshape(-1, bb)
+        pk.k_res.copy_(kv4.k_res)
+        pk.v_res.copy_(kv4.v_res)
+        pk.len.copy_(kv4.len)
+        for name, c in (("kivi4_attend_dense", kv4), ("kivi4_attend_paged", pk)):
+            ws = torch.empty(max(kvc.kvc_workspace_size(c, q) // 4, 1), dtype=torch.float32,
+                             device=dev)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(6)]
+            for e0, e1 in ev:
+                e0.record(stream)
+                kvc.kvc_decode_attend(c, q, o, workspace=ws, stream=stream)
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev[1:])
+            out[name] = {"ms": ms, "tokens": int(kv4.len[0]),
+                         "layout": "paged, 128-token pages in shuffled order" if c is pk
+                                   else "dense"}
+        del pk
     return out
 
 

@@ -148,7 +148,19 @@ typedef struct kvc_slot_cache {
  *     Then the V scales as D/32 rows of 32 fp16 values (row j holds channel
  *     group j of tokens 0..31), then the V zeros in the same [D/32][32] order.
  *   k_res, v_res [B, Hkv, R + 32, D] fp16 residual rings;  len [B] int32.
+ *   block_table  NULL for the dense layout above.  Paged layout: pages of
+ *                KVC_KIVI_PAGE_GROUPS = 4 consecutive groups (128 tokens);
+ *                group g of unit (b, h) is block g % 4 of page
+ *                block_table[b][h][g / 4] ([B, Hkv, Cq / 128] int32) in
+ *                k_blocks / v_blocks pools of [num_pages, 4, block_bytes].
+ *                Cq must be a multiple of 128; the ownership and error rules
+ *                are those of the paged slot cache (entries of pages a unit
+ *                does not use may be -1; a write through an entry outside
+ *                [0, num_pages) is skipped and sets KVC_DEV_CAPACITY, and a
+ *                read through one yields no data for that tile).
+ *   num_pages    pages in each pool (paged layout only)
  */
+#define KVC_KIVI_PAGE_GROUPS 4
 typedef struct kvc_quant_cache {
     int B, Hkv, D, bits, R, Cq; /* Cq: quantised-token capacity, a multiple of 32 */
     uint8_t *k_blocks;
@@ -156,6 +168,8 @@ typedef struct kvc_quant_cache {
     uint16_t *k_res;
     uint16_t *v_res;
     int32_t *len;
+    const int32_t *block_table;
+    int num_pages;
 } kvc_quant_cache;
 
 /* Bytes of one K (or V) block: 32*D*bits/8 + 4*D. */

@@ -28,6 +28,7 @@ KVC_KIND_SLOTS, KVC_KIND_KIVI = 0, 1
 KVC_H2O_DECODE, KVC_H2O_PREFILL = 0, 1
 KIVI_GROUP = 32
 PAGE_SLOTS = 64            # KVC_PAGE_SLOTS: slots per page of the paged layout
+KIVI_PAGE_GROUPS = 4       # KVC_KIVI_PAGE_GROUPS: 32-token groups per KIVI page
 KVC_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -47,7 +48,7 @@ class QuantCacheDesc(C.Structure):
     _fields_ = [("B", C.c_int), ("Hkv", C.c_int), ("D", C.c_int), ("bits", C.c_int),
                 ("R", C.c_int), ("Cq", C.c_int), ("k_blocks", C.c_void_p),
                 ("v_blocks", C.c_void_p), ("k_res", C.c_void_p), ("v_res", C.c_void_p),
-                ("len", C.c_void_p)]
+                ("len", C.c_void_p), ("block_table", C.c_void_p), ("num_pages", C.c_int)]
 
 
 class AttendArgs(C.Structure):
@@ -330,7 +331,9 @@ class SlotCache:
 
 @dataclass
 class QuantCache:
-    """KIVI cache in device memory (layout documented in include/kvc.h)."""
+    """KIVI cache in device memory (layout documented in include/kvc.h).  Dense layout:
+    k_blocks, v_blocks [B, Hkv, Cq / 32, block_bytes].  Paged layout: pools
+    [num_pages, 4, block_bytes] of 4-group (128-token) pages, block_table [B, Hkv, Cq / 128]."""
     k_blocks: torch.Tensor
     v_blocks: torch.Tensor
     k_res: torch.Tensor
@@ -338,6 +341,8 @@ class QuantCache:
     len: torch.Tensor
     bits: int
     R: int
+    block_table: Optional[torch.Tensor] = None
+    Cq_paged: int = 0
 
     @property
     def B(self): return self.k_res.shape[0]
@@ -349,7 +354,11 @@ class QuantCache:
     def D(self): return self.k_res.shape[3]
 
     @property
-    def Cq(self): return self.k_blocks.shape[2] * KIVI_GROUP
+    def Cq(self):
+        return self.Cq_paged if self.block_table is not None else self.k_blocks.shape[2] * KIVI_GROUP
+
+    @property
+    def num_pages(self): return self.k_blocks.shape[0] if self.block_table is not None else 0
 
     @classmethod
     def empty(cls, B, Hkv, Cq, D, bits, R, device="cuda"):
@@ -362,7 +371,28 @@ class QuantCache:
                    v_res=torch.zeros(B, Hkv, R + KIVI_GROUP, D, dtype=torch.float16, device=device),
                    len=torch.zeros(B, dtype=torch.int32, device=device), bits=bits, R=R)
 
+    @classmethod
+    def empty_paged(cls, B, Hkv, Cq, D, bits, R, num_pages, block_table=None, device="cuda"):
+        """Paged KIVI cache: pools of num_pages pages of 4 groups; block_table [B, Hkv, Cq / 128]
+        (default: unit u owns pages u * Cq / 128 .. (u + 1) * Cq / 128 - 1)."""
+        page = KIVI_GROUP * KIVI_PAGE_GROUPS
+        if Cq % page:
+            raise ValueError("Cq must be a multiple of 128 in the paged layout")
+        if block_table is None:
+            block_table = torch.arange(B * Hkv * (Cq // page), dtype=torch.int32,
+                                       device=device).view(B, Hkv, Cq // page)
+        bb = KIVI_GROUP * D * bits // 8 + 4 * D
+        pool = (num_pages, KIVI_PAGE_GROUPS, bb)
+        return cls(k_blocks=torch.zeros(pool, dtype=torch.uint8, device=device),
+                   v_blocks=torch.zeros(pool, dtype=torch.uint8, device=device),
+                   k_res=torch.zeros(B, Hkv, R + KIVI_GROUP, D, dtype=torch.float16, device=device),
+                   v_res=torch.zeros(B, Hkv, R + KIVI_GROUP, D, dtype=torch.float16, device=device),
+                   len=torch.zeros(B, dtype=torch.int32, device=device), bits=bits, R=R,
+                   block_table=block_table.to(device=device, dtype=torch.int32).contiguous(),
+                   Cq_paged=Cq)
+
     def desc(self) -> QuantCacheDesc:
         return QuantCacheDesc(self.B, self.Hkv, self.D, self.bits, self.R, self.Cq,
                               _ptr(self.k_blocks), _ptr(self.v_blocks), _ptr(self.k_res),
-                              _ptr(self.v_res), _ptr(self.len))
+                              _ptr(self.v_res), _ptr(self.len), _ptr(self.block_table),
+                              self.num_pages)

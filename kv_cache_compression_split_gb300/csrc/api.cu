@@ -152,6 +152,10 @@ kvc_status check_quant_cache(const kvc_quant_cache *c)
         return KVC_ERR_INVALID_ARG;
     if (!head_dim_ok(c->D) || (c->bits != 2 && c->bits != 4))
         return KVC_ERR_UNSUPPORTED;
+    if (c->block_table) {   // paged layout: whole pages of 4 groups, a pool of num_pages
+        if (c->Cq % (KVC_KIVI_GROUP * KVC_KIVI_PAGE_GROUPS) != 0 || c->num_pages <= 0)
+            return KVC_ERR_INVALID_ARG;
+    }
     if (!aligned16(c->k_blocks) || !aligned16(c->v_blocks) || !aligned16(c->k_res) ||
         !aligned16(c->v_res))
         return KVC_ERR_INVALID_ARG;
@@ -310,7 +314,8 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
     float *part_ml = part_o ? part_o + (size_t)f.B * a->Hq * f.plan.splits * f.D : nullptr;
     KiviAttendLaunch L{f.B, a->Hq, c.Hkv, c.D, c.bits, c.R, c.Cq, a->q, a->o, c.k_blocks,
                        c.v_blocks, c.k_res, c.v_res, c.len, a->lse, part_o, part_ml,
-                       f.plan.splits, f.plan.tiles_per_split, scale};
+                       f.plan.splits, f.plan.tiles_per_split, scale, c.block_table,
+                       c.num_pages};
     return from_cuda(launch_attend_kivi(L, stream));
 }
 

@@ -386,10 +386,10 @@ __global__ void __launch_bounds__(QTHREADS)
     k_append_quant(int Hkv, int R, int Cq, int n_new, const uint16_t *__restrict__ k_new,
                    const uint16_t *__restrict__ v_new, uint8_t *__restrict__ kb,
                    uint8_t *__restrict__ vb, uint16_t *__restrict__ k_res,
-                   uint16_t *__restrict__ v_res, const int32_t *__restrict__ len, int *status)
+                   uint16_t *__restrict__ v_res, const int32_t *__restrict__ len,
+                   const GroupBlocks blocks, int *status)
 {
     constexpr int G = KIVI_G;
-    constexpr int BLOCK = G * D * BITS / 8 + 4 * D;
     __shared__ GroupSmem<D> sm;
 
     const int unit = blockIdx.x;
@@ -408,10 +408,15 @@ __global__ void __launch_bounds__(QTHREADS)
     if (GROUPS) {
         const uint16_t *kr = k_res + (size_t)unit * CR * D;
         const uint16_t *vr = v_res + (size_t)unit * CR * D;
-        for (long g = nq0 / G + blockIdx.y; g < nq1 / G; g += gridDim.y)
-            pack_group<D, BITS>(g, T0, CR, kn, vn, kr, vr,
-                                kb + ((size_t)unit * (Cq / G) + g) * BLOCK,
-                                vb + ((size_t)unit * (Cq / G) + g) * BLOCK, sm);
+        for (long g = nq0 / G + blockIdx.y; g < nq1 / G; g += gridDim.y) {
+            const long long off = blocks.offset(unit, g);
+            if (off < 0) {   // no page behind this group: skip it, flag it
+                if (threadIdx.x == 0)
+                    flag_error(status, DEV_CAPACITY);
+                continue;
+            }
+            pack_group<D, BITS>(g, T0, CR, kn, vn, kr, vr, kb + off, vb + off, sm);
+        }
     }
     if (RESIDUAL) {
         // new tokens that stay in fp16 go to ring slot p mod (R + 32)
@@ -445,7 +450,9 @@ cudaError_t launch_quant_impl(const kvc_quant_cache &c, const uint16_t *k_new,
         // decode-sized: at most two groups flush; one CTA per unit does both parts
         k_append_quant<D, BITS, true, true><<<units, QTHREADS, 0, s>>>(
             c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
-            c.len, dev_status_ptr());
+            c.len, GroupBlocks{c.block_table, c.Cq / KIVI_G, c.num_pages,
+                               KIVI_G * D * BITS / 8 + 4 * D},
+            dev_status_ptr());
     } else {
         // bulk: the flushed groups of every unit spread over the grid, then the residual
         const long max_groups = n_new / KIVI_G + 1;
@@ -454,13 +461,17 @@ cudaError_t launch_quant_impl(const kvc_quant_cache &c, const uint16_t *k_new,
         gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
         k_append_quant<D, BITS, true, false><<<dim3(units, gy), QTHREADS, 0, s>>>(
             c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
-            c.len, dev_status_ptr());
+            c.len, GroupBlocks{c.block_table, c.Cq / KIVI_G, c.num_pages,
+                               KIVI_G * D * BITS / 8 + 4 * D},
+            dev_status_ptr());
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
         k_append_quant<D, BITS, false, true><<<units, QTHREADS, 0, s>>>(
             c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
-            c.len, dev_status_ptr());
+            c.len, GroupBlocks{c.block_table, c.Cq / KIVI_G, c.num_pages,
+                               KIVI_G * D * BITS / 8 + 4 * D},
+            dev_status_ptr());
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)

@@ -53,6 +53,7 @@ template <int D, int BITS> struct KiviCfg {
     static constexpr int CODE_BYTES = G * D * BITS / 8;
     static constexpr int BLOCK = CODE_BYTES + 4 * D;
     static constexpr int QG = NCW;                     // groups per quantised tile
+    static_assert(QG == KIVI_PAGE_GROUPS, "a quantised tile is one page of the paged layout");
     static constexpr int QT_BYTES = 2 * QG * BLOCK;
     static constexpr int RS = 32;                      // ring slots per residual tile
     static constexpr int NBOX = D / 64;
@@ -72,6 +73,7 @@ struct KiviParams {
     uint16_t *o;
     float *lse;
     const uint8_t *kb, *vb;
+    GroupBlocks blocks;             // dense or paged group blocks
     const int32_t *len;
     float *part_o, *part_ml;
     float scale, scale_log2;
@@ -172,8 +174,6 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             int it = 0;
             for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
                 const KiviItem w = kivi_item<D, BITS>(p, item);
-                const uint8_t *kblocks = p.kb + (size_t)w.unit * (p.Cq / Cfg::G) * Cfg::BLOCK;
-                const uint8_t *vblocks = p.vb + (size_t)w.unit * (p.Cq / Cfg::G) * Cfg::BLOCK;
                 const int ntiles = w.nr + w.nq;   // residual tiles first, then quantised tiles
                 for (int i = 0; i < ntiles; ++i, ++it) {
                     const int st = it % Cfg::NSTAGE;
@@ -193,12 +193,20 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                                         64 * j, row);
                         }
                     } else {
+                        // a tile is 4 groups, one page in the paged layout
                         const int g0 = (w.qt0 + i - w.nr) * Cfg::QG;
                         const int ng = min(Cfg::QG, w.n_groups - g0);
-                        mbar_arrive_expect_tx(&full[st], 2 * ng * Cfg::BLOCK);
-                        bulk_load(dst, kblocks + (size_t)g0 * Cfg::BLOCK, ng * Cfg::BLOCK, &full[st]);
-                        bulk_load(dst + Cfg::QG * Cfg::BLOCK, vblocks + (size_t)g0 * Cfg::BLOCK,
-                                  ng * Cfg::BLOCK, &full[st]);
+                        const long long off = p.blocks.offset(w.unit, g0);
+                        if (off < 0) {
+                            // no page behind the tile: no copy, the stage completes empty
+                            flag_error(p.status, DEV_CAPACITY);
+                            mbar_arrive(&full[st]);
+                        } else {
+                            mbar_arrive_expect_tx(&full[st], 2 * ng * Cfg::BLOCK);
+                            bulk_load(dst, p.kb + off, ng * Cfg::BLOCK, &full[st]);
+                            bulk_load(dst + Cfg::QG * Cfg::BLOCK, p.vb + off, ng * Cfg::BLOCK,
+                                      &full[st]);
+                        }
                     }
                 }
             }
@@ -671,6 +679,8 @@ cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s)
     kp.lse = a.lse;
     kp.kb = a.kb;
     kp.vb = a.vb;
+    kp.blocks = GroupBlocks{a.block_table, a.Cq / KIVI_G, a.num_pages,
+                            (int)kvc_kivi_block_bytes(a.D, a.bits)};
     kp.len = a.len;
     kp.part_o = a.splits > 1 ? a.part_o : nullptr;
     kp.part_ml = a.splits > 1 ? a.part_ml : nullptr;

@@ -55,6 +55,25 @@ struct SlotRows {
     }
 };
 
+// Byte offset of group block g of unit `unit` in a KIVI block array: dense
+// (unit * Cq / 32 + g) * block; paged (block_table[unit][g / 4] * 4 + g % 4) *
+// block.  -1 when the table entry lies outside the pool.
+constexpr int KIVI_PAGE_GROUPS = 4;   // KVC_KIVI_PAGE_GROUPS
+struct GroupBlocks {
+    const int32_t *table;   // nullptr: dense layout
+    int groups_per_unit, num_pages, block;
+    __device__ __forceinline__ long long offset(int unit, long g) const
+    {
+        if (!table)
+            return ((long long)unit * groups_per_unit + g) * block;
+        const int pg = table[(size_t)unit * (groups_per_unit / KIVI_PAGE_GROUPS) +
+                             g / KIVI_PAGE_GROUPS];
+        if (pg < 0 || pg >= num_pages)
+            return -1;
+        return ((long long)pg * KIVI_PAGE_GROUPS + g % KIVI_PAGE_GROUPS) * block;
+    }
+};
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)

@@ -61,6 +61,8 @@ struct KiviAttendLaunch {
     float *part_o, *part_ml;
     int splits, tiles_per_split;
     float scale;
+    const int32_t *block_table;  // paged group blocks (nullptr: dense)
+    int num_pages;
 };
 cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s);
 

@@ -178,3 +178,102 @@ def test_write_through_a_missing_page_is_flagged(kvc):
     assert torch.equal(cache.K[2, 0], k[0, 1, 0])
     assert torch.equal(cache.K[0], guard[0]) and torch.equal(cache.K[1], guard[1])
     assert kvc.kvc_read_device_status() == 0
+
+
+def _gather_kivi(cache):
+    """Logical [B, Hkv, Cq/32, block] K and V blocks of a paged KIVI cache."""
+    B, Hkv, Cq = cache.B, cache.Hkv, cache.Cq
+    tbl = cache.block_table.long().clamp(min=0)                     # [B, Hkv, Cq/128]
+    idx = (tbl[..., :, None] * 4 + torch.arange(4, device=tbl.device)).reshape(-1)
+    bb = cache.k_blocks.shape[-1]
+    kb = cache.k_blocks.reshape(-1, bb)[idx].reshape(B, Hkv, Cq // 32, bb)
+    vb = cache.v_blocks.reshape(-1, bb)[idx].reshape(B, Hkv, Cq // 32, bb)
+    return kb, vb
+
+
+def _attend_kivi(kvc, cache, q, splits=0):
+    o = torch.empty_like(q)
+    ws = torch.empty(max(kvc.kvc_workspace_size(cache, q, splits) // 4, 1), device="cuda")
+    kvc.kvc_decode_attend(cache, q, o, workspace=ws, num_splits=splits)
+    return o
+
+
+@pytest.mark.parametrize("D,bits,R", [(128, 4, 128), (128, 2, 16), (64, 4, 32)])
+def test_paged_kivi_equals_dense(kvc, D, bits, R):
+    B, Hq, Hkv, P, steps, Cq = 3, 8, 2, 500, 40, 640
+    g = torch.Generator().manual_seed(D + bits + R)
+    Ks = torch.randn(B, Hkv, P + steps, D, generator=g).half().cuda()
+    Vs = torch.randn(B, Hkv, P + steps, D, generator=g).half().cuda()
+    q = torch.randn(B, Hq, D, generator=g).half().cuda()
+    npu = Cq // 128
+    num_pages = B * Hkv * npu + 5
+    perm = torch.from_numpy(np.random.default_rng(D + bits).permutation(num_pages)
+                            [:B * Hkv * npu].astype(np.int32)).view(B, Hkv, npu)
+    dense = kvc.QuantCache.empty(B, Hkv, Cq, D, bits, R)
+    paged = kvc.QuantCache.empty_paged(B, Hkv, Cq, D, bits, R, num_pages, block_table=perm)
+    for c in (dense, paged):
+        kvc.kvc_append_quant(c, Ks[:, :, :P].contiguous(), Vs[:, :, :P].contiguous())
+    for t in range(steps + 1):
+        if t > 0:
+            for c in (dense, paged):
+                kvc.kvc_append_quant(c, Ks[:, :, P + t - 1:P + t].contiguous(),
+                                     Vs[:, :, P + t - 1:P + t].contiguous())
+        if t % 8 == 0:
+            torch.cuda.synchronize()
+            kb, vb = _gather_kivi(paged)
+            n_groups = (P + t - R) // 32 if P + t > R else 0
+            assert torch.equal(dense.k_blocks[:, :, :n_groups], kb[:, :, :n_groups])
+            assert torch.equal(dense.v_blocks[:, :, :n_groups], vb[:, :, :n_groups])
+            assert torch.equal(dense.k_res, paged.k_res) and torch.equal(dense.v_res, paged.v_res)
+            for splits in (0, 2):
+                assert torch.equal(_attend_kivi(kvc, dense, q, splits),
+                                   _attend_kivi(kvc, paged, q, splits))
+    assert device_status_clean(kvc)
+
+
+def test_ragged_paged_kivi_against_oracle(kvc, orc):
+    """Sequences of different lengths in one paged KIVI batch, each unit holding only the pages
+    its quantised groups need (-1 beyond): blocks bit-exact and attention matches the oracle."""
+    B, Hq, Hkv, D, bits, R, Cq = 3, 8, 2, 128, 4, 128, 1024
+    lens = [1100, 130, 600]
+    g = torch.Generator().manual_seed(77)
+    T = max(lens)
+    K = torch.randn(B, Hkv, T, D, generator=g).half()
+    V = torch.randn(B, Hkv, T, D, generator=g).half()
+    q = torch.randn(B, Hq, D, generator=g).half()
+    n_q = [orc.kivi_nq(L, R) for L in lens]
+    need = [(nq + 127) // 128 for nq in n_q]
+    num_pages = Hkv * sum(need) + 2
+    order = np.random.default_rng(78).permutation(num_pages)
+    table = np.full((B, Hkv, Cq // 128), -1, np.int32)
+    k = 0
+    for b in range(B):
+        for h in range(Hkv):
+            table[b, h, :need[b]] = order[k:k + need[b]]
+            k += need[b]
+    cache = kvc.QuantCache.empty_paged(B, Hkv, Cq, D, bits, R, num_pages,
+                                       block_table=torch.from_numpy(table))
+    # each sequence gets its own length: append per sequence through one-sequence views
+    for b in range(B):
+        view = kvc.QuantCache(k_blocks=cache.k_blocks, v_blocks=cache.v_blocks,
+                              k_res=cache.k_res[b:b + 1], v_res=cache.v_res[b:b + 1],
+                              len=cache.len[b:b + 1], bits=bits, R=R,
+                              block_table=cache.block_table[b:b + 1], Cq_paged=Cq)
+        kvc.kvc_append_quant(view, K[b:b + 1, :, :lens[b]].cuda().contiguous(),
+                             V[b:b + 1, :, :lens[b]].cuda().contiguous())
+    torch.cuda.synchronize()
+    kb, vb = _gather_kivi(cache)
+    o = _attend_kivi(kvc, cache, q.cuda())
+    gq = Hq // Hkv
+    for b in range(B):
+        for h in range(Hkv):
+            Kb, Vb = np16(K[b, h, :lens[b]]), np16(V[b, h, :lens[b]])
+            qz = orc.kivi_quantize_unit(Kb[:n_q[b]], Vb[:n_q[b]], n_q[b], bits)
+            rk, rv = orc.kivi_pack_unit(qz, D, bits)
+            ng = n_q[b] // 32
+            assert np.array_equal(kb[b, h, :ng].cpu().numpy(), rk[:ng])
+            assert np.array_equal(vb[b, h, :ng].cpu().numpy(), rv[:ng])
+            ref, _ = orc.kivi_attend_unit(np16(q[b, h * gq:(h + 1) * gq]), Kb, Vb, lens[b], R,
+                                          bits, qz=qz)
+            assert_o_close(np16(o[b, h * gq:(h + 1) * gq]), ref, what=f"b={b} h={h}")
+    assert device_status_clean(kvc)
