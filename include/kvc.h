@@ -159,6 +159,22 @@ typedef struct kvc_slot_cache {
  *                [0, num_pages) is skipped and sets KVC_DEV_CAPACITY, and a
  *                read through one yields no data for that tile).
  *   num_pages    pages in each pool (paged layout only)
+ *   k_gear, v_gear  NULL for KIVI.  GEAR (dense layout only): per group one
+ *                side block of kvc_gear_side_bytes(D) bytes, [B, Hkv, Cq/32,
+ *                side_bytes], holding a 2% sparse and a rank-2 correction of the
+ *                group's quantisation residual ("Rethinking KV Cache Compression"
+ *                guide, §2: GEAR sparsity 2%, rank 2; §16: the corrections act on
+ *                KIVI's quantisation residual).  With x_q = fl32(zero + code *
+ *                scale) and the fp32 residual e = fl32(x - x_q) of every element:
+ *                  n_s = ceil(2% * 32 * D) u16 flat indices t*D + d (ascending) of
+ *                    the entries with the largest |e| (ties: lower index), then
+ *                    their binary16 values RN16(e);
+ *                  A [2][32] binary16: orthonormal rows spanning the dominant
+ *                    2-dimensional left singular subspace of R = E with the
+ *                    sparse entries zeroed; B [2][D] binary16 = A R;
+ *                  zero padding to a multiple of 16 bytes.
+ *                Decode attention then uses x_hat = x_q + S + A^T B for the
+ *                quantised tokens.
  */
 #define KVC_KIVI_PAGE_GROUPS 4
 typedef struct kvc_quant_cache {
@@ -170,10 +186,16 @@ typedef struct kvc_quant_cache {
     int32_t *len;
     const int32_t *block_table;
     int num_pages;
+    uint8_t *k_gear;
+    uint8_t *v_gear;
 } kvc_quant_cache;
 
 /* Bytes of one K (or V) block: 32*D*bits/8 + 4*D. */
 KVC_API size_t kvc_kivi_block_bytes(int D, int bits);
+
+/* Bytes of one GEAR side block (see kvc_quant_cache): 976 for D = 128, 560 for
+ * D = 64, 0 for an unsupported D. */
+KVC_API size_t kvc_gear_side_bytes(int D);
 
 /*
  * kvc_append -- write n_new tokens per sequence into a slot cache.

@@ -48,7 +48,8 @@ class QuantCacheDesc(C.Structure):
     _fields_ = [("B", C.c_int), ("Hkv", C.c_int), ("D", C.c_int), ("bits", C.c_int),
                 ("R", C.c_int), ("Cq", C.c_int), ("k_blocks", C.c_void_p),
                 ("v_blocks", C.c_void_p), ("k_res", C.c_void_p), ("v_res", C.c_void_p),
-                ("len", C.c_void_p), ("block_table", C.c_void_p), ("num_pages", C.c_int)]
+                ("len", C.c_void_p), ("block_table", C.c_void_p), ("num_pages", C.c_int),
+                ("k_gear", C.c_void_p), ("v_gear", C.c_void_p)]
 
 
 class AttendArgs(C.Structure):
@@ -81,6 +82,7 @@ def lib():
             P, i, st = C.c_void_p, C.c_int, C.c_int
             sig = {
                 "kvc_kivi_block_bytes": (C.c_size_t, [i, i]),
+                "kvc_gear_side_bytes": (C.c_size_t, [i]),
                 "kvc_append": (st, [C.POINTER(SlotCacheDesc), P, P, i, P]),
                 "kvc_append_quant": (st, [C.POINTER(QuantCacheDesc), P, P, i, P]),
                 "kvc_workspace_size": (C.c_size_t, [C.POINTER(AttendArgs)]),
@@ -173,6 +175,10 @@ def _attend_args(cache, q, o, logits=None, lse=None, workspace=None, num_splits=
     a.h2o_scores = _ptr(h2o_scores)
     a.h2o_decay = float(h2o_decay)
     return a, keep
+
+
+def kvc_gear_side_bytes(D: int) -> int:
+    return int(lib().kvc_gear_side_bytes(D))
 
 
 def kvc_workspace_size(cache, q, num_splits: int = 0) -> int:
@@ -343,6 +349,8 @@ class QuantCache:
     R: int
     block_table: Optional[torch.Tensor] = None
     Cq_paged: int = 0
+    k_gear: Optional[torch.Tensor] = None   # GEAR side blocks [B, Hkv, Cq / 32, side_bytes]
+    v_gear: Optional[torch.Tensor] = None
 
     @property
     def B(self): return self.k_res.shape[0]
@@ -361,15 +369,21 @@ class QuantCache:
     def num_pages(self): return self.k_blocks.shape[0] if self.block_table is not None else 0
 
     @classmethod
-    def empty(cls, B, Hkv, Cq, D, bits, R, device="cuda"):
+    def empty(cls, B, Hkv, Cq, D, bits, R, device="cuda", gear=False):
+        """KIVI cache; gear=True adds the GEAR side blocks (sparse + rank-2 corrections)."""
         assert Cq % KIVI_GROUP == 0
         bb = KIVI_GROUP * D * bits // 8 + 4 * D
         ng = Cq // KIVI_GROUP
+        sb = kvc_gear_side_bytes(D) if gear else 0
         return cls(k_blocks=torch.zeros(B, Hkv, ng, bb, dtype=torch.uint8, device=device),
                    v_blocks=torch.zeros(B, Hkv, ng, bb, dtype=torch.uint8, device=device),
                    k_res=torch.zeros(B, Hkv, R + KIVI_GROUP, D, dtype=torch.float16, device=device),
                    v_res=torch.zeros(B, Hkv, R + KIVI_GROUP, D, dtype=torch.float16, device=device),
-                   len=torch.zeros(B, dtype=torch.int32, device=device), bits=bits, R=R)
+                   len=torch.zeros(B, dtype=torch.int32, device=device), bits=bits, R=R,
+                   k_gear=torch.zeros(B, Hkv, ng, sb, dtype=torch.uint8, device=device)
+                   if gear else None,
+                   v_gear=torch.zeros(B, Hkv, ng, sb, dtype=torch.uint8, device=device)
+                   if gear else None)
 
     @classmethod
     def empty_paged(cls, B, Hkv, Cq, D, bits, R, num_pages, block_table=None, device="cuda"):
@@ -395,4 +409,4 @@ class QuantCache:
         return QuantCacheDesc(self.B, self.Hkv, self.D, self.bits, self.R, self.Cq,
                               _ptr(self.k_blocks), _ptr(self.v_blocks), _ptr(self.k_res),
                               _ptr(self.v_res), _ptr(self.len), _ptr(self.block_table),
-                              self.num_pages)
+                              self.num_pages, _ptr(self.k_gear), _ptr(self.v_gear))

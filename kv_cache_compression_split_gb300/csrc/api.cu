@@ -156,6 +156,14 @@ kvc_status check_quant_cache(const kvc_quant_cache *c)
         if (c->Cq % (KVC_KIVI_GROUP * KVC_KIVI_PAGE_GROUPS) != 0 || c->num_pages <= 0)
             return KVC_ERR_INVALID_ARG;
     }
+    if (!c->k_gear != !c->v_gear)
+        return KVC_ERR_INVALID_ARG;
+    if (c->k_gear) {        // GEAR side blocks: dense layout only
+        if (c->block_table)
+            return KVC_ERR_UNSUPPORTED;
+        if (!aligned16(c->k_gear) || !aligned16(c->v_gear))
+            return KVC_ERR_INVALID_ARG;
+    }
     if (!aligned16(c->k_blocks) || !aligned16(c->v_blocks) || !aligned16(c->k_res) ||
         !aligned16(c->v_res))
         return KVC_ERR_INVALID_ARG;
@@ -225,6 +233,15 @@ using namespace kvc;
 
 extern "C" {
 
+size_t kvc_gear_side_bytes(int D)
+{
+    if (!head_dim_ok(D))
+        return 0;
+    const int ns = (2 * KIVI_G * D + 99) / 100;   // ceil(2% of the group's 32 x D entries)
+    const int raw = 4 * ns + 4 * KIVI_G + 4 * D;   // indices, values, A [2][32], B [2][D]
+    return (size_t)((raw + 15) / 16 * 16);
+}
+
 size_t kvc_kivi_block_bytes(int D, int bits)
 {
     if (!head_dim_ok(D) || (bits != 2 && bits != 4))
@@ -277,6 +294,8 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         return KVC_ERR_INVALID_ARG;
     if (a->kind == KVC_KIND_KIVI && (a->logits || a->h2o_scores))
         return KVC_ERR_UNSUPPORTED;
+    if (a->kind == KVC_KIND_KIVI && a->quant->k_gear)
+        return KVC_ERR_UNSUPPORTED;   // GEAR decode: see kvc_gear_attend below
     if (a->h2o_scores && (!a->logits || !a->lse))
         return KVC_ERR_INVALID_ARG;
     float h2o_keep = 1.f, h2o_add = 1.f;

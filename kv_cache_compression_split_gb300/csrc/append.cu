@@ -206,7 +206,19 @@ template <int D> struct __align__(16) GroupSmem {
     long long zfix[2 * D];       // per K channel, then per V (token, channel group)
     long long sfix[2 * D];
     float zf[2 * D];             // zero as fp32
+    float sf[2 * D];             // scale as fp32
     float inv[2 * D];            // 1 / scale (an estimate; the remainder fixes the code)
+};
+
+// Extra staging of the GEAR side data of one matrix (K, then V) of a group.
+template <int D> struct __align__(16) GearSmem {
+    float e[KIVI_G][D + 1];      // residual, then R (sparse entries zeroed); rows padded
+    float gm[KIVI_G][KIVI_G + 1];
+    float gm2[KIVI_G][KIVI_G + 1];
+    float a[2][KIVI_G];          // orthonormal left factors
+    int hist[256];
+    int scan[QTHREADS / 32 + 1];
+    int misc[2];
 };
 
 // quant_code_inv with a fast path: the fp32 estimate is within 3e-6 of the
@@ -229,15 +241,261 @@ __device__ __forceinline__ int quant_code_fast(uint16_t xb, float zero_f, float 
     return c < 0 ? 0 : (c > cmax ? cmax : c);
 }
 
+// Exclusive prefix sum over the CTA of one value per thread (sh: QTHREADS/32 + 1 ints).
+__device__ __forceinline__ int block_exclusive_scan(int v, int *sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        sh[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < QTHREADS / 32 ? sh[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o)
+                w += y;
+        }
+        if (lane < QTHREADS / 32)
+            sh[lane] = w;                      // inclusive prefix of the warp totals
+    }
+    __syncthreads();
+    const int before = warp > 0 ? sh[warp - 1] : 0;
+    __syncthreads();                           // sh may be reused right after
+    return before + x - v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// dst = src * src for a symmetric 32 x 32 matrix, a 2 x 2 block of the product
+// per thread (256 threads).
+__device__ __forceinline__ void square32(const float (*src)[KIVI_G + 1], float (*dst)[KIVI_G + 1])
+{
+    const int a = threadIdx.x / 16, b2 = threadIdx.x % 16;
+    float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < KIVI_G; ++k) {
+        const float r0 = src[2 * a][k], r1 = src[2 * a + 1][k];
+        const float c0 = src[k][2 * b2], c1 = src[k][2 * b2 + 1];
+        s00 = fmaf(r0, c0, s00);
+        s01 = fmaf(r0, c1, s01);
+        s10 = fmaf(r1, c0, s10);
+        s11 = fmaf(r1, c1, s11);
+    }
+    dst[2 * a][2 * b2] = s00;
+    dst[2 * a][2 * b2 + 1] = s01;
+    dst[2 * a + 1][2 * b2] = s10;
+    dst[2 * a + 1][2 * b2 + 1] = s11;
+}
+
+// Orthonormalise the two columns (x0, x1) a warp holds, one row per lane; a
+// column with no length left becomes a unit vector orthogonal to the other.
+__device__ __forceinline__ void orthonormalise2(float &x0, float &x1)
+{
+    const int lane = threadIdx.x & 31;
+    float n0 = warp_sum(x0 * x0);
+    if (n0 > 1e-30f)
+        x0 *= rsqrtf(n0);
+    else
+        x0 = lane == 0 ? 1.f : 0.f;
+    x1 -= warp_sum(x0 * x1) * x0;
+    float n1 = warp_sum(x1 * x1);
+    if (!(n1 > 1e-24f)) {
+        const float x0_first = __shfl_sync(0xffffffffu, x0, 0);
+        x1 = lane == (fabsf(x0_first) > 0.7f ? 1 : 0) ? 1.f : 0.f;
+        x1 -= warp_sum(x0 * x1) * x0;
+        n1 = warp_sum(x1 * x1);
+    }
+    x1 *= rsqrtf(n1);
+}
+
+// GEAR side block of one matrix of the group (K when ISK, else V), written to
+// `side`: the residual e = fl32(x - fl32(zero + code * scale)) of every element,
+// the n_s entries with the largest |e| (ties: lower flat index) as ascending u16
+// flat indices and binary16 values, and a rank-2 factorisation A^T B of the
+// rest R: A [2][32] orthonormal rows spanning the dominant left singular
+// subspace, B = A R; both binary16.  The subspace comes from 16 steps of
+// subspace iteration on (R R^T)^4 (R R^T scaled by its largest entry, then
+// squared twice), started from R R^T times a constant and a ramp.  All threads
+// of the CTA.
+template <int D, int BITS, bool ISK>
+__device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &gs, uint8_t *side)
+{
+    constexpr int G = KIVI_G, NG = D / G, N = G * D, PER = N / QTHREADS;
+    constexpr int NS = (2 * G * D + 99) / 100;
+    constexpr int RAW = 4 * NS + 4 * G + 4 * D;
+    constexpr int SIDE = (RAW + 15) / 16 * 16;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // 1. residual of my PER contiguous elements (flat index tid * PER + u)
+    uint32_t key[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int i = tid * PER + u, t = i / D, d = i % D;
+        const int pi = ISK ? d : D + t * NG + d / G;
+        const float x = __half2float(__ushort_as_half(ISK ? sm.xk[t][d] : sm.xv[t][d]));
+        const float code = (float)(ISK ? sm.ck[t][d] : sm.cv[t][d]);
+        const float e = x - fmaf(code, sm.sf[pi], sm.zf[pi]);
+        gs.e[t][d] = e;
+        key[u] = __float_as_uint(fabsf(e));
+    }
+    // 2. the NS-th largest key: radix select, 8-bit digits from the top
+    uint32_t prefix = 0, mask = 0;
+    int need = NS;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += QTHREADS)
+            gs.hist[i] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < PER; ++u)
+            if ((key[u] & mask) == prefix)
+                atomicAdd(&gs.hist[(key[u] >> shift) & 255], 1);
+        __syncthreads();
+        if (tid == 0) {
+            int cum = 0, dg = 255;
+            for (; dg > 0; --dg) {
+                if (cum + gs.hist[dg] >= need)
+                    break;
+                cum += gs.hist[dg];
+            }
+            gs.misc[0] = dg;
+            gs.misc[1] = need - cum;
+        }
+        __syncthreads();
+        prefix |= (uint32_t)gs.misc[0] << shift;
+        mask |= 255u << shift;
+        need = gs.misc[1];
+        __syncthreads();
+    }
+    // 3. keep every key above the threshold and the first `need` equal to it (flat order)
+    int ties = 0;
+#pragma unroll
+    for (int u = 0; u < PER; ++u)
+        ties += key[u] == prefix;
+    int rank = block_exclusive_scan(ties, gs.scan);
+    bool sel[PER];
+    int nsel = 0;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        sel[u] = key[u] > prefix || (key[u] == prefix && rank++ < need);
+        nsel += sel[u];
+    }
+    int o = block_exclusive_scan(nsel, gs.scan);
+    uint16_t *idx_out = reinterpret_cast<uint16_t *>(side);
+    __half *val_out = reinterpret_cast<__half *>(side + 2 * NS);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        if (sel[u] && o < NS) {                // exactly NS are selected; the bound is a guard
+            const int i = tid * PER + u, t = i / D, d = i % D;
+            idx_out[o] = (uint16_t)i;
+            val_out[o] = __float2half_rn(gs.e[t][d]);
+            gs.e[t][d] = 0.f;                  // R: the rest of the residual
+            ++o;
+        }
+    }
+    __syncthreads();
+    // 4. Gram matrix R R^T, a 2 x 2 block of it per thread, scaled by its largest entry
+    {
+        const int a = tid / 16, b2 = tid % 16;
+        float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
+        for (int d = 0; d < D; ++d) {
+            const float r0 = gs.e[2 * a][d], r1 = gs.e[2 * a + 1][d];
+            const float c0 = gs.e[2 * b2][d], c1 = gs.e[2 * b2 + 1][d];
+            s00 = fmaf(r0, c0, s00);
+            s01 = fmaf(r0, c1, s01);
+            s10 = fmaf(r1, c0, s10);
+            s11 = fmaf(r1, c1, s11);
+        }
+        float mx = fmaxf(fmaxf(fabsf(s00), fabsf(s01)), fmaxf(fabsf(s10), fabsf(s11)));
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+        if (lane == 0)
+            gs.scan[warp] = __float_as_int(mx);
+        __syncthreads();
+        float m = 0.f;
+#pragma unroll
+        for (int w = 0; w < QTHREADS / 32; ++w)
+            m = fmaxf(m, __int_as_float(gs.scan[w]));
+        const float inv_m = m > 0.f ? 1.f / m : 0.f;
+        gs.gm[2 * a][2 * b2] = s00 * inv_m;
+        gs.gm[2 * a][2 * b2 + 1] = s01 * inv_m;
+        gs.gm[2 * a + 1][2 * b2] = s10 * inv_m;
+        gs.gm[2 * a + 1][2 * b2 + 1] = s11 * inv_m;
+    }
+    __syncthreads();
+    square32(gs.gm, gs.gm2);                   // (R R^T)^2, entries <= 32
+    __syncthreads();
+    square32(gs.gm2, gs.gm);                   // (R R^T)^4, entries <= 32^3
+    __syncthreads();
+    // 5. dominant 2-dimensional subspace: subspace iteration in warp 0, one row per lane
+    if (warp == 0) {
+        float gr[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+            gr[j] = gs.gm[lane][j];
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            x0 += gr[j];
+            x1 = fmaf(gr[j], (float)j - 15.5f, x1);
+        }
+        orthonormalise2(x0, x1);
+        for (int it = 0; it < 16; ++it) {
+            float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                y0 = fmaf(gr[j], __shfl_sync(0xffffffffu, x0, j), y0);
+                y1 = fmaf(gr[j], __shfl_sync(0xffffffffu, x1, j), y1);
+            }
+            x0 = y0;
+            x1 = y1;
+            orthonormalise2(x0, x1);
+        }
+        gs.a[0][lane] = x0;
+        gs.a[1][lane] = x1;
+    }
+    __syncthreads();
+    // 6. factors: A [2][G] and B = A R [2][D], binary16; zero padding
+    __half *a_out = reinterpret_cast<__half *>(side + 4 * NS);
+    __half *b_out = reinterpret_cast<__half *>(side + 4 * NS + 4 * G);
+    for (int i = tid; i < 2 * G; i += QTHREADS)
+        a_out[i] = __float2half_rn(gs.a[i / G][i % G]);
+    for (int i = tid; i < 2 * D; i += QTHREADS) {
+        const int r = i / D, d = i % D;
+        float s = 0.f;
+#pragma unroll 8
+        for (int t = 0; t < G; ++t)
+            s = fmaf(gs.a[r][t], gs.e[t][d], s);
+        b_out[i] = __float2half_rn(s);
+    }
+    for (int i = RAW + tid; i < SIDE; i += QTHREADS)
+        side[i] = 0;
+    __syncthreads();
+}
+
 // Quantise and pack group g of one unit (all threads of the CTA take part):
 // gather its 32 tokens (old ones from the residual ring, new ones from the
 // input), compute the K per-channel and V per-(token, channel-group)
 // scale / zero, the codes, and write the K and V blocks.
-template <int D, int BITS>
+template <int D, int BITS, bool GEAR>
 __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16_t *kn,
                                            const uint16_t *vn, const uint16_t *kr,
                                            const uint16_t *vr, uint8_t *kblk, uint8_t *vblk,
-                                           GroupSmem<D> &sm)
+                                           GroupSmem<D> &sm, GearSmem<D> *gs, uint8_t *kside,
+                                           uint8_t *vside)
 {
     constexpr int G = KIVI_G;
     constexpr int WK = D * BITS / 32;           // u32 words per K token row
@@ -302,6 +560,7 @@ __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16
         sm.zfix[i] = q.zero_fix;
         sm.sfix[i] = q.scale_fix;
         sm.zf[i] = __half2float(__ushort_as_half(mnb));
+        sm.sf[i] = __half2float(__ushort_as_half(q.scale_bits));
         // a zero scale gives a zero reciprocal, so the fast path yields code 0
         sm.inv[i] = q.scale_fix ? 1.0f / __half2float(__ushort_as_half(q.scale_bits)) : 0.f;
     }
@@ -366,6 +625,10 @@ __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16
         vw[slot] = word;
     }
     __syncthreads();
+    if (GEAR) {   // 4. the GEAR corrections of the group's quantisation residual
+        gear_side<D, BITS, true>(sm, *gs, kside);
+        gear_side<D, BITS, false>(sm, *gs, vside);
+    }
 }
 
 // n_q (tokens quantised) at length T: 32 * floor(max(0, T - R) / 32).
@@ -381,16 +644,21 @@ __device__ __forceinline__ long kivi_nq(long T, int R)
 // single launch may do both only when it is one CTA per unit (the ring slots
 // it writes may be ones a flushed group still reads); bulk appends run the
 // groups on a wide grid first and the residual in a second launch.
-template <int D, int BITS, bool GROUPS, bool RESIDUAL>
+template <int D, int BITS, bool GROUPS, bool RESIDUAL, bool GEAR>
 __global__ void __launch_bounds__(QTHREADS)
     k_append_quant(int Hkv, int R, int Cq, int n_new, const uint16_t *__restrict__ k_new,
                    const uint16_t *__restrict__ v_new, uint8_t *__restrict__ kb,
                    uint8_t *__restrict__ vb, uint16_t *__restrict__ k_res,
                    uint16_t *__restrict__ v_res, const int32_t *__restrict__ len,
-                   const GroupBlocks blocks, int *status)
+                   const GroupBlocks blocks, uint8_t *__restrict__ kg, uint8_t *__restrict__ vg,
+                   int *status)
 {
     constexpr int G = KIVI_G;
+    constexpr int NS = (2 * G * D + 99) / 100;
+    constexpr long SIDE = (4 * NS + 4 * G + 4 * D + 15) / 16 * 16;
     __shared__ GroupSmem<D> sm;
+    extern __shared__ __align__(16) uint8_t gear_dyn[];
+    GearSmem<D> *gs = GEAR ? reinterpret_cast<GearSmem<D> *>(gear_dyn) : nullptr;
 
     const int unit = blockIdx.x;
     const int b = unit / Hkv;
@@ -415,7 +683,10 @@ __global__ void __launch_bounds__(QTHREADS)
                     flag_error(status, DEV_CAPACITY);
                 continue;
             }
-            pack_group<D, BITS>(g, T0, CR, kn, vn, kr, vr, kb + off, vb + off, sm);
+            const size_t gi = (size_t)unit * (Cq / G) + g;   // GEAR: dense layout only
+            pack_group<D, BITS, GEAR>(g, T0, CR, kn, vn, kr, vr, kb + off, vb + off, sm, gs,
+                                      GEAR ? kg + gi * SIDE : nullptr,
+                                      GEAR ? vg + gi * SIDE : nullptr);
         }
     }
     if (RESIDUAL) {
@@ -441,43 +712,63 @@ __global__ void k_len_bump(int B, int n_new, int32_t *len)
         len[i] += n_new;
 }
 
-template <int D, int BITS>
+template <int D, int BITS, bool GEAR>
 cudaError_t launch_quant_impl(const kvc_quant_cache &c, const uint16_t *k_new,
                               const uint16_t *v_new, int n_new, cudaStream_t s)
 {
     const int units = c.B * c.Hkv;
+    const GroupBlocks blocks{c.block_table, c.Cq / KIVI_G, c.num_pages,
+                             KIVI_G * D * BITS / 8 + 4 * D};
+    const int dyn = GEAR ? (int)sizeof(GearSmem<D>) : 0;
+    if (GEAR) {   // the GEAR stage sits in dynamic shared memory next to the static group stage
+        static int configured = -1;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (configured != dev) {
+            cudaError_t e = cudaFuncSetAttribute(k_append_quant<D, BITS, true, true, GEAR>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k_append_quant<D, BITS, true, false, GEAR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+            if (e != cudaSuccess)
+                return e;
+            configured = dev;
+        }
+    }
     if (n_new <= KIVI_G) {
         // decode-sized: at most two groups flush; one CTA per unit does both parts
-        k_append_quant<D, BITS, true, true><<<units, QTHREADS, 0, s>>>(
+        k_append_quant<D, BITS, true, true, GEAR><<<units, QTHREADS, dyn, s>>>(
             c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
-            c.len, GroupBlocks{c.block_table, c.Cq / KIVI_G, c.num_pages,
-                               KIVI_G * D * BITS / 8 + 4 * D},
-            dev_status_ptr());
+            c.len, blocks, c.k_gear, c.v_gear, dev_status_ptr());
     } else {
         // bulk: the flushed groups of every unit spread over the grid, then the residual
         const long max_groups = n_new / KIVI_G + 1;
         const long fill = (8L * sm_count() + units - 1) / units;  // >= ~8 CTAs per SM in total
         int gy = (int)(max_groups < fill ? max_groups : fill);
         gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
-        k_append_quant<D, BITS, true, false><<<dim3(units, gy), QTHREADS, 0, s>>>(
+        k_append_quant<D, BITS, true, false, GEAR><<<dim3(units, gy), QTHREADS, dyn, s>>>(
             c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
-            c.len, GroupBlocks{c.block_table, c.Cq / KIVI_G, c.num_pages,
-                               KIVI_G * D * BITS / 8 + 4 * D},
-            dev_status_ptr());
+            c.len, blocks, c.k_gear, c.v_gear, dev_status_ptr());
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
-        k_append_quant<D, BITS, false, true><<<units, QTHREADS, 0, s>>>(
+        k_append_quant<D, BITS, false, true, false><<<units, QTHREADS, 0, s>>>(
             c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
-            c.len, GroupBlocks{c.block_table, c.Cq / KIVI_G, c.num_pages,
-                               KIVI_G * D * BITS / 8 + 4 * D},
-            dev_status_ptr());
+            c.len, blocks, nullptr, nullptr, dev_status_ptr());
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
     k_len_bump<<<(c.B + 255) / 256, 256, 0, s>>>(c.B, n_new, c.len);
     return cudaGetLastError();
+}
+
+template <int D, int BITS>
+cudaError_t launch_quant_bits(const kvc_quant_cache &c, const uint16_t *k_new,
+                              const uint16_t *v_new, int n_new, cudaStream_t s)
+{
+    return c.k_gear ? launch_quant_impl<D, BITS, true>(c, k_new, v_new, n_new, s)
+                    : launch_quant_impl<D, BITS, false>(c, k_new, v_new, n_new, s);
 }
 
 } // namespace
@@ -519,10 +810,10 @@ cudaError_t launch_append_quant(const kvc_quant_cache &c, const uint16_t *k_new,
                                 const uint16_t *v_new, int n_new, cudaStream_t s)
 {
     if (c.D == 128)
-        return c.bits == 4 ? launch_quant_impl<128, 4>(c, k_new, v_new, n_new, s)
-                           : launch_quant_impl<128, 2>(c, k_new, v_new, n_new, s);
-    return c.bits == 4 ? launch_quant_impl<64, 4>(c, k_new, v_new, n_new, s)
-                       : launch_quant_impl<64, 2>(c, k_new, v_new, n_new, s);
+        return c.bits == 4 ? launch_quant_bits<128, 4>(c, k_new, v_new, n_new, s)
+                           : launch_quant_bits<128, 2>(c, k_new, v_new, n_new, s);
+    return c.bits == 4 ? launch_quant_bits<64, 4>(c, k_new, v_new, n_new, s)
+                       : launch_quant_bits<64, 2>(c, k_new, v_new, n_new, s);
 }
 
 } // namespace kvc
