@@ -198,6 +198,9 @@ def run_gpu(args, rank, world):
         Cq = 32 * ((T0 + S_total) // 32 + 1)
         kv4 = kvc.QuantCache.empty(B, Hkv, Cq, D, 4, w.kivi_R, device=dev)
         kvc.kvc_append_quant(kv4, K, V, stream=stream)
+        # GEAR-4: the same prompt through the GEAR packer (its own rows, timed after the step)
+        gear4 = kvc.QuantCache.empty(B, Hkv, Cq, D, 4, w.kivi_R, device=dev, gear=True)
+        rows.update(pack_rows(kvc, dev, stream, kv4, gear4, K, V))
         del K, V
 
         # per-step inputs, resident in HBM (distinct for every step and method)
@@ -395,6 +398,8 @@ def run_gpu(args, rank, world):
                                  n_heavy, n_recent))
     rows.update(random_rows(kvc, W, dev, stream))
     rows.update(paged_rows(kvc, dev, stream, fp, kv4, qs[0, 0], T0))
+    rows.update(gear_rows(kvc, dev, stream, gear4, qs[:, 2], kn[:, 2], vn[:, 2], hbm_peak))
+    del gear4
 
     ms_per_step = total_ms / args.steps
     eager_ms = evs[0][0].elapsed_time(evs[-1][11]) / args.steps
@@ -463,6 +468,72 @@ def h2o_variant_rows(kvc, dev, stream, src, src_scores, qs, kn, vn, n_heavy, n_r
                                    f", evict when n >= {trig} (slots attended {budget + 1}.."
                                    f"{trig})")}
             del c, sc, ws
+    return out
+
+
+def pack_rows(kvc, dev, stream, kv4, gear4, K, V):
+    """Bulk pack of the heavy-load prompt (B x Hkv units of 2047 tokens): KIVI-4 blocks alone,
+    and KIVI-4 blocks plus the GEAR side blocks (2% sparse + rank-2 per group and side).  Each
+    cache is reset and repacked; the second of two packs is timed."""
+    import torch
+    out = {}
+    with torch.cuda.stream(stream):
+        for name, c in (("kivi4_pack_prompt", kv4), ("gear4_pack_prompt", gear4)):
+            times = []
+            for _ in range(2):
+                c.len.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                kvc.kvc_append_quant(c, K, V, stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                times.append(e0.elapsed_time(e1))
+            B, Hkv, T, D = K.shape
+            out[name] = {"ms": times[-1], "tokens": B * Hkv * T,
+                         "groups_per_s": B * Hkv * (T - kv4.R) // 32 / (times[-1] * 1e-3),
+                         "shape": f"[{B},{Hkv},{T},{D}] fp16 -> 4-bit groups of 32 + ring"}
+    return out
+
+
+def gear_rows(kvc, dev, stream, gear4, qs, kn, vn, hbm_peak):
+    """GEAR-4 decode on the heavy-load workload: each step appends one token (the 32nd of a
+    group flushes it through the GEAR packer) and attends over the quantised groups with
+    their sparse and rank-2 corrections plus the fp16 ring.  Attention bytes: KIVI-4 blocks,
+    the two side blocks of every group, the ring, queries and outputs."""
+    import torch
+    B, Hkv, D, R = gear4.B, gear4.Hkv, gear4.D, gear4.R
+    Hq = qs.shape[2]
+    side = kvc.kvc_gear_side_bytes(D)
+    steps = min(qs.shape[0], 40)
+    out = {}
+    with torch.cuda.stream(stream):
+        o = torch.empty(B, Hq, D, dtype=torch.float16, device=dev)
+        ws = torch.empty(max(kvc.kvc_workspace_size(gear4, qs[0]) // 4, 1), dtype=torch.float32,
+                         device=dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        lens = []
+        for i in range(steps):
+            ev[i][0].record(stream)
+            kvc.kvc_append_quant(gear4, kn[i], vn[i], stream=stream)
+            ev[i][1].record(stream)
+            kvc.kvc_decode_attend(gear4, qs[i], o, workspace=ws, stream=stream)
+            ev[i][2].record(stream)
+            lens.append(int(gear4.len[0].item()) if i == 0 else lens[-1] + 1)
+        torch.cuda.synchronize(dev)
+        att = [ev[i][1].elapsed_time(ev[i][2]) for i in range(1, steps)]
+        app = [ev[i][0].elapsed_time(ev[i][1]) for i in range(1, steps)]
+        nbytes = [kivi_bytes(t, R, B, Hkv, Hq, D, 4) +
+                  B * Hkv * (max(0, t - R) // 32) * 2 * side for t in lens[1:]]
+        ms_att = sum(att) / len(att)
+        gbs = sum(nbytes) / len(nbytes) / (ms_att * 1e-3) / 1e9
+        out["gear4_decode"] = {
+            "ms_per_step": (sum(att) + sum(app)) / len(att), "attend_ms": ms_att,
+            "append_ms": sum(app) / len(app), "tokens_per_s": B / ((sum(att) + sum(app)) /
+                                                                  len(att) * 1e-3),
+            "attend_gbs": gbs, "attend_frac_of_hbm": gbs / hbm_peak,
+            "attend_bytes": sum(nbytes) / len(nbytes), "steps": steps - 1,
+            "shape": f"B={B} GQA {Hq}/{Hkv} D={D}, T={lens[1]}..{lens[-1]}, R={R}, "
+                     f"side block {side} B per group and side"}
     return out
 
 
@@ -667,9 +738,16 @@ def run_profile(args):
         ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), device=dev)
         for _ in range(3):
             kvc.kvc_decode_attend(cache, q, o, workspace=ws)
-    elif what == "kivi_pack":
+    elif what == "attend_gear4":
+        cache = kvc.QuantCache.empty(B, Hkv, T, D, 4, w.kivi_R, device=dev, gear=True)
+        kvc.kvc_append_quant(cache, K, V)
+        ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), device=dev)
         for _ in range(3):
-            cache = kvc.QuantCache.empty(B, Hkv, T, D, 4, w.kivi_R, device=dev)
+            kvc.kvc_decode_attend(cache, q, o, workspace=ws)
+    elif what in ("kivi_pack", "gear_pack"):
+        for _ in range(3):
+            cache = kvc.QuantCache.empty(B, Hkv, T, D, 4, w.kivi_R, device=dev,
+                                         gear=what == "gear_pack")
             kvc.kvc_append_quant(cache, K, V)
     elif what == "prefill":
         L = T - 1
@@ -886,7 +964,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None,
                     help="run one kernel on a small case for ncu: attend_fp16, attend_h2o, "
-                         "attend_kivi4, h2o_evict, stream_evict, prefill, kivi_pack")
+                         "attend_kivi4, attend_gear4, h2o_evict, stream_evict, prefill, kivi_pack, gear_pack")
     ap.add_argument("--profile-batch", type=int, default=64)
     ap.add_argument("--grid", action="store_true",
                     help="throughput profile grid over batch x KV length x method (JSON lines)")

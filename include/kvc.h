@@ -272,7 +272,10 @@ KVC_API size_t kvc_workspace_size(const kvc_attend_args *args);
  * decoding), and a combine step merges the ranges.  KIVI caches are
  * dequantised in registers: the per-channel K scale is folded into the query
  * per group and the per-token V scale into the probabilities; the fp16
- * residual tail is attended in the same pass.
+ * residual tail is attended in the same pass.  A KIVI cache with GEAR side
+ * blocks (k_gear, v_gear) is attended over x_q + S + A^T B: the sparse and
+ * rank-2 corrections are applied in the same kernel (GEAR: "Rethinking KV
+ * Cache Compression" guide, §2, sparsity 2%, rank 2).
  * Source: "Rethinking KV Cache Compression" guide, §16 "Prefill、decode、TP 的
  * 性能账" (decode reads all history and is bandwidth bound) and "4 种方法逐步
  * 执行" (KIVI dequantises on the decode read).

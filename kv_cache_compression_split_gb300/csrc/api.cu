@@ -294,8 +294,6 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         return KVC_ERR_INVALID_ARG;
     if (a->kind == KVC_KIND_KIVI && (a->logits || a->h2o_scores))
         return KVC_ERR_UNSUPPORTED;
-    if (a->kind == KVC_KIND_KIVI && a->quant->k_gear)
-        return KVC_ERR_UNSUPPORTED;   // GEAR decode: see kvc_gear_attend below
     if (a->h2o_scores && (!a->logits || !a->lse))
         return KVC_ERR_INVALID_ARG;
     float h2o_keep = 1.f, h2o_add = 1.f;
@@ -334,7 +332,7 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
     KiviAttendLaunch L{f.B, a->Hq, c.Hkv, c.D, c.bits, c.R, c.Cq, a->q, a->o, c.k_blocks,
                        c.v_blocks, c.k_res, c.v_res, c.len, a->lse, part_o, part_ml,
                        f.plan.splits, f.plan.tiles_per_split, scale, c.block_table,
-                       c.num_pages};
+                       c.num_pages, c.k_gear, c.v_gear};
     return from_cuda(launch_attend_kivi(L, stream));
 }
 

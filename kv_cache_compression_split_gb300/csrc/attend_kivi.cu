@@ -24,6 +24,16 @@
 // single AND per pair of codes is the whole conversion.  The power-of-two
 // field weights are divided out of the K operand (q~ / 2^(bits*j)) or undone
 // per output row at the end, and the 2^-24 is undone in the fp32 results.
+//
+// GEAR caches ("Rethinking KV Cache Compression" guide, §2: GEAR sparsity 2%,
+// rank 2; §16: the corrections act on KIVI's quantisation residual) add, per
+// group, x_hat = x_q + S + A^T B.  The same kernel handles them, again without
+// dequantising: the quantised tile also carries the groups' side blocks, the
+// sparse entries of a group are scattered into a per-warp fp16 tile (zero
+// elsewhere) and the corrections are extra MMAs on fp32 accumulators:
+//   scores  += S Q^T + A^T (B Q^T)        (B Q^T: 2 x heads)
+//   O^T     += S^T P^T + B^T (A P^T)       (A P^T: 2 x heads)
+// where the rank-2 products run as MMAs whose k dimension holds the two ranks.
 #include "kvc_device.cuh"
 #include "kvc_internal.h"
 
@@ -40,7 +50,7 @@ constexpr float LN2 = 0.6931471805599453f;
 constexpr float TWO24 = 16777216.0f;
 constexpr float TWOM24 = 1.0f / 16777216.0f;
 
-template <int D, int BITS> struct KiviCfg {
+template <int D, int BITS, bool GEAR = false> struct KiviCfg {
     static constexpr int G = KIVI_G;
     static constexpr int NG = D / G;                   // V channel groups
     static constexpr int WK = D * BITS / 32;           // words per K token row
@@ -54,16 +64,37 @@ template <int D, int BITS> struct KiviCfg {
     static constexpr int BLOCK = CODE_BYTES + 4 * D;
     static constexpr int QG = NCW;                     // groups per quantised tile
     static_assert(QG == KIVI_PAGE_GROUPS, "a quantised tile is one page of the paged layout");
-    static constexpr int QT_BYTES = 2 * QG * BLOCK;
+    static constexpr int NS = (2 * G * D + 99) / 100;  // GEAR sparse entries per group
+    static constexpr int NSJ = (NS + 31) / 32;         // sparse entries per lane
+    // GEAR side block: NS indices, NS values, A [2][G], B [2][D], padded to 16 bytes
+    static constexpr int SIDE = GEAR ? (4 * NS + 4 * G + 4 * D + 15) / 16 * 16 : 0;
+    static constexpr int SIDE_A = 4 * NS, SIDE_B = 4 * NS + 4 * G;   // byte offsets
+    static constexpr int QT_BYTES = 2 * QG * (BLOCK + SIDE);
     static constexpr int RS = 32;                      // ring slots per residual tile
     static constexpr int NBOX = D / 64;
     static constexpr int RT_BYTES = 2 * RS * D * 2;
     static constexpr int STAGE_BYTES =
         ((QT_BYTES > RT_BYTES ? QT_BYTES : RT_BYTES) + 1023) / 1024 * 1024;
-    static constexpr int NSTAGE = (81920 / STAGE_BYTES) < 3 ? 3 : (81920 / STAGE_BYTES);
     static constexpr int RED_STRIDE = D + 4;   // padded per-head row of the merge scratch
     static constexpr int RED_BYTES = (NCW - 1) * 8 * (RED_STRIDE + 2) * 4;
-    static constexpr int SMEM = NSTAGE * STAGE_BYTES + RED_BYTES + 2 * NSTAGE * 8 + 1024;
+    // GEAR: one 32 x D fp16 sparse tile per consumer warp, rows padded by 16 bytes
+    // (conflict-free ldmatrix)
+    static constexpr int DT_STRIDE = (D + 8) * 2;
+    static constexpr int DT_BYTES = GEAR ? NCW * G * DT_STRIDE : 0;
+    // GEAR: the plain query fragments of an item, one 16-byte chunk per (lane, 2 k-steps),
+    // double-buffered (the next item's are written during the current one)
+    static constexpr int QCH = D / 32;                 // 16-byte chunks per lane
+    static constexpr int QS_BUF = QCH * 32 * 16;
+    static constexpr int QS_BYTES = GEAR ? 2 * QS_BUF : 0;
+    static constexpr int NSTAGE_PLAIN = (81920 / STAGE_BYTES) < 3 ? 3 : (81920 / STAGE_BYTES);
+    // with the sparse tiles, as many stages as keep two CTAs resident per SM
+    static constexpr int NSTAGE_FIT =
+        (112640 - RED_BYTES - DT_BYTES - QS_BYTES - 1104) / STAGE_BYTES;
+    static constexpr int NSTAGE =
+        !GEAR ? NSTAGE_PLAIN
+              : (NSTAGE_FIT < 2 ? 2 : (NSTAGE_FIT < NSTAGE_PLAIN ? NSTAGE_FIT : NSTAGE_PLAIN));
+    static constexpr int SMEM =
+        NSTAGE * STAGE_BYTES + RED_BYTES + DT_BYTES + QS_BYTES + 2 * NSTAGE * 8 + 1024;
 };
 
 struct KiviParams {
@@ -73,6 +104,7 @@ struct KiviParams {
     uint16_t *o;
     float *lse;
     const uint8_t *kb, *vb;
+    const uint8_t *kg, *vg;         // GEAR side blocks [units, Cq / G, SIDE] (dense)
     GroupBlocks blocks;             // dense or paged group blocks
     const int32_t *len;
     float *part_o, *part_ml;
@@ -108,6 +140,61 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_u16x2(uint16_t lo, uint16_t hi)
+{
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Scatter the sparse entries of one GEAR side block into a warp's sparse tile:
+// entry e (flat index t*D + d, binary16 value) lands at row t, column d.  The
+// index is masked to the group, so a corrupt block cannot write outside the
+// tile.  addr keeps the shared addresses for gear_clear.
+template <int D, int NS, int NSJ, int STRIDE>
+__device__ __forceinline__ void gear_scatter(const uint8_t *side, uint32_t tile, int lane,
+                                             uint32_t (&addr)[NSJ])
+{
+    const uint16_t *idx = reinterpret_cast<const uint16_t *>(side);
+    const uint16_t *val = idx + NS;
+#pragma unroll
+    for (int j = 0; j < NSJ; ++j) {
+        const int e = lane + 32 * j;
+        if (e < NS) {
+            const uint32_t id = idx[e] & (KIVI_G * D - 1);
+            addr[j] = tile + (id / D) * STRIDE + (id % D) * 2;
+            st_shared_u16(addr[j], val[e]);
+        }
+    }
+}
+
+// Zero the entries gear_scatter wrote, leaving the tile all zero again.
+template <int NS, int NSJ>
+__device__ __forceinline__ void gear_clear(const uint32_t (&addr)[NSJ], int lane)
+{
+#pragma unroll
+    for (int j = 0; j < NSJ; ++j)
+        if (lane + 32 * j < NS)
+            st_shared_u16(addr[j], 0);
+}
+
+// A rank x head product F held as an MMA result (row k = rank 0, 1 at lanes
+// 4k + n/2, column n = head in register n % 2) turned into the B operand of an
+// MMA whose k dimension is the rank: lane (n, 0) gets (F[0][n], F[1][n]), the
+// other lanes zero (k >= 2).
+__device__ __forceinline__ uint32_t rank2_b_operand(const float *f, int r, int c)
+{
+    const int src = r >> 1;
+    const float x0 = __shfl_sync(0xffffffffu, f[0], src);
+    const float x1 = __shfl_sync(0xffffffffu, f[1], src);
+    const float y0 = __shfl_sync(0xffffffffu, f[0], 4 + src);
+    const float y1 = __shfl_sync(0xffffffffu, f[1], 4 + src);
+    return c == 0 ? pack_half2((r & 1) ? x1 : x0, (r & 1) ? y1 : y0) : 0u;
+}
+
 struct KiviItem {
     int unit, split, b, hk, T, n_groups, n_res, qt0, nq, nr;
 };
@@ -140,18 +227,19 @@ __device__ __forceinline__ KiviItem kivi_item(const KiviParams &p, int item)
 
 // Persistent CTAs: CTA k handles work items k, k + gridDim.x, ... (an item is one
 // (sequence, KV head, split)); one TMA pipeline runs across all of its items.
-template <int D, int BITS>
+template <int D, int BITS, bool GEAR>
 __global__ void __launch_bounds__(NTHREADS, 2)
     k_attend_kivi(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const KiviParams p)
 {
-    using Cfg = KiviCfg<D, BITS>;
+    using Cfg = KiviCfg<D, BITS, GEAR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *red = reinterpret_cast<float *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES +
-                                                  Cfg::RED_BYTES);
+    uint8_t *dtiles = smem + Cfg::NSTAGE * Cfg::STAGE_BYTES + Cfg::RED_BYTES;
+    uint8_t *qstage = dtiles + Cfg::DT_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(qstage + Cfg::QS_BYTES);
     uint64_t *empty = full + Cfg::NSTAGE;
     __shared__ int s_abort;   // set when a wait ran out; every warp then stops
     volatile int *abort = &s_abort;
@@ -202,10 +290,19 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                             flag_error(p.status, DEV_CAPACITY);
                             mbar_arrive(&full[st]);
                         } else {
-                            mbar_arrive_expect_tx(&full[st], 2 * ng * Cfg::BLOCK);
+                            mbar_arrive_expect_tx(&full[st], 2 * ng * (Cfg::BLOCK + Cfg::SIDE));
                             bulk_load(dst, p.kb + off, ng * Cfg::BLOCK, &full[st]);
                             bulk_load(dst + Cfg::QG * Cfg::BLOCK, p.vb + off, ng * Cfg::BLOCK,
                                       &full[st]);
+                            if constexpr (GEAR) {
+                                // side blocks of the same groups (dense layout)
+                                const long long so =
+                                    ((long long)w.unit * (p.Cq / Cfg::G) + g0) * Cfg::SIDE;
+                                uint8_t *sd = dst + 2 * Cfg::QG * Cfg::BLOCK;
+                                bulk_load(sd, p.kg + so, ng * Cfg::SIDE, &full[st]);
+                                bulk_load(sd + Cfg::QG * Cfg::SIDE, p.vg + so, ng * Cfg::SIDE,
+                                          &full[st]);
+                            }
                         }
                     }
                 }
@@ -218,8 +315,34 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const int h0 = 2 * c, h1 = 2 * c + 1;
     const bool hv = r < p.g;
     int it = 0;
+    // GEAR: this warp's sparse tile, all zero between groups
+    const uint32_t dt = smem_u32(dtiles) + warp * Cfg::G * Cfg::DT_STRIDE;
+    // GEAR: Q^T B-operand fragments of item `item` (head r: words 8s + c and 8s + c + 4 of
+    // the query row, s = 0 .. D/16-1) into q buffer qb, written by warp 0
+    auto stage_q = [&](int item, int qb) {
+        const int unit = item / p.splits;
+        const int bb = unit / p.Hkv, hh = unit % p.Hkv;
+        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
+            p.q + ((size_t)bb * p.Hq + hh * p.g + (hv ? r : 0)) * D);
+        uint4 *dst = reinterpret_cast<uint4 *>(qstage + qb * Cfg::QS_BUF) + lane;
+#pragma unroll
+        for (int k = 0; k < Cfg::QCH; ++k)
+            dst[32 * k] = hv ? make_uint4(q32[16 * k + c], q32[16 * k + c + 4],
+                                          q32[16 * k + 8 + c], q32[16 * k + 12 + c])
+                             : make_uint4(0u, 0u, 0u, 0u);
+    };
+    if constexpr (GEAR) {
+        uint4 *z = reinterpret_cast<uint4 *>(dtiles + warp * Cfg::G * Cfg::DT_STRIDE);
+        for (int e = lane; e < Cfg::G * Cfg::DT_STRIDE / 16; e += 32)
+            z[e] = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+        if (warp == 0 && (int)blockIdx.x < p.n_items)
+            stage_q(blockIdx.x, 0);
+        consumer_bar();
+    }
+    int qbuf = 0;   // q buffer of the current item
 
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, qbuf ^= 1) {
     const KiviItem wi = kivi_item<D, BITS>(p, item);
     const int b = wi.b, hk = wi.hk, T = wi.T, n_groups = wi.n_groups, n_res = wi.n_res;
     const int qt0 = wi.qt0, nr = wi.nr, ntiles = wi.nr + wi.nq;
@@ -382,6 +505,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             const uint32_t *ksz = reinterpret_cast<const uint32_t *>(kblk + Cfg::CODE_BYTES);
             const uint32_t *vss = reinterpret_cast<const uint32_t *>(vblk + Cfg::CODE_BYTES);
             const uint32_t *vzz = vss + Cfg::NG * Cfg::G / 2;
+            // GEAR side blocks of this warp's group; the K entries go into the tile now
+            const uint8_t *kside = tile + 2 * Cfg::QG * Cfg::BLOCK + warp * Cfg::SIDE;
+            const uint8_t *vside = kside + Cfg::QG * Cfg::SIDE;
+            uint32_t saddr[Cfg::NSJ];
+            if constexpr (GEAR)
+                gear_scatter<D, Cfg::NS, Cfg::NSJ, Cfg::DT_STRIDE>(kside, dt, lane, saddr);
 
             // ---- q~ pairs (B operand) and the bias sum_d q_d z_d of head r
             uint32_t qt[D / 8];
@@ -449,14 +578,72 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                            fmaf(sa1[0], sk, bias0), fmaf(sa1[2], sk, bias0)};
             float xb[4] = {fmaf(sa0[1], sk, bias1), fmaf(sa0[3], sk, bias1),
                            fmaf(sa1[1], sk, bias1), fmaf(sa1[3], sk, bias1)};
+            if constexpr (GEAR) {
+                // ---- GEAR score correction  S Q^T + A^T (B Q^T)  (fp32, plain units)
+                __syncwarp();   // every lane's K entries are in the tile
+                float dk0[4] = {0.f, 0.f, 0.f, 0.f}, dk1[4] = {0.f, 0.f, 0.f, 0.f};
+                float uf[4] = {0.f, 0.f, 0.f, 0.f};   // U = B Q^T: rank rows 0, 1
+                float ug[4] = {0.f, 0.f, 0.f, 0.f};   // (odd k-steps: a second chain)
+                uint4 qv[Cfg::QCH];
+                {
+                    const uint4 *qsrc =
+                        reinterpret_cast<const uint4 *>(qstage + qbuf * Cfg::QS_BUF) + lane;
+#pragma unroll
+                    for (int k = 0; k < Cfg::QCH; ++k)
+                        qv[k] = qsrc[32 * k];
+                }
+                const uint32_t *bk = reinterpret_cast<const uint32_t *>(kside + Cfg::SIDE_B);
+                const bool rk = r < 2;
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s) {
+                    // Q^T as the B operand: Q[head r][16s + 2c, +1] and [16s + 2c + 8, +1]
+                    const uint32_t q0 = (s & 1) ? qv[s >> 1].z : qv[s >> 1].x;
+                    const uint32_t q1 = (s & 1) ? qv[s >> 1].w : qv[s >> 1].y;
+                    mma16816((s & 1) ? ug : uf, rk ? bk[r * (D / 2) + 8 * s + c] : 0u, 0u,
+                             rk ? bk[r * (D / 2) + 8 * s + 4 + c] : 0u, 0u, q0, q1);
+                    const int ch = 2 * s + (mi >> 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(dt + (ri + 8 * (mi & 1)) * Cfg::DT_STRIDE + ch * 16, a0, a1, a2, a3);
+                    mma16816(dk0, a0, a1, a2, a3, q0, q1);
+                    ldsm_x4(dt + (16 + ri + 8 * (mi & 1)) * Cfg::DT_STRIDE + ch * 16, a0, a1, a2,
+                            a3);
+                    mma16816(dk1, a0, a1, a2, a3, q0, q1);
+                }
+                uf[0] += ug[0];
+                uf[1] += ug[1];
+                const uint32_t ub = rank2_b_operand(uf, r, c);
+                const uint16_t *ak = reinterpret_cast<const uint16_t *>(kside + Cfg::SIDE_A);
+                const bool c0 = c == 0;
+                mma16816(dk0, c0 ? pack_u16x2(ak[r], ak[Cfg::G + r]) : 0u,
+                         c0 ? pack_u16x2(ak[r + 8], ak[Cfg::G + r + 8]) : 0u, 0u, 0u, ub, 0u);
+                mma16816(dk1, c0 ? pack_u16x2(ak[r + 16], ak[Cfg::G + r + 16]) : 0u,
+                         c0 ? pack_u16x2(ak[r + 24], ak[Cfg::G + r + 24]) : 0u, 0u, 0u, ub, 0u);
+                const float sl = p.scale_log2;
+                xa[0] = fmaf(dk0[0], sl, xa[0]);
+                xa[1] = fmaf(dk0[2], sl, xa[1]);
+                xa[2] = fmaf(dk1[0], sl, xa[2]);
+                xa[3] = fmaf(dk1[2], sl, xa[3]);
+                xb[0] = fmaf(dk0[1], sl, xb[0]);
+                xb[1] = fmaf(dk0[3], sl, xb[1]);
+                xb[2] = fmaf(dk1[1], sl, xb[2]);
+                xb[3] = fmaf(dk1[3], sl, xb[3]);
+                // swap the K entries for the V entries
+                __syncwarp();
+                gear_clear<Cfg::NS, Cfg::NSJ>(saddr, lane);
+                __syncwarp();
+                gear_scatter<D, Cfg::NS, Cfg::NSJ, Cfg::DT_STRIDE>(vside, dt, lane, saddr);
+            }
             softmax_update(xa, xb, 4);
 
             const uint32_t *vw = reinterpret_cast<const uint32_t *>(vblk);
+            uint32_t pbs[2][2];   // P^T fragments of both 16-token blocks (GEAR)
 #pragma unroll
             for (int rb = 0; rb < 2; ++rb) {
                 // P^T fragments: pb0 = p[tokens 2c, 2c+1][head r], pb1 = tokens 2c+8, 2c+9
                 const uint32_t pb0 = movmatrix_t(pack_half2(xa[2 * rb], xb[2 * rb]));
                 const uint32_t pb1 = movmatrix_t(pack_half2(xa[2 * rb + 1], xb[2 * rb + 1]));
+                pbs[rb][0] = pb0;
+                pbs[rb][1] = pb1;
                 const int t0 = 16 * rb + 2 * c;
                 // zero term Z[group][head] += sum_t z_t p_t (A rows = channel groups)
                 {
@@ -494,6 +681,44 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                              ptb1[m / 2]);
                 }
             }
+            if constexpr (GEAR) {
+                // ---- GEAR output correction  S^T P^T + B^T (A P^T), added in code units
+                __syncwarp();   // every lane's V entries are in the tile
+                const bool rk = r < 2, c0 = c == 0;
+                const uint32_t *av = reinterpret_cast<const uint32_t *>(vside + Cfg::SIDE_A);
+                float wf[4] = {0.f, 0.f, 0.f, 0.f};   // W = A P^T: rank rows 0, 1
+#pragma unroll
+                for (int rb = 0; rb < 2; ++rb)
+                    mma16816(wf, rk ? av[r * (Cfg::G / 2) + 8 * rb + c] : 0u, 0u,
+                             rk ? av[r * (Cfg::G / 2) + 8 * rb + 4 + c] : 0u, 0u, pbs[rb][0],
+                             pbs[rb][1]);
+                const uint32_t wbo = rank2_b_operand(wf, r, c);
+                const uint16_t *bv = reinterpret_cast<const uint16_t *>(vside + Cfg::SIDE_B);
+#pragma unroll
+                for (int m = 0; m < D / 16; ++m) {
+                    float t4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int rb = 0; rb < 2; ++rb) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_t(dt + (16 * rb + ri + 8 * (mi >> 1)) * Cfg::DT_STRIDE +
+                                      (2 * m + (mi & 1)) * 16,
+                                  a0, a1, a2, a3);
+                        mma16816(t4, a0, a1, a2, a3, pbs[rb][0], pbs[rb][1]);
+                    }
+                    const int d = 16 * m + r;
+                    mma16816(t4, c0 ? pack_u16x2(bv[d], bv[D + d]) : 0u,
+                             c0 ? pack_u16x2(bv[d + 8], bv[D + d + 8]) : 0u, 0u, 0u, wbo, 0u);
+                    const int jj = m % Cfg::MPW;
+                    const float wr = pair_weight<BITS>(2 * jj) * TWOM24;
+                    const float wr8 = pair_weight<BITS>(2 * jj + 1) * TWOM24;
+                    acc[m][0] = fmaf(t4[0], wr, acc[m][0]);
+                    acc[m][1] = fmaf(t4[1], wr, acc[m][1]);
+                    acc[m][2] = fmaf(t4[2], wr8, acc[m][2]);
+                    acc[m][3] = fmaf(t4[3], wr8, acc[m][3]);
+                }
+                __syncwarp();
+                gear_clear<Cfg::NS, Cfg::NSJ>(saddr, lane);
+            }
         }
         __syncwarp();
         if (lane == 0)
@@ -529,6 +754,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     for (int off = 4; off < 32; off <<= 1) {
         l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, off);
         l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, off);
+    }
+    if constexpr (GEAR) {
+        // the next item's query fragments go to the other buffer: its readers finished
+        // before the previous merge, and this item's readers before the barrier below
+        if (warp == 0 && item + (int)gridDim.x < p.n_items)
+            stage_q(item + gridDim.x, qbuf ^ 1);
     }
     consumer_bar();   // warp 0 has finished reading the previous item's scratch
     if (*abort)
@@ -626,22 +857,22 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }   // items
 }
 
-template <int D, int BITS>
+template <int D, int BITS, bool GEAR>
 cudaError_t launch_kivi_impl(const CUtensorMap &tk, const CUtensorMap &tv, const KiviParams &kp,
                              cudaStream_t s)
 {
-    using Cfg = KiviCfg<D, BITS>;
+    using Cfg = KiviCfg<D, BITS, GEAR>;
     static int configured_device = -1;
     static int resident = 1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_attend_kivi<D, BITS>,
+        cudaError_t e = cudaFuncSetAttribute(k_attend_kivi<D, BITS, GEAR>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
         if (e != cudaSuccess)
             return e;
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attend_kivi<D, BITS>,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attend_kivi<D, BITS, GEAR>,
                                                           NTHREADS, Cfg::SMEM);
         if (e != cudaSuccess)
             return e;
@@ -651,8 +882,18 @@ cudaError_t launch_kivi_impl(const CUtensorMap &tk, const CUtensorMap &tv, const
     const int grid = kp.n_items < resident ? kp.n_items : resident;
     if (grid <= 0)
         return cudaSuccess;
-    k_attend_kivi<D, BITS><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, kp);
+    k_attend_kivi<D, BITS, GEAR><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, kp);
     return cudaGetLastError();
+}
+
+template <int D, int BITS>
+cudaError_t launch_kivi_bits(const CUtensorMap &tk, const CUtensorMap &tv, const KiviParams &kp,
+                             cudaStream_t s)
+{
+    static_assert(KiviCfg<128, BITS, true>::SIDE == 976 && KiviCfg<64, BITS, true>::SIDE == 560,
+                  "GEAR side block size");
+    return kp.kg ? launch_kivi_impl<D, BITS, true>(tk, tv, kp, s)
+                 : launch_kivi_impl<D, BITS, false>(tk, tv, kp, s);
 }
 
 } // namespace
@@ -679,6 +920,8 @@ cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s)
     kp.lse = a.lse;
     kp.kb = a.kb;
     kp.vb = a.vb;
+    kp.kg = a.kg;
+    kp.vg = a.vg;
     kp.blocks = GroupBlocks{a.block_table, a.Cq / KIVI_G, a.num_pages,
                             (int)kvc_kivi_block_bytes(a.D, a.bits)};
     kp.len = a.len;
@@ -690,11 +933,11 @@ cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s)
     kp.n_items = a.B * a.Hkv * a.splits;
     cudaError_t e;
     if (a.D == 128)
-        e = a.bits == 4 ? launch_kivi_impl<128, 4>(tk, tv, kp, s)
-                        : launch_kivi_impl<128, 2>(tk, tv, kp, s);
+        e = a.bits == 4 ? launch_kivi_bits<128, 4>(tk, tv, kp, s)
+                        : launch_kivi_bits<128, 2>(tk, tv, kp, s);
     else
-        e = a.bits == 4 ? launch_kivi_impl<64, 4>(tk, tv, kp, s)
-                        : launch_kivi_impl<64, 2>(tk, tv, kp, s);
+        e = a.bits == 4 ? launch_kivi_bits<64, 4>(tk, tv, kp, s)
+                        : launch_kivi_bits<64, 2>(tk, tv, kp, s);
     if (e != cudaSuccess || a.splits == 1)
         return e;
     return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);

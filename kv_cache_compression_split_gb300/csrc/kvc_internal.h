@@ -63,6 +63,7 @@ struct KiviAttendLaunch {
     float scale;
     const int32_t *block_table;  // paged group blocks (nullptr: dense)
     int num_pages;
+    const uint8_t *kg, *vg;      // GEAR side blocks (nullptr: KIVI)
 };
 cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s);
 
