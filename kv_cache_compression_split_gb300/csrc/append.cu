@@ -303,6 +303,31 @@ __device__ __forceinline__ void square32(const float (*src)[KIVI_G + 1], float (
 
 // Orthonormalise the two columns (x0, x1) a warp holds, one row per lane; a
 // column with no length left becomes a unit vector orthogonal to the other.
+__device__ __forceinline__ void orthonormalise2(float &x0, float &x1);
+
+// The same with the three inner products reduced together (one round of
+// shuffles): x0 / |x0| and x1 - (x0.x1 / x0.x0) x0, normalised.  Falls back to
+// orthonormalise2 when |x0| vanishes or x1 loses more than 1 - 1e-3 of its
+// squared length to the projection (cancellation).
+__device__ __forceinline__ void orthonormalise2_fast(float &x0, float &x1)
+{
+    float n0 = x0 * x0, dp = x0 * x1, n1 = x1 * x1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        n0 += __shfl_xor_sync(0xffffffffu, n0, o);
+        dp += __shfl_xor_sync(0xffffffffu, dp, o);
+        n1 += __shfl_xor_sync(0xffffffffu, n1, o);
+    }
+    const float rest = n1 - dp * dp / n0;
+    if (!(n0 > 1e-30f) || !(rest > 1e-3f * n1) || !(n1 > 1e-24f)) {
+        orthonormalise2(x0, x1);
+        return;
+    }
+    const float f = dp / n0;
+    x1 = (x1 - f * x0) * rsqrtf(rest);
+    x0 *= rsqrtf(n0);
+}
+
 __device__ __forceinline__ void orthonormalise2(float &x0, float &x1)
 {
     const int lane = threadIdx.x & 31;
@@ -358,20 +383,50 @@ __device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &g
         for (int i = tid; i < 256; i += QTHREADS)
             gs.hist[i] = 0;
         __syncthreads();
+        // histogram of the digit among keys matching the prefix; lanes with equal
+        // digits add once (keys concentrate on a few exponents)
 #pragma unroll
-        for (int u = 0; u < PER; ++u)
-            if ((key[u] & mask) == prefix)
-                atomicAdd(&gs.hist[(key[u] >> shift) & 255], 1);
+        for (int u = 0; u < PER; ++u) {
+            const bool in = (key[u] & mask) == prefix;
+            const int dg = in ? (int)((key[u] >> shift) & 255) : 256;
+            const unsigned same = __match_any_sync(0xffffffffu, dg);
+            if (in && lane == __ffs(same) - 1)
+                atomicAdd(&gs.hist[dg], __popc(same));
+        }
         __syncthreads();
-        if (tid == 0) {
-            int cum = 0, dg = 255;
-            for (; dg > 0; --dg) {
-                if (cum + gs.hist[dg] >= need)
-                    break;
-                cum += gs.hist[dg];
+        if (warp == 0) {
+            // lane L holds digits 255 - 8L - k, k = 0..7 (descending); the digit is the
+            // first one from the top whose cumulative count reaches `need`
+            int h[8], tot = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                h[k] = gs.hist[255 - 8 * lane - k];
+                tot += h[k];
             }
-            gs.misc[0] = dg;
-            gs.misc[1] = need - cum;
+            int incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            const bool mine = incl - tot < need && incl >= need;
+            const unsigned any = __ballot_sync(0xffffffffu, mine);
+            if (mine) {
+                int cum = incl - tot, k = 0;
+                for (; k < 7; ++k) {
+                    if (cum + h[k] >= need)
+                        break;
+                    cum += h[k];
+                }
+                gs.misc[0] = 255 - 8 * lane - k;
+                gs.misc[1] = need - cum;
+            } else if (any == 0 && lane == 31) {
+                // fewer matching keys than needed (cannot happen for consistent input):
+                // digit 0, as a downward scan would end
+                gs.misc[0] = 0;
+                gs.misc[1] = need - (incl - h[7]);
+            }
         }
         __syncthreads();
         prefix |= (uint32_t)gs.misc[0] << shift;
@@ -454,15 +509,29 @@ __device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &g
         }
         orthonormalise2(x0, x1);
         for (int it = 0; it < 16; ++it) {
+            // y = M x, the vectors broadcast from shared memory four entries at a time
+            gs.a[0][lane] = x0;
+            gs.a[1][lane] = x1;
+            __syncwarp();
+            const float4 *a0 = reinterpret_cast<const float4 *>(gs.a[0]);
+            const float4 *a1 = reinterpret_cast<const float4 *>(gs.a[1]);
             float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                y0 = fmaf(gr[j], __shfl_sync(0xffffffffu, x0, j), y0);
-                y1 = fmaf(gr[j], __shfl_sync(0xffffffffu, x1, j), y1);
+            for (int j = 0; j < G / 4; ++j) {
+                const float4 u = a0[j], v = a1[j];
+                y0 = fmaf(gr[4 * j], u.x, y0);
+                y0 = fmaf(gr[4 * j + 1], u.y, y0);
+                y0 = fmaf(gr[4 * j + 2], u.z, y0);
+                y0 = fmaf(gr[4 * j + 3], u.w, y0);
+                y1 = fmaf(gr[4 * j], v.x, y1);
+                y1 = fmaf(gr[4 * j + 1], v.y, y1);
+                y1 = fmaf(gr[4 * j + 2], v.z, y1);
+                y1 = fmaf(gr[4 * j + 3], v.w, y1);
             }
+            __syncwarp();
             x0 = y0;
             x1 = y1;
-            orthonormalise2(x0, x1);
+            orthonormalise2_fast(x0, x1);
         }
         gs.a[0][lane] = x0;
         gs.a[1][lane] = x1;

@@ -58,7 +58,6 @@ template <int D, int BITS, bool GEAR = false> struct KiviCfg {
     static constexpr int W = D * BITS / 128;           // V words per lane-row per pair
     static constexpr int FPW = 32 / BITS;              // fields per word
     static constexpr int HALF = FPW / 2;               // fields per 16-bit half
-    static constexpr int QUART = HALF / 2;             // fields taken before shifting by 8
     static constexpr int MPW = 8 / BITS;               // V m-tiles per word
     static constexpr int CODE_BYTES = G * D * BITS / 8;
     static constexpr int BLOCK = CODE_BYTES + 4 * D;
@@ -69,6 +68,7 @@ template <int D, int BITS, bool GEAR = false> struct KiviCfg {
     // GEAR side block: NS indices, NS values, A [2][G], B [2][D], padded to 16 bytes
     static constexpr int SIDE = GEAR ? (4 * NS + 4 * G + 4 * D + 15) / 16 * 16 : 0;
     static constexpr int SIDE_A = 4 * NS, SIDE_B = 4 * NS + 4 * G;   // byte offsets
+    static_assert(SIDE_B == SIDE_A + 4 * G, "A [2][G] binary16 precedes B");
     static constexpr int QT_BYTES = 2 * QG * (BLOCK + SIDE);
     static constexpr int RS = 32;                      // ring slots per residual tile
     static constexpr int NBOX = D / 64;
@@ -458,19 +458,24 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 
     // ======================= quantised tiles: warp w takes group w (32 tokens)
     // query pairs: lane c covers channels [c D/4, (c+1) D/4); pair pi holds channels
-    // (lo, lo + HALF) divided by the pair's field weight.  qh: the same channels in order.
-    uint32_t qpair[D / 8], qh[D / 8];
+    // (lo, lo + HALF) divided by the pair's field weight
+    uint32_t qpair[D / 8];
+    uint32_t qh[GEAR ? 1 : D / 8];   // KIVI: the same channels in order (for the bias)
     {
+        uint32_t qh_[D / 8];
         const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow + c * (D / 4));
 #pragma unroll
-        for (int e = 0; e < D / 8; ++e)
-            qh[e] = hv ? q32[e] : 0u;
+        for (int e = 0; e < D / 8; ++e) {
+            qh_[e] = hv ? q32[e] : 0u;
+            if constexpr (!GEAR)
+                qh[e] = qh_[e];
+        }
 #pragma unroll
         for (int pi = 0; pi < D / 8; ++pi) {
             const int j = pi % Cfg::HALF;
             const int lo = Cfg::FPW * (pi / Cfg::HALF) + j, hi = lo + Cfg::HALF;
-            const __half2 wl = *reinterpret_cast<const __half2 *>(&qh[lo >> 1]);
-            const __half2 wh = *reinterpret_cast<const __half2 *>(&qh[hi >> 1]);
+            const __half2 wl = *reinterpret_cast<const __half2 *>(&qh_[lo >> 1]);
+            const __half2 wh = *reinterpret_cast<const __half2 *>(&qh_[hi >> 1]);
             const float qlo = (lo & 1) ? __high2float(wl) : __low2float(wl);
             const float qhi = (hi & 1) ? __high2float(wh) : __low2float(wh);
             const float wgt = 1.0f / pair_weight<BITS>(j);
@@ -512,12 +517,66 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             if constexpr (GEAR)
                 gear_scatter<D, Cfg::NS, Cfg::NSJ, Cfg::DT_STRIDE>(kside, dt, lane, saddr);
 
-            // ---- q~ pairs (B operand) and the bias sum_d q_d z_d of head r
+            // ---- the bias beta_h = sum_d q_hd z_d of the K zeros.  GEAR: one MMA chain over
+            // the plain query Q^T whose A rows 0, 1 hold B (U = B Q^T) and row 2 the zeros,
+            // with the sparse tile's S Q^T alongside.  KIVI: fp32 FMAs, reduced over c.
+            float dk0[4] = {0.f, 0.f, 0.f, 0.f}, dk1[4] = {0.f, 0.f, 0.f, 0.f};
+            float uf[4] = {0.f, 0.f, 0.f, 0.f};   // rows 0-2: U, beta (GEAR)
+            float ug[4] = {0.f, 0.f, 0.f, 0.f};   // (odd k-steps: a second chain)
+            float bias0, bias1;   // log2-domain bias of heads 2c, 2c+1
+            if constexpr (GEAR) {
+                __syncwarp();   // every lane's K entries are in the tile
+                uint4 qv[Cfg::QCH];
+                const uint4 *qsrc =
+                    reinterpret_cast<const uint4 *>(qstage + qbuf * Cfg::QS_BUF) + lane;
+#pragma unroll
+                for (int k = 0; k < Cfg::QCH; ++k)
+                    qv[k] = qsrc[32 * k];
+                const uint32_t *arow =
+                    r == 2 ? ksz + D / 2
+                           : reinterpret_cast<const uint32_t *>(kside + Cfg::SIDE_B) + r * (D / 2);
+                const bool ra = r <= 2;
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s) {
+                    // Q^T as the B operand: Q[head r][16s + 2c, +1] and [16s + 2c + 8, +1]
+                    const uint32_t q0 = (s & 1) ? qv[s >> 1].z : qv[s >> 1].x;
+                    const uint32_t q1 = (s & 1) ? qv[s >> 1].w : qv[s >> 1].y;
+                    mma16816((s & 1) ? ug : uf, ra ? arow[8 * s + c] : 0u, 0u,
+                             ra ? arow[8 * s + 4 + c] : 0u, 0u, q0, q1);
+                    const int ch = 2 * s + (mi >> 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(dt + (ri + 8 * (mi & 1)) * Cfg::DT_STRIDE + ch * 16, a0, a1, a2, a3);
+                    mma16816(dk0, a0, a1, a2, a3, q0, q1);
+                    ldsm_x4(dt + (16 + ri + 8 * (mi & 1)) * Cfg::DT_STRIDE + ch * 16, a0, a1, a2,
+                            a3);
+                    mma16816(dk1, a0, a1, a2, a3, q0, q1);
+                }
+                uf[0] += ug[0];
+                uf[1] += ug[1];
+                // beta of heads 2c, 2c+1: row 2 of the result, lane 8 + c
+                bias0 = __shfl_sync(0xffffffffu, uf[0], 8 + c) * p.scale_log2;
+                bias1 = __shfl_sync(0xffffffffu, uf[1], 8 + c) * p.scale_log2;
+            } else {
+                float beta = 0.f;
+                const uint32_t *zl = ksz + D / 2 + c * (D / 8);
+#pragma unroll
+                for (int e = 0; e < D / 8; ++e) {
+                    const uint32_t zw = zl[e];
+                    const float2 zf = __half22float2(*reinterpret_cast<const __half2 *>(&zw));
+                    const float2 qf2 = __half22float2(*reinterpret_cast<const __half2 *>(&qh[e]));
+                    beta = fmaf(qf2.x, zf.x, beta);
+                    beta = fmaf(qf2.y, zf.y, beta);
+                }
+                beta += __shfl_xor_sync(0xffffffffu, beta, 1);
+                beta += __shfl_xor_sync(0xffffffffu, beta, 2);
+                // beta of head h sits in lanes 4h .. 4h + 3
+                bias0 = __shfl_sync(0xffffffffu, beta, 4 * h0) * p.scale_log2;
+                bias1 = __shfl_sync(0xffffffffu, beta, 4 * h1) * p.scale_log2;
+            }
+            // ---- q~ pairs (B operand)
             uint32_t qt[D / 8];
-            float beta = 0.f;
             {
                 const uint32_t *sl = ksz + c * (D / 8);
-                const uint32_t *zl = ksz + D / 2 + c * (D / 8);
                 uint32_t sw[D / 8];
 #pragma unroll
                 for (int e = 0; e < D / 8; ++e)
@@ -531,19 +590,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                                                         ((hi & 1) ? 0x7600 : 0x5400));
                     qt[pi] = hmul2_u32(qpair[pi], sp);
                 }
-#pragma unroll
-                for (int e = 0; e < D / 8; ++e) {
-                    const uint32_t zw = zl[e];
-                    const float2 zf = __half22float2(*reinterpret_cast<const __half2 *>(&zw));
-                    const float2 qf2 = __half22float2(*reinterpret_cast<const __half2 *>(&qh[e]));
-                    beta = fmaf(qf2.x, zf.x, beta);
-                    beta = fmaf(qf2.y, zf.y, beta);
-                }
-                beta += __shfl_xor_sync(0xffffffffu, beta, 1);
-                beta += __shfl_xor_sync(0xffffffffu, beta, 2);
             }
-            const float bias0 = __shfl_sync(0xffffffffu, beta, 4 * h0) * p.scale_log2;
-            const float bias1 = __shfl_sync(0xffffffffu, beta, 4 * h1) * p.scale_log2;
             const float sk = TWO24 * p.scale_log2;
 
             // ---- S^T = C_K Q~^T for both 16-token row blocks of the group
@@ -579,38 +626,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             float xb[4] = {fmaf(sa0[1], sk, bias1), fmaf(sa0[3], sk, bias1),
                            fmaf(sa1[1], sk, bias1), fmaf(sa1[3], sk, bias1)};
             if constexpr (GEAR) {
-                // ---- GEAR score correction  S Q^T + A^T (B Q^T)  (fp32, plain units)
-                __syncwarp();   // every lane's K entries are in the tile
-                float dk0[4] = {0.f, 0.f, 0.f, 0.f}, dk1[4] = {0.f, 0.f, 0.f, 0.f};
-                float uf[4] = {0.f, 0.f, 0.f, 0.f};   // U = B Q^T: rank rows 0, 1
-                float ug[4] = {0.f, 0.f, 0.f, 0.f};   // (odd k-steps: a second chain)
-                uint4 qv[Cfg::QCH];
-                {
-                    const uint4 *qsrc =
-                        reinterpret_cast<const uint4 *>(qstage + qbuf * Cfg::QS_BUF) + lane;
-#pragma unroll
-                    for (int k = 0; k < Cfg::QCH; ++k)
-                        qv[k] = qsrc[32 * k];
-                }
-                const uint32_t *bk = reinterpret_cast<const uint32_t *>(kside + Cfg::SIDE_B);
-                const bool rk = r < 2;
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s) {
-                    // Q^T as the B operand: Q[head r][16s + 2c, +1] and [16s + 2c + 8, +1]
-                    const uint32_t q0 = (s & 1) ? qv[s >> 1].z : qv[s >> 1].x;
-                    const uint32_t q1 = (s & 1) ? qv[s >> 1].w : qv[s >> 1].y;
-                    mma16816((s & 1) ? ug : uf, rk ? bk[r * (D / 2) + 8 * s + c] : 0u, 0u,
-                             rk ? bk[r * (D / 2) + 8 * s + 4 + c] : 0u, 0u, q0, q1);
-                    const int ch = 2 * s + (mi >> 1);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(dt + (ri + 8 * (mi & 1)) * Cfg::DT_STRIDE + ch * 16, a0, a1, a2, a3);
-                    mma16816(dk0, a0, a1, a2, a3, q0, q1);
-                    ldsm_x4(dt + (16 + ri + 8 * (mi & 1)) * Cfg::DT_STRIDE + ch * 16, a0, a1, a2,
-                            a3);
-                    mma16816(dk1, a0, a1, a2, a3, q0, q1);
-                }
-                uf[0] += ug[0];
-                uf[1] += ug[1];
+                // ---- GEAR score correction  S Q^T + A^T U  (fp32, plain units)
                 const uint32_t ub = rank2_b_operand(uf, r, c);
                 const uint16_t *ak = reinterpret_cast<const uint16_t *>(kside + Cfg::SIDE_A);
                 const bool c0 = c == 0;
