@@ -802,7 +802,7 @@ def run_reference(args):
 def run_grid(args):
     """Throughput profile grid: batch x KV length x method on the heavy-load head layout (GQA 64/8,
     D 128), the per-method cost table a router consumes.  Per (B, T) cell and method:
-      prefill_ms  compress a T-token prompt: FP16 append; KIVI-b pack; StreamingLLM and H2O evict
+      prefill_ms  compress a T-token prompt: FP16 append; KIVI-b / GEAR-4 pack; StreamingLLM and H2O evict
                   to 64 + 448 (H2O after its two-pass score pass); random eviction at each keep
                   ratio with the first min(1024, T/2) tokens locked
       decode_ms   one decode step: append + attention (+ H2O's fused score update + eviction, or
@@ -928,11 +928,11 @@ def run_grid(args):
                 cell["decode_ms"]["h2o512"] = timed(h2o_step)
                 cell["slots_attended"]["h2o512"] = n_heavy + n_recent + 1
                 del fp, scores, logits, lse
-                # ---- KIVI-4 / KIVI-2: pack the prompt, then append + attention
-                for bits in (4, 2):
-                    name = f"kivi{bits}"
+                # ---- KIVI-4 / KIVI-2 / GEAR-4: pack the prompt, then append + attention
+                for bits, gear in ((4, False), (2, False), (4, True)):
+                    name = f"gear{bits}" if gear else f"kivi{bits}"
                     kv = kvc.QuantCache.empty(B, Hkv, 32 * ((T + 1) // 32 + 1), D, bits, R,
-                                              device=dev)
+                                              device=dev, gear=gear)
                     cell["prefill_ms"][name] = timed(
                         lambda: kvc.kvc_append_quant(kv, K, V, stream=stream),
                         setup=lambda: kv.len.zero_())

@@ -159,9 +159,11 @@ typedef struct kvc_slot_cache {
  *                [0, num_pages) is skipped and sets KVC_DEV_CAPACITY, and a
  *                read through one yields no data for that tile).
  *   num_pages    pages in each pool (paged layout only)
- *   k_gear, v_gear  NULL for KIVI.  GEAR (dense layout only): per group one
- *                side block of kvc_gear_side_bytes(D) bytes, [B, Hkv, Cq/32,
- *                side_bytes], holding a 2% sparse and a rank-2 correction of the
+ *   k_gear, v_gear  NULL for KIVI.  GEAR: per group one side block of
+ *                kvc_gear_side_bytes(D) bytes, [B, Hkv, Cq/32, side_bytes] (paged
+ *                layout: pools [num_pages, 4, side_bytes], group g of a unit at
+ *                the same page and slot as its K / V block), holding a 2% sparse
+ *                and a rank-2 correction of the
  *                group's quantisation residual ("Rethinking KV Cache Compression"
  *                guide, §2: GEAR sparsity 2%, rank 2; §16: the corrections act on
  *                KIVI's quantisation residual).  With x_q = fl32(zero + code *

@@ -386,9 +386,11 @@ class QuantCache:
                    if gear else None)
 
     @classmethod
-    def empty_paged(cls, B, Hkv, Cq, D, bits, R, num_pages, block_table=None, device="cuda"):
+    def empty_paged(cls, B, Hkv, Cq, D, bits, R, num_pages, block_table=None, device="cuda",
+                    gear=False):
         """Paged KIVI cache: pools of num_pages pages of 4 groups; block_table [B, Hkv, Cq / 128]
-        (default: unit u owns pages u * Cq / 128 .. (u + 1) * Cq / 128 - 1)."""
+        (default: unit u owns pages u * Cq / 128 .. (u + 1) * Cq / 128 - 1).  gear=True adds
+        GEAR side-block pools [num_pages, 4, side_bytes] behind the same table."""
         page = KIVI_GROUP * KIVI_PAGE_GROUPS
         if Cq % page:
             raise ValueError("Cq must be a multiple of 128 in the paged layout")
@@ -397,13 +399,16 @@ class QuantCache:
                                        device=device).view(B, Hkv, Cq // page)
         bb = KIVI_GROUP * D * bits // 8 + 4 * D
         pool = (num_pages, KIVI_PAGE_GROUPS, bb)
+        side = (num_pages, KIVI_PAGE_GROUPS, kvc_gear_side_bytes(D))
         return cls(k_blocks=torch.zeros(pool, dtype=torch.uint8, device=device),
                    v_blocks=torch.zeros(pool, dtype=torch.uint8, device=device),
                    k_res=torch.zeros(B, Hkv, R + KIVI_GROUP, D, dtype=torch.float16, device=device),
                    v_res=torch.zeros(B, Hkv, R + KIVI_GROUP, D, dtype=torch.float16, device=device),
                    len=torch.zeros(B, dtype=torch.int32, device=device), bits=bits, R=R,
                    block_table=block_table.to(device=device, dtype=torch.int32).contiguous(),
-                   Cq_paged=Cq)
+                   Cq_paged=Cq,
+                   k_gear=torch.zeros(side, dtype=torch.uint8, device=device) if gear else None,
+                   v_gear=torch.zeros(side, dtype=torch.uint8, device=device) if gear else None)
 
     def desc(self) -> QuantCacheDesc:
         return QuantCacheDesc(self.B, self.Hkv, self.D, self.bits, self.R, self.Cq,

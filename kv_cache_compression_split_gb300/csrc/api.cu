@@ -158,9 +158,7 @@ kvc_status check_quant_cache(const kvc_quant_cache *c)
     }
     if (!c->k_gear != !c->v_gear)
         return KVC_ERR_INVALID_ARG;
-    if (c->k_gear) {        // GEAR side blocks: dense layout only
-        if (c->block_table)
-            return KVC_ERR_UNSUPPORTED;
+    if (c->k_gear) {        // GEAR side blocks
         if (!aligned16(c->k_gear) || !aligned16(c->v_gear))
             return KVC_ERR_INVALID_ARG;
     }

@@ -280,25 +280,55 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-// dst = src * src for a symmetric 32 x 32 matrix, a 2 x 2 block of the product
-// per thread (256 threads).
+// One 16 x 8 tile C[i][j] = sum_k X[i0 + i][k] Y[j0 + j][k] of fp32 row-major matrices
+// in shared memory (leading dimension LD), with tensor cores: sc * X and sc * Y are
+// split into binary16 high and low parts and C = Xh Yh^T + Xh Yl^T + Xl Yh^T (fp32
+// accumulation; each product carries a relative error of about 2^-22, and sc keeps the
+// values in binary16's normal range).  One warp; fragment layout of mma m16n8k16.
+__device__ __forceinline__ void split_h2(float x, float y, uint32_t &hi, uint32_t &lo)
+{
+    const __half2 h = __floats2half2_rn(x, y);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+template <int K, int LD>
+__device__ __forceinline__ void xyt_tile(const float *X, int i0, const float *Y, int j0,
+                                         float sc, float (&c)[4])
+{
+    const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const float *x0 = X + (i0 + gid) * LD, *x1 = x0 + 8 * LD;
+    const float *y0 = Y + (j0 + gid) * LD;
+#pragma unroll
+    for (int s = 0; s < K / 16; ++s) {
+        const int k = 16 * s + 2 * tig;
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_h2(sc * x0[k], sc * x0[k + 1], ah[0], al[0]);
+        split_h2(sc * x1[k], sc * x1[k + 1], ah[1], al[1]);
+        split_h2(sc * x0[k + 8], sc * x0[k + 9], ah[2], al[2]);
+        split_h2(sc * x1[k + 8], sc * x1[k + 9], ah[3], al[3]);
+        split_h2(sc * y0[k], sc * y0[k + 1], bh[0], bl[0]);
+        split_h2(sc * y0[k + 8], sc * y0[k + 9], bh[1], bl[1]);
+        mma16816(c, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
+        mma16816(c, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+        mma16816(c, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+    }
+}
+
+// dst = src * src for a symmetric 32 x 32 matrix (entries of magnitude <= 32), one
+// 16 x 8 tile per warp (8 warps).
 __device__ __forceinline__ void square32(const float (*src)[KIVI_G + 1], float (*dst)[KIVI_G + 1])
 {
-    const int a = threadIdx.x / 16, b2 = threadIdx.x % 16;
-    float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < KIVI_G; ++k) {
-        const float r0 = src[2 * a][k], r1 = src[2 * a + 1][k];
-        const float c0 = src[k][2 * b2], c1 = src[k][2 * b2 + 1];
-        s00 = fmaf(r0, c0, s00);
-        s01 = fmaf(r0, c1, s01);
-        s10 = fmaf(r1, c0, s10);
-        s11 = fmaf(r1, c1, s11);
-    }
-    dst[2 * a][2 * b2] = s00;
-    dst[2 * a][2 * b2 + 1] = s01;
-    dst[2 * a + 1][2 * b2] = s10;
-    dst[2 * a + 1][2 * b2 + 1] = s11;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i0 = 16 * (warp >> 2), j0 = 8 * (warp & 3), gid = lane >> 2, tig = lane & 3;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    xyt_tile<KIVI_G, KIVI_G + 1>(&src[0][0], i0, &src[0][0], j0, 1.f, c);
+    dst[i0 + gid][j0 + 2 * tig] = c[0];
+    dst[i0 + gid][j0 + 2 * tig + 1] = c[1];
+    dst[i0 + gid + 8][j0 + 2 * tig] = c[2];
+    dst[i0 + gid + 8][j0 + 2 * tig + 1] = c[3];
 }
 
 // Orthonormalise the two columns (x0, x1) a warp holds, one row per lane; a
@@ -388,6 +418,8 @@ __device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &g
 #pragma unroll
         for (int u = 0; u < PER; ++u) {
             const bool in = (key[u] & mask) == prefix;
+            if (!__any_sync(0xffffffffu, in))
+                continue;
             const int dg = in ? (int)((key[u] >> shift) & 255) : 256;
             const unsigned same = __match_any_sync(0xffffffffu, dg);
             if (in && lane == __ffs(same) - 1)
@@ -461,19 +493,17 @@ __device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &g
         }
     }
     __syncthreads();
-    // 4. Gram matrix R R^T, a 2 x 2 block of it per thread, scaled by its largest entry
+    // 4. Gram matrix R R^T with tensor cores, one 16 x 8 tile per warp, scaled by its
+    //    largest entry.  Every entry of R is at most the threshold key, so R * 2^(130 - e)
+    //    (e: the threshold's exponent field) stays below 16 in binary16.
     {
-        const int a = tid / 16, b2 = tid % 16;
-        float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
-        for (int d = 0; d < D; ++d) {
-            const float r0 = gs.e[2 * a][d], r1 = gs.e[2 * a + 1][d];
-            const float c0 = gs.e[2 * b2][d], c1 = gs.e[2 * b2 + 1][d];
-            s00 = fmaf(r0, c0, s00);
-            s01 = fmaf(r0, c1, s01);
-            s10 = fmaf(r1, c0, s10);
-            s11 = fmaf(r1, c1, s11);
-        }
-        float mx = fmaxf(fmaxf(fabsf(s00), fabsf(s01)), fmaxf(fabsf(s10), fabsf(s11)));
+        static_assert(QTHREADS == 256, "eight warps cover the 32 x 32 Gram matrix");
+        const int ex = (int)((prefix >> 23) & 255);
+        const float sc = prefix ? __int_as_float(min(257 - ex, 254) << 23) : 1.f;
+        const int i0 = 16 * (warp >> 2), j0 = 8 * (warp & 3), gid = lane >> 2, tig = lane & 3;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        xyt_tile<D, D + 1>(&gs.e[0][0], i0, &gs.e[0][0], j0, sc, c);
+        float mx = fmaxf(fmaxf(fabsf(c[0]), fabsf(c[1])), fmaxf(fabsf(c[2]), fabsf(c[3])));
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1)
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
@@ -485,10 +515,10 @@ __device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &g
         for (int w = 0; w < QTHREADS / 32; ++w)
             m = fmaxf(m, __int_as_float(gs.scan[w]));
         const float inv_m = m > 0.f ? 1.f / m : 0.f;
-        gs.gm[2 * a][2 * b2] = s00 * inv_m;
-        gs.gm[2 * a][2 * b2 + 1] = s01 * inv_m;
-        gs.gm[2 * a + 1][2 * b2] = s10 * inv_m;
-        gs.gm[2 * a + 1][2 * b2 + 1] = s11 * inv_m;
+        gs.gm[i0 + gid][j0 + 2 * tig] = c[0] * inv_m;
+        gs.gm[i0 + gid][j0 + 2 * tig + 1] = c[1] * inv_m;
+        gs.gm[i0 + gid + 8][j0 + 2 * tig] = c[2] * inv_m;
+        gs.gm[i0 + gid + 8][j0 + 2 * tig + 1] = c[3] * inv_m;
     }
     __syncthreads();
     square32(gs.gm, gs.gm2);                   // (R R^T)^2, entries <= 32
@@ -746,13 +776,13 @@ __global__ void __launch_bounds__(QTHREADS)
         const uint16_t *kr = k_res + (size_t)unit * CR * D;
         const uint16_t *vr = v_res + (size_t)unit * CR * D;
         for (long g = nq0 / G + blockIdx.y; g < nq1 / G; g += gridDim.y) {
-            const long long off = blocks.offset(unit, g);
-            if (off < 0) {   // no page behind this group: skip it, flag it
+            const long long gi = blocks.index(unit, g);
+            if (gi < 0) {   // no page behind this group: skip it, flag it
                 if (threadIdx.x == 0)
                     flag_error(status, DEV_CAPACITY);
                 continue;
             }
-            const size_t gi = (size_t)unit * (Cq / G) + g;   // GEAR: dense layout only
+            const long long off = gi * blocks.block;
             pack_group<D, BITS, GEAR>(g, T0, CR, kn, vn, kr, vr, kb + off, vb + off, sm, gs,
                                       GEAR ? kg + gi * SIDE : nullptr,
                                       GEAR ? vg + gi * SIDE : nullptr);

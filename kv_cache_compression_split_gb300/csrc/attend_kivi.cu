@@ -104,7 +104,7 @@ struct KiviParams {
     uint16_t *o;
     float *lse;
     const uint8_t *kb, *vb;
-    const uint8_t *kg, *vg;         // GEAR side blocks [units, Cq / G, SIDE] (dense)
+    const uint8_t *kg, *vg;         // GEAR side blocks, indexed like the group blocks
     GroupBlocks blocks;             // dense or paged group blocks
     const int32_t *len;
     float *part_o, *part_ml;
@@ -284,8 +284,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                         // a tile is 4 groups, one page in the paged layout
                         const int g0 = (w.qt0 + i - w.nr) * Cfg::QG;
                         const int ng = min(Cfg::QG, w.n_groups - g0);
-                        const long long off = p.blocks.offset(w.unit, g0);
-                        if (off < 0) {
+                        const long long bi = p.blocks.index(w.unit, g0);
+                        const long long off = bi * p.blocks.block;
+                        if (bi < 0) {
                             // no page behind the tile: no copy, the stage completes empty
                             flag_error(p.status, DEV_CAPACITY);
                             mbar_arrive(&full[st]);
@@ -295,9 +296,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                             bulk_load(dst + Cfg::QG * Cfg::BLOCK, p.vb + off, ng * Cfg::BLOCK,
                                       &full[st]);
                             if constexpr (GEAR) {
-                                // side blocks of the same groups (dense layout)
-                                const long long so =
-                                    ((long long)w.unit * (p.Cq / Cfg::G) + g0) * Cfg::SIDE;
+                                // side blocks of the same groups, at the same pool index
+                                const long long so = bi * Cfg::SIDE;
                                 uint8_t *sd = dst + 2 * Cfg::QG * Cfg::BLOCK;
                                 bulk_load(sd, p.kg + so, ng * Cfg::SIDE, &full[st]);
                                 bulk_load(sd + Cfg::QG * Cfg::SIDE, p.vg + so, ng * Cfg::SIDE,

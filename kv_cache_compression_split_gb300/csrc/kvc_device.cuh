@@ -62,15 +62,22 @@ constexpr int KIVI_PAGE_GROUPS = 4;   // KVC_KIVI_PAGE_GROUPS
 struct GroupBlocks {
     const int32_t *table;   // nullptr: dense layout
     int groups_per_unit, num_pages, block;
-    __device__ __forceinline__ long long offset(int unit, long g) const
+    // Index of group g's block in its pool (-1: no page behind it); GEAR side blocks
+    // use the same index in their own pools.
+    __device__ __forceinline__ long long index(int unit, long g) const
     {
         if (!table)
-            return ((long long)unit * groups_per_unit + g) * block;
+            return (long long)unit * groups_per_unit + g;
         const int pg = table[(size_t)unit * (groups_per_unit / KIVI_PAGE_GROUPS) +
                              g / KIVI_PAGE_GROUPS];
         if (pg < 0 || pg >= num_pages)
             return -1;
-        return ((long long)pg * KIVI_PAGE_GROUPS + g % KIVI_PAGE_GROUPS) * block;
+        return (long long)pg * KIVI_PAGE_GROUPS + g % KIVI_PAGE_GROUPS;
+    }
+    __device__ __forceinline__ long long offset(int unit, long g) const
+    {
+        const long long i = index(unit, g);
+        return i < 0 ? -1 : i * block;
     }
 };
 

@@ -180,15 +180,18 @@ def test_write_through_a_missing_page_is_flagged(kvc):
     assert kvc.kvc_read_device_status() == 0
 
 
-def _gather_kivi(cache):
-    """Logical [B, Hkv, Cq/32, block] K and V blocks of a paged KIVI cache."""
+def _gather_kivi(cache, pools=("k_blocks", "v_blocks")):
+    """Logical [B, Hkv, Cq/32, block] views of a paged KIVI cache's pools (the K and V blocks,
+    or the GEAR side blocks)."""
     B, Hkv, Cq = cache.B, cache.Hkv, cache.Cq
     tbl = cache.block_table.long().clamp(min=0)                     # [B, Hkv, Cq/128]
     idx = (tbl[..., :, None] * 4 + torch.arange(4, device=tbl.device)).reshape(-1)
-    bb = cache.k_blocks.shape[-1]
-    kb = cache.k_blocks.reshape(-1, bb)[idx].reshape(B, Hkv, Cq // 32, bb)
-    vb = cache.v_blocks.reshape(-1, bb)[idx].reshape(B, Hkv, Cq // 32, bb)
-    return kb, vb
+    out = []
+    for name in pools:
+        pool = getattr(cache, name)
+        bb = pool.shape[-1]
+        out.append(pool.reshape(-1, bb)[idx].reshape(B, Hkv, Cq // 32, bb))
+    return tuple(out)
 
 
 def _attend_kivi(kvc, cache, q, splits=0):
@@ -198,8 +201,13 @@ def _attend_kivi(kvc, cache, q, splits=0):
     return o
 
 
-@pytest.mark.parametrize("D,bits,R", [(128, 4, 128), (128, 2, 16), (64, 4, 32)])
-def test_paged_kivi_equals_dense(kvc, D, bits, R):
+@pytest.mark.parametrize("D,bits,R,gear", [(128, 4, 128, False), (128, 2, 16, False),
+                                            (64, 4, 32, False), (128, 4, 128, True),
+                                            (64, 4, 32, True)])
+def test_paged_kivi_equals_dense(kvc, D, bits, R, gear):
+    """KIVI (and GEAR: side blocks in pools behind the same table) through shuffled pages:
+    bulk and decode appends write the same blocks as the dense layout, and attention is
+    bit-identical."""
     B, Hq, Hkv, P, steps, Cq = 3, 8, 2, 500, 40, 640
     g = torch.Generator().manual_seed(D + bits + R)
     Ks = torch.randn(B, Hkv, P + steps, D, generator=g).half().cuda()
@@ -209,8 +217,9 @@ def test_paged_kivi_equals_dense(kvc, D, bits, R):
     num_pages = B * Hkv * npu + 5
     perm = torch.from_numpy(np.random.default_rng(D + bits).permutation(num_pages)
                             [:B * Hkv * npu].astype(np.int32)).view(B, Hkv, npu)
-    dense = kvc.QuantCache.empty(B, Hkv, Cq, D, bits, R)
-    paged = kvc.QuantCache.empty_paged(B, Hkv, Cq, D, bits, R, num_pages, block_table=perm)
+    dense = kvc.QuantCache.empty(B, Hkv, Cq, D, bits, R, gear=gear)
+    paged = kvc.QuantCache.empty_paged(B, Hkv, Cq, D, bits, R, num_pages, block_table=perm,
+                                       gear=gear)
     for c in (dense, paged):
         kvc.kvc_append_quant(c, Ks[:, :, :P].contiguous(), Vs[:, :, :P].contiguous())
     for t in range(steps + 1):
@@ -225,6 +234,10 @@ def test_paged_kivi_equals_dense(kvc, D, bits, R):
             assert torch.equal(dense.k_blocks[:, :, :n_groups], kb[:, :, :n_groups])
             assert torch.equal(dense.v_blocks[:, :, :n_groups], vb[:, :, :n_groups])
             assert torch.equal(dense.k_res, paged.k_res) and torch.equal(dense.v_res, paged.v_res)
+            if gear:
+                kg, vg = _gather_kivi(paged, ("k_gear", "v_gear"))
+                assert torch.equal(dense.k_gear[:, :, :n_groups], kg[:, :, :n_groups])
+                assert torch.equal(dense.v_gear[:, :, :n_groups], vg[:, :, :n_groups])
             for splits in (0, 2):
                 assert torch.equal(_attend_kivi(kvc, dense, q, splits),
                                    _attend_kivi(kvc, paged, q, splits))
