@@ -211,10 +211,13 @@ template <int D> struct __align__(16) GroupSmem {
 };
 
 // Extra staging of the GEAR side data of one matrix (K, then V) of a group.
+// Rows are padded by 8 words: 64-bit fragment loads of a half-warp (8 rows x 2 columns
+// pairs) then hit every bank once.
+constexpr int GM_LD = KIVI_G + 8;
 template <int D> struct __align__(16) GearSmem {
-    float e[KIVI_G][D + 1];      // residual, then R (sparse entries zeroed); rows padded
-    float gm[KIVI_G][KIVI_G + 1];
-    float gm2[KIVI_G][KIVI_G + 1];
+    float e[KIVI_G][D + 8];      // residual, then R (sparse entries zeroed)
+    float gm[KIVI_G][GM_LD];
+    float gm2[KIVI_G][GM_LD];
     float a[2][KIVI_G];          // orthonormal left factors
     int hist[256];
     int scan[QTHREADS / 32 + 1];
@@ -239,37 +242,6 @@ __device__ __forceinline__ int quant_code_fast(uint16_t xb, float zero_f, float 
         return quant_code_inv(xb, sm.zfix[pi], zero_f, sm.sfix[pi], inv, cmax);
     const int c = __float2int_rn(est);
     return c < 0 ? 0 : (c > cmax ? cmax : c);
-}
-
-// Exclusive prefix sum over the CTA of one value per thread (sh: QTHREADS/32 + 1 ints).
-__device__ __forceinline__ int block_exclusive_scan(int v, int *sh)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o)
-            x += y;
-    }
-    if (lane == 31)
-        sh[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int w = lane < QTHREADS / 32 ? sh[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o)
-                w += y;
-        }
-        if (lane < QTHREADS / 32)
-            sh[lane] = w;                      // inclusive prefix of the warp totals
-    }
-    __syncthreads();
-    const int before = warp > 0 ? sh[warp - 1] : 0;
-    __syncthreads();                           // sh may be reused right after
-    return before + x - v;
 }
 
 __device__ __forceinline__ float warp_sum(float v)
@@ -298,19 +270,23 @@ template <int K, int LD>
 __device__ __forceinline__ void xyt_tile(const float *X, int i0, const float *Y, int j0,
                                          float sc, float (&c)[4])
 {
+    static_assert(LD % 32 == 8, "conflict-free 64-bit fragment loads need LD = 8 mod 32");
     const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     const float *x0 = X + (i0 + gid) * LD, *x1 = x0 + 8 * LD;
     const float *y0 = Y + (j0 + gid) * LD;
+    auto ld2 = [](const float *p) { return *reinterpret_cast<const float2 *>(p); };
 #pragma unroll
     for (int s = 0; s < K / 16; ++s) {
         const int k = 16 * s + 2 * tig;
         uint32_t ah[4], al[4], bh[2], bl[2];
-        split_h2(sc * x0[k], sc * x0[k + 1], ah[0], al[0]);
-        split_h2(sc * x1[k], sc * x1[k + 1], ah[1], al[1]);
-        split_h2(sc * x0[k + 8], sc * x0[k + 9], ah[2], al[2]);
-        split_h2(sc * x1[k + 8], sc * x1[k + 9], ah[3], al[3]);
-        split_h2(sc * y0[k], sc * y0[k + 1], bh[0], bl[0]);
-        split_h2(sc * y0[k + 8], sc * y0[k + 9], bh[1], bl[1]);
+        const float2 p0 = ld2(x0 + k), p1 = ld2(x1 + k), p2 = ld2(x0 + k + 8),
+                     p3 = ld2(x1 + k + 8), q0 = ld2(y0 + k), q1 = ld2(y0 + k + 8);
+        split_h2(sc * p0.x, sc * p0.y, ah[0], al[0]);
+        split_h2(sc * p1.x, sc * p1.y, ah[1], al[1]);
+        split_h2(sc * p2.x, sc * p2.y, ah[2], al[2]);
+        split_h2(sc * p3.x, sc * p3.y, ah[3], al[3]);
+        split_h2(sc * q0.x, sc * q0.y, bh[0], bl[0]);
+        split_h2(sc * q1.x, sc * q1.y, bh[1], bl[1]);
         mma16816(c, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
         mma16816(c, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
         mma16816(c, al[0], al[1], al[2], al[3], bh[0], bh[1]);
@@ -319,12 +295,12 @@ __device__ __forceinline__ void xyt_tile(const float *X, int i0, const float *Y,
 
 // dst = src * src for a symmetric 32 x 32 matrix (entries of magnitude <= 32), one
 // 16 x 8 tile per warp (8 warps).
-__device__ __forceinline__ void square32(const float (*src)[KIVI_G + 1], float (*dst)[KIVI_G + 1])
+__device__ __forceinline__ void square32(const float (*src)[GM_LD], float (*dst)[GM_LD])
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i0 = 16 * (warp >> 2), j0 = 8 * (warp & 3), gid = lane >> 2, tig = lane & 3;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
-    xyt_tile<KIVI_G, KIVI_G + 1>(&src[0][0], i0, &src[0][0], j0, 1.f, c);
+    xyt_tile<KIVI_G, GM_LD>(&src[0][0], i0, &src[0][0], j0, 1.f, c);
     dst[i0 + gid][j0 + 2 * tig] = c[0];
     dst[i0 + gid][j0 + 2 * tig + 1] = c[1];
     dst[i0 + gid + 8][j0 + 2 * tig] = c[2];
@@ -394,11 +370,14 @@ __device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &g
     constexpr int RAW = 4 * NS + 4 * G + 4 * D;
     constexpr int SIDE = (RAW + 15) / 16 * 16;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // 1. residual of my PER contiguous elements (flat index tid * PER + u)
+    // 1. residual of my PER elements: warp w owns flat indices [32 PER w, 32 PER (w + 1)),
+    //    lane L of it 32 u + L (u < PER), so a warp's accesses cover 32 consecutive
+    //    elements of one row
+    const auto flat = [&](int u) { return 32 * PER * warp + 32 * u + lane; };
     uint32_t key[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
-        const int i = tid * PER + u, t = i / D, d = i % D;
+        const int i = flat(u), t = i / D, d = i % D;
         const int pi = ISK ? d : D + t * NG + d / G;
         const float x = __half2float(__ushort_as_half(ISK ? sm.xk[t][d] : sm.xv[t][d]));
         const float code = (float)(ISK ? sm.ck[t][d] : sm.cv[t][d]);
@@ -466,31 +445,50 @@ __device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &g
         need = gs.misc[1];
         __syncthreads();
     }
-    // 3. keep every key above the threshold and the first `need` equal to it (flat order)
-    int ties = 0;
+    // 3. keep every key above the threshold and the first `need` equal to it, in flat
+    //    order: ranks from per-u ballots within the warp plus the earlier warps' totals
+    const unsigned lt = (1u << lane) - 1u;
+    int wcount = 0;
 #pragma unroll
     for (int u = 0; u < PER; ++u)
-        ties += key[u] == prefix;
-    int rank = block_exclusive_scan(ties, gs.scan);
-    bool sel[PER];
-    int nsel = 0;
+        wcount += __popc(__ballot_sync(0xffffffffu, key[u] == prefix));
+    if (lane == 0)
+        gs.scan[warp] = wcount;
+    __syncthreads();
+    int run = 0;
+    for (int w = 0; w < warp; ++w)
+        run += gs.scan[w];
+    __syncthreads();                           // gs.scan is written again below
+    uint32_t selm = 0;                         // bit u: element u selected
+    wcount = 0;
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
-        sel[u] = key[u] > prefix || (key[u] == prefix && rank++ < need);
-        nsel += sel[u];
+        const unsigned tb = __ballot_sync(0xffffffffu, key[u] == prefix);
+        const bool sel = key[u] > prefix || (((tb >> lane) & 1u) && run + __popc(tb & lt) < need);
+        run += __popc(tb);
+        selm |= (uint32_t)sel << u;
+        wcount += __popc(__ballot_sync(0xffffffffu, sel));
     }
-    int o = block_exclusive_scan(nsel, gs.scan);
+    if (lane == 0)
+        gs.scan[warp] = wcount;
+    __syncthreads();
+    int o = 0;
+    for (int w = 0; w < warp; ++w)
+        o += gs.scan[w];
     uint16_t *idx_out = reinterpret_cast<uint16_t *>(side);
     __half *val_out = reinterpret_cast<__half *>(side + 2 * NS);
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
-        if (sel[u] && o < NS) {                // exactly NS are selected; the bound is a guard
-            const int i = tid * PER + u, t = i / D, d = i % D;
-            idx_out[o] = (uint16_t)i;
-            val_out[o] = __float2half_rn(gs.e[t][d]);
+        const bool sel = (selm >> u) & 1u;
+        const unsigned sb = __ballot_sync(0xffffffffu, sel);
+        const int pos = o + __popc(sb & lt);
+        if (sel && pos < NS) {                 // exactly NS are selected; the bound is a guard
+            const int i = flat(u), t = i / D, d = i % D;
+            idx_out[pos] = (uint16_t)i;
+            val_out[pos] = __float2half_rn(gs.e[t][d]);
             gs.e[t][d] = 0.f;                  // R: the rest of the residual
-            ++o;
         }
+        o += __popc(sb);
     }
     __syncthreads();
     // 4. Gram matrix R R^T with tensor cores, one 16 x 8 tile per warp, scaled by its
@@ -502,7 +500,7 @@ __device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &g
         const float sc = prefix ? __int_as_float(min(257 - ex, 254) << 23) : 1.f;
         const int i0 = 16 * (warp >> 2), j0 = 8 * (warp & 3), gid = lane >> 2, tig = lane & 3;
         float c[4] = {0.f, 0.f, 0.f, 0.f};
-        xyt_tile<D, D + 1>(&gs.e[0][0], i0, &gs.e[0][0], j0, sc, c);
+        xyt_tile<D, D + 8>(&gs.e[0][0], i0, &gs.e[0][0], j0, sc, c);
         float mx = fmaxf(fmaxf(fabsf(c[0]), fabsf(c[1])), fmaxf(fabsf(c[2]), fabsf(c[3])));
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1)
@@ -744,7 +742,7 @@ __device__ __forceinline__ long kivi_nq(long T, int R)
 // it writes may be ones a flushed group still reads); bulk appends run the
 // groups on a wide grid first and the residual in a second launch.
 template <int D, int BITS, bool GROUPS, bool RESIDUAL, bool GEAR>
-__global__ void __launch_bounds__(QTHREADS)
+__global__ void __launch_bounds__(QTHREADS, GEAR ? 2 : 3)
     k_append_quant(int Hkv, int R, int Cq, int n_new, const uint16_t *__restrict__ k_new,
                    const uint16_t *__restrict__ v_new, uint8_t *__restrict__ kb,
                    uint8_t *__restrict__ vb, uint16_t *__restrict__ k_res,

@@ -77,6 +77,42 @@ def test_gear_pack_against_oracle(kvc, orc, D, bits, chunks):
     assert device_status_clean(kvc)
 
 
+def test_gear_pack_ties(kvc, orc):
+    """Selections decided by ties, bit-exact against the oracle: groups on the 4-bit grid
+    (every residual 0: the sparse part is the first n_s flat indices) and grid groups with 200
+    entries moved by exactly +-1/64 (all |e| equal at the threshold: the lowest 82 of them by
+    flat index, spread over every warp's range)."""
+    D, bits, R = 128, 4, 32
+    rng = np.random.default_rng(21)
+    td = (np.arange(G)[:, None] + np.arange(D)[None, :]) % 32
+    pin = (td == 0) | (td == 1)
+
+    def grid_group(n_moved):
+        C = rng.integers(1, 15, (G, D)).astype(np.float64)
+        C[td == 0], C[td == 1] = 0, 15
+        x = 4.0 * (-1.0 + C / 16.0)
+        free = np.flatnonzero(~pin.reshape(-1))
+        moved = rng.choice(free, n_moved, replace=False)
+        x.reshape(-1)[moved] += rng.choice([-1.0, 1.0], n_moved) / 64
+        return x.astype(np.float16)
+
+    groups = [grid_group(0), grid_group(200), grid_group(200), grid_group(0)]
+    n_ring = 40
+    X = np.concatenate(groups + [(rng.standard_normal((n_ring, D)) - 2).astype(np.float16)])
+    K = torch.from_numpy(X)[None, None]
+    V = torch.from_numpy(np.ascontiguousarray(X[::-1]))[None, None]   # other tie positions
+    T = X.shape[0]
+    cache, _ = _build_gear(kvc, K, V, bits, R, 512, [T - 3, 3], [0])
+    n_q = kivi_nq(T, R)
+    gz = gr.quantize_unit(np16(K[0, 0, :n_q]), np16(V[0, 0, :n_q]), n_q, bits)
+    kg, vg = cache.k_gear[0, 0].cpu().numpy(), cache.v_gear[0, 0].cpu().numpy()
+    for gi in range(n_q // G):
+        for side, ref in ((kg[gi], gz["k"][gi]), (vg[gi], gz["v"][gi])):
+            _check_group(side, ref, D)
+    assert np.array_equal(gz["k"][0]["idx"].astype(np.int64), np.arange(gr.n_sparse(D)))
+    assert device_status_clean(kvc)
+
+
 # ------------------------------------------------------------------ decode attention
 # Logits carry the KIVI path's binary16 rounding of q * s (see test_gpu_kivi.py) plus the
 # rank-2 factors' difference between the GPU's subspace iteration and the oracle's SVD.
