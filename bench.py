@@ -5,7 +5,7 @@ Workload (N=1): the heavy-load LLaMA3-70B-shaped layer -- GQA 64 query / 8 KV he
 head_dim 128, batch 512, KV length 2048, fp16 N(0,1) from a seed.  One timed step is
 one decode step of every method on that batch, all through the C ABI:
   FP16      append the new token, attend over the full cache
-  H2O-512   append, attend (writing logits / lse), accumulate scores, evict to 64 + 448
+  H2O-512   append, attend with the score update fused (logits on chip), evict to 64 + 448
   KIVI-4    append (quantising a group when the residual fills), attend
   Stream-512 append, attend, evict to 64 sinks + 448 recent
 value = tokens produced per second by the whole step (4 methods x batch per step).
@@ -109,8 +109,8 @@ def slot_bytes(n_slots, B, Hkv, Hq, D):
 
 # DRAM bytes (read + write) per (sequence, KV head) unit and cached token that ncu measured
 # for k_attend_slots on the FP16 cache (64-sequence case of the heavy-load workload:
-# dram__bytes_read.sum + dram__bytes_write.sum = 538.0 + 4.1 MB over 64 x 8 units x 2048 tokens).
-SLOT_ATTEND_DRAM_BYTES_PER_UNIT_TOKEN = 542.1e6 / (64 * 8 * 2048)
+# dram__bytes_read.sum + dram__bytes_write.sum = 538.0 + 4.4 MB over 64 x 8 units x 2048 tokens).
+SLOT_ATTEND_DRAM_BYTES_PER_UNIT_TOKEN = 542.3e6 / (64 * 8 * 2048)
 
 
 def kivi_bytes(T, R, B, Hkv, Hq, D, bits):
@@ -210,7 +210,6 @@ def run_gpu(args, rank, world):
         vn = torch.randn(S_total, 4, B, Hkv, 1, D, generator=gq, device=dev).half()
         outs = torch.empty(4, B, Hq, D, dtype=torch.float16, device=dev)
         outs_base = outs
-        logits = torch.empty(B, Hq, Ch, dtype=torch.float32, device=dev)
         lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
 
         def ws_for(cache):
@@ -243,8 +242,8 @@ def run_gpu(args, rank, world):
         kvc.kvc_append(fp, kn[i, 0], vn[i, 0], stream=stream); mark(1)
         kvc.kvc_decode_attend(fp, qs[i, 0], outs[0], workspace=ws_fp, stream=stream); mark(2)
         kvc.kvc_append(h2o, kn[i, 1], vn[i, 1], stream=stream); mark(3)
-        # attention and the heavy-hitter score update in one launch
-        kvc.kvc_decode_attend(h2o, qs[i, 1], outs[1], logits=logits, lse=lse, workspace=ws_h2o,
+        # attention and the heavy-hitter score update in one launch (logits kept on chip)
+        kvc.kvc_decode_attend(h2o, qs[i, 1], outs[1], lse=lse, workspace=ws_h2o,
                               h2o_scores=h2o_scores, stream=stream); mark(4)
         mark(5)
         kvc.kvc_h2o_evict(h2o, h2o_scores, n_heavy, n_recent, stream=stream); mark(6)
@@ -434,7 +433,6 @@ def h2o_variant_rows(kvc, dev, stream, src, src_scores, qs, kn, vn, n_heavy, n_r
     out = {}
     with torch.cuda.stream(stream):
         o = torch.empty(B, Hq, D, dtype=torch.float16, device=dev)
-        logits = torch.empty(B, Hq, C, dtype=torch.float32, device=dev)
         lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
         for name, decay, trig in (("h2o512_decay", 0.99, None), ("h2o512_batched", 0.0, trigger)):
             c = kvc.SlotCache.empty(B, Hkv, C, D, device=dev)
@@ -453,8 +451,8 @@ def h2o_variant_rows(kvc, dev, stream, src, src_scores, qs, kn, vn, n_heavy, n_r
             for i in range(steps):
                 k = i % qs.shape[0]
                 kvc.kvc_append(c, kn[k], vn[k], stream=stream)
-                kvc.kvc_decode_attend(c, qs[k], o, logits=logits, lse=lse, workspace=ws,
-                                      num_splits=1, h2o_scores=sc, h2o_decay=decay, stream=stream)
+                kvc.kvc_decode_attend(c, qs[k], o, lse=lse, workspace=ws, num_splits=1,
+                                      h2o_scores=sc, h2o_decay=decay, stream=stream)
                 if trig is None:
                     kvc.kvc_h2o_evict(c, sc, n_heavy, n_recent, stream=stream)
                 else:
@@ -719,13 +717,13 @@ def run_profile(args):
         cache = kvc.SlotCache.empty(B, Hkv, n_slots + 7, D, device=dev)
         kvc.kvc_append(cache, K[:, :, :n_slots].contiguous(), V[:, :, :n_slots].contiguous())
         ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), device=dev)
-        logits = torch.empty(B, Hq, cache.C, dtype=torch.float32, device=dev)
         lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
         scores = torch.rand(B, Hkv, cache.C, device=dev)
         for _ in range(3):
-            if what.startswith("attend"):
-                kvc.kvc_decode_attend(cache, q, o, logits=logits if what == "attend_h2o" else None,
-                                      lse=lse, workspace=ws)
+            if what == "attend_h2o":   # attention + fused score update, logits on chip
+                kvc.kvc_decode_attend(cache, q, o, lse=lse, num_splits=1, h2o_scores=scores)
+            elif what.startswith("attend"):
+                kvc.kvc_decode_attend(cache, q, o, lse=lse, workspace=ws)
             elif what == "h2o_evict":
                 c = kvc.SlotCache(cache.K, cache.V, cache.pos.clone(), cache.n.clone(), cache.seqlen)
                 kvc.kvc_h2o_evict(c, scores.clone(), w.n_heavy, w.n_recent)

@@ -240,13 +240,19 @@ enum { KVC_KIND_SLOTS = 0, KVC_KIND_KIVI = 1 };
  *               (may be NULL when that size is 0)
  *   num_splits  KV splits per unit (0 = chosen from the SM count)
  *   softmax_scale 0 for 1/sqrt(D)
- *   h2o_scores  optional [B, Hkv, C] fp32 (slot caches only; needs logits and
- *               lse): the step's attention probabilities are folded into the
- *               heavy-hitter scores in the same launch, exactly as
- *               kvc_h2o_accumulate(KVC_H2O_DECODE) with decay h2o_decay would
+ *   h2o_scores  optional [B, Hkv, C] fp32 (slot caches only; needs lse): the
+ *               step's attention probabilities are folded into the heavy-hitter
+ *               scores in the same launch, exactly as
+ *               kvc_h2o_accumulate(KVC_H2O_DECODE) with decay h2o_decay would.
+ *               With logits NULL the launch keeps the logits on chip: it then
+ *               runs in one split (num_splits 0 or 1; another value is
+ *               KVC_ERR_INVALID_ARG) and needs C <= KVC_H2O_ONCHIP_MAX_SLOTS
+ *               (else KVC_ERR_UNSUPPORTED).  With logits given, any split count
+ *               works (several splits add one kvc_h2o_accumulate launch).
  *   h2o_decay   0 (plain H2O, scores += p) or lambda in (0, 1) (decayed
  *               scores = lambda * scores + (1 - lambda) * p); see kvc_h2o_args
  */
+#define KVC_H2O_ONCHIP_MAX_SLOTS 1024
 typedef struct kvc_attend_args {
     int kind;
     int Hq;

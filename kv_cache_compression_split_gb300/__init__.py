@@ -29,6 +29,7 @@ KVC_H2O_DECODE, KVC_H2O_PREFILL = 0, 1
 KIVI_GROUP = 32
 PAGE_SLOTS = 64            # KVC_PAGE_SLOTS: slots per page of the paged layout
 KIVI_PAGE_GROUPS = 4       # KVC_KIVI_PAGE_GROUPS: 32-token groups per KIVI page
+H2O_ONCHIP_MAX_SLOTS = 1024   # KVC_H2O_ONCHIP_MAX_SLOTS: fused H2O with logits kept on chip
 KVC_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 

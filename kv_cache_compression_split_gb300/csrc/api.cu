@@ -194,7 +194,17 @@ AttendPlanFull plan_full(const kvc_attend_args *a)
         f.Hkv = a->slots->Hkv;
         f.D = a->slots->D;
         const int tiles = (a->slots->C + TILE - 1) / TILE;
-        f.plan = plan_attend(f.B * f.Hkv, tiles, a->num_splits);
+        int splits = a->num_splits;
+        if (a->h2o_scores && !a->logits) {   // fused H2O with the logits on chip
+            if (splits > 1)
+                return f;
+            if (a->slots->C > H2O_ONCHIP_MAX_SLOTS) {
+                f.st = KVC_ERR_UNSUPPORTED;
+                return f;
+            }
+            splits = 1;
+        }
+        f.plan = plan_attend(f.B * f.Hkv, tiles, splits);
         f.ws = f.plan.splits > 1 ? (size_t)f.B * a->Hq * f.plan.splits * (f.D + 2) * sizeof(float)
                                  : 0;
     } else if (a->kind == KVC_KIND_KIVI) {
@@ -292,7 +302,7 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         return KVC_ERR_INVALID_ARG;
     if (a->kind == KVC_KIND_KIVI && (a->logits || a->h2o_scores))
         return KVC_ERR_UNSUPPORTED;
-    if (a->h2o_scores && (!a->logits || !a->lse))
+    if (a->h2o_scores && !a->lse)
         return KVC_ERR_INVALID_ARG;
     float h2o_keep = 1.f, h2o_add = 1.f;
     if (!h2o_decay_weights(a->h2o_decay, &h2o_keep, &h2o_add))

@@ -32,12 +32,16 @@ constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-template <int D> struct SlotCfg {
+// LSM: the fused H2O launch keeps the unit's logits in shared memory ([8][LSM_SLOTS]
+// fp32) instead of an output array, with fewer stages to make room.
+constexpr int LSM_SLOTS = H2O_ONCHIP_MAX_SLOTS;
+template <int D, bool LSM = false> struct SlotCfg {
     static constexpr int NBOX = D / 64;                 // 64-half (128-byte) boxes per row
     static constexpr int TILE_BYTES = TILE * D * 2;     // one K or V tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K + V
-    static constexpr int NSTAGE = (D == 128) ? 3 : 6;
-    static constexpr int SMEM = NSTAGE * STAGE_BYTES + 1024 + 2 * NSTAGE * 8;
+    static constexpr int NSTAGE = LSM ? ((D == 128) ? 2 : 4) : ((D == 128) ? 3 : 6);
+    static constexpr int LSM_BYTES = LSM ? 8 * LSM_SLOTS * 4 : 0;
+    static constexpr int SMEM = NSTAGE * STAGE_BYTES + LSM_BYTES + 1024 + 2 * NSTAGE * 8;
     static_assert(NCW * (8 * D + 16) * 4 <= NSTAGE * STAGE_BYTES, "combine scratch must fit");
 };
 
@@ -62,16 +66,18 @@ __device__ __forceinline__ void consumer_bar()
 }
 
 // Slots [0, n) of each unit are valid.
-template <int D>
+template <int D, bool LSM>
 __global__ void __launch_bounds__(NTHREADS, 2)
     k_attend_slots(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const SlotParams p)
 {
-    using Cfg = SlotCfg<D>;
+    using Cfg = SlotCfg<D, LSM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES);
+    float *lsm = reinterpret_cast<float *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES);  // LSM only
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES +
+                                                  Cfg::LSM_BYTES);
     uint64_t *empty = full + Cfg::NSTAGE;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -155,7 +161,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
     const int h0 = 2 * c, h1 = 2 * c + 1;
     float *lg0 = nullptr, *lg1 = nullptr;
-    if (p.logits) {
+    if (LSM) {
+        lg0 = h0 < p.g ? lsm + h0 * LSM_SLOTS : nullptr;
+        lg1 = h1 < p.g ? lsm + h1 * LSM_SLOTS : nullptr;
+    } else if (p.logits) {
         const size_t rowbase = ((size_t)b * p.Hq + hk * p.g) * p.C;
         lg0 = h0 < p.g ? p.logits + rowbase + (size_t)h0 * p.C : nullptr;
         lg1 = h1 < p.g ? p.logits + rowbase + (size_t)h1 * p.C : nullptr;
@@ -312,7 +321,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             s_lse2[h] = ls > 0.f ? ms + __log2f(ls) : INFINITY;
         }
         consumer_bar();
-        const float *lrow = p.logits + ((size_t)b * p.Hq + hk * p.g) * p.C;
+        const float *lrow = LSM ? lsm : p.logits + ((size_t)b * p.Hq + hk * p.g) * p.C;
+        const size_t lstride = LSM ? LSM_SLOTS : p.C;
         float *sc = p.h2o_scores + (size_t)unit * p.C;
         // four slots per thread per round, every load issued before any is used
         constexpr int U = 4;
@@ -324,17 +334,21 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 add[u] = 0.f;
                 old[u] = j < t_end ? sc[j] : 0.f;
             }
-            for (int h = 0; h < p.g; ++h) {
-                float lg[U];
+            // all heads' logits of the round in flight at once (g <= 8)
+            float lg[8][U];
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int j = j0 + u * NCW * 32;
-                    lg[u] = j < t_end ? lrow[(size_t)h * p.C + j] : 0.f;
+                    lg[h][u] = h < p.g && j < t_end ? lrow[(size_t)h * lstride + j] : 0.f;
                 }
 #pragma unroll
-                for (int u = 0; u < U; ++u)
-                    add[u] += ex2(fmaf(lg[u], LOG2E, -s_lse2[h]));
-            }
+            for (int h = 0; h < 8; ++h)
+                if (h < p.g)
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        add[u] += ex2(fmaf(lg[h][u], LOG2E, -s_lse2[h]));
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int j = j0 + u * NCW * 32;
@@ -374,22 +388,22 @@ __global__ void k_combine(int Hq, int Hkv, int g, int D, int splits, const float
         lse[bh] = ls > 0.f ? (ms + __log2f(ls)) * LN2 : -INFINITY;
 }
 
-template <int D>
+template <int D, bool LSM>
 cudaError_t launch_slots_impl(const CUtensorMap &tk, const CUtensorMap &tv, const SlotParams &sp,
                               int grid, cudaStream_t s)
 {
-    using Cfg = SlotCfg<D>;
+    using Cfg = SlotCfg<D, LSM>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_attend_slots<D>,
+        cudaError_t e = cudaFuncSetAttribute(k_attend_slots<D, LSM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
         if (e != cudaSuccess)
             return e;
         configured_device = dev;
     }
-    k_attend_slots<D><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
+    k_attend_slots<D, LSM><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
     return cudaGetLastError();
 }
 
@@ -426,8 +440,15 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
     sp.rows = SlotRows{a.block_table, a.C, a.num_pages};
     sp.status = dev_status_ptr();
     const int grid = units * a.splits;
-    cudaError_t e = a.D == 128 ? launch_slots_impl<128>(tk, tv, sp, grid, s)
-                               : launch_slots_impl<64>(tk, tv, sp, grid, s);
+    // fused H2O without a logits array: the logits stay in shared memory (one split,
+    // C <= LSM_SLOTS, checked by the caller)
+    const bool lsm = a.h2o_scores && !a.logits;
+    if (lsm && (a.splits != 1 || a.C > LSM_SLOTS))
+        return cudaErrorInvalidValue;
+    cudaError_t e = a.D == 128 ? (lsm ? launch_slots_impl<128, true>(tk, tv, sp, grid, s)
+                                      : launch_slots_impl<128, false>(tk, tv, sp, grid, s))
+                               : (lsm ? launch_slots_impl<64, true>(tk, tv, sp, grid, s)
+                                      : launch_slots_impl<64, false>(tk, tv, sp, grid, s));
     if (e != cudaSuccess || a.splits == 1)
         return e;
     return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);

@@ -11,6 +11,7 @@
 namespace kvc {
 
 constexpr int TILE = 64;           // tokens per pipeline stage of the decode kernels
+constexpr int H2O_ONCHIP_MAX_SLOTS = KVC_H2O_ONCHIP_MAX_SLOTS;   // fused H2O, logits on chip
 constexpr int KIVI_G = KVC_KIVI_GROUP;
 
 // Device status word of the current device (set-up once per device).

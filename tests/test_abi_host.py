@@ -77,6 +77,21 @@ def test_null_arguments_are_rejected_without_touching_a_gpu(kvc):
         a.logits = a.lse = a.h2o_scores = 16
         a.h2o_decay = bad
         assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_INVALID_ARG, bad
+    # fused H2O with the logits on chip: one split only, and C within the on-chip bound
+    a = kvc.AttendArgs()
+    a.kind, a.Hq, a.q, a.o, a.slots = kvc.KVC_KIND_SLOTS, 1, 16, 16, ctypes.pointer(d)
+    a.lse = a.h2o_scores = 16
+    a.num_splits = 2
+    assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_INVALID_ARG
+    a.h2o_scores = 0
+    a.lse = 0
+    a.num_splits = 1
+    big = kvc.SlotCacheDesc(1, 1, 128, kvc.H2O_ONCHIP_MAX_SLOTS + 64, 16, 16, 16, 16, 16)
+    a.slots = ctypes.pointer(big)
+    a.lse = a.h2o_scores = 16
+    assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_UNSUPPORTED
+    a.logits = 16                    # with a logits array any capacity is fine for the checks
+    assert lib.kvc_workspace_size(ctypes.byref(a)) == 0
 
 
 def test_product_path_does_not_import_the_oracle():

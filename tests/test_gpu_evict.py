@@ -133,17 +133,18 @@ def test_h2o_prefill_scores_and_evict(kvc, orc, B, Hq, Hkv, L, D, n_heavy, n_rec
     assert device_status_clean(kvc)
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,D,fused,splits,decay", [(4, 64, 8, 128, False, 0, 0.0),
-                                                           (3, 8, 8, 64, False, 0, 0.0),
-                                                           (4, 64, 8, 128, True, 1, 0.0),
-                                                           (3, 8, 8, 64, True, 3, 0.0),
-                                                           (4, 64, 8, 128, True, 1, 0.99),
-                                                           (3, 8, 8, 64, False, 0, 0.9),
-                                                           (3, 8, 8, 64, True, 3, 0.99)])
-def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, fused, splits, decay):
+@pytest.mark.parametrize("B,Hq,Hkv,D,mode,splits,decay", [
+    (4, 64, 8, 128, "separate", 0, 0.0), (3, 8, 8, 64, "separate", 0, 0.0),
+    (4, 64, 8, 128, "fused", 1, 0.0), (3, 8, 8, 64, "fused", 3, 0.0),
+    (4, 64, 8, 128, "fused", 1, 0.99), (3, 8, 8, 64, "separate", 0, 0.9),
+    (3, 8, 8, 64, "fused", 3, 0.99), (4, 64, 8, 128, "onchip", 0, 0.0),
+    (3, 8, 8, 64, "onchip", 1, 0.99), (2, 24, 8, 128, "onchip", 1, 0.0)])
+def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, mode, splits, decay):
     """One decode step from a seeded post-prefill state: 64 heavy slots from [0, 1600) plus the
     recent 448; append token 2048, attend over 513 slots, accumulate (plain, or the decayed
-    activity score with decay lambda), evict back to 512."""
+    activity score with decay lambda), evict back to 512.  Modes: attention then a separate
+    accumulate launch; the accumulate fused into the attention (logits written); fused with the
+    logits kept on chip (no logits array)."""
     T, n_heavy, n_recent = 2048, 64, 448
     g = torch.Generator().manual_seed(B * Hq)
     rng = np.random.default_rng(B * Hq)
@@ -175,9 +176,12 @@ def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, fused, splits, decay):
     lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
     ws = torch.empty(max(kvc.kvc_workspace_size(cache, q, splits) // 4, 1), dtype=torch.float32,
                      device="cuda")
-    if fused:   # probabilities added to the scores by the attention launch itself
+    if mode == "fused":   # probabilities added to the scores by the attention launch itself
         kvc.kvc_decode_attend(cache, q.cuda(), o, logits=logits, lse=lse, workspace=ws,
                               num_splits=splits, h2o_scores=scores, h2o_decay=decay)
+    elif mode == "onchip":
+        kvc.kvc_decode_attend(cache, q.cuda(), o, lse=lse, workspace=ws, num_splits=splits,
+                              h2o_scores=scores, h2o_decay=decay)
     else:
         kvc.kvc_decode_attend(cache, q.cuda(), o, logits=logits, lse=lse, workspace=ws,
                               num_splits=splits)
@@ -205,6 +209,33 @@ def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, fused, splits, decay):
             _check_keep_with_ties(pos[b, hk, :512], pos513[b, hk], sc_ref[b, hk], T + 1, n_heavy,
                                   n_recent)
             _assert_content(cache, Kseq, Vseq, b, hk, pos[b, hk, :512])
+    assert device_status_clean(kvc)
+
+
+@pytest.mark.parametrize("D,C,n", [(128, 520, 513), (64, 1024, 1024), (128, 1024, 700)])
+def test_h2o_onchip_logits_match_written_logits(kvc, D, C, n):
+    """The fused H2O launch with the logits kept on chip gives bit-identical outputs, lse and
+    scores to the same launch writing a logits array (same arithmetic, other storage), up to
+    the on-chip capacity bound."""
+    B, Hq, Hkv = 3, 64, 8
+    g = torch.Generator().manual_seed(C + n)
+    K = torch.randn(B, Hkv, n, D, generator=g).half()
+    V = torch.randn(B, Hkv, n, D, generator=g).half()
+    q = torch.randn(B, Hq, D, generator=g).half().cuda()
+    cache = slot_cache_from(kvc, K, V, np.full((B, Hkv), n), C)
+    base = torch.rand(B, Hkv, C, generator=g).cuda()
+    outs = []
+    for onchip in (False, True):
+        o = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+        lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+        sc = base.clone()
+        logits = None if onchip else torch.empty(B, Hq, C, dtype=torch.float32, device="cuda")
+        kvc.kvc_decode_attend(cache, q, o, logits=logits, lse=lse, num_splits=1,
+                              h2o_scores=sc, h2o_decay=0.99)
+        torch.cuda.synchronize()
+        outs.append((o, lse, sc))
+    for a, b_ in zip(*outs):
+        assert torch.equal(a, b_)
     assert device_status_clean(kvc)
 
 
