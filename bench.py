@@ -319,6 +319,14 @@ def run_gpu(args, rank, world):
     for kd in kernels.values():
         kd["gbs"] = kd["bytes_per_step"] / (kd["ms_per_step"] * 1e-3) / 1e9
         kd["frac_of_hbm"] = kd["gbs"] / hbm_peak
+
+    def spread(nm):
+        v = sorted(per_call[nm])
+        q = lambda f: v[min(len(v) - 1, int(f * (len(v) - 1) + 0.5))]
+        return {"ms_median": statistics.median(v), "ms_p10": q(0.1), "ms_p90": q(0.9)}
+    for key, nm in (("attend_fp16", "fp16_attend"), ("attend_h2o512", "h2o_attend_accumulate"),
+                    ("attend_stream512", "stream_attend"), ("attend_kivi4", "kivi4_attend")):
+        kernels[key].update(spread(nm))
     methods = {
         "fp16": ms("fp16_append") + ms("fp16_attend"),
         "h2o512": ms("h2o_append") + ms("h2o_attend_accumulate") + ms("h2o_evict"),

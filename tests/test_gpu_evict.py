@@ -212,6 +212,84 @@ def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, mode, splits, decay):
     assert device_status_clean(kvc)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,D,L,n_heavy,n_recent,steps,onchip,decay", [
+    (1, 4, 4, 64, 64, 8, 8, 32, True, 0.0),          # the tiny workload's H2O 8+8
+    (2, 16, 2, 128, 300, 32, 64, 40, False, 0.0),
+    (2, 8, 1, 128, 200, 16, 48, 40, True, 0.99)])
+def test_h2o_free_running_decode(kvc, orc, B, Hq, Hkv, D, L, n_heavy, n_recent, steps, onchip,
+                                 decay):
+    """GPU and oracle run the whole H2O life independently from the same seeded inputs: prompt
+    score pass, eviction to the budget, then `steps` decode steps of append -> attention with
+    the fused score update -> eviction.  Every step's outputs, keep-sets and scores agree; a
+    swap between near-tied candidates (accepted) ends the comparison, since the two runs then
+    hold different caches."""
+    g = torch.Generator().manual_seed(L + steps + Hq)
+    T1 = L + steps
+    C = L + 4
+    budget = n_heavy + n_recent
+    Qp = torch.randn(B, Hq, L, D, generator=g).half()
+    Kseq = torch.randn(B, Hkv, T1, D, generator=g).half()
+    Vseq = torch.randn(B, Hkv, T1, D, generator=g).half()
+    qs = torch.randn(steps, B, Hq, D, generator=g).half()
+    # ---- GPU
+    cache = slot_cache_from(kvc, Kseq[:, :, :L], Vseq[:, :, :L], np.full((B, Hkv), L), C,
+                            seqlen=[L] * B)
+    scores = torch.zeros(B, Hkv, C, dtype=torch.float32, device="cuda")
+    ws = torch.empty(kvc.kvc_h2o_workspace_size(B, Hq, L) // 4, dtype=torch.float32, device="cuda")
+    kvc.kvc_h2o_accumulate_prefill(Qp.cuda(), cache.K, scores, ws, L)
+    kvc.kvc_h2o_evict(cache, scores, n_heavy, n_recent)
+    # ---- oracle state per unit: positions and scores of the kept slots
+    ref_sc = orc.h2o_prefill_scores(np16(Qp), np16(Kseq[:, :, :L]), L, threads=4)
+    st_pos, st_sc = {}, {}
+    for b in range(B):
+        for hk in range(Hkv):
+            pos = np.arange(L, dtype=np.int32)
+            keep, _ = orc.h2o_keep(pos, ref_sc[b, hk], L, n_heavy, n_recent)
+            st_pos[b, hk], st_sc[b, hk] = pos[keep], ref_sc[b, hk][keep]
+    K16, V16 = np16(Kseq), np16(Vseq)
+    o = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    logits = None if onchip else torch.empty(B, Hq, C, dtype=torch.float32, device="cuda")
+    gq = Hq // Hkv
+    for s_ in range(steps):
+        T = L + s_
+        kvc.kvc_append(cache, Kseq[:, :, T:T + 1].cuda().contiguous(),
+                       Vseq[:, :, T:T + 1].cuda().contiguous())
+        kvc.kvc_decode_attend(cache, qs[s_].cuda(), o, logits=logits, lse=lse, num_splits=1,
+                              h2o_scores=scores, h2o_decay=decay)
+        kvc.kvc_h2o_evict(cache, scores, n_heavy, n_recent)
+        torch.cuda.synchronize()
+        n, pos_g, _, _ = _units(cache)
+        sc_g = scores.cpu().numpy()
+        diverged = False
+        for b in range(B):
+            for hk in range(Hkv):
+                pos = np.concatenate([st_pos[b, hk], [T]]).astype(np.int32)
+                sc = np.concatenate([st_sc[b, hk], [0.0]])
+                q_u = np16(qs[s_, b, hk * gq:(hk + 1) * gq])[None]
+                o_r, lse_r, lg_r = orc.decode_attend(q_u, K16[b, hk][pos][None, None],
+                                                     V16[b, hk][pos][None, None],
+                                                     np.array([[pos.size]]), want_logits=True)
+                assert_o_close(np16(o[b, hk * gq:(hk + 1) * gq]), o_r[0], what=f"step {s_}")
+                sc = orc.h2o_accumulate(sc[None, None], lg_r, lse_r, np.array([[pos.size]]),
+                                        decay=float(np.float32(decay)))[0, 0]
+                keep, _ = orc.h2o_keep(pos, sc, T + 1, n_heavy, n_recent)
+                got = pos_g[b, hk, :n[b, hk]]
+                assert n[b, hk] == budget
+                if _check_keep_with_ties(got, pos, sc, T + 1, n_heavy, n_recent):
+                    diverged = True
+                else:
+                    order = np.argsort(got)
+                    want = dict(zip(pos.tolist(), sc.tolist()))
+                    np.testing.assert_allclose(sc_g[b, hk, :n[b, hk]][order],
+                                               [want[int(p)] for p in got[order]],
+                                               rtol=SCORE_REL_TOL)
+                st_pos[b, hk], st_sc[b, hk] = pos[keep], sc[keep]
+        if diverged:
+            break
+    assert device_status_clean(kvc)
+
+
 @pytest.mark.parametrize("D,C,n", [(128, 520, 513), (64, 1024, 1024), (128, 1024, 700)])
 def test_h2o_onchip_logits_match_written_logits(kvc, D, C, n):
     """The fused H2O launch with the logits kept on chip gives bit-identical outputs, lse and
