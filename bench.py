@@ -134,7 +134,7 @@ def run_gpu(args, rank, world):
     w = W.HEAVY
     B, Hq, Hkv, D, T0 = w.B, w.Hq, w.Hkv, w.D, w.T
     # warm-up steps, the graph-timed steps, then as many again with per-call events
-    S_total = args.warmup + 2 * args.steps
+    S_total = args.warmup + 3 * args.steps
     g = Hq // Hkv
     n_heavy, n_recent, n_sink = w.n_heavy, w.n_recent, w.n_sink
     rows = {}
@@ -253,6 +253,34 @@ def run_gpu(args, rank, world):
         kvc.kvc_decode_attend(st, qs[i, 3], outs[3], workspace=ws_st, stream=stream); mark(10)
         kvc.kvc_stream_evict(st, n_sink, n_recent, stream=stream); mark(11)
 
+    branches = [torch.cuda.Stream(dev) for _ in range(4)]
+
+    def step_par(i, outs_override=None):
+        """One decode step of the four methods, each on its own stream, forked from and joined
+        back into the launch stream (the methods share no data; each method's launches stay in
+        order on its stream)."""
+        outs = outs_base if outs_override is None else outs_override
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for bs in branches:
+            bs.wait_event(fork)
+        s0, s1, s2, s3 = branches
+        kvc.kvc_append(fp, kn[i, 0], vn[i, 0], stream=s0)
+        kvc.kvc_decode_attend(fp, qs[i, 0], outs[0], workspace=ws_fp, stream=s0)
+        kvc.kvc_append(h2o, kn[i, 1], vn[i, 1], stream=s1)
+        kvc.kvc_decode_attend(h2o, qs[i, 1], outs[1], lse=lse, workspace=ws_h2o,
+                              h2o_scores=h2o_scores, stream=s1)
+        kvc.kvc_h2o_evict(h2o, h2o_scores, n_heavy, n_recent, stream=s1)
+        kvc.kvc_append_quant(kv4, kn[i, 2], vn[i, 2], stream=s2)
+        kvc.kvc_decode_attend(kv4, qs[i, 2], outs[2], workspace=ws_kv, stream=s2)
+        kvc.kvc_append(st, kn[i, 3], vn[i, 3], stream=s3)
+        kvc.kvc_decode_attend(st, qs[i, 3], outs[3], workspace=ws_st, stream=s3)
+        kvc.kvc_stream_evict(st, n_sink, n_recent, stream=s3)
+        for bs in branches:
+            join = torch.cuda.Event()
+            join.record(bs)
+            stream.wait_event(join)
+
     def barrier():
         if world > 1:
             import torch.distributed as dist
@@ -260,17 +288,23 @@ def run_gpu(args, rank, world):
 
     # ---------------- device-resident timing
     # The K timed steps are captured once into a CUDA graph (every launch of all four
-    # methods, in order) and the graph is launched once inside the timed region, so the
-    # step time carries no host launch gaps.  A second run of K fresh steps, launched
-    # eagerly with an event between calls, gives the per-kernel breakdown.
+    # methods; each step forks the methods onto four streams and joins them) and the graph
+    # is launched once inside the timed region, so the step time carries no host launch
+    # gaps.  K more steps captured with the methods one after another on the launch stream
+    # give the serial step time, and K fresh steps launched eagerly with an event between
+    # calls give the per-kernel breakdown.
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            step(i)
+            step_par(i)
         torch.cuda.synchronize(dev)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for k in range(args.steps):
-                step(args.warmup + k)
+                step_par(args.warmup + k)
+        graph_ser = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ser, stream=stream):
+            for k in range(args.steps):
+                step(args.warmup + args.steps + k)
         torch.cuda.synchronize(dev)
         barrier()
         torch.cuda.synchronize(dev)
@@ -283,12 +317,19 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize(dev)
         clocks = clk.stop()
         barrier()
+        s_start, s_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_start.record(stream)
+        graph_ser.replay()
+        s_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(args.steps)]
         for k in range(args.steps):
-            step(args.warmup + args.steps + k, ev=evs[k])
+            step(args.warmup + 2 * args.steps + k, ev=evs[k])
         torch.cuda.synchronize(dev)
-        del graph
+        del graph, graph_ser
     total_ms = t_start.elapsed_time(t_end)
+    serial_ms = s_start.elapsed_time(s_end)
     per_call = {nm: [] for nm in names}
     for k in range(args.steps):
         for j, nm in enumerate(names):
@@ -297,7 +338,7 @@ def run_gpu(args, rank, world):
 
     # algorithmic bytes per step of each attention launch (sizes of the timed steps)
     hbm_peak, peak_kind = _peaks()
-    steps_T = [T0 + args.warmup + args.steps + k for k in range(args.steps)]   # tokens attended (FP16)
+    steps_T = [T0 + args.warmup + 2 * args.steps + k for k in range(args.steps)]   # FP16 tokens attended
     b_fp = [slot_bytes(t, B, Hkv, Hq, D) for t in steps_T]
     b_h2o = slot_bytes(513, B, Hkv, Hq, D)
     b_st = slot_bytes(513, B, Hkv, Hq, D)
@@ -387,7 +428,7 @@ def run_gpu(args, rank, world):
             if k >= 2:
                 stream.wait_event(ev_free[k - 2])   # that output buffer has been read back
             step_outs = o_buf
-            step(base + k, outs_override=step_outs)
+            step_par(base + k, outs_override=step_outs)
             ev_done[k].record(stream)
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(ev_done[k])
@@ -414,7 +455,8 @@ def run_gpu(args, rank, world):
     fp16_traffic = SLOT_ATTEND_DRAM_BYTES_PER_UNIT_TOKEN * B * Hkv * t_avg
     res = {
         "fp16_traffic": fp16_traffic,
-        "ms_per_step": ms_per_step, "eager_ms_per_step": eager_ms, "e2e_ms_per_step": e2e_ms,
+        "ms_per_step": ms_per_step, "serial_ms_per_step": serial_ms / args.steps,
+        "eager_ms_per_step": eager_ms, "e2e_ms_per_step": e2e_ms,
         "calls_ms": calls,
         "kernels": kernels, "methods": methods, "rows": rows, "clocks": clocks,
         "device_status": status, "tokens_per_step": 4 * B,
@@ -1030,7 +1072,9 @@ def main():
                        "methods": ["fp16", "h2o512", "kivi4", "stream512"],
                        "kv_len": "2048 + step index (each step appends one token)",
                        "l2": "inputs larger than L2 (8 GB of cache read per step)",
-                       "launch": "the timed steps captured in one CUDA graph, launched once"},
+                       "launch": "the timed steps captured in one CUDA graph, launched once; "
+                                 "each step runs the four methods on four streams (fork/join "
+                                 "per step)"},
             "e2e": {"value": world * res["tokens_per_step"] / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
@@ -1043,6 +1087,7 @@ def main():
             "clocks": res["clocks"],
             "kernels": res["kernels"], "methods": res["methods"], "rows": res["rows"],
             "calls_ms": res["calls_ms"], "eager_ms_per_step": res["eager_ms_per_step"],
+            "serial_ms_per_step": res["serial_ms_per_step"],
             "device_status": res["device_status"],
         }
         print(json.dumps(line))
