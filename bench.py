@@ -41,6 +41,16 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _tensor_peak():
+    """(dense 16-bit tensor TFLOP/s for a kernel timed alone, max SM MHz): measured, else the
+    fallback figures."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), float(d.get("sm_max_mhz", 2070.0))
+    return 1900.0, 2070.0
+
+
 # ------------------------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -163,8 +173,19 @@ def run_gpu(args, rank, world):
             pre_ms.append(ev0.elapsed_time(ev1))
         L = T0 - 1
         flops = 2 * 2 * B * Hq * (L * (L + 1) // 2) * D
+        # two bounds: the tensor cores (QK^T twice) and the SFU (one exp2 per causal score in
+        # each pass), which issues 32 exp2 per clock per SM on this GPU (a throughput loop of
+        # independent ex2.approx chains sustains ~30 at 2.07 GHz)
+        exps = 2 * B * Hq * (L * (L + 1) // 2)
+        tensor_tflops, sm_mhz = _tensor_peak()
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        t_tensor = flops / (tensor_tflops * 1e12) * 1e3
+        t_sfu = exps / (n_sm * 32 * sm_mhz * 1e6) * 1e3
         rows["h2o_prefill_score_pass"] = {
             "ms": min(pre_ms), "tflops": flops / (min(pre_ms) * 1e-3) / 1e12,
+            "frac_of_tensor_peak": t_tensor / min(pre_ms), "exp2": exps,
+            "sfu_bound_ms": t_sfu, "tensor_bound_ms": t_tensor,
+            "frac_of_bound": max(t_sfu, t_tensor) / min(pre_ms),
             "shape": f"Qp[{B},{Hq},{L},{D}] x Kp[{B},{Hkv},{L},{D}], causal, two passes"}
         del Qp, ws_pre
         Ch = 520
