@@ -1062,10 +1062,13 @@ def main():
         orc.build()
         threads = cpu_cores()
         dt, tk = oracle_sample(args.cpu_seqs, threads)
+        dt1, tk1 = oracle_sample(2, 1)   # the same work per sequence on one core
         cpu = {"value": tk / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "value_1_core": tk1 / dt1,
                "sample": f"{args.cpu_seqs} sequences x 8 KV heads of the heavy-load workload, one "
                          f"decode step of FP16, StreamingLLM-512, H2O-512 and KIVI-4 "
-                         f"({dt:.1f} s of fp64 oracle work)"}
+                         f"({dt:.1f} s of fp64 oracle work); value_1_core: 2 sequences on one "
+                         f"thread ({dt1:.1f} s)"}
 
     if world > 1:
         import torch
