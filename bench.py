@@ -1022,6 +1022,23 @@ def run_grid(args):
             torch.cuda.empty_cache()
 
 
+def max_over_ranks(values, world: int, device):
+    """Per-rank timings reduced with MAX over all ranks (every rank gets the result)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world: int, tokens_per_step_per_rank: int, ms_per_step: float) -> float:
+    """Tokens/s of the whole job: every rank processes its own batch (weak scaling) and the
+    step time is the slowest rank's."""
+    return world * tokens_per_step_per_rank / (ms_per_step * 1e-3)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1076,18 +1093,12 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
     res = run_gpu(args, rank, world)
-    ms = res["ms_per_step"]
-    e2e_ms = res["e2e_ms_per_step"]
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = t.tolist()
+    ms, e2e_ms = max_over_ranks([res["ms_per_step"], res["e2e_ms_per_step"]], world, "cuda")
     if rank == 0:
         dom = res["kernels"]["attend_fp16"]
         line = {
-            "metric": METRIC, "value": world * res["tokens_per_step"] / (ms * 1e-3), "unit": UNIT,
+            "metric": METRIC, "value": whole_job_rate(world, res["tokens_per_step"], ms),
+            "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic",
@@ -1099,7 +1110,7 @@ def main():
                        "launch": "the timed steps captured in one CUDA graph, launched once; "
                                  "each step runs the four methods on four streams (fork/join "
                                  "per step)"},
-            "e2e": {"value": world * res["tokens_per_step"] / (e2e_ms * 1e-3), "unit": UNIT,
+            "e2e": {"value": whole_job_rate(world, res["tokens_per_step"], e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
             "roofline": {"bound": "hbm", "kernel": "k_attend_slots (FP16 cache launch)",
