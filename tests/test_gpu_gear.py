@@ -113,6 +113,28 @@ def test_gear_pack_ties(kvc, orc):
     assert device_status_clean(kvc)
 
 
+def test_gear_ragged_edge_lengths(kvc, orc):
+    """GEAR at the edges of the flush rule (empty, one token, R, R + 31, R + 32, R + 33,
+    R + 100), one batch, on groups whose values sit on the 4-bit grid: every residual is 0, so
+    the corrections vanish and the attention must equal KIVI's (the C oracle's)."""
+    from test_gpu_kivi import _check_ragged, _ragged_quant_cache
+    D, Hq, Hkv, R, bits = 128, 8, 2, 64, 4
+    lens = [0, 1, R, R + 31, R + 32, R + 33, R + 100]
+    T = max(lens)
+    rng = np.random.default_rng(31)
+    td = (np.arange(T)[:, None] + np.arange(D)[None, :]) % 32
+    def grid(nb):
+        c = rng.integers(0, 16, (nb, Hkv, T, D))
+        c[..., td == 0], c[..., td == 1] = 0, 15
+        return torch.from_numpy((-1.0 + c / 16.0).astype(np.float16))
+    K, V = grid(len(lens)), grid(len(lens))
+    q = torch.from_numpy(rng.standard_normal((len(lens), Hq, D))).half()
+    cache = _ragged_quant_cache(kvc, K, V, lens, bits, R, 128, gear=True)
+    o, lse = _attend(kvc, cache, q.cuda())
+    _check_ragged(orc, q, K, V, lens, R, bits, o, lse)
+    assert device_status_clean(kvc)
+
+
 # ------------------------------------------------------------------ decode attention
 # Logits carry the KIVI path's binary16 rounding of q * s (see test_gpu_kivi.py) plus the
 # rank-2 factors' difference between the GPU's subspace iteration and the oracle's SVD.

@@ -230,3 +230,56 @@ def test_pack_bit_exact_crafted(kvc, orc, bits, kind):
             assert np.array_equal(cache.k_blocks[b, hk].cpu().numpy(), kb), (b, hk)
             assert np.array_equal(cache.v_blocks[b, hk].cpu().numpy(), vb), (b, hk)
     assert device_status_clean(kvc)
+
+
+def _ragged_quant_cache(kvc, K, V, lens, bits, R, Cq, gear=False):
+    """A KIVI (or GEAR) cache whose sequence b holds the first lens[b] tokens of K/V
+    [B, Hkv, T, D] (host), each appended through a one-sequence view of the batch."""
+    B = K.shape[0]
+    cache = kvc.QuantCache.empty(B, K.shape[1], Cq, K.shape[3], bits, R, gear=gear)
+    for b in range(B):
+        if lens[b] == 0:
+            continue
+        view = kvc.QuantCache(k_blocks=cache.k_blocks[b:b + 1], v_blocks=cache.v_blocks[b:b + 1],
+                              k_res=cache.k_res[b:b + 1], v_res=cache.v_res[b:b + 1],
+                              len=cache.len[b:b + 1], bits=bits, R=R,
+                              k_gear=cache.k_gear[b:b + 1] if gear else None,
+                              v_gear=cache.v_gear[b:b + 1] if gear else None)
+        kvc.kvc_append_quant(view, K[b:b + 1, :, :lens[b]].cuda().contiguous(),
+                             V[b:b + 1, :, :lens[b]].cuda().contiguous())
+    torch.cuda.synchronize()
+    assert cache.len.cpu().tolist() == list(lens)
+    return cache
+
+
+def _check_ragged(orc, q, K, V, lens, R, bits, o, lse):
+    gq = q.shape[1] // K.shape[1]
+    for b, T in enumerate(lens):
+        for hk in range(K.shape[1]):
+            og = np16(o[b, hk * gq:(hk + 1) * gq])
+            lg = lse[b, hk * gq:(hk + 1) * gq].cpu().numpy()
+            if T == 0:   # an empty softmax: no mass
+                assert not og.astype(np.float64).any() and np.isneginf(lg).all()
+                continue
+            ref, ref_lse = orc.kivi_attend_unit(np16(q[b, hk * gq:(hk + 1) * gq]),
+                                                np16(K[b, hk]), np16(V[b, hk]), T, R, bits)
+            assert_o_close(og, ref, what=f"T={T} hk={hk}")
+            np.testing.assert_allclose(lg, ref_lse, atol=KIVI_LSE_TOL, rtol=0)
+
+
+@pytest.mark.parametrize("bits,splits", [(4, 0), (2, 0), (4, 3)])
+def test_ragged_edge_lengths(kvc, orc, bits, splits):
+    """One batch whose sequences sit at the edges of the flush rule: empty, a single token,
+    R - 1, R (ring full, nothing quantised), R + 31 (one short of a flush), R + 32 (first
+    group), R + 33 and R + 100."""
+    D, Hq, Hkv, R = 128, 8, 2, 64
+    lens = [0, 1, R - 1, R, R + 31, R + 32, R + 33, R + 100]
+    g = torch.Generator().manual_seed(bits + 10 * splits)
+    T = max(lens)
+    K = (torch.randn(len(lens), Hkv, T, D, generator=g) * 2).half()
+    V = torch.randn(len(lens), Hkv, T, D, generator=g).half()
+    q = torch.randn(len(lens), Hq, D, generator=g).half()
+    cache = _ragged_quant_cache(kvc, K, V, lens, bits, R, 128)
+    o, lse = _attend(kvc, cache, q.cuda(), splits)
+    _check_ragged(orc, q, K, V, lens, R, bits, o, lse)
+    assert device_status_clean(kvc)
