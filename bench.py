@@ -469,6 +469,7 @@ def run_gpu(args, rank, world):
     rows.update(paged_rows(kvc, dev, stream, fp, kv4, qs[0, 0], T0))
     rows.update(gear_rows(kvc, dev, stream, gear4, qs[:, 2], kn[:, 2], vn[:, 2], hbm_peak))
     del gear4
+    rows.update(config_rows(kvc, W, dev, stream, hbm_peak))
 
     ms_per_step = total_ms / args.steps
     eager_ms = evs[0][0].elapsed_time(evs[-1][11]) / args.steps
@@ -603,6 +604,84 @@ def gear_rows(kvc, dev, stream, gear4, qs, kn, vn, hbm_peak):
             "attend_bytes": sum(nbytes) / len(nbytes), "steps": steps - 1,
             "shape": f"B={B} GQA {Hq}/{Hkv} D={D}, T={lens[1]}..{lens[-1]}, R={R}, "
                      f"side block {side} B per group and side"}
+    return out
+
+
+def config_rows(kvc, W, dev, stream, hbm_peak):
+    """Decode attention on the two MHA workloads (median of 5 after one warm-up, L2 flushed by a
+    512 MB write before each, as their compressed caches fit in L2): llama7b-b8-h32-d128-t2048
+    (FP16 over T+1 slots; H2O-512 and StreamingLLM-512 over 513 slots) and
+    kivi-b32-h32-d128-t4096 (FP16, KIVI-4 and KIVI-2 over T tokens)."""
+    import torch
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+
+    def timed(fn):
+        ts = []
+        for r in range(6):
+            flush.add_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if r > 0:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    with torch.cuda.stream(stream):
+        # ---- llama7b-b8-h32-d128-t2048: 32 MHA heads, 2% outlier channels in K and V
+        w = W.LLAMA7B
+        B, Hq, Hkv, D, T = w.B, w.Hq, w.Hkv, w.D, w.T
+        K, V = W.kv_tensors(w, T=T + 1, device=dev)
+        q = W.q_tensor(w, device=dev)
+        o = torch.empty_like(q)
+        for name, n in (("fp16", T + 1), ("h2o512", 513), ("stream512", 513)):
+            c = kvc.SlotCache.empty(B, Hkv, n + 7, D, device=dev)
+            kvc.kvc_append(c, K[:, :, :n].contiguous(), V[:, :, :n].contiguous(), stream=stream)
+            lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+            sc = torch.zeros(B, Hkv, c.C, dtype=torch.float32, device=dev)
+            ws = torch.empty(max(kvc.kvc_workspace_size(c, q) // 4, 1), dtype=torch.float32,
+                             device=dev)
+            if name == "h2o512":
+                fn = lambda: kvc.kvc_decode_attend(c, q, o, lse=lse, num_splits=1, h2o_scores=sc,
+                                                   stream=stream)
+            else:
+                fn = lambda: kvc.kvc_decode_attend(c, q, o, workspace=ws, stream=stream)
+            ms = timed(fn)
+            nb = slot_bytes(n, B, Hkv, Hq, D)
+            out[f"{w.name}/{name}"] = {"ms": ms, "slots": n, "gbs": nb / (ms * 1e-3) / 1e9,
+                                       "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm_peak,
+                                       "tokens_per_s": B / (ms * 1e-3)}
+            del c, sc, ws
+        del K, V
+        # ---- kivi-b32-h32-d128-t4096: offsets U(-2, 2) on Q, K, V
+        w = W.KIVI_MHA
+        B, Hq, Hkv, D, T = w.B, w.Hq, w.Hkv, w.D, w.T
+        K, V = W.kv_tensors(w, T=T, device=dev)
+        q = W.q_tensor(w, device=dev)
+        o = torch.empty_like(q)
+        c = kvc.SlotCache.empty(B, Hkv, T + 8, D, device=dev)
+        kvc.kvc_append(c, K, V, stream=stream)
+        ws = torch.empty(max(kvc.kvc_workspace_size(c, q) // 4, 1), dtype=torch.float32, device=dev)
+        ms = timed(lambda: kvc.kvc_decode_attend(c, q, o, workspace=ws, stream=stream))
+        nb = slot_bytes(T, B, Hkv, Hq, D)
+        out[f"{w.name}/fp16"] = {"ms": ms, "slots": T, "gbs": nb / (ms * 1e-3) / 1e9,
+                                 "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm_peak,
+                                 "tokens_per_s": B / (ms * 1e-3)}
+        del c, ws
+        for bits in (4, 2):
+            kq = kvc.QuantCache.empty(B, Hkv, T, D, bits, w.kivi_R, device=dev)
+            kvc.kvc_append_quant(kq, K, V, stream=stream)
+            ws = torch.empty(max(kvc.kvc_workspace_size(kq, q) // 4, 1), dtype=torch.float32,
+                             device=dev)
+            ms = timed(lambda: kvc.kvc_decode_attend(kq, q, o, workspace=ws, stream=stream))
+            nb = kivi_bytes(T, w.kivi_R, B, Hkv, Hq, D, bits)
+            out[f"{w.name}/kivi{bits}"] = {"ms": ms, "tokens": T, "gbs": nb / (ms * 1e-3) / 1e9,
+                                           "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm_peak,
+                                           "tokens_per_s": B / (ms * 1e-3)}
+            del kq, ws
+        del K, V, flush
     return out
 
 
