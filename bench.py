@@ -808,6 +808,20 @@ def random_rows(kvc, W, dev, stream):
 
 # ------------------------------------------------------------------------------------ CPU oracle
 
+def oracle_prefill_sample(n_seq: int, threads: int) -> float:
+    """Seconds the fp64 oracle takes for the H2O prefill score pass of n_seq sequences of the
+    heavy-load prompt (2047 tokens, all 8 KV heads)."""
+    import oracle as orc
+    from kv_cache_compression_split_gb300 import workloads as W
+    w = W.HEAVY
+    L = w.T - 1
+    Qp = W.q_tensor(w, B=n_seq, L=L).numpy()
+    Kp, _ = W.kv_tensors(w, T=L, B=n_seq)
+    t0 = time.perf_counter()
+    orc.h2o_prefill_scores(Qp, Kp.numpy(), L, threads=threads)
+    return time.perf_counter() - t0
+
+
 def oracle_sample(n_seq: int, threads: int):
     """Time the fp64 oracle on n_seq sequences (all 8 KV heads) of the heavy-load workload,
     one decode step of each method; returns (seconds, tokens produced = 4 * n_seq)."""
@@ -1159,8 +1173,13 @@ def main():
         threads = cpu_cores()
         dt, tk = oracle_sample(args.cpu_seqs, threads)
         dt1, tk1 = oracle_sample(2, 1)   # the same work per sequence on one core
+        dtp = oracle_prefill_sample(2, threads)
         cpu = {"value": tk / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
                "value_1_core": tk1 / dt1,
+               "prefill_s_extrapolated": dtp * 512 / 2,
+               "prefill_sample": "H2O prefill score pass of 2 sequences (2047-token prompt, "
+                                 f"8 KV heads) in {dtp:.1f} s on {threads} threads, scaled "
+                                 "linearly to the 512 sequences of the GPU row",
                "sample": f"{args.cpu_seqs} sequences x 8 KV heads of the heavy-load workload, one "
                          f"decode step of FP16, StreamingLLM-512, H2O-512 and KIVI-4 "
                          f"({dt:.1f} s of fp64 oracle work); value_1_core: 2 sequences on one "
