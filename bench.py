@@ -495,11 +495,20 @@ def run_gpu(args, rank, world):
 
     ms_per_step = total_ms / args.steps
     eager_ms = evs[0][0].elapsed_time(evs[-1][11]) / args.steps
+    # the whole timed step against the copy bandwidth: the four attention launches' bytes at
+    # the timed steps' own cache lengths
+    graph_T = [T0 + args.warmup + k for k in range(args.steps)]
+    step_bytes = (sum(slot_bytes(t, B, Hkv, Hq, D) + kivi_bytes(t, w.kivi_R, B, Hkv, Hq, D, 4)
+                      for t in graph_T) / args.steps + b_h2o + b_st)
+    step_roofline = {"bytes_per_step": step_bytes,
+                     "gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+                     "frac_of_hbm": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak}
     t_avg = sum(steps_T) / len(steps_T)
     fp16_traffic = SLOT_ATTEND_DRAM_BYTES_PER_UNIT_TOKEN * B * Hkv * t_avg
     res = {
         "fp16_traffic": fp16_traffic,
         "ms_per_step": ms_per_step, "serial_ms_per_step": serial_ms / args.steps,
+        "step_roofline": step_roofline,
         "eager_ms_per_step": eager_ms, "e2e_ms_per_step": e2e_ms,
         "calls_ms": calls,
         "kernels": kernels, "methods": methods, "rows": rows, "clocks": clocks,
@@ -1243,6 +1252,7 @@ def main():
             "kernels": res["kernels"], "methods": res["methods"], "rows": res["rows"],
             "calls_ms": res["calls_ms"], "eager_ms_per_step": res["eager_ms_per_step"],
             "serial_ms_per_step": res["serial_ms_per_step"],
+            "step_roofline": res["step_roofline"],
             "device_status": res["device_status"],
         }
         print(json.dumps(line))
