@@ -928,12 +928,16 @@ def run_profile(args):
     elif what == "attend_kivi4":
         cache = kvc.QuantCache.empty(B, Hkv, T, D, 4, w.kivi_R, device=dev)
         kvc.kvc_append_quant(cache, K, V)
+        del K, V   # the capture holds only what the attention reads
+        torch.cuda.empty_cache()
         ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), device=dev)
         for _ in range(3):
             kvc.kvc_decode_attend(cache, q, o, workspace=ws)
     elif what == "attend_gear4":
         cache = kvc.QuantCache.empty(B, Hkv, T, D, 4, w.kivi_R, device=dev, gear=True)
         kvc.kvc_append_quant(cache, K, V)
+        del K, V
+        torch.cuda.empty_cache()
         ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), device=dev)
         for _ in range(3):
             kvc.kvc_decode_attend(cache, q, o, workspace=ws)

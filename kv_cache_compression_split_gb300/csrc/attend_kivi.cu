@@ -195,6 +195,33 @@ __device__ __forceinline__ uint32_t rank2_b_operand(const float *f, int r, int c
     return c == 0 ? pack_half2((r & 1) ? x1 : x0, (r & 1) ? y1 : y0) : 0u;
 }
 
+// N consecutive 32-bit words of shared memory (aligned to the widest of 16, 8 or
+// 4 bytes that N allows) in as few loads as that alignment permits.
+template <int N> __device__ __forceinline__ void lds_words(const uint32_t *src, uint32_t (&dst)[N])
+{
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int e = 0; e < N / 4; ++e) {
+            const uint4 v = reinterpret_cast<const uint4 *>(src)[e];
+            dst[4 * e] = v.x;
+            dst[4 * e + 1] = v.y;
+            dst[4 * e + 2] = v.z;
+            dst[4 * e + 3] = v.w;
+        }
+    } else if constexpr (N % 2 == 0) {
+#pragma unroll
+        for (int e = 0; e < N / 2; ++e) {
+            const uint2 v = reinterpret_cast<const uint2 *>(src)[e];
+            dst[2 * e] = v.x;
+            dst[2 * e + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            dst[e] = src[e];
+    }
+}
+
 struct KiviItem {
     int unit, split, b, hk, T, n_groups, n_res, qt0, nq, nr;
 };
@@ -234,8 +261,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 {
     using Cfg = KiviCfg<D, BITS, GEAR>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_align1024(smem_raw);
     float *red = reinterpret_cast<float *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES);
     uint8_t *dtiles = smem + Cfg::NSTAGE * Cfg::STAGE_BYTES + Cfg::RED_BYTES;
     uint8_t *qstage = dtiles + Cfg::DT_BYTES;
@@ -519,7 +545,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 
             // ---- the bias beta_h = sum_d q_hd z_d of the K zeros.  GEAR: one MMA chain over
             // the plain query Q^T whose A rows 0, 1 hold B (U = B Q^T) and row 2 the zeros,
-            // with the sparse tile's S Q^T alongside.  KIVI: fp32 FMAs, reduced over c.
+            // with the sparse tile's S Q^T alongside.  KIVI: an MMA chain whose A rows 0-7
+            // all hold the zeros, so every result row is beta; the k order is permuted so
+            // that lane c's channels are the 32 it already holds (words 16c .. 16c + 15
+            // of both rows, k-step s taking words 2s and 2s + 1).
             float dk0[4] = {0.f, 0.f, 0.f, 0.f}, dk1[4] = {0.f, 0.f, 0.f, 0.f};
             float uf[4] = {0.f, 0.f, 0.f, 0.f};   // rows 0-2: U, beta (GEAR)
             float ug[4] = {0.f, 0.f, 0.f, 0.f};   // (odd k-steps: a second chain)
@@ -557,30 +586,30 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 bias0 = __shfl_sync(0xffffffffu, uf[0], 8 + c) * p.scale_log2;
                 bias1 = __shfl_sync(0xffffffffu, uf[1], 8 + c) * p.scale_log2;
             } else {
-                float beta = 0.f;
-                const uint32_t *zl = ksz + D / 2 + c * (D / 8);
+                const uint4 *zl = reinterpret_cast<const uint4 *>(ksz + D / 2 + c * (D / 8));
+                float bz0[4] = {0.f, 0.f, 0.f, 0.f}, bz1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int e = 0; e < D / 8; ++e) {
-                    const uint32_t zw = zl[e];
-                    const float2 zf = __half22float2(*reinterpret_cast<const __half2 *>(&zw));
-                    const float2 qf2 = __half22float2(*reinterpret_cast<const __half2 *>(&qh[e]));
-                    beta = fmaf(qf2.x, zf.x, beta);
-                    beta = fmaf(qf2.y, zf.y, beta);
+                for (int e = 0; e < D / 32; ++e) {
+                    const uint4 z4 = zl[e];
+                    mma16816(bz0, z4.x, 0u, z4.y, 0u, qh[4 * e], qh[4 * e + 1]);
+                    mma16816(bz1, z4.z, 0u, z4.w, 0u, qh[4 * e + 2], qh[4 * e + 3]);
                 }
-                beta += __shfl_xor_sync(0xffffffffu, beta, 1);
-                beta += __shfl_xor_sync(0xffffffffu, beta, 2);
-                // beta of head h sits in lanes 4h .. 4h + 3
-                bias0 = __shfl_sync(0xffffffffu, beta, 4 * h0) * p.scale_log2;
-                bias1 = __shfl_sync(0xffffffffu, beta, 4 * h1) * p.scale_log2;
+                bias0 = (bz0[0] + bz1[0]) * p.scale_log2;
+                bias1 = (bz0[1] + bz1[1]) * p.scale_log2;
             }
             // ---- q~ pairs (B operand)
             uint32_t qt[D / 8];
             {
-                const uint32_t *sl = ksz + c * (D / 8);
+                const uint4 *sl = reinterpret_cast<const uint4 *>(ksz + c * (D / 8));
                 uint32_t sw[D / 8];
 #pragma unroll
-                for (int e = 0; e < D / 8; ++e)
-                    sw[e] = sl[e];
+                for (int e = 0; e < D / 32; ++e) {
+                    const uint4 s4 = sl[e];
+                    sw[4 * e] = s4.x;
+                    sw[4 * e + 1] = s4.y;
+                    sw[4 * e + 2] = s4.z;
+                    sw[4 * e + 3] = s4.w;
+                }
 #pragma unroll
                 for (int pi = 0; pi < D / 8; ++pi) {
                     const int lo = Cfg::FPW * (pi / Cfg::HALF) + pi % Cfg::HALF;
@@ -598,13 +627,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             {
                 const uint32_t *kw = reinterpret_cast<const uint32_t *>(kblk);
                 uint32_t w0[Cfg::WPL], w1[Cfg::WPL], w2[Cfg::WPL], w3[Cfg::WPL];
-#pragma unroll
-                for (int k = 0; k < Cfg::WPL; ++k) {
-                    w0[k] = kw[(r)*Cfg::WK + c * Cfg::WPL + k];
-                    w1[k] = kw[(r + 8) * Cfg::WK + c * Cfg::WPL + k];
-                    w2[k] = kw[(r + 16) * Cfg::WK + c * Cfg::WPL + k];
-                    w3[k] = kw[(r + 24) * Cfg::WK + c * Cfg::WPL + k];
-                }
+                lds_words(kw + r * Cfg::WK + c * Cfg::WPL, w0);
+                lds_words(kw + (r + 8) * Cfg::WK + c * Cfg::WPL, w1);
+                lds_words(kw + (r + 16) * Cfg::WK + c * Cfg::WPL, w2);
+                lds_words(kw + (r + 24) * Cfg::WK + c * Cfg::WPL, w3);
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
                     const int pa = 2 * s, pb = 2 * s + 1;
@@ -682,11 +708,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 // stored rotated by twice the pair index
                 const int pc = 8 * rb + c, pd = pc + 4;
                 uint32_t wa[Cfg::W], wb[Cfg::W];
-#pragma unroll
-                for (int k = 0; k < Cfg::W; ++k) {
-                    wa[k] = vw[pc * 2 * Cfg::WK + ((r + 2 * pc) & 7) * Cfg::W + k];
-                    wb[k] = vw[pd * 2 * Cfg::WK + ((r + 2 * pd) & 7) * Cfg::W + k];
-                }
+                lds_words(vw + pc * 2 * Cfg::WK + ((r + 2 * pc) & 7) * Cfg::W, wa);
+                lds_words(vw + pd * 2 * Cfg::WK + ((r + 2 * pd) & 7) * Cfg::W, wb);
 #pragma unroll
                 for (int m = 0; m < D / 16; ++m) {
                     const int k = m / Cfg::MPW, jj = m % Cfg::MPW;

@@ -73,8 +73,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 {
     using Cfg = SlotCfg<D, LSM>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_align1024(smem_raw);
     float *lsm = reinterpret_cast<float *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES);  // LSM only
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES +
                                                   Cfg::LSM_BYTES);

@@ -228,8 +228,7 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
 {
     using Cfg = TcCfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_align1024(smem_raw);
     uint8_t *stat = smem;                                   // stationary tile
     uint8_t *ring = smem + Cfg::TILE_BYTES;                 // NS streaming tiles
     float *lse_buf = reinterpret_cast<float *>(smem + (1 + NS) * Cfg::TILE_BYTES);

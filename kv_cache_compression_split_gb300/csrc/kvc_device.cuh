@@ -22,6 +22,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-byte aligned byte at or after p, a pointer into a __shared__
+// array.  The offset is added to p itself, so the compiler still knows that
+// the result (and everything derived from it) is shared memory and emits
+// shared loads and stores; rounding the address as an integer would turn every
+// access through it into a generic one.
+__device__ __forceinline__ uint8_t *smem_align1024(uint8_t *p)
+{
+    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ unsigned long long globaltimer()
 {
     unsigned long long t;
