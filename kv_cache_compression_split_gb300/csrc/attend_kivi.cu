@@ -86,7 +86,12 @@ template <int D, int BITS, bool GEAR = false> struct KiviCfg {
     static constexpr int QCH = D / 32;                 // 16-byte chunks per lane
     static constexpr int QS_BUF = QCH * 32 * 16;
     static constexpr int QS_BYTES = GEAR ? 2 * QS_BUF : 0;
-    static constexpr int NSTAGE_PLAIN = (81920 / STAGE_BYTES) < 3 ? 3 : (81920 / STAGE_BYTES);
+    // CTAs per SM: three for KIVI (each within a third of the SM's 228 KB of shared
+    // memory, 1 KB of it reserved per CTA), two for GEAR
+    static constexpr int CTAS = GEAR ? 2 : 3;
+    static constexpr int NSTAGE_PLAIN =
+        GEAR ? ((81920 / STAGE_BYTES) < 3 ? 3 : (81920 / STAGE_BYTES))
+             : (233472 / 3 - 1024 - RED_BYTES - 1024 - 64) / STAGE_BYTES;
     // with the sparse tiles, as many stages as keep two CTAs resident per SM
     static constexpr int NSTAGE_FIT =
         (112640 - RED_BYTES - DT_BYTES - QS_BYTES - 1104) / STAGE_BYTES;
@@ -255,7 +260,7 @@ __device__ __forceinline__ KiviItem kivi_item(const KiviParams &p, int item)
 // Persistent CTAs: CTA k handles work items k, k + gridDim.x, ... (an item is one
 // (sequence, KV head, split)); one TMA pipeline runs across all of its items.
 template <int D, int BITS, bool GEAR>
-__global__ void __launch_bounds__(NTHREADS, 2)
+__global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
     k_attend_kivi(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const KiviParams p)
 {
