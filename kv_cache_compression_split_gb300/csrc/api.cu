@@ -94,7 +94,7 @@ bool encode_tmap_2d_f16(CUtensorMap *map, const void *base, uint64_t inner, uint
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested, int ctas_per_sm)
+SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested)
 {
     SlotAttendPlan pl{1, tiles_per_unit > 0 ? tiles_per_unit : 1};
     if (tiles_per_unit <= 0)
@@ -103,7 +103,7 @@ SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested, int cta
     if (requested > 0) {
         S = requested < tiles_per_unit ? requested : tiles_per_unit;
     } else {
-        const double slots = (double)ctas_per_sm * sm_count();
+        const double slots = 2.0 * sm_count();
         double best = 1e300;
         const int smax = tiles_per_unit < 64 ? tiles_per_unit : 64;
         for (int s = 1; s <= smax; ++s) {
@@ -204,7 +204,7 @@ AttendPlanFull plan_full(const kvc_attend_args *a)
             }
             splits = 1;
         }
-        f.plan = plan_attend(f.B * f.Hkv, tiles, splits, 2);   // two CTAs per SM
+        f.plan = plan_attend(f.B * f.Hkv, tiles, splits);
         f.ws = f.plan.splits > 1 ? (size_t)f.B * a->Hq * f.plan.splits * (f.D + 2) * sizeof(float)
                                  : 0;
     } else if (a->kind == KVC_KIND_KIVI) {
@@ -217,9 +217,7 @@ AttendPlanFull plan_full(const kvc_attend_args *a)
         f.D = a->quant->D;
         // quantised tiles of four groups; the residual ring joins the last split
         const int tiles = (a->quant->Cq / KIVI_G + 3) / 4;
-        // three persistent CTAs per SM for KIVI, two with the GEAR corrections
-        f.plan = plan_attend(f.B * f.Hkv, tiles > 0 ? tiles : 1, a->num_splits,
-                             a->quant->k_gear ? 2 : 3);
+        f.plan = plan_attend(f.B * f.Hkv, tiles > 0 ? tiles : 1, a->num_splits);
         f.ws = f.plan.splits > 1
                    ? (size_t)f.B * a->Hq * f.plan.splits * (f.D + 2) * sizeof(float)
                    : 0;

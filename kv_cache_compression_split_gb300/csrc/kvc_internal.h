@@ -30,7 +30,7 @@ struct SlotAttendPlan {
 };
 
 // Split plan shared by kvc_workspace_size and kvc_decode_attend.
-SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested_splits, int ctas_per_sm);
+SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested_splits);
 
 // ---- launchers (each returns a cudaError_t of the launch) ----
 
