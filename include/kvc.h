@@ -333,7 +333,9 @@ enum { KVC_H2O_DECODE = 0, KVC_H2O_PREFILL = 1 };
  *          rows i >= j, of softmax_i(scale * qp[b,h,i] . kp[b,hk,.])_j for
  *          j < L (causal prompt of L tokens); qp [B, Hq, L, D] fp16, kp the
  *          prompt keys [B, Hkv, kp_cap, D] fp16 with prompt token j in row j.
- *          Needs kvc_h2o_workspace_size bytes of workspace.
+ *          Needs kvc_h2o_workspace_size bytes of workspace (16-byte aligned):
+ *          -lse of every prompt row ([B * Hq, L rounded up to 128] fp32), then
+ *          16 bytes of work counters that the call zeroes on its stream.
  */
 typedef struct kvc_h2o_args {
     int mode;

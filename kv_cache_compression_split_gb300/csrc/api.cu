@@ -349,7 +349,8 @@ size_t kvc_h2o_workspace_size(const kvc_h2o_args *a)
     if (!a || a->mode != KVC_H2O_PREFILL || a->L <= 0 || a->B <= 0 || a->Hq <= 0)
         return 0;
     const size_t lpad = (size_t)((a->L + 127) / 128) * 128;   // whole 128-row query tiles
-    return (size_t)a->B * a->Hq * lpad * sizeof(float);
+    // -lse of every prompt row, then the two passes' work counters (16 bytes)
+    return (size_t)a->B * a->Hq * lpad * sizeof(float) + 16;
 }
 
 kvc_status kvc_h2o_accumulate(const kvc_h2o_args *a, cudaStream_t stream)

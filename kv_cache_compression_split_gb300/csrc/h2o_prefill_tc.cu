@@ -39,6 +39,7 @@ constexpr int NEPI = 2 * NQ;             // epilogue warps: two column halves pe
 constexpr int NTHR = (2 + NEPI) * 32;    // warp 0: TMA producer, warp 1: MMA issuer
 constexpr int NS = 2;                    // streaming stages
 constexpr int NL = 4;                    // pass 2: -lse slots of 128 floats
+constexpr int NI = 2;                    // slots of the pair feed
 constexpr int TMEM_COLS = 2 * TT;        // two fp32 accumulators of 128 columns
 constexpr int CTAS_PER_SM = 2;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -58,35 +59,22 @@ template <int D> struct TcCfg {
 struct TcParams {
     int Hq, Hkv, g, L, Lpad, kp_cap, C, nt, npairs, n_work;
     float *nlse;        // [B*Hq, Lpad]: -lse of every prompt row (pass 1 writes, pass 2 reads)
+    int *work_ctr;      // pairs handed out beyond each CTA's first (zero at launch)
     float *scores;
     float scale_log2;
     int *status;
 };
 
-// The CTA's work items in order: pair w covers tiles w % npairs and
-// nt - 1 - w % npairs of the (head or unit) w / npairs.
-struct ItemCursor {
-    int w, h;
-    __device__ bool get(const TcParams &p, int &outer, int &t) const
-    {
-        if (w >= p.n_work)
-            return false;
-        outer = w / p.npairs;
-        const int pair = w % p.npairs;
-        t = h == 0 ? pair : p.nt - 1 - pair;
-        return true;
-    }
-    __device__ void advance(const TcParams &p, int step)
-    {
-        const int pair = w % p.npairs;
-        if (h == 0 && pair != p.nt - 1 - pair) {
-            h = 1;
-        } else {
-            h = 0;
-            w += step;
-        }
-    }
-};
+// Work is handed out in pairs: pair w covers tiles w % npairs and
+// nt - 1 - w % npairs (one tile when they coincide) of the (head or unit)
+// w / npairs, so every pair costs the same.  A CTA starts with pair blockIdx.x
+// and then takes the next unclaimed pair from a global counter, so the two
+// CTAs that share an SM (which progress at different rates) finish together.
+__device__ __forceinline__ int pair_items(const TcParams &p, int w)
+{
+    const int pair = w % p.npairs;
+    return pair != p.nt - 1 - pair ? 2 : 1;
+}
 
 // Walks the stream tiles of an item on tile t in order: pass 1 key tiles
 // qt = 0 .. t; pass 2 query tiles qt = t .. nt-1 of group head hh = 0, then of
@@ -241,7 +229,9 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
     uint64_t *mma_done = bars + 2 * NS + 6;
     uint64_t *mrg_full = bars + 2 * NS + 7, *mrg_empty = bars + 2 * NS + 7 + NQ;
     uint64_t *l_full = bars + 2 * NS + 7 + 2 * NQ, *l_empty = l_full + NL;
+    uint64_t *it_full = l_empty + NL, *it_empty = it_full + NI;
     __shared__ uint32_t s_tmem;
+    __shared__ int s_item[NI];
     __shared__ int s_abort;
     volatile int *abort = &s_abort;
 
@@ -283,6 +273,10 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
             mbar_init(&l_full[i], 1);
             mbar_init(&l_empty[i], NEPI);
         }
+        for (int i = 0; i < NI; ++i) {
+            mbar_init(&it_full[i], 1);
+            mbar_init(&it_empty[i], 1 + NEPI);   // the MMA thread and every epilogue warp
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -294,6 +288,47 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
+    // The pair feed: the producer publishes the k-th pair in slot k % NI; the MMA
+    // thread and the epilogue warps read the pairs in the same order.  A pair
+    // index >= n_work ends the walk.
+    auto feed_put = [&](int k, int w) -> bool {
+        const int slot = k % NI;
+        if (k >= NI && !mbar_sleep_or_abort(&it_empty[slot], ((k / NI) & 1) ^ 1, abort))
+            return false;
+        s_item[slot] = w;
+        mbar_arrive(&it_full[slot]);
+        return true;
+    };
+    // consumers: the next item (outer index, stationary tile t) of the feed
+    struct FeedCursor {
+        int k = 0, w = 0, h = 0, nh = 0;
+    };
+    auto feed_next = [&](FeedCursor &c, int &outer, int &t, bool whole_warp) -> bool {
+        if (c.h >= c.nh) {
+            const int slot = c.k % NI;
+            bool got = mbar_sleep_or_abort(&it_full[slot], (c.k / NI) & 1, abort);
+            if (whole_warp)
+                got = __all_sync(0xffffffffu, got);
+            if (!got)
+                return false;
+            c.w = *reinterpret_cast<volatile int *>(&s_item[slot]);
+            if (whole_warp)
+                __syncwarp();
+            if (!whole_warp || lane == 0)
+                mbar_arrive(&it_empty[slot]);
+            ++c.k;
+            if (c.w >= p.n_work)
+                return false;
+            c.h = 0;
+            c.nh = pair_items(p, c.w);
+        }
+        const int pair = c.w % p.npairs;
+        outer = c.w / p.npairs;
+        t = c.h == 0 ? pair : p.nt - 1 - pair;
+        ++c.h;
+        return true;
+    };
+
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -301,8 +336,19 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
             prefetch_tmap(&tmK);
             int it = 0, n_stat = 0, outer, t;
             bool ok = true;
-            for (ItemCursor cur{(int)blockIdx.x, 0}; ok && cur.get(p, outer, t);
-                 cur.advance(p, gridDim.x)) {
+            int fk = 0, fw = blockIdx.x, fh = 0, fnh = 0;   // pairs published, current pair
+            while (ok) {
+                if (fh >= fnh) {
+                    if (fk > 0)
+                        fw = gridDim.x + atomicAdd(p.work_ctr, 1);
+                    if (!feed_put(fk++, fw) || fw >= p.n_work)
+                        break;
+                    fh = 0;
+                    fnh = pair_items(p, fw);
+                }
+                outer = fw / p.npairs;
+                t = fh == 0 ? fw % p.npairs : p.nt - 1 - fw % p.npairs;
+                ++fh;
                 int b, hk, bh, unit;
                 decode(outer, b, hk, bh, unit);
                 if (n_stat > 0 && !mbar_sleep_or_abort(stat_empty, (n_stat - 1) & 1, abort))
@@ -366,8 +412,8 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
         if (lane == 0) {
             int it = 0, tc = 0, n_item = 0, outer, t;
             bool ok = true;
-            for (ItemCursor cur{(int)blockIdx.x, 0}; ok && cur.get(p, outer, t);
-                 cur.advance(p, gridDim.x), ++n_item) {
+            FeedCursor fc;
+            for (; ok && feed_next(fc, outer, t, false); ++n_item) {
                 if (!mbar_sleep_or_abort(stat_full, n_item & 1, abort))
                     break;
                 tc_fence_after();
@@ -406,8 +452,8 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16) + 64 * half;
         int tc = 0, n_item = 0, outer, t;
         bool ok = true;
-        for (ItemCursor cur{(int)blockIdx.x, 0}; ok && cur.get(p, outer, t);
-             cur.advance(p, gridDim.x), ++n_item) {
+        FeedCursor fc;
+        for (; ok && feed_next(fc, outer, t, true); ++n_item) {
             int b, hk, bh, unit;
             decode(outer, b, hk, bh, unit);
             const int ns = n_stream<PASS>(p, t);
@@ -548,6 +594,11 @@ template <int D> cudaError_t prefill_tc_impl(const kvc_h2o_args &a, float *lse_w
     tp.kp_cap = a.kp_cap;
     tp.C = a.C;
     tp.nlse = lse_ws;
+    // the two passes' pair counters follow the -lse rows in the workspace
+    int *ctr = reinterpret_cast<int *>(lse_ws + (size_t)a.B * a.Hq * tp.Lpad);
+    cudaError_t e0 = cudaMemsetAsync(ctr, 0, 2 * sizeof(int), s);
+    if (e0 != cudaSuccess)
+        return e0;
     tp.scores = a.scores;
     const float scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / sqrtf((float)a.D);
     tp.scale_log2 = scale * LOG2E;
@@ -557,10 +608,12 @@ template <int D> cudaError_t prefill_tc_impl(const kvc_h2o_args &a, float *lse_w
         !encode_tmap_2d_f16(&tk, a.kp, D, (uint64_t)a.B * a.Hkv * a.kp_cap, 64, TT))
         return cudaErrorInvalidValue;
     tp.n_work = a.B * a.Hq * tp.npairs;
+    tp.work_ctr = ctr;
     cudaError_t e = launch_tc<D, 1>(tq, tk, tp, s);
     if (e != cudaSuccess)
         return e;
     tp.n_work = a.B * a.Hkv * tp.npairs;
+    tp.work_ctr = ctr + 1;
     return launch_tc<D, 2>(tq, tk, tp, s);
 }
 
