@@ -133,6 +133,39 @@ def test_h2o_prefill_scores_and_evict(kvc, orc, B, Hq, Hkv, L, D, n_heavy, n_rec
     assert device_status_clean(kvc)
 
 
+def test_h2o_prefill_full_size_sampled_units(kvc, orc):
+    """The prefill score pass at the benchmark's shape and launch (512 sequences, GQA 64/8,
+    D=128, a 2047-token causal prompt; the persistent CTAs claim tile pairs dynamically):
+    the oracle recomputes sampled (sequence, KV head) units, and conservation (the scores of
+    a unit sum to g * L) holds for every unit."""
+    from kv_cache_compression_split_gb300 import workloads as W
+    w = W.HEAVY
+    B, Hq, Hkv, D, L = w.B, w.Hq, w.Hkv, w.D, w.T - 1
+    g = Hq // Hkv
+    K, _ = W.kv_tensors(w, T=w.T, B=B, device="cuda")
+    kp = K[:, :, :L].contiguous()
+    del K
+    qp = W.q_tensor(w, B=B, L=L, device="cuda")
+    scores = torch.zeros(B, Hkv, L, dtype=torch.float32, device="cuda")
+    ws = torch.empty(kvc.kvc_h2o_workspace_size(B, Hq, L) // 4, dtype=torch.float32, device="cuda")
+    for _ in range(2):   # the second call reuses the workspace (its counters are re-zeroed)
+        scores.zero_()
+        kvc.kvc_h2o_accumulate_prefill(qp, kp, scores, ws, L)
+    torch.cuda.synchronize()
+    assert device_status_clean(kvc)
+    total = scores.double().sum(dim=2).cpu().numpy()
+    np.testing.assert_allclose(total, g * L, rtol=1e-4)
+    rng = np.random.default_rng(7)
+    units = sorted({(0, 0), (B - 1, Hkv - 1)} |
+                   {(int(b), int(h)) for b, h in zip(rng.integers(0, B, 2), rng.integers(0, Hkv, 2))})
+    for b, hk in units:
+        ref = orc.h2o_prefill_scores(np16(qp[b:b + 1, hk * g:(hk + 1) * g]),
+                                     np16(kp[b:b + 1, hk:hk + 1]), L, threads=8)
+        got = scores[b, hk].cpu().numpy().astype(np.float64)
+        np.testing.assert_allclose(got, ref[0, 0], rtol=SCORE_REL_TOL, atol=0,
+                                   err_msg=f"b={b} hk={hk}")
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,D,mode,splits,decay", [
     (4, 64, 8, 128, "separate", 0, 0.0), (3, 8, 8, 64, "separate", 0, 0.0),
     (4, 64, 8, 128, "fused", 1, 0.0), (3, 8, 8, 64, "fused", 3, 0.0),
