@@ -32,10 +32,15 @@ constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-// LSM: the fused H2O launch keeps the unit's logits in shared memory ([8][LSM_SLOTS]
-// fp32) instead of an output array, with fewer stages to make room.
+// Where the fused H2O launch keeps the unit's logits instead of an output array:
+//   LM_SMEM  in shared memory ([8][LSM_SLOTS] fp32), with fewer stages to make room;
+//   LM_REGS  in the registers of the thread that computed them (up to LREG_TILES
+//            tiles, i.e. C <= 576 slots), which leaves all stages in place.
+constexpr int LM_NONE = 0, LM_SMEM = 1, LM_REGS = 2;
 constexpr int LSM_SLOTS = H2O_ONCHIP_MAX_SLOTS;
-template <int D, bool LSM = false> struct SlotCfg {
+constexpr int LREG_TILES = 9;
+template <int D, int LMODE = LM_NONE> struct SlotCfg {
+    static constexpr bool LSM = LMODE == LM_SMEM;
     static constexpr int NBOX = D / 64;                 // 64-half (128-byte) boxes per row
     static constexpr int TILE_BYTES = TILE * D * 2;     // one K or V tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K + V
@@ -66,12 +71,13 @@ __device__ __forceinline__ void consumer_bar()
 }
 
 // Slots [0, n) of each unit are valid.
-template <int D, bool LSM>
+template <int D, int LMODE>
 __global__ void __launch_bounds__(NTHREADS, 2)
     k_attend_slots(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const SlotParams p)
 {
-    using Cfg = SlotCfg<D, LSM>;
+    using Cfg = SlotCfg<D, LMODE>;
+    constexpr bool LSM = Cfg::LSM, LREG = LMODE == LM_REGS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_align1024(smem_raw);
     float *lsm = reinterpret_cast<float *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES);  // LSM only
@@ -169,11 +175,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         lg1 = h1 < p.g ? p.logits + rowbase + (size_t)h1 * p.C : nullptr;
     }
 
-    for (int i = 0; i < ntiles; ++i) {
+    // one tile: wait for it, fold it into the running state, hand the stage back;
+    // lr receives this thread's four logits (tokens r, r + 8 of the warp's 16 x
+    // heads 2c, 2c + 1), the values the other storage modes write
+    auto do_tile = [&](int i, float (&lr)[4]) -> bool {
         const int st = i % Cfg::NSTAGE;
+        lr[0] = lr[1] = lr[2] = lr[3] = -INFINITY;
         if (!mbar_wait(&full[st], (i / Cfg::NSTAGE) & 1)) {
             flag_error(p.status, DEV_TIMEOUT);
-            break;
+            return false;
         }
         const int tok0 = t_begin + i * TILE + 16 * warp;
         if (tok0 < t_end) {
@@ -204,6 +214,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             const float x1 = va ? sa[1] * p.scale_log2 : -INFINITY;
             const float x2 = vb ? sa[2] * p.scale_log2 : -INFINITY;
             const float x3 = vb ? sa[3] * p.scale_log2 : -INFINITY;
+            lr[0] = sa[0] * p.scale;
+            lr[1] = sa[1] * p.scale;
+            lr[2] = sa[2] * p.scale;
+            lr[3] = sa[3] * p.scale;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
@@ -242,6 +256,33 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         __syncwarp();
         if (lane == 0)
             mbar_arrive(&empty[st]);
+        return true;
+    };
+    float lreg[LREG ? LREG_TILES : 1][4];   // LM_REGS: every tile's scores of this thread
+    // LM_REGS: lane c == 0 of each quad loads the old scores of its tokens now, so the
+    // loads are in flight while the tiles stream instead of at the end
+    float old[LREG ? LREG_TILES : 1][2];
+    if constexpr (LREG) {
+#pragma unroll
+        for (int i = 0; i < LREG_TILES; ++i) {
+            const int ta = t_begin + i * TILE + 16 * warp + r, tb = ta + 8;
+            const float *sc = p.h2o_scores + (size_t)unit * p.C;
+            const bool upd = p.h2o_scores && p.part_o == nullptr && c == 0 && i < ntiles;
+            old[i][0] = upd && ta < t_end ? sc[ta] : 0.f;
+            old[i][1] = upd && tb < t_end ? sc[tb] : 0.f;
+        }
+    }
+    if constexpr (LREG) {
+#pragma unroll
+        for (int i = 0; i < LREG_TILES; ++i) {
+            lreg[i][0] = lreg[i][1] = lreg[i][2] = lreg[i][3] = -INFINITY;
+            if (i < ntiles && !do_tile(i, lreg[i]))
+                break;
+        }
+    } else {
+        for (int i = 0; i < ntiles; ++i)
+            if (!do_tile(i, lreg[0]))
+                break;
     }
 
     // ---------------- merge the four warps
@@ -320,9 +361,39 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             s_lse2[h] = ls > 0.f ? ms + __log2f(ls) : INFINITY;
         }
         consumer_bar();
+        float *sc = p.h2o_scores + (size_t)unit * p.C;
+        if constexpr (LREG) {
+            // the same arithmetic as the other storage modes: lane c == 0 of each quad
+            // gathers the probabilities of heads 0 .. 7 for tokens r and r + 8 of every
+            // tile (heads 2c, 2c + 1 come from lane c) and adds them in head order
+            const float L0 = h0 < p.g ? s_lse2[h0] : 0.f, L1 = h1 < p.g ? s_lse2[h1] : 0.f;
+#pragma unroll
+            for (int i = 0; i < LREG_TILES; ++i) {
+                if (i >= ntiles)
+                    break;
+                const float e[4] = {h0 < p.g ? ex2(fmaf(lreg[i][0], LOG2E, -L0)) : 0.f,
+                                    h1 < p.g ? ex2(fmaf(lreg[i][1], LOG2E, -L1)) : 0.f,
+                                    h0 < p.g ? ex2(fmaf(lreg[i][2], LOG2E, -L0)) : 0.f,
+                                    h1 < p.g ? ex2(fmaf(lreg[i][3], LOG2E, -L1)) : 0.f};
+                float add_a = 0.f, add_b = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {   // heads 2q, 2q + 1 from lane 4r + q
+                    const int src = (lane & ~3) + q;
+                    add_a += __shfl_sync(0xffffffffu, e[0], src);
+                    add_a += __shfl_sync(0xffffffffu, e[1], src);
+                    add_b += __shfl_sync(0xffffffffu, e[2], src);
+                    add_b += __shfl_sync(0xffffffffu, e[3], src);
+                }
+                const int ta = t_begin + i * TILE + 16 * warp + r, tb = ta + 8;
+                if (c == 0 && ta < t_end)
+                    sc[ta] = fmaf(old[i][0], p.h2o_keep, add_a * p.h2o_add);
+                if (c == 0 && tb < t_end)
+                    sc[tb] = fmaf(old[i][1], p.h2o_keep, add_b * p.h2o_add);
+            }
+            return;
+        }
         const float *lrow = LSM ? lsm : p.logits + ((size_t)b * p.Hq + hk * p.g) * p.C;
         const size_t lstride = LSM ? LSM_SLOTS : p.C;
-        float *sc = p.h2o_scores + (size_t)unit * p.C;
         // four slots per thread per round, every load issued before any is used
         constexpr int U = 4;
         for (int j0 = threadIdx.x; j0 < t_end; j0 += U * NCW * 32) {
@@ -387,22 +458,22 @@ __global__ void k_combine(int Hq, int Hkv, int g, int D, int splits, const float
         lse[bh] = ls > 0.f ? (ms + __log2f(ls)) * LN2 : -INFINITY;
 }
 
-template <int D, bool LSM>
+template <int D, int LMODE>
 cudaError_t launch_slots_impl(const CUtensorMap &tk, const CUtensorMap &tv, const SlotParams &sp,
                               int grid, cudaStream_t s)
 {
-    using Cfg = SlotCfg<D, LSM>;
+    using Cfg = SlotCfg<D, LMODE>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_attend_slots<D, LSM>,
+        cudaError_t e = cudaFuncSetAttribute(k_attend_slots<D, LMODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
         if (e != cudaSuccess)
             return e;
         configured_device = dev;
     }
-    k_attend_slots<D, LSM><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
+    k_attend_slots<D, LMODE><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
     return cudaGetLastError();
 }
 
@@ -444,10 +515,16 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
     const bool lsm = a.h2o_scores && !a.logits;
     if (lsm && (a.splits != 1 || a.C > LSM_SLOTS))
         return cudaErrorInvalidValue;
-    cudaError_t e = a.D == 128 ? (lsm ? launch_slots_impl<128, true>(tk, tv, sp, grid, s)
-                                      : launch_slots_impl<128, false>(tk, tv, sp, grid, s))
-                               : (lsm ? launch_slots_impl<64, true>(tk, tv, sp, grid, s)
-                                      : launch_slots_impl<64, false>(tk, tv, sp, grid, s));
+    const int lmode = !lsm ? LM_NONE : (a.C <= LREG_TILES * TILE ? LM_REGS : LM_SMEM);
+    cudaError_t e;
+    if (a.D == 128)
+        e = lmode == LM_REGS   ? launch_slots_impl<128, LM_REGS>(tk, tv, sp, grid, s)
+            : lmode == LM_SMEM ? launch_slots_impl<128, LM_SMEM>(tk, tv, sp, grid, s)
+                               : launch_slots_impl<128, LM_NONE>(tk, tv, sp, grid, s);
+    else
+        e = lmode == LM_REGS   ? launch_slots_impl<64, LM_REGS>(tk, tv, sp, grid, s)
+            : lmode == LM_SMEM ? launch_slots_impl<64, LM_SMEM>(tk, tv, sp, grid, s)
+                               : launch_slots_impl<64, LM_NONE>(tk, tv, sp, grid, s);
     if (e != cudaSuccess || a.splits == 1)
         return e;
     return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);
