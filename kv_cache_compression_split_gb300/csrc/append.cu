@@ -742,8 +742,8 @@ __device__ __forceinline__ long kivi_nq(long T, int R)
 // it writes may be ones a flushed group still reads); bulk appends run the
 // groups on a wide grid first and the residual in a second launch.
 template <int D, int BITS, bool GROUPS, bool RESIDUAL, bool GEAR>
-__global__ void __launch_bounds__(QTHREADS, GEAR ? 2 : 3)
-    k_append_quant(int Hkv, int R, int Cq, int n_new, const uint16_t *__restrict__ k_new,
+__global__ void __launch_bounds__(QTHREADS, GEAR ? 2 : 6)
+    k_append_quant(int n_units, int Hkv, int R, int Cq, int n_new, const uint16_t *__restrict__ k_new,
                    const uint16_t *__restrict__ v_new, uint8_t *__restrict__ kb,
                    uint8_t *__restrict__ vb, uint16_t *__restrict__ k_res,
                    uint16_t *__restrict__ v_res, const int32_t *__restrict__ len,
@@ -757,7 +757,9 @@ __global__ void __launch_bounds__(QTHREADS, GEAR ? 2 : 3)
     extern __shared__ __align__(16) uint8_t gear_dyn[];
     GearSmem<D> *gs = GEAR ? reinterpret_cast<GearSmem<D> *>(gear_dyn) : nullptr;
 
-    const int unit = blockIdx.x;
+    // units blockIdx.x, blockIdx.x + gridDim.x, ... (decode-sized appends run one wave
+    // of CTAs over all units; bulk appends one CTA column per unit)
+    for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
     const int b = unit / Hkv;
     const int CR = R + G;
     const long T0 = len[b], T1 = T0 + n_new;
@@ -765,7 +767,7 @@ __global__ void __launch_bounds__(QTHREADS, GEAR ? 2 : 3)
     if (nq1 > Cq) {
         if (threadIdx.x == 0 && blockIdx.y == 0 && (GROUPS || !RESIDUAL))
             flag_error(status, DEV_CAPACITY);
-        return;
+        continue;
     }
     const uint16_t *kn = k_new + (size_t)unit * n_new * D;
     const uint16_t *vn = v_new + (size_t)unit * n_new * D;
@@ -800,6 +802,7 @@ __global__ void __launch_bounds__(QTHREADS, GEAR ? 2 : 3)
             vrw[slot * (D / 8) + ch] = reinterpret_cast<const uint4 *>(vn + (p - T0) * D)[ch];
         }
     }
+    }   // units
 }
 
 __global__ void k_len_bump(int B, int n_new, int32_t *len)
@@ -833,9 +836,12 @@ cudaError_t launch_quant_impl(const kvc_quant_cache &c, const uint16_t *k_new,
         }
     }
     if (n_new <= KIVI_G) {
-        // decode-sized: at most two groups flush; one CTA per unit does both parts
-        k_append_quant<D, BITS, true, true, GEAR><<<units, QTHREADS, dyn, s>>>(
-            c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
+        // decode-sized: at most two groups flush per unit; one wave of CTAs walks the
+        // units, each doing both parts for its units
+        const int per_sm = GEAR ? 2 : 6;
+        const int grid = units < per_sm * sm_count() ? units : per_sm * sm_count();
+        k_append_quant<D, BITS, true, true, GEAR><<<grid, QTHREADS, dyn, s>>>(
+            units, c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
             c.len, blocks, c.k_gear, c.v_gear, dev_status_ptr());
     } else {
         // bulk: the flushed groups of every unit spread over the grid, then the residual
@@ -844,13 +850,13 @@ cudaError_t launch_quant_impl(const kvc_quant_cache &c, const uint16_t *k_new,
         int gy = (int)(max_groups < fill ? max_groups : fill);
         gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
         k_append_quant<D, BITS, true, false, GEAR><<<dim3(units, gy), QTHREADS, dyn, s>>>(
-            c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
+            units, c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
             c.len, blocks, c.k_gear, c.v_gear, dev_status_ptr());
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
         k_append_quant<D, BITS, false, true, false><<<units, QTHREADS, 0, s>>>(
-            c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
+            units, c.Hkv, c.R, c.Cq, n_new, k_new, v_new, c.k_blocks, c.v_blocks, c.k_res, c.v_res,
             c.len, blocks, nullptr, nullptr, dev_status_ptr());
     }
     cudaError_t e = cudaGetLastError();
