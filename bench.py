@@ -111,6 +111,23 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------ GPU arm
 
+class L2Flush:
+    """Evicts the workload from the 129 MB L2 between timed repetitions: a write of a buffer
+    larger than L2, then a read of another one, so that the timed kernel starts with L2 full
+    of clean lines of unrelated data.  (A write alone leaves L2 full of dirty lines, and the
+    next kernel pays for their write-back: on the 8-sequence LLaMA-7B-shaped attention that
+    added ~15 us to a 45 us read.)"""
+
+    def __init__(self, dev, nbytes: int = 512 << 20):
+        import torch
+        self.w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(nbytes // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.add_(1)
+        self.r.sum()
+
+
 def slot_bytes(n_slots, B, Hkv, Hq, D):
     """Algorithmic bytes of one slot-cache attention launch: K and V of the attended slots,
     the queries and the outputs."""
@@ -639,18 +656,19 @@ def gear_rows(kvc, dev, stream, gear4, qs, kn, vn, hbm_peak):
 
 
 def config_rows(kvc, W, dev, stream, hbm_peak):
-    """Decode attention on the two MHA workloads (median of 5 after one warm-up, L2 flushed by a
-    512 MB write before each, as their compressed caches fit in L2): llama7b-b8-h32-d128-t2048
+    """Decode attention on the two MHA workloads (median of 5 after one warm-up, L2 flushed
+    before each by a 512 MB write and a 512 MB read, as their compressed caches fit in L2):
+    llama7b-b8-h32-d128-t2048
     (FP16 over T+1 slots; H2O-512 and StreamingLLM-512 over 513 slots) and
     kivi-b32-h32-d128-t4096 (FP16, KIVI-4 and KIVI-2 over T tokens)."""
     import torch
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     out = {}
 
     def timed(fn):
         ts = []
         for r in range(6):
-            flush.add_(1)
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn()
@@ -811,11 +829,11 @@ def random_rows(kvc, W, dev, stream):
         o = torch.empty_like(q)
         ws = torch.empty(max(kvc.kvc_workspace_size(base, q) // 4, 1), dtype=torch.float32,
                          device=dev)
-        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        flush = L2Flush(dev)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
         torch.cuda.synchronize(dev)
         for r in range(reps):
-            flush.add_(1)          # evict the cache from L2 between repetitions
+            flush()                # evict the cache from L2 between repetitions
             ev[r][0].record(stream)
             kvc.kvc_random_evict(caches[r], 1024, 0.25, W.RANDOM_EVICT_SEED, r, stream=stream)
             ev[r][1].record(stream)
@@ -1006,7 +1024,7 @@ def run_grid(args):
                   StreamingLLM's eviction) over the cache the prefill left; for random eviction,
                   attention over the kept slots
     Every timing is the median of 3 repetitions after one warm-up, with L2 flushed (a 512 MB
-    write) before each; one JSON line per cell."""
+    write, then a 512 MB read) before each; one JSON line per cell."""
     import torch
     import kv_cache_compression_split_gb300 as kvc
     from kv_cache_compression_split_gb300 import build as kbuild
@@ -1019,7 +1037,7 @@ def run_grid(args):
     ratios = [1.0, 0.75, 0.5, 0.25, 0.125]
     batches = [int(x) for x in args.grid_batches.split(",")]
     lengths = [int(x) for x in args.grid_lengths.split(",")]
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def timed(fn, setup=None, reps=3):
@@ -1027,7 +1045,7 @@ def run_grid(args):
         for r in range(reps + 1):
             if setup is not None:
                 setup()
-            flush.add_(1)
+            flush()
             e0.record(stream)
             fn()
             e1.record(stream)
