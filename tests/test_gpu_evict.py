@@ -323,6 +323,44 @@ def test_h2o_free_running_decode(kvc, orc, B, Hq, Hkv, D, L, n_heavy, n_recent, 
     assert device_status_clean(kvc)
 
 
+@pytest.mark.parametrize("D,C,Hq,Hkv,decay", [(128, 576, 64, 8, 0.0), (64, 300, 24, 8, 0.99),
+                                               (128, 65, 8, 2, 0.0)])
+def test_h2o_register_logits_ragged_vs_oracle(kvc, orc, D, C, Hq, Hkv, decay):
+    """The fused H2O launch with the logits in registers (caches of up to 576 slots) on ragged
+    units (empty, one slot, a partial tile, full capacity) and g < 8 query heads per KV head:
+    outputs, lse and scores against the oracle's attention and accumulation."""
+    B = 3
+    g = torch.Generator().manual_seed(C + Hq + D)
+    K = torch.randn(B, Hkv, C, D, generator=g).half()
+    V = torch.randn(B, Hkv, C, D, generator=g).half()
+    q = torch.randn(B, Hq, D, generator=g).half()
+    rng = np.random.default_rng(C)
+    n = rng.integers(0, C + 1, (B, Hkv))
+    n[0, 0], n[-1, -1] = 0, C
+    n[1, 0] = 1
+    cache = slot_cache_from(kvc, K, V, n, C)
+    base = torch.rand(B, Hkv, C, generator=g)
+    sc = base.clone().cuda()
+    o = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    kvc.kvc_decode_attend(cache, q.cuda(), o, lse=lse, num_splits=1, h2o_scores=sc,
+                          h2o_decay=decay)
+    torch.cuda.synchronize()
+    ref_o, ref_lse, ref_lg = orc.decode_attend(np16(q), np16(K), np16(V), n, want_logits=True)
+    assert_o_close(np16(o), ref_o)
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse.cpu().numpy()[fin], ref_lse[fin], atol=1e-4, rtol=0)
+    ref_sc = orc.h2o_accumulate(base.numpy(), ref_lg, ref_lse, n, decay)
+    got = sc.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        for hk in range(Hkv):
+            nn = int(n[b, hk])
+            np.testing.assert_allclose(got[b, hk, :nn], ref_sc[b, hk, :nn], rtol=SCORE_REL_TOL,
+                                       err_msg=f"b={b} hk={hk}")
+            assert np.array_equal(got[b, hk, nn:], base.numpy()[b, hk, nn:])   # untouched
+    assert device_status_clean(kvc)
+
+
 @pytest.mark.parametrize("D,C,n", [(128, 520, 513), (64, 1024, 1024), (128, 1024, 700)])
 def test_h2o_onchip_logits_match_written_logits(kvc, D, C, n):
     """The fused H2O launch with the logits kept on chip gives bit-identical outputs, lse and

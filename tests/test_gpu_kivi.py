@@ -82,6 +82,28 @@ def test_pack_bit_exact_with_flushes(kvc, orc, D, bits, R):
     assert device_status_clean(kvc)
 
 
+def test_decode_appends_over_more_units_than_one_wave(kvc, orc):
+    """Decode-sized appends run one wave of CTAs that walk the units (six per SM); with 1280
+    units every CTA takes more than one.  Sequences start at ragged lengths, so their groups
+    flush at different steps; sampled units are checked bit-exactly."""
+    B, Hkv, D, bits, R = 160, 8, 128, 4, 16
+    g = torch.Generator().manual_seed(1280)
+    offsets = [b % (R + G) for b in range(B)]
+    chunks = [1] * 40
+    T = max(offsets) + sum(chunks)
+    Kseq = torch.randn(B, Hkv, T, D, generator=g).half()
+    Vseq = torch.randn(B, Hkv, T, D, generator=g).half()
+    assert B * Hkv > 6 * torch.cuda.get_device_properties(0).multi_processor_count
+    cache, lens = _build(kvc, Kseq.cuda(), Vseq.cuda(), bits, R, Cq=128, chunks=chunks,
+                         offsets=offsets)
+    assert cache.len.cpu().tolist() == list(lens)
+    rng = np.random.default_rng(3)
+    for b in sorted({0, 1, 31, 47, 100, B - 1} | set(rng.integers(0, B, 4).tolist())):
+        for hk in (0, int(rng.integers(0, Hkv)), Hkv - 1):
+            _check_unit(orc, cache, Kseq, Vseq, b, hk, int(lens[b]), bits, R)
+    assert device_status_clean(kvc)
+
+
 def _attend(kvc, cache, q, splits=0):
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device="cuda")
