@@ -7,6 +7,7 @@
 #include <limits.h>
 #include <math.h>
 #include <mutex>
+#include <vector>
 
 namespace kvc {
 
@@ -77,6 +78,50 @@ int sm_count()
         g_sm_count[dev] = v > 0 ? v : 1;
     }
     return g_sm_count[dev];
+}
+
+namespace {
+struct KernelDeviceEntry {
+    const void *func;
+    int dev;
+    int value;   // resident CTAs (resident_ctas) or 1 (set_smem_once)
+    bool occupancy;
+};
+std::vector<KernelDeviceEntry> g_kernel_entries;   // guarded by g_mu
+} // namespace
+
+cudaError_t set_smem_once(const void *func, int bytes)
+{
+    const int dev = current_device();
+    if (dev < 0)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (const KernelDeviceEntry &e : g_kernel_entries)
+        if (e.func == func && e.dev == dev && !e.occupancy)
+            return cudaSuccess;
+    const cudaError_t err =
+        cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess)
+        g_kernel_entries.push_back({func, dev, 1, false});
+    return err;
+}
+
+int resident_ctas(const void *func, int threads, int smem)
+{
+    const int dev = current_device();
+    if (dev < 0)
+        return 1;
+    const int sms = sm_count();
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (const KernelDeviceEntry &e : g_kernel_entries)
+        if (e.func == func && e.dev == dev && e.occupancy)
+            return e.value;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, threads, smem) != cudaSuccess)
+        per_sm = 1;
+    const int v = (per_sm > 0 ? per_sm : 1) * sms;
+    g_kernel_entries.push_back({func, dev, v, true});
+    return v;
 }
 
 bool encode_tmap_2d_f16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,

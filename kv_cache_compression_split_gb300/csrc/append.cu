@@ -821,19 +821,13 @@ cudaError_t launch_quant_impl(const kvc_quant_cache &c, const uint16_t *k_new,
                              KIVI_G * D * BITS / 8 + 4 * D};
     const int dyn = GEAR ? (int)sizeof(GearSmem<D>) : 0;
     if (GEAR) {   // the GEAR stage sits in dynamic shared memory next to the static group stage
-        static int configured = -1;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (configured != dev) {
-            cudaError_t e = cudaFuncSetAttribute(k_append_quant<D, BITS, true, true, GEAR>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(k_append_quant<D, BITS, true, false, GEAR>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-            if (e != cudaSuccess)
-                return e;
-            configured = dev;
-        }
+        cudaError_t e = set_smem_once(
+            reinterpret_cast<const void *>(k_append_quant<D, BITS, true, true, GEAR>), dyn);
+        if (e == cudaSuccess)
+            e = set_smem_once(
+                reinterpret_cast<const void *>(k_append_quant<D, BITS, true, false, GEAR>), dyn);
+        if (e != cudaSuccess)
+            return e;
     }
     if (n_new <= KIVI_G) {
         // decode-sized: at most two groups flush per unit; one wave of CTAs walks the

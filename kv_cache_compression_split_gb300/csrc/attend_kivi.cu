@@ -906,23 +906,11 @@ cudaError_t launch_kivi_impl(const CUtensorMap &tk, const CUtensorMap &tv, const
                              cudaStream_t s)
 {
     using Cfg = KiviCfg<D, BITS, GEAR>;
-    static int configured_device = -1;
-    static int resident = 1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_attend_kivi<D, BITS, GEAR>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-        if (e != cudaSuccess)
-            return e;
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attend_kivi<D, BITS, GEAR>,
-                                                          NTHREADS, Cfg::SMEM);
-        if (e != cudaSuccess)
-            return e;
-        resident = (per_sm > 0 ? per_sm : 1) * sm_count();
-        configured_device = dev;
-    }
+    const void *fn = reinterpret_cast<const void *>(k_attend_kivi<D, BITS, GEAR>);
+    const cudaError_t e = set_smem_once(fn, Cfg::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    const int resident = resident_ctas(fn, NTHREADS, Cfg::SMEM);
     const int grid = kp.n_items < resident ? kp.n_items : resident;
     if (grid <= 0)
         return cudaSuccess;

@@ -463,16 +463,10 @@ cudaError_t launch_slots_impl(const CUtensorMap &tk, const CUtensorMap &tv, cons
                               int grid, cudaStream_t s)
 {
     using Cfg = SlotCfg<D, LMODE>;
-    static int configured_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_attend_slots<D, LMODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-        if (e != cudaSuccess)
-            return e;
-        configured_device = dev;
-    }
+    const cudaError_t e =
+        set_smem_once(reinterpret_cast<const void *>(k_attend_slots<D, LMODE>), Cfg::SMEM);
+    if (e != cudaSuccess)
+        return e;
     k_attend_slots<D, LMODE><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
     return cudaGetLastError();
 }

@@ -565,16 +565,10 @@ cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const TcPara
                       cudaStream_t s)
 {
     using Cfg = TcCfg<D>;
-    static int configured = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_prefill_tc<D, PASS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-        if (e != cudaSuccess)
-            return e;
-        configured = dev;
-    }
+    const cudaError_t e =
+        set_smem_once(reinterpret_cast<const void *>(k_prefill_tc<D, PASS>), Cfg::SMEM);
+    if (e != cudaSuccess)
+        return e;
     const int cap = CTAS_PER_SM * sm_count();
     const int grid = tp.n_work < cap ? tp.n_work : cap;
     k_prefill_tc<D, PASS><<<grid, NTHR, Cfg::SMEM, s>>>(tq, tk, tp);

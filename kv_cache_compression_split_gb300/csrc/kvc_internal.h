@@ -20,6 +20,14 @@ int *dev_status_ptr();
 // SM count of the current device.
 int sm_count();
 
+// Raise the dynamic shared-memory limit of kernel `func` to `bytes` on the current
+// device, once per (kernel, device); thread safe.  Returns the attribute call's error.
+cudaError_t set_smem_once(const void *func, int bytes);
+
+// CTAs of `func` (threads per CTA, dynamic shared memory) resident on all SMs of the
+// current device together (at least one per SM), cached per (kernel, device).
+int resident_ctas(const void *func, int threads, int smem);
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 bool encode_tmap_2d_f16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                         uint32_t box_inner, uint32_t box_rows);
