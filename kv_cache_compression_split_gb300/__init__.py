@@ -110,10 +110,21 @@ def lib():
 # ----------------------------------------------------------------------------- helpers
 
 def _ptr(t):
+    """Device address of tensor t for a descriptor field.  Every tensor handed to the library
+    must be contiguous and live on the current CUDA device: a host tensor's address given to
+    a kernel would be read as device memory (or, where the GPU can reach host memory, read
+    silently)."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"kvc: tensor on {t.device}; the library takes CUDA tensors")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"kvc: tensor on {t.device}, expected the current device "
+                         f"cuda:{torch.cuda.current_device()}")
+    if not t.is_contiguous():
+        raise ValueError("kvc: tensor arguments must be contiguous")
     return t.data_ptr()
 
 
@@ -153,7 +164,7 @@ def kvc_append_quant(cache: "QuantCache", k_new, v_new, stream=None):
 
 
 def _attend_args(cache, q, o, logits=None, lse=None, workspace=None, num_splits=0, scale=0.0,
-                 h2o_scores=None, h2o_decay=0.0):
+                 h2o_scores=None, h2o_decay=0.0, shape_only=False):
     a = AttendArgs()
     keep = []
     if isinstance(cache, SlotCache):
@@ -167,7 +178,8 @@ def _attend_args(cache, q, o, logits=None, lse=None, workspace=None, num_splits=
         a.kind = KVC_KIND_KIVI
         a.quant = C.pointer(d)
     a.Hq = int(q.shape[1])
-    a.q, a.o = _ptr(q), _ptr(o)
+    # a size query reads only q's shape (the library plans from the dimensions)
+    a.q, a.o = (None, None) if shape_only else (_ptr(q), _ptr(o))
     a.logits, a.lse = _ptr(logits), _ptr(lse)
     a.workspace = _ptr(workspace)
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -183,7 +195,7 @@ def kvc_gear_side_bytes(D: int) -> int:
 
 
 def kvc_workspace_size(cache, q, num_splits: int = 0) -> int:
-    a, _keep = _attend_args(cache, q, None, num_splits=num_splits)
+    a, _keep = _attend_args(cache, q, None, num_splits=num_splits, shape_only=True)
     return int(lib().kvc_workspace_size(C.byref(a)))
 
 

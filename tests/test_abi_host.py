@@ -102,3 +102,17 @@ def test_product_path_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, f), errors="ignore").read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
                 assert "oracle.c" not in src and "liboracle" not in src, f
+
+
+def test_binding_rejects_host_and_strided_tensors():
+    """The binding hands only contiguous tensors of the current CUDA device to the library: a
+    host tensor's address would otherwise reach a kernel as if it were device memory."""
+    import torch
+    import kv_cache_compression_split_gb300 as kvc
+    cache = kvc.SlotCache.empty(1, 1, 64, 64, device="cpu")
+    q = torch.zeros(1, 1, 64, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kvc.kvc_decode_attend(cache, q, torch.empty_like(q))
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        kvc.kvc_append(cache, torch.zeros(1, 1, 1, 64, dtype=torch.float16),
+                       torch.zeros(1, 1, 1, 64, dtype=torch.float16))
