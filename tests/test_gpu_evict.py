@@ -323,6 +323,67 @@ def test_h2o_free_running_decode(kvc, orc, B, Hq, Hkv, D, L, n_heavy, n_recent, 
     assert device_status_clean(kvc)
 
 
+def test_h2o_decode_step_full_size_sampled_units(kvc, orc):
+    """One H2O-512 decode step at the benchmark's shape and launch (512 sequences, GQA 64/8,
+    D=128, a 520-slot cache holding 64 heavy + 448 recent tokens of a 2048-token history):
+    append, attention with the score update fused and the logits in registers, eviction back
+    to 512.  Sampled units against the oracle: outputs, lse, scores and keep-sets."""
+    from kv_cache_compression_split_gb300 import workloads as W
+    w = W.HEAVY
+    B, Hq, Hkv, D, T, C = w.B, w.Hq, w.Hkv, w.D, w.T, 520
+    n_heavy, n_recent = 64, 448
+    rng = np.random.default_rng(2048)
+    Kseq, Vseq = W.kv_tensors(w, T=T + 1, B=B, device="cuda")
+    q = W.q_tensor(w, B=B, device="cuda")
+    pos0 = np.empty((B, Hkv, 512), np.int32)
+    for b in range(B):
+        for hk in range(Hkv):
+            heavy = rng.choice(T - n_recent, n_heavy, replace=False)
+            pos0[b, hk] = rng.permutation(np.concatenate([heavy, np.arange(T - n_recent, T)]))
+    sc0 = rng.uniform(0.0, 4.0, (B, Hkv, C)).astype(np.float32)
+    sc0[..., 512:] = 0.0
+    cache = kvc.SlotCache.empty(B, Hkv, C, D)
+    idx = torch.from_numpy(pos0).long().cuda()[..., None].expand(-1, -1, -1, D)
+    cache.K[:, :, :512] = torch.gather(Kseq, 2, idx)
+    cache.V[:, :, :512] = torch.gather(Vseq, 2, idx)
+    cache.pos[:, :, :512] = torch.from_numpy(pos0).cuda()
+    cache.n.fill_(512)
+    cache.seqlen.fill_(T)
+    scores = torch.from_numpy(sc0).cuda()
+    kvc.kvc_append(cache, Kseq[:, :, T:T + 1].contiguous(), Vseq[:, :, T:T + 1].contiguous())
+    o = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    kvc.kvc_decode_attend(cache, q, o, lse=lse, num_splits=1, h2o_scores=scores)
+    sc_mid = scores.clone()
+    kvc.kvc_h2o_evict(cache, scores, n_heavy, n_recent)
+    torch.cuda.synchronize()
+    assert device_status_clean(kvc)
+    n = cache.n.cpu().numpy()
+    assert (n == 512).all()
+    g = Hq // Hkv
+    pos513 = np.concatenate([pos0, np.full((B, Hkv, 1), T, np.int32)], axis=2)
+    for b, hk in sorted({(0, 0), (B - 1, Hkv - 1)} |
+                        {(int(x), int(y)) for x, y in zip(rng.integers(0, B, 4),
+                                                          rng.integers(0, Hkv, 4))}):
+        p = pos513[b, hk]
+        Ku = np16(Kseq[b:b + 1, hk:hk + 1, p])
+        Vu = np16(Vseq[b:b + 1, hk:hk + 1, p])
+        sl = slice(hk * g, (hk + 1) * g)
+        ref_o, ref_lse, ref_lg = orc.decode_attend(np16(q[b:b + 1, sl]), Ku, Vu,
+                                                   np.array([[513]], np.int32), want_logits=True)
+        assert_o_close(np16(o[b:b + 1, sl]), ref_o, what=f"b={b} hk={hk}")
+        np.testing.assert_allclose(lse[b, sl].cpu().numpy(), ref_lse[0], atol=1e-4, rtol=0)
+        ref_sc = orc.h2o_accumulate(sc0[b:b + 1, hk:hk + 1, :513].astype(np.float64), ref_lg,
+                                    ref_lse, np.array([[513]], np.int32))[0, 0]
+        np.testing.assert_allclose(sc_mid[b, hk, :513].cpu().numpy(), ref_sc,
+                                   rtol=SCORE_REL_TOL, err_msg=f"b={b} hk={hk}")
+        got_pos = cache.pos[b, hk, :512].cpu().numpy()
+        _check_keep_with_ties(got_pos, p, ref_sc, T + 1, n_heavy, n_recent)
+        rows = {int(x): i for i, x in enumerate(p)}
+        src = torch.tensor([rows[int(x)] for x in got_pos], device="cuda")
+        assert torch.equal(cache.K[b, hk, :512], Kseq[b, hk, torch.from_numpy(p).long().cuda()][src])
+
+
 @pytest.mark.parametrize("D,C,Hq,Hkv,decay", [(128, 576, 64, 8, 0.0), (64, 300, 24, 8, 0.99),
                                                (128, 65, 8, 2, 0.0)])
 def test_h2o_register_logits_ragged_vs_oracle(kvc, orc, D, C, Hq, Hkv, decay):
