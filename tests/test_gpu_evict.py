@@ -323,6 +323,39 @@ def test_h2o_free_running_decode(kvc, orc, B, Hq, Hkv, D, L, n_heavy, n_recent, 
     assert device_status_clean(kvc)
 
 
+def test_stream_decode_step_full_size_sampled_units(kvc, orc):
+    """One StreamingLLM-512 decode step at the benchmark's shape (512 sequences, 8 KV heads,
+    a 520-slot cache holding 64 sinks + 448 recent tokens of a 2048-token history in scrambled
+    slot order): append, then eviction back to 512 with the one-warp-per-unit kernel.  Every
+    unit's keep-set against the closed form, sampled units' rows against their tokens."""
+    from kv_cache_compression_split_gb300 import workloads as W
+    w = W.HEAVY
+    B, Hkv, D, T, C, n_sink, n_recent = w.B, w.Hkv, w.D, w.T, 520, 64, 448
+    rng = np.random.default_rng(512)
+    Kseq, Vseq = W.kv_tensors(w, T=T + 1, B=B, device="cuda")
+    base = np.concatenate([np.arange(n_sink), np.arange(T - n_recent, T)]).astype(np.int32)
+    pos0 = np.stack([np.stack([rng.permutation(base) for _ in range(Hkv)]) for _ in range(B)])
+    cache = kvc.SlotCache.empty(B, Hkv, C, D)
+    idx = torch.from_numpy(pos0).long().cuda()[..., None].expand(-1, -1, -1, D)
+    cache.K[:, :, :512] = torch.gather(Kseq, 2, idx)
+    cache.V[:, :, :512] = torch.gather(Vseq, 2, idx)
+    cache.pos[:, :, :512] = torch.from_numpy(pos0).cuda()
+    cache.n.fill_(512)
+    cache.seqlen.fill_(T)
+    kvc.kvc_append(cache, Kseq[:, :, T:T + 1].contiguous(), Vseq[:, :, T:T + 1].contiguous())
+    kvc.kvc_stream_evict(cache, n_sink, n_recent)
+    torch.cuda.synchronize()
+    assert device_status_clean(kvc)
+    assert (cache.n.cpu().numpy() == 512).all()
+    want = np.flatnonzero(orc.stream_keep(np.arange(T + 1), T + 1, n_sink, n_recent))
+    got = np.sort(cache.pos[:, :, :512].cpu().numpy(), axis=2)
+    assert (got == want[None, None, :]).all()
+    for b, hk in [(0, 0), (B - 1, Hkv - 1), (int(rng.integers(B)), int(rng.integers(Hkv)))]:
+        p = torch.from_numpy(cache.pos[b, hk, :512].cpu().numpy()).long().cuda()
+        assert torch.equal(cache.K[b, hk, :512], Kseq[b, hk, p])
+        assert torch.equal(cache.V[b, hk, :512], Vseq[b, hk, p])
+
+
 def test_h2o_decode_step_full_size_sampled_units(kvc, orc):
     """One H2O-512 decode step at the benchmark's shape and launch (512 sequences, GQA 64/8,
     D=128, a 520-slot cache holding 64 heavy + 448 recent tokens of a 2048-token history):
