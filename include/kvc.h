@@ -247,8 +247,11 @@ enum { KVC_KIND_SLOTS = 0, KVC_KIND_KIVI = 1 };
  *               With logits NULL the launch keeps the logits on chip: it then
  *               runs in one split (num_splits 0 or 1; another value is
  *               KVC_ERR_INVALID_ARG) and needs C <= KVC_H2O_ONCHIP_MAX_SLOTS
- *               (else KVC_ERR_UNSUPPORTED).  With logits given, any split count
- *               works (several splits add one kvc_h2o_accumulate launch).
+ *               (else KVC_ERR_UNSUPPORTED); up to 576 slots the logits stay in
+ *               registers, beyond that in shared memory (fewer pipeline stages).
+ *               All three storage modes give bit-identical o, lse and scores.
+ *               With logits given, any split count works (several splits add
+ *               one kvc_h2o_accumulate launch).
  *   h2o_decay   0 (plain H2O, scores += p) or lambda in (0, 1) (decayed
  *               scores = lambda * scores + (1 - lambda) * p); see kvc_h2o_args
  */
