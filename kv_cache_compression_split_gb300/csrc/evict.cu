@@ -440,25 +440,43 @@ __global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams 
     uint32_t *keep = s_keep[warp];
     const long rt = T - p.n_recent;
     int n_new = 0;
+    // the unit's positions (and H2O scores) in registers: slot 32 i + lane in element i,
+    // every load issued before the first is used, so the scans below cost one round trip
+    constexpr int NR = WE_MAX_SLOTS / 32;
+    int32_t pr[NR];
+    float sr[KIND == EVICT_H2O ? NR : 1];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+        const int j = 32 * i + lane;
+        pr[i] = j < n ? pos[j] : 0;
+        if constexpr (KIND == EVICT_H2O)
+            sr[i] = j < n ? sc[j] : 0.f;
+    }
 
     if (KIND == EVICT_STREAM) {
-        for (int base = 0; base < n; base += 32) {
-            const int j = base + lane;
-            const bool k = j < n && ((long)pos[j] < p.n_sink || (long)pos[j] >= rt);
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            if (32 * i >= n)
+                break;
+            const int j = 32 * i + lane;
+            const bool k = j < n && ((long)pr[i] < p.n_sink || (long)pr[i] >= rt);
             const unsigned m = __ballot_sync(0xffffffffu, k);
             if (lane == 0)
-                keep[base >> 5] = m;
+                keep[i] = m;
             n_new += __popc(m);
         }
         if (n_new == n)
             return;
     } else {
         int n_rec = 0;
-        for (int base = 0; base < n; base += 32) {
-            const int j = base + lane;
-            const unsigned m = __ballot_sync(0xffffffffu, j < n && (long)pos[j] >= rt);
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            if (32 * i >= n)
+                break;
+            const int j = 32 * i + lane;
+            const unsigned m = __ballot_sync(0xffffffffu, j < n && (long)pr[i] >= rt);
             if (lane == 0)
-                keep[base >> 5] = m;
+                keep[i] = m;
             n_rec += __popc(m);
         }
         const int take = min(p.n_heavy, n - n_rec);
@@ -471,20 +489,26 @@ __global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams 
         if (take > 0 && drops <= 4) {
             // few drops (the decode step drops one): keep every candidate, then remove
             // the worst -- the largest (descending score, position) key -- drops times
-            for (int base = 0; base < n; base += 32) {
-                const int j = base + lane;
-                const unsigned m = __ballot_sync(0xffffffffu, j < n && cand(j));
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                if (32 * i >= n)
+                    break;
+                const int j = 32 * i + lane;
+                const unsigned m = __ballot_sync(0xffffffffu, j < n && (long)pr[i] < rt);
                 if (lane == 0)
-                    keep[base >> 5] |= m;
+                    keep[i] |= m;
             }
             __syncwarp();
             for (int d = 0; d < drops; ++d) {
                 uint64_t best = 0;
                 int bj = -1;
-                for (int base = 0; base < n; base += 32) {
-                    const int j = base + lane;
-                    if (j < n && cand(j) && ((keep[base >> 5] >> lane) & 1u)) {
-                        const uint64_t k = key(j);
+#pragma unroll
+                for (int i = 0; i < NR; ++i) {
+                    if (32 * i >= n)
+                        break;
+                    const int j = 32 * i + lane;
+                    if (j < n && (long)pr[i] < rt && ((keep[i] >> lane) & 1u)) {
+                        const uint64_t k = ((uint64_t)desc_bits(sr[i]) << 32) | (uint32_t)pr[i];
                         if (bj < 0 || k > best) {
                             best = k;
                             bj = j;
