@@ -525,7 +525,7 @@ def run_gpu(args, rank, world):
     # ---------------- H2O variants and random eviction rows, timed in the same run
     rows.update(h2o_variant_rows(kvc, dev, stream, h2o, h2o_scores, qs[:, 1], kn[:, 1], vn[:, 1],
                                  n_heavy, n_recent))
-    rows.update(random_rows(kvc, W, dev, stream))
+    rows.update(random_rows(kvc, W, dev, stream, hbm_peak))
     rows.update(paged_rows(kvc, dev, stream, fp, kv4, qs[0, 0], T0))
     rows.update(gear_rows(kvc, dev, stream, gear4, qs[:, 2], kn[:, 2], vn[:, 2], hbm_peak))
     del gear4
@@ -826,53 +826,77 @@ def paged_rows(kvc, dev, stream, dense, kv4, q, T):
     return out
 
 
-def random_rows(kvc, W, dev, stream):
-    """Random eviction on the reasoning-trace workload: a cache of 1024 locked prompt tokens +
-    341 kept + 1024 new generated tokens per KV head is evicted to keep 0.25 of the 1365
-    candidates, then decode attention runs over the 1365 kept slots."""
+def random_rows(kvc, W, dev, stream, hbm_peak):
+    """Random eviction on the reasoning-trace workload, run as the trace runs: 16 sequences,
+    GQA 64/8, a locked prompt of 1024 tokens, 1024 generated tokens appended per epoch, an
+    eviction to keep 0.25 of the generated tokens per KV head at T = 2048, 3072, ..., 32768
+    (31 evictions, epochs 0..30, positions up to 32767), and decode attention after every
+    eviction.  L2 is flushed (a 512 MB write and a 512 MB read) before each eviction, so both
+    launches read the cache from HBM; the bulk appends are set-up, not timed.  The row reports
+    the steady state (epochs 5..30: 2389 -> 1365 slots per head) and every epoch's times."""
     import torch
     w = W.REASONING
     B, Hq, Hkv, D = w.B, w.Hq, w.Hkv, w.D
-    n0 = 1024 + 341 + 1024
-    reps = 5
+    P, every, T_end = w.prompt_len, w.evict_every, w.T
+    n_evict = (T_end - P) // every
     out = {}
     with torch.cuda.stream(stream):
-        K, V = W.kv_tensors(w, T=n0, device=dev)
-        C = n0 + 8
-        base = kvc.SlotCache.empty(B, Hkv, C, D, device=dev)
-        kvc.kvc_append(base, K, V, stream=stream)
-        caches = []
-        for _ in range(reps):
-            c = kvc.SlotCache(K=base.K.clone(), V=base.V.clone(), pos=base.pos.clone(),
-                              n=base.n.clone(), seqlen=base.seqlen.clone())
-            caches.append(c)
-        q = W.q_tensor(w, device=dev)
-        o = torch.empty_like(q)
-        ws = torch.empty(max(kvc.kvc_workspace_size(base, q) // 4, 1), dtype=torch.float32,
-                         device=dev)
+        K, V = W.kv_tensors(w, T=T_end, device=dev)
+        C = 2432
+        c = kvc.SlotCache.empty(B, Hkv, C, D, device=dev)
+        kvc.kvc_append(c, K[:, :, :P + every].contiguous(), V[:, :, :P + every].contiguous(),
+                       stream=stream)
+        qs = [W.q_tensor(w, device=dev, seed_offset=e) for e in range(n_evict)]
+        o = torch.empty_like(qs[0])
         flush = L2Flush(dev)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
-        torch.cuda.synchronize(dev)
-        for r in range(reps):
-            flush()                # evict the cache from L2 between repetitions
-            ev[r][0].record(stream)
-            kvc.kvc_random_evict(caches[r], 1024, 0.25, W.RANDOM_EVICT_SEED, r, stream=stream)
-            ev[r][1].record(stream)
-            kvc.kvc_decode_attend(caches[r], q, o, workspace=ws, stream=stream)
-            ev[r][2].record(stream)
-        torch.cuda.synchronize(dev)
-        t_ev = sorted(e[0].elapsed_time(e[1]) for e in ev[1:])
-        t_at = sorted(e[1].elapsed_time(e[2]) for e in ev[1:])
-        kept = int(caches[0].n[0, 0].item())
-    moved_bytes = B * Hkv * (n0 * 4 + 2 * 256 * D * 2 * 2)   # pos scan + ~256 moved rows r/w
-    att_bytes = slot_bytes(kept, B, Hkv, Hq, D)
+        t_ev, t_at, ev_bytes, at_bytes, n_before, n_after = [], [], [], [], [], []
+        for e in range(n_evict):
+            if e > 0:
+                t0 = P + every * e
+                kvc.kvc_append(c, K[:, :, t0:t0 + every].contiguous(),
+                               V[:, :, t0:t0 + every].contiguous(), stream=stream)
+            ws = torch.empty(max(kvc.kvc_workspace_size(c, qs[e]) // 4, 1), dtype=torch.float32,
+                             device=dev)
+            n0 = int(c.n[0, 0].item())
+            pre = c.pos[:, :, :n0].clone()
+            flush()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            kvc.kvc_random_evict(c, P, w.keep_ratio, W.RANDOM_EVICT_SEED, e, stream=stream)
+            ev[1].record(stream)
+            kvc.kvc_decode_attend(c, qs[e], o, workspace=ws, stream=stream)
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+            n1 = int(c.n[0, 0].item())
+            # rows the compaction moved: kept slots of [0, n1) whose position changed
+            moved = int((c.pos[:, :, :n1] != pre[:, :, :n1]).sum().item())
+            t_ev.append(ev[0].elapsed_time(ev[1]))
+            t_at.append(ev[1].elapsed_time(ev[2]))
+            # eviction: every slot's position read once, each moved row's K and V read and
+            # written, its position written
+            ev_bytes.append(B * Hkv * n0 * 4 + moved * (2 * 2 * D * 2 + 4))
+            at_bytes.append(slot_bytes(n1, B, Hkv, Hq, D))
+            n_before.append(n0)
+            n_after.append(n1)
+        st = list(range(5, n_evict))
+        ms_ev = statistics.median(t_ev[i] for i in st)
+        ms_at = statistics.median(t_at[i] for i in st)
+        gb_ev = statistics.median(ev_bytes[i] for i in st)
+        gb_at = statistics.median(at_bytes[i] for i in st)
+        assert kvc.kvc_read_device_status(stream) == 0
+        del K, V, c, flush
     out["random_evict_reasoning"] = {
-        "ms": statistics.median(t_ev), "kept_per_head": kept,
-        "shape": f"B={B} Hkv={Hkv} D={D}: {n0} -> {kept} slots per head"}
+        "ms": ms_ev, "bytes": gb_ev, "gbs": gb_ev / (ms_ev * 1e-3) / 1e9,
+        "frac_of_hbm": gb_ev / (ms_ev * 1e-3) / 1e9 / hbm_peak,
+        "slots_before": n_before[-1], "kept_per_head": n_after[-1],
+        "ms_per_epoch": [round(t, 4) for t in t_ev],
+        "shape": f"B={B} Hkv={Hkv} D={D}, prompt {P} locked, evictions at T = {P + every}.."
+                 f"{T_end} (epochs 0..{n_evict - 1}); steady state epochs 5..{n_evict - 1}: "
+                 f"{n_before[-1]} -> {n_after[-1]} slots per head; L2 flushed before each"}
     out["random_attend_reasoning"] = {
-        "ms": statistics.median(t_at), "slots": kept,
-        "gbs": att_bytes / (statistics.median(t_at) * 1e-3) / 1e9,
-        "tokens_per_s": B / (statistics.median(t_at) * 1e-3)}
+        "ms": ms_at, "slots": n_after[-1], "bytes": gb_at,
+        "gbs": gb_at / (ms_at * 1e-3) / 1e9, "frac_of_hbm": gb_at / (ms_at * 1e-3) / 1e9 / hbm_peak,
+        "tokens_per_s": B / (ms_at * 1e-3), "ms_per_epoch": [round(t, 4) for t in t_at]}
     return out
 
 
@@ -993,6 +1017,48 @@ def run_profile(args):
         ws = torch.empty(kvc.kvc_h2o_workspace_size(kp.shape[0], Hq, L) // 4, device=dev)
         for _ in range(3):
             kvc.kvc_h2o_accumulate_prefill(qp, kp, sc, ws, L)
+    elif what == "random_evict":
+        # reasoning-trace steady state (epoch 30): 1024 locked prompt tokens, 341 kept earlier
+        # tokens, 1024 new ones -> 1365 per head after the eviction; --profile-batch sequences
+        wr = W.REASONING
+        n0, P = 1024 + 341 + 1024, wr.prompt_len
+        Kr, Vr = W.kv_tensors(wr, T=n0, B=B, device=dev)
+        cache = kvc.SlotCache.empty(B, wr.Hkv, 2432, wr.D, device=dev)
+        kvc.kvc_append(cache, Kr, Vr)
+        gp = torch.Generator().manual_seed(30)
+        old = torch.randperm(31744 - P, generator=gp)[:341].sort().values + P
+        posr = torch.cat([torch.arange(P), old, torch.arange(31744, 32768)]).int().to(dev)
+        cache.pos[:, :, :n0] = posr
+        cache.seqlen.fill_(32768)
+        pos0 = cache.pos.clone()
+        for _ in range(3):
+            cache.pos.copy_(pos0)
+            cache.n.fill_(n0)
+            kvc.kvc_random_evict(cache, P, wr.keep_ratio, W.RANDOM_EVICT_SEED, 30)
+    elif what in ("attend_kivi2_mha", "attend_kivi4_mha"):
+        # the KIVI workload: 32 MHA heads, T = 4096, offsets on Q, K, V; --profile-batch sequences
+        wk = W.KIVI_MHA
+        bits = 2 if what == "attend_kivi2_mha" else 4
+        Kk, Vk = W.kv_tensors(wk, T=wk.T, B=B, device=dev)
+        qk = W.q_tensor(wk, B=B, device=dev)
+        ok = torch.empty_like(qk)
+        cache = kvc.QuantCache.empty(B, wk.Hkv, wk.T, wk.D, bits, wk.kivi_R, device=dev)
+        kvc.kvc_append_quant(cache, Kk, Vk)
+        del Kk, Vk
+        torch.cuda.empty_cache()
+        ws = torch.empty(max(kvc.kvc_workspace_size(cache, qk) // 4, 1), device=dev)
+        for _ in range(3):
+            kvc.kvc_decode_attend(cache, qk, ok, workspace=ws)
+    elif what in ("kivi_append_flush", "gear_append_flush"):
+        # decode-sized append whose token completes a group: the bulk pack of 2047 tokens
+        # (two launches), then three one-token appends from length 2047, each flushing group 59
+        cache = kvc.QuantCache.empty(B, Hkv, T + 32, D, 4, w.kivi_R, device=dev,
+                                     gear=what == "gear_append_flush")
+        kvc.kvc_append_quant(cache, K[:, :, :T - 1].contiguous(), V[:, :, :T - 1].contiguous())
+        kn, vn = K[:, :, T - 1:T].contiguous(), V[:, :, T - 1:T].contiguous()
+        for _ in range(3):
+            cache.len.fill_(T - 1)
+            kvc.kvc_append_quant(cache, kn, vn)
     else:
         raise SystemExit(f"unknown --profile {what}")
     torch.cuda.synchronize()

@@ -8,7 +8,7 @@
  *   - split-KV decode attention over an fp16 slot cache or a KIVI cache, with
  *     GQA head mapping                        -- kvc_decode_attend
  *   - H2O heavy-hitter scores and eviction    -- kvc_h2o_accumulate, kvc_h2o_evict
- *   - StreamingLLM sink + recent window       -- kvc_stream_evict
+ *   - StreamingLLM sink + recent window       -- kvc_stream_evict, kvc_stream_append
  *   - per-head uniform random eviction with the prompt locked
  *                                             -- kvc_random_evict
  *
@@ -404,6 +404,29 @@ KVC_API kvc_status kvc_h2o_evict_when(const kvc_slot_cache *cache, float *scores
  */
 KVC_API kvc_status kvc_stream_evict(const kvc_slot_cache *cache, int n_sink, int n_recent,
                             cudaStream_t stream);
+
+/*
+ * kvc_stream_append -- StreamingLLM decode step without an eviction launch.
+ * Appends one token per sequence (k_new / v_new [B, Hkv, 1, D] fp16, device) at
+ * position P = seqlen[b], then seqlen += 1.  In each unit, the token that leaves
+ * the window with this step -- position P - n_recent - 1, when that is >= n_sink --
+ * gives up its slot: the new token overwrites that slot's K, V and position and n
+ * is unchanged.  When no valid slot holds that position the token goes to slot n
+ * and n += 1 (a unit at capacity sets KVC_DEV_CAPACITY and is left unchanged).
+ * So a unit that holds the window of the previous step ([0, n_sink) and
+ * [P - 1 - n_recent, P - 1]), or the keep set of kvc_stream_evict after the
+ * prompt, holds after the call exactly this step's attention window
+ *   positions < n_sink  and  P - n_recent <= position <= P
+ * (n_sink + n_recent + 1 tokens in steady state).  The step's decode attention
+ * then reads that window, and the token that left it is dropped by the next
+ * call's overwrite, with no scan-and-move launch: the eviction is metadata only.
+ * The attention sets are those of append -> attend -> kvc_stream_evict.
+ * Source: "Rethinking KV Cache Compression" guide, §2 (64 sinks + 448 recent)
+ * and §16 "4 种方法逐步执行" (sinks plus the recent window, no scores).
+ */
+KVC_API kvc_status kvc_stream_append(const kvc_slot_cache *cache, const uint16_t *k_new,
+                             const uint16_t *v_new, int n_sink, int n_recent,
+                             cudaStream_t stream);
 
 /*
  * kvc_random_evict -- per-head uniform random eviction with the prompt locked.

@@ -94,6 +94,7 @@ def lib():
                 "kvc_h2o_evict": (st, [C.POINTER(SlotCacheDesc), P, i, i, P]),
                 "kvc_h2o_evict_when": (st, [C.POINTER(SlotCacheDesc), P, i, i, i, P]),
                 "kvc_stream_evict": (st, [C.POINTER(SlotCacheDesc), i, i, P]),
+                "kvc_stream_append": (st, [C.POINTER(SlotCacheDesc), P, P, i, i, P]),
                 "kvc_random_evict": (st, [C.POINTER(SlotCacheDesc), i, C.c_double, C.c_uint64,
                                           C.c_uint32, P]),
                 "kvc_status_string": (C.c_char_p, [i]),
@@ -271,6 +272,16 @@ def kvc_stream_evict(cache: "SlotCache", n_sink: int, n_recent: int, stream=None
     d = cache.desc()
     _check(lib().kvc_stream_evict(C.byref(d), n_sink, n_recent, _stream(stream)),
            "kvc_stream_evict")
+
+
+def kvc_stream_append(cache: "SlotCache", k_new, v_new, n_sink: int, n_recent: int, stream=None):
+    """One StreamingLLM decode token per sequence ([B, Hkv, 1, D]); the token leaving the
+    window gives up its slot (see kvc.h)."""
+    if int(k_new.shape[2]) != 1 or int(v_new.shape[2]) != 1:
+        raise ValueError("kvc_stream_append takes one token per sequence")
+    d = cache.desc()
+    _check(lib().kvc_stream_append(C.byref(d), _ptr(k_new), _ptr(v_new), n_sink, n_recent,
+                                   _stream(stream)), "kvc_stream_append")
 
 
 def kvc_random_evict(cache: "SlotCache", prompt_len: int, keep_ratio: float, seed: int,

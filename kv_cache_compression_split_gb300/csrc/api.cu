@@ -488,6 +488,17 @@ kvc_status kvc_stream_evict(const kvc_slot_cache *cache, int n_sink, int n_recen
     return from_cuda(launch_evict(e, stream));
 }
 
+kvc_status kvc_stream_append(const kvc_slot_cache *cache, const uint16_t *k_new,
+                             const uint16_t *v_new, int n_sink, int n_recent, cudaStream_t stream)
+{
+    kvc_status st = check_slot_cache(cache);
+    if (st != KVC_OK)
+        return st;
+    if (n_sink < 0 || n_recent < 0 || !k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+        return KVC_ERR_INVALID_ARG;
+    return from_cuda(launch_stream_append(*cache, k_new, v_new, n_sink, n_recent, stream));
+}
+
 kvc_status kvc_random_evict(const kvc_slot_cache *cache, int prompt_len, double keep_ratio,
                             uint64_t seed, uint32_t epoch, cudaStream_t stream)
 {

@@ -114,6 +114,94 @@ __global__ void k_append_small(int Hkv, int D, int C, int n_new, const uint4 *__
     }
 }
 
+// StreamingLLM decode append ("Rethinking KV Cache Compression" guide, §2 and §16
+// "4 种方法逐步执行": keep the sinks and the recent window, no scores).  One token per
+// sequence at position P = seqlen[b]; the token that leaves the window with this
+// step, position P - n_recent - 1 (when it is not a sink), gives up its slot to the
+// new token, so the cache holds exactly this step's attention window
+// [0, n_sink) + [P - n_recent, P] and no eviction launch is needed.  When no slot
+// holds that position (the window is not full yet) the token goes to slot n.
+// One CTA per sequence, one warp per KV head: the warp scans the unit's positions
+// (every load of a round in flight at once), then writes the row.
+__global__ void k_stream_append(int Hkv, int D, int C, int n_sink, int n_recent,
+                                const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                                uint4 *__restrict__ K, uint4 *__restrict__ V,
+                                int32_t *__restrict__ pos, int32_t *__restrict__ n,
+                                int32_t *__restrict__ seqlen, const SlotRows rows, int *status)
+{
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int P = seqlen[b];
+    const long leave = (long)P - n_recent - 1;
+    const int cpt = D / 8;
+    __shared__ int s_bad;
+    if (threadIdx.x == 0)
+        s_bad = 0;
+    __syncthreads();
+    for (int hk = warp; hk < Hkv; hk += nw) {
+        const int unit = b * Hkv + hk;
+        const int n0 = n[unit];
+        if (n0 < 0 || n0 > C) {
+            if (lane == 0)
+                s_bad = 1;
+            continue;
+        }
+        const int32_t *up = pos + (size_t)unit * C;
+        int slot = -1;
+        if (leave >= n_sink) {
+            constexpr int U = 8;
+            for (int base = 0; base < n0 && slot < 0; base += 32 * U) {
+                int32_t pv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = base + 32 * u + lane;
+                    pv[u] = j < n0 ? up[j] : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const unsigned m = __ballot_sync(0xffffffffu, (long)pv[u] == leave);
+                    if (m && slot < 0)
+                        slot = base + 32 * u + __ffs(m) - 1;
+                }
+            }
+        }
+        const bool grow = slot < 0;
+        if (grow) {
+            if (n0 + 1 > C) {
+                if (lane == 0)
+                    s_bad = 1;
+                continue;
+            }
+            slot = n0;
+        }
+        const long row = rows.row(unit, slot);
+        if (row < 0) {   // no page behind this slot
+            if (lane == 0)
+                s_bad = 1;
+            continue;
+        }
+        for (int i = lane; i < 2 * cpt; i += 32) {
+            const size_t src = (size_t)unit * cpt + (i % cpt);
+            const size_t dst = (size_t)row * cpt + (i % cpt);
+            if (i < cpt)
+                K[dst] = k_new[src];
+            else
+                V[dst] = v_new[src];
+        }
+        if (lane == 0) {
+            pos[(size_t)unit * C + slot] = P;
+            if (grow)
+                n[unit] = n0 + 1;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        seqlen[b] = P + 1;
+        if (s_bad)
+            flag_error(status, DEV_CAPACITY);
+    }
+}
+
 __global__ void k_append_bump(int B, int Hkv, int C, int n_new, int32_t *n, int32_t *seqlen)
 {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -900,6 +988,18 @@ cudaError_t launch_append_slots(const kvc_slot_cache &c, const uint16_t *k_new,
         return e;
     const int m = units > c.B ? units : c.B;
     k_append_bump<<<(m + 255) / 256, 256, 0, s>>>(c.B, c.Hkv, c.C, n_new, c.n, c.seqlen);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stream_append(const kvc_slot_cache &c, const uint16_t *k_new,
+                                 const uint16_t *v_new, int n_sink, int n_recent, cudaStream_t s)
+{
+    const int warps = c.Hkv < 16 ? c.Hkv : 16;
+    k_stream_append<<<c.B, 32 * warps, 0, s>>>(
+        c.Hkv, c.D, c.C, n_sink, n_recent, reinterpret_cast<const uint4 *>(k_new),
+        reinterpret_cast<const uint4 *>(v_new), reinterpret_cast<uint4 *>(c.K),
+        reinterpret_cast<uint4 *>(c.V), c.pos, c.n, c.seqlen,
+        SlotRows{c.block_table, c.C, c.num_pages}, dev_status_ptr());
     return cudaGetLastError();
 }
 

@@ -594,6 +594,252 @@ __global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams 
         p.n[unit] = n_new;
 }
 
+// ------------------------------------------------------------------------
+// Random eviction for caches of at most RF_MAX_SLOTS slots (the reasoning-trace
+// cadence keeps ~2400 per unit): one 1024-thread CTA per unit with the unit's
+// positions and Philox keys staged in shared memory, so every key is computed
+// once.  The n_keep-th smallest (key, pos) is found with one 2048-bin histogram
+// of the top 11 key bits: bins below the crossing bin are kept whole, bins above
+// are dropped, and the few members of the crossing bin are ranked against each
+// other exactly.  The compaction then moves all rows at once, 16-byte chunks
+// spread over the whole CTA with four loads in flight per thread.
+// ------------------------------------------------------------------------
+constexpr int RF_THREADS = 1024;
+constexpr int RF_WARPS = RF_THREADS / 32;
+constexpr int RF_BINS = 2048;                 // top 11 key bits
+constexpr int RF_SHIFT = 64 - 11;
+constexpr int RF_MAX_SLOTS = 8192;            // u16 slot indices, one keep word per thread
+constexpr int RF_UNROLL = 4;                  // row chunks in flight per thread
+
+__host__ __device__ constexpr size_t rf_align(size_t x) { return (x + 15) & ~(size_t)15; }
+
+// Shared-memory carve-up for capacity C (bytes); the layout below must match.
+__host__ __device__ constexpr size_t rf_smem_bytes(int C)
+{
+    return rf_align((size_t)C * 8)                          // keys
+           + rf_align((size_t)C * 4)                        // positions
+           + rf_align((size_t)((C + 31) / 32) * 4)          // keep bitmask
+           + rf_align((size_t)(C + 2) * 2)                  // bucket list / hole + tail lists
+           + (size_t)RF_BINS * 4                            // histogram
+           + 64 * 4;                                        // scan scratch + scalars
+}
+
+// Exclusive scan of one int per thread over the 1024-thread CTA; *total gets the
+// sum.  `wsum` holds RF_WARPS ints.  All threads must call it.
+__device__ __forceinline__ int rf_scan(int v, int *total, int *wsum)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off)
+            x += y;
+    }
+    if (lane == 31)
+        wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = wsum[lane];
+        int ti = t;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, ti, off);
+            if (lane >= off)
+                ti += y;
+        }
+        wsum[lane] = ti - t;         // exclusive prefix of warp totals
+        if (lane == 31)
+            wsum[RF_WARPS] = ti;     // grand total
+    }
+    __syncthreads();
+    const int r = wsum[warp] + x - v;
+    *total = wsum[RF_WARPS];
+    __syncthreads();                 // wsum may be reused by the next scan
+    return r;
+}
+
+__global__ void __launch_bounds__(RF_THREADS, 1) k_evict_random(const EvictParams p)
+{
+    extern __shared__ __align__(16) uint8_t rf_smem[];
+    const int C = p.C;
+    uint64_t *s_key = reinterpret_cast<uint64_t *>(rf_smem);
+    int32_t *s_pos = reinterpret_cast<int32_t *>(rf_smem + rf_align((size_t)C * 8));
+    uint32_t *s_keep = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(s_pos) +
+                                                    rf_align((size_t)C * 4));
+    const int nwords = (C + 31) / 32;
+    uint16_t *s_list = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(s_keep) +
+                                                    rf_align((size_t)nwords * 4));
+    uint32_t *s_hist = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(s_list) +
+                                                    rf_align((size_t)(C + 2) * 2));
+    int *s_misc = reinterpret_cast<int *>(s_hist + RF_BINS);   // [0, 33): scan; 40..: scalars
+
+    const int unit = blockIdx.x, b = unit / p.Hkv, hk = unit % p.Hkv;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int n = p.n[unit];
+    if (n > C || n < 0) {
+        if (tid == 0)
+            flag_error(p.status, DEV_CAPACITY);
+        return;
+    }
+    for (int i = tid; i < RF_BINS; i += RF_THREADS)
+        s_hist[i] = 0;
+    if (tid == 0)
+        s_misc[40] = 0;   // bucket list length
+    __syncthreads();
+
+    // ---- 1. positions and keys into shared memory, candidate count, top-bit histogram
+    const int32_t *pos = p.pos + (size_t)unit * C;
+    int my_cand = 0;
+    for (int j = tid; j < n; j += RF_THREADS) {
+        const int32_t pj = pos[j];
+        s_pos[j] = pj;
+        uint64_t k = ~0ull;
+        if (pj >= p.prompt_len) {
+            k = philox_key(p.seed_lo, p.seed_hi, (uint32_t)pj, (uint32_t)hk, (uint32_t)b, p.epoch);
+            ++my_cand;
+            atomicAdd(&s_hist[(uint32_t)(k >> RF_SHIFT)], 1u);
+        }
+        s_key[j] = k;
+    }
+    int n_cand;
+    rf_scan(my_cand, &n_cand, s_misc);
+    if (n_cand == 0)
+        return;
+    int n_keep = (int)((double)n_cand * p.keep_ratio);
+    n_keep = n_keep < 1 ? 1 : (n_keep > n_cand ? n_cand : n_keep);
+    if (n_keep == n_cand)
+        return;
+    const int n_new = n - n_cand + n_keep;
+
+    // ---- 2. the bin that holds the n_keep-th smallest key (two bins per thread)
+    {
+        const int h0 = (int)s_hist[2 * tid], h1 = (int)s_hist[2 * tid + 1];
+        int tot;
+        const int ex = rf_scan(h0 + h1, &tot, s_misc);
+        if (ex < n_keep && n_keep <= ex + h0 + h1) {
+            const bool first = n_keep <= ex + h0;
+            s_misc[41] = first ? 2 * tid : 2 * tid + 1;
+            s_misc[42] = first ? ex : ex + h0;
+        }
+        __syncthreads();
+    }
+    const uint32_t bstar = (uint32_t)s_misc[41];
+    const int need = n_keep - s_misc[42];   // members of bin bstar to keep, >= 1
+
+    // ---- 3. keep flags: candidates of lower bins and every prompt slot; members of
+    // bin bstar go to a list and are decided by their exact rank among themselves
+    for (int base = 0; base < n; base += RF_THREADS) {
+        const int j = base + tid;
+        bool kp = false;
+        if (j < n) {
+            const uint64_t k = s_key[j];
+            if (s_pos[j] < p.prompt_len) {
+                kp = true;
+            } else {
+                const uint32_t bin = (uint32_t)(k >> RF_SHIFT);
+                kp = bin < bstar;
+                if (bin == bstar)
+                    s_list[atomicAdd(&s_misc[40], 1)] = (uint16_t)j;
+            }
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, kp);
+        if (lane == 0 && base + 32 * (tid >> 5) < n)
+            s_keep[(base >> 5) + (tid >> 5)] = m;
+    }
+    __syncthreads();
+    const int m_b = s_misc[40];
+    for (int t = tid; t < m_b; t += RF_THREADS) {
+        const int j = s_list[t];
+        const uint64_t kj = s_key[j];
+        const int32_t pj = s_pos[j];
+        int rank = 0;
+        for (int i = 0; i < m_b; ++i) {
+            const int o = s_list[i];
+            const uint64_t ko = s_key[o];
+            rank += (ko < kj || (ko == kj && s_pos[o] < pj)) ? 1 : 0;
+        }
+        if (rank < need)
+            atomicOr(&s_keep[j >> 5], 1u << (j & 31));
+    }
+    __syncthreads();
+
+    // ---- 4. hole and tail lists (k-th hole of [0, n_new) <- k-th kept slot of [n_new, n))
+    uint16_t *s_hole = s_list;                       // ranks [0, pairs)
+    uint16_t *s_tail = s_list + (C + 2) / 2;         // pairs <= min(n_new, n - n_new) <= C / 2
+    int n_pairs;
+    {
+        const int wn = (n + 31) / 32;
+        uint32_t hb = 0, tb = 0;
+        if (tid < wn) {
+            const uint32_t w = s_keep[tid];
+            const int lo = 32 * tid;
+            const uint32_t valid = (n - lo >= 32) ? 0xffffffffu : ((1u << (n - lo)) - 1u);
+            const uint32_t below = (n_new - lo >= 32) ? 0xffffffffu
+                                   : (n_new - lo <= 0) ? 0u : ((1u << (n_new - lo)) - 1u);
+            hb = ~w & below & valid;
+            tb = w & ~below & valid;
+        }
+        const int hbase = rf_scan(__popc(hb), &n_pairs, s_misc);
+        int tt;
+        const int tbase = rf_scan(__popc(tb), &tt, s_misc);
+        for (int r = 0; hb; ++r) {
+            const int l = __ffs(hb) - 1;
+            hb &= hb - 1;
+            s_hole[hbase + r] = (uint16_t)(32 * tid + l);
+        }
+        for (int r = 0; tb; ++r) {
+            const int l = __ffs(tb) - 1;
+            tb &= tb - 1;
+            s_tail[tbase + r] = (uint16_t)(32 * tid + l);
+        }
+    }
+    __syncthreads();
+
+    // ---- 5. moves: pair k's K row then V row as 16-byte chunks, RF_UNROLL per thread in flight
+    const int chunks = p.D / 8;                  // per row
+    const int per_pair = 2 * chunks;
+    const int total = n_pairs * per_pair;
+    uint4 *K4 = reinterpret_cast<uint4 *>(p.K), *V4 = reinterpret_cast<uint4 *>(p.V);
+    for (int base = 0; base < total; base += RF_THREADS * RF_UNROLL) {
+        uint4 v[RF_UNROLL];
+        long dst[RF_UNROLL];
+        bool isv[RF_UNROLL];
+#pragma unroll
+        for (int u = 0; u < RF_UNROLL; ++u) {
+            const int idx = base + u * RF_THREADS + tid;
+            dst[u] = -1;
+            isv[u] = false;
+            if (idx < total) {
+                const int k = idx / per_pair, c = idx % per_pair;
+                const long rs = p.rows.row(unit, s_tail[k]), rd = p.rows.row(unit, s_hole[k]);
+                isv[u] = c >= chunks;
+                const int cc = isv[u] ? c - chunks : c;
+                if (rs < 0 || rd < 0) {   // no page behind a slot: skip the chunk, flag it
+                    flag_error(p.status, DEV_CAPACITY);
+                } else {
+                    v[u] = isv[u] ? V4[rs * chunks + cc] : K4[rs * chunks + cc];
+                    dst[u] = rd * chunks + cc;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < RF_UNROLL; ++u) {
+            if (dst[u] >= 0) {
+                if (isv[u])
+                    V4[dst[u]] = v[u];
+                else
+                    K4[dst[u]] = v[u];
+            }
+        }
+    }
+    int32_t *gpos = p.pos + (size_t)unit * C;
+    for (int k = tid; k < n_pairs; k += RF_THREADS)
+        gpos[s_hole[k]] = s_pos[s_tail[k]];
+    if (tid == 0)
+        p.n[unit] = n_new;
+}
+
 } // namespace
 
 cudaError_t launch_evict(const EvictLaunch &e, cudaStream_t s)
@@ -636,7 +882,16 @@ cudaError_t launch_evict(const EvictLaunch &e, cudaStream_t s)
             k_evict<EVICT_STREAM><<<units, ETHREADS, 0, s>>>(p);
         break;
     default:
-        k_evict<EVICT_RANDOM><<<units, ETHREADS, 0, s>>>(p);
+        if (e.c.C <= RF_MAX_SLOTS) {
+            const int smem = (int)rf_smem_bytes(e.c.C);
+            const cudaError_t err = set_smem_once(reinterpret_cast<const void *>(k_evict_random),
+                                                  (int)rf_smem_bytes(RF_MAX_SLOTS));
+            if (err != cudaSuccess)
+                return err;
+            k_evict_random<<<units, RF_THREADS, smem, s>>>(p);
+        } else {
+            k_evict<EVICT_RANDOM><<<units, ETHREADS, 0, s>>>(p);
+        }
         break;
     }
     return cudaGetLastError();

@@ -83,6 +83,8 @@ cudaError_t launch_append_slots(const kvc_slot_cache &c, const uint16_t *k_new,
                                 const uint16_t *v_new, int n_new, cudaStream_t s);
 cudaError_t launch_append_quant(const kvc_quant_cache &c, const uint16_t *k_new,
                                 const uint16_t *v_new, int n_new, cudaStream_t s);
+cudaError_t launch_stream_append(const kvc_slot_cache &c, const uint16_t *k_new,
+                                 const uint16_t *v_new, int n_sink, int n_recent, cudaStream_t s);
 
 // Weights of the decode score update scores = keep * scores + add * p for a
 // decay of 0 (plain: 1, 1) or lambda in (0, 1) (lambda, 1 - lambda); false
