@@ -249,12 +249,20 @@ def run_gpu(args, rank, world):
         st.seqlen.copy_(tmp.seqlen)
         del tmp
         # KIVI-4: the prompt through the packer
-        Cq = 32 * ((T0 + S_total) // 32 + 1)
+        Cq = 32 * ((T0 + S_total + KIVI_AMORT_STEPS) // 32 + 1)
         kv4 = kvc.QuantCache.empty(B, Hkv, Cq, D, 4, w.kivi_R, device=dev)
         kvc.kvc_append_quant(kv4, K, V, stream=stream)
         # GEAR-4: the same prompt through the GEAR packer (its own rows, timed after the step)
         gear4 = kvc.QuantCache.empty(B, Hkv, Cq, D, 4, w.kivi_R, device=dev, gear=True)
         rows.update(pack_rows(kvc, dev, stream, kv4, gear4, K, V))
+        # KIVI-4's decode steps start on a group flush: the prompt is cut so that the token of
+        # the first timed step completes a group, so a window of K steps holds ceil(K / 32)
+        # flushes (one every 32 tokens, R1-R5) rather than possibly none
+        kv_shift = (T0 + args.warmup - w.kivi_R) % 32
+        Lk = T0 - 1 - kv_shift
+        kv4.len.zero_()
+        kvc.kvc_append_quant(kv4, K[:, :, :Lk].contiguous(), V[:, :, :Lk].contiguous(),
+                             stream=stream)
         del K, V
 
         # per-step inputs, resident in HBM (distinct for every step and method)
@@ -276,14 +284,13 @@ def run_gpu(args, rank, world):
         ws_kv, nb_kv = ws_for(kv4)
         # kernels per step: a one-token slot append is 1 launch, a KIVI append 2 (pack +
         # length), attention 1 (+1 combine with several splits; +1 score pass for H2O then),
-        # each eviction 1
+        # the H2O eviction 1; StreamingLLM's append takes the leaving token's slot (no eviction)
         launches_per_step = ((1 + 1 + (nb_fp > 0)) + (1 + 1 + 2 * (nb_h2o > 0) + 1) +
-                             (2 + 1 + (nb_kv > 0)) + (1 + 1 + (nb_st > 0) + 1))
+                             (2 + 1 + (nb_kv > 0)) + (1 + 1 + (nb_st > 0)))
         torch.cuda.synchronize(dev)
 
-    names = ["fp16_append", "fp16_attend", "h2o_append", "h2o_attend_accumulate", "h2o_unused",
-             "h2o_evict", "kivi4_append", "kivi4_attend", "stream_append", "stream_attend",
-             "stream_evict"]
+    names = ["fp16_append", "fp16_attend", "h2o_append", "h2o_attend_accumulate", "h2o_evict",
+             "kivi4_append", "kivi4_attend", "stream_append", "stream_attend"]
 
     def step(i, ev=None, outs_override=None):
         """One decode step of all four methods on the launch stream; ev: per-call events."""
@@ -299,13 +306,12 @@ def run_gpu(args, rank, world):
         # attention and the heavy-hitter score update in one launch (logits kept on chip)
         kvc.kvc_decode_attend(h2o, qs[i, 1], outs[1], lse=lse, workspace=ws_h2o,
                               h2o_scores=h2o_scores, stream=stream); mark(4)
-        mark(5)
-        kvc.kvc_h2o_evict(h2o, h2o_scores, n_heavy, n_recent, stream=stream); mark(6)
-        kvc.kvc_append_quant(kv4, kn[i, 2], vn[i, 2], stream=stream); mark(7)
-        kvc.kvc_decode_attend(kv4, qs[i, 2], outs[2], workspace=ws_kv, stream=stream); mark(8)
-        kvc.kvc_append(st, kn[i, 3], vn[i, 3], stream=stream); mark(9)
-        kvc.kvc_decode_attend(st, qs[i, 3], outs[3], workspace=ws_st, stream=stream); mark(10)
-        kvc.kvc_stream_evict(st, n_sink, n_recent, stream=stream); mark(11)
+        kvc.kvc_h2o_evict(h2o, h2o_scores, n_heavy, n_recent, stream=stream); mark(5)
+        kvc.kvc_append_quant(kv4, kn[i, 2], vn[i, 2], stream=stream); mark(6)
+        kvc.kvc_decode_attend(kv4, qs[i, 2], outs[2], workspace=ws_kv, stream=stream); mark(7)
+        # StreamingLLM: the leaving token's slot takes the new token; no eviction launch
+        kvc.kvc_stream_append(st, kn[i, 3], vn[i, 3], n_sink, n_recent, stream=stream); mark(8)
+        kvc.kvc_decode_attend(st, qs[i, 3], outs[3], workspace=ws_st, stream=stream); mark(9)
 
     branches = [torch.cuda.Stream(dev) for _ in range(4)]
 
@@ -327,9 +333,8 @@ def run_gpu(args, rank, world):
         kvc.kvc_h2o_evict(h2o, h2o_scores, n_heavy, n_recent, stream=s1)
         kvc.kvc_append_quant(kv4, kn[i, 2], vn[i, 2], stream=s2)
         kvc.kvc_decode_attend(kv4, qs[i, 2], outs[2], workspace=ws_kv, stream=s2)
-        kvc.kvc_append(st, kn[i, 3], vn[i, 3], stream=s3)
+        kvc.kvc_stream_append(st, kn[i, 3], vn[i, 3], n_sink, n_recent, stream=s3)
         kvc.kvc_decode_attend(st, qs[i, 3], outs[3], workspace=ws_st, stream=s3)
-        kvc.kvc_stream_evict(st, n_sink, n_recent, stream=s3)
         for bs in branches:
             join = torch.cuda.Event()
             join.record(bs)
@@ -377,7 +382,8 @@ def run_gpu(args, rank, world):
         s_end.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(args.steps)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+               for _ in range(args.steps)]
         for k in range(args.steps):
             step(args.warmup + 2 * args.steps + k, ev=evs[k])
         torch.cuda.synchronize(dev)
@@ -396,7 +402,8 @@ def run_gpu(args, rank, world):
     b_fp = [slot_bytes(t, B, Hkv, Hq, D) for t in steps_T]
     b_h2o = slot_bytes(513, B, Hkv, Hq, D)
     b_st = slot_bytes(513, B, Hkv, Hq, D)
-    b_kv = [kivi_bytes(t, w.kivi_R, B, Hkv, Hq, D, 4) for t in steps_T]
+    kv_T = [t - kv_shift for t in steps_T]   # KIVI-4 tokens attended (its prompt is shorter)
+    b_kv = [kivi_bytes(t, w.kivi_R, B, Hkv, Hq, D, 4) for t in kv_T]
     ms = lambda nm: sum(per_call[nm])
     slot_bytes_total = sum(b_fp) + b_h2o * args.steps + b_st * args.steps
     slot_ms = ms("fp16_attend") + ms("h2o_attend_accumulate") + ms("stream_attend")
@@ -426,13 +433,13 @@ def run_gpu(args, rank, world):
         "fp16": ms("fp16_append") + ms("fp16_attend"),
         "h2o512": ms("h2o_append") + ms("h2o_attend_accumulate") + ms("h2o_evict"),
         "kivi4": ms("kivi4_append") + ms("kivi4_attend"),
-        "stream512": ms("stream_append") + ms("stream_attend") + ms("stream_evict"),
+        "stream512": ms("stream_append") + ms("stream_attend"),
     }
     methods = {k: {"ms_per_step": v / args.steps, "tokens_per_s": B / (v / args.steps * 1e-3)}
                for k, v in methods.items()}
     for k, v in methods.items():
         v["speedup_vs_fp16"] = methods["fp16"]["ms_per_step"] / v["ms_per_step"]
-    calls = {nm: sum(v) / len(v) for nm, v in per_call.items() if nm != "h2o_unused"}
+    calls = {nm: sum(v) / len(v) for nm, v in per_call.items()}
 
     # ---------------- end to end: host buffers, copies inside the timed region.
     # Every step uploads its own queries and new K/V from pinned host memory and reads its
@@ -529,14 +536,16 @@ def run_gpu(args, rank, world):
     rows.update(paged_rows(kvc, dev, stream, fp, kv4, qs[0, 0], T0))
     rows.update(gear_rows(kvc, dev, stream, gear4, qs[:, 2], kn[:, 2], vn[:, 2], hbm_peak))
     del gear4
+    rows.update(kivi_amortized_rows(kvc, dev, stream, kv4, qs[:, 2], kn[:, 2], vn[:, 2], hbm_peak))
     rows.update(config_rows(kvc, W, dev, stream, hbm_peak))
 
     ms_per_step = total_ms / args.steps
-    eager_ms = evs[0][0].elapsed_time(evs[-1][11]) / args.steps
+    eager_ms = evs[0][0].elapsed_time(evs[-1][len(names)]) / args.steps
     # the whole timed step against the copy bandwidth: the four attention launches' bytes at
     # the timed steps' own cache lengths
     graph_T = [T0 + args.warmup + k for k in range(args.steps)]
-    step_bytes = (sum(slot_bytes(t, B, Hkv, Hq, D) + kivi_bytes(t, w.kivi_R, B, Hkv, Hq, D, 4)
+    step_bytes = (sum(slot_bytes(t, B, Hkv, Hq, D) +
+                      kivi_bytes(t - kv_shift, w.kivi_R, B, Hkv, Hq, D, 4)
                       for t in graph_T) / args.steps + b_h2o + b_st)
     step_roofline = {"bytes_per_step": step_bytes,
                      "gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
@@ -554,6 +563,9 @@ def run_gpu(args, rank, world):
         "launches_per_step": launches_per_step, "h2d": h2d, "d2h": d2h,
         "hbm_peak": hbm_peak, "peak_kind": peak_kind,
         "splits": {"fp16": nb_fp, "h2o": nb_h2o, "stream": nb_st, "kivi": nb_kv},
+        "kivi_window": {"first_timed_T": graph_T[0] - kv_shift,
+                        "flushes_in_timed_window":
+                            sum(1 for t in graph_T if (t - kv_shift - w.kivi_R) % 32 == 0)},
     }
     return res
 
@@ -607,6 +619,50 @@ def h2o_variant_rows(kvc, dev, stream, src, src_scores, qs, kn, vn, n_heavy, n_r
                                    f", evict when n >= {trig} (slots attended {budget + 1}.."
                                    f"{trig})")}
             del c, sc, ws
+    return out
+
+
+KIVI_AMORT_STEPS = 64   # two flushes of a 32-token group
+
+
+def kivi_amortized_rows(kvc, dev, stream, kv4, qs, kn, vn, hbm_peak):
+    """KIVI-4 decode with its periodic group flush amortised: KIVI_AMORT_STEPS consecutive
+    decode steps (append + attention; every 32nd append quantises and packs the group that
+    leaves the fp16 residual) captured in one CUDA graph and timed as a whole, so the per-step
+    figure carries exactly two flushes per 64 steps."""
+    import torch
+    B, Hkv, D, R = kv4.B, kv4.Hkv, kv4.D, kv4.R
+    Hq = qs.shape[2]
+    S = KIVI_AMORT_STEPS
+    out = {}
+    with torch.cuda.stream(stream):
+        o = torch.empty(B, Hq, D, dtype=torch.float16, device=dev)
+        ws = torch.empty(max(kvc.kvc_workspace_size(kv4, qs[0]) // 4, 1), dtype=torch.float32,
+                         device=dev)
+        T_start = int(kv4.len[0].item())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(S):
+                k = i % qs.shape[0]
+                kvc.kvc_append_quant(kv4, kn[k], vn[k], stream=stream)
+                kvc.kvc_decode_attend(kv4, qs[k], o, workspace=ws, stream=stream)
+        torch.cuda.synchronize(dev)
+        kv4.len.fill_(T_start)   # capture ran nothing; the replay appends S tokens
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        del g
+        ms = e0.elapsed_time(e1) / S
+        flushes = sum(1 for t in range(T_start + 1, T_start + S + 1) if (t - R) % 32 == 0)
+        nbytes = sum(kivi_bytes(t, R, B, Hkv, Hq, D, 4) for t in range(T_start + 1, T_start + S + 1)) / S
+    out["kivi4_decode_amortized"] = {
+        "ms_per_step": ms, "tokens_per_s": B / (ms * 1e-3), "steps": S, "flushes": flushes,
+        "attend_bytes_per_step": nbytes,
+        "step_gbs": nbytes / (ms * 1e-3) / 1e9, "step_frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+        "shape": f"B={B} GQA {Hq}/{Hkv} D={D}, T={T_start + 1}..{T_start + S}, R={R}: "
+                 f"append (+ group flush every 32 tokens) + attention, one CUDA graph"}
     return out
 
 
@@ -679,8 +735,8 @@ def gear_rows(kvc, dev, stream, gear4, qs, kn, vn, hbm_peak):
 def config_rows(kvc, W, dev, stream, hbm_peak):
     """Decode attention on the two MHA workloads (median of 5 after one warm-up, L2 flushed
     before each by a 512 MB write and a 512 MB read, as their compressed caches fit in L2):
-    llama7b-b8-h32-d128-t2048
-    (FP16 over T+1 slots; H2O-512 and StreamingLLM-512 over 513 slots) and
+    llama7b-b8-h32-d128-t2048 (FP16 over T+1 slots; H2O-512 from the prefill score pass and
+    StreamingLLM-512 from the prompt gather, each over 513 slots in its decode step) and
     kivi-b32-h32-d128-t4096 (FP16, KIVI-4 and KIVI-2 over T tokens)."""
     import torch
     flush = L2Flush(dev)
@@ -700,31 +756,113 @@ def config_rows(kvc, W, dev, stream, hbm_peak):
         return statistics.median(ts)
 
     with torch.cuda.stream(stream):
-        # ---- llama7b-b8-h32-d128-t2048: 32 MHA heads, 2% outlier channels in K and V
+        # ---- llama7b-b8-h32-d128-t2048: 32 MHA heads, 2% outlier channels in K and V.
+        # FP16 attends over the 2048-token prompt + the new token.  H2O-512: the prefill score
+        # pass over the 2048-token causal prompt (queries ~ N(0,1)), eviction to 64 heavy + 448
+        # recent, then the decode step append -> attention with the fused score update (logits
+        # on chip) -> eviction 513 -> 512.  StreamingLLM-512: the prompt gathered to 64 sinks +
+        # 448 recent, then the decode step kvc_stream_append -> attention.
         w = W.LLAMA7B
         B, Hq, Hkv, D, T = w.B, w.Hq, w.Hkv, w.D, w.T
         K, V = W.kv_tensors(w, T=T + 1, device=dev)
         q = W.q_tensor(w, device=dev)
         o = torch.empty_like(q)
-        for name, n in (("fp16", T + 1), ("h2o512", 513), ("stream512", 513)):
-            c = kvc.SlotCache.empty(B, Hkv, n + 7, D, device=dev)
-            kvc.kvc_append(c, K[:, :, :n].contiguous(), V[:, :, :n].contiguous(), stream=stream)
-            lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
-            sc = torch.zeros(B, Hkv, c.C, dtype=torch.float32, device=dev)
-            ws = torch.empty(max(kvc.kvc_workspace_size(c, q) // 4, 1), dtype=torch.float32,
-                             device=dev)
-            if name == "h2o512":
-                fn = lambda: kvc.kvc_decode_attend(c, q, o, lse=lse, num_splits=1, h2o_scores=sc,
-                                                   stream=stream)
-            else:
-                fn = lambda: kvc.kvc_decode_attend(c, q, o, workspace=ws, stream=stream)
-            ms = timed(fn)
-            nb = slot_bytes(n, B, Hkv, Hq, D)
-            out[f"{w.name}/{name}"] = {"ms": ms, "slots": n, "gbs": nb / (ms * 1e-3) / 1e9,
-                                       "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm_peak,
-                                       "tokens_per_s": B / (ms * 1e-3)}
-            del c, sc, ws
-        del K, V
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+        kn, vn = K[:, :, T:T + 1].contiguous(), V[:, :, T:T + 1].contiguous()
+        c = kvc.SlotCache.empty(B, Hkv, T + 8, D, device=dev)
+        kvc.kvc_append(c, K, V, stream=stream)
+        ws = torch.empty(max(kvc.kvc_workspace_size(c, q) // 4, 1), dtype=torch.float32, device=dev)
+        ms = timed(lambda: kvc.kvc_decode_attend(c, q, o, workspace=ws, stream=stream))
+        nb = slot_bytes(T + 1, B, Hkv, Hq, D)
+        out[f"{w.name}/fp16"] = {"ms": ms, "slots": T + 1, "gbs": nb / (ms * 1e-3) / 1e9,
+                                 "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm_peak,
+                                 "tokens_per_s": B / (ms * 1e-3)}
+        del c, ws
+        # the two compressed caches after the prompt (set-up, untimed)
+        full = kvc.SlotCache.empty(B, Hkv, T + 8, D, device=dev)
+        kvc.kvc_append(full, K[:, :, :T].contiguous(), V[:, :, :T].contiguous(), stream=stream)
+        qp = W.q_tensor(w, L=T, device=dev)
+        sc_full = torch.zeros(B, Hkv, T + 8, dtype=torch.float32, device=dev)
+        pws = torch.empty(kvc.kvc_h2o_workspace_size(B, Hq, T) // 4, dtype=torch.float32,
+                          device=dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush()
+        e0.record(stream)
+        kvc.kvc_h2o_accumulate_prefill(qp, full.K, sc_full, pws, T, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        pre_ms = e0.elapsed_time(e1)
+        del qp, pws
+        pos0, K0, V0, n0, sl0 = (full.pos.clone(), full.K.clone(), full.V.clone(), full.n.clone(),
+                                 full.seqlen.clone())
+        kvc.kvc_h2o_evict(full, sc_full, w.n_heavy, w.n_recent, stream=stream)
+        Ch = 520
+        h2o0 = {"K": full.K[:, :, :Ch].clone(), "V": full.V[:, :, :Ch].clone(),
+                "pos": full.pos[:, :, :Ch].clone(), "n": full.n.clone(), "seqlen": full.seqlen.clone(),
+                "sc": sc_full[:, :, :Ch].clone()}
+        full.pos.copy_(pos0); full.K.copy_(K0); full.V.copy_(V0); full.n.copy_(n0)
+        full.seqlen.copy_(sl0)
+        del pos0, K0, V0, n0, sl0, sc_full
+        kvc.kvc_stream_evict(full, w.n_sink, w.n_recent, stream=stream)
+        st0 = {"K": full.K[:, :, :Ch].clone(), "V": full.V[:, :, :Ch].clone(),
+               "pos": full.pos[:, :, :Ch].clone(), "n": full.n.clone(), "seqlen": full.seqlen.clone()}
+        del full
+        hc = kvc.SlotCache.empty(B, Hkv, Ch, D, device=dev)
+        hsc = torch.zeros(B, Hkv, Ch, dtype=torch.float32, device=dev)
+        stc = kvc.SlotCache.empty(B, Hkv, Ch, D, device=dev)
+        ws_h = torch.empty(max(kvc.kvc_workspace_size(hc, q) // 4, 1), dtype=torch.float32,
+                           device=dev)
+
+        def reset_h2o():
+            for k_ in ("K", "V", "pos", "n", "seqlen"):
+                getattr(hc, k_).copy_(h2o0[k_])
+            hsc.copy_(h2o0["sc"])
+
+        def reset_st():
+            for k_ in ("K", "V", "pos", "n", "seqlen"):
+                getattr(stc, k_).copy_(st0[k_])
+
+        def step_times(reset, launches):
+            """Median over 5 repetitions (one warm-up) of each launch of the step, the cache
+            reset and L2 flushed before each repetition."""
+            ts = [[] for _ in launches]
+            for r in range(6):
+                reset()
+                flush()
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
+                evs[0].record(stream)
+                for j, fn in enumerate(launches):
+                    fn()
+                    evs[j + 1].record(stream)
+                evs[-1].synchronize()
+                if r > 0:
+                    for j in range(len(launches)):
+                        ts[j].append(evs[j].elapsed_time(evs[j + 1]))
+            return [statistics.median(t) for t in ts]
+
+        t_app, t_att, t_ev = step_times(reset_h2o, [
+            lambda: kvc.kvc_append(hc, kn, vn, stream=stream),
+            lambda: kvc.kvc_decode_attend(hc, q, o, lse=lse, workspace=ws_h, h2o_scores=hsc,
+                                          stream=stream),
+            lambda: kvc.kvc_h2o_evict(hc, hsc, w.n_heavy, w.n_recent, stream=stream)])
+        nb = slot_bytes(513, B, Hkv, Hq, D)
+        out[f"{w.name}/h2o512"] = {
+            "ms": t_att, "slots": 513, "gbs": nb / (t_att * 1e-3) / 1e9,
+            "frac_of_hbm": nb / (t_att * 1e-3) / 1e9 / hbm_peak, "tokens_per_s": B / (t_att * 1e-3),
+            "step_ms": t_app + t_att + t_ev, "append_ms": t_app, "evict_ms": t_ev,
+            "prefill_score_pass_ms": pre_ms,
+            "cache": "prefill scores of the 2048-token causal prompt, evicted to 64 heavy + "
+                     "448 recent; step: append, attention + fused score update, 513 -> 512"}
+        t_app, t_att = step_times(reset_st, [
+            lambda: kvc.kvc_stream_append(stc, kn, vn, w.n_sink, w.n_recent, stream=stream),
+            lambda: kvc.kvc_decode_attend(stc, q, o, workspace=ws_h, stream=stream)])
+        out[f"{w.name}/stream512"] = {
+            "ms": t_att, "slots": 513, "gbs": nb / (t_att * 1e-3) / 1e9,
+            "frac_of_hbm": nb / (t_att * 1e-3) / 1e9 / hbm_peak, "tokens_per_s": B / (t_att * 1e-3),
+            "step_ms": t_app + t_att, "append_ms": t_app,
+            "cache": "the prompt gathered to 64 sinks + 448 recent; step: kvc_stream_append "
+                     "(the leaving token's slot), attention over 513"}
+        del hc, hsc, stc, ws_h, h2o0, st0, K, V
         # ---- kivi-b32-h32-d128-t4096: offsets U(-2, 2) on Q, K, V
         w = W.KIVI_MHA
         B, Hq, Hkv, D, T = w.B, w.Hq, w.Hkv, w.D, w.T
@@ -1017,6 +1155,20 @@ def run_profile(args):
         ws = torch.empty(kvc.kvc_h2o_workspace_size(kp.shape[0], Hq, L) // 4, device=dev)
         for _ in range(3):
             kvc.kvc_h2o_accumulate_prefill(qp, kp, sc, ws, L)
+    elif what == "stream_append":
+        # the heavy-load StreamingLLM-512 decode append: 512 slots of sinks + recent window,
+        # then three one-token appends (the first grows the window to 513, the next two
+        # overwrite the slot of the token that leaves it)
+        cache = kvc.SlotCache.empty(B, Hkv, 520, D, device=dev)
+        kvc.kvc_append(cache, K[:, :, :T - 1].contiguous()[:, :, :512].contiguous(),
+                       V[:, :, :512].contiguous())
+        cache.pos[:, :, :512] = torch.cat([torch.arange(w.n_sink),
+                                           torch.arange(T - 1 - w.n_recent, T - 1)]).int().to(dev)
+        cache.seqlen.fill_(T - 1)
+        for i in range(3):
+            kvc.kvc_stream_append(cache, K[:, :, T - 1 + i - 2:T - 1 + i - 1].contiguous(),
+                                  V[:, :, T - 1 + i - 2:T - 1 + i - 1].contiguous(), w.n_sink,
+                                  w.n_recent)
     elif what == "random_evict":
         # reasoning-trace steady state (epoch 30): 1024 locked prompt tokens, 341 kept earlier
         # tokens, 1024 new ones -> 1365 per head after the eviction; --profile-batch sequences
@@ -1197,9 +1349,8 @@ def run_grid(args):
                 ws_s = ws_for(fp, q)
 
                 def stream_step():
-                    kvc.kvc_append(fp, kn, vn, stream=stream)
+                    kvc.kvc_stream_append(fp, kn, vn, n_sink, n_recent, stream=stream)
                     kvc.kvc_decode_attend(fp, q, o, workspace=ws_s, stream=stream)
-                    kvc.kvc_stream_evict(fp, n_sink, n_recent, stream=stream)
                 cell["decode_ms"]["stream512"] = timed(stream_step)
                 cell["slots_attended"]["stream512"] = n_sink + n_recent + 1
                 # ---- H2O: two-pass prefill score pass (in batch chunks of <= 8 GB of queries)
@@ -1283,7 +1434,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None,
                     help="run one kernel on a small case for ncu: attend_fp16, attend_h2o, "
-                         "attend_kivi4, attend_gear4, h2o_evict, stream_evict, prefill, kivi_pack, gear_pack")
+                         "attend_kivi4, attend_gear4, attend_kivi2_mha, attend_kivi4_mha, "
+                         "h2o_evict, stream_evict, stream_append, random_evict, prefill, "
+                         "kivi_pack, gear_pack, kivi_append_flush, gear_append_flush")
     ap.add_argument("--profile-batch", type=int, default=64)
     ap.add_argument("--grid", action="store_true",
                     help="throughput profile grid over batch x KV length x method (JSON lines)")
@@ -1355,7 +1508,17 @@ def main():
                          "achieved": dom["gbs"], "peak": res["hbm_peak"], "unit": "GB/s",
                          "frac": dom["frac_of_hbm"], "traffic": res["fp16_traffic"],
                          "algorithmic_bytes": dom["bytes_per_step"],
-                         "peak_source": res["peak_kind"]},
+                         "peak_source": res["peak_kind"],
+                         # the compressed decode-attention launches of the same step
+                         "compressed": {
+                             nm: {"kernel": kn_, "achieved": res["kernels"][k]["gbs"],
+                                  "frac": res["kernels"][k]["frac_of_hbm"],
+                                  "algorithmic_bytes": res["kernels"][k]["bytes_per_step"]}
+                             for nm, k, kn_ in (
+                                 ("h2o512", "attend_h2o512",
+                                  "k_attend_slots (H2O-512, fused score update)"),
+                                 ("stream512", "attend_stream512", "k_attend_slots (Stream-512)"),
+                                 ("kivi4", "attend_kivi4", "k_attend_kivi (KIVI-4)"))}},
             "cpu_baseline": cpu,
             "clocks": res["clocks"],
             "kernels": res["kernels"], "methods": res["methods"], "rows": res["rows"],
@@ -1363,6 +1526,7 @@ def main():
             "serial_ms_per_step": res["serial_ms_per_step"],
             "step_roofline": res["step_roofline"],
             "device_status": res["device_status"],
+            "kivi_window": res["kivi_window"],
         }
         print(json.dumps(line))
 

@@ -310,9 +310,11 @@ KVC_API kvc_status kvc_decode_attend(const kvc_attend_args *args, cudaStream_t s
  * by every GPU that loads the library until the process exits).  The call
  * allocates nothing.  Arguments whose kvc_workspace_size exceeds
  * KVC_NOALLOC_SCRATCH_BYTES are rejected with KVC_ERR_WORKSPACE.
- * The first call on a device looks up that array's device address
- * (cudaGetSymbolAddress) with the device current; make that first call before
- * any stream capture.  All calls on a device share the array, so calls whose
+ * The first call on a device that needs scratch looks up that array's device
+ * address (cudaGetSymbolAddress) with the device current and keeps it; make
+ * that first call before any stream capture.  The kept address belongs to the
+ * device code loaded at that time: do not call this entry point after a
+ * cudaDeviceReset.  All calls on a device share the array, so calls whose
  * kernels may overlap on the GPU (unordered streams) race; order them.
  */
 KVC_API kvc_status kvc_decode_attend_noalloc(const kvc_attend_args *args, cudaStream_t stream);

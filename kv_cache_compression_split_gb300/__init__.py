@@ -209,11 +209,13 @@ def kvc_decode_attend(cache, q, o, logits=None, lse=None, workspace=None, num_sp
 
 
 def kvc_decode_attend_noalloc(cache, q, o, logits=None, lse=None, num_splits: int = 0,
-                              softmax_scale: float = 0.0, stream=None):
+                              softmax_scale: float = 0.0, h2o_scores=None, h2o_decay: float = 0.0,
+                              stream=None):
     """kvc_decode_attend without a caller workspace: for callers that cannot allocate device
     memory on their decode path, the split scratch comes from a fixed array the library owns
     (KVC_NOALLOC_SCRATCH_BYTES per GPU).  Calls that may overlap on the GPU race on it."""
-    a, _keep = _attend_args(cache, q, o, logits, lse, None, num_splits, softmax_scale)
+    a, _keep = _attend_args(cache, q, o, logits, lse, None, num_splits, softmax_scale,
+                            h2o_scores, h2o_decay)
     _check(lib().kvc_decode_attend_noalloc(C.byref(a), _stream(stream)),
            "kvc_decode_attend_noalloc")
 

@@ -139,7 +139,7 @@ bool encode_tmap_2d_f16(CUtensorMap *map, const void *base, uint64_t inner, uint
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested)
+SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested, int max_splits)
 {
     SlotAttendPlan pl{1, tiles_per_unit > 0 ? tiles_per_unit : 1};
     if (tiles_per_unit <= 0)
@@ -148,12 +148,22 @@ SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested)
     if (requested > 0) {
         S = requested < tiles_per_unit ? requested : tiles_per_unit;
     } else {
-        const double slots = 2.0 * sm_count();
+        // Cost in tile-times (one SM streaming one tile at its share of HBM bandwidth):
+        // the whole cache at the full-chip rate, or the busiest SM's CTAs one after another
+        // (one CTA already draws about an SM's share), plus ~1.5 per round of two resident
+        // CTAs per SM for a CTA's start and merge, plus 2 for merging split partials.
+        // Measured on the LLaMA-7B, reasoning-trace and heavy-load shapes: 128 or more
+        // units run fastest unsplit; a few long units need splits to fill the SMs.
+        const double sms = (double)sm_count();
         double best = 1e300;
-        const int smax = tiles_per_unit < 64 ? tiles_per_unit : 64;
+        int smax = tiles_per_unit < 64 ? tiles_per_unit : 64;
+        if (smax > max_splits)
+            smax = max_splits > 0 ? max_splits : 1;
         for (int s = 1; s <= smax; ++s) {
-            const double waves = ceil(units * (double)s / slots);
-            const double cost = waves * (ceil(tiles_per_unit / (double)s) + 1.5) + (s > 1 ? 0.5 : 0.0);
+            const double ctas = (double)units * s;
+            const double per_cta = ceil(tiles_per_unit / (double)s);
+            const double stream = fmax((double)units * tiles_per_unit / sms, ceil(ctas / sms) * per_cta);
+            const double cost = stream + 1.5 * ceil(ctas / (2.0 * sms)) + (s > 1 ? 2.0 : 0.0);
             if (cost < best - 1e-9) {
                 best = cost;
                 S = s;
@@ -221,6 +231,7 @@ struct AttendPlanFull {
     kvc_status st;
     int B, Hkv, D;
     SlotAttendPlan plan;
+    bool cluster;   // slot caches: 2..8 splits merged in a thread-block cluster
     size_t ws;
 };
 
@@ -239,19 +250,33 @@ AttendPlanFull plan_full(const kvc_attend_args *a)
         f.Hkv = a->slots->Hkv;
         f.D = a->slots->D;
         const int tiles = (a->slots->C + TILE - 1) / TILE;
-        int splits = a->num_splits;
-        if (a->h2o_scores && !a->logits) {   // fused H2O with the logits on chip
-            if (splits > 1)
+        const int splits = a->num_splits;
+        if (splits < 0)
+            return f;
+        if (a->h2o_scores && !a->logits) {
+            // fused H2O with the logits on chip: every split keeps at most
+            // H2O_ONCHIP_MAX_SLOTS logits and the splits merge in one cluster
+            const int tmax = H2O_ONCHIP_MAX_SLOTS / TILE;
+            const int need = (tiles + tmax - 1) / tmax;
+            if (splits > SLOT_CLUSTER_MAX)
                 return f;
-            if (a->slots->C > H2O_ONCHIP_MAX_SLOTS) {
+            if (need > SLOT_CLUSTER_MAX || (splits > 0 && (tiles + splits - 1) / splits > tmax)) {
                 f.st = KVC_ERR_UNSUPPORTED;
                 return f;
             }
-            splits = 1;
+            f.plan = plan_attend(f.B * f.Hkv, tiles, splits, SLOT_CLUSTER_MAX);
+            if (f.plan.tiles_per_split > tmax)
+                f.plan = plan_attend(f.B * f.Hkv, tiles, need);
+        } else {
+            f.plan = plan_attend(f.B * f.Hkv, tiles, splits);
         }
-        f.plan = plan_attend(f.B * f.Hkv, tiles, splits);
-        f.ws = f.plan.splits > 1 ? (size_t)f.B * a->Hq * f.plan.splits * (f.D + 2) * sizeof(float)
-                                 : 0;
+        // the fused H2O update merges its splits inside their cluster (the logits stay with
+        // the CTA that computed them); plain attention merges through the workspace, which
+        // measured as fast or faster for 2-4 splits of small batches
+        f.cluster = a->h2o_scores && f.plan.splits > 1 && f.plan.splits <= SLOT_CLUSTER_MAX;
+        f.ws = f.plan.splits > 1 && !f.cluster
+                   ? (size_t)f.B * a->Hq * f.plan.splits * (f.D + 2) * sizeof(float)
+                   : 0;
     } else if (a->kind == KVC_KIND_KIVI) {
         if (check_quant_cache(a->quant) != KVC_OK) {
             f.st = check_quant_cache(a->quant);
@@ -361,9 +386,9 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         float *part_ml = part_o ? part_o + (size_t)f.B * a->Hq * f.plan.splits * f.D : nullptr;
         AttendLaunch L{f.B, a->Hq, c.Hkv, c.D, c.C, a->q, a->o, c.K, c.V, c.n, a->logits, a->lse,
                        part_o, part_ml, f.plan.splits, f.plan.tiles_per_split, scale,
-                       a->h2o_scores, h2o_keep, h2o_add, c.block_table, c.num_pages};
+                       a->h2o_scores, h2o_keep, h2o_add, f.cluster, c.block_table, c.num_pages};
         cudaError_t e = launch_attend_slots(L, stream);
-        if (e != cudaSuccess || !a->h2o_scores || f.plan.splits == 1)
+        if (e != cudaSuccess || !a->h2o_scores || f.plan.splits == 1 || f.cluster)
             return from_cuda(e);
         // several splits: the probabilities need the combined lse first
         kvc_h2o_args h{};

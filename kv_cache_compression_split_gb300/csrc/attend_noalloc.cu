@@ -15,12 +15,16 @@
 // Every GPU that loads the library holds it until the process exits.  Its
 // host-side name is only a stand-in for the symbol, so the host looks up the
 // real device address with cudaGetSymbolAddress once per device (with that
-// device current) on the first call and passes that address to the kernels.
-// Every call on a device shares the array: two calls whose kernels overlap
-// on the GPU (different streams without ordering) race on it.  Each call
-// overwrites every scratch word it reads, so nothing has to be cleared.
+// device current) on the first call that needs scratch, and passes that
+// address to the kernels; later calls read the cached address without taking
+// the lock.  A cudaDeviceReset unloads the module the address belongs to, so
+// the entry point must not be used after one.  Every call on a device shares
+// the array: two calls whose kernels overlap on the GPU (different streams
+// without ordering) race on it.  Each call overwrites every scratch word it
+// reads, so nothing has to be cleared.
 #include "kvc_internal.h"
 
+#include <atomic>
 #include <mutex>
 
 namespace kvc {
@@ -29,7 +33,7 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KVC_NOALLOC_SCRATCH_BYTES];
 
 constexpr int MAX_DEVICES = 64;
-void *g_scratch_addr[MAX_DEVICES];
+std::atomic<void *> g_scratch_addr[MAX_DEVICES];
 std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device (nullptr on failure).
@@ -38,14 +42,17 @@ void *scratch_address()
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
         return nullptr;
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
+    void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (p)
+        return p;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);   // first call on this device: set-up
+    p = g_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess)
             return nullptr;
-        g_scratch_addr[dev] = p;
+        g_scratch_addr[dev].store(p, std::memory_order_release);
     }
-    return g_scratch_addr[dev];
+    return p;
 }
 
 } // namespace

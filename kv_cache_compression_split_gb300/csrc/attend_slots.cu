@@ -11,8 +11,14 @@
 //   O^T += V_tile^T P^T       (D x 8 heads, fp32; P^T is the S^T fragment
 //                              transposed in registers with movmatrix)
 // The four warps' (m, l, O) are merged through shared memory at the end.
-// With one split the CTA writes o and lse directly; otherwise it writes a
-// partial (m, l, unnormalised O) that the combine kernel merges.
+// With one split the CTA writes o and lse directly.  With several splits each
+// CTA writes its partial (m, l, unnormalised O) to a workspace that the combine
+// kernel merges -- except for the fused H2O score update with 2..8 splits: then
+// the splits of a unit form one thread-block cluster, each CTA leaves its
+// partial in its shared memory, and after a cluster barrier the CTAs read each
+// other's partials through distributed shared memory, write o and lse, and
+// fold their own tokens' probabilities (logits still on chip) into the scores,
+// all in one launch.
 //
 // Method: scaled dot-product attention of one decode query over the kept
 // cache ("Rethinking KV Cache Compression" guide, §16 "Prefill、decode、TP 的
@@ -48,7 +54,11 @@ template <int D, int LMODE = LM_NONE> struct SlotCfg {
     static constexpr int LSM_BYTES = LSM ? 8 * LSM_SLOTS * 4 : 0;
     static constexpr int SMEM = NSTAGE * STAGE_BYTES + LSM_BYTES + 1024 + 2 * NSTAGE * 8;
     static_assert(NCW * (8 * D + 16) * 4 <= NSTAGE * STAGE_BYTES, "combine scratch must fit");
+    // this CTA's merged partial for the cluster merge, after the warps' scratch
+    static constexpr int CP_OFF = NCW * (8 * D + 16) * 4;
+    static_assert(CP_OFF + (8 * D + 16) * 4 <= NSTAGE * STAGE_BYTES, "cluster partial must fit");
 };
+constexpr int MAX_CLUSTER = 8;   // portable thread-block cluster size
 
 struct SlotParams {
     int Hq, Hkv, C, g;
@@ -59,7 +69,8 @@ struct SlotParams {
     float *logits, *lse;
     float *part_o, *part_ml;
     float scale, scale_log2;
-    float *h2o_scores;              // optional: add this step's probabilities (one split)
+    int cluster;                    // > 1: the splits of a unit are one cluster, merged on chip
+    float *h2o_scores;              // optional: add this step's probabilities (fused update)
     float h2o_keep, h2o_add;        // scores = keep * scores + add * p
     SlotRows rows;                  // dense or paged K / V rows
     int *status;
@@ -139,6 +150,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 }
             }
         }
+        __syncwarp();
+        if (p.cluster > 1) {   // the consumers' two cluster barriers
+            cluster_sync_all();
+            cluster_sync_all();
+        }
         return;
     }
 
@@ -166,6 +182,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
     const int h0 = 2 * c, h1 = 2 * c + 1;
     float *lg0 = nullptr, *lg1 = nullptr;
+    const int lofs = LSM ? t_begin : 0;   // the shared-memory logits hold this split's tokens
     if (LSM) {
         lg0 = h0 < p.g ? lsm + h0 * LSM_SLOTS : nullptr;
         lg1 = h1 < p.g ? lsm + h1 * LSM_SLOTS : nullptr;
@@ -203,12 +220,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             const int ta = tok0 + r, tb = tok0 + r + 8;
             const bool va = ta < t_end, vb = tb < t_end;
             if (lg0) {
-                if (va) lg0[ta] = sa[0] * p.scale;
-                if (vb) lg0[tb] = sa[2] * p.scale;
+                if (va) lg0[ta - lofs] = sa[0] * p.scale;
+                if (vb) lg0[tb - lofs] = sa[2] * p.scale;
             }
             if (lg1) {
-                if (va) lg1[ta] = sa[1] * p.scale;
-                if (vb) lg1[tb] = sa[3] * p.scale;
+                if (va) lg1[ta - lofs] = sa[1] * p.scale;
+                if (vb) lg1[tb - lofs] = sa[3] * p.scale;
             }
             const float x0 = va ? sa[0] * p.scale_log2 : -INFINITY;
             const float x1 = va ? sa[1] * p.scale_log2 : -INFINITY;
@@ -312,7 +329,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         }
     }
     consumer_bar();
-    const bool single = (p.part_o == nullptr);
+    const bool clustered = p.cluster > 1;
+    const bool single = !clustered && p.part_o == nullptr;
+    float *cp_o = reinterpret_cast<float *>(smem + Cfg::CP_OFF);   // [8][D] cluster partial
+    float *cp_ml = cp_o + 8 * D;                                    // [8][2] max (log2), sum
     for (int e = threadIdx.x; e < p.g * D; e += NCW * 32) {
         const int h = e / D, d = e % D;
         float ms = -INFINITY;
@@ -327,7 +347,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             ls += sc * redL[w * 8 + h];
             os += sc * redO[(w * 8 + h) * D + d];
         }
-        if (single) {
+        if (clustered) {
+            cp_o[h * D + d] = os;
+            if (d == 0) {
+                cp_ml[2 * h] = ls > 0.f ? ms : -INFINITY;
+                cp_ml[2 * h + 1] = ls;
+            }
+        } else if (single) {
             const size_t oi = ((size_t)b * p.Hq + hk * p.g + h) * D + d;
             p.o[oi] = __half_as_ushort(__float2half_rn(ls > 0.f ? os / ls : 0.f));
             if (d == 0 && p.lse)
@@ -342,11 +368,47 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             }
         }
     }
-    if (single && p.h2o_scores) {
-        // H2O decode scores: score[j] += sum_h exp(logit_hj - lse_h) over this unit's
-        // query heads (logits written above by this CTA; log2 domain here)
-        __shared__ float s_lse2[8];
+    __shared__ float s_lse2[8];   // log2-domain lse per head (H2O epilogue)
+    if (clustered) {
+        // merge the cluster's partials: split s has weight 2^(m_s - M) in head h
+        __shared__ float s_w[8][MAX_CLUSTER], s_l[8];
+        __syncwarp();
+        cluster_sync_all();   // every CTA's partial is written and visible
         if (threadIdx.x < p.g) {
+            const int h = threadIdx.x;
+            float mm = -INFINITY;
+            for (int r = 0; r < p.cluster; ++r)
+                mm = fmaxf(mm, ld_cluster_f32(cp_ml + 2 * h, r));
+            float ls = 0.f;
+            for (int r = 0; r < p.cluster; ++r) {
+                const float m = ld_cluster_f32(cp_ml + 2 * h, r);
+                const float w = m == -INFINITY ? 0.f : ex2(m - mm);
+                s_w[h][r] = w;
+                ls += w * ld_cluster_f32(cp_ml + 2 * h + 1, r);
+            }
+            s_l[h] = ls;
+            s_lse2[h] = ls > 0.f ? mm + __log2f(ls) : INFINITY;
+            if (split == 0 && p.lse)
+                p.lse[(size_t)b * p.Hq + hk * p.g + h] =
+                    ls > 0.f ? (mm + __log2f(ls)) * LN2 : -INFINITY;
+        }
+        consumer_bar();
+        for (int e = split * NCW * 32 + threadIdx.x; e < p.g * D; e += p.cluster * NCW * 32) {
+            const int h = e / D, d = e % D;
+            float os = 0.f;
+            for (int r = 0; r < p.cluster; ++r)
+                if (s_w[h][r] != 0.f)
+                    os += s_w[h][r] * ld_cluster_f32(cp_o + h * D + d, r);
+            const size_t oi = ((size_t)b * p.Hq + hk * p.g + h) * D + d;
+            p.o[oi] = __half_as_ushort(__float2half_rn(s_l[h] > 0.f ? os / s_l[h] : 0.f));
+        }
+        __syncwarp();
+        cluster_sync_all();   // no CTA leaves while another still reads its partial
+    }
+    if ((single || clustered) && p.h2o_scores) {
+        // H2O decode scores: score[j] += sum_h exp(logit_hj - lse_h) over this unit's
+        // query heads, for this CTA's tokens (logits kept by this CTA; log2 domain here)
+        if (!clustered && threadIdx.x < p.g) {
             const int h = threadIdx.x;
             float ms = -INFINITY;
 #pragma unroll
@@ -396,7 +458,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const size_t lstride = LSM ? LSM_SLOTS : p.C;
         // four slots per thread per round, every load issued before any is used
         constexpr int U = 4;
-        for (int j0 = threadIdx.x; j0 < t_end; j0 += U * NCW * 32) {
+        for (int j0 = t_begin + threadIdx.x; j0 < t_end; j0 += U * NCW * 32) {
             float add[U], old[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -411,7 +473,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int j = j0 + u * NCW * 32;
-                    lg[h][u] = h < p.g && j < t_end ? lrow[(size_t)h * lstride + j] : 0.f;
+                    lg[h][u] = h < p.g && j < t_end ? lrow[(size_t)h * lstride + (j - lofs)] : 0.f;
                 }
 #pragma unroll
             for (int h = 0; h < 8; ++h)
@@ -467,8 +529,24 @@ cudaError_t launch_slots_impl(const CUtensorMap &tk, const CUtensorMap &tv, cons
         set_smem_once(reinterpret_cast<const void *>(k_attend_slots<D, LMODE>), Cfg::SMEM);
     if (e != cudaSuccess)
         return e;
-    k_attend_slots<D, LMODE><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
-    return cudaGetLastError();
+    if (sp.cluster <= 1) {
+        k_attend_slots<D, LMODE><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
+        return cudaGetLastError();
+    }
+    // the splits of a unit (consecutive blocks) form one cluster
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = sp.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_attend_slots<D, LMODE>, tk, tv, sp);
 }
 
 } // namespace
@@ -492,24 +570,31 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
     sp.q = a.q;
     sp.o = a.o;
     sp.n = a.n;
+    // one split, or 2..8 splits merged in their cluster: o, lse and the fused H2O update in
+    // this launch; more splits: partials to the workspace, merged by the combine kernel
+    const bool on_chip = a.splits == 1 || a.cluster;
+    if (a.cluster && (a.splits < 2 || a.splits > MAX_CLUSTER))
+        return cudaErrorInvalidValue;
     sp.logits = a.logits;
-    sp.lse = a.splits == 1 ? a.lse : nullptr;
-    sp.part_o = a.splits == 1 ? nullptr : a.part_o;
-    sp.part_ml = a.splits == 1 ? nullptr : a.part_ml;
+    sp.lse = on_chip ? a.lse : nullptr;
+    sp.part_o = on_chip ? nullptr : a.part_o;
+    sp.part_ml = on_chip ? nullptr : a.part_ml;
     sp.scale = a.scale;
     sp.scale_log2 = a.scale * LOG2E;
-    sp.h2o_scores = a.splits == 1 ? a.h2o_scores : nullptr;
+    sp.cluster = a.cluster ? a.splits : 1;
+    sp.h2o_scores = on_chip ? a.h2o_scores : nullptr;
     sp.h2o_keep = a.h2o_keep;
     sp.h2o_add = a.h2o_add;
     sp.rows = SlotRows{a.block_table, a.C, a.num_pages};
     sp.status = dev_status_ptr();
     const int grid = units * a.splits;
-    // fused H2O without a logits array: the logits stay in shared memory (one split,
-    // C <= LSM_SLOTS, checked by the caller)
+    // fused H2O without a logits array: each CTA keeps its split's logits on chip (in
+    // registers up to LREG_TILES tiles, else in shared memory, at most LSM_SLOTS; checked
+    // by the caller)
     const bool lsm = a.h2o_scores && !a.logits;
-    if (lsm && (a.splits != 1 || a.C > LSM_SLOTS))
+    if (lsm && (!on_chip || a.tiles_per_split * TILE > LSM_SLOTS))
         return cudaErrorInvalidValue;
-    const int lmode = !lsm ? LM_NONE : (a.C <= LREG_TILES * TILE ? LM_REGS : LM_SMEM);
+    const int lmode = !lsm ? LM_NONE : (a.tiles_per_split <= LREG_TILES ? LM_REGS : LM_SMEM);
     cudaError_t e;
     if (a.D == 128)
         e = lmode == LM_REGS   ? launch_slots_impl<128, LM_REGS>(tk, tv, sp, grid, s)
@@ -519,7 +604,7 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
         e = lmode == LM_REGS   ? launch_slots_impl<64, LM_REGS>(tk, tv, sp, grid, s)
             : lmode == LM_SMEM ? launch_slots_impl<64, LM_SMEM>(tk, tv, sp, grid, s)
                                : launch_slots_impl<64, LM_NONE>(tk, tv, sp, grid, s);
-    if (e != cudaSuccess || a.splits == 1)
+    if (e != cudaSuccess || on_chip)
         return e;
     return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);
 }

@@ -601,17 +601,20 @@ __global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams 
 // once.  The n_keep-th smallest (key, pos) is found with one 2048-bin histogram
 // of the top 11 key bits: bins below the crossing bin are kept whole, bins above
 // are dropped, and the few members of the crossing bin are ranked against each
-// other exactly.  The compaction then moves all rows at once, 16-byte chunks
-// spread over the whole CTA with four loads in flight per thread.
+// other exactly.  The compaction then moves all rows at once, a warp per row
+// pair (16-byte chunks per lane) with eight pairs in flight per warp.
 // ------------------------------------------------------------------------
 constexpr int RF_THREADS = 1024;
 constexpr int RF_WARPS = RF_THREADS / 32;
 constexpr int RF_BINS = 2048;                 // top 11 key bits
 constexpr int RF_SHIFT = 64 - 11;
 constexpr int RF_MAX_SLOTS = 8192;            // u16 slot indices, one keep word per thread
-constexpr int RF_UNROLL = 4;                  // row chunks in flight per thread
+constexpr int RF_UNROLL = 8;                  // moved rows in flight per warp
 
 __host__ __device__ constexpr size_t rf_align(size_t x) { return (x + 15) & ~(size_t)15; }
+
+constexpr int RF_MISC = 128;                  // ints: two scans' scratch, then scalars
+constexpr int RF_SCAN_A = 0, RF_SCAN_B = 48, RF_SCALARS = 96;
 
 // Shared-memory carve-up for capacity C (bytes); the layout below must match.
 __host__ __device__ constexpr size_t rf_smem_bytes(int C)
@@ -620,12 +623,13 @@ __host__ __device__ constexpr size_t rf_smem_bytes(int C)
            + rf_align((size_t)C * 4)                        // positions
            + rf_align((size_t)((C + 31) / 32) * 4)          // keep bitmask
            + rf_align((size_t)(C + 2) * 2)                  // bucket list / hole + tail lists
-           + (size_t)RF_BINS * 4                            // histogram
-           + 64 * 4;                                        // scan scratch + scalars
+           + (size_t)RF_BINS * 4                            // histogram, then word lists
+           + RF_MISC * 4;                                   // scan scratch + scalars
 }
 
 // Exclusive scan of one int per thread over the 1024-thread CTA; *total gets the
-// sum.  `wsum` holds RF_WARPS ints.  All threads must call it.
+// sum.  `wsum` holds RF_WARPS + 1 ints that no other scan uses before the next
+// barrier.  All threads must call it.
 __device__ __forceinline__ int rf_scan(int v, int *total, int *wsum)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -640,7 +644,7 @@ __device__ __forceinline__ int rf_scan(int v, int *total, int *wsum)
         wsum[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int t = wsum[lane];
+        const int t = wsum[lane];
         int ti = t;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -653,10 +657,8 @@ __device__ __forceinline__ int rf_scan(int v, int *total, int *wsum)
             wsum[RF_WARPS] = ti;     // grand total
     }
     __syncthreads();
-    const int r = wsum[warp] + x - v;
     *total = wsum[RF_WARPS];
-    __syncthreads();                 // wsum may be reused by the next scan
-    return r;
+    return wsum[warp] + x - v;
 }
 
 __global__ void __launch_bounds__(RF_THREADS, 1) k_evict_random(const EvictParams p)
@@ -672,38 +674,58 @@ __global__ void __launch_bounds__(RF_THREADS, 1) k_evict_random(const EvictParam
                                                     rf_align((size_t)nwords * 4));
     uint32_t *s_hist = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(s_list) +
                                                     rf_align((size_t)(C + 2) * 2));
-    int *s_misc = reinterpret_cast<int *>(s_hist + RF_BINS);   // [0, 33): scan; 40..: scalars
+    int *s_misc = reinterpret_cast<int *>(s_hist + RF_BINS);
+    // [0] bucket list length, [1] bin, [2] keys below it, [3] bin size
+    int *s_sc = s_misc + RF_SCALARS;
 
     const int unit = blockIdx.x, b = unit / p.Hkv, hk = unit % p.Hkv;
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t *pos = p.pos + (size_t)unit * C;
     const int n = p.n[unit];
+    for (int i = tid; i < RF_BINS; i += RF_THREADS)
+        s_hist[i] = 0;
+    if (tid == 0)
+        s_sc[0] = 0;
+    __syncthreads();
+
+    // ---- 1. positions and keys into shared memory, top-bit histogram of the candidates.
+    // The position loads of a round do not wait for n (slots up to C are readable).
+    constexpr int PU = 4;
+    const int nv = n < C ? n : C;   // a count above C is flagged below, after the loads
+    for (int base = 0; base < C; base += PU * RF_THREADS) {
+        int32_t pv[PU];
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+            const int j = base + u * RF_THREADS + tid;
+            pv[u] = j < C ? pos[j] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+            const int j = base + u * RF_THREADS + tid;
+            if (j < nv) {
+                s_pos[j] = pv[u];
+                uint64_t k = ~0ull;
+                if (pv[u] >= p.prompt_len) {
+                    k = philox_key(p.seed_lo, p.seed_hi, (uint32_t)pv[u], (uint32_t)hk,
+                                   (uint32_t)b, p.epoch);
+                    atomicAdd(&s_hist[(uint32_t)(k >> RF_SHIFT)], 1u);
+                }
+                s_key[j] = k;
+            }
+        }
+    }
     if (n > C || n < 0) {
         if (tid == 0)
             flag_error(p.status, DEV_CAPACITY);
         return;
     }
-    for (int i = tid; i < RF_BINS; i += RF_THREADS)
-        s_hist[i] = 0;
-    if (tid == 0)
-        s_misc[40] = 0;   // bucket list length
     __syncthreads();
 
-    // ---- 1. positions and keys into shared memory, candidate count, top-bit histogram
-    const int32_t *pos = p.pos + (size_t)unit * C;
-    int my_cand = 0;
-    for (int j = tid; j < n; j += RF_THREADS) {
-        const int32_t pj = pos[j];
-        s_pos[j] = pj;
-        uint64_t k = ~0ull;
-        if (pj >= p.prompt_len) {
-            k = philox_key(p.seed_lo, p.seed_hi, (uint32_t)pj, (uint32_t)hk, (uint32_t)b, p.epoch);
-            ++my_cand;
-            atomicAdd(&s_hist[(uint32_t)(k >> RF_SHIFT)], 1u);
-        }
-        s_key[j] = k;
-    }
+    // ---- 2. candidate count (the histogram's total) and the bin holding the n_keep-th
+    // smallest key, two bins per thread
+    const int h0 = (int)s_hist[2 * tid], h1 = (int)s_hist[2 * tid + 1];
     int n_cand;
-    rf_scan(my_cand, &n_cand, s_misc);
+    const int ex = rf_scan(h0 + h1, &n_cand, s_misc + RF_SCAN_A);
     if (n_cand == 0)
         return;
     int n_keep = (int)((double)n_cand * p.keep_ratio);
@@ -711,65 +733,66 @@ __global__ void __launch_bounds__(RF_THREADS, 1) k_evict_random(const EvictParam
     if (n_keep == n_cand)
         return;
     const int n_new = n - n_cand + n_keep;
-
-    // ---- 2. the bin that holds the n_keep-th smallest key (two bins per thread)
-    {
-        const int h0 = (int)s_hist[2 * tid], h1 = (int)s_hist[2 * tid + 1];
-        int tot;
-        const int ex = rf_scan(h0 + h1, &tot, s_misc);
-        if (ex < n_keep && n_keep <= ex + h0 + h1) {
-            const bool first = n_keep <= ex + h0;
-            s_misc[41] = first ? 2 * tid : 2 * tid + 1;
-            s_misc[42] = first ? ex : ex + h0;
-        }
-        __syncthreads();
+    if (ex < n_keep && n_keep <= ex + h0 + h1) {
+        const bool first = n_keep <= ex + h0;
+        s_sc[1] = first ? 2 * tid : 2 * tid + 1;
+        s_sc[2] = first ? ex : ex + h0;
+        s_sc[3] = first ? h0 : h1;
     }
-    const uint32_t bstar = (uint32_t)s_misc[41];
-    const int need = n_keep - s_misc[42];   // members of bin bstar to keep, >= 1
+    __syncthreads();
+    const uint32_t bstar = (uint32_t)s_sc[1];
+    const int need = n_keep - s_sc[2];   // members of bin bstar to keep, in [1, s_sc[3]]
+    const bool whole = need == s_sc[3];  // the whole bin is kept (the usual case)
 
-    // ---- 3. keep flags: candidates of lower bins and every prompt slot; members of
-    // bin bstar go to a list and are decided by their exact rank among themselves
+    // ---- 3. keep flags: every prompt slot and the candidates of lower bins (of bin bstar
+    // too when it is kept whole); otherwise bin bstar's members go to a list and are
+    // decided by their exact rank among themselves
     for (int base = 0; base < n; base += RF_THREADS) {
         const int j = base + tid;
         bool kp = false;
         if (j < n) {
-            const uint64_t k = s_key[j];
             if (s_pos[j] < p.prompt_len) {
                 kp = true;
             } else {
-                const uint32_t bin = (uint32_t)(k >> RF_SHIFT);
-                kp = bin < bstar;
-                if (bin == bstar)
-                    s_list[atomicAdd(&s_misc[40], 1)] = (uint16_t)j;
+                const uint32_t bin = (uint32_t)(s_key[j] >> RF_SHIFT);
+                kp = bin < bstar || (whole && bin == bstar);
+                if (!whole && bin == bstar)
+                    s_list[atomicAdd(&s_sc[0], 1)] = (uint16_t)j;
             }
         }
         const unsigned m = __ballot_sync(0xffffffffu, kp);
-        if (lane == 0 && base + 32 * (tid >> 5) < n)
-            s_keep[(base >> 5) + (tid >> 5)] = m;
+        if (lane == 0 && base + 32 * warp < n)
+            s_keep[(base >> 5) + warp] = m;
     }
     __syncthreads();
-    const int m_b = s_misc[40];
-    for (int t = tid; t < m_b; t += RF_THREADS) {
-        const int j = s_list[t];
-        const uint64_t kj = s_key[j];
-        const int32_t pj = s_pos[j];
-        int rank = 0;
-        for (int i = 0; i < m_b; ++i) {
-            const int o = s_list[i];
-            const uint64_t ko = s_key[o];
-            rank += (ko < kj || (ko == kj && s_pos[o] < pj)) ? 1 : 0;
+    if (!whole) {
+        const int m_b = s_sc[0];
+        for (int t = tid; t < m_b; t += RF_THREADS) {
+            const int j = s_list[t];
+            const uint64_t kj = s_key[j];
+            const int32_t pj = s_pos[j];
+            int rank = 0;
+            for (int i = 0; i < m_b; ++i) {
+                const int o = s_list[i];
+                const uint64_t ko = s_key[o];
+                rank += (ko < kj || (ko == kj && s_pos[o] < pj)) ? 1 : 0;
+            }
+            if (rank < need)
+                atomicOr(&s_keep[j >> 5], 1u << (j & 31));
         }
-        if (rank < need)
-            atomicOr(&s_keep[j >> 5], 1u << (j & 31));
+        __syncthreads();
     }
-    __syncthreads();
 
-    // ---- 4. hole and tail lists (k-th hole of [0, n_new) <- k-th kept slot of [n_new, n))
+    // ---- 4. hole and tail lists (k-th hole of [0, n_new) <- k-th kept slot of [n_new, n)):
+    // per 32-slot word its hole and tail bits and their ranks (one thread per word), then
+    // one warp per word writes the slots at their ranks
     uint16_t *s_hole = s_list;                       // ranks [0, pairs)
     uint16_t *s_tail = s_list + (C + 2) / 2;         // pairs <= min(n_new, n - n_new) <= C / 2
+    uint32_t *s_hw = s_hist, *s_tw = s_hist + 256;   // nwords <= 256
+    int *s_wb = reinterpret_cast<int *>(s_hist + 512);
+    const int wn = (n + 31) / 32;
     int n_pairs;
     {
-        const int wn = (n + 31) / 32;
         uint32_t hb = 0, tb = 0;
         if (tid < wn) {
             const uint32_t w = s_keep[tid];
@@ -780,62 +803,64 @@ __global__ void __launch_bounds__(RF_THREADS, 1) k_evict_random(const EvictParam
             hb = ~w & below & valid;
             tb = w & ~below & valid;
         }
-        const int hbase = rf_scan(__popc(hb), &n_pairs, s_misc);
-        int tt;
-        const int tbase = rf_scan(__popc(tb), &tt, s_misc);
-        for (int r = 0; hb; ++r) {
-            const int l = __ffs(hb) - 1;
-            hb &= hb - 1;
-            s_hole[hbase + r] = (uint16_t)(32 * tid + l);
-        }
-        for (int r = 0; tb; ++r) {
-            const int l = __ffs(tb) - 1;
-            tb &= tb - 1;
-            s_tail[tbase + r] = (uint16_t)(32 * tid + l);
+        // hole counts in the low 16 bits, tail counts in the high 16 (totals <= 8192)
+        int both;
+        const int exw = rf_scan(__popc(hb) | (__popc(tb) << 16), &both, s_misc + RF_SCAN_B);
+        n_pairs = both & 0xffff;
+        if (tid < wn) {
+            s_hw[tid] = hb;
+            s_tw[tid] = tb;
+            s_wb[tid] = exw;
         }
     }
     __syncthreads();
-
-    // ---- 5. moves: pair k's K row then V row as 16-byte chunks, RF_UNROLL per thread in flight
-    const int chunks = p.D / 8;                  // per row
-    const int per_pair = 2 * chunks;
-    const int total = n_pairs * per_pair;
-    uint4 *K4 = reinterpret_cast<uint4 *>(p.K), *V4 = reinterpret_cast<uint4 *>(p.V);
-    for (int base = 0; base < total; base += RF_THREADS * RF_UNROLL) {
-        uint4 v[RF_UNROLL];
-        long dst[RF_UNROLL];
-        bool isv[RF_UNROLL];
-#pragma unroll
-        for (int u = 0; u < RF_UNROLL; ++u) {
-            const int idx = base + u * RF_THREADS + tid;
-            dst[u] = -1;
-            isv[u] = false;
-            if (idx < total) {
-                const int k = idx / per_pair, c = idx % per_pair;
-                const long rs = p.rows.row(unit, s_tail[k]), rd = p.rows.row(unit, s_hole[k]);
-                isv[u] = c >= chunks;
-                const int cc = isv[u] ? c - chunks : c;
-                if (rs < 0 || rd < 0) {   // no page behind a slot: skip the chunk, flag it
-                    flag_error(p.status, DEV_CAPACITY);
-                } else {
-                    v[u] = isv[u] ? V4[rs * chunks + cc] : K4[rs * chunks + cc];
-                    dst[u] = rd * chunks + cc;
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < RF_UNROLL; ++u) {
-            if (dst[u] >= 0) {
-                if (isv[u])
-                    V4[dst[u]] = v[u];
-                else
-                    K4[dst[u]] = v[u];
-            }
-        }
+    for (int wd = warp; wd < wn; wd += RF_WARPS) {
+        const uint32_t hb = s_hw[wd], tb = s_tw[wd];
+        const int wb = s_wb[wd];
+        const uint32_t lt = (1u << lane) - 1u;
+        if ((hb >> lane) & 1u)
+            s_hole[(wb & 0xffff) + __popc(hb & lt)] = (uint16_t)(32 * wd + lane);
+        if ((tb >> lane) & 1u)
+            s_tail[(wb >> 16) + __popc(tb & lt)] = (uint16_t)(32 * wd + lane);
     }
+    __syncthreads();
+
+    // ---- 5. moves: a warp (half a warp at D = 64) per pair, lane c copies 16-byte chunk c
+    // of the pair's K row then V row; RF_UNROLL pairs per warp in flight
+    const int chunks = p.D / 8;                  // per row
+    const int per_pair = 2 * chunks;             // 32 (D = 128) or 16 (D = 64)
+    const int ppw = 32 / per_pair;
+    const int c = lane % per_pair;
+    const bool isv = c >= chunks;
+    const int cc = isv ? c - chunks : c;
+    uint4 *base4 = reinterpret_cast<uint4 *>(isv ? p.V : p.K);
     int32_t *gpos = p.pos + (size_t)unit * C;
-    for (int k = tid; k < n_pairs; k += RF_THREADS)
-        gpos[s_hole[k]] = s_pos[s_tail[k]];
+    for (int k0 = 0; k0 < n_pairs; k0 += RF_WARPS * ppw * RF_UNROLL) {
+        uint4 v[RF_UNROLL];
+        int rd[RF_UNROLL];
+#pragma unroll
+        for (int u = 0; u < RF_UNROLL; ++u) {
+            const int k = k0 + (u * RF_WARPS + warp) * ppw + lane / per_pair;
+            rd[u] = -1;
+            if (k < n_pairs) {
+                const int src = s_tail[k], dst = s_hole[k];
+                const long rs = p.rows.row(unit, src), rdl = p.rows.row(unit, dst);
+                if (rs < 0 || rdl < 0) {   // no page behind a slot: skip the row, flag it
+                    if (c == 0)
+                        flag_error(p.status, DEV_CAPACITY);
+                } else {
+                    v[u] = base4[(size_t)rs * chunks + cc];
+                    rd[u] = (int)rdl;
+                }
+                if (c == 0)
+                    gpos[dst] = s_pos[src];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < RF_UNROLL; ++u)
+            if (rd[u] >= 0)
+                base4[(size_t)rd[u] * chunks + cc] = v[u];
+    }
     if (tid == 0)
         p.n[unit] = n_new;
 }

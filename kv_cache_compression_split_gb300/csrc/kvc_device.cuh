@@ -45,6 +45,28 @@ __device__ __forceinline__ void flag_error(int *status, int bit)
         atomicOr(status, bit);
 }
 
+// ---------------------------------------------------------------- clusters
+
+// Every thread of every CTA of the cluster arrives, then waits for all of them;
+// shared-memory writes made before it are visible cluster-wide after it.  The
+// calling warp must be converged.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// fp32 load from the shared memory of CTA `rank` of this cluster, at the offset
+// that `local` has in this CTA's shared memory.
+__device__ __forceinline__ float ld_cluster_f32(const float *local, uint32_t rank)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- slot rows
 
 constexpr int PAGE_SLOTS = 64;   // KVC_PAGE_SLOTS

@@ -37,8 +37,12 @@ struct SlotAttendPlan {
     int tiles_per_split;
 };
 
-// Split plan shared by kvc_workspace_size and kvc_decode_attend.
-SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested_splits);
+// Split plan shared by kvc_workspace_size and kvc_decode_attend (at most
+// max_splits splits when none are requested).
+SlotAttendPlan plan_attend(int units, int tiles_per_unit, int requested_splits, int max_splits = 64);
+
+// Splits of one unit that the slot attention merges inside a thread-block cluster.
+constexpr int SLOT_CLUSTER_MAX = 8;
 
 // ---- launchers (each returns a cudaError_t of the launch) ----
 
@@ -54,6 +58,7 @@ struct AttendLaunch {
     float scale;
     float *h2o_scores;
     float h2o_keep, h2o_add;   // scores = keep * scores + add * p
+    bool cluster;              // 2..8 splits merged in a cluster (no workspace)
     const int32_t *block_table; // paged layout (nullptr: dense)
     int num_pages;
 };

@@ -78,21 +78,26 @@ def test_null_arguments_are_rejected_without_touching_a_gpu(kvc):
         a.logits = a.lse = a.h2o_scores = 16
         a.h2o_decay = bad
         assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_INVALID_ARG, bad
-    # fused H2O with the logits on chip: one split only, and C within the on-chip bound
+    # fused H2O with the logits on chip: at most one cluster of 8 splits, each split within
+    # the on-chip bound of KVC_H2O_ONCHIP_MAX_SLOTS slots
     a = kvc.AttendArgs()
     a.kind, a.Hq, a.q, a.o, a.slots = kvc.KVC_KIND_SLOTS, 1, 16, 16, ctypes.pointer(d)
     a.lse = a.h2o_scores = 16
-    a.num_splits = 2
+    a.num_splits = 9
     assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_INVALID_ARG
-    a.h2o_scores = 0
-    a.lse = 0
     a.num_splits = 1
     big = kvc.SlotCacheDesc(1, 1, 128, kvc.H2O_ONCHIP_MAX_SLOTS + 64, 16, 16, 16, 16, 16)
     a.slots = ctypes.pointer(big)
-    a.lse = a.h2o_scores = 16
     assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_UNSUPPORTED
-    a.logits = 16                    # with a logits array any capacity is fine for the checks
+    a.num_splits = 2                 # two splits of at most 1024 slots: planned, no workspace
     assert lib.kvc_workspace_size(ctypes.byref(a)) == 0
+    huge = kvc.SlotCacheDesc(1, 1, 128, 8 * kvc.H2O_ONCHIP_MAX_SLOTS + 64, 16, 16, 16, 16, 16)
+    a.slots = ctypes.pointer(huge)
+    a.num_splits = 0                 # would need 9 splits
+    assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_UNSUPPORTED
+    a.logits = 16                    # with a logits array any capacity and split count is fine
+    a.num_splits = 12                # more splits than a cluster: partials in a workspace
+    assert lib.kvc_workspace_size(ctypes.byref(a)) > 0
 
 
 def test_product_path_does_not_import_the_oracle():

@@ -171,7 +171,9 @@ def test_h2o_prefill_full_size_sampled_units(kvc, orc):
     (4, 64, 8, 128, "fused", 1, 0.0), (3, 8, 8, 64, "fused", 3, 0.0),
     (4, 64, 8, 128, "fused", 1, 0.99), (3, 8, 8, 64, "separate", 0, 0.9),
     (3, 8, 8, 64, "fused", 3, 0.99), (4, 64, 8, 128, "onchip", 0, 0.0),
-    (3, 8, 8, 64, "onchip", 1, 0.99), (2, 24, 8, 128, "onchip", 1, 0.0)])
+    (3, 8, 8, 64, "onchip", 1, 0.99), (2, 24, 8, 128, "onchip", 1, 0.0),
+    (4, 64, 8, 128, "onchip", 3, 0.0), (3, 8, 8, 64, "onchip", 2, 0.99),
+    (2, 64, 8, 128, "fused", 12, 0.0)])
 def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, mode, splits, decay):
     """One decode step from a seeded post-prefill state: 64 heavy slots from [0, 1600) plus the
     recent 448; append token 2048, attend over 513 slots, accumulate (plain, or the decayed
@@ -417,11 +419,15 @@ def test_h2o_decode_step_full_size_sampled_units(kvc, orc):
         assert torch.equal(cache.K[b, hk, :512], Kseq[b, hk, torch.from_numpy(p).long().cuda()][src])
 
 
-@pytest.mark.parametrize("D,C,Hq,Hkv,decay", [(128, 576, 64, 8, 0.0), (64, 300, 24, 8, 0.99),
-                                               (128, 65, 8, 2, 0.0)])
-def test_h2o_register_logits_ragged_vs_oracle(kvc, orc, D, C, Hq, Hkv, decay):
-    """The fused H2O launch with the logits in registers (caches of up to 576 slots) on ragged
-    units (empty, one slot, a partial tile, full capacity) and g < 8 query heads per KV head:
+@pytest.mark.parametrize("D,C,Hq,Hkv,decay,splits", [
+    (128, 576, 64, 8, 0.0, 1), (64, 300, 24, 8, 0.99, 1), (128, 65, 8, 2, 0.0, 1),
+    (128, 1500, 64, 8, 0.0, 3),     # three splits of <= 9 tiles: registers, cluster merge
+    (64, 2048, 16, 4, 0.99, 2),     # two splits of 16 tiles: shared memory, cluster merge
+    (128, 4000, 8, 2, 0.0, 0)])     # automatic plan (at least 4 splits for the on-chip bound)
+def test_h2o_register_logits_ragged_vs_oracle(kvc, orc, D, C, Hq, Hkv, decay, splits):
+    """The fused H2O launch with the logits kept on chip (registers for splits of up to nine
+    tiles, else shared memory; the splits of a unit merged in their cluster) on ragged units
+    (empty, one slot, a partial tile, full capacity) and g < 8 query heads per KV head:
     outputs, lse and scores against the oracle's attention and accumulation."""
     B = 3
     g = torch.Generator().manual_seed(C + Hq + D)
@@ -437,7 +443,7 @@ def test_h2o_register_logits_ragged_vs_oracle(kvc, orc, D, C, Hq, Hkv, decay):
     sc = base.clone().cuda()
     o = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
     lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
-    kvc.kvc_decode_attend(cache, q.cuda(), o, lse=lse, num_splits=1, h2o_scores=sc,
+    kvc.kvc_decode_attend(cache, q.cuda(), o, lse=lse, num_splits=splits, h2o_scores=sc,
                           h2o_decay=decay)
     torch.cuda.synchronize()
     ref_o, ref_lse, ref_lg = orc.decode_attend(np16(q), np16(K), np16(V), n, want_logits=True)
@@ -455,8 +461,10 @@ def test_h2o_register_logits_ragged_vs_oracle(kvc, orc, D, C, Hq, Hkv, decay):
     assert device_status_clean(kvc)
 
 
-@pytest.mark.parametrize("D,C,n", [(128, 520, 513), (64, 1024, 1024), (128, 1024, 700)])
-def test_h2o_onchip_logits_match_written_logits(kvc, D, C, n):
+@pytest.mark.parametrize("D,C,n,splits", [(128, 520, 513, 1), (64, 1024, 1024, 1),
+                                          (128, 1024, 700, 1), (128, 1500, 1400, 3),
+                                          (64, 2048, 2000, 2)])
+def test_h2o_onchip_logits_match_written_logits(kvc, D, C, n, splits):
     """The fused H2O launch with the logits kept on chip gives bit-identical outputs, lse and
     scores to the same launch writing a logits array (same arithmetic, other storage), up to
     the on-chip capacity bound."""
@@ -473,7 +481,7 @@ def test_h2o_onchip_logits_match_written_logits(kvc, D, C, n):
         lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
         sc = base.clone()
         logits = None if onchip else torch.empty(B, Hq, C, dtype=torch.float32, device="cuda")
-        kvc.kvc_decode_attend(cache, q, o, logits=logits, lse=lse, num_splits=1,
+        kvc.kvc_decode_attend(cache, q, o, logits=logits, lse=lse, num_splits=splits,
                               h2o_scores=sc, h2o_decay=0.99)
         torch.cuda.synchronize()
         outs.append((o, lse, sc))

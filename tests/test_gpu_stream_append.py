@@ -86,7 +86,7 @@ def test_stream_append_small_windows(kvc, orc, T0, n_sink, n_recent, steps, page
     short enough to need none), then decode steps; the window grows until it holds
     n_sink + n_recent + 1 tokens and then slides with n fixed."""
     B, Hq, Hkv, D = 2, 4, 4, 64
-    C = 64
+    C = 128
     g = torch.Generator().manual_seed(T0 * 7 + n_recent)
     Kseq = torch.randn(B, Hkv, T0 + steps, D, generator=g).half()
     Vseq = torch.randn(B, Hkv, T0 + steps, D, generator=g).half()
