@@ -70,7 +70,11 @@ template <int D, int BITS, bool GEAR = false> struct KiviCfg {
     static constexpr int SIDE_A = 4 * NS, SIDE_B = 4 * NS + 4 * G;   // byte offsets
     static_assert(SIDE_B == SIDE_A + 4 * G, "A [2][G] binary16 precedes B");
     static constexpr int QT_BYTES = 2 * QG * (BLOCK + SIDE);
-    static constexpr int RS = 32;                      // ring slots per residual tile
+    // ring slots per residual tile (16 for 2-bit codes, which would size the stages by the
+    // smaller quantised tile and keep five in flight instead of three, measured 129 vs 119 us
+    // on the 32-sequence MHA workload: the 2-bit read path is bound by instructions, not by
+    // bytes in flight, and the extra residual tiles cost more than the deeper ring gains)
+    static constexpr int RS = 32;
     static constexpr int NBOX = D / 64;
     static constexpr int RT_BYTES = 2 * RS * D * 2;
     static constexpr int STAGE_BYTES =
@@ -231,10 +235,10 @@ struct KiviItem {
     int unit, split, b, hk, T, n_groups, n_res, qt0, nq, nr;
 };
 
-template <int D, int BITS>
+template <int D, int BITS, bool GEAR>
 __device__ __forceinline__ KiviItem kivi_item(const KiviParams &p, int item)
 {
-    using Cfg = KiviCfg<D, BITS>;
+    using Cfg = KiviCfg<D, BITS, GEAR>;
     KiviItem w;
     w.unit = item / p.splits;
     w.split = item % p.splits;
@@ -292,7 +296,7 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
             prefetch_tmap(&tmV);
             int it = 0;
             for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-                const KiviItem w = kivi_item<D, BITS>(p, item);
+                const KiviItem w = kivi_item<D, BITS, GEAR>(p, item);
                 const int ntiles = w.nr + w.nq;   // residual tiles first, then quantised tiles
                 for (int i = 0; i < ntiles; ++i, ++it) {
                     const int st = it % Cfg::NSTAGE;
@@ -374,7 +378,7 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
     int qbuf = 0;   // q buffer of the current item
 
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, qbuf ^= 1) {
-    const KiviItem wi = kivi_item<D, BITS>(p, item);
+    const KiviItem wi = kivi_item<D, BITS, GEAR>(p, item);
     const int b = wi.b, hk = wi.hk, T = wi.T, n_groups = wi.n_groups, n_res = wi.n_res;
     const int qt0 = wi.qt0, nr = wi.nr, ntiles = wi.nr + wi.nq;
     const uint16_t *qrow = p.q + ((size_t)b * p.Hq + hk * p.g + (hv ? r : 0)) * D;
@@ -450,9 +454,9 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
                 i = ntiles + 1;
                 break;
             }
-            // warps 0, 1 take 16 ring slots each
+            // warps 0 .. RS/16 - 1 take 16 ring slots each
             const int s0 = i * Cfg::RS + 16 * warp;
-            if (warp < 2 && s0 < p.CR) {
+            if (warp < Cfg::RS / 16 && s0 < p.CR) {
                 const uint32_t kbase = smem_u32(smem + st * Cfg::STAGE_BYTES);
                 const uint32_t vbase = kbase + Cfg::NBOX * Cfg::RS * 128;
                 float sa[4] = {0.f, 0.f, 0.f, 0.f};
@@ -902,10 +906,15 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
 }
 
 template <int D, int BITS, bool GEAR>
-cudaError_t launch_kivi_impl(const CUtensorMap &tk, const CUtensorMap &tv, const KiviParams &kp,
-                             cudaStream_t s)
+cudaError_t launch_kivi_impl(const KiviAttendLaunch &a, const KiviParams &kp, cudaStream_t s)
 {
     using Cfg = KiviCfg<D, BITS, GEAR>;
+    // the residual rings as [B * Hkv * (R + 32), D] fp16, one box = RS ring slots
+    CUtensorMap tk, tv;
+    const uint64_t rows = (uint64_t)a.B * a.Hkv * kp.CR;
+    if (!encode_tmap_2d_f16(&tk, a.k_res, D, rows, 64, Cfg::RS) ||
+        !encode_tmap_2d_f16(&tv, a.v_res, D, rows, 64, Cfg::RS))
+        return cudaErrorInvalidValue;
     const void *fn = reinterpret_cast<const void *>(k_attend_kivi<D, BITS, GEAR>);
     const cudaError_t e = set_smem_once(fn, Cfg::SMEM);
     if (e != cudaSuccess)
@@ -919,13 +928,12 @@ cudaError_t launch_kivi_impl(const CUtensorMap &tk, const CUtensorMap &tv, const
 }
 
 template <int D, int BITS>
-cudaError_t launch_kivi_bits(const CUtensorMap &tk, const CUtensorMap &tv, const KiviParams &kp,
-                             cudaStream_t s)
+cudaError_t launch_kivi_bits(const KiviAttendLaunch &a, const KiviParams &kp, cudaStream_t s)
 {
     static_assert(KiviCfg<128, BITS, true>::SIDE == 976 && KiviCfg<64, BITS, true>::SIDE == 560,
                   "GEAR side block size");
-    return kp.kg ? launch_kivi_impl<D, BITS, true>(tk, tv, kp, s)
-                 : launch_kivi_impl<D, BITS, false>(tk, tv, kp, s);
+    return kp.kg ? launch_kivi_impl<D, BITS, true>(a, kp, s)
+                 : launch_kivi_impl<D, BITS, false>(a, kp, s);
 }
 
 } // namespace
@@ -933,11 +941,6 @@ cudaError_t launch_kivi_bits(const CUtensorMap &tk, const CUtensorMap &tv, const
 cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s)
 {
     const int CR = a.R + KIVI_G;
-    CUtensorMap tk, tv;
-    const uint64_t rows = (uint64_t)a.B * a.Hkv * CR;
-    if (!encode_tmap_2d_f16(&tk, a.k_res, a.D, rows, 64, 32) ||
-        !encode_tmap_2d_f16(&tv, a.v_res, a.D, rows, 64, 32))
-        return cudaErrorInvalidValue;
     KiviParams kp{};
     kp.Hq = a.Hq;
     kp.Hkv = a.Hkv;
@@ -965,11 +968,9 @@ cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s)
     kp.n_items = a.B * a.Hkv * a.splits;
     cudaError_t e;
     if (a.D == 128)
-        e = a.bits == 4 ? launch_kivi_bits<128, 4>(tk, tv, kp, s)
-                        : launch_kivi_bits<128, 2>(tk, tv, kp, s);
+        e = a.bits == 4 ? launch_kivi_bits<128, 4>(a, kp, s) : launch_kivi_bits<128, 2>(a, kp, s);
     else
-        e = a.bits == 4 ? launch_kivi_bits<64, 4>(tk, tv, kp, s)
-                        : launch_kivi_bits<64, 2>(tk, tv, kp, s);
+        e = a.bits == 4 ? launch_kivi_bits<64, 4>(a, kp, s) : launch_kivi_bits<64, 2>(a, kp, s);
     if (e != cudaSuccess || a.splits == 1)
         return e;
     return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);
