@@ -138,6 +138,38 @@ class L2Flush:
         self.r.sum()
 
 
+def in_graph_ms(stream, fn, flush, reset=None, R=10):
+    """Milliseconds one call of fn adds to a CUDA graph of R repetitions of [reset, L2 flush,
+    fn], against the same graph without fn (median of three replays each): the kernel's cost
+    as it runs inside a captured decode step, without the host launch latency that an
+    isolated event pair around one launch also measures (~4-5 us on this system)."""
+    import torch
+    graphs = []
+    for with_fn in (True, False):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(R):
+                if reset is not None:
+                    reset()
+                flush()
+                if with_fn:
+                    fn()
+        graphs.append(g)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ts = ([], [])
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for g, t in zip(graphs, ts):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                t.append(e0.elapsed_time(e1))
+    del graphs
+    return (statistics.median(ts[0]) - statistics.median(ts[1])) / R
+
+
 def slot_bytes(n_slots, B, Hkv, Hq, D):
     """Algorithmic bytes of one slot-cache attention launch: K and V of the attended slots,
     the queries and the outputs."""
@@ -772,10 +804,14 @@ def config_rows(kvc, W, dev, stream, hbm_peak):
         c = kvc.SlotCache.empty(B, Hkv, T + 8, D, device=dev)
         kvc.kvc_append(c, K, V, stream=stream)
         ws = torch.empty(max(kvc.kvc_workspace_size(c, q) // 4, 1), dtype=torch.float32, device=dev)
-        ms = timed(lambda: kvc.kvc_decode_attend(c, q, o, workspace=ws, stream=stream))
+        fn = lambda: kvc.kvc_decode_attend(c, q, o, workspace=ws, stream=stream)
+        ms = timed(fn)
+        mg = in_graph_ms(stream, fn, flush)
         nb = slot_bytes(T + 1, B, Hkv, Hq, D)
         out[f"{w.name}/fp16"] = {"ms": ms, "slots": T + 1, "gbs": nb / (ms * 1e-3) / 1e9,
                                  "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm_peak,
+                                 "ms_in_graph": mg,
+                                 "frac_of_hbm_in_graph": nb / (mg * 1e-3) / 1e9 / hbm_peak,
                                  "tokens_per_s": B / (ms * 1e-3)}
         del c, ws
         # the two compressed caches after the prompt (set-up, untimed)
@@ -846,9 +882,17 @@ def config_rows(kvc, W, dev, stream, hbm_peak):
                                           stream=stream),
             lambda: kvc.kvc_h2o_evict(hc, hsc, w.n_heavy, w.n_recent, stream=stream)])
         nb = slot_bytes(513, B, Hkv, Hq, D)
+        h_app = lambda: kvc.kvc_append(hc, kn, vn, stream=stream)
+        h_att = lambda: kvc.kvc_decode_attend(hc, q, o, lse=lse, workspace=ws_h, h2o_scores=hsc,
+                                              stream=stream)
+        h_ev = lambda: kvc.kvc_h2o_evict(hc, hsc, w.n_heavy, w.n_recent, stream=stream)
+        g_att = in_graph_ms(stream, h_att, flush, reset=lambda: (reset_h2o(), h_app()))
+        g_step = in_graph_ms(stream, lambda: (h_app(), h_att(), h_ev()), flush, reset=reset_h2o)
         out[f"{w.name}/h2o512"] = {
             "ms": t_att, "slots": 513, "gbs": nb / (t_att * 1e-3) / 1e9,
             "frac_of_hbm": nb / (t_att * 1e-3) / 1e9 / hbm_peak, "tokens_per_s": B / (t_att * 1e-3),
+            "ms_in_graph": g_att, "frac_of_hbm_in_graph": nb / (g_att * 1e-3) / 1e9 / hbm_peak,
+            "step_ms_in_graph": g_step,
             "step_ms": t_app + t_att + t_ev, "append_ms": t_app, "evict_ms": t_ev,
             "prefill_score_pass_ms": pre_ms,
             "cache": "prefill scores of the 2048-token causal prompt, evicted to 64 heavy + "
@@ -856,9 +900,15 @@ def config_rows(kvc, W, dev, stream, hbm_peak):
         t_app, t_att = step_times(reset_st, [
             lambda: kvc.kvc_stream_append(stc, kn, vn, w.n_sink, w.n_recent, stream=stream),
             lambda: kvc.kvc_decode_attend(stc, q, o, workspace=ws_h, stream=stream)])
+        s_app = lambda: kvc.kvc_stream_append(stc, kn, vn, w.n_sink, w.n_recent, stream=stream)
+        s_att = lambda: kvc.kvc_decode_attend(stc, q, o, workspace=ws_h, stream=stream)
+        g_att = in_graph_ms(stream, s_att, flush, reset=lambda: (reset_st(), s_app()))
+        g_step = in_graph_ms(stream, lambda: (s_app(), s_att()), flush, reset=reset_st)
         out[f"{w.name}/stream512"] = {
             "ms": t_att, "slots": 513, "gbs": nb / (t_att * 1e-3) / 1e9,
             "frac_of_hbm": nb / (t_att * 1e-3) / 1e9 / hbm_peak, "tokens_per_s": B / (t_att * 1e-3),
+            "ms_in_graph": g_att, "frac_of_hbm_in_graph": nb / (g_att * 1e-3) / 1e9 / hbm_peak,
+            "step_ms_in_graph": g_step,
             "step_ms": t_app + t_att, "append_ms": t_app,
             "cache": "the prompt gathered to 64 sinks + 448 recent; step: kvc_stream_append "
                      "(the leaving token's slot), attention over 513"}
@@ -872,10 +922,14 @@ def config_rows(kvc, W, dev, stream, hbm_peak):
         c = kvc.SlotCache.empty(B, Hkv, T + 8, D, device=dev)
         kvc.kvc_append(c, K, V, stream=stream)
         ws = torch.empty(max(kvc.kvc_workspace_size(c, q) // 4, 1), dtype=torch.float32, device=dev)
-        ms = timed(lambda: kvc.kvc_decode_attend(c, q, o, workspace=ws, stream=stream))
+        fn = lambda: kvc.kvc_decode_attend(c, q, o, workspace=ws, stream=stream)
+        ms = timed(fn)
+        mg = in_graph_ms(stream, fn, flush)
         nb = slot_bytes(T, B, Hkv, Hq, D)
         out[f"{w.name}/fp16"] = {"ms": ms, "slots": T, "gbs": nb / (ms * 1e-3) / 1e9,
                                  "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm_peak,
+                                 "ms_in_graph": mg,
+                                 "frac_of_hbm_in_graph": nb / (mg * 1e-3) / 1e9 / hbm_peak,
                                  "tokens_per_s": B / (ms * 1e-3)}
         del c, ws
         for bits in (4, 2):
@@ -883,10 +937,15 @@ def config_rows(kvc, W, dev, stream, hbm_peak):
             kvc.kvc_append_quant(kq, K, V, stream=stream)
             ws = torch.empty(max(kvc.kvc_workspace_size(kq, q) // 4, 1), dtype=torch.float32,
                              device=dev)
-            ms = timed(lambda: kvc.kvc_decode_attend(kq, q, o, workspace=ws, stream=stream))
+            fn = lambda: kvc.kvc_decode_attend(kq, q, o, workspace=ws, stream=stream)
+            ms = timed(fn)
+            mg = in_graph_ms(stream, fn, flush)
             nb = kivi_bytes(T, w.kivi_R, B, Hkv, Hq, D, bits)
             out[f"{w.name}/kivi{bits}"] = {"ms": ms, "tokens": T, "gbs": nb / (ms * 1e-3) / 1e9,
                                            "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm_peak,
+                                           "ms_in_graph": mg,
+                                           "frac_of_hbm_in_graph":
+                                               nb / (mg * 1e-3) / 1e9 / hbm_peak,
                                            "tokens_per_s": B / (ms * 1e-3)}
             del kq, ws
         del K, V, flush
@@ -1016,6 +1075,25 @@ def random_rows(kvc, W, dev, stream, hbm_peak):
             at_bytes.append(slot_bytes(n1, B, Hkv, Hq, D))
             n_before.append(n0)
             n_after.append(n1)
+        # the last eviction again, inside a CUDA graph (its pre-eviction positions and count
+        # restored before each repetition: the same keep-set and the same moved rows)
+        n0_last = n_before[-1]
+
+        def reset_last():
+            c.pos[:, :, :n0_last].copy_(pre)
+            c.n.fill_(n0_last)
+        e = n_evict - 1
+        g_ev = in_graph_ms(stream, lambda: kvc.kvc_random_evict(c, P, w.keep_ratio,
+                                                                W.RANDOM_EVICT_SEED, e,
+                                                                stream=stream),
+                           flush, reset=reset_last)
+        # the baseline graph ran last and left the pre-eviction state: evict once more
+        reset_last()
+        kvc.kvc_random_evict(c, P, w.keep_ratio, W.RANDOM_EVICT_SEED, e, stream=stream)
+        torch.cuda.synchronize(dev)
+        assert int(c.n[0, 0].item()) == n_after[-1]
+        g_at = in_graph_ms(stream, lambda: kvc.kvc_decode_attend(c, qs[e], o, workspace=ws,
+                                                                 stream=stream), flush)
         st = list(range(5, n_evict))
         ms_ev = statistics.median(t_ev[i] for i in st)
         ms_at = statistics.median(t_at[i] for i in st)
@@ -1026,6 +1104,7 @@ def random_rows(kvc, W, dev, stream, hbm_peak):
     out["random_evict_reasoning"] = {
         "ms": ms_ev, "bytes": gb_ev, "gbs": gb_ev / (ms_ev * 1e-3) / 1e9,
         "frac_of_hbm": gb_ev / (ms_ev * 1e-3) / 1e9 / hbm_peak,
+        "ms_in_graph": g_ev, "frac_of_hbm_in_graph": ev_bytes[-1] / (g_ev * 1e-3) / 1e9 / hbm_peak,
         "slots_before": n_before[-1], "kept_per_head": n_after[-1],
         "ms_per_epoch": [round(t, 4) for t in t_ev],
         "shape": f"B={B} Hkv={Hkv} D={D}, prompt {P} locked, evictions at T = {P + every}.."
@@ -1034,6 +1113,7 @@ def random_rows(kvc, W, dev, stream, hbm_peak):
     out["random_attend_reasoning"] = {
         "ms": ms_at, "slots": n_after[-1], "bytes": gb_at,
         "gbs": gb_at / (ms_at * 1e-3) / 1e9, "frac_of_hbm": gb_at / (ms_at * 1e-3) / 1e9 / hbm_peak,
+        "ms_in_graph": g_at, "frac_of_hbm_in_graph": at_bytes[-1] / (g_at * 1e-3) / 1e9 / hbm_peak,
         "tokens_per_s": B / (ms_at * 1e-3), "ms_per_epoch": [round(t, 4) for t in t_at]}
     return out
 
