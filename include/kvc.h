@@ -8,6 +8,8 @@
  *   - split-KV decode attention over an fp16 slot cache or a KIVI cache, with
  *     GQA head mapping                        -- kvc_decode_attend
  *   - H2O heavy-hitter scores and eviction    -- kvc_h2o_accumulate, kvc_h2o_evict
+ *   - whole decode steps in one launch        -- kvc_h2o_decode_step,
+ *                                                kvc_stream_decode_step
  *   - StreamingLLM sink + recent window       -- kvc_stream_evict, kvc_stream_append
  *   - per-head uniform random eviction with the prompt locked
  *                                             -- kvc_random_evict
@@ -429,6 +431,47 @@ KVC_API kvc_status kvc_stream_evict(const kvc_slot_cache *cache, int n_sink, int
 KVC_API kvc_status kvc_stream_append(const kvc_slot_cache *cache, const uint16_t *k_new,
                              const uint16_t *v_new, int n_sink, int n_recent,
                              cudaStream_t stream);
+
+/*
+ * kvc_h2o_decode_step -- one H2O decode step in one launch: append, attention with
+ * the heavy-hitter score update, and the eviction back to n_heavy + n_recent.
+ * The same results as kvc_append (k_new / v_new [B, Hkv, 1, D] fp16, position
+ * P = seqlen[b]) -> kvc_decode_attend (o [B, Hq, D], lse [B, Hq] optional, with
+ * h2o_scores = scores and h2o_decay = decay) -> kvc_h2o_evict(n_heavy, n_recent),
+ * for caches whose units hold at most n_heavy + n_recent slots before the step (the
+ * decode steady state: at most one slot leaves per step).  The new token attends
+ * from k_new / v_new; afterwards at most one K/V row is written: into the slot
+ * that leaves (the worst non-recent slot by score descending, position
+ * ascending), with its score set to the new token's, or into slot n while the
+ * unit is below budget (n += 1); with n_recent = 0 the new token itself may be
+ * the one that leaves, and then nothing is written.  seqlen += 1.  One split per unit; C at most
+ * KVC_H2O_ONCHIP_MAX_SLOTS (else KVC_ERR_UNSUPPORTED); Hkv at most 127; positions
+ * below 2^24 - 1.  A unit above budget or at capacity sets KVC_DEV_CAPACITY and
+ * keeps its slots (its o, lse and scores are still written).  While the kernel
+ * runs, seqlen[b] carries an arrival count in its top 8 bits: nothing else may
+ * read it concurrently.
+ * Source: "Rethinking KV Cache Compression" guide, §2 (64 heavy + 448 recent) and
+ * §16 "4 种方法逐步执行" (accumulate attention, update the keep set).
+ */
+KVC_API kvc_status kvc_h2o_decode_step(const kvc_slot_cache *cache, float *scores, int Hq,
+                               const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                               uint16_t *o, float *lse, int n_heavy, int n_recent, float decay,
+                               cudaStream_t stream);
+
+/*
+ * kvc_stream_decode_step -- one StreamingLLM decode step in one launch: the same
+ * results as kvc_stream_append -> kvc_decode_attend (o, lse optional).  The token
+ * that left the window with the previous step (position P - n_recent - 1, when
+ * >= n_sink) is not attended and its slot takes the new token after the attention;
+ * otherwise the token goes to slot n (n += 1).  seqlen += 1.  One split per unit;
+ * Hkv at most 127; positions below 2^24 - 1; the seqlen arrival count of
+ * kvc_h2o_decode_step applies.
+ * Source: "Rethinking KV Cache Compression" guide, §2 (64 sinks + 448 recent) and
+ * §16 "4 种方法逐步执行".
+ */
+KVC_API kvc_status kvc_stream_decode_step(const kvc_slot_cache *cache, int Hq, const uint16_t *q,
+                                  const uint16_t *k_new, const uint16_t *v_new, uint16_t *o,
+                                  float *lse, int n_sink, int n_recent, cudaStream_t stream);
 
 /*
  * kvc_random_evict -- per-head uniform random eviction with the prompt locked.

@@ -95,6 +95,10 @@ def lib():
                 "kvc_h2o_evict_when": (st, [C.POINTER(SlotCacheDesc), P, i, i, i, P]),
                 "kvc_stream_evict": (st, [C.POINTER(SlotCacheDesc), i, i, P]),
                 "kvc_stream_append": (st, [C.POINTER(SlotCacheDesc), P, P, i, i, P]),
+                "kvc_h2o_decode_step": (st, [C.POINTER(SlotCacheDesc), P, i, P, P, P, P, P, i, i,
+                                             C.c_float, P]),
+                "kvc_stream_decode_step": (st, [C.POINTER(SlotCacheDesc), i, P, P, P, P, P, i, i,
+                                                P]),
                 "kvc_random_evict": (st, [C.POINTER(SlotCacheDesc), i, C.c_double, C.c_uint64,
                                           C.c_uint32, P]),
                 "kvc_status_string": (C.c_char_p, [i]),
@@ -284,6 +288,26 @@ def kvc_stream_append(cache: "SlotCache", k_new, v_new, n_sink: int, n_recent: i
     d = cache.desc()
     _check(lib().kvc_stream_append(C.byref(d), _ptr(k_new), _ptr(v_new), n_sink, n_recent,
                                    _stream(stream)), "kvc_stream_append")
+
+
+def kvc_h2o_decode_step(cache: "SlotCache", scores, q, k_new, v_new, o, lse=None,
+                        n_heavy: int = 64, n_recent: int = 448, decay: float = 0.0, stream=None):
+    """One H2O decode step (append + attention + score update + eviction) in one launch."""
+    d = cache.desc()
+    _check(lib().kvc_h2o_decode_step(C.byref(d), _ptr(scores), int(q.shape[1]), _ptr(q),
+                                     _ptr(k_new), _ptr(v_new), _ptr(o), _ptr(lse), n_heavy,
+                                     n_recent, float(decay), _stream(stream)),
+           "kvc_h2o_decode_step")
+
+
+def kvc_stream_decode_step(cache: "SlotCache", q, k_new, v_new, o, lse=None, n_sink: int = 64,
+                           n_recent: int = 448, stream=None):
+    """One StreamingLLM decode step (append into the leaving token's slot + attention) in one
+    launch."""
+    d = cache.desc()
+    _check(lib().kvc_stream_decode_step(C.byref(d), int(q.shape[1]), _ptr(q), _ptr(k_new),
+                                        _ptr(v_new), _ptr(o), _ptr(lse), n_sink, n_recent,
+                                        _stream(stream)), "kvc_stream_decode_step")
 
 
 def kvc_random_evict(cache: "SlotCache", prompt_len: int, keep_ratio: float, seed: int,

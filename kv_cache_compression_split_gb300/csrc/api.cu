@@ -513,6 +513,72 @@ kvc_status kvc_stream_evict(const kvc_slot_cache *cache, int n_sink, int n_recen
     return from_cuda(launch_evict(e, stream));
 }
 
+static kvc_status decode_step_common(const kvc_slot_cache *cache, int Hq, const uint16_t *q,
+                                     const uint16_t *k_new, const uint16_t *v_new, uint16_t *o,
+                                     int n_recent, int n_other)
+{
+    kvc_status st = check_slot_cache(cache);
+    if (st != KVC_OK)
+        return st;
+    if (!q || !o || !k_new || !v_new || !aligned16(q) || !aligned16(k_new) || !aligned16(v_new))
+        return KVC_ERR_INVALID_ARG;
+    if (Hq <= 0 || Hq % cache->Hkv != 0 || n_recent < 0 || n_other < 0)
+        return KVC_ERR_INVALID_ARG;
+    if (Hq / cache->Hkv > 8 || cache->Hkv > 127)
+        return KVC_ERR_UNSUPPORTED;
+    return KVC_OK;
+}
+
+kvc_status kvc_h2o_decode_step(const kvc_slot_cache *cache, float *scores, int Hq,
+                               const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                               uint16_t *o, float *lse, int n_heavy, int n_recent, float decay,
+                               cudaStream_t stream)
+{
+    kvc_status st = decode_step_common(cache, Hq, q, k_new, v_new, o, n_recent, n_heavy);
+    if (st != KVC_OK)
+        return st;
+    if (!scores)
+        return KVC_ERR_INVALID_ARG;
+    if (cache->C > H2O_ONCHIP_MAX_SLOTS)
+        return KVC_ERR_UNSUPPORTED;
+    StepLaunch L{};
+    L.c = *cache;
+    L.Hq = Hq;
+    L.q = q;
+    L.o = o;
+    L.lse = lse;
+    L.k_new = k_new;
+    L.v_new = v_new;
+    L.scores = scores;
+    if (!h2o_decay_weights(decay, &L.h2o_keep, &L.h2o_add))
+        return KVC_ERR_INVALID_ARG;
+    L.n_heavy = n_heavy;
+    L.n_recent = n_recent;
+    L.scale = 1.0f / sqrtf((float)cache->D);
+    return from_cuda(launch_decode_step(L, stream));
+}
+
+kvc_status kvc_stream_decode_step(const kvc_slot_cache *cache, int Hq, const uint16_t *q,
+                                  const uint16_t *k_new, const uint16_t *v_new, uint16_t *o,
+                                  float *lse, int n_sink, int n_recent, cudaStream_t stream)
+{
+    kvc_status st = decode_step_common(cache, Hq, q, k_new, v_new, o, n_recent, n_sink);
+    if (st != KVC_OK)
+        return st;
+    StepLaunch L{};
+    L.c = *cache;
+    L.Hq = Hq;
+    L.q = q;
+    L.o = o;
+    L.lse = lse;
+    L.k_new = k_new;
+    L.v_new = v_new;
+    L.n_sink = n_sink;
+    L.n_recent = n_recent;
+    L.scale = 1.0f / sqrtf((float)cache->D);
+    return from_cuda(launch_decode_step(L, stream));
+}
+
 kvc_status kvc_stream_append(const kvc_slot_cache *cache, const uint16_t *k_new,
                              const uint16_t *v_new, int n_sink, int n_recent, cudaStream_t stream)
 {

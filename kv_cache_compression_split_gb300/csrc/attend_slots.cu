@@ -52,7 +52,10 @@ template <int D, int LMODE = LM_NONE> struct SlotCfg {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K + V
     static constexpr int NSTAGE = LSM ? ((D == 128) ? 2 : 4) : ((D == 128) ? 3 : 6);
     static constexpr int LSM_BYTES = LSM ? 8 * LSM_SLOTS * 4 : 0;
-    static constexpr int SMEM = NSTAGE * STAGE_BYTES + LSM_BYTES + 1024 + 2 * NSTAGE * 8;
+    // the mbarriers (full, empty, new token), then the decode step's new K and V rows
+    static constexpr int BAR_BYTES = (2 * NSTAGE + 1) * 8;
+    static constexpr int NEWTOK_OFF = (BAR_BYTES + 15) / 16 * 16;
+    static constexpr int SMEM = NSTAGE * STAGE_BYTES + LSM_BYTES + 1024 + NEWTOK_OFF + 2 * D * 2;
     static_assert(NCW * (8 * D + 16) * 4 <= NSTAGE * STAGE_BYTES, "combine scratch must fit");
     // this CTA's merged partial for the cluster merge, after the warps' scratch
     static constexpr int CP_OFF = NCW * (8 * D + 16) * 4;
@@ -74,7 +77,17 @@ struct SlotParams {
     float h2o_keep, h2o_add;        // scores = keep * scores + add * p
     SlotRows rows;                  // dense or paged K / V rows
     int *status;
+    // fused decode steps (STEP_H2O / STEP_STREAM): the new token of every unit, the cache
+    // arrays the step writes, and the method's window
+    const uint16_t *k_new, *v_new;  // [B, Hkv, 1, D]
+    uint16_t *K, *V;
+    int32_t *pos, *n_w, *seqlen;
+    int n_heavy, n_recent, n_sink;
 };
+
+// Decode-step modes of the slot kernel: plain attention, or one whole decode step of a
+// method in one launch (append + attention + the method's eviction).
+constexpr int STEP_NONE = 0, STEP_H2O = 1, STEP_STREAM = 2;
 
 __device__ __forceinline__ void consumer_bar()
 {
@@ -82,7 +95,20 @@ __device__ __forceinline__ void consumer_bar()
 }
 
 // Slots [0, n) of each unit are valid.
-template <int D, int LMODE>
+//
+// STEP_H2O / STEP_STREAM (one split): the unit's new token, at position P = seqlen[b],
+// joins the attention from k_new / v_new (the cache is not written until the end), and
+// the step then writes exactly one K/V row:
+//   H2O     the scores are updated as in the fused accumulate, the new token gets its
+//           own; if the unit held n_heavy + n_recent slots, the worst non-recent slot by
+//           (score desc, position asc) is the one dropped, and the new token takes its
+//           slot (with its score); otherwise the token goes to slot n and n grows.
+//   STREAM  the token that left the window with the previous step (position
+//           P - n_recent - 1, when >= n_sink) is not attended and gives up its slot;
+//           otherwise the token goes to slot n.
+// seqlen[b] advances once all Hkv CTAs of sequence b have read it: each adds 1 << 24 on
+// arrival, and the last to arrive removes the counts and adds 1.
+template <int D, int LMODE, int STEP>
 __global__ void __launch_bounds__(NTHREADS, 2)
     k_attend_slots(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const SlotParams p)
@@ -95,6 +121,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::NSTAGE * Cfg::STAGE_BYTES +
                                                   Cfg::LSM_BYTES);
     uint64_t *empty = full + Cfg::NSTAGE;
+    uint64_t *ntbar = empty + Cfg::NSTAGE;   // the decode step's new K/V rows have landed
+    uint8_t *newtok = reinterpret_cast<uint8_t *>(full) + Cfg::NEWTOK_OFF;   // K row, V row
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int unit = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
@@ -113,17 +141,33 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const int t_end = min(n_valid, t_begin + p.tiles_per_split * TILE);
     const int ntiles = t_end > t_begin ? (t_end - t_begin + TILE - 1) / TILE : 0;
 
+    __shared__ int s_step[4];   // [0] P, [1] the stream step's leaving slot, [2] H2O victim
     if (threadIdx.x == 0) {
         for (int i = 0; i < Cfg::NSTAGE; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], NCW);
         }
+        mbar_init(ntbar, 1);
         fence_mbar_init();
+        if constexpr (STEP != STEP_NONE) {
+            const int old = atomicAdd(&p.seqlen[b], 1 << 24);
+            if ((old >> 24) + 1 == p.Hkv)
+                atomicAdd(&p.seqlen[b], 1 - (p.Hkv << 24));
+            s_step[0] = old & 0xffffff;
+            s_step[1] = -1;
+            s_step[2] = -1;
+        }
     }
     __syncthreads();
 
     if (warp == NCW) {
-        // ---------------- producer: TMA K/V tiles into the stage ring
+        // ---------------- producer: the step's new K/V rows (bulk copies), then TMA K/V
+        // tiles into the stage ring
+        if (STEP != STEP_NONE && lane == 0) {
+            mbar_arrive_expect_tx(ntbar, 2 * D * 2);
+            bulk_load(newtok, p.k_new + (size_t)unit * D, D * 2, ntbar);
+            bulk_load(newtok + D * 2, p.v_new + (size_t)unit * D, D * 2, ntbar);
+        }
         if (lane == 0 && ntiles > 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
@@ -175,6 +219,19 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         }
     }
 
+    if constexpr (STEP == STEP_STREAM) {
+        // the slot of the token that left the window with the previous step
+        const long leave = (long)s_step[0] - p.n_recent - 1;
+        if (leave >= p.n_sink) {
+            const int32_t *up = p.pos + (size_t)unit * p.C;
+            for (int j = threadIdx.x; j < n_valid; j += NCW * 32)
+                if ((long)up[j] == leave)
+                    s_step[1] = j;
+        }
+        consumer_bar();
+    }
+    const int skip = STEP == STEP_STREAM ? s_step[1] : -1;   // a slot not attended
+
     float acc[D / 16][4];
 #pragma unroll
     for (int m = 0; m < D / 16; ++m)
@@ -218,7 +275,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             }
 
             const int ta = tok0 + r, tb = tok0 + r + 8;
-            const bool va = ta < t_end, vb = tb < t_end;
+            const bool va = ta < t_end && ta != skip, vb = tb < t_end && tb != skip;
             if (lg0) {
                 if (va) lg0[ta - lofs] = sa[0] * p.scale;
                 if (vb) lg0[tb - lofs] = sa[2] * p.scale;
@@ -279,6 +336,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     // LM_REGS: lane c == 0 of each quad loads the old scores of its tokens now, so the
     // loads are in flight while the tiles stream instead of at the end
     float old[LREG ? LREG_TILES : 1][2];
+    int opos[LREG && STEP == STEP_H2O ? LREG_TILES : 1][2];   // H2O step: their positions
     if constexpr (LREG) {
 #pragma unroll
         for (int i = 0; i < LREG_TILES; ++i) {
@@ -287,6 +345,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             const bool upd = p.h2o_scores && p.part_o == nullptr && c == 0 && i < ntiles;
             old[i][0] = upd && ta < t_end ? sc[ta] : 0.f;
             old[i][1] = upd && tb < t_end ? sc[tb] : 0.f;
+            if constexpr (STEP == STEP_H2O) {
+                const int32_t *up = p.pos + (size_t)unit * p.C;
+                opos[i][0] = upd && ta < t_end ? up[ta] : 0;
+                opos[i][1] = upd && tb < t_end ? up[tb] : 0;
+            }
         }
     }
     if constexpr (LREG) {
@@ -300,6 +363,60 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         for (int i = 0; i < ntiles; ++i)
             if (!do_tile(i, lreg[0]))
                 break;
+    }
+
+    // ---------------- decode steps: the new token joins warp 0's running state (row 0 of
+    // a 16-row block; the padding rows have no mass)
+    float lnew[2] = {-INFINITY, -INFINITY};   // warp 0, lanes 0-3: its logits, heads 2c, 2c + 1
+    if constexpr (STEP != STEP_NONE) {
+        if (warp == 0) {
+            // K for S^T = K Q^T: lanes 0-3 (row 0) take words 8s + c and 8s + c + 4 of the
+            // new K row; V for O^T += V^T P^T: lanes with c == 0 (token column 0) take
+            // channels 16m + r and 16m + r + 8 of the new V row
+            if (!mbar_wait(ntbar, 0))
+                flag_error(p.status, DEV_TIMEOUT);
+            const uint32_t *k32 = reinterpret_cast<const uint32_t *>(newtok);
+            const uint16_t *v16 = reinterpret_cast<const uint16_t *>(newtok + D * 2);
+            float sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s = 0; s < D / 16; ++s)
+                mma16816(sa, r == 0 ? k32[8 * s + c] : 0u, 0u, r == 0 ? k32[8 * s + c + 4] : 0u,
+                         0u, qf[s][0], qf[s][1]);
+            const bool va = r == 0;
+            if (va) {
+                lnew[0] = sa[0] * p.scale;
+                lnew[1] = sa[1] * p.scale;
+            }
+            const float x0 = va ? sa[0] * p.scale_log2 : -INFINITY;
+            const float x1 = va ? sa[1] * p.scale_log2 : -INFINITY;
+            float mx0 = x0, mx1 = x1;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
+            const float al0 = mn0 == -INFINITY ? 1.f : ex2(m_run0 - mn0);
+            const float al1 = mn1 == -INFINITY ? 1.f : ex2(m_run1 - mn1);
+            const float p0 = mn0 == -INFINITY ? 0.f : ex2(x0 - mn0);
+            const float p1 = mn1 == -INFINITY ? 0.f : ex2(x1 - mn1);
+            m_run0 = mn0;
+            m_run1 = mn1;
+            l_run0 = l_run0 * al0 + p0;
+            l_run1 = l_run1 * al1 + p1;
+#pragma unroll
+            for (int m = 0; m < D / 16; ++m) {
+                acc[m][0] *= al0;
+                acc[m][1] *= al1;
+                acc[m][2] *= al0;
+                acc[m][3] *= al1;
+            }
+            const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
+#pragma unroll
+            for (int m = 0; m < D / 16; ++m)
+                mma16816(acc[m], c == 0 ? (uint32_t)v16[16 * m + r] : 0u,
+                         c == 0 ? (uint32_t)v16[16 * m + r + 8] : 0u, 0u, 0u, pb0, 0u);
+        }
     }
 
     // ---------------- merge the four warps
@@ -405,6 +522,24 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         __syncwarp();
         cluster_sync_all();   // no CTA leaves while another still reads its partial
     }
+    // H2O decode step: the worst non-recent slot by (score desc, position asc), tracked as
+    // the largest key (descending-score bits << 32 | position) while the scores are written
+    const long h2o_rt = STEP == STEP_H2O ? (long)s_step[0] + 1 - p.n_recent : 0;   // recent: >= rt
+    unsigned long long vkey = 0ull;
+    int vslot = -1;
+    auto candidate = [&](int slot, int32_t ps, float score) {
+        if constexpr (STEP == STEP_H2O) {
+            if ((long)ps < h2o_rt) {
+                const unsigned long long k =
+                    ((unsigned long long)desc_bits(score) << 32) | (uint32_t)ps;
+                if (vslot < 0 || k > vkey) {
+                    vkey = k;
+                    vslot = slot;
+                }
+            }
+        }
+    };
+    float s_new = 0.f;   // H2O step: the new token's score (warp 0, lane 0)
     if ((single || clustered) && p.h2o_scores) {
         // H2O decode scores: score[j] += sum_h exp(logit_hj - lse_h) over this unit's
         // query heads, for this CTA's tokens (logits kept by this CTA; log2 domain here)
@@ -424,6 +559,22 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         }
         consumer_bar();
         float *sc = p.h2o_scores + (size_t)unit * p.C;
+        if constexpr (STEP == STEP_H2O) {
+            // the new token's probabilities (warp 0, lanes 0-3 hold heads 2c, 2c + 1), added
+            // in head order like every other slot's
+            if (warp == 0) {
+                const float L0 = h0 < p.g ? s_lse2[h0] : 0.f, L1 = h1 < p.g ? s_lse2[h1] : 0.f;
+                const float e0 = h0 < p.g ? ex2(fmaf(lnew[0], LOG2E, -L0)) : 0.f;
+                const float e1 = h1 < p.g ? ex2(fmaf(lnew[1], LOG2E, -L1)) : 0.f;
+                float add = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    add += __shfl_sync(0xffffffffu, e0, q);
+                    add += __shfl_sync(0xffffffffu, e1, q);
+                }
+                s_new = fmaf(0.f, p.h2o_keep, add * p.h2o_add);
+            }
+        }
         if constexpr (LREG) {
             // the same arithmetic as the other storage modes: lane c == 0 of each quad
             // gathers the probabilities of heads 0 .. 7 for tokens r and r + 8 of every
@@ -447,45 +598,143 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                     add_b += __shfl_sync(0xffffffffu, e[3], src);
                 }
                 const int ta = t_begin + i * TILE + 16 * warp + r, tb = ta + 8;
-                if (c == 0 && ta < t_end)
-                    sc[ta] = fmaf(old[i][0], p.h2o_keep, add_a * p.h2o_add);
-                if (c == 0 && tb < t_end)
-                    sc[tb] = fmaf(old[i][1], p.h2o_keep, add_b * p.h2o_add);
+                if (c == 0 && ta < t_end) {
+                    const float v = fmaf(old[i][0], p.h2o_keep, add_a * p.h2o_add);
+                    sc[ta] = v;
+                    if constexpr (STEP == STEP_H2O)
+                        candidate(ta, opos[i][0], v);
+                }
+                if (c == 0 && tb < t_end) {
+                    const float v = fmaf(old[i][1], p.h2o_keep, add_b * p.h2o_add);
+                    sc[tb] = v;
+                    if constexpr (STEP == STEP_H2O)
+                        candidate(tb, opos[i][1], v);
+                }
             }
-            return;
-        }
-        const float *lrow = LSM ? lsm : p.logits + ((size_t)b * p.Hq + hk * p.g) * p.C;
-        const size_t lstride = LSM ? LSM_SLOTS : p.C;
-        // four slots per thread per round, every load issued before any is used
-        constexpr int U = 4;
-        for (int j0 = t_begin + threadIdx.x; j0 < t_end; j0 += U * NCW * 32) {
-            float add[U], old[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = j0 + u * NCW * 32;
-                add[u] = 0.f;
-                old[u] = j < t_end ? sc[j] : 0.f;
-            }
-            // all heads' logits of the round in flight at once (g <= 8)
-            float lg[8][U];
-#pragma unroll
-            for (int h = 0; h < 8; ++h)
+        } else {
+            const float *lrow = LSM ? lsm : p.logits + ((size_t)b * p.Hq + hk * p.g) * p.C;
+            const size_t lstride = LSM ? LSM_SLOTS : p.C;
+            const int32_t *upos = p.pos + (size_t)unit * p.C;
+            // four slots per thread per round, every load issued before any is used
+            constexpr int U = 4;
+            for (int j0 = t_begin + threadIdx.x; j0 < t_end; j0 += U * NCW * 32) {
+                float add[U], old[U];
+                int32_t ps[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int j = j0 + u * NCW * 32;
-                    lg[h][u] = h < p.g && j < t_end ? lrow[(size_t)h * lstride + (j - lofs)] : 0.f;
+                    add[u] = 0.f;
+                    old[u] = j < t_end ? sc[j] : 0.f;
+                    ps[u] = STEP == STEP_H2O && j < t_end ? upos[j] : 0;
                 }
+                // all heads' logits of the round in flight at once (g <= 8)
+                float lg[8][U];
 #pragma unroll
-            for (int h = 0; h < 8; ++h)
-                if (h < p.g)
+                for (int h = 0; h < 8; ++h)
 #pragma unroll
-                    for (int u = 0; u < U; ++u)
-                        add[u] += ex2(fmaf(lg[h][u], LOG2E, -s_lse2[h]));
+                    for (int u = 0; u < U; ++u) {
+                        const int j = j0 + u * NCW * 32;
+                        lg[h][u] =
+                            h < p.g && j < t_end ? lrow[(size_t)h * lstride + (j - lofs)] : 0.f;
+                    }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = j0 + u * NCW * 32;
-                if (j < t_end)
-                    sc[j] = fmaf(old[u], p.h2o_keep, add[u] * p.h2o_add);
+                for (int h = 0; h < 8; ++h)
+                    if (h < p.g)
+#pragma unroll
+                        for (int u = 0; u < U; ++u)
+                            add[u] += ex2(fmaf(lg[h][u], LOG2E, -s_lse2[h]));
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = j0 + u * NCW * 32;
+                    if (j < t_end) {
+                        const float v = fmaf(old[u], p.h2o_keep, add[u] * p.h2o_add);
+                        sc[j] = v;
+                        candidate(j, ps[u], v);
+                    }
+                }
+            }
+        }
+    }
+
+    // ---------------- decode steps: the one row the step writes
+    if constexpr (STEP != STEP_NONE) {
+        __shared__ unsigned long long s_vkey[NCW];
+        __shared__ int s_vslot[NCW];
+        if constexpr (STEP == STEP_H2O) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const unsigned long long ok = __shfl_xor_sync(0xffffffffu, vkey, off);
+                const int os = __shfl_xor_sync(0xffffffffu, vslot, off);
+                if (os >= 0 && (vslot < 0 || ok > vkey)) {
+                    vkey = ok;
+                    vslot = os;
+                }
+            }
+            if (lane == 0) {
+                s_vkey[warp] = vkey;
+                s_vslot[warp] = vslot;
+            }
+            consumer_bar();
+        }
+        if (warp == 0) {
+            const int P = s_step[0];
+            int slot = -1;
+            bool grow = false;
+            if constexpr (STEP == STEP_H2O) {
+                const int budget = p.n_heavy + p.n_recent;
+                if (n_valid < budget) {
+                    slot = n_valid;
+                    grow = true;
+                } else {
+                    // at budget: the worst candidate leaves and the new token takes its slot
+                    unsigned long long best = 0ull;
+#pragma unroll
+                    for (int w = 0; w < NCW; ++w)
+                        if (s_vslot[w] >= 0 && (slot < 0 || s_vkey[w] > best)) {
+                            best = s_vkey[w];
+                            slot = s_vslot[w];
+                        }
+                    if (h2o_rt > (long)P) {
+                        // no recent window: the new token is a candidate too, and may be the
+                        // one that leaves (then nothing is written)
+                        const unsigned long long knew =
+                            ((unsigned long long)desc_bits(s_new) << 32) | (uint32_t)P;
+                        if (slot < 0 || knew > best)
+                            slot = -2;
+                    }
+                    if (n_valid > budget)
+                        slot = -1;   // more than one slot would have to go: not a decode step
+                }
+            } else {
+                slot = skip >= 0 ? skip : n_valid;
+                grow = skip < 0;
+            }
+            if (grow && slot >= p.C)
+                slot = -1;
+            if (slot == -2) {
+                // the new token left at once: the cache keeps its slots
+            } else if (slot < 0 || (p.n[unit] < 0 || p.n[unit] > p.C) || P >= (1 << 24) - 1) {
+                if (lane == 0)
+                    flag_error(p.status, DEV_CAPACITY);
+            } else {
+                const long row = p.rows.row(unit, slot);
+                constexpr int CH = D / 8;   // 16-byte chunks per row
+                if (row < 0) {
+                    if (lane == 0)
+                        flag_error(p.status, DEV_CAPACITY);
+                } else if (lane < 2 * CH) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(newtok) + lane;
+                    uint4 *dst = reinterpret_cast<uint4 *>(lane < CH ? p.K : p.V) +
+                                 (size_t)row * CH + (lane % CH);
+                    *dst = *src;
+                }
+                if (lane == 0) {
+                    p.pos[(size_t)unit * p.C + slot] = P;
+                    if constexpr (STEP == STEP_H2O)
+                        p.h2o_scores[(size_t)unit * p.C + slot] = s_new;
+                    if (grow)
+                        p.n_w[unit] = n_valid + 1;
+                }
             }
         }
     }
@@ -520,17 +769,17 @@ __global__ void k_combine(int Hq, int Hkv, int g, int D, int splits, const float
         lse[bh] = ls > 0.f ? (ms + __log2f(ls)) * LN2 : -INFINITY;
 }
 
-template <int D, int LMODE>
+template <int D, int LMODE, int STEP = STEP_NONE>
 cudaError_t launch_slots_impl(const CUtensorMap &tk, const CUtensorMap &tv, const SlotParams &sp,
                               int grid, cudaStream_t s)
 {
     using Cfg = SlotCfg<D, LMODE>;
     const cudaError_t e =
-        set_smem_once(reinterpret_cast<const void *>(k_attend_slots<D, LMODE>), Cfg::SMEM);
+        set_smem_once(reinterpret_cast<const void *>(k_attend_slots<D, LMODE, STEP>), Cfg::SMEM);
     if (e != cudaSuccess)
         return e;
     if (sp.cluster <= 1) {
-        k_attend_slots<D, LMODE><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
+        k_attend_slots<D, LMODE, STEP><<<grid, NTHREADS, Cfg::SMEM, s>>>(tk, tv, sp);
         return cudaGetLastError();
     }
     // the splits of a unit (consecutive blocks) form one cluster
@@ -546,7 +795,7 @@ cudaError_t launch_slots_impl(const CUtensorMap &tk, const CUtensorMap &tv, cons
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_attend_slots<D, LMODE>, tk, tv, sp);
+    return cudaLaunchKernelEx(&cfg, k_attend_slots<D, LMODE, STEP>, tk, tv, sp);
 }
 
 } // namespace
@@ -607,6 +856,58 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
     if (e != cudaSuccess || on_chip)
         return e;
     return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);
+}
+
+cudaError_t launch_decode_step(const StepLaunch &a, cudaStream_t s)
+{
+    const kvc_slot_cache &c = a.c;
+    const int units = c.B * c.Hkv;
+    CUtensorMap tk, tv;
+    const uint64_t rows = c.block_table ? (uint64_t)c.num_pages * TILE : (uint64_t)units * c.C;
+    if (!encode_tmap_2d_f16(&tk, c.K, c.D, rows, 64, TILE) ||
+        !encode_tmap_2d_f16(&tv, c.V, c.D, rows, 64, TILE))
+        return cudaErrorInvalidValue;
+    const bool h2o = a.scores != nullptr;
+    if (h2o && c.C > LSM_SLOTS)
+        return cudaErrorInvalidValue;
+    SlotParams sp{};
+    sp.Hq = a.Hq;
+    sp.Hkv = c.Hkv;
+    sp.C = c.C;
+    sp.g = a.Hq / c.Hkv;
+    sp.splits = 1;
+    sp.tiles_per_split = (c.C + TILE - 1) / TILE;
+    sp.q = a.q;
+    sp.o = a.o;
+    sp.n = c.n;
+    sp.lse = a.lse;
+    sp.scale = a.scale;
+    sp.scale_log2 = a.scale * LOG2E;
+    sp.cluster = 1;
+    sp.h2o_scores = a.scores;
+    sp.h2o_keep = a.h2o_keep;
+    sp.h2o_add = a.h2o_add;
+    sp.rows = SlotRows{c.block_table, c.C, c.num_pages};
+    sp.status = dev_status_ptr();
+    sp.k_new = a.k_new;
+    sp.v_new = a.v_new;
+    sp.K = c.K;
+    sp.V = c.V;
+    sp.pos = c.pos;
+    sp.n_w = c.n;
+    sp.seqlen = c.seqlen;
+    sp.n_heavy = a.n_heavy;
+    sp.n_recent = a.n_recent;
+    sp.n_sink = a.n_sink;
+    if (!h2o)
+        return c.D == 128 ? launch_slots_impl<128, LM_NONE, STEP_STREAM>(tk, tv, sp, units, s)
+                          : launch_slots_impl<64, LM_NONE, STEP_STREAM>(tk, tv, sp, units, s);
+    const bool regs = c.C <= LREG_TILES * TILE;
+    if (c.D == 128)
+        return regs ? launch_slots_impl<128, LM_REGS, STEP_H2O>(tk, tv, sp, units, s)
+                    : launch_slots_impl<128, LM_SMEM, STEP_H2O>(tk, tv, sp, units, s);
+    return regs ? launch_slots_impl<64, LM_REGS, STEP_H2O>(tk, tv, sp, units, s)
+                : launch_slots_impl<64, LM_SMEM, STEP_H2O>(tk, tv, sp, units, s);
 }
 
 cudaError_t launch_combine(int B, int Hq, int Hkv, int D, int splits, const float *part_o,

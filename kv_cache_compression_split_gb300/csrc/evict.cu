@@ -67,15 +67,6 @@ __device__ __forceinline__ uint64_t philox_key(uint32_t k0, uint32_t k1, uint32_
     return ((uint64_t)c0 << 32) | c1;
 }
 
-// Order-preserving map of a float to uint32, reversed so larger scores give
-// smaller keys.
-__device__ __forceinline__ uint32_t desc_bits(float x)
-{
-    uint32_t u = __float_as_uint(x);
-    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return ~u;
-}
-
 struct Shared {
     uint32_t hist[256];
     int warp_tot[NWARPS];

@@ -45,6 +45,15 @@ __device__ __forceinline__ void flag_error(int *status, int bit)
         atomicOr(status, bit);
 }
 
+// Order-preserving map of a float to uint32, reversed so larger scores give
+// smaller keys (the H2O eviction order: score descending).
+__device__ __forceinline__ uint32_t desc_bits(float x)
+{
+    uint32_t u = __float_as_uint(x);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ~u;
+}
+
 // ---------------------------------------------------------------- clusters
 
 // Every thread of every CTA of the cluster arrives, then waits for all of them;

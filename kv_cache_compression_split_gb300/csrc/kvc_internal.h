@@ -64,6 +64,22 @@ struct AttendLaunch {
 };
 cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s);
 
+// One decode step of H2O (scores != nullptr) or StreamingLLM in one launch of the slot
+// attention kernel (one split): the new token joins the attention and takes one slot.
+struct StepLaunch {
+    kvc_slot_cache c;
+    int Hq;
+    const uint16_t *q;
+    uint16_t *o;
+    float *lse;
+    const uint16_t *k_new, *v_new;
+    float *scores;
+    float h2o_keep, h2o_add;
+    int n_heavy, n_recent, n_sink;
+    float scale;
+};
+cudaError_t launch_decode_step(const StepLaunch &a, cudaStream_t s);
+
 struct KiviAttendLaunch {
     int B, Hq, Hkv, D, bits, R, Cq;
     const uint16_t *q;

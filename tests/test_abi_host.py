@@ -50,6 +50,10 @@ def test_null_arguments_are_rejected_without_touching_a_gpu(kvc):
     assert lib.kvc_h2o_evict(None, None, 1, 1, None) == kvc.KVC_ERR_INVALID_ARG
     assert lib.kvc_stream_evict(None, 1, 1, None) == kvc.KVC_ERR_INVALID_ARG
     assert lib.kvc_stream_append(None, None, None, 1, 1, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_h2o_decode_step(None, None, 8, None, None, None, None, None, 64, 448, 0.0,
+                                   None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_stream_decode_step(None, 8, None, None, None, None, None, 64, 448,
+                                      None) == kvc.KVC_ERR_INVALID_ARG
     assert lib.kvc_random_evict(None, 0, 0.5, 1, 0, None) == kvc.KVC_ERR_INVALID_ARG
     assert lib.kvc_read_device_status(None, None) == kvc.KVC_ERR_INVALID_ARG
     # a descriptor with an unsupported head dim (pointers are never dereferenced on the host)
