@@ -314,15 +314,16 @@ def run_gpu(args, rank, world):
         ws_h2o, nb_h2o = ws_for(h2o)
         ws_st, nb_st = ws_for(st)
         ws_kv, nb_kv = ws_for(kv4)
-        # kernels per step: a one-token slot append is 1 launch, a KIVI append 2 (pack +
-        # length), attention 1 (+1 combine with several splits; +1 score pass for H2O then),
-        # the H2O eviction 1; StreamingLLM's append takes the leaving token's slot (no eviction)
-        launches_per_step = ((1 + 1 + (nb_fp > 0)) + (1 + 1 + 2 * (nb_h2o > 0) + 1) +
-                             (2 + 1 + (nb_kv > 0)) + (1 + 1 + (nb_st > 0)))
+        # kernels per step: the FP16 append 1 + attention 1 (+1 combine with several splits);
+        # the H2O and StreamingLLM decode steps 1 each (append, attention, score update and
+        # eviction in one launch); the KIVI append 2 (pack + length) + attention 1 (+1)
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        h2o_launches = 1 if B * Hkv <= 4 * n_sm else 3   # kvc_h2o_decode_step's own choice
+        launches_per_step = (1 + 1 + (nb_fp > 0)) + h2o_launches + (2 + 1 + (nb_kv > 0)) + 1
         torch.cuda.synchronize(dev)
 
-    names = ["fp16_append", "fp16_attend", "h2o_append", "h2o_attend_accumulate", "h2o_evict",
-             "kivi4_append", "kivi4_attend", "stream_append", "stream_attend"]
+    names = ["fp16_append", "fp16_attend", "h2o_step", "kivi4_append", "kivi4_attend",
+             "stream_step"]
 
     def step(i, ev=None, outs_override=None):
         """One decode step of all four methods on the launch stream; ev: per-call events."""
@@ -334,16 +335,15 @@ def run_gpu(args, rank, world):
         mark(0)
         kvc.kvc_append(fp, kn[i, 0], vn[i, 0], stream=stream); mark(1)
         kvc.kvc_decode_attend(fp, qs[i, 0], outs[0], workspace=ws_fp, stream=stream); mark(2)
-        kvc.kvc_append(h2o, kn[i, 1], vn[i, 1], stream=stream); mark(3)
-        # attention and the heavy-hitter score update in one launch (logits kept on chip)
-        kvc.kvc_decode_attend(h2o, qs[i, 1], outs[1], lse=lse, workspace=ws_h2o,
-                              h2o_scores=h2o_scores, stream=stream); mark(4)
-        kvc.kvc_h2o_evict(h2o, h2o_scores, n_heavy, n_recent, stream=stream); mark(5)
-        kvc.kvc_append_quant(kv4, kn[i, 2], vn[i, 2], stream=stream); mark(6)
-        kvc.kvc_decode_attend(kv4, qs[i, 2], outs[2], workspace=ws_kv, stream=stream); mark(7)
-        # StreamingLLM: the leaving token's slot takes the new token; no eviction launch
-        kvc.kvc_stream_append(st, kn[i, 3], vn[i, 3], n_sink, n_recent, stream=stream); mark(8)
-        kvc.kvc_decode_attend(st, qs[i, 3], outs[3], workspace=ws_st, stream=stream); mark(9)
+        # H2O: append + attention + score update (logits on chip) + eviction in one call (one
+        # launch, or three for batches of more than four units per SM)
+        kvc.kvc_h2o_decode_step(h2o, h2o_scores, qs[i, 1], kn[i, 1], vn[i, 1], outs[1], lse,
+                                n_heavy, n_recent, stream=stream); mark(3)
+        kvc.kvc_append_quant(kv4, kn[i, 2], vn[i, 2], stream=stream); mark(4)
+        kvc.kvc_decode_attend(kv4, qs[i, 2], outs[2], workspace=ws_kv, stream=stream); mark(5)
+        # StreamingLLM: attention without the token that left; its slot takes the new one
+        kvc.kvc_stream_decode_step(st, qs[i, 3], kn[i, 3], vn[i, 3], outs[3], None, n_sink,
+                                   n_recent, stream=stream); mark(6)
 
     branches = [torch.cuda.Stream(dev) for _ in range(4)]
 
@@ -359,14 +359,12 @@ def run_gpu(args, rank, world):
         s0, s1, s2, s3 = branches
         kvc.kvc_append(fp, kn[i, 0], vn[i, 0], stream=s0)
         kvc.kvc_decode_attend(fp, qs[i, 0], outs[0], workspace=ws_fp, stream=s0)
-        kvc.kvc_append(h2o, kn[i, 1], vn[i, 1], stream=s1)
-        kvc.kvc_decode_attend(h2o, qs[i, 1], outs[1], lse=lse, workspace=ws_h2o,
-                              h2o_scores=h2o_scores, stream=s1)
-        kvc.kvc_h2o_evict(h2o, h2o_scores, n_heavy, n_recent, stream=s1)
+        kvc.kvc_h2o_decode_step(h2o, h2o_scores, qs[i, 1], kn[i, 1], vn[i, 1], outs[1], lse,
+                                n_heavy, n_recent, stream=s1)
         kvc.kvc_append_quant(kv4, kn[i, 2], vn[i, 2], stream=s2)
         kvc.kvc_decode_attend(kv4, qs[i, 2], outs[2], workspace=ws_kv, stream=s2)
-        kvc.kvc_stream_append(st, kn[i, 3], vn[i, 3], n_sink, n_recent, stream=s3)
-        kvc.kvc_decode_attend(st, qs[i, 3], outs[3], workspace=ws_st, stream=s3)
+        kvc.kvc_stream_decode_step(st, qs[i, 3], kn[i, 3], vn[i, 3], outs[3], None, n_sink,
+                                   n_recent, stream=s3)
         for bs in branches:
             join = torch.cuda.Event()
             join.record(bs)
@@ -437,16 +435,21 @@ def run_gpu(args, rank, world):
     kv_T = [t - kv_shift for t in steps_T]   # KIVI-4 tokens attended (its prompt is shorter)
     b_kv = [kivi_bytes(t, w.kivi_R, B, Hkv, Hq, D, 4) for t in kv_T]
     ms = lambda nm: sum(per_call[nm])
-    slot_bytes_total = sum(b_fp) + b_h2o * args.steps + b_st * args.steps
-    slot_ms = ms("fp16_attend") + ms("h2o_attend_accumulate") + ms("stream_attend")
+    # the H2O step also reads and writes the 513 scores of every unit and writes one row
+    b_h2o_step = b_h2o + B * Hkv * 513 * 4 * 2 + B * Hkv * D * 2 * 2
+    b_st_step = b_st + B * Hkv * D * 2 * 2
+    slot_bytes_total = sum(b_fp) + b_h2o_step * args.steps + b_st_step * args.steps
+    slot_ms = ms("fp16_attend") + ms("h2o_step") + ms("stream_step")
     kernels = {
         "attend_slots(fp16+h2o+stream)": {"bytes_per_step": slot_bytes_total / args.steps,
                                           "ms_per_step": slot_ms / args.steps},
         "attend_fp16": {"bytes_per_step": sum(b_fp) / args.steps,
                         "ms_per_step": ms("fp16_attend") / args.steps},
-        "attend_h2o512": {"bytes_per_step": b_h2o,
-                          "ms_per_step": ms("h2o_attend_accumulate") / args.steps},
-        "attend_stream512": {"bytes_per_step": b_st, "ms_per_step": ms("stream_attend") / args.steps},
+        "attend_h2o512": {"bytes_per_step": b_h2o_step, "ms_per_step": ms("h2o_step") / args.steps,
+                          "launch": "kvc_h2o_decode_step: append + attention + score update + "
+                                    "eviction (three launches at this batch)"},
+        "attend_stream512": {"bytes_per_step": b_st_step, "ms_per_step": ms("stream_step") / args.steps,
+                             "launch": "kvc_stream_decode_step: append + attention"},
         "attend_kivi4": {"bytes_per_step": sum(b_kv) / args.steps,
                          "ms_per_step": ms("kivi4_attend") / args.steps},
     }
@@ -458,14 +461,14 @@ def run_gpu(args, rank, world):
         v = sorted(per_call[nm])
         q = lambda f: v[min(len(v) - 1, int(f * (len(v) - 1) + 0.5))]
         return {"ms_median": statistics.median(v), "ms_p10": q(0.1), "ms_p90": q(0.9)}
-    for key, nm in (("attend_fp16", "fp16_attend"), ("attend_h2o512", "h2o_attend_accumulate"),
-                    ("attend_stream512", "stream_attend"), ("attend_kivi4", "kivi4_attend")):
+    for key, nm in (("attend_fp16", "fp16_attend"), ("attend_h2o512", "h2o_step"),
+                    ("attend_stream512", "stream_step"), ("attend_kivi4", "kivi4_attend")):
         kernels[key].update(spread(nm))
     methods = {
         "fp16": ms("fp16_append") + ms("fp16_attend"),
-        "h2o512": ms("h2o_append") + ms("h2o_attend_accumulate") + ms("h2o_evict"),
+        "h2o512": ms("h2o_step"),
         "kivi4": ms("kivi4_append") + ms("kivi4_attend"),
-        "stream512": ms("stream_append") + ms("stream_attend"),
+        "stream512": ms("stream_step"),
     }
     methods = {k: {"ms_per_step": v / args.steps, "tokens_per_s": B / (v / args.steps * 1e-3)}
                for k, v in methods.items()}
@@ -578,7 +581,7 @@ def run_gpu(args, rank, world):
     graph_T = [T0 + args.warmup + k for k in range(args.steps)]
     step_bytes = (sum(slot_bytes(t, B, Hkv, Hq, D) +
                       kivi_bytes(t - kv_shift, w.kivi_R, B, Hkv, Hq, D, 4)
-                      for t in graph_T) / args.steps + b_h2o + b_st)
+                      for t in graph_T) / args.steps + b_h2o_step + b_st_step)
     step_roofline = {"bytes_per_step": step_bytes,
                      "gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
                      "frac_of_hbm": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak}
@@ -635,19 +638,21 @@ def h2o_variant_rows(kvc, dev, stream, src, src_scores, qs, kn, vn, n_heavy, n_r
             e0.record(stream)
             for i in range(steps):
                 k = i % qs.shape[0]
+                if trig is None:   # decayed scores, eviction every step: the one-launch step
+                    kvc.kvc_h2o_decode_step(c, sc, qs[k], kn[k], vn[k], o, lse, n_heavy, n_recent,
+                                            decay, stream=stream)
+                    continue
                 kvc.kvc_append(c, kn[k], vn[k], stream=stream)
                 kvc.kvc_decode_attend(c, qs[k], o, lse=lse, workspace=ws, num_splits=1,
                                       h2o_scores=sc, h2o_decay=decay, stream=stream)
-                if trig is None:
-                    kvc.kvc_h2o_evict(c, sc, n_heavy, n_recent, stream=stream)
-                else:
-                    kvc.kvc_h2o_evict_when(c, sc, n_heavy, n_recent, trig, stream=stream)
+                kvc.kvc_h2o_evict_when(c, sc, n_heavy, n_recent, trig, stream=stream)
             e1.record(stream)
             torch.cuda.synchronize(dev)
             ms = e0.elapsed_time(e1) / steps
             out[name] = {"ms_per_step": ms, "tokens_per_s": B / (ms * 1e-3), "steps": steps,
                          "shape": f"B={B} GQA {Hq}/{Hkv} D={D}, budget {budget}" +
-                                  (f", decay {decay}, evict every step" if trig is None else
+                                  (f", decay {decay}, evict every step (kvc_h2o_decode_step)"
+                                   if trig is None else
                                    f", evict when n >= {trig} (slots attended {budget + 1}.."
                                    f"{trig})")}
             del c, sc, ws
@@ -888,7 +893,13 @@ def config_rows(kvc, W, dev, stream, hbm_peak):
         h_ev = lambda: kvc.kvc_h2o_evict(hc, hsc, w.n_heavy, w.n_recent, stream=stream)
         g_att = in_graph_ms(stream, h_att, flush, reset=lambda: (reset_h2o(), h_app()))
         g_step = in_graph_ms(stream, lambda: (h_app(), h_att(), h_ev()), flush, reset=reset_h2o)
+        h_step = lambda: kvc.kvc_h2o_decode_step(hc, hsc, q, kn, vn, o, lse, w.n_heavy, w.n_recent,
+                                                 stream=stream)
+        (t_fused,) = step_times(reset_h2o, [h_step])
+        g_fused = in_graph_ms(stream, h_step, flush, reset=reset_h2o)
         out[f"{w.name}/h2o512"] = {
+            "fused_step_ms": t_fused, "fused_step_ms_in_graph": g_fused,
+            "fused_step_frac_of_hbm_in_graph": nb / (g_fused * 1e-3) / 1e9 / hbm_peak,
             "ms": t_att, "slots": 513, "gbs": nb / (t_att * 1e-3) / 1e9,
             "frac_of_hbm": nb / (t_att * 1e-3) / 1e9 / hbm_peak, "tokens_per_s": B / (t_att * 1e-3),
             "ms_in_graph": g_att, "frac_of_hbm_in_graph": nb / (g_att * 1e-3) / 1e9 / hbm_peak,
@@ -904,7 +915,13 @@ def config_rows(kvc, W, dev, stream, hbm_peak):
         s_att = lambda: kvc.kvc_decode_attend(stc, q, o, workspace=ws_h, stream=stream)
         g_att = in_graph_ms(stream, s_att, flush, reset=lambda: (reset_st(), s_app()))
         g_step = in_graph_ms(stream, lambda: (s_app(), s_att()), flush, reset=reset_st)
+        s_step = lambda: kvc.kvc_stream_decode_step(stc, q, kn, vn, o, None, w.n_sink, w.n_recent,
+                                                    stream=stream)
+        (t_fused,) = step_times(reset_st, [s_step])
+        g_fused = in_graph_ms(stream, s_step, flush, reset=reset_st)
         out[f"{w.name}/stream512"] = {
+            "fused_step_ms": t_fused, "fused_step_ms_in_graph": g_fused,
+            "fused_step_frac_of_hbm_in_graph": nb / (g_fused * 1e-3) / 1e9 / hbm_peak,
             "ms": t_att, "slots": 513, "gbs": nb / (t_att * 1e-3) / 1e9,
             "frac_of_hbm": nb / (t_att * 1e-3) / 1e9 / hbm_peak, "tokens_per_s": B / (t_att * 1e-3),
             "ms_in_graph": g_att, "frac_of_hbm_in_graph": nb / (g_att * 1e-3) / 1e9 / hbm_peak,
@@ -1235,6 +1252,22 @@ def run_profile(args):
         ws = torch.empty(kvc.kvc_h2o_workspace_size(kp.shape[0], Hq, L) // 4, device=dev)
         for _ in range(3):
             kvc.kvc_h2o_accumulate_prefill(qp, kp, sc, ws, L)
+    elif what in ("h2o_step", "stream_step"):
+        # the one-launch decode steps at the heavy-load shape: 512 slots per unit (64 sinks or
+        # heavy + 448 recent), then three steps (each appends one token and keeps 512 / 513)
+        cache = kvc.SlotCache.empty(B, Hkv, 520, D, device=dev)
+        kvc.kvc_append(cache, K[:, :, T - 512:T].contiguous(), V[:, :, T - 512:T].contiguous())
+        cache.pos[:, :, :512] = torch.cat([torch.arange(w.n_sink),
+                                           torch.arange(T - w.n_recent, T)]).int().to(dev)
+        cache.seqlen.fill_(T)
+        sc = torch.rand(B, Hkv, 520, device=dev)
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+        kn = torch.randn(B, Hkv, 1, D, device=dev, dtype=torch.float16)
+        for _ in range(3):
+            if what == "h2o_step":
+                kvc.kvc_h2o_decode_step(cache, sc, q, kn, kn, o, lse, w.n_heavy, w.n_recent)
+            else:
+                kvc.kvc_stream_decode_step(cache, q, kn, kn, o, None, w.n_sink, w.n_recent)
     elif what == "stream_append":
         # the heavy-load StreamingLLM-512 decode append: 512 slots of sinks + recent window,
         # then three one-token appends (the first grows the window to 513, the next two
@@ -1339,9 +1372,9 @@ def run_grid(args):
       prefill_ms  compress a T-token prompt: FP16 append; KIVI-b / GEAR-4 pack; StreamingLLM and H2O evict
                   to 64 + 448 (H2O after its two-pass score pass); random eviction at each keep
                   ratio with the first min(1024, T/2) tokens locked
-      decode_ms   one decode step: append + attention (+ H2O's fused score update + eviction, or
-                  StreamingLLM's eviction) over the cache the prefill left; for random eviction,
-                  attention over the kept slots
+      decode_ms   one decode step over the cache the prefill left: FP16 and KIVI append +
+                  attention; H2O and StreamingLLM one launch each (kvc_h2o_decode_step,
+                  kvc_stream_decode_step); for random eviction, attention over the kept slots
     Every timing is the median of 3 repetitions after one warm-up, with L2 flushed (a 512 MB
     write, then a 512 MB read) before each; one JSON line per cell."""
     import torch
@@ -1393,6 +1426,17 @@ def run_grid(args):
                 C = T + 8
                 fp = kvc.SlotCache.empty(B, Hkv, C, D, device=dev)
 
+                def small_cache(src, Cs=520):
+                    # the first Cs slots of an evicted cache as a decode cache of capacity Cs
+                    c = kvc.SlotCache.empty(B, Hkv, Cs, D, device=dev)
+                    m = min(Cs, src.C)
+                    c.K[:, :, :m] = src.K[:, :, :m]
+                    c.V[:, :, :m] = src.V[:, :, :m]
+                    c.pos[:, :, :m] = src.pos[:, :, :m]
+                    c.n.copy_(src.n)
+                    c.seqlen.copy_(src.seqlen)
+                    return c
+
                 def refill():
                     fp.n.zero_()
                     fp.seqlen.zero_()
@@ -1426,13 +1470,15 @@ def run_grid(args):
                 # ---- StreamingLLM: evict the prompt to 64 sinks + 448 recent, then steady steps
                 cell["prefill_ms"]["stream512"] = timed(
                     lambda: kvc.kvc_stream_evict(fp, n_sink, n_recent, stream=stream), setup=refill)
-                ws_s = ws_for(fp, q)
+                # the decode cache: the kept window in a 520-slot cache, one-launch steps
+                st = small_cache(fp)
 
                 def stream_step():
-                    kvc.kvc_stream_append(fp, kn, vn, n_sink, n_recent, stream=stream)
-                    kvc.kvc_decode_attend(fp, q, o, workspace=ws_s, stream=stream)
+                    kvc.kvc_stream_decode_step(st, q, kn, vn, o, None, n_sink, n_recent,
+                                               stream=stream)
                 cell["decode_ms"]["stream512"] = timed(stream_step)
                 cell["slots_attended"]["stream512"] = n_sink + n_recent + 1
+                del st
                 # ---- H2O: two-pass prefill score pass (in batch chunks of <= 8 GB of queries)
                 # then evict to 64 heavy + 448 recent; decode steps with the fused update
                 scores = torch.zeros(B, Hkv, C, dtype=torch.float32, device=dev)
@@ -1449,18 +1495,17 @@ def run_grid(args):
                     kvc.kvc_h2o_evict(fp, scores, n_heavy, n_recent, stream=stream)
                 cell["prefill_ms"]["h2o512"] = timed(h2o_prefill, setup=refill, reps=1)
                 del qp, pws
-                logits = torch.empty(B, Hq, C, dtype=torch.float32, device=dev)
                 lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
-                ws_h = ws_for(fp, q, 1)
+                hc = small_cache(fp)
+                hsc = torch.zeros(B, Hkv, 520, dtype=torch.float32, device=dev)
+                hsc[:, :, :min(520, C)] = scores[:, :, :min(520, C)]
 
                 def h2o_step():
-                    kvc.kvc_append(fp, kn, vn, stream=stream)
-                    kvc.kvc_decode_attend(fp, q, o, logits=logits, lse=lse, workspace=ws_h,
-                                          num_splits=1, h2o_scores=scores, stream=stream)
-                    kvc.kvc_h2o_evict(fp, scores, n_heavy, n_recent, stream=stream)
+                    kvc.kvc_h2o_decode_step(hc, hsc, q, kn, vn, o, lse, n_heavy, n_recent,
+                                            stream=stream)
                 cell["decode_ms"]["h2o512"] = timed(h2o_step)
                 cell["slots_attended"]["h2o512"] = n_heavy + n_recent + 1
-                del fp, scores, logits, lse
+                del fp, scores, lse, hc, hsc
                 # ---- KIVI-4 / KIVI-2 / GEAR-4: pack the prompt, then append + attention
                 for bits, gear in ((4, False), (2, False), (4, True)):
                     name = f"gear{bits}" if gear else f"kivi{bits}"
@@ -1596,8 +1641,10 @@ def main():
                                   "algorithmic_bytes": res["kernels"][k]["bytes_per_step"]}
                              for nm, k, kn_ in (
                                  ("h2o512", "attend_h2o512",
-                                  "k_attend_slots (H2O-512, fused score update)"),
-                                 ("stream512", "attend_stream512", "k_attend_slots (Stream-512)"),
+                                  "k_attend_slots decode step (H2O-512: append, attention, "
+                                  "score update, eviction)"),
+                                 ("stream512", "attend_stream512",
+                                  "k_attend_slots decode step (Stream-512: append, attention)"),
                                  ("kivi4", "attend_kivi4", "k_attend_kivi (KIVI-4)"))}},
             "cpu_baseline": cpu,
             "clocks": res["clocks"],

@@ -246,14 +246,18 @@ enum { KVC_KIND_SLOTS = 0, KVC_KIND_KIVI = 1 };
  *               step's attention probabilities are folded into the heavy-hitter
  *               scores in the same launch, exactly as
  *               kvc_h2o_accumulate(KVC_H2O_DECODE) with decay h2o_decay would.
- *               With logits NULL the launch keeps the logits on chip: it then
- *               runs in one split (num_splits 0 or 1; another value is
- *               KVC_ERR_INVALID_ARG) and needs C <= KVC_H2O_ONCHIP_MAX_SLOTS
- *               (else KVC_ERR_UNSUPPORTED); up to 576 slots the logits stay in
- *               registers, beyond that in shared memory (fewer pipeline stages).
- *               All three storage modes give bit-identical o, lse and scores.
- *               With logits given, any split count works (several splits add
- *               one kvc_h2o_accumulate launch).
+ *               With logits NULL the launch keeps the logits on chip, each
+ *               split its own: it then runs in at most 8 splits (a larger
+ *               num_splits is KVC_ERR_INVALID_ARG) of at most
+ *               KVC_H2O_ONCHIP_MAX_SLOTS slots each (else KVC_ERR_UNSUPPORTED);
+ *               up to 576 slots per split the logits stay in registers, beyond
+ *               that in shared memory (fewer pipeline stages).  With 2 to 8
+ *               splits (logits on chip or not) the splits of a unit run as one
+ *               thread-block cluster that merges them on chip and updates the
+ *               scores in the same launch; with more splits (a logits array is
+ *               then needed) the scores are updated by one kvc_h2o_accumulate
+ *               launch after the combine.  For the same split count all
+ *               storage modes give bit-identical o, lse and scores.
  *   h2o_decay   0 (plain H2O, scores += p) or lambda in (0, 1) (decayed
  *               scores = lambda * scores + (1 - lambda) * p); see kvc_h2o_args
  */
@@ -444,9 +448,13 @@ KVC_API kvc_status kvc_stream_append(const kvc_slot_cache *cache, const uint16_t
  * that leaves (the worst non-recent slot by score descending, position
  * ascending), with its score set to the new token's, or into slot n while the
  * unit is below budget (n += 1); with n_recent = 0 the new token itself may be
- * the one that leaves, and then nothing is written.  seqlen += 1.  One split per unit; C at most
- * KVC_H2O_ONCHIP_MAX_SLOTS (else KVC_ERR_UNSUPPORTED); Hkv at most 127; positions
- * below 2^24 - 1.  A unit above budget or at capacity sets KVC_DEV_CAPACITY and
+ * the one that leaves, and then nothing is written.  seqlen += 1.  One split per
+ * unit; C at most KVC_H2O_ONCHIP_MAX_SLOTS and a multiple of 4 (else
+ * KVC_ERR_UNSUPPORTED); Hkv at most 127; positions below 2^24 - 1.  For batches
+ * of more than four units per SM the call issues the three launches instead
+ * (append, attention with the fused update, eviction; the results are the same),
+ * which measured faster there.  A unit above budget is outside the contract: the
+ * one-launch form sets KVC_DEV_CAPACITY and
  * keeps its slots (its o, lse and scores are still written).  While the kernel
  * runs, seqlen[b] carries an arrival count in its top 8 bits: nothing else may
  * read it concurrently.

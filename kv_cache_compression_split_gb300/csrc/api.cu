@@ -539,7 +539,7 @@ kvc_status kvc_h2o_decode_step(const kvc_slot_cache *cache, float *scores, int H
         return st;
     if (!scores)
         return KVC_ERR_INVALID_ARG;
-    if (cache->C > H2O_ONCHIP_MAX_SLOTS)
+    if (cache->C > H2O_ONCHIP_MAX_SLOTS || cache->C % 4 != 0)
         return KVC_ERR_UNSUPPORTED;
     StepLaunch L{};
     L.c = *cache;
@@ -555,7 +555,31 @@ kvc_status kvc_h2o_decode_step(const kvc_slot_cache *cache, float *scores, int H
     L.n_heavy = n_heavy;
     L.n_recent = n_recent;
     L.scale = 1.0f / sqrtf((float)cache->D);
-    return from_cuda(launch_decode_step(L, stream));
+    const int units = cache->B * cache->Hkv;
+    if (units <= 4 * sm_count())
+        return from_cuda(launch_decode_step(L, stream));
+    // Many units (more than four per SM): the same step as three launches, append ->
+    // attention with the fused score update (logits on chip, one split) -> eviction, which
+    // measured faster there (the one-launch kernel's longer tail per CTA is not hidden over
+    // many waves; at 4096 units 192 vs 201 us, at 256 units 25 vs 22 us in a CUDA graph)
+    cudaError_t e = launch_append_slots(*cache, k_new, v_new, 1, stream);
+    if (e == cudaSuccess) {
+        AttendLaunch A{cache->B, Hq, cache->Hkv, cache->D, cache->C, q, o, cache->K, cache->V,
+                       cache->n, nullptr, lse, nullptr, nullptr, 1, (cache->C + TILE - 1) / TILE,
+                       L.scale, scores, L.h2o_keep, L.h2o_add, false, cache->block_table,
+                       cache->num_pages};
+        e = launch_attend_slots(A, stream);
+    }
+    if (e == cudaSuccess) {
+        EvictLaunch ev{};
+        ev.kind = EVICT_H2O;
+        ev.c = *cache;
+        ev.scores = scores;
+        ev.n_heavy = n_heavy;
+        ev.n_recent = n_recent;
+        e = launch_evict(ev, stream);
+    }
+    return from_cuda(e);
 }
 
 kvc_status kvc_stream_decode_step(const kvc_slot_cache *cache, int Hq, const uint16_t *q,

@@ -55,7 +55,9 @@ template <int D, int LMODE = LM_NONE> struct SlotCfg {
     // the mbarriers (full, empty, new token), then the decode step's new K and V rows
     static constexpr int BAR_BYTES = (2 * NSTAGE + 1) * 8;
     static constexpr int NEWTOK_OFF = (BAR_BYTES + 15) / 16 * 16;
-    static constexpr int SMEM = NSTAGE * STAGE_BYTES + LSM_BYTES + 1024 + NEWTOK_OFF + 2 * D * 2;
+    // then the H2O step's copy of the unit's positions (up to LSM_SLOTS)
+    static constexpr int SPOS_OFF = NEWTOK_OFF + 2 * D * 2;
+    static constexpr int SMEM = NSTAGE * STAGE_BYTES + LSM_BYTES + 1024 + SPOS_OFF + LSM_SLOTS * 4;
     static_assert(NCW * (8 * D + 16) * 4 <= NSTAGE * STAGE_BYTES, "combine scratch must fit");
     // this CTA's merged partial for the cluster merge, after the warps' scratch
     static constexpr int CP_OFF = NCW * (8 * D + 16) * 4;
@@ -123,6 +125,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     uint64_t *empty = full + Cfg::NSTAGE;
     uint64_t *ntbar = empty + Cfg::NSTAGE;   // the decode step's new K/V rows have landed
     uint8_t *newtok = reinterpret_cast<uint8_t *>(full) + Cfg::NEWTOK_OFF;   // K row, V row
+    const int32_t *spos = reinterpret_cast<const int32_t *>(reinterpret_cast<uint8_t *>(full) +
+                                                            Cfg::SPOS_OFF);   // H2O step
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int unit = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
@@ -130,6 +134,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 
     // token range of this split
     int n_valid = p.n[unit];
+    const bool n_bad = n_valid > p.C || n_valid < 0;   // flagged; a decode step then writes nothing
     if (n_valid > p.C) {
         if (threadIdx.x == 0)
             flag_error(p.status, DEV_CAPACITY);
@@ -147,16 +152,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], NCW);
         }
-        mbar_init(ntbar, 1);
+        // decode steps: complete when the new rows have landed (the producer's bulk copies)
+        // and the position P has been read (consumer warp 1)
+        mbar_init(ntbar, STEP != STEP_NONE ? 2 : 1);
         fence_mbar_init();
-        if constexpr (STEP != STEP_NONE) {
-            const int old = atomicAdd(&p.seqlen[b], 1 << 24);
-            if ((old >> 24) + 1 == p.Hkv)
-                atomicAdd(&p.seqlen[b], 1 - (p.Hkv << 24));
-            s_step[0] = old & 0xffffff;
-            s_step[1] = -1;
-            s_step[2] = -1;
-        }
+        s_step[1] = -1;
+        s_step[2] = -1;
     }
     __syncthreads();
 
@@ -164,9 +165,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         // ---------------- producer: the step's new K/V rows (bulk copies), then TMA K/V
         // tiles into the stage ring
         if (STEP != STEP_NONE && lane == 0) {
-            mbar_arrive_expect_tx(ntbar, 2 * D * 2);
+            // the H2O step also copies the unit's positions (C is a multiple of 4, so the
+            // row starts on 16 bytes; n_valid rounded up to 4 slots stays within C)
+            const int pbytes = STEP == STEP_H2O ? (n_valid + 3) / 4 * 16 : 0;
+            mbar_arrive_expect_tx(ntbar, 2 * D * 2 + pbytes);
             bulk_load(newtok, p.k_new + (size_t)unit * D, D * 2, ntbar);
             bulk_load(newtok + D * 2, p.v_new + (size_t)unit * D, D * 2, ntbar);
+            if (pbytes > 0)
+                bulk_load(reinterpret_cast<uint8_t *>(full) + Cfg::SPOS_OFF,
+                          p.pos + (size_t)unit * p.C, pbytes, ntbar);
         }
         if (lane == 0 && ntiles > 0) {
             prefetch_tmap(&tmK);
@@ -206,6 +213,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const int r = lane >> 2, c = lane & 3;
     const int mi = lane >> 3, ri = lane & 7;
 
+    if (STEP != STEP_NONE && warp == 1 && lane == 0) {
+        // the new token's position: every CTA of the sequence adds an arrival and the last
+        // one advances seqlen.  The round trip overlaps the first tiles' loads; the threads
+        // that need P wait on ntbar.
+        const int old = atomicAdd(&p.seqlen[b], 1 << 24);
+        if ((old >> 24) + 1 == p.Hkv)
+            atomicAdd(&p.seqlen[b], 1 - (p.Hkv << 24));
+        s_step[0] = old & 0xffffff;
+        mbar_arrive(ntbar);
+    }
+
     // Q^T as the B operand: b0 = Q[head r][16s + 2c, +1], b1 = Q[head r][16s + 2c + 8, +1]
     uint32_t qf[D / 16][2];
     {
@@ -220,7 +238,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
 
     if constexpr (STEP == STEP_STREAM) {
-        // the slot of the token that left the window with the previous step
+        // the slot of the token that left the window with the previous step (P first)
+        if (!mbar_wait(ntbar, 0))
+            flag_error(p.status, DEV_TIMEOUT);
         const long leave = (long)s_step[0] - p.n_recent - 1;
         if (leave >= p.n_sink) {
             const int32_t *up = p.pos + (size_t)unit * p.C;
@@ -336,7 +356,6 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     // LM_REGS: lane c == 0 of each quad loads the old scores of its tokens now, so the
     // loads are in flight while the tiles stream instead of at the end
     float old[LREG ? LREG_TILES : 1][2];
-    int opos[LREG && STEP == STEP_H2O ? LREG_TILES : 1][2];   // H2O step: their positions
     if constexpr (LREG) {
 #pragma unroll
         for (int i = 0; i < LREG_TILES; ++i) {
@@ -345,11 +364,6 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             const bool upd = p.h2o_scores && p.part_o == nullptr && c == 0 && i < ntiles;
             old[i][0] = upd && ta < t_end ? sc[ta] : 0.f;
             old[i][1] = upd && tb < t_end ? sc[tb] : 0.f;
-            if constexpr (STEP == STEP_H2O) {
-                const int32_t *up = p.pos + (size_t)unit * p.C;
-                opos[i][0] = upd && ta < t_end ? up[ta] : 0;
-                opos[i][1] = upd && tb < t_end ? up[tb] : 0;
-            }
         }
     }
     if constexpr (LREG) {
@@ -524,7 +538,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
     // H2O decode step: the worst non-recent slot by (score desc, position asc), tracked as
     // the largest key (descending-score bits << 32 | position) while the scores are written
-    const long h2o_rt = STEP == STEP_H2O ? (long)s_step[0] + 1 - p.n_recent : 0;   // recent: >= rt
+    long h2o_rt = 0;   // recent: positions >= rt (set once P is known)
     unsigned long long vkey = 0ull;
     int vslot = -1;
     auto candidate = [&](int slot, int32_t ps, float score) {
@@ -560,6 +574,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         consumer_bar();
         float *sc = p.h2o_scores + (size_t)unit * p.C;
         if constexpr (STEP == STEP_H2O) {
+            // the positions copied at the start and P (their phase completed long ago)
+            if (!mbar_wait(ntbar, 0))
+                flag_error(p.status, DEV_TIMEOUT);
+            h2o_rt = (long)s_step[0] + 1 - p.n_recent;
             // the new token's probabilities (warp 0, lanes 0-3 hold heads 2c, 2c + 1), added
             // in head order like every other slot's
             if (warp == 0) {
@@ -602,19 +620,18 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                     const float v = fmaf(old[i][0], p.h2o_keep, add_a * p.h2o_add);
                     sc[ta] = v;
                     if constexpr (STEP == STEP_H2O)
-                        candidate(ta, opos[i][0], v);
+                        candidate(ta, spos[ta], v);
                 }
                 if (c == 0 && tb < t_end) {
                     const float v = fmaf(old[i][1], p.h2o_keep, add_b * p.h2o_add);
                     sc[tb] = v;
                     if constexpr (STEP == STEP_H2O)
-                        candidate(tb, opos[i][1], v);
+                        candidate(tb, spos[tb], v);
                 }
             }
         } else {
             const float *lrow = LSM ? lsm : p.logits + ((size_t)b * p.Hq + hk * p.g) * p.C;
             const size_t lstride = LSM ? LSM_SLOTS : p.C;
-            const int32_t *upos = p.pos + (size_t)unit * p.C;
             // four slots per thread per round, every load issued before any is used
             constexpr int U = 4;
             for (int j0 = t_begin + threadIdx.x; j0 < t_end; j0 += U * NCW * 32) {
@@ -625,7 +642,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                     const int j = j0 + u * NCW * 32;
                     add[u] = 0.f;
                     old[u] = j < t_end ? sc[j] : 0.f;
-                    ps[u] = STEP == STEP_H2O && j < t_end ? upos[j] : 0;
+                    ps[u] = STEP == STEP_H2O && j < t_end ? spos[j] : 0;
                 }
                 // all heads' logits of the round in flight at once (g <= 8)
                 float lg[8][U];
@@ -713,7 +730,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 slot = -1;
             if (slot == -2) {
                 // the new token left at once: the cache keeps its slots
-            } else if (slot < 0 || (p.n[unit] < 0 || p.n[unit] > p.C) || P >= (1 << 24) - 1) {
+            } else if (slot < 0 || n_bad || P >= (1 << 24) - 1) {
                 if (lane == 0)
                     flag_error(p.status, DEV_CAPACITY);
             } else {

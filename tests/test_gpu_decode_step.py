@@ -111,16 +111,18 @@ def test_h2o_decode_step_free_running(kvc, orc, B, Hq, Hkv, D, L, n_heavy, n_rec
     assert device_status_clean(kvc)
 
 
-def test_h2o_decode_step_matches_separate_launches_bench_shape(kvc):
-    """64 sequences of the heavy-load shape (GQA 64/8, D 128, 520-slot caches at the 512
-    budget after a seeded prefill state): 24 steps of the fused step against the same steps
-    as kvc_append -> kvc_decode_attend(h2o_scores) -> kvc_h2o_evict from an identical start.
-    Keep-sets must agree (as sets; near-ties within 1e-6 relative may swap), outputs within the
-    fp16 tolerance and scores within 1e-4 relative."""
+@pytest.mark.parametrize("B", [64, 512])
+def test_h2o_decode_step_matches_separate_launches_bench_shape(kvc, B):
+    """The heavy-load shape (GQA 64/8, D 128, 520-slot caches at the 512 budget after a seeded
+    prefill state): 24 steps of kvc_h2o_decode_step against the same steps as kvc_append ->
+    kvc_decode_attend(h2o_scores) -> kvc_h2o_evict from an identical start, at 64 sequences
+    (one launch, 24 steps) and at the benchmark's 512 (more than four units per SM: the call
+    issues the three launches itself; 6 steps).  Keep-sets must agree (as sets; near-ties within 1e-6 relative
+    may swap), outputs within the fp16 tolerance and scores within 1e-4 relative."""
     from kv_cache_compression_split_gb300 import workloads as W
     w = W.HEAVY
-    B, Hq, Hkv, D, T0, C = 64, w.Hq, w.Hkv, w.D, w.T, 520
-    n_heavy, n_recent, steps = w.n_heavy, w.n_recent, 24
+    Hq, Hkv, D, T0, C = w.Hq, w.Hkv, w.D, w.T, 520
+    n_heavy, n_recent, steps = w.n_heavy, w.n_recent, (24 if B <= 64 else 6)
     Kseq, Vseq = W.kv_tensors(w, T=T0 + steps, B=B, device="cuda")
     rng = np.random.default_rng(64)
     pos0 = np.zeros((B, Hkv, 512), np.int32)
@@ -174,7 +176,7 @@ def test_h2o_decode_step_matches_separate_launches_bench_shape(kvc):
                 kk = sorted(ma)
                 np.testing.assert_allclose([ma[k] for k in kk], [mz[k] for k in kk],
                                            rtol=SCORE_REL_TOL)
-        assert swaps <= 2, f"step {s_}: {swaps} units with different keep-sets"
+        assert swaps <= max(2, B * Hkv // 256), f"step {s_}: {swaps} units with different keep-sets"
         # the fused cache's rows are its tokens'
         idx = fused.pos[:, :, :512].long()[..., None].expand(B, Hkv, 512, D)
         assert torch.equal(fused.K[:, :, :512], torch.gather(Kseq, 2, idx))
