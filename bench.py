@@ -1252,6 +1252,34 @@ def run_profile(args):
         ws = torch.empty(kvc.kvc_h2o_workspace_size(kp.shape[0], Hq, L) // 4, device=dev)
         for _ in range(3):
             kvc.kvc_h2o_accumulate_prefill(qp, kp, sc, ws, L)
+    elif what == "decode_steps":
+        # the benchmark's decode step (its four methods one after another) at --profile-batch
+        # sequences, five times, after an untimed set-up: for a launch list of one step
+        Ch = 520
+        fp = kvc.SlotCache.empty(B, Hkv, T + 8, D, device=dev)
+        kvc.kvc_append(fp, K[:, :, :T - 1].contiguous(), V[:, :, :T - 1].contiguous())
+        h2o = kvc.SlotCache.empty(B, Hkv, Ch, D, device=dev)
+        st = kvc.SlotCache.empty(B, Hkv, Ch, D, device=dev)
+        for c in (h2o, st):
+            kvc.kvc_append(c, K[:, :, T - 513:T - 1].contiguous(), V[:, :, T - 513:T - 1].contiguous())
+            c.pos[:, :, :512] = torch.cat([torch.arange(w.n_sink),
+                                           torch.arange(T - 1 - w.n_recent, T - 1)]).int().to(dev)
+            c.seqlen.fill_(T - 1)
+        sc = torch.rand(B, Hkv, Ch, device=dev)
+        kv4 = kvc.QuantCache.empty(B, Hkv, T + 64, D, 4, w.kivi_R, device=dev)
+        kvc.kvc_append_quant(kv4, K[:, :, :T - 1].contiguous(), V[:, :, :T - 1].contiguous())
+        ws_fp = torch.empty(max(kvc.kvc_workspace_size(fp, q) // 4, 1), device=dev)
+        ws_kv = torch.empty(max(kvc.kvc_workspace_size(kv4, q) // 4, 1), device=dev)
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+        kn = torch.randn(B, Hkv, 1, D, device=dev, dtype=torch.float16)
+        torch.cuda.synchronize()
+        for _ in range(5):
+            kvc.kvc_append(fp, kn, kn)
+            kvc.kvc_decode_attend(fp, q, o, workspace=ws_fp)
+            kvc.kvc_h2o_decode_step(h2o, sc, q, kn, kn, o, lse, w.n_heavy, w.n_recent)
+            kvc.kvc_append_quant(kv4, kn, kn)
+            kvc.kvc_decode_attend(kv4, q, o, workspace=ws_kv)
+            kvc.kvc_stream_decode_step(st, q, kn, kn, o, None, w.n_sink, w.n_recent)
     elif what in ("h2o_step", "stream_step"):
         # the one-launch decode steps at the heavy-load shape: 512 slots per unit (64 sinks or
         # heavy + 448 recent), then three steps (each appends one token and keeps 512 / 513)
