@@ -298,18 +298,19 @@ template <int D> struct __align__(16) GroupSmem {
     float inv[2 * D];            // 1 / scale (an estimate; the remainder fixes the code)
 };
 
-// Extra staging of the GEAR side data of one matrix (K, then V) of a group.
-// Rows are padded by 8 words: 64-bit fragment loads of a half-warp (8 rows x 2 columns
+// Extra staging of the GEAR side data of a group's two matrices (index 0: K,
+// 1: V), worked on together so that each serial step serves both.  Rows are
+// padded by 8 words: 64-bit fragment loads of a half-warp (8 rows x 2 columns
 // pairs) then hit every bank once.
 constexpr int GM_LD = KIVI_G + 8;
 template <int D> struct __align__(16) GearSmem {
-    float e[KIVI_G][D + 8];      // residual, then R (sparse entries zeroed)
-    float gm[KIVI_G][GM_LD];
-    float gm2[KIVI_G][GM_LD];
-    float a[2][KIVI_G];          // orthonormal left factors
-    int hist[256];
-    int scan[QTHREADS / 32 + 1];
-    int misc[2];
+    float e[2][KIVI_G][D + 8];   // residual, then R (sparse entries zeroed)
+    float gm[2][KIVI_G][GM_LD];
+    float gm2[2][KIVI_G][GM_LD];
+    float a[2][2][KIVI_G];       // orthonormal left factors
+    int hist[3][2][256];         // radix digit counts, three buffers in rotation
+    int scan[2][QTHREADS / 32];
+    int red[2][QTHREADS / 32];
 };
 
 // quant_code_inv with a fast path: the fp32 estimate is within 3e-6 of the
@@ -441,182 +442,235 @@ __device__ __forceinline__ void orthonormalise2(float &x0, float &x1)
     x1 *= rsqrtf(n1);
 }
 
-// GEAR side block of one matrix of the group (K when ISK, else V), written to
-// `side`: the residual e = fl32(x - fl32(zero + code * scale)) of every element,
-// the n_s entries with the largest |e| (ties: lower flat index) as ascending u16
-// flat indices and binary16 values, and a rank-2 factorisation A^T B of the
-// rest R: A [2][32] orthonormal rows spanning the dominant left singular
-// subspace, B = A R; both binary16.  The subspace comes from 16 steps of
-// subspace iteration on (R R^T)^4 (R R^T scaled by its largest entry, then
+// Digit of the radix select over one matrix's keys, found by every warp from
+// the same histogram h (no barrier needed to share it): lane L reads digits
+// 255 - 8L - k (k = 0..7, descending); the digit is the first one from the top
+// whose cumulative count reaches `need`, and `need` becomes the rank left
+// within it.  With fewer matching keys than needed (cannot happen for
+// consistent input) the digit is 0, as a downward scan would end.
+__device__ __forceinline__ void radix_digit(const int *h_all, int &digit, int &need)
+{
+    const int lane = threadIdx.x & 31;
+    int h[8], tot = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        h[k] = h_all[255 - 8 * lane - k];
+        tot += h[k];
+    }
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    const bool mine = incl - tot < need && incl >= need;
+    const unsigned any = __ballot_sync(0xffffffffu, mine);
+    int dg, nd;
+    if (any) {
+        int cum = incl - tot, k = 0;
+        for (; k < 7; ++k) {
+            if (cum + h[k] >= need)
+                break;
+            cum += h[k];
+        }
+        dg = 255 - 8 * lane - k;
+        nd = need - cum;
+    } else {
+        dg = 0;
+        nd = need - (incl - h[7]);
+    }
+    const int src = any ? __ffs(any) - 1 : 31;
+    digit = __shfl_sync(0xffffffffu, dg, src);
+    need = __shfl_sync(0xffffffffu, nd, src);
+}
+
+// GEAR side blocks of both matrices of the group, written to kside (K) and
+// vside (V): the residual e = fl32(x - fl32(zero + code * scale)) of every
+// element, the n_s entries with the largest |e| (ties: lower flat index) as
+// ascending u16 flat indices and binary16 values, and a rank-2 factorisation
+// A^T B of the rest R: A [2][32] orthonormal rows spanning the dominant left
+// singular subspace, B = A R; both binary16.  The subspace comes from 16 steps
+// of subspace iteration on (R R^T)^4 (R R^T scaled by its largest entry, then
 // squared twice), started from R R^T times a constant and a ramp.  All threads
-// of the CTA.
-template <int D, int BITS, bool ISK>
-__device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &gs, uint8_t *side)
+// of the CTA; the two matrices share every barrier, and their iterations run
+// in warps 0 (K) and 1 (V) at the same time.
+template <int D, int BITS>
+__device__ __forceinline__ void gear_sides(const GroupSmem<D> &sm, GearSmem<D> &gs,
+                                           uint8_t *kside, uint8_t *vside)
 {
     constexpr int G = KIVI_G, NG = D / G, N = G * D, PER = N / QTHREADS;
     constexpr int NS = (2 * G * D + 99) / 100;
     constexpr int RAW = 4 * NS + 4 * G + 4 * D;
     constexpr int SIDE = (RAW + 15) / 16 * 16;
+    static_assert(QTHREADS == 256, "eight warps cover the 32 x 32 Gram matrix");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // 1. residual of my PER elements: warp w owns flat indices [32 PER w, 32 PER (w + 1)),
-    //    lane L of it 32 u + L (u < PER), so a warp's accesses cover 32 consecutive
-    //    elements of one row
+    uint8_t *const sides[2] = {kside, vside};
+    // 1. residuals of my PER elements of each matrix: warp w owns flat indices
+    //    [32 PER w, 32 PER (w + 1)), lane L of it 32 u + L (u < PER), so a warp's
+    //    accesses cover 32 consecutive elements of one row
     const auto flat = [&](int u) { return 32 * PER * warp + 32 * u + lane; };
-    uint32_t key[PER];
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int i = flat(u), t = i / D, d = i % D;
-        const int pi = ISK ? d : D + t * NG + d / G;
-        const float x = __half2float(__ushort_as_half(ISK ? sm.xk[t][d] : sm.xv[t][d]));
-        const float code = (float)(ISK ? sm.ck[t][d] : sm.cv[t][d]);
-        const float e = x - fmaf(code, sm.sf[pi], sm.zf[pi]);
-        gs.e[t][d] = e;
-        key[u] = __float_as_uint(fabsf(e));
+    for (int m = 0; m < 2; ++m) {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int i = flat(u), t = i / D, d = i % D;
+            const int pi = m == 0 ? d : D + t * NG + d / G;
+            const float x = __half2float(__ushort_as_half(m == 0 ? sm.xk[t][d] : sm.xv[t][d]));
+            const float code = (float)(m == 0 ? sm.ck[t][d] : sm.cv[t][d]);
+            gs.e[m][t][d] = x - fmaf(code, sm.sf[pi], sm.zf[pi]);
+        }
     }
-    // 2. the NS-th largest key: radix select, 8-bit digits from the top
-    uint32_t prefix = 0, mask = 0;
-    int need = NS;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += QTHREADS)
-            gs.hist[i] = 0;
-        __syncthreads();
+    const auto key = [&](int m, int u) {
+        const int i = flat(u);
+        return __float_as_uint(gs.e[m][i / D][i % D]) & 0x7fffffffu;   // bits of |e|
+    };
+    for (int i = tid; i < 2 * 2 * 256; i += QTHREADS)
+        (&gs.hist[0][0][0])[i] = 0;
+    __syncthreads();
+    // 2. the NS-th largest key of each matrix: radix select, 8-bit digits from the
+    //    top.  Pass p counts into buffer p mod 3 and clears buffer (p + 1) mod 3, whose
+    //    last readers (pass p - 2) finished before pass p - 1's barrier.
+    uint32_t prefix[2] = {0u, 0u}, mask = 0;
+    int need[2] = {NS, NS};
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        int(*hc)[256] = gs.hist[pass % 3];
+        int *hz = &gs.hist[(pass + 1) % 3][0][0];
         // histogram of the digit among keys matching the prefix; lanes with equal
         // digits add once (keys concentrate on a few exponents)
 #pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const bool in = (key[u] & mask) == prefix;
-            if (!__any_sync(0xffffffffu, in))
-                continue;
-            const int dg = in ? (int)((key[u] >> shift) & 255) : 256;
-            const unsigned same = __match_any_sync(0xffffffffu, dg);
-            if (in && lane == __ffs(same) - 1)
-                atomicAdd(&gs.hist[dg], __popc(same));
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // lane L holds digits 255 - 8L - k, k = 0..7 (descending); the digit is the
-            // first one from the top whose cumulative count reaches `need`
-            int h[8], tot = 0;
+        for (int m = 0; m < 2; ++m) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                h[k] = gs.hist[255 - 8 * lane - k];
-                tot += h[k];
-            }
-            int incl = tot;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o)
-                    incl += y;
-            }
-            const bool mine = incl - tot < need && incl >= need;
-            const unsigned any = __ballot_sync(0xffffffffu, mine);
-            if (mine) {
-                int cum = incl - tot, k = 0;
-                for (; k < 7; ++k) {
-                    if (cum + h[k] >= need)
-                        break;
-                    cum += h[k];
-                }
-                gs.misc[0] = 255 - 8 * lane - k;
-                gs.misc[1] = need - cum;
-            } else if (any == 0 && lane == 31) {
-                // fewer matching keys than needed (cannot happen for consistent input):
-                // digit 0, as a downward scan would end
-                gs.misc[0] = 0;
-                gs.misc[1] = need - (incl - h[7]);
+            for (int u = 0; u < PER; ++u) {
+                const uint32_t k = key(m, u);
+                const bool in = (k & mask) == prefix[m];
+                if (!__any_sync(0xffffffffu, in))
+                    continue;
+                const int dg = in ? (int)((k >> shift) & 255) : 256;
+                const unsigned same = __match_any_sync(0xffffffffu, dg);
+                if (in && lane == __ffs(same) - 1)
+                    atomicAdd(&hc[m][dg], __popc(same));
             }
         }
+        if (pass < 3)
+            for (int i = tid; i < 2 * 256; i += QTHREADS)
+                hz[i] = 0;
         __syncthreads();
-        prefix |= (uint32_t)gs.misc[0] << shift;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            int dg;
+            radix_digit(hc[m], dg, need[m]);
+            prefix[m] |= (uint32_t)dg << shift;
+        }
         mask |= 255u << shift;
-        need = gs.misc[1];
-        __syncthreads();
     }
     // 3. keep every key above the threshold and the first `need` equal to it, in flat
     //    order: ranks from per-u ballots within the warp plus the earlier warps' totals
     const unsigned lt = (1u << lane) - 1u;
-    int wcount = 0;
 #pragma unroll
-    for (int u = 0; u < PER; ++u)
-        wcount += __popc(__ballot_sync(0xffffffffu, key[u] == prefix));
-    if (lane == 0)
-        gs.scan[warp] = wcount;
-    __syncthreads();
-    int run = 0;
-    for (int w = 0; w < warp; ++w)
-        run += gs.scan[w];
-    __syncthreads();                           // gs.scan is written again below
-    uint32_t selm = 0;                         // bit u: element u selected
-    wcount = 0;
+    for (int m = 0; m < 2; ++m) {
+        int wcount = 0;
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const unsigned tb = __ballot_sync(0xffffffffu, key[u] == prefix);
-        const bool sel = key[u] > prefix || (((tb >> lane) & 1u) && run + __popc(tb & lt) < need);
-        run += __popc(tb);
-        selm |= (uint32_t)sel << u;
-        wcount += __popc(__ballot_sync(0xffffffffu, sel));
-    }
-    if (lane == 0)
-        gs.scan[warp] = wcount;
-    __syncthreads();
-    int o = 0;
-    for (int w = 0; w < warp; ++w)
-        o += gs.scan[w];
-    uint16_t *idx_out = reinterpret_cast<uint16_t *>(side);
-    __half *val_out = reinterpret_cast<__half *>(side + 2 * NS);
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const bool sel = (selm >> u) & 1u;
-        const unsigned sb = __ballot_sync(0xffffffffu, sel);
-        const int pos = o + __popc(sb & lt);
-        if (sel && pos < NS) {                 // exactly NS are selected; the bound is a guard
-            const int i = flat(u), t = i / D, d = i % D;
-            idx_out[pos] = (uint16_t)i;
-            val_out[pos] = __float2half_rn(gs.e[t][d]);
-            gs.e[t][d] = 0.f;                  // R: the rest of the residual
-        }
-        o += __popc(sb);
-    }
-    __syncthreads();
-    // 4. Gram matrix R R^T with tensor cores, one 16 x 8 tile per warp, scaled by its
-    //    largest entry.  Every entry of R is at most the threshold key, so R * 2^(130 - e)
-    //    (e: the threshold's exponent field) stays below 16 in binary16.
-    {
-        static_assert(QTHREADS == 256, "eight warps cover the 32 x 32 Gram matrix");
-        const int ex = (int)((prefix >> 23) & 255);
-        const float sc = prefix ? __int_as_float(min(257 - ex, 254) << 23) : 1.f;
-        const int i0 = 16 * (warp >> 2), j0 = 8 * (warp & 3), gid = lane >> 2, tig = lane & 3;
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        xyt_tile<D, D + 8>(&gs.e[0][0], i0, &gs.e[0][0], j0, sc, c);
-        float mx = fmaxf(fmaxf(fabsf(c[0]), fabsf(c[1])), fmaxf(fabsf(c[2]), fabsf(c[3])));
-#pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+        for (int u = 0; u < PER; ++u)
+            wcount += __popc(__ballot_sync(0xffffffffu, key(m, u) == prefix[m]));
         if (lane == 0)
-            gs.scan[warp] = __float_as_int(mx);
-        __syncthreads();
-        float m = 0.f;
-#pragma unroll
-        for (int w = 0; w < QTHREADS / 32; ++w)
-            m = fmaxf(m, __int_as_float(gs.scan[w]));
-        const float inv_m = m > 0.f ? 1.f / m : 0.f;
-        gs.gm[i0 + gid][j0 + 2 * tig] = c[0] * inv_m;
-        gs.gm[i0 + gid][j0 + 2 * tig + 1] = c[1] * inv_m;
-        gs.gm[i0 + gid + 8][j0 + 2 * tig] = c[2] * inv_m;
-        gs.gm[i0 + gid + 8][j0 + 2 * tig + 1] = c[3] * inv_m;
+            gs.scan[m][warp] = wcount;
     }
     __syncthreads();
-    square32(gs.gm, gs.gm2);                   // (R R^T)^2, entries <= 32
+    uint32_t selm[2] = {0u, 0u};   // bit u: element u selected
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        int run = 0;
+        for (int w = 0; w < warp; ++w)
+            run += gs.scan[m][w];
+        int wcount = 0;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const uint32_t k = key(m, u);
+            const unsigned tb = __ballot_sync(0xffffffffu, k == prefix[m]);
+            const bool sel =
+                k > prefix[m] || (((tb >> lane) & 1u) && run + __popc(tb & lt) < need[m]);
+            run += __popc(tb);
+            selm[m] |= (uint32_t)sel << u;
+            wcount += __popc(__ballot_sync(0xffffffffu, sel));
+        }
+        if (lane == 0)
+            gs.red[m][warp] = wcount;
+    }
     __syncthreads();
-    square32(gs.gm2, gs.gm);                   // (R R^T)^4, entries <= 32^3
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        int o = 0;
+        for (int w = 0; w < warp; ++w)
+            o += gs.red[m][w];
+        uint16_t *idx_out = reinterpret_cast<uint16_t *>(sides[m]);
+        __half *val_out = reinterpret_cast<__half *>(sides[m] + 2 * NS);
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const bool sel = (selm[m] >> u) & 1u;
+            const unsigned sb = __ballot_sync(0xffffffffu, sel);
+            const int pos = o + __popc(sb & lt);
+            if (sel && pos < NS) {             // exactly NS are selected; the bound is a guard
+                const int i = flat(u), t = i / D, d = i % D;
+                idx_out[pos] = (uint16_t)i;
+                val_out[pos] = __float2half_rn(gs.e[m][t][d]);
+                gs.e[m][t][d] = 0.f;           // R: the rest of the residual
+            }
+            o += __popc(sb);
+        }
+    }
     __syncthreads();
-    // 5. dominant 2-dimensional subspace: subspace iteration in warp 0, one row per lane
-    if (warp == 0) {
+    // 4. Gram matrices R R^T with tensor cores, one 16 x 8 tile of each per warp, scaled
+    //    by their largest entry.  Every entry of R is at most the threshold key, so
+    //    R * 2^(130 - e) (e: the threshold's exponent field) stays below 16 in binary16.
+    {
+        const int i0 = 16 * (warp >> 2), j0 = 8 * (warp & 3), gid = lane >> 2, tig = lane & 3;
+        float c[2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int ex = (int)((prefix[m] >> 23) & 255);
+            const float sc = prefix[m] ? __int_as_float(min(257 - ex, 254) << 23) : 1.f;
+            c[m][0] = c[m][1] = c[m][2] = c[m][3] = 0.f;
+            xyt_tile<D, D + 8>(&gs.e[m][0][0], i0, &gs.e[m][0][0], j0, sc, c[m]);
+            float mx = fmaxf(fmaxf(fabsf(c[m][0]), fabsf(c[m][1])),
+                             fmaxf(fabsf(c[m][2]), fabsf(c[m][3])));
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1)
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+            if (lane == 0)
+                gs.scan[m][warp] = __float_as_int(mx);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            float mm = 0.f;
+#pragma unroll
+            for (int w = 0; w < QTHREADS / 32; ++w)
+                mm = fmaxf(mm, __int_as_float(gs.scan[m][w]));
+            const float inv_m = mm > 0.f ? 1.f / mm : 0.f;
+            gs.gm[m][i0 + gid][j0 + 2 * tig] = c[m][0] * inv_m;
+            gs.gm[m][i0 + gid][j0 + 2 * tig + 1] = c[m][1] * inv_m;
+            gs.gm[m][i0 + gid + 8][j0 + 2 * tig] = c[m][2] * inv_m;
+            gs.gm[m][i0 + gid + 8][j0 + 2 * tig + 1] = c[m][3] * inv_m;
+        }
+    }
+    __syncthreads();
+    square32(gs.gm[0], gs.gm2[0]);             // (R R^T)^2, entries <= 32
+    square32(gs.gm[1], gs.gm2[1]);
+    __syncthreads();
+    square32(gs.gm2[0], gs.gm[0]);             // (R R^T)^4, entries <= 32^3
+    square32(gs.gm2[1], gs.gm[1]);
+    __syncthreads();
+    // 5. dominant 2-dimensional subspaces: subspace iteration, K in warp 0 and V in
+    //    warp 1, one row per lane
+    if (warp < 2) {
+        const int m = warp;
         float gr[G];
 #pragma unroll
         for (int j = 0; j < G; ++j)
-            gr[j] = gs.gm[lane][j];
+            gr[j] = gs.gm[m][lane][j];
         float x0 = 0.f, x1 = 0.f;
 #pragma unroll
         for (int j = 0; j < G; ++j) {
@@ -626,11 +680,11 @@ __device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &g
         orthonormalise2(x0, x1);
         for (int it = 0; it < 16; ++it) {
             // y = M x, the vectors broadcast from shared memory four entries at a time
-            gs.a[0][lane] = x0;
-            gs.a[1][lane] = x1;
+            gs.a[m][0][lane] = x0;
+            gs.a[m][1][lane] = x1;
             __syncwarp();
-            const float4 *a0 = reinterpret_cast<const float4 *>(gs.a[0]);
-            const float4 *a1 = reinterpret_cast<const float4 *>(gs.a[1]);
+            const float4 *a0 = reinterpret_cast<const float4 *>(gs.a[m][0]);
+            const float4 *a1 = reinterpret_cast<const float4 *>(gs.a[m][1]);
             float y0 = 0.f, y1 = 0.f;
 #pragma unroll
             for (int j = 0; j < G / 4; ++j) {
@@ -649,25 +703,28 @@ __device__ __forceinline__ void gear_side(const GroupSmem<D> &sm, GearSmem<D> &g
             x1 = y1;
             orthonormalise2_fast(x0, x1);
         }
-        gs.a[0][lane] = x0;
-        gs.a[1][lane] = x1;
+        gs.a[m][0][lane] = x0;
+        gs.a[m][1][lane] = x1;
     }
     __syncthreads();
     // 6. factors: A [2][G] and B = A R [2][D], binary16; zero padding
-    __half *a_out = reinterpret_cast<__half *>(side + 4 * NS);
-    __half *b_out = reinterpret_cast<__half *>(side + 4 * NS + 4 * G);
-    for (int i = tid; i < 2 * G; i += QTHREADS)
-        a_out[i] = __float2half_rn(gs.a[i / G][i % G]);
-    for (int i = tid; i < 2 * D; i += QTHREADS) {
-        const int r = i / D, d = i % D;
-        float s = 0.f;
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        __half *a_out = reinterpret_cast<__half *>(sides[m] + 4 * NS);
+        __half *b_out = reinterpret_cast<__half *>(sides[m] + 4 * NS + 4 * G);
+        for (int i = tid; i < 2 * G; i += QTHREADS)
+            a_out[i] = __float2half_rn(gs.a[m][i / G][i % G]);
+        for (int i = tid; i < 2 * D; i += QTHREADS) {
+            const int r = i / D, d = i % D;
+            float s = 0.f;
 #pragma unroll 8
-        for (int t = 0; t < G; ++t)
-            s = fmaf(gs.a[r][t], gs.e[t][d], s);
-        b_out[i] = __float2half_rn(s);
+            for (int t = 0; t < G; ++t)
+                s = fmaf(gs.a[m][r][t], gs.e[m][t][d], s);
+            b_out[i] = __float2half_rn(s);
+        }
+        for (int i = RAW + tid; i < SIDE; i += QTHREADS)
+            sides[m][i] = 0;
     }
-    for (int i = RAW + tid; i < SIDE; i += QTHREADS)
-        side[i] = 0;
     __syncthreads();
 }
 
@@ -811,8 +868,7 @@ __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16
     }
     __syncthreads();
     if (GEAR) {   // 4. the GEAR corrections of the group's quantisation residual
-        gear_side<D, BITS, true>(sm, *gs, kside);
-        gear_side<D, BITS, false>(sm, *gs, vside);
+        gear_sides<D, BITS>(sm, *gs, kside, vside);
     }
 }
 

@@ -85,17 +85,24 @@ template <int D, int BITS, bool GEAR = false> struct KiviCfg {
     // (conflict-free ldmatrix)
     static constexpr int DT_STRIDE = (D + 8) * 2;
     static constexpr int DT_BYTES = GEAR ? NCW * G * DT_STRIDE : 0;
-    // GEAR: the plain query fragments of an item, one 16-byte chunk per (lane, 2 k-steps),
-    // double-buffered (the next item's are written during the current one)
+    // The plain query words of an item, one 16-byte chunk per (lane, 2 k-steps),
+    // double-buffered (the next item's are written during the current one).  GEAR reads
+    // them as the Q^T fragments of its correction MMAs; KIVI as the B operand of the
+    // bias chain, when the buffers fit beside the stages it would have anyway (they
+    // free 16 registers per thread that the 128-register cap of three CTAs per SM
+    // would otherwise spill)
     static constexpr int QCH = D / 32;                 // 16-byte chunks per lane
     static constexpr int QS_BUF = QCH * 32 * 16;
-    static constexpr int QS_BYTES = GEAR ? 2 * QS_BUF : 0;
     // CTAs per SM: three for KIVI (each within a third of the SM's 228 KB of shared
     // memory, 1 KB of it reserved per CTA), two for GEAR
     static constexpr int CTAS = GEAR ? 2 : 3;
+    static constexpr int KIVI_ROOM = 233472 / 3 - 1024 - RED_BYTES - 1024 - 64;
+    static constexpr bool QS_BIAS =
+        !GEAR && (KIVI_ROOM - 2 * QS_BUF) / STAGE_BYTES == KIVI_ROOM / STAGE_BYTES;
+    static constexpr int QS_BYTES = (GEAR || QS_BIAS) ? 2 * QS_BUF : 0;
     static constexpr int NSTAGE_PLAIN =
         GEAR ? ((81920 / STAGE_BYTES) < 3 ? 3 : (81920 / STAGE_BYTES))
-             : (233472 / 3 - 1024 - RED_BYTES - 1024 - 64) / STAGE_BYTES;
+             : (KIVI_ROOM - QS_BYTES) / STAGE_BYTES;
     // with the sparse tiles, as many stages as keep two CTAs resident per SM
     static constexpr int NSTAGE_FIT =
         (112640 - RED_BYTES - DT_BYTES - QS_BYTES - 1104) / STAGE_BYTES;
@@ -352,8 +359,11 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
     int it = 0;
     // GEAR: this warp's sparse tile, all zero between groups
     const uint32_t dt = smem_u32(dtiles) + warp * Cfg::G * Cfg::DT_STRIDE;
-    // GEAR: Q^T B-operand fragments of item `item` (head r: words 8s + c and 8s + c + 4 of
-    // the query row, s = 0 .. D/16-1) into q buffer qb, written by warp 0
+    // The query words of item `item` into q buffer qb, written by warp 0.  GEAR: the
+    // Q^T B-operand fragments (head r: words 8s + c and 8s + c + 4 of the query row,
+    // s = 0 .. D/16-1).  KIVI bias: the D/8 words of head r that lane c covers
+    // (channels [c D/4, (c+1) D/4)) in order, chunk k holding the lane's words 4k .. 4k + 3.
+    constexpr bool QSTAGE = GEAR || Cfg::QS_BIAS;
     auto stage_q = [&](int item, int qb) {
         const int unit = item / p.splits;
         const int bb = unit / p.Hkv, hh = unit % p.Hkv;
@@ -361,16 +371,25 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
             p.q + ((size_t)bb * p.Hq + hh * p.g + (hv ? r : 0)) * D);
         uint4 *dst = reinterpret_cast<uint4 *>(qstage + qb * Cfg::QS_BUF) + lane;
 #pragma unroll
-        for (int k = 0; k < Cfg::QCH; ++k)
-            dst[32 * k] = hv ? make_uint4(q32[16 * k + c], q32[16 * k + c + 4],
-                                          q32[16 * k + 8 + c], q32[16 * k + 12 + c])
-                             : make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < Cfg::QCH; ++k) {
+            if constexpr (GEAR)
+                dst[32 * k] = hv ? make_uint4(q32[16 * k + c], q32[16 * k + c + 4],
+                                              q32[16 * k + 8 + c], q32[16 * k + 12 + c])
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            else
+            {
+                const uint32_t *w = q32 + c * (D / 8) + 4 * k;
+                dst[32 * k] = hv ? make_uint4(w[0], w[1], w[2], w[3]) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
     };
     if constexpr (GEAR) {
         uint4 *z = reinterpret_cast<uint4 *>(dtiles + warp * Cfg::G * Cfg::DT_STRIDE);
         for (int e = lane; e < Cfg::G * Cfg::DT_STRIDE / 16; e += 32)
             z[e] = make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
+    }
+    if constexpr (QSTAGE) {
         if (warp == 0 && (int)blockIdx.x < p.n_items)
             stage_q(blockIdx.x, 0);
         consumer_bar();
@@ -495,14 +514,15 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
     // query pairs: lane c covers channels [c D/4, (c+1) D/4); pair pi holds channels
     // (lo, lo + HALF) divided by the pair's field weight
     uint32_t qpair[D / 8];
-    uint32_t qh[GEAR ? 1 : D / 8];   // KIVI: the same channels in order (for the bias)
+    // KIVI without the staged query: the same channels in order (for the bias)
+    uint32_t qh[QSTAGE ? 1 : D / 8];
     {
         uint32_t qh_[D / 8];
         const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow + c * (D / 4));
 #pragma unroll
         for (int e = 0; e < D / 8; ++e) {
             qh_[e] = hv ? q32[e] : 0u;
-            if constexpr (!GEAR)
+            if constexpr (!QSTAGE)
                 qh[e] = qh_[e];
         }
 #pragma unroll
@@ -596,12 +616,19 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
                 bias1 = __shfl_sync(0xffffffffu, uf[1], 8 + c) * p.scale_log2;
             } else {
                 const uint4 *zl = reinterpret_cast<const uint4 *>(ksz + D / 2 + c * (D / 8));
+                const uint4 *qsrc =
+                    reinterpret_cast<const uint4 *>(qstage + qbuf * Cfg::QS_BUF) + lane;
                 float bz0[4] = {0.f, 0.f, 0.f, 0.f}, bz1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < D / 32; ++e) {
                     const uint4 z4 = zl[e];
-                    mma16816(bz0, z4.x, 0u, z4.y, 0u, qh[4 * e], qh[4 * e + 1]);
-                    mma16816(bz1, z4.z, 0u, z4.w, 0u, qh[4 * e + 2], qh[4 * e + 3]);
+                    uint4 q4;
+                    if constexpr (QSTAGE)
+                        q4 = qsrc[32 * e];
+                    else
+                        q4 = make_uint4(qh[4 * e], qh[4 * e + 1], qh[4 * e + 2], qh[4 * e + 3]);
+                    mma16816(bz0, z4.x, 0u, z4.y, 0u, q4.x, q4.y);
+                    mma16816(bz1, z4.z, 0u, z4.w, 0u, q4.z, q4.w);
                 }
                 bias0 = (bz0[0] + bz1[0]) * p.scale_log2;
                 bias1 = (bz0[1] + bz1[1]) * p.scale_log2;
@@ -803,8 +830,8 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
         l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, off);
         l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, off);
     }
-    if constexpr (GEAR) {
-        // the next item's query fragments go to the other buffer: its readers finished
+    if constexpr (QSTAGE) {
+        // the next item's query words go to the other buffer: its readers finished
         // before the previous merge, and this item's readers before the barrier below
         if (warp == 0 && item + (int)gridDim.x < p.n_items)
             stage_q(item + gridDim.x, qbuf ^ 1);

@@ -179,7 +179,6 @@ __device__ __forceinline__ float fold_tile(uint32_t taddr, uint64_t *acc_empty, 
                                            int col0, int gi, const TcParams &p, const float *nlse,
                                            float &m, float &l)
 {
-    const int lane = threadIdx.x & 31;
     float tile_sum = 0.f;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -190,8 +189,7 @@ __device__ __forceinline__ float fold_tile(uint32_t taddr, uint64_t *acc_empty, 
         if (k == 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(acc_empty);
+            mbar_arrive_warp(acc_empty);
         }
         const int c0 = col0 + 32 * k;
         if (PASS == 1) {
@@ -466,11 +464,11 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
             for (int s = 0; s < ns; ++s, ++tc, sp.next(p, t)) {
                 const int buf = tc & 1;
                 const int ls = tc % NL;
-                // pass 2: the tile's -lse has landed in slot ls (every lane
-                // acquires it); then one lane waits for the accumulator
-                bool got = PASS == 1 || mbar_sleep_or_abort(&l_full[ls], (tc / NL) & 1, abort);
-                if (lane == 0 && got)
-                    got = mbar_sleep_or_abort(&acc_full[buf], (tc / 2) & 1, abort);
+                // pass 2: the tile's -lse has landed in slot ls; then the
+                // accumulator (every lane acquires both)
+                const bool got =
+                    (PASS == 1 || mbar_wait_or_abort(&l_full[ls], (tc / NL) & 1, abort)) &&
+                    mbar_wait_or_abort(&acc_full[buf], (tc / 2) & 1, abort);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
@@ -511,8 +509,7 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
                         run = 0.f;
                     }
                     __syncwarp();   // every lane has read the slot
-                    if (lane == 0)
-                        mbar_arrive(&l_empty[ls]);
+                    mbar_arrive_warp(&l_empty[ls]);
                 }
             }
             if (!ok)

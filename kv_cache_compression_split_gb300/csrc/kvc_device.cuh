@@ -147,6 +147,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrival on `bar` for the whole warp, made by the lane that elect.sync
+// picks.  Every lane of the warp calls it; the arrival is a predicated
+// instruction, so the warp does not branch around it.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
