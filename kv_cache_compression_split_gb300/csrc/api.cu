@@ -368,7 +368,7 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
     AttendPlanFull f = plan_full(a);
     if (f.st != KVC_OK)
         return f.st;
-    if (!a->q || !a->o || !aligned16(a->q))
+    if (!a->q || !a->o || !aligned16(a->q) || !aligned16(a->o))
         return KVC_ERR_INVALID_ARG;
     if (a->kind == KVC_KIND_KIVI && (a->logits || a->h2o_scores))
         return KVC_ERR_UNSUPPORTED;
@@ -520,7 +520,8 @@ static kvc_status decode_step_common(const kvc_slot_cache *cache, int Hq, const 
     kvc_status st = check_slot_cache(cache);
     if (st != KVC_OK)
         return st;
-    if (!q || !o || !k_new || !v_new || !aligned16(q) || !aligned16(k_new) || !aligned16(v_new))
+    if (!q || !o || !k_new || !v_new || !aligned16(q) || !aligned16(o) || !aligned16(k_new) ||
+        !aligned16(v_new))
         return KVC_ERR_INVALID_ARG;
     if (Hq <= 0 || Hq % cache->Hkv != 0 || n_recent < 0 || n_other < 0)
         return KVC_ERR_INVALID_ARG;

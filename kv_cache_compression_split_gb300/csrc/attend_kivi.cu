@@ -242,13 +242,25 @@ struct KiviItem {
     int unit, split, b, hk, T, n_groups, n_res, qt0, nq, nr;
 };
 
+// Work item -> (unit, split).  Items run split-major with the last split (the
+// one that also holds the residual ring, so the largest) first: the CTAs that
+// take items k, k + gridDim.x, ... then get a mix of splits whatever gridDim.x
+// is, instead of all the last splits landing on the same CTAs.
+__device__ __forceinline__ void kivi_unit_split(const KiviParams &p, int item, int &unit,
+                                                int &split)
+{
+    const int units = p.n_items / p.splits;
+    const int s = item / units;
+    unit = item - s * units;
+    split = p.splits - 1 - s;
+}
+
 template <int D, int BITS, bool GEAR>
 __device__ __forceinline__ KiviItem kivi_item(const KiviParams &p, int item)
 {
     using Cfg = KiviCfg<D, BITS, GEAR>;
     KiviItem w;
-    w.unit = item / p.splits;
-    w.split = item % p.splits;
+    kivi_unit_split(p, item, w.unit, w.split);
     w.b = w.unit / p.Hkv;
     w.hk = w.unit % p.Hkv;
     w.T = p.len[w.b];
@@ -365,7 +377,8 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
     // (channels [c D/4, (c+1) D/4)) in order, chunk k holding the lane's words 4k .. 4k + 3.
     constexpr bool QSTAGE = GEAR || Cfg::QS_BIAS;
     auto stage_q = [&](int item, int qb) {
-        const int unit = item / p.splits;
+        int unit, split_unused;
+        kivi_unit_split(p, item, unit, split_unused);
         const int bb = unit / p.Hkv, hh = unit % p.Hkv;
         const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
             p.q + ((size_t)bb * p.Hq + hh * p.g + (hv ? r : 0)) * D);

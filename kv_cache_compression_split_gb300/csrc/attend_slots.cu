@@ -758,31 +758,73 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 }
 
 // Merge split partials: o = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s.
-__global__ void k_combine(int Hq, int Hkv, int g, int D, int splits, const float *__restrict__ part_o,
-                          const float *__restrict__ part_ml, uint16_t *__restrict__ o,
-                          float *__restrict__ lse)
+// One warp per (sequence, query head) row, eight rows per block: the lanes read
+// the splits' (m, l) pairs 32 at a time, then every lane walks the splits for
+// its D/32 channels, so the partial rows stream in with 16-byte loads.
+constexpr int COMBINE_ROWS = 8;
+
+template <int D>
+__global__ void __launch_bounds__(32 * COMBINE_ROWS)
+    k_combine(int rows, int Hq, int Hkv, int g, int splits, const float *__restrict__ part_o,
+              const float *__restrict__ part_ml, uint16_t *__restrict__ o, float *__restrict__ lse)
 {
-    const int bh = blockIdx.x;
+    constexpr int V = D / 32;   // channels per lane
+    static_assert(V == 2 || V == 4, "head dim 64 or 128");
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x * COMBINE_ROWS + (threadIdx.x >> 5);
+    if (bh >= rows)
+        return;
     const int b = bh / Hq, hq = bh % Hq, hk = hq / g, h = hq % g;
     const size_t base = ((size_t)(b * Hkv + hk) * splits) * g + h;
+    const float *ml = part_ml + 2 * base;   // split sp at ml[2 sp g], ml[2 sp g + 1]
     float ms = -INFINITY;
-    for (int s = 0; s < splits; ++s)
-        ms = fmaxf(ms, part_ml[2 * (base + (size_t)s * g)]);
+    for (int sp = lane; sp < splits; sp += 32)
+        ms = fmaxf(ms, ml[2 * (size_t)sp * g]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, off));
     float ls = 0.f;
-    for (int s = 0; s < splits; ++s) {
-        const float m = part_ml[2 * (base + (size_t)s * g)];
-        ls += (m == -INFINITY ? 0.f : ex2(m - ms)) * part_ml[2 * (base + (size_t)s * g) + 1];
+    for (int sp = lane; sp < splits; sp += 32) {
+        const float m = ml[2 * (size_t)sp * g];
+        ls += (m == -INFINITY ? 0.f : ex2(m - ms)) * ml[2 * (size_t)sp * g + 1];
     }
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float os = 0.f;
-        for (int s = 0; s < splits; ++s) {
-            const float m = part_ml[2 * (base + (size_t)s * g)];
-            if (m != -INFINITY)
-                os += ex2(m - ms) * part_o[(base + (size_t)s * g) * D + d];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        ls += __shfl_xor_sync(0xffffffffu, ls, off);
+    float os[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+        os[v] = 0.f;
+#pragma unroll 4
+    for (int sp = 0; sp < splits; ++sp) {
+        const float m = ml[2 * (size_t)sp * g];
+        const float w = m == -INFINITY ? 0.f : ex2(m - ms);
+        const float *src = part_o + (base + (size_t)sp * g) * D + V * lane;
+        if constexpr (V == 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(src);
+            os[0] = fmaf(w, x.x, os[0]);
+            os[1] = fmaf(w, x.y, os[1]);
+            os[2] = fmaf(w, x.z, os[2]);
+            os[3] = fmaf(w, x.w, os[3]);
+        } else {
+            const float2 x = *reinterpret_cast<const float2 *>(src);
+            os[0] = fmaf(w, x.x, os[0]);
+            os[1] = fmaf(w, x.y, os[1]);
         }
-        o[(size_t)bh * D + d] = __half_as_ushort(__float2half_rn(ls > 0.f ? os / ls : 0.f));
     }
-    if (threadIdx.x == 0 && lse)
+    uint32_t packed[V / 2];
+#pragma unroll
+    for (int v = 0; v < V / 2; ++v) {
+        const float lo = ls > 0.f ? os[2 * v] / ls : 0.f, hi = ls > 0.f ? os[2 * v + 1] / ls : 0.f;
+        packed[v] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) |
+                    ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+    }
+    uint16_t *dst = o + (size_t)bh * D + V * lane;
+    if constexpr (V == 4)
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+    else
+        *reinterpret_cast<uint32_t *>(dst) = packed[0];
+    if (lane == 0 && lse)
         lse[bh] = ls > 0.f ? (ms + __log2f(ls)) * LN2 : -INFINITY;
 }
 
@@ -930,7 +972,14 @@ cudaError_t launch_decode_step(const StepLaunch &a, cudaStream_t s)
 cudaError_t launch_combine(int B, int Hq, int Hkv, int D, int splits, const float *part_o,
                            const float *part_ml, uint16_t *o, float *lse, cudaStream_t s)
 {
-    k_combine<<<B * Hq, D, 0, s>>>(Hq, Hkv, Hq / Hkv, D, splits, part_o, part_ml, o, lse);
+    const int rows = B * Hq;
+    const int grid = (rows + COMBINE_ROWS - 1) / COMBINE_ROWS;
+    if (D == 128)
+        k_combine<128><<<grid, 32 * COMBINE_ROWS, 0, s>>>(rows, Hq, Hkv, Hq / Hkv, splits, part_o,
+                                                          part_ml, o, lse);
+    else
+        k_combine<64><<<grid, 32 * COMBINE_ROWS, 0, s>>>(rows, Hq, Hkv, Hq / Hkv, splits, part_o,
+                                                         part_ml, o, lse);
     return cudaGetLastError();
 }
 

@@ -82,6 +82,13 @@ def test_null_arguments_are_rejected_without_touching_a_gpu(kvc):
         a.logits = a.lse = a.h2o_scores = 16
         a.h2o_decay = bad
         assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_INVALID_ARG, bad
+    # q and o are 16-byte aligned like every other pointer (the split combine writes o
+    # 8 bytes at a time)
+    a = kvc.AttendArgs()
+    a.kind, a.Hq, a.q, a.o, a.slots = kvc.KVC_KIND_SLOTS, 1, 16, 18, ctypes.pointer(d)
+    assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_INVALID_ARG
+    a.q, a.o = 24, 16
+    assert lib.kvc_decode_attend(ctypes.byref(a), None) == kvc.KVC_ERR_INVALID_ARG
     # fused H2O with the logits on chip: at most one cluster of 8 splits, each split within
     # the on-chip bound of KVC_H2O_ONCHIP_MAX_SLOTS slots
     a = kvc.AttendArgs()
