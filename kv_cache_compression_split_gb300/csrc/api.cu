@@ -231,6 +231,7 @@ struct AttendPlanFull {
     kvc_status st;
     int B, Hkv, D;
     SlotAttendPlan plan;
+    int full_units;  // KIVI with plan.splits > 1: units 0 .. full_units-1 run unsplit
     bool cluster;   // slot caches: 2..8 splits merged in a thread-block cluster
     size_t ws;
 };
@@ -287,10 +288,30 @@ AttendPlanFull plan_full(const kvc_attend_args *a)
         f.D = a->quant->D;
         // quantised tiles of four groups; the residual ring joins the last split
         const int tiles = (a->quant->Cq / KIVI_G + 3) / 4;
-        f.plan = plan_attend(f.B * f.Hkv, tiles > 0 ? tiles : 1, a->num_splits);
-        f.ws = f.plan.splits > 1
-                   ? (size_t)f.B * a->Hq * f.plan.splits * (f.D + 2) * sizeof(float)
-                   : 0;
+        const int units = f.B * f.Hkv;
+        f.plan = plan_attend(units, tiles > 0 ? tiles : 1, a->num_splits);
+        f.full_units = 0;
+        if (a->num_splits <= 0 && f.plan.splits == 1 && tiles >= 2) {
+            // The persistent CTAs (three per SM, two for GEAR) take whole units in
+            // rounds.  When the last round fills at most half of them, only its units
+            // are split (up to four ways), so that every CTA ends with about the same
+            // work; the other units still run whole, without partials.
+            const int ctas = (a->quant->k_gear ? 2 : 3) * sm_count();
+            const int tail = ctas > 0 ? units % ctas : 0;
+            if (units > ctas && tail > 0 && 2 * tail <= ctas) {
+                int st = ctas / tail;
+                st = st < 4 ? st : 4;
+                st = st < tiles ? st : tiles;
+                const int per = (tiles + st - 1) / st;
+                f.plan.splits = (tiles + per - 1) / per;
+                f.plan.tiles_per_split = per;
+                f.full_units = f.plan.splits > 1 ? units - tail : 0;
+            }
+        }
+        const int split_units = units - f.full_units;
+        f.ws = f.plan.splits > 1 ? (size_t)split_units * (a->Hq / f.Hkv) * f.plan.splits *
+                                       (f.D + 2) * sizeof(float)
+                                 : 0;
     } else {
         return f;
     }
@@ -406,11 +427,12 @@ kvc_status kvc_decode_attend(const kvc_attend_args *a, cudaStream_t stream)
         return from_cuda(launch_h2o_decode_acc(h, stream));
     }
     const kvc_quant_cache &c = *a->quant;
-    float *part_ml = part_o ? part_o + (size_t)f.B * a->Hq * f.plan.splits * f.D : nullptr;
+    const size_t split_rows = (size_t)(f.B * f.Hkv - f.full_units) * (a->Hq / f.Hkv);
+    float *part_ml = part_o ? part_o + split_rows * f.plan.splits * f.D : nullptr;
     KiviAttendLaunch L{f.B, a->Hq, c.Hkv, c.D, c.bits, c.R, c.Cq, a->q, a->o, c.k_blocks,
                        c.v_blocks, c.k_res, c.v_res, c.len, a->lse, part_o, part_ml,
-                       f.plan.splits, f.plan.tiles_per_split, scale, c.block_table,
-                       c.num_pages, c.k_gear, c.v_gear};
+                       f.plan.splits, f.plan.tiles_per_split, f.full_units, scale,
+                       c.block_table, c.num_pages, c.k_gear, c.v_gear};
     return from_cuda(launch_attend_kivi(L, stream));
 }
 

@@ -116,6 +116,7 @@ template <int D, int BITS, bool GEAR = false> struct KiviCfg {
 struct KiviParams {
     int Hq, Hkv, g, Cq, R, CR;
     int splits, qtiles_per_split, n_items;
+    int full_units;                 // units 0 .. full_units-1 run unsplit, the rest in `splits`
     const uint16_t *q;
     uint16_t *o;
     float *lse;
@@ -239,20 +240,30 @@ template <int N> __device__ __forceinline__ void lds_words(const uint32_t *src, 
 }
 
 struct KiviItem {
-    int unit, split, b, hk, T, n_groups, n_res, qt0, nq, nr;
+    int unit, split, nsplit, b, hk, T, n_groups, n_res, qt0, nq, nr;
 };
 
-// Work item -> (unit, split).  Items run split-major with the last split (the
-// one that also holds the residual ring, so the largest) first: the CTAs that
-// take items k, k + gridDim.x, ... then get a mix of splits whatever gridDim.x
-// is, instead of all the last splits landing on the same CTAs.
+// Work item -> (unit, split, splits of that unit).  Items 0 .. full_units-1 are
+// whole units; the other units are split `splits` ways, and their items run
+// split-major with the last split (the one that also holds the residual ring,
+// so the largest) first: the CTAs that take items k, k + gridDim.x, ... then
+// get a mix of splits whatever gridDim.x is, instead of all the last splits
+// landing on the same CTAs.
 __device__ __forceinline__ void kivi_unit_split(const KiviParams &p, int item, int &unit,
-                                                int &split)
+                                                int &split, int &nsplit)
 {
-    const int units = p.n_items / p.splits;
-    const int s = item / units;
-    unit = item - s * units;
+    if (item < p.full_units) {
+        unit = item;
+        split = 0;
+        nsplit = 1;
+        return;
+    }
+    const int k = item - p.full_units;
+    const int units = (p.n_items - p.full_units) / p.splits;
+    const int s = k / units;
+    unit = p.full_units + (k - s * units);
     split = p.splits - 1 - s;
+    nsplit = p.splits;
 }
 
 template <int D, int BITS, bool GEAR>
@@ -260,7 +271,7 @@ __device__ __forceinline__ KiviItem kivi_item(const KiviParams &p, int item)
 {
     using Cfg = KiviCfg<D, BITS, GEAR>;
     KiviItem w;
-    kivi_unit_split(p, item, w.unit, w.split);
+    kivi_unit_split(p, item, w.unit, w.split, w.nsplit);
     w.b = w.unit / p.Hkv;
     w.hk = w.unit % p.Hkv;
     w.T = p.len[w.b];
@@ -273,10 +284,11 @@ __device__ __forceinline__ KiviItem kivi_item(const KiviParams &p, int item)
     }
     w.n_res = w.T - w.n_groups * Cfg::G;
     const int unit_qtiles = (w.n_groups + Cfg::QG - 1) / Cfg::QG;
-    w.qt0 = w.split * p.qtiles_per_split;
-    const int qt1 = min(unit_qtiles, w.qt0 + p.qtiles_per_split);
+    const int per = w.nsplit == 1 ? unit_qtiles : p.qtiles_per_split;
+    w.qt0 = w.split * per;
+    const int qt1 = min(unit_qtiles, w.qt0 + per);
     w.nq = qt1 > w.qt0 ? qt1 - w.qt0 : 0;
-    w.nr = (w.split == p.splits - 1) ? (p.CR + Cfg::RS - 1) / Cfg::RS : 0;
+    w.nr = (w.split == w.nsplit - 1) ? (p.CR + Cfg::RS - 1) / Cfg::RS : 0;
     return w;
 }
 
@@ -377,8 +389,8 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
     // (channels [c D/4, (c+1) D/4)) in order, chunk k holding the lane's words 4k .. 4k + 3.
     constexpr bool QSTAGE = GEAR || Cfg::QS_BIAS;
     auto stage_q = [&](int item, int qb) {
-        int unit, split_unused;
-        kivi_unit_split(p, item, unit, split_unused);
+        int unit, split_unused, nsplit_unused;
+        kivi_unit_split(p, item, unit, split_unused, nsplit_unused);
         const int bb = unit / p.Hkv, hh = unit % p.Hkv;
         const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
             p.q + ((size_t)bb * p.Hq + hh * p.g + (hv ? r : 0)) * D);
@@ -908,7 +920,7 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
             acc[m][2] = o[2];
             acc[m][3] = o[3];
         }
-        const bool single = p.part_o == nullptr;
+        const bool single = wi.nsplit == 1;
         const int hs[2] = {h0, h1};
         const float lss[2] = {ls0, ls1}, mss[2] = {ms0, ms1};
 #pragma unroll
@@ -928,7 +940,8 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
                     p.lse[(size_t)b * p.Hq + hk * p.g + h] =
                         lss[e] > 0.f ? (mss[e] + __log2f(lss[e])) * LN2 : -INFINITY;
             } else {
-                const size_t pi = ((size_t)wi.unit * p.splits + wi.split) * p.g + h;
+                const size_t pi =
+                    ((size_t)(wi.unit - p.full_units) * p.splits + wi.split) * p.g + h;
                 float *po = p.part_o + pi * D;
 #pragma unroll
                 for (int m = 0; m < D / 16; ++m) {
@@ -1005,7 +1018,9 @@ cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s)
     kp.scale = a.scale;
     kp.scale_log2 = a.scale * LOG2E;
     kp.status = dev_status_ptr();
-    kp.n_items = a.B * a.Hkv * a.splits;
+    const int units = a.B * a.Hkv;
+    kp.full_units = a.splits > 1 ? a.full_units : units;
+    kp.n_items = kp.full_units + (units - kp.full_units) * a.splits;
     cudaError_t e;
     if (a.D == 128)
         e = a.bits == 4 ? launch_kivi_bits<128, 4>(a, kp, s) : launch_kivi_bits<128, 2>(a, kp, s);
@@ -1013,7 +1028,8 @@ cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s)
         e = a.bits == 4 ? launch_kivi_bits<64, 4>(a, kp, s) : launch_kivi_bits<64, 2>(a, kp, s);
     if (e != cudaSuccess || a.splits == 1)
         return e;
-    return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);
+    return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.full_units, units - a.full_units,
+                          a.part_o, a.part_ml, a.o, a.lse, s);
 }
 
 } // namespace kvc

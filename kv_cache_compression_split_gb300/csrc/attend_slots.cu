@@ -765,17 +765,20 @@ constexpr int COMBINE_ROWS = 8;
 
 template <int D>
 __global__ void __launch_bounds__(32 * COMBINE_ROWS)
-    k_combine(int rows, int Hq, int Hkv, int g, int splits, const float *__restrict__ part_o,
-              const float *__restrict__ part_ml, uint16_t *__restrict__ o, float *__restrict__ lse)
+    k_combine(int rows, int unit0, int Hq, int Hkv, int g, int splits,
+              const float *__restrict__ part_o, const float *__restrict__ part_ml,
+              uint16_t *__restrict__ o, float *__restrict__ lse)
 {
     constexpr int V = D / 32;   // channels per lane
     static_assert(V == 2 || V == 4, "head dim 64 or 128");
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x * COMBINE_ROWS + (threadIdx.x >> 5);
-    if (bh >= rows)
+    const int row = blockIdx.x * COMBINE_ROWS + (threadIdx.x >> 5);
+    if (row >= rows)
         return;
-    const int b = bh / Hq, hq = bh % Hq, hk = hq / g, h = hq % g;
-    const size_t base = ((size_t)(b * Hkv + hk) * splits) * g + h;
+    // row = (unit - unit0) * g + h; the unit is (b, hk), its query heads hk g .. hk g + g-1
+    const int j = row / g, h = row % g, unit = unit0 + j;
+    const int bh = (unit / Hkv) * Hq + (unit % Hkv) * g + h;
+    const size_t base = ((size_t)j * splits) * g + h;
     const float *ml = part_ml + 2 * base;   // split sp at ml[2 sp g], ml[2 sp g + 1]
     float ms = -INFINITY;
     for (int sp = lane; sp < splits; sp += 32)
@@ -914,7 +917,8 @@ cudaError_t launch_attend_slots(const AttendLaunch &a, cudaStream_t s)
                                : launch_slots_impl<64, LM_NONE>(tk, tv, sp, grid, s);
     if (e != cudaSuccess || on_chip)
         return e;
-    return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, a.part_o, a.part_ml, a.o, a.lse, s);
+    return launch_combine(a.B, a.Hq, a.Hkv, a.D, a.splits, 0, a.B * a.Hkv, a.part_o, a.part_ml,
+                          a.o, a.lse, s);
 }
 
 cudaError_t launch_decode_step(const StepLaunch &a, cudaStream_t s)
@@ -969,16 +973,21 @@ cudaError_t launch_decode_step(const StepLaunch &a, cudaStream_t s)
                 : launch_slots_impl<64, LM_SMEM, STEP_H2O>(tk, tv, sp, units, s);
 }
 
-cudaError_t launch_combine(int B, int Hq, int Hkv, int D, int splits, const float *part_o,
-                           const float *part_ml, uint16_t *o, float *lse, cudaStream_t s)
+cudaError_t launch_combine(int B, int Hq, int Hkv, int D, int splits, int unit0, int n_units,
+                           const float *part_o, const float *part_ml, uint16_t *o, float *lse,
+                           cudaStream_t s)
 {
-    const int rows = B * Hq;
+    (void)B;
+    const int g = Hq / Hkv;
+    const int rows = n_units * g;
+    if (rows <= 0)
+        return cudaSuccess;
     const int grid = (rows + COMBINE_ROWS - 1) / COMBINE_ROWS;
     if (D == 128)
-        k_combine<128><<<grid, 32 * COMBINE_ROWS, 0, s>>>(rows, Hq, Hkv, Hq / Hkv, splits, part_o,
+        k_combine<128><<<grid, 32 * COMBINE_ROWS, 0, s>>>(rows, unit0, Hq, Hkv, g, splits, part_o,
                                                           part_ml, o, lse);
     else
-        k_combine<64><<<grid, 32 * COMBINE_ROWS, 0, s>>>(rows, Hq, Hkv, Hq / Hkv, splits, part_o,
+        k_combine<64><<<grid, 32 * COMBINE_ROWS, 0, s>>>(rows, unit0, Hq, Hkv, g, splits, part_o,
                                                          part_ml, o, lse);
     return cudaGetLastError();
 }

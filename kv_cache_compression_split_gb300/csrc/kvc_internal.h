@@ -90,6 +90,7 @@ struct KiviAttendLaunch {
     float *lse;
     float *part_o, *part_ml;
     int splits, tiles_per_split;
+    int full_units;              // with splits > 1: units 0 .. full_units-1 run unsplit
     float scale;
     const int32_t *block_table;  // paged group blocks (nullptr: dense)
     int num_pages;
@@ -97,8 +98,11 @@ struct KiviAttendLaunch {
 };
 cudaError_t launch_attend_kivi(const KiviAttendLaunch &a, cudaStream_t s);
 
-cudaError_t launch_combine(int B, int Hq, int Hkv, int D, int splits, const float *part_o,
-                           const float *part_ml, uint16_t *o, float *lse, cudaStream_t s);
+// Merge the split partials of units unit0 .. unit0 + n_units - 1 (partial rows
+// indexed from unit0) into o and lse.
+cudaError_t launch_combine(int B, int Hq, int Hkv, int D, int splits, int unit0, int n_units,
+                           const float *part_o, const float *part_ml, uint16_t *o, float *lse,
+                           cudaStream_t s);
 
 cudaError_t launch_append_slots(const kvc_slot_cache &c, const uint16_t *k_new,
                                 const uint16_t *v_new, int n_new, cudaStream_t s);

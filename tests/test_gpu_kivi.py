@@ -305,3 +305,46 @@ def test_ragged_edge_lengths(kvc, orc, bits, splits):
     o, lse = _attend(kvc, cache, q.cuda(), splits)
     _check_ragged(orc, q, K, V, lens, R, bits, o, lse)
     assert device_status_clean(kvc)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_tail_units_split_over_idle_ctas(kvc, orc, bits):
+    """The automatic plan when the persistent CTAs (three per SM) take whole units in rounds and
+    the last round fills few of them: 3 x SMs + 10 units, so the last 10 units are split four
+    ways (partials merged afterwards) and the rest run whole.  Ragged lengths; every unit is
+    compared with the single-split launch, the split units and some whole ones with the
+    oracle."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    D, Hq, Hkv, R, Cq = 128, 4, 2, 32, 512
+    units = 3 * n_sm + 10
+    B = units // Hkv
+    pattern = [575, 1, 400, 544, 100, 0, 33, 64]
+    lens = [pattern[b % len(pattern)] for b in range(B)]
+    g = torch.Generator().manual_seed(40 + bits)
+    T = max(lens)
+    K = torch.randn(B, Hkv, T, D, generator=g).half()
+    V = torch.randn(B, Hkv, T, D, generator=g).half()
+    q = torch.randn(B, Hq, D, generator=g).half()
+    cache = _ragged_quant_cache(kvc, K, V, lens, bits, R, Cq)
+    qd = q.cuda()
+    assert kvc.kvc_workspace_size(cache, qd) > 0            # the tail plan is in use
+    o, lse = _attend(kvc, cache, qd)
+    o1, lse1 = _attend(kvc, cache, qd, 1)
+    assert_o_close(np16(o), np16(o1).astype(np.float64), what="auto vs one split")
+    fin = torch.isfinite(lse1)
+    assert torch.equal(fin, torch.isfinite(lse))
+    assert torch.allclose(lse[fin], lse1[fin], atol=KIVI_LSE_TOL, rtol=0)
+    gq = Hq // Hkv
+    first_split = units - units % (3 * n_sm)
+    check = sorted({u // Hkv for u in range(first_split, units)} | {0, 1, first_split // Hkv - 1})
+    for b in check:
+        for hk in range(Hkv):
+            if lens[b] == 0:
+                assert not np16(o[b, hk * gq:(hk + 1) * gq]).astype(np.float64).any()
+                continue
+            ref, ref_lse = orc.kivi_attend_unit(np16(q[b, hk * gq:(hk + 1) * gq]), np16(K[b, hk]),
+                                                np16(V[b, hk]), lens[b], R, bits)
+            assert_o_close(np16(o[b, hk * gq:(hk + 1) * gq]), ref, what=f"b={b} hk={hk}")
+            np.testing.assert_allclose(lse[b, hk * gq:(hk + 1) * gq].cpu().numpy(), ref_lse,
+                                       atol=KIVI_LSE_TOL, rtol=0)
+    assert device_status_clean(kvc)

@@ -10,6 +10,8 @@ merge on chip), for automatic and single-split plans, and with the fused H2O sco
 a second call changes neither torch's allocations nor the device's free memory; shapes that
 need more scratch than the fixed array are rejected.  This file is collected last on
 purpose."""
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -48,13 +50,18 @@ def _twice(kvc, cache, q, splits, logits=None, scores0=None, decay=0.0):
         sc = None if scores0 is None else scores0.clone()
         torch.cuda.synchronize()
         if i == 1:   # the second call allocates nothing, neither through torch nor the driver
+            gc.collect()   # no collection of earlier garbage may free tensors during the call
+            gc.disable()
             alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
-        kvc.kvc_decode_attend_noalloc(cache, q, o, logits=logits, lse=lse, num_splits=splits,
-                                      h2o_scores=sc, h2o_decay=decay)
-        torch.cuda.synchronize()
-        if i == 1:
-            assert torch.cuda.memory_allocated() == alloc0
-            assert torch.cuda.mem_get_info()[0] == free0
+        try:
+            kvc.kvc_decode_attend_noalloc(cache, q, o, logits=logits, lse=lse, num_splits=splits,
+                                          h2o_scores=sc, h2o_decay=decay)
+            torch.cuda.synchronize()
+            if i == 1:
+                assert torch.cuda.memory_allocated() == alloc0
+                assert torch.cuda.mem_get_info()[0] == free0
+        finally:
+            gc.enable()
         outs.append((o, lse, sc))
     return outs
 
