@@ -79,8 +79,19 @@ template <int D, int BITS, bool GEAR = false> struct KiviCfg {
     static constexpr int RT_BYTES = 2 * RS * D * 2;
     static constexpr int STAGE_BYTES =
         ((QT_BYTES > RT_BYTES ? QT_BYTES : RT_BYTES) + 1023) / 1024 * 1024;
-    static constexpr int RED_STRIDE = D + 4;   // padded per-head row of the merge scratch
-    static constexpr int RED_BYTES = (NCW - 1) * 8 * (RED_STRIDE + 2) * 4;
+    // 4-bit codes: the four consumer warps share the end-of-item merge (each owns D/4
+    // output channels) and take the residual tiles in pairs, in turn.  2-bit codes keep
+    // the merge in warp 0 and the residual tiles in warps 0-1: at D 128 both changes cost
+    // more than they save (the extra live values spill under the 128-register cap).
+    static constexpr bool WIDE = BITS == 4;
+    // merge scratch.  4-bit: every warp's (m, l) per head, then per owner warp (OWN m-tiles
+    // of output channels each) the other three warps' accumulators of those channels;
+    // 2-bit: warps 1-3's accumulators and (m, l), per head a row of D + 4 words.  Rows are
+    // padded by 4 words (conflict-free fragment stores).
+    static constexpr int OWN = (D / 16) / NCW;
+    static constexpr int OSTR = 16 * OWN + 4;
+    static constexpr int RED_BYTES = WIDE ? (NCW * 16 + NCW * (NCW - 1) * 8 * OSTR) * 4
+                                          : (NCW - 1) * 8 * (D + 4 + 2) * 4;
     // GEAR: one 32 x D fp16 sparse tile per consumer warp, rows padded by 16 bytes
     // (conflict-free ldmatrix)
     static constexpr int DT_STRIDE = (D + 8) * 2;
@@ -498,13 +509,18 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
                 i = ntiles + 1;
                 break;
             }
-            // warps 0 .. RS/16 - 1 take 16 ring slots each
-            const int s0 = i * Cfg::RS + 16 * warp;
-            if (warp < Cfg::RS / 16 && s0 < p.CR) {
+            // RS/16 warps take 16 ring slots each (4-bit codes: the warp groups take the
+            // tiles in turn; 2-bit codes: warps 0 .. RS/16 - 1 take them all)
+            constexpr int PW = Cfg::RS / 16, NPG = NCW / PW;
+            static_assert(NCW % PW == 0, "whole warp groups per residual tile");
+            const int wl = Cfg::WIDE ? warp % PW : warp;
+            const int s0 = i * Cfg::RS + 16 * wl;
+            const bool mine = Cfg::WIDE ? warp / PW == i % NPG : warp < PW;
+            if (mine && s0 < p.CR) {
                 const uint32_t kbase = smem_u32(smem + st * Cfg::STAGE_BYTES);
                 const uint32_t vbase = kbase + Cfg::NBOX * Cfg::RS * 128;
                 float sa[4] = {0.f, 0.f, 0.f, 0.f};
-                const int krow = 16 * warp + ri + 8 * (mi & 1);
+                const int krow = 16 * wl + ri + 8 * (mi & 1);
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
                     const int ch = 2 * s + (mi >> 1);
@@ -520,7 +536,7 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
                 softmax_update(xa, xb, 2);
                 const uint32_t pb0 = movmatrix_t(pack_half2(xa[0], xb[0]));
                 const uint32_t pb1 = movmatrix_t(pack_half2(xa[1], xb[1]));
-                const int vrow = 16 * warp + ri + 8 * (mi >> 1);
+                const int vrow = 16 * wl + ri + 8 * (mi >> 1);
 #pragma unroll
                 for (int m = 0; m < D / 16; ++m) {
                     const int ch = 2 * m + (mi & 1);
@@ -861,96 +877,221 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
         if (warp == 0 && item + (int)gridDim.x < p.n_items)
             stage_q(item + gridDim.x, qbuf ^ 1);
     }
-    consumer_bar();   // warp 0 has finished reading the previous item's scratch
+    consumer_bar();   // every warp has finished reading the previous item's scratch
     if (*abort)
         break;        // every consumer warp sees the same flag after the barrier
-    constexpr int RS = Cfg::RED_STRIDE;
-    if (warp > 0) {
-        float *wo = red + (warp - 1) * 8 * (RS + 2);
-#pragma unroll
-        for (int m = 0; m < D / 16; ++m) {
-            wo[h0 * RS + 16 * m + r] = acc[m][0];
-            wo[h1 * RS + 16 * m + r] = acc[m][1];
-            wo[h0 * RS + 16 * m + r + 8] = acc[m][2];
-            wo[h1 * RS + 16 * m + r + 8] = acc[m][3];
-        }
+    if constexpr (Cfg::WIDE) {
+        // Each warp merges the output channels of its own m-tiles: it publishes its (m, l)
+        // and hands the accumulators of the other warps' m-tiles to their owners.
+        constexpr int MT = D / 16, OWN = Cfg::OWN, OSTR = Cfg::OSTR;
+        float *const mlb = red;                 // [NCW][8 heads][m, l]
+        float *const ob = red + NCW * 16;       // [owner][source slot][8 heads][OSTR]
         if (r == 0) {
-            wo[8 * RS + 2 * h0] = m_run0;
-            wo[8 * RS + 2 * h0 + 1] = l_run0;
-            wo[8 * RS + 2 * h1] = m_run1;
-            wo[8 * RS + 2 * h1 + 1] = l_run1;
+            mlb[(warp * 8 + h0) * 2] = m_run0;
+            mlb[(warp * 8 + h0) * 2 + 1] = l_run0;
+            mlb[(warp * 8 + h1) * 2] = m_run1;
+            mlb[(warp * 8 + h1) * 2 + 1] = l_run1;
         }
-    }
-    consumer_bar();
-    if (warp == 0) {
-        float ms0 = m_run0, ms1 = m_run1;
-#pragma unroll
-        for (int v = 0; v < NCW - 1; ++v) {
-            const float *wo = red + v * 8 * (RS + 2) + 8 * RS;
-            ms0 = fmaxf(ms0, wo[2 * h0]);
-            ms1 = fmaxf(ms1, wo[2 * h1]);
-        }
-        float sc0[NCW], sc1[NCW];
-        sc0[0] = m_run0 == -INFINITY ? 0.f : ex2(m_run0 - ms0);
-        sc1[0] = m_run1 == -INFINITY ? 0.f : ex2(m_run1 - ms1);
-        float ls0 = sc0[0] * l_run0, ls1 = sc1[0] * l_run1;
-#pragma unroll
-        for (int v = 0; v < NCW - 1; ++v) {
-            const float *wo = red + v * 8 * (RS + 2) + 8 * RS;
-            const float mw0 = wo[2 * h0], mw1 = wo[2 * h1];
-            sc0[v + 1] = mw0 == -INFINITY ? 0.f : ex2(mw0 - ms0);
-            sc1[v + 1] = mw1 == -INFINITY ? 0.f : ex2(mw1 - ms1);
-            ls0 += sc0[v + 1] * wo[2 * h0 + 1];
-            ls1 += sc1[v + 1] * wo[2 * h1 + 1];
-        }
-#pragma unroll
-        for (int m = 0; m < D / 16; ++m) {
-            float o[4] = {acc[m][0] * sc0[0], acc[m][1] * sc1[0], acc[m][2] * sc0[0],
-                          acc[m][3] * sc1[0]};
-#pragma unroll
-            for (int v = 0; v < NCW - 1; ++v) {
-                const float *wo = red + v * 8 * (RS + 2);
-                o[0] += sc0[v + 1] * wo[h0 * RS + 16 * m + r];
-                o[1] += sc1[v + 1] * wo[h1 * RS + 16 * m + r];
-                o[2] += sc0[v + 1] * wo[h0 * RS + 16 * m + r + 8];
-                o[3] += sc1[v + 1] * wo[h1 * RS + 16 * m + r + 8];
-            }
-            acc[m][0] = o[0];
-            acc[m][1] = o[1];
-            acc[m][2] = o[2];
-            acc[m][3] = o[3];
-        }
-        const bool single = wi.nsplit == 1;
-        const int hs[2] = {h0, h1};
-        const float lss[2] = {ls0, ls1}, mss[2] = {ms0, ms1};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int h = hs[e];
-            if (h >= p.g)
+    #pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const int ow = m / OWN;
+            if (ow == warp)
                 continue;
-            if (single) {
-                const float inv = lss[e] > 0.f ? 1.f / lss[e] : 0.f;
-                uint16_t *orow = p.o + ((size_t)b * p.Hq + hk * p.g + h) * D;
-#pragma unroll
-                for (int m = 0; m < D / 16; ++m) {
-                    orow[16 * m + r] = __half_as_ushort(__float2half_rn(acc[m][e] * inv));
-                    orow[16 * m + r + 8] = __half_as_ushort(__float2half_rn(acc[m][2 + e] * inv));
+            const int slot = warp < ow ? warp : warp - 1;
+            float *dst = ob + (ow * (NCW - 1) + slot) * 8 * OSTR + (m - ow * OWN) * 16;
+            dst[h0 * OSTR + r] = acc[m][0];
+            dst[h1 * OSTR + r] = acc[m][1];
+            dst[h0 * OSTR + r + 8] = acc[m][2];
+            dst[h1 * OSTR + r + 8] = acc[m][3];
+        }
+        consumer_bar();
+        {
+            // the warps' weights, summed in warp order
+            float ms0 = mlb[h0 * 2], ms1 = mlb[h1 * 2];
+    #pragma unroll
+            for (int v = 1; v < NCW; ++v) {
+                ms0 = fmaxf(ms0, mlb[(v * 8 + h0) * 2]);
+                ms1 = fmaxf(ms1, mlb[(v * 8 + h1) * 2]);
+            }
+            float sc0[NCW], sc1[NCW], ls0 = 0.f, ls1 = 0.f;
+    #pragma unroll
+            for (int v = 0; v < NCW; ++v) {
+                const float mw0 = mlb[(v * 8 + h0) * 2], mw1 = mlb[(v * 8 + h1) * 2];
+                sc0[v] = mw0 == -INFINITY ? 0.f : ex2(mw0 - ms0);
+                sc1[v] = mw1 == -INFINITY ? 0.f : ex2(mw1 - ms1);
+                if (v == 0) {
+                    ls0 = sc0[0] * mlb[h0 * 2 + 1];
+                    ls1 = sc1[0] * mlb[h1 * 2 + 1];
+                } else {
+                    ls0 += sc0[v] * mlb[(v * 8 + h0) * 2 + 1];
+                    ls1 += sc1[v] * mlb[(v * 8 + h1) * 2 + 1];
                 }
-                if (r == 0 && p.lse)
-                    p.lse[(size_t)b * p.Hq + hk * p.g + h] =
-                        lss[e] > 0.f ? (mss[e] + __log2f(lss[e])) * LN2 : -INFINITY;
-            } else {
-                const size_t pi =
-                    ((size_t)(wi.unit - p.full_units) * p.splits + wi.split) * p.g + h;
-                float *po = p.part_o + pi * D;
-#pragma unroll
-                for (int m = 0; m < D / 16; ++m) {
-                    po[16 * m + r] = acc[m][e];
-                    po[16 * m + r + 8] = acc[m][2 + e];
+            }
+            int iu, isp, ins;   // found again here rather than kept live through the item
+            kivi_unit_split(p, item, iu, isp, ins);
+            const bool single = ins == 1;
+            const size_t pi0 = ((size_t)(iu - p.full_units) * p.splits + isp) * p.g;
+            const int hs[2] = {h0, h1};
+            const float lss[2] = {ls0, ls1}, mss[2] = {ms0, ms1};
+    #pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m / OWN != warp)
+                    continue;
+                const float *src = ob + warp * (NCW - 1) * 8 * OSTR + (m - warp * OWN) * 16;
+                float o[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+                for (int v = 0; v < NCW; ++v) {
+                    float x[4];
+                    if (v == warp) {
+                        x[0] = acc[m][0];
+                        x[1] = acc[m][1];
+                        x[2] = acc[m][2];
+                        x[3] = acc[m][3];
+                    } else {
+                        const float *sv = src + (v < warp ? v : v - 1) * 8 * OSTR;
+                        x[0] = sv[h0 * OSTR + r];
+                        x[1] = sv[h1 * OSTR + r];
+                        x[2] = sv[h0 * OSTR + r + 8];
+                        x[3] = sv[h1 * OSTR + r + 8];
+                    }
+                    if (v == 0) {
+                        o[0] = x[0] * sc0[0];
+                        o[1] = x[1] * sc1[0];
+                        o[2] = x[2] * sc0[0];
+                        o[3] = x[3] * sc1[0];
+                    } else {
+                        o[0] += sc0[v] * x[0];
+                        o[1] += sc1[v] * x[1];
+                        o[2] += sc0[v] * x[2];
+                        o[3] += sc1[v] * x[3];
+                    }
                 }
-                if (r == 0) {
-                    p.part_ml[2 * pi] = lss[e] > 0.f ? mss[e] : -INFINITY;
-                    p.part_ml[2 * pi + 1] = lss[e];
+    #pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int h = hs[e];
+                    if (h >= p.g)
+                        continue;
+                    if (single) {
+                        const float inv = lss[e] > 0.f ? 1.f / lss[e] : 0.f;
+                        uint16_t *orow = p.o + ((size_t)b * p.Hq + hk * p.g + h) * D;
+                        orow[16 * m + r] = __half_as_ushort(__float2half_rn(o[e] * inv));
+                        orow[16 * m + r + 8] = __half_as_ushort(__float2half_rn(o[2 + e] * inv));
+                    } else {
+                        float *po = p.part_o + (pi0 + h) * D;
+                        po[16 * m + r] = o[e];
+                        po[16 * m + r + 8] = o[2 + e];
+                    }
+                }
+            }
+            if (warp == 0 && r == 0) {
+    #pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int h = hs[e];
+                    if (h >= p.g)
+                        continue;
+                    if (single) {
+                        if (p.lse)
+                            p.lse[(size_t)b * p.Hq + hk * p.g + h] =
+                                lss[e] > 0.f ? (mss[e] + __log2f(lss[e])) * LN2 : -INFINITY;
+                    } else {
+                        p.part_ml[2 * (pi0 + h)] = lss[e] > 0.f ? mss[e] : -INFINITY;
+                        p.part_ml[2 * (pi0 + h) + 1] = lss[e];
+                    }
+                }
+            }
+        }
+    } else {
+    // warps 1-3 hand their state to warp 0, which merges all channels
+        constexpr int RS = D + 4;   // padded per-head row of the merge scratch
+        if (warp > 0) {
+            float *wo = red + (warp - 1) * 8 * (RS + 2);
+    #pragma unroll
+            for (int m = 0; m < D / 16; ++m) {
+                wo[h0 * RS + 16 * m + r] = acc[m][0];
+                wo[h1 * RS + 16 * m + r] = acc[m][1];
+                wo[h0 * RS + 16 * m + r + 8] = acc[m][2];
+                wo[h1 * RS + 16 * m + r + 8] = acc[m][3];
+            }
+            if (r == 0) {
+                wo[8 * RS + 2 * h0] = m_run0;
+                wo[8 * RS + 2 * h0 + 1] = l_run0;
+                wo[8 * RS + 2 * h1] = m_run1;
+                wo[8 * RS + 2 * h1 + 1] = l_run1;
+            }
+        }
+        consumer_bar();
+        if (warp == 0) {
+            float ms0 = m_run0, ms1 = m_run1;
+    #pragma unroll
+            for (int v = 0; v < NCW - 1; ++v) {
+                const float *wo = red + v * 8 * (RS + 2) + 8 * RS;
+                ms0 = fmaxf(ms0, wo[2 * h0]);
+                ms1 = fmaxf(ms1, wo[2 * h1]);
+            }
+            float sc0[NCW], sc1[NCW];
+            sc0[0] = m_run0 == -INFINITY ? 0.f : ex2(m_run0 - ms0);
+            sc1[0] = m_run1 == -INFINITY ? 0.f : ex2(m_run1 - ms1);
+            float ls0 = sc0[0] * l_run0, ls1 = sc1[0] * l_run1;
+    #pragma unroll
+            for (int v = 0; v < NCW - 1; ++v) {
+                const float *wo = red + v * 8 * (RS + 2) + 8 * RS;
+                const float mw0 = wo[2 * h0], mw1 = wo[2 * h1];
+                sc0[v + 1] = mw0 == -INFINITY ? 0.f : ex2(mw0 - ms0);
+                sc1[v + 1] = mw1 == -INFINITY ? 0.f : ex2(mw1 - ms1);
+                ls0 += sc0[v + 1] * wo[2 * h0 + 1];
+                ls1 += sc1[v + 1] * wo[2 * h1 + 1];
+            }
+    #pragma unroll
+            for (int m = 0; m < D / 16; ++m) {
+                float o[4] = {acc[m][0] * sc0[0], acc[m][1] * sc1[0], acc[m][2] * sc0[0],
+                              acc[m][3] * sc1[0]};
+    #pragma unroll
+                for (int v = 0; v < NCW - 1; ++v) {
+                    const float *wo = red + v * 8 * (RS + 2);
+                    o[0] += sc0[v + 1] * wo[h0 * RS + 16 * m + r];
+                    o[1] += sc1[v + 1] * wo[h1 * RS + 16 * m + r];
+                    o[2] += sc0[v + 1] * wo[h0 * RS + 16 * m + r + 8];
+                    o[3] += sc1[v + 1] * wo[h1 * RS + 16 * m + r + 8];
+                }
+                acc[m][0] = o[0];
+                acc[m][1] = o[1];
+                acc[m][2] = o[2];
+                acc[m][3] = o[3];
+            }
+            int iu, isp, ins;   // found again here rather than kept live through the item
+            kivi_unit_split(p, item, iu, isp, ins);
+            const bool single = ins == 1;
+            const int hs[2] = {h0, h1};
+            const float lss[2] = {ls0, ls1}, mss[2] = {ms0, ms1};
+    #pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = hs[e];
+                if (h >= p.g)
+                    continue;
+                if (single) {
+                    const float inv = lss[e] > 0.f ? 1.f / lss[e] : 0.f;
+                    uint16_t *orow = p.o + ((size_t)b * p.Hq + hk * p.g + h) * D;
+    #pragma unroll
+                    for (int m = 0; m < D / 16; ++m) {
+                        orow[16 * m + r] = __half_as_ushort(__float2half_rn(acc[m][e] * inv));
+                        orow[16 * m + r + 8] = __half_as_ushort(__float2half_rn(acc[m][2 + e] * inv));
+                    }
+                    if (r == 0 && p.lse)
+                        p.lse[(size_t)b * p.Hq + hk * p.g + h] =
+                            lss[e] > 0.f ? (mss[e] + __log2f(lss[e])) * LN2 : -INFINITY;
+                } else {
+                    const size_t pi =
+                        ((size_t)(iu - p.full_units) * p.splits + isp) * p.g + h;
+                    float *po = p.part_o + pi * D;
+    #pragma unroll
+                    for (int m = 0; m < D / 16; ++m) {
+                        po[16 * m + r] = acc[m][e];
+                        po[16 * m + r + 8] = acc[m][2 + e];
+                    }
+                    if (r == 0) {
+                        p.part_ml[2 * pi] = lss[e] > 0.f ? mss[e] : -INFINITY;
+                        p.part_ml[2 * pi + 1] = lss[e];
+                    }
                 }
             }
         }
