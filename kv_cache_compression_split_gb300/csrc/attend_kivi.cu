@@ -79,19 +79,12 @@ template <int D, int BITS, bool GEAR = false> struct KiviCfg {
     static constexpr int RT_BYTES = 2 * RS * D * 2;
     static constexpr int STAGE_BYTES =
         ((QT_BYTES > RT_BYTES ? QT_BYTES : RT_BYTES) + 1023) / 1024 * 1024;
-    // 4-bit codes: the four consumer warps share the end-of-item merge (each owns D/4
-    // output channels) and take the residual tiles in pairs, in turn.  2-bit codes keep
-    // the merge in warp 0 and the residual tiles in warps 0-1: at D 128 both changes cost
-    // more than they save (the extra live values spill under the 128-register cap).
-    static constexpr bool WIDE = BITS == 4;
-    // merge scratch.  4-bit: every warp's (m, l) per head, then per owner warp (OWN m-tiles
-    // of output channels each) the other three warps' accumulators of those channels;
-    // 2-bit: warps 1-3's accumulators and (m, l), per head a row of D + 4 words.  Rows are
-    // padded by 4 words (conflict-free fragment stores).
+    // merge scratch: every warp's (m, l) per head, then per owner warp (OWN m-tiles of
+    // output channels each) the other three warps' accumulators of those channels; rows
+    // padded by 4 words (conflict-free fragment stores)
     static constexpr int OWN = (D / 16) / NCW;
     static constexpr int OSTR = 16 * OWN + 4;
-    static constexpr int RED_BYTES = WIDE ? (NCW * 16 + NCW * (NCW - 1) * 8 * OSTR) * 4
-                                          : (NCW - 1) * 8 * (D + 4 + 2) * 4;
+    static constexpr int RED_BYTES = (NCW * 16 + NCW * (NCW - 1) * 8 * OSTR) * 4;
     // GEAR: one 32 x D fp16 sparse tile per consumer warp, rows padded by 16 bytes
     // (conflict-free ldmatrix)
     static constexpr int DT_STRIDE = (D + 8) * 2;
@@ -102,15 +95,23 @@ template <int D, int BITS, bool GEAR = false> struct KiviCfg {
     // bias chain, when the buffers fit beside the stages it would have anyway (they
     // free 16 registers per thread that the 128-register cap of three CTAs per SM
     // would otherwise spill)
+    // Where a second area fits too, KIVI also stages the scaled query pairs q / 2^(bits j)
+    // of the K operand (16 more registers freed per thread).
     static constexpr int QCH = D / 32;                 // 16-byte chunks per lane
-    static constexpr int QS_BUF = QCH * 32 * 16;
+    static constexpr int QS_BUF = QCH * 32 * 16;       // one area: a chunk per (lane, k)
     // CTAs per SM: three for KIVI (each within a third of the SM's 228 KB of shared
     // memory, 1 KB of it reserved per CTA), two for GEAR
     static constexpr int CTAS = GEAR ? 2 : 3;
     static constexpr int KIVI_ROOM = 233472 / 3 - 1024 - RED_BYTES - 1024 - 64;
-    static constexpr bool QS_BIAS =
-        !GEAR && (KIVI_ROOM - 2 * QS_BUF) / STAGE_BYTES == KIVI_ROOM / STAGE_BYTES;
-    static constexpr int QS_BYTES = (GEAR || QS_BIAS) ? 2 * QS_BUF : 0;
+    static constexpr bool fits(int areas)
+    {
+        return (KIVI_ROOM - 2 * areas * QS_BUF) / STAGE_BYTES == KIVI_ROOM / STAGE_BYTES;
+    }
+    static constexpr int QS_AREAS = GEAR ? 1 : (fits(2) ? 2 : (fits(1) ? 1 : 0));
+    static constexpr bool QS_BIAS = !GEAR && QS_AREAS >= 1;
+    static constexpr bool QS_PAIRS = !GEAR && QS_AREAS == 2;
+    static constexpr int QS_ITEM = QS_AREAS * QS_BUF;  // per item; two items in flight
+    static constexpr int QS_BYTES = 2 * QS_ITEM;
     static constexpr int NSTAGE_PLAIN =
         GEAR ? ((81920 / STAGE_BYTES) < 3 ? 3 : (81920 / STAGE_BYTES))
              : (KIVI_ROOM - QS_BYTES) / STAGE_BYTES;
@@ -160,6 +161,26 @@ template <int BITS> __device__ __forceinline__ uint32_t code_pair(uint32_t w, ui
 template <int BITS> __host__ __device__ constexpr float pair_weight(int j)
 {
     return (float)(1u << (BITS * (j % (8 / BITS))));
+}
+
+// The K operand's query pairs of one lane: lane c covers channels [c D/4, (c+1) D/4)
+// (w: those channels' words in order); pair pi holds channels (lo, lo + 16/BITS)
+// divided by the pair's field weight 2^(BITS (pi mod 8/BITS)), in binary16.
+template <int D, int BITS>
+__device__ __forceinline__ void query_pairs(const uint32_t (&w)[D / 8], uint32_t (&qp)[D / 8])
+{
+    constexpr int FPW = 32 / BITS, HALF = FPW / 2;
+#pragma unroll
+    for (int pi = 0; pi < D / 8; ++pi) {
+        const int j = pi % HALF;
+        const int lo = FPW * (pi / HALF) + j, hi = lo + HALF;
+        const __half2 wl = *reinterpret_cast<const __half2 *>(&w[lo >> 1]);
+        const __half2 wh = *reinterpret_cast<const __half2 *>(&w[hi >> 1]);
+        const float qlo = (lo & 1) ? __high2float(wl) : __low2float(wl);
+        const float qhi = (hi & 1) ? __high2float(wh) : __low2float(wh);
+        const float wgt = 1.0f / pair_weight<BITS>(j);
+        qp[pi] = pack_half2(qlo * wgt, qhi * wgt);
+    }
 }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
@@ -405,17 +426,28 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
         const int bb = unit / p.Hkv, hh = unit % p.Hkv;
         const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
             p.q + ((size_t)bb * p.Hq + hh * p.g + (hv ? r : 0)) * D);
-        uint4 *dst = reinterpret_cast<uint4 *>(qstage + qb * Cfg::QS_BUF) + lane;
+        uint4 *dst = reinterpret_cast<uint4 *>(qstage + qb * Cfg::QS_ITEM) + lane;
+        if constexpr (GEAR) {
 #pragma unroll
-        for (int k = 0; k < Cfg::QCH; ++k) {
-            if constexpr (GEAR)
+            for (int k = 0; k < Cfg::QCH; ++k)
                 dst[32 * k] = hv ? make_uint4(q32[16 * k + c], q32[16 * k + c + 4],
                                               q32[16 * k + 8 + c], q32[16 * k + 12 + c])
                                  : make_uint4(0u, 0u, 0u, 0u);
-            else
-            {
-                const uint32_t *w = q32 + c * (D / 8) + 4 * k;
-                dst[32 * k] = hv ? make_uint4(w[0], w[1], w[2], w[3]) : make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            uint32_t w[D / 8];
+#pragma unroll
+            for (int e = 0; e < D / 8; ++e)
+                w[e] = hv ? q32[c * (D / 8) + e] : 0u;
+#pragma unroll
+            for (int k = 0; k < Cfg::QCH; ++k)
+                dst[32 * k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            if constexpr (Cfg::QS_PAIRS) {
+                uint32_t qp[D / 8];
+                query_pairs<D, BITS>(w, qp);
+#pragma unroll
+                for (int k = 0; k < Cfg::QCH; ++k)
+                    dst[32 * (Cfg::QCH + k)] =
+                        make_uint4(qp[4 * k], qp[4 * k + 1], qp[4 * k + 2], qp[4 * k + 3]);
             }
         }
     };
@@ -509,14 +541,12 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
                 i = ntiles + 1;
                 break;
             }
-            // RS/16 warps take 16 ring slots each (4-bit codes: the warp groups take the
-            // tiles in turn; 2-bit codes: warps 0 .. RS/16 - 1 take them all)
+            // RS/16 warps take 16 ring slots each; the warp groups take the tiles in turn
             constexpr int PW = Cfg::RS / 16, NPG = NCW / PW;
             static_assert(NCW % PW == 0, "whole warp groups per residual tile");
-            const int wl = Cfg::WIDE ? warp % PW : warp;
+            const int wl = warp % PW;
             const int s0 = i * Cfg::RS + 16 * wl;
-            const bool mine = Cfg::WIDE ? warp / PW == i % NPG : warp < PW;
-            if (mine && s0 < p.CR) {
+            if (warp / PW == i % NPG && s0 < p.CR) {
                 const uint32_t kbase = smem_u32(smem + st * Cfg::STAGE_BYTES);
                 const uint32_t vbase = kbase + Cfg::NBOX * Cfg::RS * 128;
                 float sa[4] = {0.f, 0.f, 0.f, 0.f};
@@ -554,10 +584,11 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
     // ======================= quantised tiles: warp w takes group w (32 tokens)
     // query pairs: lane c covers channels [c D/4, (c+1) D/4); pair pi holds channels
     // (lo, lo + HALF) divided by the pair's field weight
-    uint32_t qpair[D / 8];
+    // (staged: read per group from shared memory instead)
+    uint32_t qpair[Cfg::QS_PAIRS ? 1 : D / 8];
     // KIVI without the staged query: the same channels in order (for the bias)
     uint32_t qh[QSTAGE ? 1 : D / 8];
-    {
+    if constexpr (!Cfg::QS_PAIRS) {
         uint32_t qh_[D / 8];
         const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow + c * (D / 4));
 #pragma unroll
@@ -566,17 +597,7 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
             if constexpr (!QSTAGE)
                 qh[e] = qh_[e];
         }
-#pragma unroll
-        for (int pi = 0; pi < D / 8; ++pi) {
-            const int j = pi % Cfg::HALF;
-            const int lo = Cfg::FPW * (pi / Cfg::HALF) + j, hi = lo + Cfg::HALF;
-            const __half2 wl = *reinterpret_cast<const __half2 *>(&qh_[lo >> 1]);
-            const __half2 wh = *reinterpret_cast<const __half2 *>(&qh_[hi >> 1]);
-            const float qlo = (lo & 1) ? __high2float(wl) : __low2float(wl);
-            const float qhi = (hi & 1) ? __high2float(wh) : __low2float(wh);
-            const float wgt = 1.0f / pair_weight<BITS>(j);
-            qpair[pi] = pack_half2(qlo * wgt, qhi * wgt);
-        }
+        query_pairs<D, BITS>(qh_, qpair);
     }
     bool code_units = false;   // acc scaled to the quantised tiles' units
     for (; i < ntiles; ++i, ++it) {
@@ -627,7 +648,7 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
                 __syncwarp();   // every lane's K entries are in the tile
                 uint4 qv[Cfg::QCH];
                 const uint4 *qsrc =
-                    reinterpret_cast<const uint4 *>(qstage + qbuf * Cfg::QS_BUF) + lane;
+                    reinterpret_cast<const uint4 *>(qstage + qbuf * Cfg::QS_ITEM) + lane;
 #pragma unroll
                 for (int k = 0; k < Cfg::QCH; ++k)
                     qv[k] = qsrc[32 * k];
@@ -658,7 +679,7 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
             } else {
                 const uint4 *zl = reinterpret_cast<const uint4 *>(ksz + D / 2 + c * (D / 8));
                 const uint4 *qsrc =
-                    reinterpret_cast<const uint4 *>(qstage + qbuf * Cfg::QS_BUF) + lane;
+                    reinterpret_cast<const uint4 *>(qstage + qbuf * Cfg::QS_ITEM) + lane;
                 float bz0[4] = {0.f, 0.f, 0.f, 0.f}, bz1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < D / 32; ++e) {
@@ -677,6 +698,20 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
             // ---- q~ pairs (B operand)
             uint32_t qt[D / 8];
             {
+                uint32_t qps[Cfg::QS_PAIRS ? D / 8 : 1];
+                if constexpr (Cfg::QS_PAIRS) {
+                    const uint4 *qsp = reinterpret_cast<const uint4 *>(
+                                           qstage + qbuf * Cfg::QS_ITEM + Cfg::QS_BUF) + lane;
+#pragma unroll
+                    for (int k = 0; k < Cfg::QCH; ++k) {
+                        const uint4 v = qsp[32 * k];
+                        qps[4 * k] = v.x;
+                        qps[4 * k + 1] = v.y;
+                        qps[4 * k + 2] = v.z;
+                        qps[4 * k + 3] = v.w;
+                    }
+                }
+                const uint32_t *qsrc_pairs = Cfg::QS_PAIRS ? qps : qpair;
                 const uint4 *sl = reinterpret_cast<const uint4 *>(ksz + c * (D / 8));
                 uint32_t sw[D / 8];
 #pragma unroll
@@ -694,7 +729,7 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
                     const uint32_t sp = __byte_perm(sw[lo >> 1], sw[hi >> 1],
                                                     ((lo & 1) ? 0x0032 : 0x0010) |
                                                         ((hi & 1) ? 0x7600 : 0x5400));
-                    qt[pi] = hmul2_u32(qpair[pi], sp);
+                    qt[pi] = hmul2_u32(qsrc_pairs[pi], sp);
                 }
             }
             const float sk = TWO24 * p.scale_log2;
@@ -880,190 +915,92 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
     consumer_bar();   // every warp has finished reading the previous item's scratch
     if (*abort)
         break;        // every consumer warp sees the same flag after the barrier
-    if constexpr (Cfg::WIDE) {
-        // Each warp merges the output channels of its own m-tiles: it publishes its (m, l)
-        // and hands the accumulators of the other warps' m-tiles to their owners.
-        constexpr int MT = D / 16, OWN = Cfg::OWN, OSTR = Cfg::OSTR;
-        float *const mlb = red;                 // [NCW][8 heads][m, l]
-        float *const ob = red + NCW * 16;       // [owner][source slot][8 heads][OSTR]
-        if (r == 0) {
-            mlb[(warp * 8 + h0) * 2] = m_run0;
-            mlb[(warp * 8 + h0) * 2 + 1] = l_run0;
-            mlb[(warp * 8 + h1) * 2] = m_run1;
-            mlb[(warp * 8 + h1) * 2 + 1] = l_run1;
+    // Each warp merges the output channels of its own m-tiles: it publishes its (m, l)
+    // and hands the accumulators of the other warps' m-tiles to their owners.
+    constexpr int MT = D / 16, OWN = Cfg::OWN, OSTR = Cfg::OSTR;
+    float *const mlb = red;                 // [NCW][8 heads][m, l]
+    float *const ob = red + NCW * 16;       // [owner][source slot][8 heads][OSTR]
+    if (r == 0) {
+        mlb[(warp * 8 + h0) * 2] = m_run0;
+        mlb[(warp * 8 + h0) * 2 + 1] = l_run0;
+        mlb[(warp * 8 + h1) * 2] = m_run1;
+        mlb[(warp * 8 + h1) * 2 + 1] = l_run1;
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        const int ow = m / OWN;
+        if (ow == warp)
+            continue;
+        const int slot = warp < ow ? warp : warp - 1;
+        float *dst = ob + (ow * (NCW - 1) + slot) * 8 * OSTR + (m - ow * OWN) * 16;
+        dst[h0 * OSTR + r] = acc[m][0];
+        dst[h1 * OSTR + r] = acc[m][1];
+        dst[h0 * OSTR + r + 8] = acc[m][2];
+        dst[h1 * OSTR + r + 8] = acc[m][3];
+    }
+    consumer_bar();
+    {
+        // the warps' weights, summed in warp order
+        float ms0 = mlb[h0 * 2], ms1 = mlb[h1 * 2];
+#pragma unroll
+        for (int v = 1; v < NCW; ++v) {
+            ms0 = fmaxf(ms0, mlb[(v * 8 + h0) * 2]);
+            ms1 = fmaxf(ms1, mlb[(v * 8 + h1) * 2]);
         }
-    #pragma unroll
+        float sc0[NCW], sc1[NCW], ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+        for (int v = 0; v < NCW; ++v) {
+            const float mw0 = mlb[(v * 8 + h0) * 2], mw1 = mlb[(v * 8 + h1) * 2];
+            sc0[v] = mw0 == -INFINITY ? 0.f : ex2(mw0 - ms0);
+            sc1[v] = mw1 == -INFINITY ? 0.f : ex2(mw1 - ms1);
+            if (v == 0) {
+                ls0 = sc0[0] * mlb[h0 * 2 + 1];
+                ls1 = sc1[0] * mlb[h1 * 2 + 1];
+            } else {
+                ls0 += sc0[v] * mlb[(v * 8 + h0) * 2 + 1];
+                ls1 += sc1[v] * mlb[(v * 8 + h1) * 2 + 1];
+            }
+        }
+        int iu, isp, ins;   // found again here rather than kept live through the item
+        kivi_unit_split(p, item, iu, isp, ins);
+        const bool single = ins == 1;
+        const size_t pi0 = ((size_t)(iu - p.full_units) * p.splits + isp) * p.g;
+        const int hs[2] = {h0, h1};
+        const float lss[2] = {ls0, ls1}, mss[2] = {ms0, ms1};
+#pragma unroll
         for (int m = 0; m < MT; ++m) {
-            const int ow = m / OWN;
-            if (ow == warp)
+            if (m / OWN != warp)
                 continue;
-            const int slot = warp < ow ? warp : warp - 1;
-            float *dst = ob + (ow * (NCW - 1) + slot) * 8 * OSTR + (m - ow * OWN) * 16;
-            dst[h0 * OSTR + r] = acc[m][0];
-            dst[h1 * OSTR + r] = acc[m][1];
-            dst[h0 * OSTR + r + 8] = acc[m][2];
-            dst[h1 * OSTR + r + 8] = acc[m][3];
-        }
-        consumer_bar();
-        {
-            // the warps' weights, summed in warp order
-            float ms0 = mlb[h0 * 2], ms1 = mlb[h1 * 2];
-    #pragma unroll
-            for (int v = 1; v < NCW; ++v) {
-                ms0 = fmaxf(ms0, mlb[(v * 8 + h0) * 2]);
-                ms1 = fmaxf(ms1, mlb[(v * 8 + h1) * 2]);
-            }
-            float sc0[NCW], sc1[NCW], ls0 = 0.f, ls1 = 0.f;
-    #pragma unroll
+            const float *src = ob + warp * (NCW - 1) * 8 * OSTR + (m - warp * OWN) * 16;
+            float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
             for (int v = 0; v < NCW; ++v) {
-                const float mw0 = mlb[(v * 8 + h0) * 2], mw1 = mlb[(v * 8 + h1) * 2];
-                sc0[v] = mw0 == -INFINITY ? 0.f : ex2(mw0 - ms0);
-                sc1[v] = mw1 == -INFINITY ? 0.f : ex2(mw1 - ms1);
-                if (v == 0) {
-                    ls0 = sc0[0] * mlb[h0 * 2 + 1];
-                    ls1 = sc1[0] * mlb[h1 * 2 + 1];
+                float x[4];
+                if (v == warp) {
+                    x[0] = acc[m][0];
+                    x[1] = acc[m][1];
+                    x[2] = acc[m][2];
+                    x[3] = acc[m][3];
                 } else {
-                    ls0 += sc0[v] * mlb[(v * 8 + h0) * 2 + 1];
-                    ls1 += sc1[v] * mlb[(v * 8 + h1) * 2 + 1];
+                    const float *sv = src + (v < warp ? v : v - 1) * 8 * OSTR;
+                    x[0] = sv[h0 * OSTR + r];
+                    x[1] = sv[h1 * OSTR + r];
+                    x[2] = sv[h0 * OSTR + r + 8];
+                    x[3] = sv[h1 * OSTR + r + 8];
+                }
+                if (v == 0) {
+                    o[0] = x[0] * sc0[0];
+                    o[1] = x[1] * sc1[0];
+                    o[2] = x[2] * sc0[0];
+                    o[3] = x[3] * sc1[0];
+                } else {
+                    o[0] += sc0[v] * x[0];
+                    o[1] += sc1[v] * x[1];
+                    o[2] += sc0[v] * x[2];
+                    o[3] += sc1[v] * x[3];
                 }
             }
-            int iu, isp, ins;   // found again here rather than kept live through the item
-            kivi_unit_split(p, item, iu, isp, ins);
-            const bool single = ins == 1;
-            const size_t pi0 = ((size_t)(iu - p.full_units) * p.splits + isp) * p.g;
-            const int hs[2] = {h0, h1};
-            const float lss[2] = {ls0, ls1}, mss[2] = {ms0, ms1};
-    #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (m / OWN != warp)
-                    continue;
-                const float *src = ob + warp * (NCW - 1) * 8 * OSTR + (m - warp * OWN) * 16;
-                float o[4] = {0.f, 0.f, 0.f, 0.f};
-    #pragma unroll
-                for (int v = 0; v < NCW; ++v) {
-                    float x[4];
-                    if (v == warp) {
-                        x[0] = acc[m][0];
-                        x[1] = acc[m][1];
-                        x[2] = acc[m][2];
-                        x[3] = acc[m][3];
-                    } else {
-                        const float *sv = src + (v < warp ? v : v - 1) * 8 * OSTR;
-                        x[0] = sv[h0 * OSTR + r];
-                        x[1] = sv[h1 * OSTR + r];
-                        x[2] = sv[h0 * OSTR + r + 8];
-                        x[3] = sv[h1 * OSTR + r + 8];
-                    }
-                    if (v == 0) {
-                        o[0] = x[0] * sc0[0];
-                        o[1] = x[1] * sc1[0];
-                        o[2] = x[2] * sc0[0];
-                        o[3] = x[3] * sc1[0];
-                    } else {
-                        o[0] += sc0[v] * x[0];
-                        o[1] += sc1[v] * x[1];
-                        o[2] += sc0[v] * x[2];
-                        o[3] += sc1[v] * x[3];
-                    }
-                }
-    #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int h = hs[e];
-                    if (h >= p.g)
-                        continue;
-                    if (single) {
-                        const float inv = lss[e] > 0.f ? 1.f / lss[e] : 0.f;
-                        uint16_t *orow = p.o + ((size_t)b * p.Hq + hk * p.g + h) * D;
-                        orow[16 * m + r] = __half_as_ushort(__float2half_rn(o[e] * inv));
-                        orow[16 * m + r + 8] = __half_as_ushort(__float2half_rn(o[2 + e] * inv));
-                    } else {
-                        float *po = p.part_o + (pi0 + h) * D;
-                        po[16 * m + r] = o[e];
-                        po[16 * m + r + 8] = o[2 + e];
-                    }
-                }
-            }
-            if (warp == 0 && r == 0) {
-    #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int h = hs[e];
-                    if (h >= p.g)
-                        continue;
-                    if (single) {
-                        if (p.lse)
-                            p.lse[(size_t)b * p.Hq + hk * p.g + h] =
-                                lss[e] > 0.f ? (mss[e] + __log2f(lss[e])) * LN2 : -INFINITY;
-                    } else {
-                        p.part_ml[2 * (pi0 + h)] = lss[e] > 0.f ? mss[e] : -INFINITY;
-                        p.part_ml[2 * (pi0 + h) + 1] = lss[e];
-                    }
-                }
-            }
-        }
-    } else {
-    // warps 1-3 hand their state to warp 0, which merges all channels
-        constexpr int RS = D + 4;   // padded per-head row of the merge scratch
-        if (warp > 0) {
-            float *wo = red + (warp - 1) * 8 * (RS + 2);
-    #pragma unroll
-            for (int m = 0; m < D / 16; ++m) {
-                wo[h0 * RS + 16 * m + r] = acc[m][0];
-                wo[h1 * RS + 16 * m + r] = acc[m][1];
-                wo[h0 * RS + 16 * m + r + 8] = acc[m][2];
-                wo[h1 * RS + 16 * m + r + 8] = acc[m][3];
-            }
-            if (r == 0) {
-                wo[8 * RS + 2 * h0] = m_run0;
-                wo[8 * RS + 2 * h0 + 1] = l_run0;
-                wo[8 * RS + 2 * h1] = m_run1;
-                wo[8 * RS + 2 * h1 + 1] = l_run1;
-            }
-        }
-        consumer_bar();
-        if (warp == 0) {
-            float ms0 = m_run0, ms1 = m_run1;
-    #pragma unroll
-            for (int v = 0; v < NCW - 1; ++v) {
-                const float *wo = red + v * 8 * (RS + 2) + 8 * RS;
-                ms0 = fmaxf(ms0, wo[2 * h0]);
-                ms1 = fmaxf(ms1, wo[2 * h1]);
-            }
-            float sc0[NCW], sc1[NCW];
-            sc0[0] = m_run0 == -INFINITY ? 0.f : ex2(m_run0 - ms0);
-            sc1[0] = m_run1 == -INFINITY ? 0.f : ex2(m_run1 - ms1);
-            float ls0 = sc0[0] * l_run0, ls1 = sc1[0] * l_run1;
-    #pragma unroll
-            for (int v = 0; v < NCW - 1; ++v) {
-                const float *wo = red + v * 8 * (RS + 2) + 8 * RS;
-                const float mw0 = wo[2 * h0], mw1 = wo[2 * h1];
-                sc0[v + 1] = mw0 == -INFINITY ? 0.f : ex2(mw0 - ms0);
-                sc1[v + 1] = mw1 == -INFINITY ? 0.f : ex2(mw1 - ms1);
-                ls0 += sc0[v + 1] * wo[2 * h0 + 1];
-                ls1 += sc1[v + 1] * wo[2 * h1 + 1];
-            }
-    #pragma unroll
-            for (int m = 0; m < D / 16; ++m) {
-                float o[4] = {acc[m][0] * sc0[0], acc[m][1] * sc1[0], acc[m][2] * sc0[0],
-                              acc[m][3] * sc1[0]};
-    #pragma unroll
-                for (int v = 0; v < NCW - 1; ++v) {
-                    const float *wo = red + v * 8 * (RS + 2);
-                    o[0] += sc0[v + 1] * wo[h0 * RS + 16 * m + r];
-                    o[1] += sc1[v + 1] * wo[h1 * RS + 16 * m + r];
-                    o[2] += sc0[v + 1] * wo[h0 * RS + 16 * m + r + 8];
-                    o[3] += sc1[v + 1] * wo[h1 * RS + 16 * m + r + 8];
-                }
-                acc[m][0] = o[0];
-                acc[m][1] = o[1];
-                acc[m][2] = o[2];
-                acc[m][3] = o[3];
-            }
-            int iu, isp, ins;   // found again here rather than kept live through the item
-            kivi_unit_split(p, item, iu, isp, ins);
-            const bool single = ins == 1;
-            const int hs[2] = {h0, h1};
-            const float lss[2] = {ls0, ls1}, mss[2] = {ms0, ms1};
-    #pragma unroll
+#pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int h = hs[e];
                 if (h >= p.g)
@@ -1071,27 +1008,28 @@ __global__ void __launch_bounds__(NTHREADS, KiviCfg<D, BITS, GEAR>::CTAS)
                 if (single) {
                     const float inv = lss[e] > 0.f ? 1.f / lss[e] : 0.f;
                     uint16_t *orow = p.o + ((size_t)b * p.Hq + hk * p.g + h) * D;
-    #pragma unroll
-                    for (int m = 0; m < D / 16; ++m) {
-                        orow[16 * m + r] = __half_as_ushort(__float2half_rn(acc[m][e] * inv));
-                        orow[16 * m + r + 8] = __half_as_ushort(__float2half_rn(acc[m][2 + e] * inv));
-                    }
-                    if (r == 0 && p.lse)
+                    orow[16 * m + r] = __half_as_ushort(__float2half_rn(o[e] * inv));
+                    orow[16 * m + r + 8] = __half_as_ushort(__float2half_rn(o[2 + e] * inv));
+                } else {
+                    float *po = p.part_o + (pi0 + h) * D;
+                    po[16 * m + r] = o[e];
+                    po[16 * m + r + 8] = o[2 + e];
+                }
+            }
+        }
+        if (warp == 0 && r == 0) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = hs[e];
+                if (h >= p.g)
+                    continue;
+                if (single) {
+                    if (p.lse)
                         p.lse[(size_t)b * p.Hq + hk * p.g + h] =
                             lss[e] > 0.f ? (mss[e] + __log2f(lss[e])) * LN2 : -INFINITY;
                 } else {
-                    const size_t pi =
-                        ((size_t)(iu - p.full_units) * p.splits + isp) * p.g + h;
-                    float *po = p.part_o + pi * D;
-    #pragma unroll
-                    for (int m = 0; m < D / 16; ++m) {
-                        po[16 * m + r] = acc[m][e];
-                        po[16 * m + r + 8] = acc[m][2 + e];
-                    }
-                    if (r == 0) {
-                        p.part_ml[2 * pi] = lss[e] > 0.f ? mss[e] : -INFINITY;
-                        p.part_ml[2 * pi + 1] = lss[e];
-                    }
+                    p.part_ml[2 * (pi0 + h)] = lss[e] > 0.f ? mss[e] : -INFINITY;
+                    p.part_ml[2 * (pi0 + h) + 1] = lss[e];
                 }
             }
         }
