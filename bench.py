@@ -190,6 +190,39 @@ def kivi_bytes(T, R, B, Hkv, Hq, D, bits):
     return B * Hkv * ((n_q // G) * 2 * block + ring) + 2 * B * Hq * D * 2
 
 
+def _parse_cpulist(txt: str) -> set:
+    cpus = set()
+    for part in txt.strip().split(","):
+        if not part:
+            continue
+        a, _, b = part.partition("-")
+        cpus.update(range(int(a), int(b or a) + 1))
+    return cpus
+
+
+def bind_gpu_local_cpus(dev) -> dict:
+    """Run on the CPU cores next to the GPU (those of them this process may use): pinned host
+    buffers land in the memory of the node whose core first touches them, and host<->device
+    copies from a far node cross the CPU interconnect.  Best effort; reports what it found."""
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bdf = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        base = os.path.join("/sys/bus/pci/devices", bdf)
+        with open(os.path.join(base, "local_cpulist")) as f:
+            local = _parse_cpulist(f.read())
+        with open(os.path.join(base, "numa_node")) as f:
+            node = int(f.read())
+        allowed = os.sched_getaffinity(0)
+        use = local & allowed
+        if use and use != allowed:
+            os.sched_setaffinity(0, use)
+        return {"gpu_numa_node": node, "gpu_local_cpus": len(local), "allowed_cpus": len(allowed),
+                "bound_to": len(use) if use else len(allowed)}
+    except (OSError, ValueError, AttributeError) as e:
+        return {"unknown": str(e)[:100]}
+
+
 def run_gpu(args, rank, world):
     import torch
     import kv_cache_compression_split_gb300 as kvc
@@ -199,6 +232,7 @@ def run_gpu(args, rank, world):
     kbuild.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
+    host_binding = bind_gpu_local_cpus(dev)
     stream = torch.cuda.Stream(dev)
     w = W.HEAVY
     B, Hq, Hkv, D, T0 = w.B, w.Hq, w.Hkv, w.D, w.T
@@ -596,6 +630,7 @@ def run_gpu(args, rank, world):
         "kernels": kernels, "methods": methods, "rows": rows, "clocks": clocks,
         "device_status": status, "tokens_per_step": 4 * B,
         "launches_per_step": launches_per_step, "h2d": h2d, "d2h": d2h,
+        "host_binding": host_binding,
         "hbm_peak": hbm_peak, "peak_kind": peak_kind,
         "splits": {"fp16": nb_fp, "h2o": nb_h2o, "stream": nb_st, "kivi": nb_kv},
         "kivi_window": {"first_timed_T": graph_T[0] - kv_shift,
@@ -1655,7 +1690,8 @@ def main():
                                  "each step runs the four methods on four streams (fork/join "
                                  "per step)"},
             "e2e": {"value": whole_job_rate(world, res["tokens_per_step"], e2e_ms), "unit": UNIT,
-                    "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+                    "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                    "host_binding": res["host_binding"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
             "roofline": {"bound": "hbm", "kernel": "k_attend_slots (FP16 cache launch)",
                          "achieved": dom["gbs"], "peak": res["hbm_peak"], "unit": "GB/s",
