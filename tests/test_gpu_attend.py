@@ -32,7 +32,9 @@ def _run(kvc, cache, q, want_logits=False, splits=0):
     (2, 4, 4, 100, 64, 0), (2, 4, 4, 100, 64, 3), (3, 16, 2, 300, 128, 0),
     (3, 16, 2, 300, 128, 1), (3, 16, 2, 300, 128, 4), (2, 8, 8, 129, 128, 2),
     (1, 8, 1, 513, 128, 0), (2, 6, 2, 70, 64, 2),
-    (2, 16, 2, 1024, 128, 8), (1, 8, 1, 1500, 128, 12), (3, 4, 4, 200, 64, 4)])
+    (2, 16, 2, 1024, 128, 8), (1, 8, 1, 1500, 128, 12), (3, 4, 4, 200, 64, 4),
+    # more than 32 splits: the combine reads the (m, l) pairs in two rounds of lanes
+    (1, 8, 2, 4096, 128, 64), (1, 4, 4, 2560, 64, 40)])
 def test_slots_ragged(kvc, orc, B, Hq, Hkv, C, D, splits):
     g = torch.Generator().manual_seed(B * 1000 + C + D + splits)
     K = torch.randn(B, Hkv, C, D, generator=g).half()

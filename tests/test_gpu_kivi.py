@@ -348,3 +348,29 @@ def test_tail_units_split_over_idle_ctas(kvc, orc, bits):
             np.testing.assert_allclose(lse[b, hk * gq:(hk + 1) * gq].cpu().numpy(), ref_lse,
                                        atol=KIVI_LSE_TOL, rtol=0)
     assert device_status_clean(kvc)
+
+
+def test_tail_units_split_over_idle_ctas_gear(kvc):
+    """The same plan for a GEAR cache, whose kernel keeps two CTAs per SM: 2 x SMs + 6 units;
+    every unit matches the single-split launch (itself checked against the GEAR oracle in
+    tests/test_gpu_gear.py)."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    D, Hq, Hkv, R, Cq = 128, 8, 2, 32, 256
+    units = 2 * n_sm + 6
+    B = units // Hkv
+    pattern = [287, 1, 200, 256, 64, 0, 40]
+    lens = [pattern[b % len(pattern)] for b in range(B)]
+    g = torch.Generator().manual_seed(77)
+    T = max(lens)
+    K = torch.randn(B, Hkv, T, D, generator=g).half()
+    V = torch.randn(B, Hkv, T, D, generator=g).half()
+    q = torch.randn(B, Hq, D, generator=g).half().cuda()
+    cache = _ragged_quant_cache(kvc, K, V, lens, 4, R, Cq, gear=True)
+    assert kvc.kvc_workspace_size(cache, q) > 0            # the tail plan is in use
+    o, lse = _attend(kvc, cache, q)
+    o1, lse1 = _attend(kvc, cache, q, 1)
+    assert_o_close(np16(o), np16(o1).astype(np.float64), what="auto vs one split")
+    fin = torch.isfinite(lse1)
+    assert torch.equal(fin, torch.isfinite(lse))
+    assert torch.allclose(lse[fin], lse1[fin], atol=KIVI_LSE_TOL, rtol=0)
+    assert device_status_clean(kvc)
