@@ -348,9 +348,13 @@ __global__ void __launch_bounds__(ETHREADS) k_evict(const EvictParams p)
 // Decode-sized caches (C <= WE_MAX_SLOTS): one warp per unit, warp-level
 // primitives only (no CTA barriers), so every unit of the batch is resident at
 // once.  Same keep rules and the same fill-the-holes-from-the-tail compaction.
+// A second instance for C <= WE_SMALL_SLOTS (a 512-slot budget plus its decode
+// slack) holds half the registers per lane, so four CTAs fit per SM instead of
+// two and a 4096-unit batch runs in one round.
 // ------------------------------------------------------------------------
 constexpr int WE_WARPS = 8;
 constexpr int WE_MAX_SLOTS = 1024;
+constexpr int WE_SMALL_SLOTS = 576;
 
 template <typename KeyFn, typename FiltFn>
 __device__ uint64_t warp_radix_select(int n, int k, KeyFn key, FiltFn filt, uint32_t *hist)
@@ -407,12 +411,14 @@ __device__ uint64_t warp_radix_select(int n, int k, KeyFn key, FiltFn filt, uint
     return prefix;
 }
 
-template <int KIND>
-__global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams p, int n_units)
+template <int KIND, int MAXS>
+__global__ void __launch_bounds__(WE_WARPS * 32, MAXS <= WE_SMALL_SLOTS ? 4 : 1)
+    k_evict_warp(const EvictParams p, int n_units)
 {
-    __shared__ uint32_t s_keep[WE_WARPS][WE_MAX_SLOTS / 32];
+    static_assert(MAXS % 32 == 0, "whole words of slots");
+    __shared__ uint32_t s_keep[WE_WARPS][MAXS / 32];
     __shared__ uint32_t s_hist[WE_WARPS][256];
-    __shared__ uint16_t s_hole[WE_WARPS][WE_MAX_SLOTS / 2];
+    __shared__ uint16_t s_hole[WE_WARPS][MAXS / 2];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int unit = blockIdx.x * WE_WARPS + warp;
     if (unit >= n_units)
@@ -433,7 +439,7 @@ __global__ void __launch_bounds__(WE_WARPS * 32) k_evict_warp(const EvictParams 
     int n_new = 0;
     // the unit's positions (and H2O scores) in registers: slot 32 i + lane in element i,
     // every load issued before the first is used, so the scans below cost one round trip
-    constexpr int NR = WE_MAX_SLOTS / 32;
+    constexpr int NR = MAXS / 32;
     int32_t pr[NR];
     float sr[KIND == EVICT_H2O ? NR : 1];
 #pragma unroll
@@ -886,14 +892,18 @@ cudaError_t launch_evict(const EvictLaunch &e, cudaStream_t s)
     const int wgrid = (units + WE_WARPS - 1) / WE_WARPS;
     switch (e.kind) {
     case EVICT_H2O:
-        if (small)
-            k_evict_warp<EVICT_H2O><<<wgrid, WE_WARPS * 32, 0, s>>>(p, units);
+        if (e.c.C <= WE_SMALL_SLOTS)
+            k_evict_warp<EVICT_H2O, WE_SMALL_SLOTS><<<wgrid, WE_WARPS * 32, 0, s>>>(p, units);
+        else if (small)
+            k_evict_warp<EVICT_H2O, WE_MAX_SLOTS><<<wgrid, WE_WARPS * 32, 0, s>>>(p, units);
         else
             k_evict<EVICT_H2O><<<units, ETHREADS, 0, s>>>(p);
         break;
     case EVICT_STREAM:
-        if (small)
-            k_evict_warp<EVICT_STREAM><<<wgrid, WE_WARPS * 32, 0, s>>>(p, units);
+        if (e.c.C <= WE_SMALL_SLOTS)
+            k_evict_warp<EVICT_STREAM, WE_SMALL_SLOTS><<<wgrid, WE_WARPS * 32, 0, s>>>(p, units);
+        else if (small)
+            k_evict_warp<EVICT_STREAM, WE_MAX_SLOTS><<<wgrid, WE_WARPS * 32, 0, s>>>(p, units);
         else
             k_evict<EVICT_STREAM><<<units, ETHREADS, 0, s>>>(p);
         break;
