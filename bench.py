@@ -1258,14 +1258,16 @@ def run_profile(args):
             else:
                 c = kvc.SlotCache(cache.K, cache.V, cache.pos.clone(), cache.n.clone(), cache.seqlen)
                 kvc.kvc_stream_evict(c, w.n_sink, w.n_recent)
-    elif what == "attend_kivi4":
+    elif what in ("attend_kivi4", "combine"):
+        # combine: the same attention forced into two splits, for the merge launch
+        splits = 2 if what == "combine" else 0
         cache = kvc.QuantCache.empty(B, Hkv, T, D, 4, w.kivi_R, device=dev)
         kvc.kvc_append_quant(cache, K, V)
         del K, V   # the capture holds only what the attention reads
         torch.cuda.empty_cache()
-        ws = torch.empty(max(kvc.kvc_workspace_size(cache, q) // 4, 1), device=dev)
+        ws = torch.empty(max(kvc.kvc_workspace_size(cache, q, splits) // 4, 1), device=dev)
         for _ in range(3):
-            kvc.kvc_decode_attend(cache, q, o, workspace=ws)
+            kvc.kvc_decode_attend(cache, q, o, workspace=ws, num_splits=splits)
     elif what == "attend_gear4":
         cache = kvc.QuantCache.empty(B, Hkv, T, D, 4, w.kivi_R, device=dev, gear=True)
         kvc.kvc_append_quant(cache, K, V)
@@ -1624,7 +1626,8 @@ def main():
                     help="run one kernel on a small case for ncu: attend_fp16, attend_h2o, "
                          "attend_kivi4, attend_gear4, attend_kivi2_mha, attend_kivi4_mha, "
                          "h2o_evict, stream_evict, stream_append, random_evict, prefill, "
-                         "kivi_pack, gear_pack, kivi_append_flush, gear_append_flush")
+                         "kivi_pack, gear_pack, kivi_append_flush, gear_append_flush, "
+                         "combine (KIVI-4 attention in two splits and their merge)")
     ap.add_argument("--profile-batch", type=int, default=64)
     ap.add_argument("--grid", action="store_true",
                     help="throughput profile grid over batch x KV length x method (JSON lines)")
