@@ -125,16 +125,30 @@ def _ptr(t):
         return t
     if not t.is_cuda:
         raise ValueError(f"kvc: tensor on {t.device}; the library takes CUDA tensors")
-    if t.device.index != torch.cuda.current_device():
-        raise ValueError(f"kvc: tensor on {t.device}, expected the current device "
-                         f"cuda:{torch.cuda.current_device()}")
-    if not t.is_contiguous():
+    if t.get_device() != torch.cuda.current_device() or not t.is_contiguous():
+        if t.device.index != torch.cuda.current_device():
+            raise ValueError(f"kvc: tensor on {t.device}, expected the current device "
+                             f"cuda:{torch.cuda.current_device()}")
         raise ValueError("kvc: tensor arguments must be contiguous")
     return t.data_ptr()
 
 
+# torch's raw current-stream query, where this torch version has it (a few hundred ns
+# against a few microseconds for torch.cuda.current_stream())
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _desc_key(tensors):
+    """What a cache descriptor depends on: each field tensor's address, device, shape and
+    strides (None for an absent field)."""
+    return tuple(None if t is None else (t.data_ptr(), t.get_device(), t.shape, t.stride())
+                 for t in tensors)
+
+
 def _stream(stream):
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
@@ -172,16 +186,14 @@ def _attend_args(cache, q, o, logits=None, lse=None, workspace=None, num_splits=
                  h2o_scores=None, h2o_decay=0.0, shape_only=False):
     a = AttendArgs()
     keep = []
+    d = cache.desc()
+    keep.append(d)
     if isinstance(cache, SlotCache):
-        d = cache.desc()
-        keep.append(d)
         a.kind = KVC_KIND_SLOTS
-        a.slots = C.pointer(d)
+        a.slots = cache.__dict__["_desc_p"]
     else:
-        d = cache.desc()
-        keep.append(d)
         a.kind = KVC_KIND_KIVI
-        a.quant = C.pointer(d)
+        a.quant = cache.__dict__["_desc_p"]
     a.Hq = int(q.shape[1])
     # a size query reads only q's shape (the library plans from the dimensions)
     a.q, a.o = (None, None) if shape_only else (_ptr(q), _ptr(o))
@@ -380,9 +392,19 @@ class SlotCache:
                    block_table=block_table.to(device=device, dtype=torch.int32).contiguous())
 
     def desc(self) -> SlotCacheDesc:
-        return SlotCacheDesc(self.B, self.Hkv, self.D, self.C, _ptr(self.K), _ptr(self.V),
-                             _ptr(self.pos), _ptr(self.n), _ptr(self.seqlen),
-                             _ptr(self.block_table), self.num_pages)
+        # built once and kept while the fields' storage, shapes and strides stay the same (a
+        # field replaced or resized in place yields a new key, and the fields are checked again)
+        t = (self.K, self.V, self.pos, self.n, self.seqlen, self.block_table)
+        key = _desc_key(t)
+        d = self.__dict__.get("_desc")
+        if d is not None and self.__dict__.get("_desc_key") == key:
+            return d
+        d = SlotCacheDesc(self.B, self.Hkv, self.D, self.C, _ptr(self.K), _ptr(self.V),
+                          _ptr(self.pos), _ptr(self.n), _ptr(self.seqlen),
+                          _ptr(self.block_table), self.num_pages)
+        self.__dict__["_desc"], self.__dict__["_desc_key"] = d, key
+        self.__dict__["_desc_p"] = C.pointer(d)
+        return d
 
 
 @dataclass
@@ -461,7 +483,17 @@ class QuantCache:
                    v_gear=torch.zeros(side, dtype=torch.uint8, device=device) if gear else None)
 
     def desc(self) -> QuantCacheDesc:
-        return QuantCacheDesc(self.B, self.Hkv, self.D, self.bits, self.R, self.Cq,
-                              _ptr(self.k_blocks), _ptr(self.v_blocks), _ptr(self.k_res),
-                              _ptr(self.v_res), _ptr(self.len), _ptr(self.block_table),
-                              self.num_pages, _ptr(self.k_gear), _ptr(self.v_gear))
+        # kept while the fields' storage, shapes and strides stay the same (see SlotCache)
+        t = (self.k_blocks, self.v_blocks, self.k_res, self.v_res, self.len, self.block_table,
+             self.k_gear, self.v_gear)
+        key = _desc_key(t) + (self.bits, self.R, self.Cq_paged)
+        d = self.__dict__.get("_desc")
+        if d is not None and self.__dict__.get("_desc_key") == key:
+            return d
+        d = QuantCacheDesc(self.B, self.Hkv, self.D, self.bits, self.R, self.Cq,
+                           _ptr(self.k_blocks), _ptr(self.v_blocks), _ptr(self.k_res),
+                           _ptr(self.v_res), _ptr(self.len), _ptr(self.block_table),
+                           self.num_pages, _ptr(self.k_gear), _ptr(self.v_gear))
+        self.__dict__["_desc"], self.__dict__["_desc_key"] = d, key
+        self.__dict__["_desc_p"] = C.pointer(d)
+        return d
