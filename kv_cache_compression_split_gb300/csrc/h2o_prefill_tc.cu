@@ -145,7 +145,8 @@ __device__ __forceinline__ void p1_chunk(const float *v, int j0, int gi, int L, 
 }
 
 // Pass 2: sum over 32 query columns i0 + c of 2^(s scale - lse_i) for key row gi;
-// nlse holds -lse_i of those columns.
+// nlse holds -lse_i of those columns (-inf past the prompt, so only the causal
+// diagonal needs a mask).
 template <bool MASK>
 __device__ __forceinline__ float p2_chunk(const float *v, const float *nlse, int i0, int gi, int L,
                                           float scale)
@@ -161,7 +162,7 @@ __device__ __forceinline__ float p2_chunk(const float *v, const float *nlse, int
         if (MASK) {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                e[u] = (i0 + c + u >= gi && i0 + c + u < L) ? e[u] : 0.f;
+                e[u] = i0 + c + u >= gi ? e[u] : 0.f;
         }
         a0 = fadd2(a0, make_float2(e[0], e[1]));
         a1 = fadd2(a1, make_float2(e[2], e[3]));
@@ -478,8 +479,7 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
                 // otherwise each of this warp's 32-column chunks is classified.
                 const int col0 = sp.qt * TT + 64 * half;   // first key (1) / query (2) column
                 const float *nl = lse_buf + ls * TT + 64 * half;
-                const bool inside =
-                    PASS == 1 ? sp.qt < t : (sp.qt > t && sp.qt * TT + TT <= p.L);
+                const bool inside = PASS == 1 ? sp.qt < t : sp.qt > t;
                 float tile_sum;
                 if (inside) {
                     tile_sum = fold_tile<PASS>(lane_addr + buf * TT, &acc_empty[buf], CH_FULL,
@@ -494,9 +494,9 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
                                      : (c0 + 31 <= r0 && c0 + 31 < p.L)   ? CH_FULL
                                                                           : CH_PART;
                         else
-                            cls[k] = (c0 >= p.L || c0 + 31 < r0)          ? CH_NONE
-                                     : (c0 >= r0 + 31 && c0 + 31 < p.L)   ? CH_FULL
-                                                                          : CH_PART;
+                            cls[k] = (c0 >= p.L || c0 + 31 < r0) ? CH_NONE
+                                     : c0 >= r0 + 31                 ? CH_FULL
+                                                                     : CH_PART;
                     }
                     tile_sum = fold_tile<PASS>(lane_addr + buf * TT, &acc_empty[buf], cls[0],
                                                cls[1], col0, gi, p, nl, m, l);
@@ -533,15 +533,15 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM)
                     break;
                 double other = mq[lane];
                 mbar_arrive(&mrg_empty[quarter]);
-                if (gi < p.L) {
-                    if (PASS == 1) {
-                        const float2 o = *reinterpret_cast<const float2 *>(&other);
-                        const float mm = fmaxf(m, o.x);
-                        const float ll = l * ex2o(m - mm) + o.y * ex2o(o.x - mm);
-                        p.nlse[(size_t)bh * p.Lpad + gi] = -(mm + __log2f(ll));
-                    } else {
-                        p.scores[(size_t)unit * p.C + gi] = (float)(acc + other);
-                    }
+                if (PASS == 1) {
+                    // rows of the last tile past L get -lse = -inf, so their
+                    // columns add 2^-inf = 0 in pass 2 without a mask
+                    const float2 o = *reinterpret_cast<const float2 *>(&other);
+                    const float mm = fmaxf(m, o.x);
+                    const float ll = l * ex2o(m - mm) + o.y * ex2o(o.x - mm);
+                    p.nlse[(size_t)bh * p.Lpad + gi] = gi < p.L ? -(mm + __log2f(ll)) : -INFINITY;
+                } else if (gi < p.L) {
+                    p.scores[(size_t)unit * p.C + gi] = (float)(acc + other);
                 }
             }
         }
