@@ -1240,7 +1240,7 @@ def run_profile(args):
     q = W.q_tensor(w, B=B, device=dev)
     o = torch.empty_like(q)
     what = args.profile
-    if what in ("attend_fp16", "attend_h2o", "h2o_evict", "stream_evict"):
+    if what in ("attend_fp16", "attend_h2o", "h2o_evict", "stream_evict", "h2o_acc"):
         n_slots = T if what == "attend_fp16" else 513
         cache = kvc.SlotCache.empty(B, Hkv, n_slots + 7, D, device=dev)
         kvc.kvc_append(cache, K[:, :, :n_slots].contiguous(), V[:, :, :n_slots].contiguous())
@@ -1250,6 +1250,11 @@ def run_profile(args):
         for _ in range(3):
             if what == "attend_h2o":   # attention + fused score update, logits on chip
                 kvc.kvc_decode_attend(cache, q, o, lse=lse, num_splits=1, h2o_scores=scores)
+            elif what == "h2o_acc":    # score update from logits the attention wrote to HBM
+                if _ == 0:
+                    logits = torch.empty(B, Hq, cache.C, device=dev)
+                    kvc.kvc_decode_attend(cache, q, o, logits=logits, lse=lse, workspace=ws)
+                kvc.kvc_h2o_accumulate_decode(cache, scores, logits, lse, Hq)
             elif what.startswith("attend"):
                 kvc.kvc_decode_attend(cache, q, o, lse=lse, workspace=ws)
             elif what == "h2o_evict":
@@ -1625,7 +1630,7 @@ def main():
     ap.add_argument("--profile", default=None,
                     help="run one kernel on a small case for ncu: attend_fp16, attend_h2o, "
                          "attend_kivi4, attend_gear4, attend_kivi2_mha, attend_kivi4_mha, "
-                         "h2o_evict, stream_evict, stream_append, random_evict, prefill, "
+                         "h2o_evict, stream_evict, stream_append, random_evict, prefill, h2o_acc, "
                          "kivi_pack, gear_pack, kivi_append_flush, gear_append_flush, "
                          "combine (KIVI-4 attention in two splits and their merge)")
     ap.add_argument("--profile-batch", type=int, default=64)

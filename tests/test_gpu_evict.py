@@ -247,6 +247,39 @@ def test_h2o_decode_step(kvc, orc, B, Hq, Hkv, D, mode, splits, decay):
     assert device_status_clean(kvc)
 
 
+@pytest.mark.parametrize("C", [517, 520])           # scalar rows / 16-byte rows
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (64, 8), (32, 2)])
+@pytest.mark.parametrize("decay", [0.0, 0.9])
+def test_h2o_accumulate_decode_layouts(kvc, orc, C, Hq, Hkv, decay):
+    """The standalone decode score update against the oracle's definition (H2O: the step's
+    attention probabilities summed over the group's query heads), for both row layouts,
+    groups of 1, 8 and 16 heads, ragged slot counts (0, C, and values off a multiple of 4),
+    plain and decayed scores; slots at or past n keep their old score bit for bit."""
+    rng = np.random.default_rng(SEED + C + 7 * Hq)
+    B = 3
+    logits = rng.normal(0.0, 3.0, (B, Hq, C)).astype(np.float32)
+    lse = (np.log(np.exp(logits.astype(np.float64)).sum(-1)) + rng.uniform(0, 2, (B, Hq)))
+    lse = lse.astype(np.float32)
+    sc0 = rng.uniform(0.0, 4.0, (B, Hkv, C)).astype(np.float32)
+    n = rng.integers(0, C + 1, (B, Hkv)).astype(np.int32)
+    n.flat[0], n.flat[-1] = 0, C
+    n.flat[1 % n.size] = C - 1
+    cache = kvc.SlotCache.empty(B, Hkv, C, 64)
+    cache.n.copy_(torch.from_numpy(n))
+    scores = torch.from_numpy(sc0).cuda()
+    kvc.kvc_h2o_accumulate_decode(cache, scores, torch.from_numpy(logits).cuda(),
+                                  torch.from_numpy(lse).cuda(), Hq, decay=decay)
+    got = scores.cpu().numpy()
+    ref = orc.h2o_accumulate(sc0.astype(np.float64), logits, lse, n,
+                             decay=float(np.float32(decay)))
+    for b in range(B):
+        for hk in range(Hkv):
+            k = n[b, hk]
+            np.testing.assert_allclose(got[b, hk, :k], ref[b, hk, :k], rtol=SCORE_REL_TOL)
+            assert np.array_equal(got[b, hk, k:].view(np.uint32), sc0[b, hk, k:].view(np.uint32))
+    assert device_status_clean(kvc)
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,D,L,n_heavy,n_recent,steps,onchip,decay", [
     (1, 4, 4, 64, 64, 8, 8, 32, True, 0.0),          # the tiny workload's H2O 8+8
     (2, 16, 2, 128, 300, 32, 64, 40, False, 0.0),
