@@ -313,24 +313,14 @@ template <int D> struct __align__(16) GearSmem {
     int red[2][QTHREADS / 32];
 };
 
-// quant_code_inv with a fast path: the fp32 estimate is within 3e-6 of the
-// true quotient whenever it is below cmax + 1 (three roundings of relative
-// 2^-24 on a quotient of at most 16), so unless it lies within 1e-4 of a
-// rounding midpoint its nearest integer is the exact code; an estimate of
-// cmax + 1 or more means a code clamped to cmax, and a zero reciprocal (scale 0)
-// gives code 0.  Only near-midpoints read the exact parameters of set pi.
-template <int D>
-__device__ __forceinline__ int quant_code_fast(uint16_t xb, float zero_f, float inv, int pi,
-                                               const GroupSmem<D> &sm, int cmax)
+__device__ __forceinline__ uint32_t h2_bits(__half2 h)
 {
-    const float est = (__half2float(__ushort_as_half(xb)) - zero_f) * inv;
-    if (est >= (float)(cmax + 1))
-        return cmax;
-    const float fr = est - floorf(est);
-    if (fabsf(fr - 0.5f) < 1e-4f)
-        return quant_code_inv(xb, sm.zfix[pi], zero_f, sm.sfix[pi], inv, cmax);
-    const int c = __float2int_rn(est);
-    return c < 0 ? 0 : (c > cmax ? cmax : c);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ __half2 bits_h2(uint32_t u)
+{
+    return *reinterpret_cast<const __half2 *>(&u);
 }
 
 __device__ __forceinline__ float warp_sum(float v)
@@ -763,39 +753,60 @@ __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16
     __syncthreads();
     uint16_t *ksz = reinterpret_cast<uint16_t *>(kblk + CODE_BYTES);
     uint16_t *vsz = reinterpret_cast<uint16_t *>(vblk + CODE_BYTES);
-    // 1. parameters: D K channels (over the group's 32 tokens) and G * NG = D V
-    //    (token, 32-channel group) sets, one thread each.  Binary16 values compare
-    //    exactly as fp32, so any scan order finds the same extremes (equal values
-    //    share their bits except +-0, and a -0 zero point is stored as +0); the V
-    //    scan starts at a per-thread rotation so that a warp's reads fall in
-    //    distinct banks.
-    for (int i = threadIdx.x; i < 2 * D; i += QTHREADS) {
-        const bool isk = i < D;
-        const int a = isk ? i : i - D;
-        const int t = a / NG, j = a % NG;       // V: token t, channel group j
-        const int rot = 2 * (t + 8 * (j >> 1));
-        auto val = [&](int e) -> uint16_t {
-            return isk ? sm.xk[e][a] : sm.xv[t][j * G + ((e + rot) & (G - 1))];
-        };
-        uint16_t mnb = val(0), mxb = mnb;
-        float mnf = __half2float(__ushort_as_half(mnb)), mxf = mnf;
-        for (int e = 1; e < G; ++e) {
-            const uint16_t hb = val(e);
-            const float v = __half2float(__ushort_as_half(hb));
-            if (v < mnf) {
-                mnf = v;
-                mnb = hb;
+    // 1. parameters, one set per thread: sets [0, D) are the K channels (over the
+    //    group's 32 tokens), sets [D, 2D) the V (token, 32-channel group) pairs.
+    //    The extremes are taken on binary16 pairs: min and max of binary16 values
+    //    are exact and do not depend on the scan order (a -0 / +0 tie is harmless:
+    //    a -0 zero point is stored as +0, and both are 0 in fixed point).  K: the
+    //    threads 2p and 2p + 1 scan channels 2p, 2p + 1 over tokens [0, 16) and
+    //    [16, 32) and swap their partial extremes; thread 2p + c keeps channel
+    //    2p + c.  V: a thread reads its set's 32 contiguous values as four 16-byte
+    //    chunks, starting at a chunk rotated by (token, group) so that a warp's
+    //    loads spread over all banks.
+    static_assert(2 * D <= QTHREADS, "one parameter set per thread");
+    if (threadIdx.x < 2 * D) {
+        const int i = threadIdx.x;
+        uint16_t mnb, mxb;
+        if (i < D) {
+            const int pr = i >> 1, c = i & 1;
+            const __half2 *col = reinterpret_cast<const __half2 *>(&sm.xk[16 * c][2 * pr]);
+            __half2 mn2 = col[0], mx2 = mn2;
+#pragma unroll
+            for (int e = 1; e < G / 2; ++e) {
+                const __half2 v = col[e * (D / 2)];
+                mn2 = __hmin2(mn2, v);
+                mx2 = __hmax2(mx2, v);
             }
-            if (v > mxf) {
-                mxf = v;
-                mxb = hb;
+            const uint32_t omn = __shfl_xor_sync(0xffffffffu, h2_bits(mn2), 1);
+            const uint32_t omx = __shfl_xor_sync(0xffffffffu, h2_bits(mx2), 1);
+            const uint32_t a = h2_bits(__hmin2(mn2, bits_h2(omn)));
+            const uint32_t b = h2_bits(__hmax2(mx2, bits_h2(omx)));
+            mnb = (uint16_t)(c ? a >> 16 : a & 0xffffu);
+            mxb = (uint16_t)(c ? b >> 16 : b & 0xffffu);
+        } else {
+            const int a = i - D, t = a / NG, j = a % NG;
+            const uint4 *row = reinterpret_cast<const uint4 *>(&sm.xv[t][j * G]);
+            const int rot = t + 2 * (j >> 1);
+            __half2 mn2, mx2;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const uint4 w = row[(cc + rot) & 3];
+                const __half2 v0 = bits_h2(w.x), v1 = bits_h2(w.y), v2 = bits_h2(w.z),
+                              v3 = bits_h2(w.w);
+                const __half2 lo = __hmin2(__hmin2(v0, v1), __hmin2(v2, v3));
+                const __half2 hi = __hmax2(__hmax2(v0, v1), __hmax2(v2, v3));
+                mn2 = cc == 0 ? lo : __hmin2(mn2, lo);
+                mx2 = cc == 0 ? hi : __hmax2(mx2, hi);
             }
+            mnb = __half_as_ushort(__hmin(__low2half(mn2), __high2half(mn2)));
+            mxb = __half_as_ushort(__hmax(__low2half(mx2), __high2half(mx2)));
         }
         const GroupQ q = group_params<BITS>(h2fix(mnb), mnb, h2fix(mxb));
-        if (isk) {
-            ksz[a] = q.scale_bits;
-            ksz[D + a] = q.zero_bits;
+        if (i < D) {
+            ksz[i] = q.scale_bits;
+            ksz[D + i] = q.zero_bits;
         } else {
+            const int a = i - D, t = a / NG, j = a % NG;
             vsz[j * G + t] = q.scale_bits;
             vsz[NG * G + j * G + t] = q.zero_bits;
         }
@@ -803,41 +814,65 @@ __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16
         sm.sfix[i] = q.scale_fix;
         sm.zf[i] = __half2float(__ushort_as_half(mnb));
         sm.sf[i] = __half2float(__ushort_as_half(q.scale_bits));
-        // a zero scale gives a zero reciprocal, so the fast path yields code 0
+        // a zero scale gives a zero reciprocal, so the estimate below is 0 (code 0)
         sm.inv[i] = q.scale_fix ? 1.0f / __half2float(__ushort_as_half(q.scale_bits)) : 0.f;
     }
     __syncthreads();
-    // 2. codes of the 2 * G * D elements, four channels (one word of codes) per step
+    // 2. codes of the 2 * G * D elements, four channels (one word of codes) per
+    //    step, on packed fp32 pairs.  est = (x - zero) * (1 / scale) in fp32 is
+    //    within 3e-6 of the true quotient while below cmax + 1 (three roundings of
+    //    relative 2^-24 on a quotient of at most 16), so away from a rounding
+    //    midpoint its nearest integer is the exact code.  Clamped to cmax, it is
+    //    rounded half-even by adding 1.5 * 2^23 (the sum's low mantissa byte is the
+    //    code); a word with an estimate within 1e-4 of a midpoint is redone in
+    //    exact integer arithmetic (quant_code_inv).  A zero scale has a zero
+    //    reciprocal: estimate 0, code 0.
+    constexpr float MAGIC = 12582912.0f;   // 1.5 * 2^23: ulp 1 over [2^23, 2^24)
+    const float2 magic2 = make_float2(MAGIC, MAGIC);
     for (int i = threadIdx.x; i < 2 * G * D / 4; i += QTHREADS) {
         const bool isk = i < G * D / 4;
         const int e = 4 * (isk ? i : i - G * D / 4);
         const int t = e / D, d0 = e % D;
         const uint2 xw = *reinterpret_cast<const uint2 *>(isk ? &sm.xk[t][d0] : &sm.xv[t][d0]);
-        const uint16_t xs[4] = {(uint16_t)(xw.x & 0xffff), (uint16_t)(xw.x >> 16),
-                                (uint16_t)(xw.y & 0xffff), (uint16_t)(xw.y >> 16)};
-        float zf[4], inv[4];
+        float2 z01, z23, i01, i23;
         int pis[4];
         if (isk) {   // per-channel parameters of channels d0 .. d0 + 3
             const float4 z4 = *reinterpret_cast<const float4 *>(&sm.zf[d0]);
             const float4 i4 = *reinterpret_cast<const float4 *>(&sm.inv[d0]);
-            zf[0] = z4.x, zf[1] = z4.y, zf[2] = z4.z, zf[3] = z4.w;
-            inv[0] = i4.x, inv[1] = i4.y, inv[2] = i4.z, inv[3] = i4.w;
+            z01 = make_float2(z4.x, z4.y), z23 = make_float2(z4.z, z4.w);
+            i01 = make_float2(i4.x, i4.y), i23 = make_float2(i4.z, i4.w);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 pis[u] = d0 + u;
         } else {     // the four channels share one (token, channel group) set
             const int pi = D + t * NG + d0 / G;
+            const float zz = sm.zf[pi], ii = sm.inv[pi];
+            z01 = z23 = make_float2(zz, zz);
+            i01 = i23 = make_float2(ii, ii);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                zf[u] = sm.zf[pi];
-                inv[u] = sm.inv[pi];
+            for (int u = 0; u < 4; ++u)
                 pis[u] = pi;
-            }
         }
-        uint32_t word = 0;
+        float2 e01 = fmul2(fsub2(__half22float2(bits_h2(xw.x)), z01), i01);
+        float2 e23 = fmul2(fsub2(__half22float2(bits_h2(xw.y)), z23), i23);
+        e01 = make_float2(fminf(e01.x, (float)CMAX), fminf(e01.y, (float)CMAX));
+        e23 = make_float2(fminf(e23.x, (float)CMAX), fminf(e23.y, (float)CMAX));
+        const float2 r01 = fadd2(e01, magic2), r23 = fadd2(e23, magic2);
+        const float2 f01 = fsub2(e01, fsub2(r01, magic2)), f23 = fsub2(e23, fsub2(r23, magic2));
+        uint32_t word = (__float_as_uint(r01.x) & 0xffu) | ((__float_as_uint(r01.y) & 0xffu) << 8) |
+                        ((__float_as_uint(r23.x) & 0xffu) << 16) | (__float_as_uint(r23.y) << 24);
+        constexpr float NEAR = 0.5f - 1e-4f;
+        if (fabsf(f01.x) > NEAR || fabsf(f01.y) > NEAR || fabsf(f23.x) > NEAR ||
+            fabsf(f23.y) > NEAR) {
+            const uint16_t xs[4] = {(uint16_t)(xw.x & 0xffff), (uint16_t)(xw.x >> 16),
+                                    (uint16_t)(xw.y & 0xffff), (uint16_t)(xw.y >> 16)};
+            const float zs[4] = {z01.x, z01.y, z23.x, z23.y}, is[4] = {i01.x, i01.y, i23.x, i23.y};
+            word = 0;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            word |= (uint32_t)quant_code_fast(xs[u], zf[u], inv[u], pis[u], sm, CMAX) << (8 * u);
+            for (int u = 0; u < 4; ++u)
+                word |= (uint32_t)quant_code_inv(xs[u], sm.zfix[pis[u]], zs[u], sm.sfix[pis[u]],
+                                                 is[u], CMAX) << (8 * u);
+        }
         *reinterpret_cast<uint32_t *>(isk ? &sm.ck[t][d0] : &sm.cv[t][d0]) = word;
     }
     __syncthreads();
