@@ -818,8 +818,8 @@ __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16
         sm.inv[i] = q.scale_fix ? 1.0f / __half2float(__ushort_as_half(q.scale_bits)) : 0.f;
     }
     __syncthreads();
-    // 2. codes of the 2 * G * D elements, four channels (one word of codes) per
-    //    step, on packed fp32 pairs.  est = (x - zero) * (1 / scale) in fp32 is
+    // 2. codes of the 2 * G * D elements, on packed fp32 pairs.  est =
+    //    (x - zero) * (1 / scale) in fp32 is
     //    within 3e-6 of the true quotient while below cmax + 1 (three roundings of
     //    relative 2^-24 on a quotient of at most 16), so away from a rounding
     //    midpoint its nearest integer is the exact code.  Clamped to cmax, it is
@@ -828,10 +828,61 @@ __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16
     //    exact integer arithmetic (quant_code_inv).  A zero scale has a zero
     //    reciprocal: estimate 0, code 0.
     constexpr float MAGIC = 12582912.0f;   // 1.5 * 2^23: ulp 1 over [2^23, 2^24)
+    constexpr float NEAR = 0.5f - 1e-4f;
     const float2 magic2 = make_float2(MAGIC, MAGIC);
-    for (int i = threadIdx.x; i < 2 * G * D / 4; i += QTHREADS) {
-        const bool isk = i < G * D / 4;
-        const int e = 4 * (isk ? i : i - G * D / 4);
+    // est of a pair of elements, clamped; r holds the rounded codes, the return
+    // value says whether either estimate lies near a midpoint
+    auto pair_codes = [&](uint32_t x2, float2 z, float2 inv, float2 &r) -> bool {
+        float2 e = fmul2(fsub2(__half22float2(bits_h2(x2)), z), inv);
+        e = make_float2(fminf(e.x, (float)CMAX), fminf(e.y, (float)CMAX));
+        r = fadd2(e, magic2);
+        const float2 f = fsub2(e, fsub2(r, magic2));
+        return fabsf(f.x) > NEAR || fabsf(f.y) > NEAR;
+    };
+    // 2a. 4-bit K token rows, straight into the block: field f of word w holds
+    //     the code of channel 8w + f (one 16-byte chunk of inputs per word).
+    //     2-bit words (16 channels) measured slower this way, and GEAR reads the
+    //     K codes back as bytes; both are packed from bytes in 3a.
+    constexpr int FPW = 32 / BITS;
+    constexpr bool K_DIRECT = BITS == 4 && !GEAR;
+    uint32_t *kw = reinterpret_cast<uint32_t *>(kblk);
+    for (int i = threadIdx.x; K_DIRECT && i < G * WK; i += QTHREADS) {
+        const int t = i / WK, c0 = FPW * (i % WK);
+        uint32_t word = 0;
+        bool near = false;
+#pragma unroll
+        for (int q = 0; q < FPW / 8; ++q) {
+            const int c = c0 + 8 * q;
+            const uint4 xw = *reinterpret_cast<const uint4 *>(&sm.xk[t][c]);
+            const float4 za = *reinterpret_cast<const float4 *>(&sm.zf[c]);
+            const float4 zb = *reinterpret_cast<const float4 *>(&sm.zf[c + 4]);
+            const float4 ia = *reinterpret_cast<const float4 *>(&sm.inv[c]);
+            const float4 ib = *reinterpret_cast<const float4 *>(&sm.inv[c + 4]);
+            float2 r[4];
+            near |= pair_codes(xw.x, make_float2(za.x, za.y), make_float2(ia.x, ia.y), r[0]);
+            near |= pair_codes(xw.y, make_float2(za.z, za.w), make_float2(ia.z, ia.w), r[1]);
+            near |= pair_codes(xw.z, make_float2(zb.x, zb.y), make_float2(ib.x, ib.y), r[2]);
+            near |= pair_codes(xw.w, make_float2(zb.z, zb.w), make_float2(ib.z, ib.w), r[3]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                word |= (__float_as_uint(r[u].x) & CMAX) << (BITS * (8 * q + 2 * u));
+                word |= (__float_as_uint(r[u].y) & CMAX) << (BITS * (8 * q + 2 * u + 1));
+            }
+        }
+        if (near) {
+            word = 0;
+            for (int f = 0; f < FPW; ++f)
+                word |= (uint32_t)quant_code_inv(sm.xk[t][c0 + f], sm.zfix[c0 + f], sm.zf[c0 + f],
+                                                 sm.sfix[c0 + f], sm.inv[c0 + f], CMAX)
+                        << (BITS * f);
+        }
+        kw[i] = word;
+    }
+    // 2b. codes as bytes, four channels per step: the V elements (the four share
+    //     one (token, channel group) set) and, unless 2a took them, the K elements
+    for (int i = threadIdx.x; i < (K_DIRECT ? 1 : 2) * G * D / 4; i += QTHREADS) {
+        const bool isk = !K_DIRECT && i >= G * D / 4;
+        const int e = 4 * (isk ? i - G * D / 4 : i);
         const int t = e / D, d0 = e % D;
         const uint2 xw = *reinterpret_cast<const uint2 *>(isk ? &sm.xk[t][d0] : &sm.xv[t][d0]);
         float2 z01, z23, i01, i23;
@@ -844,7 +895,7 @@ __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 pis[u] = d0 + u;
-        } else {     // the four channels share one (token, channel group) set
+        } else {
             const int pi = D + t * NG + d0 / G;
             const float zz = sm.zf[pi], ii = sm.inv[pi];
             z01 = z23 = make_float2(zz, zz);
@@ -853,17 +904,11 @@ __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16
             for (int u = 0; u < 4; ++u)
                 pis[u] = pi;
         }
-        float2 e01 = fmul2(fsub2(__half22float2(bits_h2(xw.x)), z01), i01);
-        float2 e23 = fmul2(fsub2(__half22float2(bits_h2(xw.y)), z23), i23);
-        e01 = make_float2(fminf(e01.x, (float)CMAX), fminf(e01.y, (float)CMAX));
-        e23 = make_float2(fminf(e23.x, (float)CMAX), fminf(e23.y, (float)CMAX));
-        const float2 r01 = fadd2(e01, magic2), r23 = fadd2(e23, magic2);
-        const float2 f01 = fsub2(e01, fsub2(r01, magic2)), f23 = fsub2(e23, fsub2(r23, magic2));
+        float2 r01, r23;
+        const bool near = pair_codes(xw.x, z01, i01, r01) | pair_codes(xw.y, z23, i23, r23);
         uint32_t word = (__float_as_uint(r01.x) & 0xffu) | ((__float_as_uint(r01.y) & 0xffu) << 8) |
                         ((__float_as_uint(r23.x) & 0xffu) << 16) | (__float_as_uint(r23.y) << 24);
-        constexpr float NEAR = 0.5f - 1e-4f;
-        if (fabsf(f01.x) > NEAR || fabsf(f01.y) > NEAR || fabsf(f23.x) > NEAR ||
-            fabsf(f23.y) > NEAR) {
+        if (near) {
             const uint16_t xs[4] = {(uint16_t)(xw.x & 0xffff), (uint16_t)(xw.x >> 16),
                                     (uint16_t)(xw.y & 0xffff), (uint16_t)(xw.y >> 16)};
             const float zs[4] = {z01.x, z01.y, z23.x, z23.y}, is[4] = {i01.x, i01.y, i23.x, i23.y};
@@ -876,17 +921,17 @@ __device__ __forceinline__ void pack_group(long g, long T0, int CR, const uint16
         *reinterpret_cast<uint32_t *>(isk ? &sm.ck[t][d0] : &sm.cv[t][d0]) = word;
     }
     __syncthreads();
-    // 3. pack K token rows: field i of word w holds channel (32/BITS)*w + i
-    uint32_t *kw = reinterpret_cast<uint32_t *>(kblk);
-    for (int i = threadIdx.x; i < G * WK; i += QTHREADS) {
+    // 3a. K token rows from the bytes (2-bit, GEAR): field f of word w holds
+    //     channel (32/BITS)*w + f
+    for (int i = threadIdx.x; !K_DIRECT && i < G * WK; i += QTHREADS) {
         const int t = i / WK, w = i % WK;
         uint32_t word = 0;
 #pragma unroll
-        for (int f = 0; f < 32 / BITS; ++f)
-            word |= (uint32_t)sm.ck[t][(32 / BITS) * w + f] << (BITS * f);
+        for (int f = 0; f < FPW; ++f)
+            word |= (uint32_t)sm.ck[t][FPW * w + f] << (BITS * f);
         kw[i] = word;
     }
-    // pack V token pairs: word ((rr + 2 pair) mod 8)*W + k, field j holds channel
+    // 3b. V token pairs: word ((rr + 2 pair) mod 8)*W + k, field j holds channel
     // 16*(k*(8/BITS) + j/2) + 8*(j%2) + rr; low half token 2i, high half 2i+1
     uint32_t *vw = reinterpret_cast<uint32_t *>(vblk);
     for (int i = threadIdx.x; i < (G / 2) * 8 * W; i += QTHREADS) {
