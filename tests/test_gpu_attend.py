@@ -76,6 +76,37 @@ def test_splits_agree_bitwise_with_each_other_run_to_run(kvc):
     assert torch.equal(a, b)   # deterministic: no atomics in the reduction
 
 
+def test_binding_descriptor_follows_replaced_fields(kvc, orc):
+    """The binding keeps each cache's descriptor between calls; replacing a field (a new
+    tensor for n, K and V swapped for other storage) must reach the next call, and in-place
+    updates of the same tensors must need no rebuild."""
+    g = torch.Generator().manual_seed(11)
+    B, Hq, Hkv, C, D = 2, 8, 2, 96, 64
+    K = torch.randn(B, Hkv, C, D, generator=g).half()
+    V = torch.randn(B, Hkv, C, D, generator=g).half()
+    q = torch.randn(B, Hq, D, generator=g).half()
+    n0 = np.array([[96, 40], [7, 64]])
+    cache = slot_cache_from(kvc, K, V, n0, C)
+
+    def check(Kh, Vh, n):
+        o, lse, _ = _run(kvc, cache, q.cuda())
+        ref_o, ref_lse, _ = orc.decode_attend(np16(q), np16(Kh), np16(Vh), n)
+        assert_o_close(np16(o), ref_o)
+        np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, atol=LSE_ABS_TOL, rtol=0)
+
+    check(K, V, n0)
+    n1 = np.array([[13, 96], [50, 1]])
+    cache.n = torch.as_tensor(n1, dtype=torch.int32).cuda()       # a new tensor
+    check(K, V, n1)
+    cache.n.copy_(torch.as_tensor(n0, dtype=torch.int32))        # in place, same storage
+    check(K, V, n0)
+    K2 = torch.randn(B, Hkv, C, D, generator=g).half()
+    V2 = torch.randn(B, Hkv, C, D, generator=g).half()
+    cache.K, cache.V = K2.cuda(), V2.cuda()                      # other storage
+    check(K2, V2, n0)
+    assert device_status_clean(kvc)
+
+
 @pytest.mark.parametrize("wname", ["llama7b-b8-h32-d128-t2048", "heavy-gqa64x8-b512-d128-t2048"])
 def test_full_size_sampled_units(kvc, orc, wname):
     """Full-size workloads in the benchmark's launch configuration (automatic splits); the
