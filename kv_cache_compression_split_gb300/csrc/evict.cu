@@ -483,6 +483,61 @@ __global__ void __launch_bounds__(WE_WARPS * 32, MAXS <= WE_SMALL_SLOTS ? 4 : 1)
         auto key = [&](int j) { return ((uint64_t)desc_bits(sc[j]) << 32) | (uint32_t)pos[j]; };
         auto cand = [&](int j) { return (long)pos[j] < rt; };
         const int drops = n - n_rec - take;
+        if (drops == 1) {
+            // the decode step's case: the worst candidate -- the largest (descending
+            // score, position) key -- leaves and the last slot moves into its place,
+            // which is what the hole / tail compaction below does for a single hole
+            uint64_t best = 0;
+            int bj = -1;
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                if (32 * i >= n)
+                    break;
+                const int j = 32 * i + lane;
+                if (j < n && (long)pr[i] < rt) {
+                    const uint64_t k = ((uint64_t)desc_bits(sr[i]) << 32) | (uint32_t)pr[i];
+                    if (bj < 0 || k > best) {
+                        best = k;
+                        bj = j;
+                    }
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const uint64_t ok = __shfl_xor_sync(0xffffffffu, best, off);
+                const int oj = __shfl_xor_sync(0xffffffffu, bj, off);
+                if (oj >= 0 && (bj < 0 || ok > best)) {
+                    best = ok;
+                    bj = oj;
+                }
+            }
+            const int last = n - 1;
+            if (bj != last) {
+                const int chunks = p.D / 8;
+                uint4 *K4 = reinterpret_cast<uint4 *>(p.K), *V4 = reinterpret_cast<uint4 *>(p.V);
+                const long rs = p.rows.row(unit, last), rd = p.rows.row(unit, bj);
+                if (rs < 0 || rd < 0) {   // no page behind a slot: skip the row, flag it
+                    if (lane == 0)
+                        flag_error(p.status, DEV_CAPACITY);
+                } else {
+                    for (int ch = lane; ch < 2 * chunks; ch += 32) {
+                        if (ch < chunks)
+                            K4[rd * chunks + ch] = K4[rs * chunks + ch];
+                        else
+                            V4[rd * chunks + ch - chunks] = V4[rs * chunks + ch - chunks];
+                    }
+                }
+                if (lane == 0) {
+                    p.pos[(size_t)unit * p.C + bj] = p.pos[(size_t)unit * p.C + last];
+                    sc[bj] = sc[last];
+                }
+            }
+            if (lane == 0) {
+                sc[last] = 0.f;   // the freed slot starts from a zero score
+                p.n[unit] = last;
+            }
+            return;
+        }
         if (take > 0 && drops <= 4) {
             // few drops (the decode step drops one): keep every candidate, then remove
             // the worst -- the largest (descending score, position) key -- drops times
