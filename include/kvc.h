@@ -347,6 +347,12 @@ enum { KVC_H2O_DECODE = 0, KVC_H2O_PREFILL = 1 };
  *          Needs kvc_h2o_workspace_size bytes of workspace (16-byte aligned):
  *          -lse of every prompt row ([B * Hq, L rounded up to 128] fp32), then
  *          16 bytes of work counters that the call zeroes on its stream.
+ *          lse (optional): [B, Hq, L] fp32, each prompt row's natural-log
+ *          normaliser log sum_{j <= i} exp(scale * qp[b,h,i] . kp[b,hk,j]), as a
+ *          causal flash-attention forward over the same prompt returns it.
+ *          When given, the pass that computes these is skipped and only the
+ *          column-sum pass runs (the one extra pass over the prompt); when NULL
+ *          the call computes them itself.  The values are read as given.
  */
 typedef struct kvc_h2o_args {
     int mode;
@@ -370,8 +376,9 @@ KVC_API size_t kvc_h2o_workspace_size(const kvc_h2o_args *args);
 /*
  * kvc_h2o_accumulate -- add attention probabilities into the heavy-hitter
  * scores (DECODE) or compute the prompt's scores in a second pass over the
- * causal prompt (PREFILL: one pass for the row log-sum-exp, one that
- * recomputes the probabilities and sums them per key).
+ * causal prompt (PREFILL: one pass for the row log-sum-exp, unless the caller
+ * supplies it, and one that recomputes the probabilities and sums them per
+ * key).
  * Source: "Rethinking KV Cache Compression" guide, §16 "4 种方法逐步执行" (H2O
  * accumulates attention scores) and "局限与最终结论" (the extra pass).
  */

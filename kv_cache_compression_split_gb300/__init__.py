@@ -261,11 +261,12 @@ def kvc_h2o_accumulate_decode(cache: "SlotCache", scores, logits, lse, Hq: int,
     _check(lib().kvc_h2o_accumulate(C.byref(a), _stream(stream)), "kvc_h2o_accumulate")
 
 
-def kvc_h2o_accumulate_prefill(qp, kp, scores, workspace, L: int, stream=None):
+def kvc_h2o_accumulate_prefill(qp, kp, scores, workspace, L: int, lse=None, stream=None):
+    """lse: optional [B, Hq, L] fp32 natural-log row normalisers (skips the row pass)."""
     B, Hq, _, D = qp.shape
     _, Hkv, kp_cap, _ = kp.shape
-    a = _h2o_args(KVC_H2O_PREFILL, B, Hq, Hkv, D, int(scores.shape[-1]), scores, L=L, qp=qp,
-                  kp=kp, kp_cap=kp_cap, workspace=workspace)
+    a = _h2o_args(KVC_H2O_PREFILL, B, Hq, Hkv, D, int(scores.shape[-1]), scores, lse=lse, L=L,
+                  qp=qp, kp=kp, kp_cap=kp_cap, workspace=workspace)
     _check(lib().kvc_h2o_accumulate(C.byref(a), _stream(stream)), "kvc_h2o_accumulate")
 
 

@@ -8,7 +8,10 @@
 //   pass 1  lse_i = log2 sum_{j <= i} 2^(s_ij)          (s = scale log2e q_i . k_j)
 //   pass 2  score_j = sum_{h in group} sum_{i >= j} 2^(s_ij - lse_i)
 // Pass 1 stores -lse_i; pass 2 brings each query tile's 128 values into a small
-// shared-memory ring with the tile, so its epilogue reads them from there.
+// shared-memory ring with the tile, so its epilogue reads them from there.  A
+// caller that already holds the rows' normalisers (a causal flash-attention
+// forward over the prompt computes them) passes them in and skips pass 1: then
+// only the extra pass of the guide's statement runs.
 //
 // A work item is one 128-row "stationary" tile held in shared memory -- a query
 // tile in pass 1, a key tile in pass 2 -- against every 128-row tile of the
@@ -572,6 +575,20 @@ cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const TcPara
     return cudaGetLastError();
 }
 
+// -lse rows for pass 2 from normalisers the caller already has (the natural-log
+// log-sum-exp of each prompt row, as a causal flash-attention forward returns
+// it): -lse * log2e in the log2 domain of pass 1, -inf on the padding rows.
+__global__ void k_nlse_from_lse(const float *__restrict__ lse, float *__restrict__ nlse,
+                                long long rows, int L, int Lpad)
+{
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= rows * Lpad)
+        return;
+    const long long r = i / Lpad;
+    const int c = (int)(i - r * Lpad);
+    nlse[i] = c < L ? -lse[r * L + c] * LOG2E : -INFINITY;
+}
+
 template <int D> cudaError_t prefill_tc_impl(const kvc_h2o_args &a, float *lse_ws, cudaStream_t s)
 {
     TcParams tp{};
@@ -598,11 +615,20 @@ template <int D> cudaError_t prefill_tc_impl(const kvc_h2o_args &a, float *lse_w
     if (!encode_tmap_2d_f16(&tq, a.qp, D, (uint64_t)a.B * a.Hq * a.L, 64, TT) ||
         !encode_tmap_2d_f16(&tk, a.kp, D, (uint64_t)a.B * a.Hkv * a.kp_cap, 64, TT))
         return cudaErrorInvalidValue;
-    tp.n_work = a.B * a.Hq * tp.npairs;
-    tp.work_ctr = ctr;
-    cudaError_t e = launch_tc<D, 1>(tq, tk, tp, s);
-    if (e != cudaSuccess)
-        return e;
+    if (a.lse) {   // the rows' normalisers are given: only the column-sum pass runs
+        const long long rows = (long long)a.B * a.Hq, total = rows * tp.Lpad;
+        k_nlse_from_lse<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(a.lse, lse_ws, rows, a.L,
+                                                                        tp.Lpad);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    } else {
+        tp.n_work = a.B * a.Hq * tp.npairs;
+        tp.work_ctr = ctr;
+        const cudaError_t e = launch_tc<D, 1>(tq, tk, tp, s);
+        if (e != cudaSuccess)
+            return e;
+    }
     tp.n_work = a.B * a.Hkv * tp.npairs;
     tp.work_ctr = ctr + 1;
     return launch_tc<D, 2>(tq, tk, tp, s);

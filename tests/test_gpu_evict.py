@@ -133,6 +133,39 @@ def test_h2o_prefill_scores_and_evict(kvc, orc, B, Hq, Hkv, L, D, n_heavy, n_rec
     assert device_status_clean(kvc)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,L,D", [(1, 4, 4, 64, 64), (2, 8, 2, 300, 128),
+                                            (1, 8, 1, 1500, 128), (3, 6, 3, 384, 64)])
+def test_h2o_prefill_scores_given_row_normalisers(kvc, orc, B, Hq, Hkv, L, D):
+    """Prefill scores with the rows' log-sum-exp supplied (as a causal flash-attention forward
+    returns it), so only the column-sum pass runs: the oracle's scores and the two-pass
+    call's scores, both within the score tolerance."""
+    g = torch.Generator().manual_seed(3 * L + D)
+    C = L + 4
+    Qp = torch.randn(B, Hq, L, D, generator=g).half()
+    Kseq = torch.randn(B, Hkv, C, D, generator=g).half()
+    # the rows' natural-log normalisers in fp64 from the fp16 inputs, handed over in fp32
+    q64 = Qp.double().numpy()
+    k64 = np.repeat(Kseq.double().numpy()[:, :, :L], Hq // Hkv, axis=1)
+    s = np.einsum("bhid,bhjd->bhij", q64, k64) / np.sqrt(D)
+    s = np.where(np.tril(np.ones((L, L), bool)), s, -np.inf)
+    m = s.max(-1, keepdims=True)
+    lse = (m[..., 0] + np.log(np.exp(s - m).sum(-1))).astype(np.float32)
+    ws = torch.empty(kvc.kvc_h2o_workspace_size(B, Hq, L) // 4, dtype=torch.float32, device="cuda")
+    kp = Kseq.cuda()
+    given = torch.zeros(B, Hkv, C, dtype=torch.float32, device="cuda")
+    kvc.kvc_h2o_accumulate_prefill(Qp.cuda(), kp, given, ws, L, lse=torch.from_numpy(lse).cuda())
+    both = torch.zeros(B, Hkv, C, dtype=torch.float32, device="cuda")
+    kvc.kvc_h2o_accumulate_prefill(Qp.cuda(), kp, both, ws, L)
+    torch.cuda.synchronize()
+    ref = orc.h2o_prefill_scores(np16(Qp), np16(Kseq), L, threads=4)
+    got = given.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(got[..., :L], ref, rtol=SCORE_REL_TOL, atol=0)
+    assert (got[..., L:] == 0).all()
+    np.testing.assert_allclose(got[..., :L], both.cpu().numpy()[..., :L], rtol=SCORE_REL_TOL,
+                               atol=0)
+    assert device_status_clean(kvc)
+
+
 def test_h2o_prefill_full_size_sampled_units(kvc, orc):
     """The prefill score pass at the benchmark's shape and launch (512 sequences, GQA 64/8,
     D=128, a 2047-token causal prompt; the persistent CTAs claim tile pairs dynamically):
