@@ -133,3 +133,16 @@ def test_binding_rejects_host_and_strided_tensors():
     with pytest.raises(ValueError, match="CUDA tensors"):
         kvc.kvc_append(cache, torch.zeros(1, 1, 1, 64, dtype=torch.float16),
                        torch.zeros(1, 1, 1, 64, dtype=torch.float16))
+
+
+def test_prefill_args_carry_the_row_normalisers(kvc):
+    """The prefill arguments pass the optional row normalisers through to the C struct (NULL
+    when absent), and a prefill without workspace is refused before anything is launched."""
+    h = kvc._h2o_args(kvc.KVC_H2O_PREFILL, 1, 8, 1, 128, 300, 16, lse=4096, L=300, qp=16, kp=16,
+                      kp_cap=300)
+    assert h.lse == 4096 and h.mode == kvc.KVC_H2O_PREFILL
+    h2 = kvc._h2o_args(kvc.KVC_H2O_PREFILL, 1, 8, 1, 128, 300, 16, L=300, qp=16, kp=16,
+                       kp_cap=300)
+    assert h2.lse is None
+    lib = kvc.lib()
+    assert lib.kvc_h2o_accumulate(ctypes.byref(h), None) == kvc.KVC_ERR_WORKSPACE
