@@ -606,18 +606,24 @@ def run_gpu(args, rank, world):
     with torch.cuda.stream(stream):   # replay() launches on the current stream
         g_e2e.replay()
     torch.cuda.synchronize(dev)
-    rewind()
-    torch.cuda.synchronize(dev)
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        g_e2e.replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
+    # three timed replays, the caches rewound before each; the median is reported (the
+    # host-memory side of the copies shares the machine with other jobs, and a single
+    # replay once in a few runs came out 1.5-2x slower)
+    e2e_runs = []
+    for _ in range(3):
+        rewind()
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g_e2e.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_runs.append(e0.elapsed_time(e1) / n_e2e)
     del g_e2e
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_ms = statistics.median(e2e_runs)
     h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
     d2h = host_out[0].numel() * host_out[0].element_size()
 
@@ -648,7 +654,7 @@ def run_gpu(args, rank, world):
         "fp16_traffic": fp16_traffic,
         "ms_per_step": ms_per_step, "serial_ms_per_step": serial_ms / args.steps,
         "step_roofline": step_roofline,
-        "eager_ms_per_step": eager_ms, "e2e_ms_per_step": e2e_ms,
+        "eager_ms_per_step": eager_ms, "e2e_ms_per_step": e2e_ms, "e2e_runs_ms": e2e_runs,
         "calls_ms": calls,
         "kernels": kernels, "methods": methods, "rows": rows, "clocks": clocks,
         "device_status": status, "tokens_per_step": 4 * B,
@@ -1722,6 +1728,7 @@ def main():
                                  "per step)"},
             "e2e": {"value": whole_job_rate(world, res["tokens_per_step"], e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                    "ms_per_step_replays": res["e2e_runs_ms"],
                     "host_binding": res["host_binding"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
             "roofline": {"bound": "hbm", "kernel": "k_attend_slots (FP16 cache launch)",
