@@ -556,6 +556,60 @@ def test_h2o_onchip_logits_match_written_logits(kvc, D, C, n, splits):
     assert device_status_clean(kvc)
 
 
+@pytest.mark.parametrize("n_heavy", [9, 0])
+def test_h2o_single_drop_cases(kvc, orc, n_heavy):
+    """Units that drop exactly one slot (the decode step's case, a path of its own in the
+    warp-per-unit kernel): the victim in a middle slot, in the last slot (nothing moves), in
+    slot 0, and two candidates tied on the lowest score (the later position leaves); with
+    n_heavy = 0 the single candidate leaves.  Keep-sets equal the oracle's exactly, rows and
+    scores travel with their positions, and the freed slot's score is 0."""
+    B, Hkv, C, D, T, n_recent = 1, 4, 64, 64, 100, 30
+    rng = np.random.default_rng(41 + n_heavy)
+    g = torch.Generator().manual_seed(41)
+    Kseq = torch.randn(B, Hkv, T, D, generator=g).half()
+    Vseq = torch.randn(B, Hkv, T, D, generator=g).half()
+    n = n_heavy + 1 + n_recent
+    pos0 = np.zeros((B, Hkv, C), np.int32)
+    sc0 = np.zeros((B, Hkv, C), np.float32)
+    for hk in range(Hkv):
+        cand = np.sort(rng.choice(T - n_recent, n_heavy + 1, replace=False))
+        p = rng.permutation(np.concatenate([cand, np.arange(T - n_recent, T)])).astype(np.int32)
+        s = rng.uniform(1.0, 4.0, n).astype(np.float32)
+        cslots = np.flatnonzero(p < T - n_recent)
+        victim = {0: cslots[len(cslots) // 2], 1: n - 1, 2: cslots[-1], 3: 0}[hk]
+        if p[victim] >= T - n_recent:   # bring a candidate into the chosen slot
+            o = cslots[0]
+            p[[victim, o]] = p[[o, victim]]
+            s[[victim, o]] = s[[o, victim]]
+        s[victim] = 0.5
+        if hk == 2 and n_heavy > 0:     # a tie on the lowest score with another candidate
+            other = [c for c in np.flatnonzero(p < T - n_recent) if c != victim][0]
+            s[other] = 0.5
+        pos0[0, hk, :n], sc0[0, hk, :n] = p, s
+    pos_t = torch.from_numpy(pos0).long()
+    cache = kvc.SlotCache.empty(B, Hkv, C, D)
+    cache.K.copy_(torch.gather(Kseq, 2, pos_t[..., None].expand(-1, -1, -1, D)).cuda())
+    cache.V.copy_(torch.gather(Vseq, 2, pos_t[..., None].expand(-1, -1, -1, D)).cuda())
+    cache.pos.copy_(torch.from_numpy(pos0).cuda())
+    cache.n.fill_(n)
+    cache.seqlen.fill_(T)
+    scores = torch.from_numpy(sc0).cuda()
+    kvc.kvc_h2o_evict(cache, scores, n_heavy, n_recent)
+    torch.cuda.synchronize()
+    nn, pos, _, _ = _units(cache)
+    sc = scores.cpu().numpy()
+    for hk in range(Hkv):
+        assert nn[0, hk] == n - 1
+        keep, _ = orc.h2o_keep(pos0[0, hk, :n], sc0[0, hk, :n].astype(np.float64), T, n_heavy,
+                               n_recent)
+        assert set(pos[0, hk, :n - 1].tolist()) == set(pos0[0, hk, :n][keep].tolist()), hk
+        _assert_content(cache, Kseq, Vseq, 0, hk, pos[0, hk, :n - 1])
+        src = {int(q): v for q, v in zip(pos0[0, hk, :n], sc0[0, hk, :n])}
+        assert all(sc[0, hk, j] == src[int(pos[0, hk, j])] for j in range(n - 1))
+        assert sc[0, hk, n - 1] == 0
+    assert device_status_clean(kvc)
+
+
 @pytest.mark.parametrize("C", [600, 1100])   # warp-per-unit and CTA-per-unit kernels
 def test_h2o_evict_when_trigger(kvc, orc, C):
     """Batched H2O eviction ("Practical Online KV Cache Compaction for LLM Agents", §5.2): units
