@@ -197,6 +197,17 @@ def test_h2o_prefill_full_size_sampled_units(kvc, orc):
         got = scores[b, hk].cpu().numpy().astype(np.float64)
         np.testing.assert_allclose(got, ref[0, 0], rtol=SCORE_REL_TOL, atol=0,
                                    err_msg=f"b={b} hk={hk}")
+    # the column-sum pass alone, with the rows' normalisers supplied (here the ones the
+    # two-pass call left in its workspace, -lse in log2 units, turned back to natural log)
+    lpad = (L + 127) // 128 * 128
+    lse = (ws[:B * Hq * lpad].view(B, Hq, lpad)[:, :, :L] * (-np.log(2.0))).contiguous()
+    one = torch.zeros_like(scores)
+    kvc.kvc_h2o_accumulate_prefill(qp, kp, one, ws, L, lse=lse)
+    torch.cuda.synchronize()
+    assert device_status_clean(kvc)
+    np.testing.assert_allclose(one.double().sum(dim=2).cpu().numpy(), g * L, rtol=1e-4)
+    np.testing.assert_allclose(one.cpu().numpy(), scores.cpu().numpy(), rtol=SCORE_REL_TOL,
+                               atol=1e-30)
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,D,mode,splits,decay", [
