@@ -145,6 +145,19 @@ def _desc_key(tensors):
                  for t in tensors)
 
 
+_DESC_CACHE_KEYS = ("_desc", "_desc_key", "_desc_p")
+
+
+def _state_without_desc(obj):
+    """A cache object's state for pickling and copying: its fields, without the kept ctypes
+    descriptor (rebuilt on the next call; ctypes pointers do not pickle)."""
+    state = dict(obj.__dict__)
+    for k in _DESC_CACHE_KEYS:
+        state.pop(k, None)
+    return state
+
+
+
 def _stream(stream):
     if stream is None:
         if _raw_stream is not None:
@@ -392,6 +405,9 @@ class SlotCache:
                    seqlen=torch.zeros(B, dtype=torch.int32, device=device),
                    block_table=block_table.to(device=device, dtype=torch.int32).contiguous())
 
+    def __getstate__(self):
+        return _state_without_desc(self)
+
     def desc(self) -> SlotCacheDesc:
         # built once and kept while the fields' storage, shapes and strides stay the same (a
         # field replaced or resized in place yields a new key, and the fields are checked again)
@@ -482,6 +498,9 @@ class QuantCache:
                    Cq_paged=Cq,
                    k_gear=torch.zeros(side, dtype=torch.uint8, device=device) if gear else None,
                    v_gear=torch.zeros(side, dtype=torch.uint8, device=device) if gear else None)
+
+    def __getstate__(self):
+        return _state_without_desc(self)
 
     def desc(self) -> QuantCacheDesc:
         # kept while the fields' storage, shapes and strides stay the same (see SlotCache)

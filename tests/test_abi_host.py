@@ -146,3 +146,21 @@ def test_prefill_args_carry_the_row_normalisers(kvc):
     assert h2.lse is None
     lib = kvc.lib()
     assert lib.kvc_h2o_accumulate(ctypes.byref(h), None) == kvc.KVC_ERR_WORKSPACE
+
+
+def test_cache_objects_pickle_and_copy_without_their_descriptor():
+    """A cache object keeps its ctypes descriptor between calls; pickling or copying it
+    leaves that out (ctypes pointers do not pickle), and the copy rebuilds its own."""
+    import copy
+    import pickle
+    import kv_cache_compression_split_gb300 as kvc
+    cache = kvc.SlotCache.empty(1, 2, 64, 64, device="cpu")
+    d = kvc.SlotCacheDesc()
+    cache.__dict__.update(_desc=d, _desc_key=("k",), _desc_p=ctypes.pointer(d))
+    back = pickle.loads(pickle.dumps(cache))
+    assert "_desc" not in back.__dict__ and back.K.shape == cache.K.shape
+    dup = copy.copy(cache)
+    assert "_desc_p" not in dup.__dict__ and dup.K is cache.K
+    q = kvc.QuantCache.empty(1, 2, 256, 64, 4, 128, device="cpu")
+    q.__dict__.update(_desc=kvc.QuantCacheDesc(), _desc_key=("k",))
+    assert "_desc" not in pickle.loads(pickle.dumps(q)).__dict__
